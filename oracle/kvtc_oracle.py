@@ -1,0 +1,350 @@
+"""CPU oracle for attention-aware transform coding (AATC) of the KV cache.
+
+TEST INFRASTRUCTURE. Only the tests, __graft_entry__.smoke() and bench.py's CPU-baseline / reference leg
+import this module. The product library (the C-ABI shared library and its Python binding) neither imports
+nor calls it, and this module imports nothing from the product.
+
+What it computes, in the pages' order, written plainly (numpy; fp64 for all statistics, transforms and
+attention; IEEE fp32 for the quantiser, whose op sequence is part of the record format):
+
+ 1. Calibration statistics per (layer, KV head) [AATC "KV Cache Compression Through the Lens of Transform
+    Coding", Key points 2nd bullet: bits are allocated "over a calibration set"; NOVA-KV (third abstract on
+    the "SPHERICAL KV" page): transforms "from calibration statistics"]: key/value means, centred
+    covariances (divide by n), and the un-centred query second moment M_Q pooled over the g query heads
+    that read the KV head.
+ 2. Transform coding with a KLT [SPECTRA abstract: rotate the cache "into a coordinate system computed
+    from its own statistics, removing these correlations"]: Sigma = U Lambda U^T, eigenvalues descending,
+    each eigenvector's largest-magnitude component made positive (lowest index on ties).
+ 3. Attention-aware channel importances [AATC Key points 1st bullet: under white noise the attention
+    distortion is additive over keys and values and factors over tokens and channels]:
+      keys   lambda_i = sigma_i^2 * w_i,  w_i = u_i^T M_Q u_i  (E[(q.e)^2] = sum_i w_i D_i),
+      values lambda_i = sigma_i^2         (E|sum_t p_t e_t|^2 = sum_t p_t^2 sum_i D_i).
+ 4. Reverse water-filling [AATC Full text; RDKV (first abstract on the "SPHERICAL KV" page): widths "from
+    full precision down to zero bits guided by reverse water-filling"]:
+      b_i(theta) = min(B_max, max(0, 1/2 log2(lambda_i / theta))), theta by bisection so that
+      sum_i b_i = C = 32 R_w - 32, then integer rounding (floors, then one bit each to the largest
+      fractional parts compared at 1e-9 resolution; ties to larger lambda, then lower index; never
+      above B_max).
+ 5. Storage order: channels sorted by (width desc, lambda desc, eigen index asc); T = rows of U^T in
+    that order; mu_j = rotated mean, sigma_j = sqrt(lambda_j) (fp32), inv_sigma_j = fp32(1/sigma_j).
+ 6. Per-token quantiser (fixed fp32 op sequence, no fused multiply-add):
+      y'_j = (y_j - mu_j) * inv_sigma_j                 (channels with b_j > 0)
+      m, M = min/max of y'_j over b_j > 0;  z = fp16(m), s = fp16(M - z) (round-to-nearest-even, saturated)
+      c_j = clamp(floor(((y'_j - z) / s) * 2^b_j), 0, 2^b_j - 1);  all codes 0 when s == 0.
+ 7. Fixed-width record [NOVA-KV: "a fixed per-token bit count"]: R_w 32-bit words per token; word 0 holds
+    z (bits 0-15) and s (bits 16-31); codes follow LSB-first from bit 0 of word 1 in storage order;
+    unused bits are 0.
+ 8. Decode attention over the records: y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j) for b_j > 0, else
+    mu_j; k^ = T^T y^ (and v^); o_h = softmax_t(alpha q_h . k^_t) v^ over t < seq_len, all in fp64.
+
+Readings where the pages are silent are listed in the repository's design notes (same bits/element for
+keys and values, orthogonal key KLT with query weighting in the allocation, mid-rise quantiser with bin
+centres, fp16 round-to-nearest-even, budget counting the scale/zero word, alpha = 1/sqrt(d)).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F32 = np.float32
+F64 = np.float64
+HALF_MAX = 65504.0
+
+
+# ----------------------------------------------------------------------------------------------------
+# 1. statistics
+# ----------------------------------------------------------------------------------------------------
+def calib_statistics(k, v, q):
+    """Means and centred covariances (divide by n) of calibration keys/values; un-centred second moment
+    of the pooled calibration queries (all g heads' vectors stacked in q)."""
+    k = np.asarray(k, F64)
+    v = np.asarray(v, F64)
+    q = np.asarray(q, F64)
+    mu_k = k.mean(axis=0)
+    mu_v = v.mean(axis=0)
+    ck = k - mu_k
+    cv = v - mu_v
+    sigma_k = ck.T @ ck / k.shape[0]
+    sigma_v = cv.T @ cv / v.shape[0]
+    m_q = q.T @ q / q.shape[0]
+    return mu_k, sigma_k, mu_v, sigma_v, m_q
+
+
+# ----------------------------------------------------------------------------------------------------
+# 2. KLT
+# ----------------------------------------------------------------------------------------------------
+def klt(sigma):
+    """Eigendecomposition of a symmetric covariance: (eigenvalues descending, U with eigenvectors as
+    columns), sign fixed so that each column's largest-|.| entry is positive (first such index)."""
+    lam, u = np.linalg.eigh(np.asarray(sigma, F64))
+    order = np.argsort(-lam, kind="stable")
+    lam = lam[order].copy()
+    u = u[:, order].copy()
+    for i in range(u.shape[1]):
+        j = int(np.argmax(np.abs(u[:, i])))
+        if u[j, i] < 0:
+            u[:, i] = -u[:, i]
+    return lam, u
+
+
+# ----------------------------------------------------------------------------------------------------
+# 3. importances
+# ----------------------------------------------------------------------------------------------------
+def key_weights(u, m_q):
+    """w_i = u_i^T M_Q u_i for each eigenvector column u_i."""
+    u = np.asarray(u, F64)
+    return np.einsum("ji,jk,ki->i", u, np.asarray(m_q, F64), u)
+
+
+def key_importance(lam, u, m_q):
+    return np.maximum(lam, 0.0) * key_weights(u, m_q)
+
+
+def value_importance(lam):
+    return np.maximum(np.asarray(lam, F64), 0.0)
+
+
+# ----------------------------------------------------------------------------------------------------
+# 4. reverse water-filling
+# ----------------------------------------------------------------------------------------------------
+def record_words(bits_per_elem: float, d: int) -> int:
+    """R_w = floor(bits * d / 32): the budget counts the 32-bit scale/zero word."""
+    return int(np.floor(bits_per_elem * d / 32.0 + 1e-9))
+
+
+def code_bits(r_words: int) -> int:
+    return 32 * r_words - 32
+
+
+def water_fill_continuous(lam, budget: float, max_bits: int, iters: int = 200):
+    """Continuous reverse water-filling: returns (b, theta) with b_i = clip(1/2 log2(lam_i/theta), 0, B).
+    theta is found by bisection in log2(theta) over [log2(min lam) - 40, log2(max lam)]."""
+    lam = np.asarray(lam, F64)
+    d = lam.shape[0]
+    pos = lam > 0
+    if budget <= 0 or not pos.any():
+        return np.zeros(d), None
+    if budget >= max_bits * int(pos.sum()):
+        return np.where(pos, float(max_bits), 0.0), None
+    l2 = np.full(d, -np.inf)
+    l2[pos] = np.log2(lam[pos])
+    lo = l2[pos].min() - 40.0
+    hi = l2[pos].max()
+
+    def b_of(t):
+        return np.clip(0.5 * (l2 - t), 0.0, float(max_bits))
+
+    for _ in range(iters):
+        mid = 0.5 * (lo + hi)
+        if b_of(mid).sum() > budget:
+            lo = mid
+        else:
+            hi = mid
+    t = 0.5 * (lo + hi)
+    return b_of(t), 2.0 ** t
+
+
+def water_fill_integer(lam, budget: int, max_bits: int):
+    """Integer widths: floors of the continuous solution, then the remaining bits one each to the channels
+    with the largest fractional part (ties: larger lambda, then lower index), none above max_bits."""
+    lam = np.asarray(lam, F64)
+    b_real, _ = water_fill_continuous(lam, budget, max_bits)
+    b_int = np.floor(b_real).astype(np.int64)
+    remaining = int(budget - b_int.sum())
+    # fractional parts compared at 1e-9 resolution so that ties in exact arithmetic stay ties after the
+    # bisection's rounding noise (about 1e-15)
+    frac_key = np.rint((b_real - b_int) * 1e9).astype(np.int64)
+    cand = [i for i in range(lam.shape[0]) if b_int[i] < max_bits and lam[i] > 0]
+    cand.sort(key=lambda i: (-frac_key[i], -lam[i], i))
+    for i in cand[:max(remaining, 0)]:
+        b_int[i] += 1
+    return b_int
+
+
+# ----------------------------------------------------------------------------------------------------
+# 5. parameter set
+# ----------------------------------------------------------------------------------------------------
+def storage_order(widths, lam):
+    d = len(widths)
+    return sorted(range(d), key=lambda i: (-int(widths[i]), -float(lam[i]), i))
+
+
+def bit_offsets(widths):
+    w = np.asarray(widths, np.int64)
+    return np.concatenate([[0], np.cumsum(w)[:-1]]).astype(np.int64)
+
+
+class TensorParams:
+    """One tensor's (K or V) codec parameters in storage order. T: fp32 [d, d] (rows = storage channels);
+    mu, sigma, inv_sigma: fp32 [d]; widths: int [d]; r_words: record length in 32-bit words."""
+
+    def __init__(self, T, mu, sigma, widths, r_words, eigvals=None, importance=None):
+        self.T = np.ascontiguousarray(T, F32)
+        self.mu = np.ascontiguousarray(mu, F32)
+        self.sigma = np.ascontiguousarray(sigma, F32)
+        w = np.asarray(widths, np.int64).copy()
+        w[self.sigma == 0] = 0
+        self.widths = w
+        self.inv_sigma = np.where(self.sigma > 0, (1.0 / np.where(self.sigma > 0, self.sigma, 1)
+                                                   .astype(F64)), 0.0).astype(F32)
+        self.r_words = int(r_words)
+        self.offsets = bit_offsets(self.widths)
+        self.eigvals = eigvals
+        self.importance = importance
+        if int(self.widths.sum()) > code_bits(self.r_words):
+            raise ValueError("widths exceed the record's code bits")
+
+    @property
+    def d(self):
+        return self.T.shape[0]
+
+
+def build_tensor_params(mu_raw, lam, u, importance, r_words: int, max_bits: int) -> TensorParams:
+    widths_eig = water_fill_integer(importance, code_bits(r_words), max_bits)
+    order = storage_order(widths_eig, importance)
+    T = u[:, order].T                                   # rows: storage channels
+    mu_rot = T @ np.asarray(mu_raw, F64)
+    sigma = np.sqrt(np.maximum(lam[order], 0.0))
+    return TensorParams(T=T, mu=mu_rot, sigma=sigma, widths=widths_eig[order], r_words=r_words,
+                        eigvals=lam[order], importance=np.asarray(importance)[order])
+
+
+def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8):
+    """Full calibration of one (layer, KV head) set -> (TensorParams K, TensorParams V)."""
+    d = np.asarray(k).shape[1]
+    mu_k, s_k, mu_v, s_v, m_q = calib_statistics(k, v, q)
+    lam_k, u_k = klt(s_k)
+    lam_v, u_v = klt(s_v)
+    imp_k = key_importance(lam_k, u_k, m_q)
+    imp_v = value_importance(lam_v)
+    pk = build_tensor_params(mu_k, lam_k, u_k, imp_k, record_words(bits_k, d), max_bits)
+    pv = build_tensor_params(mu_v, lam_v, u_v, imp_v, record_words(bits_v, d), max_bits)
+    return pk, pv
+
+
+# ----------------------------------------------------------------------------------------------------
+# 6. quantiser (fp32, fixed op order)
+# ----------------------------------------------------------------------------------------------------
+def half_rn_sat(x):
+    """fp32 -> fp16 round-to-nearest-even with saturation to +-65504 (numpy's conversion is RN-even)."""
+    x = np.asarray(x, F32)
+    return np.clip(x, F32(-HALF_MAX), F32(HALF_MAX)).astype(np.float16)
+
+
+def rotate(x, p: TensorParams):
+    """y = T x per token (fp64 matmul of the fp32 transform), rounded once to fp32."""
+    return (np.asarray(x, F64) @ p.T.astype(F64).T).astype(F32)
+
+
+def quantize(y32, p: TensorParams):
+    """Codes for fp32 rotated coefficients y32 [n, d] -> (z fp16 [n], s fp16 [n], codes int64 [n, d])."""
+    y32 = np.asarray(y32, F32)
+    n, d = y32.shape
+    nz = p.widths > 0
+    codes = np.zeros((n, d), np.int64)
+    if not nz.any():
+        return np.zeros(n, np.float16), np.zeros(n, np.float16), codes
+    yp = (y32[:, nz] - p.mu[nz]) * p.inv_sigma[nz]          # fp32 subtract, then fp32 multiply
+    m = yp.min(axis=1)
+    M = yp.max(axis=1)
+    z16 = half_rn_sat(m)
+    zf = z16.astype(F32)
+    s16 = half_rn_sat(M - zf)
+    sf = s16.astype(F32)
+    scale = np.ldexp(np.ones(int(nz.sum()), F32), p.widths[nz].astype(np.int32)).astype(F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = (yp - zf[:, None]) / sf[:, None]                # IEEE fp32 division
+        u = t * scale[None, :]                              # exact power-of-two scaling
+        c = np.floor(u)
+    hi = (2 ** p.widths[nz]) - 1
+    c = np.where(np.isfinite(c), c, 0.0)
+    c = np.clip(c, 0, hi[None, :]).astype(np.int64)
+    c[sf == 0] = 0
+    codes[:, nz] = c
+    return z16, s16, codes
+
+
+# ----------------------------------------------------------------------------------------------------
+# 7. record packing
+# ----------------------------------------------------------------------------------------------------
+def pack(z16, s16, codes, p: TensorParams):
+    """-> uint32 records [n, R_w]."""
+    codes = np.asarray(codes, np.int64)
+    n, d = codes.shape
+    rec = np.zeros((n, p.r_words), np.uint64)
+    zb = np.asarray(z16, np.float16).view(np.uint16).astype(np.uint64)
+    sb = np.asarray(s16, np.float16).view(np.uint16).astype(np.uint64)
+    rec[:, 0] = zb | (sb << np.uint64(16))
+    for j in range(d):
+        b = int(p.widths[j])
+        if b == 0:
+            continue
+        o = int(p.offsets[j])
+        w, sh = 1 + o // 32, o % 32
+        c = codes[:, j].astype(np.uint64)
+        rec[:, w] |= (c << np.uint64(sh)) & np.uint64(0xFFFFFFFF)
+        if sh + b > 32:
+            rec[:, w + 1] |= c >> np.uint64(32 - sh)
+    return rec.astype(np.uint32)
+
+
+def unpack(rec, p: TensorParams):
+    """uint32 records [n, R_w] -> (z fp16 [n], s fp16 [n], codes int64 [n, d])."""
+    rec = np.asarray(rec, np.uint32).astype(np.uint64)
+    n = rec.shape[0]
+    z16 = (rec[:, 0] & np.uint64(0xFFFF)).astype(np.uint16).view(np.float16)
+    s16 = (rec[:, 0] >> np.uint64(16)).astype(np.uint16).view(np.float16)
+    codes = np.zeros((n, p.d), np.int64)
+    for j in range(p.d):
+        b = int(p.widths[j])
+        if b == 0:
+            continue
+        o = int(p.offsets[j])
+        w, sh = 1 + o // 32, o % 32
+        val = rec[:, w] >> np.uint64(sh)
+        if sh + b > 32:
+            val |= rec[:, w + 1] << np.uint64(32 - sh)
+        codes[:, j] = (val & np.uint64((1 << b) - 1)).astype(np.int64)
+    return z16, s16, codes
+
+
+def encode(x, p: TensorParams):
+    """Raw vectors x [n, d] -> records [n, R_w]."""
+    z, s, c = quantize(rotate(x, p), p)
+    return pack(z, s, c, p)
+
+
+# ----------------------------------------------------------------------------------------------------
+# 8. decode attention
+# ----------------------------------------------------------------------------------------------------
+def dequantize(z16, s16, codes, p: TensorParams):
+    """Rotated-domain reconstruction y^ [n, d] in fp64."""
+    z = np.asarray(z16, np.float16).astype(F64)[:, None]
+    s = np.asarray(s16, np.float16).astype(F64)[:, None]
+    mu = p.mu.astype(F64)[None, :]
+    sig = p.sigma.astype(F64)[None, :]
+    b = p.widths[None, :]
+    y = mu + sig * (z + (np.asarray(codes, F64) + 0.5) * s * np.power(2.0, -b.astype(F64)))
+    return np.where(b > 0, y, np.broadcast_to(mu, y.shape))
+
+
+def reconstruct(rec, p: TensorParams):
+    """Records -> original-basis vectors x^ = T^T y^ [n, d] (fp64)."""
+    y = dequantize(*unpack(rec, p), p)
+    return y @ p.T.astype(F64)
+
+
+def attention(q, k, v, scale: float):
+    """Exact single-query softmax attention in fp64: q [g, d], k/v [n, d] -> [g, d]."""
+    q = np.asarray(q, F64)
+    logits = scale * (q @ np.asarray(k, F64).T)
+    logits -= logits.max(axis=1, keepdims=True)
+    p = np.exp(logits)
+    p /= p.sum(axis=1, keepdims=True)
+    return p @ np.asarray(v, F64)
+
+
+def attend_decode(q, rec_k, rec_v, pk: TensorParams, pv: TensorParams, seq_len: int, scale: float):
+    """Decode attention of the g query heads q [g, d] over the first seq_len records of one KV head."""
+    kh = reconstruct(np.asarray(rec_k)[:seq_len], pk)
+    vh = reconstruct(np.asarray(rec_v)[:seq_len], pv)
+    return attention(q, kh, vh, scale)

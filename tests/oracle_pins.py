@@ -1,0 +1,402 @@
+"""Pins of the CPU oracle to facts outside itself: hand-computed fixtures, closed forms, Monte Carlo of the
+white-noise distortion model, brute force on tiny inputs and library routines. Each pin is a plain function
+so that tests/test_oracle_mutations.py can run it against an oracle with a planted mistake."""
+import itertools
+import math
+
+import numpy as np
+
+from conftest import read_golden
+from oracle import kvtc_oracle as O
+from transform_coded_kv_02_b300 import synth
+
+
+def _floats(s):
+    return np.array([float(x) for x in s.split()], dtype=np.float64)
+
+
+def _ints(s):
+    return np.array([int(x) for x in s.split()], dtype=np.int64)
+
+
+def _params_from_row(widths, mu, sigma, r_words):
+    d = len(widths)
+    return O.TensorParams(T=np.eye(d), mu=mu, sigma=sigma, widths=widths, r_words=r_words)
+
+
+# --- statistics -------------------------------------------------------------------------------------
+def pin_statistics_closed_form():
+    """mean/centred covariance/un-centred query moment of a 3-token example, solved by hand."""
+    k = np.array([[1.0, 2.0], [3.0, 4.0], [5.0, 0.0]])
+    v = np.array([[0.0, 0.0], [2.0, 2.0], [4.0, -2.0]])
+    q = np.array([[1.0, 0.0], [0.0, 2.0]])
+    mu_k, s_k, mu_v, s_v, m_q = O.calib_statistics(k, v, q)
+    assert np.allclose(mu_k, [3.0, 2.0])
+    assert np.allclose(s_k, np.array([[8.0, -4.0], [-4.0, 8.0]]) / 3.0)
+    assert np.allclose(mu_v, [2.0, 0.0])
+    assert np.allclose(s_v, np.array([[8.0, -4.0], [-4.0, 8.0]]) / 3.0)
+    assert np.allclose(m_q, np.array([[0.5, 0.0], [0.0, 2.0]]))
+
+
+# --- KLT ----------------------------------------------------------------------------------------------
+def pin_klt_known_spectrum():
+    """Sigma = Q diag(lam) Q^T with a known spectrum: eigenvalues, reconstruction, orthogonality, signs,
+    and agreement with numpy.linalg.eigh on the same matrix."""
+    rng = np.random.default_rng(7)
+    d = 32
+    Q = synth.random_orthogonal(d, rng)
+    lam = 3.0 * 0.8 ** np.arange(d) + 0.01 * np.arange(d)[::-1]
+    sigma = (Q * lam) @ Q.T
+    l, u = O.klt(sigma)
+    assert np.allclose(l, np.sort(lam)[::-1], rtol=1e-10, atol=1e-12)
+    assert np.linalg.norm((u * l) @ u.T - sigma) <= 1e-10 * np.linalg.norm(sigma)
+    assert np.linalg.norm(u.T @ u - np.eye(d)) <= 1e-12 * d
+    for i in range(d):
+        j = int(np.argmax(np.abs(u[:, i])))
+        assert u[j, i] > 0
+    # each column spans the same line as the generating basis vector of that eigenvalue
+    order = np.argsort(-lam)
+    for i in range(d):
+        assert abs(abs(u[:, i] @ Q[:, order[i]]) - 1.0) < 1e-8
+    le, ue = np.linalg.eigh(sigma)
+    assert np.allclose(np.sort(le)[::-1], l, rtol=1e-12, atol=1e-13)
+
+
+def pin_transform_preserves_inner_products():
+    """An orthogonal transform keeps q.k: (Tq).(Tk) = q.k (fp64 eigenbasis to 1e-12; fp32 table to 1e-6)."""
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=64, steps=1)
+    pk, _ = O.calibrate(L.calib_k[0], L.calib_v[0], L.calib_q[0], 2.75, 2.75)
+    _, s_k, _, _, _ = O.calib_statistics(L.calib_k[0], L.calib_v[0], L.calib_q[0])
+    _, u = O.klt(s_k)
+    k = synth.as_float(L.k[0, 0])
+    q = synth.as_float(L.q[0, 0])
+    ref = q @ k.T
+    rot = (q @ u) @ (k @ u).T
+    assert np.max(np.abs(rot - ref)) <= 1e-12 * np.max(np.abs(ref)) * 128
+    t = pk.T.astype(np.float64)
+    rot32 = (q @ t.T) @ (k @ t.T).T
+    assert np.max(np.abs(rot32 - ref)) <= 1e-6 * np.linalg.norm(q) * np.linalg.norm(k, axis=1).max()
+
+
+def pin_sixteen_bits_preserve_attention():
+    """With every channel at 16 bits the codec is transparent: |q.k - q.k^| <= 1e-3 |q||k| and the decode
+    output is within 1e-3 relative L2 of exact attention on the raw keys and values."""
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=256, steps=1)
+    pk, pv = O.calibrate(L.calib_k[0], L.calib_v[0], L.calib_q[0], 2.75, 2.75)
+    d = pk.d
+    k = synth.as_float(L.k[0, 0])
+    v = synth.as_float(L.v[0, 0])
+    q = synth.as_float(L.q[0, 0])
+    pk16 = O.TensorParams(pk.T, pk.mu, pk.sigma, np.full(d, 16), r_words=1 + 16 * d // 32)
+    pv16 = O.TensorParams(pv.T, pv.mu, pv.sigma, np.full(d, 16), r_words=1 + 16 * d // 32)
+    rk = O.encode(k, pk16)
+    rv = O.encode(v, pv16)
+    kh = O.reconstruct(rk, pk16)
+    err = np.abs(q @ kh.T - q @ k.T)
+    bound = 1e-3 * np.linalg.norm(q, axis=1)[:, None] * np.linalg.norm(k, axis=1)[None, :]
+    assert np.all(err <= bound)
+    scale = 1.0 / math.sqrt(d)
+    o = O.attend_decode(q, rk, rv, pk16, pv16, k.shape[0], scale)
+    ex = O.attention(q, k, v, scale)
+    assert np.linalg.norm(o - ex) <= 1e-3 * np.linalg.norm(ex)
+
+
+# --- white-noise distortion model (AATC Key points, 1st bullet) ----------------------------------------
+def pin_key_distortion_monte_carlo():
+    """E[(q.e)^2] with e = U e^, e^_i ~ N(0, D_i) independent, q drawn from the calibration queries, equals
+    sum_i w_i D_i with w_i = u_i^T M_Q u_i (Monte Carlo, within 4 standard errors)."""
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    ck, cv, cq = L.calib_k[0], L.calib_v[0], L.calib_q[0]
+    _, s_k, _, _, m_q = O.calib_statistics(ck, cv, cq)
+    lam, u = O.klt(s_k)
+    d = u.shape[0]
+    D = 1e-2 * (1.0 + (np.arange(d) % 5)) * (1.0 + 10.0 * (np.arange(d) < 8))
+    w = O.key_weights(u, m_q)
+    predicted = float(w @ D)
+    rng = np.random.default_rng(11)
+    n = 200_000
+    qs = np.asarray(cq, np.float64)[rng.integers(0, cq.shape[0], n)]
+    e = (rng.standard_normal((n, d)) * np.sqrt(D)) @ u.T
+    x = np.einsum("nd,nd->n", qs, e) ** 2
+    se = x.std() / math.sqrt(n)
+    assert abs(x.mean() - predicted) <= 4 * se, (x.mean(), predicted, se)
+
+
+def pin_value_distortion_monte_carlo():
+    """E|sum_t p_t e_t|^2 with e_t = U e^_t white = sum_t p_t^2 sum_i D_i (independent of the basis)."""
+    rng = np.random.default_rng(12)
+    d, n_tok, trials = 128, 16, 20_000
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    _, _, _, s_v, _ = O.calib_statistics(L.calib_k[0], L.calib_v[0], L.calib_q[0])
+    _, u = O.klt(s_v)
+    D = 1e-2 * (1.0 + (np.arange(d) % 7))
+    p = rng.random(n_tok)
+    p /= p.sum()
+    predicted = float((p ** 2).sum() * D.sum())
+    e = (rng.standard_normal((trials, n_tok, d)) * np.sqrt(D)) @ u.T
+    x = (np.einsum("t,ntd->nd", p, e) ** 2).sum(axis=1)
+    se = x.std() / math.sqrt(trials)
+    assert abs(x.mean() - predicted) <= 4 * se
+    # the importances the oracle uses for values are the eigenvalues themselves
+    assert np.allclose(O.value_importance(np.array([2.0, 1.0, 0.0])), [2.0, 1.0, 0.0])
+
+
+def pin_additive_key_value_distortion():
+    """Small independent white noise on keys and values: the output error energy of both together equals
+    the key-only plus the value-only energy (cross terms vanish), to first order."""
+    rng = np.random.default_rng(13)
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=32, steps=1)
+    k = synth.as_float(L.k[0, 0])
+    v = synth.as_float(L.v[0, 0])
+    q = synth.as_float(L.q[0, 0])[:1]
+    scale = 1.0 / math.sqrt(k.shape[1])
+    o = O.attention(q, k, v, scale)
+    trials = 4000
+    ek = rng.standard_normal((trials,) + k.shape) * 1e-3
+    ev = rng.standard_normal((trials,) + v.shape) * 1e-3
+    both = np.array([np.sum((O.attention(q, k + ek[i], v + ev[i], scale) - o) ** 2) for i in range(trials)])
+    konly = np.array([np.sum((O.attention(q, k + ek[i], v, scale) - o) ** 2) for i in range(trials)])
+    vonly = np.array([np.sum((O.attention(q, k, v + ev[i], scale) - o) ** 2) for i in range(trials)])
+    diff = both - konly - vonly
+    assert abs(diff.mean()) <= 4 * diff.std() / math.sqrt(trials) + 1e-3 * both.mean()
+
+
+# --- water-filling -----------------------------------------------------------------------------------
+def pin_water_fill_golden():
+    for lam, C, bmax, b_real, b_int in read_golden("water_fill_small.txt"):
+        lam, C, bmax = _floats(lam), int(C), int(bmax)
+        br, _ = O.water_fill_continuous(lam, C, bmax)
+        assert np.allclose(br, _floats(b_real), atol=1e-9), (lam, br)
+        assert np.array_equal(O.water_fill_integer(lam, C, bmax), _ints(b_int)), lam
+
+
+def pin_water_fill_kkt():
+    """Continuous solution of min sum_i lam_i 2^(-2 b_i) s.t. sum b_i = C, 0 <= b_i <= Bmax: active channels
+    share one distortion theta, inactive ones have lam_i <= theta, capped ones lam_i 4^-Bmax >= theta;
+    widths are monotone in lam."""
+    rng = np.random.default_rng(3)
+    for trial in range(20):
+        d = int(rng.integers(4, 129))
+        lam = np.exp(rng.normal(0, 3, d))
+        C = int(rng.integers(1, 8 * d))
+        bmax = 8
+        b, theta = O.water_fill_continuous(lam, C, bmax)
+        assert abs(b.sum() - C) < 1e-6
+        assert np.all(b >= 0) and np.all(b <= bmax)
+        if theta is None:
+            continue
+        act = (b > 1e-9) & (b < bmax - 1e-9)
+        Dist = lam * 4.0 ** (-b)
+        assert np.allclose(Dist[act], theta, rtol=1e-6)
+        assert np.all(lam[b <= 1e-9] <= theta * (1 + 1e-6))
+        assert np.all(lam[b >= bmax - 1e-9] * 4.0 ** (-bmax) >= theta * (1 - 1e-6))
+        order = np.argsort(-lam)
+        assert np.all(np.diff(b[order]) <= 1e-9)
+
+
+def pin_water_fill_integer_properties():
+    rng = np.random.default_rng(4)
+    for trial in range(30):
+        d = int(rng.integers(2, 129))
+        lam = np.exp(rng.normal(0, 2, d))
+        C = int(rng.integers(0, 8 * d + 1))
+        bi = O.water_fill_integer(lam, C, 8)
+        br, _ = O.water_fill_continuous(lam, C, 8)
+        assert bi.sum() == min(C, 8 * d)
+        assert np.all((bi >= 0) & (bi <= 8))
+        assert np.all(np.abs(bi - br) < 1.0 + 1e-9)
+
+
+def brute_force_allocation(lam, C, bmax):
+    """Exhaustive integer allocation minimising sum lam_i 4^-b_i with sum b_i = C (tiny d only)."""
+    best, arg = math.inf, None
+    for b in itertools.product(range(bmax + 1), repeat=len(lam)):
+        if sum(b) != C:
+            continue
+        val = sum(l * 4.0 ** (-x) for l, x in zip(lam, b))
+        if val < best:
+            best, arg = val, b
+    return best, np.array(arg)
+
+
+def pin_water_fill_vs_brute_force():
+    """The rounding rule is within a small factor of the exhaustive integer optimum (reported gap)."""
+    rng = np.random.default_rng(5)
+    worst = 1.0
+    for trial in range(25):
+        d = int(rng.integers(2, 6))
+        lam = np.exp(rng.normal(0, 2, d))
+        C = int(rng.integers(1, 4 * d))
+        best, _ = brute_force_allocation(lam, C, 6)
+        b = O.water_fill_integer(lam, C, 6)
+        val = float(np.sum(lam * 4.0 ** (-b)))
+        assert val >= best * (1 - 1e-12)
+        worst = max(worst, val / best)
+    assert worst < 2.0, worst
+    return worst
+
+
+def pin_compression_accounting():
+    for bits, rw, nbytes, ratio, page in read_golden("compression_ratios.txt"):
+        r = O.record_words(float(bits), 128)
+        assert r == int(rw)
+        assert 4 * r == int(nbytes)
+        assert abs(16 * 128 / (32 * r) - float(ratio)) < 1e-12
+        if page != "none":
+            assert abs(16 * 128 / (32 * r) - float(page)) / float(page) < 0.07
+
+
+# --- quantiser / record ------------------------------------------------------------------------------
+def pin_quantize_pack_golden():
+    for name, widths, mu, sigma, y, rw, codes, words, yhat in read_golden("quantize_pack_small.txt"):
+        p = _params_from_row(_ints(widths), _floats(mu), _floats(sigma), int(rw))
+        y32 = _floats(y).astype(np.float32)[None, :]
+        z, s, c = O.quantize(y32, p)
+        assert np.array_equal(c[0], _ints(codes)), (name, c)
+        rec = O.pack(z, s, c, p)
+        assert [int(x) for x in rec[0]] == [int(w, 16) for w in words.split()], (name, [hex(x) for x in rec[0]])
+        z2, s2, c2 = O.unpack(rec, p)
+        assert np.array_equal(c2, c)
+        yh = O.dequantize(z2, s2, c2, p)
+        assert np.allclose(yh[0], _floats(yhat), atol=1e-12), (name, yh)
+
+
+def pin_pack_roundtrip():
+    rng = np.random.default_rng(6)
+    for trial in range(40):
+        d = int(rng.integers(1, 130))
+        widths = rng.integers(0, 17, d)
+        r_words = 1 + (int(widths.sum()) + 31) // 32 + int(rng.integers(0, 2))
+        p = _params_from_row(widths, np.zeros(d), np.ones(d), r_words)
+        n = 7
+        codes = np.stack([rng.integers(0, 2 ** int(b), n) if b > 0 else np.zeros(n, np.int64)
+                          for b in widths], axis=1)
+        z = rng.normal(size=n).astype(np.float16)
+        s = np.abs(rng.normal(size=n)).astype(np.float16)
+        rec = O.pack(z, s, codes, p)
+        z2, s2, c2 = O.unpack(rec, p)
+        assert np.array_equal(c2, codes)
+        assert np.array_equal(z2.view(np.uint16), z.view(np.uint16))
+        assert np.array_equal(s2.view(np.uint16), s.view(np.uint16))
+        used = int(widths.sum())
+        for wi in range(1, r_words):   # bits past the last code are zero
+            lo = 32 * (wi - 1)
+            if used <= lo:
+                assert np.all(rec[:, wi] == 0)
+            elif used < lo + 32:
+                assert np.all((rec[:, wi].astype(np.uint64) >> np.uint64(used - lo)) == 0)
+
+
+def pin_quantizer_error_bound():
+    """Codes lie in [0, 2^b - 1]; normalised reconstruction error <= half a bin (s 2^-b / 2) plus fp32
+    rounding for every value inside [z, z + s]."""
+    rng = np.random.default_rng(8)
+    d = 64
+    widths = np.concatenate([np.full(8, 8), np.full(16, 4), np.full(20, 2), np.full(12, 1), np.zeros(8, int)])
+    mu = rng.normal(size=d)
+    sigma = np.exp(rng.normal(size=d))
+    p = _params_from_row(widths, mu, sigma, r_words=1 + int(np.ceil(widths.sum() / 32)))
+    y = (rng.normal(size=(500, d)) * sigma + mu).astype(np.float32)
+    z, s, c = O.quantize(y, p)
+    nz = widths > 0
+    assert np.all(c[:, nz] >= 0) and np.all(c[:, nz] <= (2 ** widths[nz]) - 1)
+    assert np.all(c[:, ~nz] == 0)
+    yp = ((y.astype(np.float64) - p.mu.astype(np.float64)) * p.inv_sigma.astype(np.float64))[:, nz]
+    yh = O.dequantize(z, s, c, p)
+    yhp = ((yh - p.mu.astype(np.float64)) / p.sigma.astype(np.float64))[:, nz]
+    zf = z.astype(np.float64)[:, None]
+    sf = s.astype(np.float64)[:, None]
+    inside = (yp >= zf) & (yp <= zf + sf)
+    half_bin = sf * 2.0 ** (-widths[nz].astype(np.float64)) / 2
+    err = np.abs(yp - yhp)
+    assert np.all(err[inside] <= (half_bin + 1e-5 * (np.abs(yp) + 1))[inside])
+
+
+def pin_zero_bit_channels_are_the_mean():
+    rng = np.random.default_rng(9)
+    d = 16
+    widths = np.array([4] * 6 + [0] * 10)
+    mu = rng.normal(size=d).astype(np.float32)
+    p = _params_from_row(widths, mu, np.ones(d), r_words=2)
+    y = rng.normal(size=(20, d)).astype(np.float32)
+    yh = O.dequantize(*O.unpack(O.pack(*O.quantize(y, p), p), p), p)
+    assert np.array_equal(yh[:, 6:], np.broadcast_to(mu[6:].astype(np.float64), (20, 10)))
+
+
+def pin_half_conversion():
+    """fp32 -> fp16 round-to-nearest-even with saturation, per IEEE 754 binary16 (hand-picked values)."""
+    cases = [(1.0 + 2.0 ** -11, 1.0), (1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -9), (65519.0, 65504.0),
+             (65520.0, 65504.0), (1e9, 65504.0), (-1e9, -65504.0), (2.0 ** -25, 0.0),
+             (3 * 2.0 ** -26, 2.0 ** -24), (0.1, 0.0999755859375)]
+    for x, want in cases:
+        assert float(O.half_rn_sat(np.float32(x))) == want, (x, want)
+
+
+# --- decode ------------------------------------------------------------------------------------------
+def brute_force_decode(q, rec_k, rec_v, pk, pv, seq_len, scale):
+    """Explicit per-element loops: unpack bits, dequantise, rotate back, softmax, weighted sum."""
+    def rec_to_vec(rec, p):
+        d = p.d
+        word0 = int(rec[0])
+        z = float(np.array([word0 & 0xFFFF], np.uint16).view(np.float16)[0])
+        s = float(np.array([word0 >> 16], np.uint16).view(np.float16)[0])
+        bits = 0
+        for i in range(1, len(rec)):
+            bits |= int(rec[i]) << (32 * (i - 1))
+        y = []
+        off = 0
+        for j in range(d):
+            b = int(p.widths[j])
+            if b == 0:
+                y.append(float(p.mu[j]))
+                continue
+            c = (bits >> off) & ((1 << b) - 1)
+            off += b
+            y.append(float(p.mu[j]) + float(p.sigma[j]) * (z + (c + 0.5) * s / (2 ** b)))
+        x = []
+        for col in range(d):
+            acc = 0.0
+            for row in range(d):
+                acc += float(p.T[row, col]) * y[row]
+            x.append(acc)
+        return x
+
+    ks = [rec_to_vec(rec_k[t], pk) for t in range(seq_len)]
+    vs = [rec_to_vec(rec_v[t], pv) for t in range(seq_len)]
+    out = []
+    for h in range(q.shape[0]):
+        logits = [scale * sum(float(q[h, i]) * ks[t][i] for i in range(len(ks[t]))) for t in range(seq_len)]
+        mx = max(logits)
+        e = [math.exp(l - mx) for l in logits]
+        tot = sum(e)
+        out.append([sum(e[t] / tot * vs[t][i] for t in range(seq_len)) for i in range(pk.d)])
+    return np.array(out)
+
+
+def pin_decode_brute_force():
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=8, steps=1)
+    pk, pv = O.calibrate(L.calib_k[0], L.calib_v[0], L.calib_q[0], 2.75, 2.75)
+    k = synth.as_float(L.k[0, 0])
+    v = synth.as_float(L.v[0, 0])
+    q = synth.as_float(L.q[0, 0])
+    rk, rv = O.encode(k, pk), O.encode(v, pv)
+    scale = 1.0 / math.sqrt(128)
+    for T in (1, 3, 8):
+        o = O.attend_decode(q, rk, rv, pk, pv, T, scale)
+        ref = brute_force_decode(q, rk, rv, pk, pv, T, scale)
+        assert np.allclose(o, ref, rtol=1e-11, atol=1e-11), T
+
+
+def pin_calibrate_structure():
+    """Calibrated sets: orthogonal T, widths non-increasing in storage order and summing to the budget,
+    mu = T mu_raw, sigma^2 = eigenvalues."""
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    ck, cv, cq = L.calib_k[0], L.calib_v[0], L.calib_q[0]
+    pk, pv = O.calibrate(ck, cv, cq, 2.75, 2.75)
+    for p, x in ((pk, ck), (pv, cv)):
+        t = p.T.astype(np.float64)
+        assert np.linalg.norm(t @ t.T - np.eye(128)) < 1e-5
+        assert np.all(np.diff(p.widths) <= 0)
+        assert p.widths.sum() == O.code_bits(11)
+        assert np.allclose(p.mu, t @ np.asarray(x, np.float64).mean(0), atol=1e-5)
+        assert np.allclose(p.sigma.astype(np.float64) ** 2, p.eigvals, rtol=1e-5)

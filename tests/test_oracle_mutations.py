@@ -1,0 +1,144 @@
+"""Plant a plausible mistake in the CPU oracle (on the CPU, via monkeypatch) and check that a pin catches
+it: evidence that the pins constrain every step of the oracle, not just its happy path."""
+import numpy as np
+import pytest
+
+import oracle_pins as P
+from oracle import kvtc_oracle as O
+
+_orig = {name: getattr(O, name) for name in
+         ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
+          "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat"]}
+
+
+def _klt_transposed(sigma):
+    lam, u = _orig["klt"](sigma)
+    return lam, u.T.copy()
+
+
+def _klt_no_sign_fix(sigma):
+    lam, u = np.linalg.eigh(np.asarray(sigma, np.float64))
+    o = np.argsort(-lam)
+    return lam[o], -u[:, o]
+
+
+def _key_weights_rows(u, m_q):
+    u = np.asarray(u, np.float64)
+    return np.einsum("ij,jk,ik->i", u, m_q, u)
+
+
+def _stats_uncentred(k, v, q):
+    mu_k, _, mu_v, _, m_q = _orig["calib_statistics"](k, v, q)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    return mu_k, k.T @ k / len(k), mu_v, v.T @ v / len(v), m_q
+
+
+def _wf_natural_log(lam, budget, max_bits, iters=200):
+    lam = np.asarray(lam, np.float64)
+    pos = lam > 0
+    if budget <= 0 or not pos.any() or budget >= max_bits * pos.sum():
+        return _orig["water_fill_continuous"](lam, budget, max_bits, iters)
+    l = np.full(len(lam), -np.inf)
+    l[pos] = np.log(lam[pos])
+    lo, hi = l[pos].min() - 40, l[pos].max()
+    f = lambda t: np.clip(0.5 * (l - t), 0, max_bits)
+    for _ in range(iters):
+        mid = 0.5 * (lo + hi)
+        lo, hi = (mid, hi) if f(mid).sum() > budget else (lo, mid)
+    return f(0.5 * (lo + hi)), np.exp(0.5 * (lo + hi))
+
+
+def _wi_ties_to_smaller(lam, budget, max_bits):
+    lam = np.asarray(lam, np.float64)
+    br, _ = O.water_fill_continuous(lam, budget, max_bits)
+    bi = np.floor(br).astype(np.int64)
+    key = np.rint((br - bi) * 1e9)
+    cand = sorted([i for i in range(len(lam)) if bi[i] < max_bits and lam[i] > 0],
+                  key=lambda i: (-key[i], lam[i], i))
+    for i in cand[:int(budget - bi.sum())]:
+        bi[i] += 1
+    return bi
+
+
+def _quantize_zero_from_max(y32, p):
+    z, s, c = _orig["quantize"](y32, p)
+    nz = p.widths > 0
+    yp = (np.asarray(y32, np.float32)[:, nz] - p.mu[nz]) * p.inv_sigma[nz]
+    return O.half_rn_sat(yp.max(1)), s, c
+
+
+def _quantize_half_scale(y32, p):
+    q = O.TensorParams(p.T, p.mu, p.sigma, np.maximum(p.widths - 1, 0), p.r_words)
+    z, s, c = _orig["quantize"](y32, q)
+    return z, s, c
+
+
+def _pack_one_word_late(z16, s16, codes, p):
+    rec = _orig["pack"](z16, s16, codes, p)
+    out = np.zeros_like(rec)
+    out[:, 0] = rec[:, 0]
+    out[:, 2:] = rec[:, 1:-1]
+    return out
+
+
+def _pack_msb_first(z16, s16, codes, p):
+    rec = _orig["pack"](z16, s16, codes, p)
+    out = rec.copy()
+    for w in range(1, rec.shape[1]):
+        x = rec[:, w].astype(np.uint64)
+        r = np.zeros_like(x)
+        for b in range(32):
+            r |= ((x >> np.uint64(b)) & np.uint64(1)) << np.uint64(31 - b)
+        out[:, w] = r.astype(np.uint32)
+    return out
+
+
+def _dequant_no_half(z16, s16, codes, p):
+    return _orig["dequantize"](z16, s16, np.asarray(codes) - 0.5, p)
+
+
+def _rotate_transposed(x, p):
+    return (np.asarray(x, np.float64) @ p.T.astype(np.float64)).astype(np.float32)
+
+
+def _reconstruct_transposed(rec, p):
+    y = O.dequantize(*O.unpack(rec, p), p)
+    return y @ p.T.astype(np.float64).T
+
+
+def _attention_unscaled(q, k, v, scale):
+    return _orig["attention"](q, k, v, 1.0)
+
+
+def _half_truncate(x):
+    x = np.clip(np.asarray(x, np.float32), -65504, 65504)
+    h = x.astype(np.float16)
+    over = np.abs(h.astype(np.float32)) > np.abs(x)
+    return np.where(over, np.nextafter(h, np.float16(0)), h).astype(np.float16)
+
+
+MUTATIONS = [
+    ("klt", _klt_transposed, P.pin_klt_known_spectrum),
+    ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
+    ("key_weights", _key_weights_rows, P.pin_key_distortion_monte_carlo),
+    ("calib_statistics", _stats_uncentred, P.pin_statistics_closed_form),
+    ("water_fill_continuous", _wf_natural_log, P.pin_water_fill_golden),
+    ("water_fill_integer", _wi_ties_to_smaller, P.pin_water_fill_golden),
+    ("quantize", _quantize_zero_from_max, P.pin_quantize_pack_golden),
+    ("quantize", _quantize_half_scale, P.pin_quantize_pack_golden),
+    ("pack", _pack_one_word_late, P.pin_quantize_pack_golden),
+    ("pack", _pack_msb_first, P.pin_quantize_pack_golden),
+    ("dequantize", _dequant_no_half, P.pin_quantizer_error_bound),
+    ("rotate", _rotate_transposed, P.pin_sixteen_bits_preserve_attention),
+    ("reconstruct", _reconstruct_transposed, P.pin_decode_brute_force),
+    ("attention", _attention_unscaled, P.pin_decode_brute_force),
+    ("half_rn_sat", _half_truncate, P.pin_half_conversion),
+]
+
+
+@pytest.mark.parametrize("name,mutant,pin", MUTATIONS, ids=[f"{m[0]}:{m[1].__name__}" for m in MUTATIONS])
+def test_pin_catches_planted_mistake(monkeypatch, name, mutant, pin):
+    monkeypatch.setattr(O, name, mutant)
+    with pytest.raises(AssertionError):
+        pin()

@@ -1,0 +1,79 @@
+"""CPU oracle pinned to facts outside itself (see oracle_pins.py for each pin's source)."""
+import oracle_pins as P
+
+
+def test_statistics_closed_form():
+    P.pin_statistics_closed_form()
+
+
+def test_klt_known_spectrum():
+    P.pin_klt_known_spectrum()
+
+
+def test_transform_preserves_inner_products():
+    P.pin_transform_preserves_inner_products()
+
+
+def test_sixteen_bits_preserve_attention():
+    P.pin_sixteen_bits_preserve_attention()
+
+
+def test_key_distortion_monte_carlo():
+    P.pin_key_distortion_monte_carlo()
+
+
+def test_value_distortion_monte_carlo():
+    P.pin_value_distortion_monte_carlo()
+
+
+def test_additive_key_value_distortion():
+    P.pin_additive_key_value_distortion()
+
+
+def test_water_fill_golden():
+    P.pin_water_fill_golden()
+
+
+def test_water_fill_kkt():
+    P.pin_water_fill_kkt()
+
+
+def test_water_fill_integer_properties():
+    P.pin_water_fill_integer_properties()
+
+
+def test_water_fill_vs_brute_force():
+    worst = P.pin_water_fill_vs_brute_force()
+    print(f"worst integer-rounding distortion ratio vs exhaustive optimum: {worst:.4f}")
+
+
+def test_compression_accounting():
+    P.pin_compression_accounting()
+
+
+def test_quantize_pack_golden():
+    P.pin_quantize_pack_golden()
+
+
+def test_pack_roundtrip():
+    P.pin_pack_roundtrip()
+
+
+def test_quantizer_error_bound():
+    P.pin_quantizer_error_bound()
+
+
+def test_zero_bit_channels_are_the_mean():
+    P.pin_zero_bit_channels_are_the_mean()
+
+
+def test_half_conversion():
+    P.pin_half_conversion()
+
+
+def test_decode_brute_force():
+    P.pin_decode_brute_force()
+
+
+def test_calibrate_structure():
+    P.pin_calibrate_structure()
