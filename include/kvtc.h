@@ -1,0 +1,207 @@
+/*
+ * kvtc.h - C ABI of the transform-coded KV cache library (B300 / sm_103a).
+ *
+ * Attention-aware transform coding of the KV cache: per (layer, KV head) an orthogonal d x d transform
+ * (a KLT of calibration statistics) rotates each token's key and value; each rotated channel is scalar
+ * quantised at a width of 0-8 bits chosen by reverse water-filling over attention-aware importances; the
+ * codes are bit-packed into fixed-width per-token records; decode attention runs directly over the
+ * records.
+ *
+ * Sources (web pages on the method; they describe it in words only):
+ *   [AATC]    "KV Cache Compression Through the Lens of Transform Coding" - At a glance, Key points
+ *             (white-noise additive key/value distortion; transform coding + reverse water-filling over a
+ *             calibration set), Full text.
+ *   [SPECTRA] "SPECTRA: Pushing the KV Cache Beyond the 2-Bit Cliff via Spectral Transform Coding" -
+ *             abstract (rotate into a basis computed from the cache's own statistics; concentrate bits).
+ *   [RDKV]    "SPHERICAL KV: Angle-Domain Attention and Rate-Distortion Retention ..." - first abstract
+ *             (bit widths from full precision down to zero by reverse water-filling, applied once).
+ *   [NOVA-KV] same page, third abstract (decode is bandwidth-bound; fixed per-token bit count; transforms
+ *             from calibration statistics).
+ *
+ * Conventions
+ *   - d = 128 (head dimension) is the only supported value; g = Hq / Hkv query heads share a KV head
+ *     (query head hq reads KV head hq / g); g <= 8.
+ *   - Device pointers are owned by the caller. kv_encode and kv_attend_decode never allocate device
+ *     memory and never synchronise the host; they enqueue work on the given stream.
+ *   - Argument errors are returned synchronously before any launch. Errors raised inside a kernel
+ *     (a bounded wait that ran out, a record index out of range) set a per-device status word that
+ *     kv_check_status reports (and clears).
+ *   - kv_stream_t is a cudaStream_t passed as an opaque pointer (NULL = legacy default stream).
+ *   - Every function returns KV_OK (0) on success; kv_last_error() gives a message for the calling
+ *     thread's last failure.
+ */
+#ifndef KVTC_H
+#define KVTC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int kv_status;
+enum {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer, set index out of range      */
+  KV_ERR_UNSUPPORTED = 2, /* d != 128, g > 8, unknown dtype                                           */
+  KV_ERR_BUDGET = 3,      /* bits per element gives fewer than 1 or more than 1 + 8*d/32 record words */
+  KV_ERR_NUMERIC = 4,     /* non-finite calibration data or statistics                                */
+  KV_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed                              */
+  KV_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out (reported by kv_check_status)         */
+  KV_ERR_IO = 7,          /* parameter file missing, truncated, wrong version or bad checksum         */
+  KV_ERR_DEVICE = 8       /* a kernel reported a bad index (reported by kv_check_status)              */
+};
+
+enum { KV_DTYPE_F32 = 0, KV_DTYPE_BF16 = 1 };
+enum { KV_TENSOR_K = 0, KV_TENSOR_V = 1 };
+
+typedef void* kv_stream_t;
+
+/* ------------------------------------------------------------------------------------------------------
+ * Calibration (host).  [AATC Key points 2nd bullet; RDKV; SPECTRA; NOVA-KV]
+ * ------------------------------------------------------------------------------------------------------ */
+
+/* Opaque parameter table: for each calibration set and each tensor (K, V) the transform T (rows = storage
+ * channels), rotated means mu, standard deviations sigma, channel widths, record length. Owned by the
+ * library; free with kv_params_free. */
+typedef struct kv_params kv_params;
+
+/* One calibration set (one KV head of one layer, or of one sequence). Host fp32, row-major.
+ *   k, v: [n_tok][d] keys and values; q: [n_q][d] query vectors of the g query heads that read this KV
+ *   head, stacked (pooled into one second moment). */
+typedef struct {
+  const float* k;
+  const float* v;
+  const float* q;
+  int64_t n_tok;
+  int64_t n_q;
+} kv_calib_set;
+
+typedef struct {
+  int d;          /* head dimension, must be 128                                                    */
+  float bits_k;   /* budget in bits per key element, counting the per-token fp16 scale/zero (2.75 -> 11 words) */
+  float bits_v;   /* same for values                                                                */
+  int max_bits;   /* largest channel width, 1..8 (8)                                                 */
+  int n_threads;  /* host threads for calibration; 0 = all hardware threads                         */
+} kv_calib_opts;
+
+/* Calibrate n_sets sets: fp64 mean/covariance of K and V, query second moment M_Q, Jacobi
+ * eigendecomposition (eigenvalues descending, largest-|.| component of each eigenvector positive),
+ * importances lambda_K = sigma^2 * (u^T M_Q u), lambda_V = sigma^2, reverse water-filling to
+ * C = 32*R_w - 32 code bits with R_w = floor(bits*d/32), storage order (width desc, lambda desc, index asc).
+ * The result lives on the host; call kv_params_upload before encoding or decoding.
+ * Errors: KV_ERR_INVALID_ARG (null, n_tok < 2, n_q < 1), KV_ERR_UNSUPPORTED (d), KV_ERR_BUDGET,
+ * KV_ERR_NUMERIC (non-finite input). */
+kv_status kv_calibrate(int n_sets, const kv_calib_set* sets, const kv_calib_opts* opts, kv_params** out);
+
+/* Build a parameter table from explicit arrays (host, fp32, set-major): T_* [n_sets][d][d] (rows =
+ * storage channels), mu_* / sigma_* [n_sets][d], widths_* [n_sets][d] (0..max 8, sum <= 32*r_words-32).
+ * Channels with sigma == 0 get width 0. Used to feed externally computed parameters (e.g. by a reference
+ * implementation) to the codec. */
+kv_status kv_params_from_arrays(int d, int n_sets,
+                                const float* T_k, const float* mu_k, const float* sigma_k,
+                                const int32_t* widths_k, int r_words_k,
+                                const float* T_v, const float* mu_v, const float* sigma_v,
+                                const int32_t* widths_v, int r_words_v, kv_params** out);
+
+/* Copy the table to the current CUDA device (allocates device memory owned by the table; the stream
+ * orders the copies). Must be called again after switching devices. */
+kv_status kv_params_upload(kv_params* p, kv_stream_t stream);
+
+int kv_params_num_sets(const kv_params* p);
+int kv_params_record_words(const kv_params* p, int tensor);
+
+/* Read back one set/tensor (host arrays, any may be NULL): widths [d], eigenvalues (variances of the
+ * rotated channels, storage order) [d], importances [d], T [d][d], mu [d], sigma [d]. */
+kv_status kv_params_info(const kv_params* p, int set, int tensor, int32_t* widths, double* eigvals,
+                         double* importance, float* T, float* mu, float* sigma);
+
+/* Versioned binary file with a CRC32 of the payload. */
+kv_status kv_params_save(const kv_params* p, const char* path);
+kv_status kv_params_load(const char* path, kv_params** out);
+void kv_params_free(kv_params* p);
+
+/* ------------------------------------------------------------------------------------------------------
+ * Packed cache (device, caller-owned).  [NOVA-KV: fixed per-token bit count]
+ * Record of one token and tensor: r_words 32-bit words; word 0 = fp16 zero point z (bits 0-15) | fp16
+ * scale s (bits 16-31); channel codes LSB-first from bit 0 of word 1 in storage order; unused bits 0.
+ * ------------------------------------------------------------------------------------------------------ */
+typedef struct {
+  uint32_t* k_rec;      /* [B][Hkv][T_cap][r_words_k], 16-byte aligned                                 */
+  uint32_t* v_rec;      /* [B][Hkv][T_cap][r_words_v], 16-byte aligned                                 */
+  int B;
+  int Hkv;
+  int64_t T_cap;        /* token capacity per (sequence, head); multiple of 16                          */
+  int per_seq_params;   /* 0: parameter set = KV head h; 1: set = b*Hkv + h                           */
+} kv_cache;
+
+size_t kv_cache_bytes(const kv_params* p, int tensor, int B, int Hkv, int64_t T_cap);
+
+/* Encode t_new tokens per sequence (prefill or append).  [AATC; SPECTRA "re-encodes the cache into this
+ * coordinate system"]
+ *   k, v: device [B][Hkv][t_new][d] in dtype (KV_DTYPE_BF16 or KV_DTYPE_F32), 16-byte aligned;
+ *   dst_pos_dev: device int64 [B], token i of sequence b is written at position dst_pos[b] + i, which must
+ *   be <= T_cap - t_new (checked on the device: violations are skipped and reported as KV_ERR_DEVICE).
+ * Rotation y = T x, then per token y'_j = (y_j - mu_j) * (1/sigma_j), z = fp16(min y'), s = fp16(max y' - z),
+ * c_j = clamp(floor(((y'_j - z)/s) * 2^b_j), 0, 2^b_j - 1), packed as above. */
+kv_status kv_encode(const kv_params* p, const kv_cache* cache, const void* k, const void* v, int dtype,
+                    int B, int64_t t_new, const int64_t* dst_pos_dev, kv_stream_t stream);
+
+/* Decode attention over the packed cache for one query per head.  [NOVA-KV: decode re-reads the cache
+ * every step and is bandwidth-bound; AATC / SPECTRA transform coding]
+ *   q: device bf16 [B][Hq][d]; seq_lens_dev: device int32 [B], 1 <= seq_len <= T_cap (0 gives zeros);
+ *   out: device fp32 [B][Hq][d]; softmax_scale (alpha) typically 1/sqrt(d).
+ *   o_h = sum_t softmax_t(alpha q_h . k^_t) v^_t, k^ = T_K^T y^ with y^_j = mu_j + sigma_j (z + (c_j + 1/2)
+ *   s 2^-b_j) for b_j > 0 and mu_j otherwise (v^ likewise). Computed in the rotated bases: q is rotated
+ *   once, the output once inverse-rotated.
+ *   workspace: device, at least kv_decode_workspace_bytes(...) bytes, 16-byte aligned, reused across
+ *   calls (no initialisation needed); calls that share a workspace must not overlap on the device. */
+size_t kv_decode_workspace_bytes(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap);
+kv_status kv_attend_decode(const kv_params* p, const kv_cache* cache, const void* q, int B, int Hq,
+                           const int32_t* seq_lens_dev, float softmax_scale, float* out,
+                           void* workspace, size_t ws_bytes, kv_stream_t stream);
+
+/* Uncompressed bf16 split-K flash-decode over k, v: device bf16 [B][Hkv][T_cap][d]; same q, seq_lens,
+ * out conventions. The measurement comparator for the packed path (no page counterpart beyond the
+ * full-cache FlashAttention-2 decoding that RDKV compares against). */
+size_t kv_decode_bf16_workspace_bytes(int B, int Hkv, int Hq, int64_t T_cap);
+kv_status kv_attend_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap,
+                                const void* q, const int32_t* seq_lens_dev, float softmax_scale,
+                                float* out, void* workspace, size_t ws_bytes, kv_stream_t stream);
+
+/* Synchronise the stream and return (and clear) the device status word of the current device:
+ * KV_OK, KV_ERR_TIMEOUT or KV_ERR_DEVICE; KV_ERR_CUDA if the stream reports an error. */
+kv_status kv_check_status(kv_stream_t stream);
+const char* kv_last_error(void);
+int kv_version(void);
+
+/* ------------------------------------------------------------------------------------------------------
+ * Parity and test entry points (same kernels' device code; no separate math).
+ * ------------------------------------------------------------------------------------------------------ */
+/* Quantise + pack n rotated fp32 vectors y_dev [n][d] (storage order) of one set/tensor into rec_dev
+ * [n][r_words], running the encode kernels' quantiser. variant 0: warp-per-token (append / fp32 path);
+ * variant 1: thread-per-token (tensor-core prefill epilogue). */
+kv_status kv_debug_quantize_pack(const kv_params* p, int set, int tensor, const float* y_dev, int64_t n,
+                                 uint32_t* rec_dev, int variant, kv_stream_t stream);
+/* Run the decode kernel's record unpacker over n records rec_dev [n][r_words] of one set/tensor and write
+ * codes_dev [n][d] (uint16, channels in storage order; 0 for zero-width channels). */
+kv_status kv_debug_unpack(const kv_params* p, int set, int tensor, const uint32_t* rec_dev, int64_t n,
+                          uint16_t* codes_dev, kv_stream_t stream);
+/* Host water-filling used by kv_calibrate: integer widths for importances lam [d] and budget bits. */
+kv_status kv_debug_water_fill(const double* lam, int d, int budget_bits, int max_bits, int32_t* widths);
+/* Host Jacobi eigensolver used by kv_calibrate: sym [d][d] -> eigenvalues descending [d] and eigenvectors
+ * as columns evecs [d][d] (row-major), sign-normalised. */
+kv_status kv_debug_eigh(const double* sym, int d, double* evals, double* evecs);
+/* Encode path selection for tests: 0 auto, 1 warp-per-token, 2 tensor-core tiles (bf16 only). */
+kv_status kv_debug_set_encode_path(int path);
+/* Device wait limit in nanoseconds for the bounded mbarrier waits (default 2e9). */
+kv_status kv_debug_set_wait_limit_ns(long long ns);
+/* Launch a kernel that waits on an mbarrier nothing will complete, with the current wait limit; it must
+ * return, leaving KV_ERR_TIMEOUT for kv_check_status. */
+kv_status kv_debug_wait_timeout_selftest(kv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVTC_H */

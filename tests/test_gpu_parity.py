@@ -1,0 +1,274 @@
+"""Parity of the CUDA path (through the C-ABI) with the CPU oracle on the same seeded inputs.
+
+Bars: quantise+pack and unpack bit-exact given the same fp32 rotated input; end-to-end codes differ by at most
+1 LSB on at most 1e-4 of entries (rounding ties of the rotation); decode within 2e-3 relative L2 of the oracle
+run on the same records."""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+from oracle import kvtc_oracle as O
+from transform_coded_kv_02_b300 import kvtc, synth
+
+import gpu_helpers as G
+
+pytestmark = pytest.mark.gpu
+DEC_TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    w = synth.WORKLOADS["tiny"]
+    L = synth.make_layer(w, steps=2)
+    sets = G.calibrate_oracle(L, 2.75, 2.75)
+    return w, L, sets, G.lib_params(sets)
+
+
+def _special_rows(p, rng, n=64):
+    """Rotated fp32 rows with the codec's corner cases: constant rows (s = 0), saturating magnitudes,
+    tiny magnitudes (subnormal fp16 z/s), negative zero, values on a coarse grid (exact bin edges)."""
+    d = p.d
+    mu, sg = p.mu.astype(np.float64), p.sigma.astype(np.float64)
+    rows = [np.full(d, mu[0]), mu.copy(), mu + 1e6 * sg, mu - 3e5 * sg * np.sign(np.arange(d) - 60.5),
+            mu + 1e-7 * sg * rng.normal(size=d), mu + 1e-9 * sg * rng.normal(size=d), -mu * 0.0]
+    grid = mu + sg * (np.round(rng.normal(size=(n, d)) * 4) / 4)
+    rows = np.vstack([np.array(rows), grid, mu + sg * rng.normal(size=(n, d)) * 3])
+    return rows.astype(np.float32)
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("bits", [2.75, 1.33, 4.0, 8.0])
+def test_quantize_pack_bitexact(tiny, variant, bits):
+    w, L, _, _ = tiny
+    sets = G.calibrate_oracle(L, bits, bits)
+    P = G.lib_params(sets)
+    rng = np.random.default_rng(100)
+    for t, p in ((0, sets[0][0]), (1, sets[0][1])):
+        x = synth.as_float(L.k[0, 0] if t == 0 else L.v[0, 0])
+        y = np.vstack([O.rotate(x, p), _special_rows(p, rng)])
+        ref = O.pack(*O.quantize(y, p), p)
+        yd = torch.from_numpy(y).cuda()
+        rec = torch.zeros((y.shape[0], p.r_words), dtype=torch.int32, device="cuda")
+        kvtc.kv_debug_quantize_pack(P, 0, t, yd, y.shape[0], rec, variant)
+        assert kvtc.kv_check_status() == kvtc.KV_OK
+        got = G.u32(rec)
+        bad = np.argwhere(got != ref)
+        assert bad.size == 0, (t, bad[:5], got[bad[0][0]], ref[bad[0][0]])
+
+
+@pytest.mark.parametrize("bits", [2.75, 1.33, 3.0, 8.0])
+def test_unpack_bitexact(tiny, bits):
+    w, L, _, _ = tiny
+    sets = G.calibrate_oracle(L, bits, bits)
+    P = G.lib_params(sets)
+    for t, p in ((0, sets[0][0]), (1, sets[0][1])):
+        x = synth.as_float(L.k[0, 0] if t == 0 else L.v[0, 0])[:333]
+        rec = O.encode(x, p)
+        _, _, codes = O.unpack(rec, p)
+        out = torch.zeros((rec.shape[0], 128), dtype=torch.int16, device="cuda")
+        kvtc.kv_debug_unpack(P, 0, t, G.dev_u32(rec), rec.shape[0], out)
+        assert kvtc.kv_check_status() == kvtc.KV_OK
+        got = out.cpu().numpy().view(np.uint16).astype(np.int64)
+        assert np.array_equal(got, codes)
+
+
+def _encode_gpu(P, k_st, v_st, per_seq, T_cap=None, dst0=0):
+    B, Hkv, T, d = k_st.shape
+    T_cap = T_cap or ((T + 15) // 16 * 16)
+    Rk, Rv = P.record_words(0), P.record_words(1)
+    rk = torch.zeros((B, Hkv, T_cap, Rk), dtype=torch.int32, device="cuda")
+    rv = torch.zeros((B, Hkv, T_cap, Rv), dtype=torch.int32, device="cuda")
+    cache = kvtc.make_cache(rk, rv, B, Hkv, T_cap, per_seq)
+    dt = kvtc.KV_DTYPE_BF16 if k_st.dtype == np.uint16 else kvtc.KV_DTYPE_F32
+    pos = torch.full((B,), dst0, dtype=torch.int64, device="cuda")
+    kvtc.kv_encode(P, cache, G.to_dev_storage(k_st), G.to_dev_storage(v_st), dt, B, T, pos)
+    assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
+    return G.u32(rk), G.u32(rv)
+
+
+def _check_end_to_end(rk_gpu, rv_gpu, k, v, sets, per_seq):
+    B, Hkv, T, _ = k.shape
+    tok_frac, code_frac, max_dc, max_dz = 0.0, 0.0, 0, 0
+    n = 0
+    for b in range(B):
+        for h in range(Hkv):
+            pk, pv = sets[G.set_index(b, h, Hkv, per_seq)]
+            for rec, x, p in ((rk_gpu[b, h, :T], k[b, h], pk), (rv_gpu[b, h, :T], v[b, h], pv)):
+                ref = O.encode(x, p)
+                tf, dz, ds, cf, dc = G.code_diff(rec, ref, p)
+                tok_frac += tf
+                code_frac += cf
+                max_dc = max(max_dc, dc)
+                max_dz = max(max_dz, dz, ds)
+                n += 1
+    tok_frac /= n
+    code_frac /= n
+    assert max_dc <= 1 and max_dz <= 1, (max_dc, max_dz)
+    assert code_frac <= 1e-4, code_frac
+    assert tok_frac <= 1e-3, tok_frac
+    return code_frac, tok_frac
+
+
+def test_encode_end_to_end_tiny_fp32(tiny):
+    w, L, sets, P = tiny
+    rk, rv = _encode_gpu(P, L.k, L.v, False)
+    print("code mismatch fraction %.2e, token z/s mismatch fraction %.2e" %
+          _check_end_to_end(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, False))
+
+
+def test_encode_end_to_end_bf16_per_sequence():
+    w = synth.WORKLOADS["qwen_batched_8k"]
+    L = synth.make_layer(w, T=1024, B=2, steps=1)
+    for bits in w.bits:
+        sets = G.calibrate_oracle(L, bits, bits)
+        P = G.lib_params(sets)
+        rk, rv = _encode_gpu(P, L.k, L.v, True)
+        _check_end_to_end(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, True)
+
+
+def test_append_matches_prefill(tiny):
+    w, L, sets, P = tiny
+    T = 200
+    k, v = L.k[:, :, :T], L.v[:, :, :T]
+    rk_all, rv_all = _encode_gpu(P, k, v, False, T_cap=256)
+    rk = torch.zeros((1, 1, 256, P.record_words(0)), dtype=torch.int32, device="cuda")
+    rv = torch.zeros((1, 1, 256, P.record_words(1)), dtype=torch.int32, device="cuda")
+    cache = kvtc.make_cache(rk, rv, 1, 1, 256, False)
+    kd, vd = G.to_dev_storage(np.ascontiguousarray(k)), G.to_dev_storage(np.ascontiguousarray(v))
+    for i in range(T):
+        pos = torch.tensor([i], dtype=torch.int64, device="cuda")
+        kvtc.kv_encode(P, cache, kd[:, :, i:i + 1].contiguous(), vd[:, :, i:i + 1].contiguous(),
+                       kvtc.KV_DTYPE_F32, 1, 1, pos)
+    assert kvtc.kv_check_status() == kvtc.KV_OK
+    assert np.array_equal(G.u32(rk), rk_all) and np.array_equal(G.u32(rv), rv_all)
+
+
+def test_encode_out_of_range_position_is_reported(tiny):
+    w, L, sets, P = tiny
+    k, v = np.ascontiguousarray(L.k[:, :, :4]), np.ascontiguousarray(L.v[:, :, :4])
+    rk = torch.zeros((1, 1, 64, P.record_words(0)), dtype=torch.int32, device="cuda")
+    rv = torch.zeros((1, 1, 64, P.record_words(1)), dtype=torch.int32, device="cuda")
+    cache = kvtc.make_cache(rk, rv, 1, 1, 64, False)
+    pos = torch.tensor([62], dtype=torch.int64, device="cuda")  # tokens 2, 3 fall past T_cap
+    kvtc.kv_encode(P, cache, G.to_dev_storage(k), G.to_dev_storage(v), kvtc.KV_DTYPE_F32, 1, 4, pos)
+    assert kvtc.kv_check_status() == kvtc.KV_ERR_DEVICE
+    ref = O.encode(synth.as_float(L.k[0, 0, :2]), sets[0][0])
+    tok, dz, ds, cf, dc = G.code_diff(G.u32(rk)[0, 0, 62:64], ref, sets[0][0])
+    assert dc <= 1 and dz <= 1 and ds <= 1
+    assert kvtc.kv_check_status() == kvtc.KV_OK  # cleared
+
+
+def _decode_case(L, sets, P, Hq, per_seq, seq_lens, T_cap, scale=None):
+    k, v = synth.as_float(L.k), synth.as_float(L.v)
+    rk, rv = G.oracle_cache(k, v, sets, per_seq, T_cap)
+    q = L.q[0]
+    got = G.run_decode(P, rk, rv, q, seq_lens, Hq, per_seq, scale)
+    ref = G.oracle_decode(rk, rv, q, seq_lens, sets, Hq, per_seq, scale)
+    return G.rel_l2_rows(got, ref)
+
+
+def test_decode_tiny(tiny):
+    w, L, sets, P = tiny
+    err = _decode_case(L, sets, P, w.Hq, False, [w.T], 1024)
+    assert err.max() <= DEC_TOL, err
+
+
+@pytest.mark.parametrize("seq_len", [1, 2, 3, 15, 16, 17, 31, 33, 63, 64, 65, 100, 127, 129, 1000])
+def test_decode_ragged_lengths(tiny, seq_len):
+    w, L, sets, P = tiny
+    err = _decode_case(L, sets, P, w.Hq, False, [seq_len], 1024)
+    assert err.max() <= DEC_TOL, (seq_len, err)
+
+
+def test_decode_split_count_invariance(tiny):
+    """Different cache capacities give different split plans over the same 1000 tokens."""
+    w, L, sets, P = tiny
+    k, v = synth.as_float(L.k), synth.as_float(L.v)
+    outs = []
+    for T_cap in (1024, 4096, 65536):
+        rk, rv = G.oracle_cache(k, v, sets, False, T_cap)
+        outs.append(G.run_decode(P, rk, rv, L.q[0], [1000], w.Hq, False))
+    for o in outs[1:]:
+        assert G.rel_l2_rows(o, outs[0]).max() <= 1e-5
+
+
+@pytest.mark.parametrize("bits", [2.0, 3.0, 4.0])
+def test_decode_qwen_shape_per_sequence(bits):
+    w = synth.WORKLOADS["qwen_batched_8k"]
+    L = synth.make_layer(w, T=512, B=2, steps=1)
+    sets = G.calibrate_oracle(L, bits, bits)
+    P = G.lib_params(sets)
+    err = _decode_case(L, sets, P, w.Hq, True, [512, 300], 512)
+    assert err.max() <= DEC_TOL, err
+
+
+def test_decode_high_compression_llama_shape():
+    w = synth.WORKLOADS["llama_long_128k"]
+    L = synth.make_layer(w, T=2048, steps=1)
+    sets = G.calibrate_oracle(L, 1.33, 1.33)
+    P = G.lib_params(sets)
+    err = _decode_case(L, sets, P, w.Hq, False, [2048], 2048)
+    assert err.max() <= DEC_TOL, err
+
+
+def test_decode_other_softmax_scale(tiny):
+    w, L, sets, P = tiny
+    err = _decode_case(L, sets, P, w.Hq, False, [777], 1024, scale=0.3)
+    assert err.max() <= DEC_TOL, err
+
+
+def test_decode_bf16_comparator_matches_exact_attention():
+    w = synth.WORKLOADS["qwen_batched_8k"]
+    L = synth.make_layer(w, T=700, B=2, steps=1)
+    B, Hkv, T, d = L.k.shape
+    T_cap = 704
+    kp = np.zeros((B, Hkv, T_cap, d), np.uint16)
+    vp = np.zeros((B, Hkv, T_cap, d), np.uint16)
+    kp[:, :, :T] = L.k
+    vp[:, :, :T] = L.v
+    seq = [700, 333]
+    q = L.q[0]
+    kd, vd, qd = G.to_dev_storage(kp), G.to_dev_storage(vp), G.to_dev_storage(q)
+    sl = torch.tensor(seq, dtype=torch.int32, device="cuda")
+    out = torch.empty((B, w.Hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvtc.kv_decode_bf16_workspace_bytes(B, Hkv, w.Hq, T_cap), dtype=torch.uint8, device="cuda")
+    scale = 1 / math.sqrt(d)
+    kvtc.kv_attend_decode_bf16(kd, vd, B, Hkv, w.Hq, T_cap, qd, sl, scale, out, ws)
+    assert kvtc.kv_check_status() == kvtc.KV_OK
+    got = out.cpu().numpy().astype(np.float64)
+    kf, vf, qf = synth.as_float(kp), synth.as_float(vp), synth.as_float(q)
+    g = w.g
+    ref = np.zeros_like(got)
+    for b in range(B):
+        for h in range(Hkv):
+            ref[b, h * g:(h + 1) * g] = O.attention(qf[b, h * g:(h + 1) * g], kf[b, h, :seq[b]], vf[b, h, :seq[b]],
+                                                    scale)
+    err = G.rel_l2_rows(got, ref)
+    assert err.max() <= 1e-4, err
+
+
+def test_decode_full_size_llama_32k():
+    """The 32K-token Llama-shaped layer (32 q / 8 KV heads, 2.75 bits) in the bench's launch configuration:
+    every output row against the oracle on the same records."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    L = synth.make_layer(w, steps=1)
+    sets = G.calibrate_oracle(L, 2.75, 2.75)
+    P = G.lib_params(sets)
+    T_cap = w.T + 512
+    err = _decode_case(L, sets, P, w.Hq, False, [w.T], T_cap)
+    assert err.max() <= DEC_TOL, err
+
+
+def test_wait_timeout_is_reported_not_hung():
+    kvtc.kv_debug_set_wait_limit_ns(1_000_000)
+    try:
+        kvtc.kv_debug_wait_timeout_selftest()
+        assert kvtc.kv_check_status() == kvtc.KV_ERR_TIMEOUT
+        assert kvtc.kv_check_status() == kvtc.KV_OK
+    finally:
+        kvtc.kv_debug_set_wait_limit_ns(2_000_000_000)

@@ -1,0 +1,169 @@
+"""C-ABI library on the CPU: exported symbols, host calibration against the oracle, persistence and argument
+errors. No compute kernel is launched here."""
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import kvtc_oracle as O
+from transform_coded_kv_02_b300 import kvtc, synth
+
+from conftest import read_golden
+
+
+def test_library_exports_every_declared_symbol():
+    out = subprocess.run(["nm", "-D", "--defined-only", kvtc.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    declared = kvtc.exported_symbols()
+    assert len(declared) >= 25
+    missing = [s for s in declared if s not in syms]
+    assert not missing, missing
+    for s in declared:  # and they resolve through the dynamic loader
+        assert getattr(kvtc._lib, s) is not None
+
+
+def test_water_fill_golden_library():
+    for lam, C, bmax, b_real, b_int in read_golden("water_fill_small.txt"):
+        lam = np.array([float(x) for x in lam.split()])
+        got = kvtc.kv_debug_water_fill(lam, int(C), int(bmax))
+        assert got.tolist() == [int(x) for x in b_int.split()]
+
+
+def test_water_fill_library_matches_oracle():
+    rng = np.random.default_rng(21)
+    for trial in range(200):
+        d = int(rng.integers(1, 129))
+        lam = np.exp(rng.normal(0, 3, d))
+        lam[rng.random(d) < 0.05] = 0.0
+        if trial % 7 == 0:
+            lam = np.round(lam)  # ties
+        C = int(rng.integers(0, 8 * d + 8))
+        assert np.array_equal(kvtc.kv_debug_water_fill(lam, C, 8), O.water_fill_integer(lam, C, 8)), trial
+
+
+def test_jacobi_eigensolver_against_lapack():
+    rng = np.random.default_rng(22)
+    for d in (2, 5, 32, 128):
+        Q = synth.random_orthogonal(d, rng)
+        lam = np.exp(rng.normal(0, 2, d))
+        S = (Q * lam) @ Q.T
+        ev, vec = kvtc.kv_debug_eigh(S)
+        le, _ = np.linalg.eigh(S)
+        assert np.allclose(ev, np.sort(le)[::-1], rtol=1e-10, atol=1e-13 * lam.max())
+        assert np.linalg.norm(vec.T @ vec - np.eye(d)) < 1e-12 * d
+        assert np.linalg.norm((vec * ev) @ vec.T - S) < 1e-11 * np.linalg.norm(S)
+        lo, uo = O.klt(S)
+        for i in range(d):  # same sign convention -> same vectors for distinct eigenvalues
+            assert np.allclose(vec[:, i], uo[:, i], atol=1e-8)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_batched_8k"])
+def test_host_calibration_matches_oracle(name):
+    w = synth.WORKLOADS[name]
+    L = synth.make_layer(w, T=256 if name != "tiny" else 64, B=2 if name != "tiny" else 1, steps=1)
+    bits = w.bits[0]
+    sets = list(zip(L.calib_k, L.calib_v, L.calib_q))
+    P = kvtc.kv_calibrate(sets, bits, bits)
+    assert P.num_sets == len(sets)
+    for s, (ck, cv, cq) in enumerate(sets):
+        pk, pv = O.calibrate(ck, cv, cq, bits, bits)
+        for t, po in ((0, pk), (1, pv)):
+            info = P.info(s, t)
+            assert info["r_words"] == po.r_words
+            assert np.array_equal(info["widths"], po.widths)
+            assert np.allclose(info["eigvals"], po.eigvals, rtol=1e-9, atol=1e-12 * po.eigvals.max())
+            # rows of T: same channels in the same order, same sign (non-degenerate spectra)
+            assert np.max(np.abs(info["T"].astype(np.float64) - po.T.astype(np.float64))) < 1e-5
+            assert np.allclose(info["mu"], po.mu, atol=1e-5)
+            assert np.allclose(info["sigma"], po.sigma, rtol=1e-6)
+            if t == 0:
+                assert np.allclose(info["importance"], po.importance, rtol=1e-8)
+
+
+def test_params_save_load_roundtrip(tmp_path):
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75)
+    path = str(tmp_path / "p.kvtc")
+    P.save(path)
+    Q = kvtc.kv_params_load(path)
+    for t in (0, 1):
+        a, b = P.info(0, t), Q.info(0, t)
+        for key in a:
+            assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
+    raw = bytearray(open(path, "rb").read())
+    raw[100] ^= 0x40
+    open(path, "wb").write(bytes(raw))
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_params_load(path)
+    assert e.value.status == kvtc.KV_ERR_IO
+    open(path, "wb").write(bytes(raw[:50]))
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_params_load(path)
+    assert e.value.status == kvtc.KV_ERR_IO
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_params_load(str(tmp_path / "missing"))
+    assert e.value.status == kvtc.KV_ERR_IO
+
+
+def test_calibrate_argument_errors():
+    rng = np.random.default_rng(0)
+    k = rng.normal(size=(64, 128)).astype(np.float32)
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_calibrate([(k, k, k)], 2.75, 2.75, d=64)
+    assert e.value.status == kvtc.KV_ERR_UNSUPPORTED
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_calibrate([(k, k, k)], 8.5, 2.75)
+    assert e.value.status == kvtc.KV_ERR_BUDGET
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_calibrate([(k, k, k)], 0.1, 2.75)
+    assert e.value.status == kvtc.KV_ERR_BUDGET
+    bad = k.copy()
+    bad[3, 7] = np.nan
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_calibrate([(k, bad, k)], 2.75, 2.75)
+    assert e.value.status == kvtc.KV_ERR_NUMERIC
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_calibrate([(k[:1], k[:1], k)], 2.75, 2.75)
+    assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+
+
+def test_params_from_arrays_validation():
+    d = 128
+    T = np.eye(d, dtype=np.float32)[None]
+    mu = np.zeros((1, d), np.float32)
+    sg = np.ones((1, d), np.float32)
+    w = np.zeros((1, d), np.int32)
+    w[0, :40] = 8
+    with pytest.raises(kvtc.KvError) as e:  # 320 bits > 10 words of codes
+        kvtc.kv_params_from_arrays(T, mu, sg, w, 10, T, mu, sg, w, 11)
+    assert e.value.status == kvtc.KV_ERR_BUDGET
+    w2 = np.zeros((1, d), np.int32)
+    w2[0, 5] = 3  # not a prefix
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_params_from_arrays(T, mu, sg, w2, 11, T, mu, sg, w2, 11)
+    assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+    P = kvtc.kv_params_from_arrays(T, mu, sg, w, 11, T, mu, sg, w, 11)
+    assert P.record_words(0) == 11 and P.info(0, 0)["widths"].sum() == 320
+
+
+def test_encode_refuses_params_not_uploaded():
+    d = 128
+    T = np.eye(d, dtype=np.float32)[None]
+    z = np.zeros((1, d), np.float32)
+    w = np.zeros((1, d), np.int32)
+    P = kvtc.kv_params_from_arrays(T, z, z + 1, w, 1, T, z, z + 1, w, 1)
+    cache = kvtc.make_cache(16, 16, 1, 1, 64)
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_encode(P, cache, 16, 16, kvtc.KV_DTYPE_BF16, 1, 4, 16, stream=0)
+    assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+    assert "not uploaded" in str(e.value)
+
+
+def test_sizes():
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 1.33)
+    assert kvtc.kv_cache_bytes(P, 0, 2, 8, 1024) == 2 * 8 * 1024 * 11 * 4
+    assert kvtc.kv_cache_bytes(P, 1, 2, 8, 1024) == 2 * 8 * 1024 * 5 * 4

@@ -1,0 +1,858 @@
+// Host side of the transform-coded KV cache library: calibration (statistics, KLT, attention-aware
+// importances, reverse water-filling), the parameter table and its device copy, persistence, and the
+// argument checks in front of every kernel launch.
+//
+// Method sources: "KV Cache Compression Through the Lens of Transform Coding" (AATC) - Key points (additive
+// white-noise key/value distortion; transform coding + reverse water-filling over a calibration set);
+// "SPECTRA: Pushing the KV Cache Beyond the 2-Bit Cliff" - abstract (rotate into a basis from the cache's
+// own statistics); "SPHERICAL KV ..." page, first abstract (RDKV: widths from full precision to zero by
+// reverse water-filling, once) and third abstract (NOVA-KV: transforms from calibration statistics, fixed
+// per-token bit count).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <numeric>
+#include <thread>
+#include <vector>
+
+#include "kvtc_internal.h"
+
+using namespace kvtc;
+
+// ------------------------------------------------------------------------------------------------------
+// errors
+// ------------------------------------------------------------------------------------------------------
+static thread_local std::string g_err;
+
+void kvtc::set_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+}
+void kvtc::clear_error() { g_err.clear(); }
+
+extern "C" const char* kv_last_error(void) { return g_err.c_str(); }
+extern "C" int kv_version(void) { return 1; }
+
+#define KV_REQUIRE(cond, code, ...)   \
+  do {                                \
+    if (!(cond)) {                    \
+      kvtc::set_error(__VA_ARGS__);   \
+      return code;                    \
+    }                                 \
+  } while (0)
+
+static kv_status cuda_fail(cudaError_t e, const char* what) {
+  kvtc::set_error("%s: %s", what, cudaGetErrorString(e));
+  return KV_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------------------
+// symmetric eigensolver: cyclic Jacobi (Golub & Van Loan, "Matrix Computations", symmetric Jacobi /
+// cyclic-by-row), eigenvalues descending, eigenvector columns sign-normalised so that the entry of
+// largest magnitude is positive (lowest index on ties).
+// ------------------------------------------------------------------------------------------------------
+static void jacobi_eigh(const double* sym, int d, double* evals, double* evecs /*[d][d] cols*/) {
+  std::vector<double> A(sym, sym + (size_t)d * d), V((size_t)d * d, 0.0);
+  for (int i = 0; i < d; ++i) V[(size_t)i * d + i] = 1.0;
+  double fro = 0.0;
+  for (size_t i = 0; i < A.size(); ++i) fro += A[i] * A[i];
+  fro = sqrt(fro);
+  for (int sweep = 0; sweep < 100; ++sweep) {
+    double off = 0.0;
+    for (int p = 0; p < d; ++p)
+      for (int q = 0; q < d; ++q)
+        if (p != q) off += A[(size_t)p * d + q] * A[(size_t)p * d + q];
+    if (sqrt(off) <= 1e-15 * fro || off == 0.0) break;
+    for (int p = 0; p < d - 1; ++p) {
+      for (int q = p + 1; q < d; ++q) {
+        const double apq = A[(size_t)p * d + q];
+        if (apq == 0.0) continue;
+        const double app = A[(size_t)p * d + p], aqq = A[(size_t)q * d + q];
+        // skip rotations that cannot change the diagonal in double precision
+        if (fabs(apq) < 1e-300 || (fabs(apq) * 1e18 < fabs(app) && fabs(apq) * 1e18 < fabs(aqq))) {
+          A[(size_t)p * d + q] = A[(size_t)q * d + p] = 0.0;
+          continue;
+        }
+        const double tau = (aqq - app) / (2.0 * apq);
+        const double t = (tau >= 0 ? 1.0 : -1.0) / (fabs(tau) + sqrt(1.0 + tau * tau));
+        const double c = 1.0 / sqrt(1.0 + t * t), s = t * c;
+        for (int k = 0; k < d; ++k) {  // A <- A J (columns p, q)
+          const double akp = A[(size_t)k * d + p], akq = A[(size_t)k * d + q];
+          A[(size_t)k * d + p] = c * akp - s * akq;
+          A[(size_t)k * d + q] = s * akp + c * akq;
+        }
+        for (int k = 0; k < d; ++k) {  // A <- J^T A (rows p, q)
+          const double apk = A[(size_t)p * d + k], aqk = A[(size_t)q * d + k];
+          A[(size_t)p * d + k] = c * apk - s * aqk;
+          A[(size_t)q * d + k] = s * apk + c * aqk;
+        }
+        A[(size_t)p * d + q] = A[(size_t)q * d + p] = 0.0;
+        for (int k = 0; k < d; ++k) {  // V <- V J
+          const double vkp = V[(size_t)k * d + p], vkq = V[(size_t)k * d + q];
+          V[(size_t)k * d + p] = c * vkp - s * vkq;
+          V[(size_t)k * d + q] = s * vkp + c * vkq;
+        }
+      }
+    }
+  }
+  std::vector<int> order(d);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return A[(size_t)a * d + a] > A[(size_t)b * d + b]; });
+  for (int i = 0; i < d; ++i) {
+    const int src = order[i];
+    evals[i] = A[(size_t)src * d + src];
+    int jmax = 0;
+    double amax = -1.0;
+    for (int k = 0; k < d; ++k) {
+      const double a = fabs(V[(size_t)k * d + src]);
+      if (a > amax) { amax = a; jmax = k; }
+    }
+    const double sgn = V[(size_t)jmax * d + src] < 0 ? -1.0 : 1.0;
+    for (int k = 0; k < d; ++k) evecs[(size_t)k * d + i] = sgn * V[(size_t)k * d + src];
+  }
+}
+
+// ------------------------------------------------------------------------------------------------------
+// reverse water-filling: b_i(theta) = clip(1/2 log2(lam_i/theta), 0, Bmax), sum b_i = C by bisection on
+// log2(theta) in [log2(min lam) - 40, log2(max lam)] (200 halvings); integer widths = floors, then one bit
+// each to the largest fractional parts (compared at 1e-9), ties to larger lam then lower index.
+// ------------------------------------------------------------------------------------------------------
+static void water_fill(const double* lam, int d, int budget, int bmax, int32_t* out) {
+  std::vector<double> b(d, 0.0), l2(d, -INFINITY);
+  int npos = 0;
+  double lo = INFINITY, hi = -INFINITY;
+  for (int i = 0; i < d; ++i)
+    if (lam[i] > 0) {
+      l2[i] = log2(lam[i]);
+      lo = std::min(lo, l2[i]);
+      hi = std::max(hi, l2[i]);
+      ++npos;
+    }
+  if (budget > 0 && npos > 0) {
+    if ((long long)budget >= (long long)bmax * npos) {
+      for (int i = 0; i < d; ++i) b[i] = lam[i] > 0 ? bmax : 0.0;
+    } else {
+      auto eval = [&](double t, std::vector<double>* dst) {
+        double sum = 0.0;
+        for (int i = 0; i < d; ++i) {
+          double x = 0.5 * (l2[i] - t);
+          x = x < 0 ? 0.0 : (x > bmax ? (double)bmax : x);
+          if (dst) (*dst)[i] = x;
+          sum += x;
+        }
+        return sum;
+      };
+      lo -= 40.0;
+      for (int it = 0; it < 200; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        if (eval(mid, nullptr) > budget) lo = mid; else hi = mid;
+      }
+      eval(0.5 * (lo + hi), &b);
+    }
+  }
+  long long used = 0;
+  std::vector<long long> fk(d);
+  for (int i = 0; i < d; ++i) {
+    out[i] = (int32_t)floor(b[i]);
+    used += out[i];
+    fk[i] = llrint((b[i] - out[i]) * 1e9);
+  }
+  long long rem = (long long)budget - used;
+  std::vector<int> cand;
+  for (int i = 0; i < d; ++i)
+    if (out[i] < bmax && lam[i] > 0) cand.push_back(i);
+  std::sort(cand.begin(), cand.end(), [&](int a, int c) {
+    if (fk[a] != fk[c]) return fk[a] > fk[c];
+    if (lam[a] != lam[c]) return lam[a] > lam[c];
+    return a < c;
+  });
+  for (size_t k = 0; k < cand.size() && rem > 0; ++k, --rem) out[cand[k]] += 1;
+}
+
+static int record_words(float bits, int d) { return (int)floor((double)bits * d / 32.0 + 1e-9); }
+
+// ------------------------------------------------------------------------------------------------------
+// calibration of one set
+// ------------------------------------------------------------------------------------------------------
+struct SetResult {
+  std::vector<float> T[2], mu[2], sigma[2];
+  std::vector<int32_t> widths[2];
+  std::vector<double> eig[2], imp[2];
+  bool ok = true;
+  std::string err;
+};
+
+static bool finite_all(const float* x, size_t n) {
+  for (size_t i = 0; i < n; ++i)
+    if (!std::isfinite(x[i])) return false;
+  return true;
+}
+
+static void moments(const float* x, int64_t n, int d, bool centre, std::vector<double>& mean,
+                    std::vector<double>& cov) {
+  mean.assign(d, 0.0);
+  cov.assign((size_t)d * d, 0.0);
+  if (centre) {
+    for (int64_t t = 0; t < n; ++t)
+      for (int i = 0; i < d; ++i) mean[i] += x[t * d + i];
+    for (int i = 0; i < d; ++i) mean[i] /= (double)n;
+  }
+  std::vector<double> row(d);
+  for (int64_t t = 0; t < n; ++t) {
+    for (int i = 0; i < d; ++i) row[i] = (double)x[t * d + i] - mean[i];
+    for (int i = 0; i < d; ++i) {
+      const double ri = row[i];
+      double* c = &cov[(size_t)i * d];
+      for (int j = i; j < d; ++j) c[j] += ri * row[j];
+    }
+  }
+  for (int i = 0; i < d; ++i)
+    for (int j = i; j < d; ++j) {
+      const double v = cov[(size_t)i * d + j] / (double)n;
+      cov[(size_t)i * d + j] = v;
+      cov[(size_t)j * d + i] = v;
+    }
+}
+
+static void build_tensor(const std::vector<double>& mu_raw, const std::vector<double>& lam,
+                         const std::vector<double>& U, const std::vector<double>& imp, int rw, int bmax,
+                         int d, SetResult& r, int t) {
+  std::vector<int32_t> w(d);
+  water_fill(imp.data(), d, 32 * rw - 32, bmax, w.data());
+  std::vector<int> order(d);
+  std::iota(order.begin(), order.end(), 0);
+  std::sort(order.begin(), order.end(), [&](int a, int b) {
+    if (w[a] != w[b]) return w[a] > w[b];
+    if (imp[a] != imp[b]) return imp[a] > imp[b];
+    return a < b;
+  });
+  r.T[t].resize((size_t)d * d);
+  r.mu[t].resize(d);
+  r.sigma[t].resize(d);
+  r.widths[t].resize(d);
+  r.eig[t].resize(d);
+  r.imp[t].resize(d);
+  for (int j = 0; j < d; ++j) {
+    const int e = order[j];
+    double m = 0.0;
+    for (int k = 0; k < d; ++k) {
+      const double u = U[(size_t)k * d + e];  // column e of U = row j of T
+      r.T[t][(size_t)j * d + k] = (float)u;
+      m += u * mu_raw[k];
+    }
+    r.mu[t][j] = (float)m;
+    r.sigma[t][j] = (float)sqrt(std::max(lam[e], 0.0));
+    r.widths[t][j] = r.sigma[t][j] > 0.f ? w[e] : 0;
+    r.eig[t][j] = lam[e];
+    r.imp[t][j] = imp[e];
+  }
+}
+
+static void calibrate_one(const kv_calib_set& s, const kv_calib_opts& o, SetResult& r) {
+  const int d = o.d;
+  if (!finite_all(s.k, (size_t)s.n_tok * d) || !finite_all(s.v, (size_t)s.n_tok * d) ||
+      !finite_all(s.q, (size_t)s.n_q * d)) {
+    r.ok = false;
+    r.err = "non-finite calibration data";
+    return;
+  }
+  std::vector<double> mk, ck, mv, cv, mq, cq;
+  moments(s.k, s.n_tok, d, true, mk, ck);
+  moments(s.v, s.n_tok, d, true, mv, cv);
+  moments(s.q, s.n_q, d, false, mq, cq);
+  std::vector<double> lk(d), uk((size_t)d * d), lv(d), uv((size_t)d * d);
+  jacobi_eigh(ck.data(), d, lk.data(), uk.data());
+  jacobi_eigh(cv.data(), d, lv.data(), uv.data());
+  // key importances: sigma_i^2 * u_i^T M_Q u_i; value importances: sigma_i^2
+  std::vector<double> ik(d), iv(d), tmp(d);
+  for (int i = 0; i < d; ++i) {
+    for (int a = 0; a < d; ++a) {
+      double acc = 0.0;
+      for (int b = 0; b < d; ++b) acc += cq[(size_t)a * d + b] * uk[(size_t)b * d + i];
+      tmp[a] = acc;
+    }
+    double w = 0.0;
+    for (int a = 0; a < d; ++a) w += uk[(size_t)a * d + i] * tmp[a];
+    ik[i] = std::max(lk[i], 0.0) * w;
+    iv[i] = std::max(lv[i], 0.0);
+  }
+  for (int i = 0; i < d; ++i)
+    if (!std::isfinite(ik[i]) || !std::isfinite(iv[i])) {
+      r.ok = false;
+      r.err = "non-finite statistics";
+      return;
+    }
+  build_tensor(mk, lk, uk, ik, record_words(o.bits_k, d), o.max_bits, d, r, 0);
+  build_tensor(mv, lv, uv, iv, record_words(o.bits_v, d), o.max_bits, d, r, 1);
+}
+
+static kv_status check_budget(float bits, int d, int bmax, int* rw_out) {
+  const int rw = record_words(bits, d);
+  KV_REQUIRE(rw >= 1 && rw <= 1 + bmax * d / 32, KV_ERR_BUDGET,
+             "budget %.4f bits/element gives %d record words (valid 1..%d)", bits, rw, 1 + bmax * d / 32);
+  *rw_out = rw;
+  return KV_OK;
+}
+
+extern "C" kv_status kv_calibrate(int n_sets, const kv_calib_set* sets, const kv_calib_opts* opts,
+                                  kv_params** out) {
+  clear_error();
+  KV_REQUIRE(sets && opts && out && n_sets >= 1, KV_ERR_INVALID_ARG, "kv_calibrate: null argument or n_sets < 1");
+  KV_REQUIRE(opts->d == D, KV_ERR_UNSUPPORTED, "kv_calibrate: d=%d unsupported (128 only)", opts->d);
+  KV_REQUIRE(opts->max_bits >= 1 && opts->max_bits <= MAX_BITS, KV_ERR_INVALID_ARG, "max_bits must be 1..8");
+  int rwk, rwv;
+  kv_status st;
+  if ((st = check_budget(opts->bits_k, opts->d, opts->max_bits, &rwk)) != KV_OK) return st;
+  if ((st = check_budget(opts->bits_v, opts->d, opts->max_bits, &rwv)) != KV_OK) return st;
+  for (int i = 0; i < n_sets; ++i) {
+    KV_REQUIRE(sets[i].k && sets[i].v && sets[i].q, KV_ERR_INVALID_ARG, "set %d: null pointer", i);
+    KV_REQUIRE(sets[i].n_tok >= 2 && sets[i].n_q >= 1, KV_ERR_INVALID_ARG, "set %d: need n_tok >= 2, n_q >= 1", i);
+  }
+  std::vector<SetResult> res(n_sets);
+  int nth = opts->n_threads > 0 ? opts->n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
+  nth = std::min(nth, n_sets);
+  std::atomic<int> next{0};
+  auto worker = [&]() {
+    for (int i; (i = next.fetch_add(1)) < n_sets;) calibrate_one(sets[i], *opts, res[i]);
+  };
+  std::vector<std::thread> pool;
+  for (int t = 1; t < nth; ++t) pool.emplace_back(worker);
+  worker();
+  for (auto& th : pool) th.join();
+  for (int i = 0; i < n_sets; ++i)
+    KV_REQUIRE(res[i].ok, KV_ERR_NUMERIC, "set %d: %s", i, res[i].err.c_str());
+  kv_params* p = new kv_params();
+  p->d = opts->d;
+  p->n_sets = n_sets;
+  p->max_bits = opts->max_bits;
+  p->r_words[0] = rwk;
+  p->r_words[1] = rwv;
+  for (int t = 0; t < 2; ++t) {
+    for (int i = 0; i < n_sets; ++i) {
+      auto app = [](auto& dst, const auto& src) { dst.insert(dst.end(), src.begin(), src.end()); };
+      app(p->T[t], res[i].T[t]);
+      app(p->mu[t], res[i].mu[t]);
+      app(p->sigma[t], res[i].sigma[t]);
+      app(p->widths[t], res[i].widths[t]);
+      app(p->eig[t], res[i].eig[t]);
+      app(p->imp[t], res[i].imp[t]);
+    }
+  }
+  *out = p;
+  return KV_OK;
+}
+
+extern "C" kv_status kv_params_from_arrays(int d, int n_sets, const float* T_k, const float* mu_k,
+                                           const float* sigma_k, const int32_t* widths_k, int r_words_k,
+                                           const float* T_v, const float* mu_v, const float* sigma_v,
+                                           const int32_t* widths_v, int r_words_v, kv_params** out) {
+  clear_error();
+  KV_REQUIRE(out && T_k && mu_k && sigma_k && widths_k && T_v && mu_v && sigma_v && widths_v && n_sets >= 1,
+             KV_ERR_INVALID_ARG, "kv_params_from_arrays: null argument");
+  KV_REQUIRE(d == D, KV_ERR_UNSUPPORTED, "d=%d unsupported (128 only)", d);
+  const float* Ts[2] = {T_k, T_v};
+  const float* mus[2] = {mu_k, mu_v};
+  const float* sgs[2] = {sigma_k, sigma_v};
+  const int32_t* ws[2] = {widths_k, widths_v};
+  const int rws[2] = {r_words_k, r_words_v};
+  kv_params* p = new kv_params();
+  p->d = d;
+  p->n_sets = n_sets;
+  p->max_bits = MAX_BITS;
+  for (int t = 0; t < 2; ++t) {
+    if (rws[t] < 1 || rws[t] > MAX_RW) {
+      delete p;
+      KV_REQUIRE(false, KV_ERR_BUDGET, "r_words %d out of range 1..%d", rws[t], MAX_RW);
+    }
+    p->r_words[t] = rws[t];
+    const size_t n = (size_t)n_sets * d;
+    p->T[t].assign(Ts[t], Ts[t] + n * d);
+    p->mu[t].assign(mus[t], mus[t] + n);
+    p->sigma[t].assign(sgs[t], sgs[t] + n);
+    p->widths[t].assign(ws[t], ws[t] + n);
+    p->eig[t].resize(n);
+    p->imp[t].assign(n, 0.0);
+    for (int s = 0; s < n_sets; ++s) {
+      long long sum = 0;
+      for (int j = 0; j < d; ++j) {
+        const size_t i = (size_t)s * d + j;
+        if (!(p->sigma[t][i] > 0.f)) p->widths[t][i] = 0;
+        if (p->widths[t][i] < 0 || p->widths[t][i] > MAX_BITS) {
+          delete p;
+          KV_REQUIRE(false, KV_ERR_INVALID_ARG, "set %d channel %d: width out of range 0..8", s, j);
+        }
+        if (j > 0 && p->widths[t][i] > 0 && p->widths[t][i - 1] == 0) {
+          delete p;
+          KV_REQUIRE(false, KV_ERR_INVALID_ARG,
+                     "set %d: channels with width > 0 must form a prefix of the storage order", s);
+        }
+        sum += p->widths[t][i];
+        p->eig[t][i] = (double)p->sigma[t][i] * p->sigma[t][i];
+      }
+      if (sum > 32LL * rws[t] - 32) {
+        delete p;
+        KV_REQUIRE(false, KV_ERR_BUDGET, "set %d: widths use %lld bits > %d", s, sum, 32 * rws[t] - 32);
+      }
+    }
+  }
+  *out = p;
+  return KV_OK;
+}
+
+// ------------------------------------------------------------------------------------------------------
+// device copy of the table, with the derived arrays the kernels use
+// ------------------------------------------------------------------------------------------------------
+static uint16_t f32_to_bf16_rn(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  const uint32_t r = u + 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(r >> 16);
+}
+static float bf16_to_f32(uint16_t h) {
+  const uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+// Unpack descriptor of channels 4q..4q+3 (storage order): the decode kernel extracts the four codes with
+// one funnel shift of record words (1+wq, 2+wq) by sh, then builds two fp16 pairs:
+//   pair01 = (x & m0) | ((x << s1) & m1hi),  pair23 = (y & m2) | ((y << s3) & m3hi),  y = x >> s2.
+static void quad_descriptor(const int32_t* w, const uint16_t* off, int q, uint4* out2) {
+  const int j = 4 * q;
+  const int b0 = w[j], b1 = w[j + 1], b2 = w[j + 2], b3 = w[j + 3];
+  const int o = (b0 + b1 + b2 + b3) ? off[j] : 0;
+  const uint32_t wq = (uint32_t)(o / 32), sh = (uint32_t)(o % 32);
+  const uint32_t s1 = 16 - b0, s2 = b0 + b1, s3 = 16 - b2;
+  auto m = [](int b) { return b ? ((1u << b) - 1u) : 0u; };
+  out2[0] = make_uint4(wq | (sh << 8) | (s1 << 16) | (s2 << 24), m(b0), m(b1) << 16, s3);
+  out2[1] = make_uint4(m(b2), m(b3) << 16, 0u, 0u);
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
+  clear_error();
+  KV_REQUIRE(p, KV_ERR_INVALID_ARG, "kv_params_upload: null");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (p->dev_blob) {
+    cudaFree(p->dev_blob);
+    p->dev_blob = nullptr;
+  }
+  const int S = p->n_sets, d = p->d;
+  // host staging of every device array, laid out in one blob
+  struct Piece { size_t off, bytes; };
+  std::vector<uint8_t> blob;
+  auto reserve = [&](size_t bytes) {
+    const size_t off = align_up(blob.size(), 256);
+    blob.resize(off + bytes);
+    return Piece{off, bytes};
+  };
+  Piece pT[2], pTT[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], poff[2], pnz[2], pq[2];
+  for (int t = 0; t < 2; ++t) {
+    pT[t] = reserve((size_t)S * d * d * 4);
+    pTT[t] = reserve((size_t)S * d * d * 4);
+    pTs[t] = reserve((size_t)S * 3 * d * d * 2);
+    pmu[t] = reserve((size_t)S * d * 4);
+    psg[t] = reserve((size_t)S * d * 4);
+    pinv[t] = reserve((size_t)S * d * 4);
+    pbase[t] = reserve((size_t)S * d * 4);
+    pw[t] = reserve((size_t)S * d);
+    poff[t] = reserve((size_t)S * d * 2);
+    pnz[t] = reserve((size_t)S * 4);
+    pq[t] = reserve((size_t)S * 32 * 2 * sizeof(uint4));
+  }
+  for (int t = 0; t < 2; ++t) {
+    float* T = (float*)&blob[pT[t].off];
+    float* TT = (float*)&blob[pTT[t].off];
+    uint16_t* Ts = (uint16_t*)&blob[pTs[t].off];
+    float* mu = (float*)&blob[pmu[t].off];
+    float* sg = (float*)&blob[psg[t].off];
+    float* inv = (float*)&blob[pinv[t].off];
+    float* base = (float*)&blob[pbase[t].off];
+    uint8_t* w8 = (uint8_t*)&blob[pw[t].off];
+    uint16_t* of = (uint16_t*)&blob[poff[t].off];
+    int32_t* nz = (int32_t*)&blob[pnz[t].off];
+    uint4* qd = (uint4*)&blob[pq[t].off];
+    for (int s = 0; s < S; ++s) {
+      const float* Tsrc = &p->T[t][(size_t)s * d * d];
+      for (int j = 0; j < d; ++j)
+        for (int k = 0; k < d; ++k) {
+          const float v = Tsrc[(size_t)j * d + k];
+          T[(size_t)s * d * d + (size_t)j * d + k] = v;
+          TT[(size_t)s * d * d + (size_t)k * d + j] = v;
+          const uint16_t hi = f32_to_bf16_rn(v);
+          const float r1 = v - bf16_to_f32(hi);
+          const uint16_t mid = f32_to_bf16_rn(r1);
+          const float r2 = r1 - bf16_to_f32(mid);
+          const uint16_t lo = f32_to_bf16_rn(r2);
+          Ts[((size_t)s * 3 + 0) * d * d + (size_t)j * d + k] = hi;
+          Ts[((size_t)s * 3 + 1) * d * d + (size_t)j * d + k] = mid;
+          Ts[((size_t)s * 3 + 2) * d * d + (size_t)j * d + k] = lo;
+        }
+      int n_nz = 0, bitpos = 0;
+      std::vector<int32_t> wv(d);
+      std::vector<uint16_t> ov(d);
+      for (int j = 0; j < d; ++j) {
+        const size_t i = (size_t)s * d + j;
+        mu[i] = p->mu[t][i];
+        sg[i] = p->sigma[t][i];
+        const int w = p->sigma[t][i] > 0.f ? p->widths[t][i] : 0;
+        inv[i] = w > 0 ? (float)(1.0 / (double)p->sigma[t][i]) : 0.f;
+        w8[i] = (uint8_t)w;
+        wv[j] = w;
+        of[i] = (uint16_t)bitpos;
+        ov[j] = (uint16_t)bitpos;
+        bitpos += w;
+        if (w > 0) n_nz = j + 1;
+      }
+      nz[s] = n_nz;
+      for (int k = 0; k < d; ++k) {
+        double acc = 0.0;
+        for (int j = 0; j < d; ++j) acc += (double)Tsrc[(size_t)j * d + k] * (double)p->mu[t][(size_t)s * d + j];
+        base[(size_t)s * d + k] = (float)acc;
+      }
+      for (int q = 0; q < 32; ++q) quad_descriptor(wv.data(), ov.data(), q, &qd[((size_t)s * 32 + q) * 2]);
+    }
+  }
+  void* dblob = nullptr;
+  e = cudaMalloc(&dblob, blob.size());
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(params)");
+  e = cudaMemcpyAsync(dblob, blob.data(), blob.size(), cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    cudaFree(dblob);
+    return cuda_fail(e, "upload params");
+  }
+  p->dev_blob = dblob;
+  p->dev_bytes = blob.size();
+  p->device = dev;
+  uint8_t* b = (uint8_t*)dblob;
+  for (int t = 0; t < 2; ++t) {
+    TensorDev& td = p->dev.t[t];
+    td.T = (const float*)(b + pT[t].off);
+    td.TT = (const float*)(b + pTT[t].off);
+    td.Tsplit = (const __nv_bfloat16*)(b + pTs[t].off);
+    td.mu = (const float*)(b + pmu[t].off);
+    td.sigma = (const float*)(b + psg[t].off);
+    td.inv_sigma = (const float*)(b + pinv[t].off);
+    td.base = (const float*)(b + pbase[t].off);
+    td.widths = (const uint8_t*)(b + pw[t].off);
+    td.offs = (const uint16_t*)(b + poff[t].off);
+    td.nz = (const int32_t*)(b + pnz[t].off);
+    td.quads = (const uint4*)(b + pq[t].off);
+    td.r_words = p->r_words[t];
+  }
+  p->dev.n_sets = S;
+  return KV_OK;
+}
+
+extern "C" int kv_params_num_sets(const kv_params* p) { return p ? p->n_sets : 0; }
+extern "C" int kv_params_record_words(const kv_params* p, int tensor) {
+  return (p && (tensor == 0 || tensor == 1)) ? p->r_words[tensor] : 0;
+}
+
+extern "C" kv_status kv_params_info(const kv_params* p, int set, int tensor, int32_t* widths, double* eigvals,
+                                    double* importance, float* T, float* mu, float* sigma) {
+  clear_error();
+  KV_REQUIRE(p && set >= 0 && set < p->n_sets && (tensor == 0 || tensor == 1), KV_ERR_INVALID_ARG,
+             "kv_params_info: bad argument");
+  const int d = p->d;
+  const size_t o = (size_t)set * d;
+  for (int j = 0; j < d; ++j) {
+    if (widths) widths[j] = p->widths[tensor][o + j];
+    if (eigvals) eigvals[j] = p->eig[tensor][o + j];
+    if (importance) importance[j] = p->imp[tensor][o + j];
+    if (mu) mu[j] = p->mu[tensor][o + j];
+    if (sigma) sigma[j] = p->sigma[tensor][o + j];
+  }
+  if (T) memcpy(T, &p->T[tensor][o * d], (size_t)d * d * 4);
+  return KV_OK;
+}
+
+extern "C" void kv_params_free(kv_params* p) {
+  if (!p) return;
+  if (p->dev_blob) cudaFree(p->dev_blob);
+  delete p;
+}
+
+// ------------------------------------------------------------------------------------------------------
+// persistence: "KVTC" magic, version, dims, arrays, CRC-32 (IEEE 802.3 polynomial, reflected) of the payload
+// ------------------------------------------------------------------------------------------------------
+static uint32_t crc32(const uint8_t* data, size_t n) {
+  uint32_t c = 0xFFFFFFFFu;
+  for (size_t i = 0; i < n; ++i) {
+    c ^= data[i];
+    for (int k = 0; k < 8; ++k) c = (c >> 1) ^ (0xEDB88320u & (0u - (c & 1u)));
+  }
+  return ~c;
+}
+
+static const uint32_t FILE_MAGIC = 0x4354564Bu;  // "KVTC"
+static const uint32_t FILE_VERSION = 1;
+
+extern "C" kv_status kv_params_save(const kv_params* p, const char* path) {
+  clear_error();
+  KV_REQUIRE(p && path, KV_ERR_INVALID_ARG, "kv_params_save: null");
+  std::vector<uint8_t> pay;
+  auto put = [&](const void* src, size_t n) {
+    const uint8_t* s = (const uint8_t*)src;
+    pay.insert(pay.end(), s, s + n);
+  };
+  int32_t hdr[5] = {p->d, p->n_sets, p->max_bits, p->r_words[0], p->r_words[1]};
+  put(hdr, sizeof(hdr));
+  for (int t = 0; t < 2; ++t) {
+    put(p->T[t].data(), p->T[t].size() * 4);
+    put(p->mu[t].data(), p->mu[t].size() * 4);
+    put(p->sigma[t].data(), p->sigma[t].size() * 4);
+    put(p->widths[t].data(), p->widths[t].size() * 4);
+    put(p->eig[t].data(), p->eig[t].size() * 8);
+    put(p->imp[t].data(), p->imp[t].size() * 8);
+  }
+  FILE* f = fopen(path, "wb");
+  KV_REQUIRE(f, KV_ERR_IO, "cannot open %s for writing", path);
+  const uint32_t head[4] = {FILE_MAGIC, FILE_VERSION, (uint32_t)pay.size(), crc32(pay.data(), pay.size())};
+  bool ok = fwrite(head, sizeof(head), 1, f) == 1 && fwrite(pay.data(), 1, pay.size(), f) == pay.size();
+  ok = (fclose(f) == 0) && ok;
+  KV_REQUIRE(ok, KV_ERR_IO, "write to %s failed", path);
+  return KV_OK;
+}
+
+extern "C" kv_status kv_params_load(const char* path, kv_params** out) {
+  clear_error();
+  KV_REQUIRE(path && out, KV_ERR_INVALID_ARG, "kv_params_load: null");
+  FILE* f = fopen(path, "rb");
+  KV_REQUIRE(f, KV_ERR_IO, "cannot open %s", path);
+  uint32_t head[4];
+  if (fread(head, sizeof(head), 1, f) != 1 || head[0] != FILE_MAGIC || head[1] != FILE_VERSION) {
+    fclose(f);
+    KV_REQUIRE(false, KV_ERR_IO, "%s: not a version-%u parameter file", path, FILE_VERSION);
+  }
+  std::vector<uint8_t> pay(head[2]);
+  const size_t got = fread(pay.data(), 1, pay.size(), f);
+  fclose(f);
+  KV_REQUIRE(got == pay.size(), KV_ERR_IO, "%s: truncated", path);
+  KV_REQUIRE(crc32(pay.data(), pay.size()) == head[3], KV_ERR_IO, "%s: checksum mismatch", path);
+  size_t pos = 0;
+  auto get = [&](void* dst, size_t n) {
+    if (pos + n > pay.size()) return false;
+    memcpy(dst, &pay[pos], n);
+    pos += n;
+    return true;
+  };
+  int32_t hdr[5];
+  KV_REQUIRE(get(hdr, sizeof(hdr)), KV_ERR_IO, "%s: truncated header", path);
+  KV_REQUIRE(hdr[0] == D && hdr[1] >= 1 && hdr[3] >= 1 && hdr[4] >= 1 && hdr[3] <= MAX_RW && hdr[4] <= MAX_RW,
+             KV_ERR_IO, "%s: bad dimensions", path);
+  kv_params* p = new kv_params();
+  p->d = hdr[0];
+  p->n_sets = hdr[1];
+  p->max_bits = hdr[2];
+  p->r_words[0] = hdr[3];
+  p->r_words[1] = hdr[4];
+  const size_t n = (size_t)p->n_sets * p->d;
+  bool ok = true;
+  for (int t = 0; t < 2 && ok; ++t) {
+    p->T[t].resize(n * p->d);
+    p->mu[t].resize(n);
+    p->sigma[t].resize(n);
+    p->widths[t].resize(n);
+    p->eig[t].resize(n);
+    p->imp[t].resize(n);
+    ok = get(p->T[t].data(), n * p->d * 4) && get(p->mu[t].data(), n * 4) && get(p->sigma[t].data(), n * 4) &&
+         get(p->widths[t].data(), n * 4) && get(p->eig[t].data(), n * 8) && get(p->imp[t].data(), n * 8);
+  }
+  if (!ok || pos != pay.size()) {
+    delete p;
+    KV_REQUIRE(false, KV_ERR_IO, "%s: payload size mismatch", path);
+  }
+  *out = p;
+  return KV_OK;
+}
+
+// ------------------------------------------------------------------------------------------------------
+// sizing
+// ------------------------------------------------------------------------------------------------------
+extern "C" size_t kv_cache_bytes(const kv_params* p, int tensor, int B, int Hkv, int64_t T_cap) {
+  if (!p || (tensor != 0 && tensor != 1) || B < 1 || Hkv < 1 || T_cap < 1) return 0;
+  return (size_t)B * Hkv * (size_t)T_cap * p->r_words[tensor] * 4;
+}
+
+static int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+
+extern "C" size_t kv_decode_workspace_bytes(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap) {
+  if (!p || B < 1 || Hkv < 1 || Hq < Hkv || T_cap < 1) return 0;
+  return kvtc::decode_layout(B, Hkv, T_cap, current_device()).total;
+}
+
+extern "C" size_t kv_decode_bf16_workspace_bytes(int B, int Hkv, int Hq, int64_t T_cap) {
+  if (B < 1 || Hkv < 1 || Hq < Hkv || T_cap < 1) return 0;
+  return kvtc::decode_bf16_layout(B, Hkv, T_cap, current_device()).total;
+}
+
+// ------------------------------------------------------------------------------------------------------
+// validated entry points
+// ------------------------------------------------------------------------------------------------------
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static kv_status check_params_on_device(const kv_params* p) {
+  KV_REQUIRE(p, KV_ERR_INVALID_ARG, "null parameter table");
+  KV_REQUIRE(p->dev_blob, KV_ERR_INVALID_ARG, "parameter table not uploaded (kv_params_upload)");
+  KV_REQUIRE(p->device == current_device(), KV_ERR_INVALID_ARG,
+             "parameter table uploaded to device %d, current device is %d", p->device, current_device());
+  return KV_OK;
+}
+
+static kv_status check_cache(const kv_params* p, const kv_cache* c, int B) {
+  KV_REQUIRE(c && c->k_rec && c->v_rec, KV_ERR_INVALID_ARG, "null cache");
+  KV_REQUIRE(aligned16(c->k_rec) && aligned16(c->v_rec), KV_ERR_INVALID_ARG, "cache buffers must be 16-byte aligned");
+  KV_REQUIRE(c->B >= 1 && c->Hkv >= 1 && c->T_cap >= 16 && c->T_cap % 16 == 0, KV_ERR_INVALID_ARG,
+             "cache dims B=%d Hkv=%d T_cap=%lld (T_cap must be a positive multiple of 16)", c->B, c->Hkv,
+             (long long)c->T_cap);
+  KV_REQUIRE(B >= 1 && B <= c->B, KV_ERR_INVALID_ARG, "batch %d outside cache batch %d", B, c->B);
+  const long long need = c->per_seq_params ? (long long)c->B * c->Hkv : c->Hkv;
+  KV_REQUIRE(need <= p->n_sets, KV_ERR_INVALID_ARG, "cache needs %lld parameter sets, table has %d", need, p->n_sets);
+  return KV_OK;
+}
+
+static int g_encode_path = 0;
+
+extern "C" kv_status kv_debug_set_encode_path(int path) {
+  KV_REQUIRE(path >= 0 && path <= 2, KV_ERR_INVALID_ARG, "encode path 0..2");
+  g_encode_path = path;
+  return KV_OK;
+}
+
+extern "C" kv_status kv_encode(const kv_params* p, const kv_cache* c, const void* k, const void* v, int dtype,
+                               int B, int64_t t_new, const int64_t* dst_pos_dev, kv_stream_t stream) {
+  clear_error();
+  kv_status st;
+  if ((st = check_params_on_device(p)) != KV_OK) return st;
+  if ((st = check_cache(p, c, B)) != KV_OK) return st;
+  KV_REQUIRE(dtype == KV_DTYPE_BF16 || dtype == KV_DTYPE_F32, KV_ERR_UNSUPPORTED, "dtype %d unsupported", dtype);
+  KV_REQUIRE(t_new >= 0 && t_new <= c->T_cap, KV_ERR_INVALID_ARG, "t_new=%lld outside 0..T_cap", (long long)t_new);
+  if (t_new == 0) return KV_OK;
+  KV_REQUIRE(k && v && dst_pos_dev, KV_ERR_INVALID_ARG, "null k, v or dst_pos");
+  KV_REQUIRE(aligned16(k) && aligned16(v), KV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  return kvtc::launch_encode(p->dev, *c, k, v, dtype, B, t_new, dst_pos_dev, g_encode_path, (cudaStream_t)stream);
+}
+
+extern "C" kv_status kv_attend_decode(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
+                                      const int32_t* seq_lens_dev, float softmax_scale, float* out,
+                                      void* workspace, size_t ws_bytes, kv_stream_t stream) {
+  clear_error();
+  kv_status st;
+  if ((st = check_params_on_device(p)) != KV_OK) return st;
+  if ((st = check_cache(p, c, B)) != KV_OK) return st;
+  KV_REQUIRE(q && seq_lens_dev && out && workspace, KV_ERR_INVALID_ARG, "null q, seq_lens, out or workspace");
+  KV_REQUIRE(Hq >= c->Hkv && Hq % c->Hkv == 0, KV_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, c->Hkv);
+  KV_REQUIRE(Hq / c->Hkv <= MAX_G, KV_ERR_UNSUPPORTED, "g = Hq/Hkv = %d > 8", Hq / c->Hkv);
+  KV_REQUIRE(aligned16(q) && aligned16(out) && aligned16(workspace), KV_ERR_INVALID_ARG,
+             "q, out and workspace must be 16-byte aligned");
+  KV_REQUIRE(std::isfinite(softmax_scale), KV_ERR_INVALID_ARG, "non-finite softmax scale");
+  const DecodeLayout L = kvtc::decode_layout(B, c->Hkv, c->T_cap, current_device());
+  KV_REQUIRE(ws_bytes >= L.total, KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+  return kvtc::launch_decode(p->dev, *c, q, B, Hq, seq_lens_dev, softmax_scale, out, workspace, L,
+                             (cudaStream_t)stream);
+}
+
+extern "C" kv_status kv_attend_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap,
+                                           const void* q, const int32_t* seq_lens_dev, float softmax_scale,
+                                           float* out, void* workspace, size_t ws_bytes, kv_stream_t stream) {
+  clear_error();
+  KV_REQUIRE(k && v && q && seq_lens_dev && out && workspace, KV_ERR_INVALID_ARG, "null argument");
+  KV_REQUIRE(B >= 1 && Hkv >= 1 && T_cap >= 16 && T_cap % 16 == 0, KV_ERR_INVALID_ARG,
+             "bad dims B=%d Hkv=%d T_cap=%lld", B, Hkv, (long long)T_cap);
+  KV_REQUIRE(Hq >= Hkv && Hq % Hkv == 0, KV_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+  KV_REQUIRE(Hq / Hkv <= MAX_G, KV_ERR_UNSUPPORTED, "g = %d > 8", Hq / Hkv);
+  KV_REQUIRE(aligned16(k) && aligned16(v) && aligned16(q) && aligned16(out) && aligned16(workspace),
+             KV_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  const DecodeLayout L = kvtc::decode_bf16_layout(B, Hkv, T_cap, current_device());
+  KV_REQUIRE(ws_bytes >= L.total, KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+  return kvtc::launch_decode_bf16(k, v, B, Hkv, Hq, T_cap, q, seq_lens_dev, softmax_scale, out, workspace, L,
+                                  (cudaStream_t)stream);
+}
+
+extern "C" kv_status kv_check_status(kv_stream_t stream) {
+  clear_error();
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "stream");
+  unsigned st = 0;
+  kv_status r = kvtc::read_and_clear_device_status(&st);
+  if (r != KV_OK) return r;
+  if (st & ST_TIMEOUT) {
+    kvtc::set_error("a device-side bounded wait ran out");
+    return KV_ERR_TIMEOUT;
+  }
+  if (st & ST_BAD_INDEX) {
+    kvtc::set_error("a kernel skipped an out-of-range record write");
+    return KV_ERR_DEVICE;
+  }
+  return KV_OK;
+}
+
+extern "C" kv_status kv_debug_quantize_pack(const kv_params* p, int set, int tensor, const float* y_dev, int64_t n,
+                                            uint32_t* rec_dev, int variant, kv_stream_t stream) {
+  clear_error();
+  kv_status st;
+  if ((st = check_params_on_device(p)) != KV_OK) return st;
+  KV_REQUIRE(set >= 0 && set < p->n_sets && (tensor == 0 || tensor == 1) && n >= 0 && (variant == 0 || variant == 1),
+             KV_ERR_INVALID_ARG, "kv_debug_quantize_pack: bad argument");
+  if (n == 0) return KV_OK;
+  KV_REQUIRE(y_dev && rec_dev, KV_ERR_INVALID_ARG, "null buffer");
+  return kvtc::launch_debug_quantize_pack(p->dev, set, tensor, y_dev, n, rec_dev, variant, (cudaStream_t)stream);
+}
+
+extern "C" kv_status kv_debug_unpack(const kv_params* p, int set, int tensor, const uint32_t* rec_dev, int64_t n,
+                                     uint16_t* codes_dev, kv_stream_t stream) {
+  clear_error();
+  kv_status st;
+  if ((st = check_params_on_device(p)) != KV_OK) return st;
+  KV_REQUIRE(set >= 0 && set < p->n_sets && (tensor == 0 || tensor == 1) && n >= 0, KV_ERR_INVALID_ARG,
+             "kv_debug_unpack: bad argument");
+  if (n == 0) return KV_OK;
+  KV_REQUIRE(rec_dev && codes_dev, KV_ERR_INVALID_ARG, "null buffer");
+  return kvtc::launch_debug_unpack(p->dev, set, tensor, rec_dev, n, codes_dev, (cudaStream_t)stream);
+}
+
+extern "C" kv_status kv_debug_water_fill(const double* lam, int d, int budget_bits, int max_bits, int32_t* widths) {
+  clear_error();
+  KV_REQUIRE(lam && widths && d >= 1 && budget_bits >= 0 && max_bits >= 1 && max_bits <= 16, KV_ERR_INVALID_ARG,
+             "kv_debug_water_fill: bad argument");
+  water_fill(lam, d, budget_bits, max_bits, widths);
+  return KV_OK;
+}
+
+extern "C" kv_status kv_debug_eigh(const double* sym, int d, double* evals, double* evecs) {
+  clear_error();
+  KV_REQUIRE(sym && evals && evecs && d >= 1 && d <= 1024, KV_ERR_INVALID_ARG, "kv_debug_eigh: bad argument");
+  jacobi_eigh(sym, d, evals, evecs);
+  return KV_OK;
+}
+
+extern "C" kv_status kv_debug_set_wait_limit_ns(long long ns) {
+  KV_REQUIRE(ns > 0, KV_ERR_INVALID_ARG, "wait limit must be positive");
+  kvtc::set_wait_limit_ns(ns);
+  return KV_OK;
+}
+
+extern "C" kv_status kv_debug_wait_timeout_selftest(kv_stream_t stream) {
+  clear_error();
+  return kvtc::launch_wait_selftest((cudaStream_t)stream);
+}

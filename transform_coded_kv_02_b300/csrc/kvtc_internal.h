@@ -1,0 +1,90 @@
+// Internal declarations shared by the host library (kvtc_host.cpp) and the kernels (kvtc_kernels.cu).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/kvtc.h"
+
+namespace kvtc {
+
+constexpr int D = 128;          // head dimension
+constexpr int MAX_BITS = 8;     // largest channel width in the library
+constexpr int MAX_G = 8;        // query heads per KV head
+constexpr int MAX_RW = 1 + MAX_BITS * D / 32;  // 33 record words
+
+// device status bits (read by kv_check_status)
+constexpr unsigned ST_TIMEOUT = 1u;
+constexpr unsigned ST_BAD_INDEX = 2u;
+
+// One tensor's (K or V) parameters for all sets, device pointers. Arrays are set-major.
+struct TensorDev {
+  const float* T;                  // [S][D][D]  rows = storage channels
+  const float* TT;                 // [S][D][D]  TT[k][j] = T[j][k]
+  const __nv_bfloat16* Tsplit;     // [S][3][D][D]  T = hi + mid + lo, each bf16
+  const float* mu;                 // [S][D]  rotated means (storage order)
+  const float* sigma;              // [S][D]
+  const float* inv_sigma;          // [S][D]  fp32(1/sigma) computed in double; 0 for zero-width
+  const float* base;               // [S][D]  T^T mu (original-basis vector of the all-mean record)
+  const uint8_t* widths;           // [S][D]
+  const uint16_t* offs;            // [S][D]  bit offset of each channel's code in the code area
+  const int32_t* nz;               // [S]     number of channels with width > 0 (a prefix)
+  const uint4* quads;              // [S][32][2] unpack descriptors of channel quads (see kernels)
+  int r_words;                     // record words per token (same for every set)
+};
+
+struct ParamsDev {
+  TensorDev t[2];
+  int n_sets;
+};
+
+// host-side error message of the calling thread
+void set_error(const char* fmt, ...);
+void clear_error();
+
+// Kernel launchers (kvtc_kernels.cu). They assume validated arguments.
+kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, const void* v, int dtype,
+                        int B, int64_t t_new, const int64_t* dst_pos, int path, cudaStream_t s);
+struct DecodeLayout {
+  int splits;
+  int chunk;                  // tokens per split, multiple of the decode tile
+  size_t off_qa, off_qc, off_cnt, off_part, total;
+};
+DecodeLayout decode_layout(int B, int Hkv, int64_t T_cap, int device);
+DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device);
+kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
+                        const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
+                        cudaStream_t s);
+kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap,
+                             const void* q, const int32_t* seq_lens, float scale, float* out, void* ws,
+                             const DecodeLayout& L, cudaStream_t s);
+kv_status launch_debug_quantize_pack(const ParamsDev& P, int set, int tensor, const float* y, int64_t n,
+                                     uint32_t* rec, int variant, cudaStream_t s);
+kv_status launch_debug_unpack(const ParamsDev& P, int set, int tensor, const uint32_t* rec, int64_t n,
+                              uint16_t* codes, cudaStream_t s);
+kv_status launch_wait_selftest(cudaStream_t s);
+void set_wait_limit_ns(long long ns);
+kv_status read_and_clear_device_status(unsigned* out);
+
+}  // namespace kvtc
+
+// Host-side parameter table.
+struct kv_params {
+  int d = 0;
+  int n_sets = 0;
+  int max_bits = 8;
+  int r_words[2] = {0, 0};
+  std::vector<float> T[2];         // [S][D][D]
+  std::vector<float> mu[2];        // [S][D]
+  std::vector<float> sigma[2];     // [S][D]
+  std::vector<int32_t> widths[2];  // [S][D]
+  std::vector<double> eig[2];      // [S][D] variances of the rotated channels (storage order)
+  std::vector<double> imp[2];      // [S][D] importances (storage order)
+  int device = -1;
+  void* dev_blob = nullptr;
+  size_t dev_bytes = 0;
+  kvtc::ParamsDev dev{};
+};

@@ -1,0 +1,1048 @@
+// sm_103a kernels of the transform-coded KV cache and their launchers.
+//
+//  encode_warp_kernel   one warp per (tensor, sequence, head, token): y = T x with CUDA-core FMAs from the
+//                       transposed transform, then the warp quantiser/packer (append path, fp32 inputs).
+//  qprep_kernel         per (sequence, KV head): q~ = T_K q for the g query heads, folded constants
+//                       C0 = a q~.mu, C1 = a sum q~_j sigma_j, and q'_j = a q~_j sigma_j 2^-b_j split into
+//                       fp16 hi + lo rows of a 16-row MMA operand (all scaled by log2 e for exp2).
+//  decode_kernel        split-K flash-decode over packed records: 1-D bulk copies of record tiles into a
+//                       shared-memory ring (mbarriers, bounded waits), cooperative unpack to fp16 (c + 1/2)
+//                       tiles, logits and P.V on warp MMAs, online softmax in registers, accumulation in the
+//                       rotated value basis; the last CTA of each (sequence, KV head) merges the splits and
+//                       inverse-rotates once.
+//  decode_bf16_kernel   the same split-K structure over an uncompressed bf16 cache (measurement comparator).
+//
+// Method sources: "KV Cache Compression Through the Lens of Transform Coding" (AATC), Key points;
+// "SPECTRA ..." abstract; "SPHERICAL KV ..." page, third abstract (NOVA-KV: decode reads the cache every step
+// and is bandwidth-bound; reconstruction must stay cheap).
+//
+// Decode algebra (rotated domain). With y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j) for b_j > 0:
+//   a q.k^ = a (T q).y^ = C0 + z C1 + s sum_{b_j>0} q'_j (c_j + 1/2)
+//   sum_t p_t v^_t = T_V^T o^,  o^_j = mu_j + sigma_j (Z + 2^-b_j A_j) / l for b_j > 0 (mu_j otherwise),
+//   Z = sum_t p_t z_t, A_j = sum_t p_t s_t (c_tj + 1/2), l = sum_t p_t.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdio.h>
+
+#include <algorithm>
+
+#include "kvtc_codec.cuh"
+#include "kvtc_internal.h"
+#include "kvtc_ptx.cuh"
+
+namespace kvtc {
+
+static long long g_wait_limit_ns = 2000000000LL;
+
+void set_wait_limit_ns(long long ns) { g_wait_limit_ns = ns; }
+
+static kv_status launch_check(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("%s: %s", what, cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
+  return KV_OK;
+}
+
+kv_status read_and_clear_device_status(unsigned* out) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+  if (e != cudaSuccess) {
+    set_error("device status: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
+  *out = v;
+  return KV_OK;
+}
+
+__device__ __forceinline__ float bf16_bits_f(uint32_t b) { return __uint_as_float(b << 16); }
+
+// ======================================================================================================
+// encode: warp per token
+// ======================================================================================================
+struct EncArgs {
+  const void* src[2];
+  uint32_t* dst[2];
+  const int64_t* dst_pos;
+  int B, Hkv, per_seq;
+  long long t_new, T_cap;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) encode_warp_kernel(ParamsDev P, EncArgs a) {
+  __shared__ uint32_t rec_s[8][MAX_RW + 3];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long per_tensor = (long long)a.B * a.Hkv * a.t_new;
+  const long long idx = (long long)blockIdx.x * 8 + warp;
+  if (idx >= 2 * per_tensor) return;
+  const int tensor = (int)(idx / per_tensor);
+  long long r = idx - (long long)tensor * per_tensor;
+  const long long t = r % a.t_new;
+  r /= a.t_new;
+  const int h = (int)(r % a.Hkv);
+  const int b = (int)(r / a.Hkv);
+  const int set = a.per_seq ? b * a.Hkv + h : h;
+  const TensorDev& td = P.t[tensor];
+  const size_t xo = (((size_t)b * a.Hkv + h) * a.t_new + t) * D + 4 * lane;
+  float x[4];
+  if (BF16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.src[tensor]) + xo);
+    x[0] = bf16_bits_f(u.x & 0xFFFFu);
+    x[1] = bf16_bits_f(u.x >> 16);
+    x[2] = bf16_bits_f(u.y & 0xFFFFu);
+    x[3] = bf16_bits_f(u.y >> 16);
+  } else {
+    const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(a.src[tensor]) + xo);
+    x[0] = f.x;
+    x[1] = f.y;
+    x[2] = f.z;
+    x[3] = f.w;
+  }
+  // y_j = sum_k T[j][k] x_k for j = 4 lane + i, reading row k of T^T (coalesced float4 per lane)
+  const float4* TT = reinterpret_cast<const float4*>(td.TT + (size_t)set * D * D) + lane;
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+  for (int k4 = 0; k4 < 32; ++k4) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float xk = __shfl_sync(0xffffffffu, x[i], k4);
+      const float4 tt = __ldg(TT + (size_t)(4 * k4 + i) * 32);
+      y[0] = fmaf(tt.x, xk, y[0]);
+      y[1] = fmaf(tt.y, xk, y[1]);
+      y[2] = fmaf(tt.z, xk, y[2]);
+      y[3] = fmaf(tt.w, xk, y[3]);
+    }
+  }
+  const long long pos = a.dst_pos[b] + t;
+  uint32_t* out = nullptr;
+  if (pos >= 0 && pos < a.T_cap) {
+    out = a.dst[tensor] + (((size_t)b * a.Hkv + h) * (size_t)a.T_cap + (size_t)pos) * td.r_words;
+  } else if (lane == 0) {
+    atomicOr(&g_status, ST_BAD_INDEX);
+  }
+  quantize_pack_warp(td, set, y, lane, rec_s[warp], out);
+}
+
+kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, const void* v, int dtype, int B,
+                        int64_t t_new, const int64_t* dst_pos, int path, cudaStream_t s) {
+  if (path == 2) {
+    set_error("tensor-core encode path not available in this build");
+    return KV_ERR_UNSUPPORTED;
+  }
+  EncArgs a;
+  a.src[0] = k;
+  a.src[1] = v;
+  a.dst[0] = c.k_rec;
+  a.dst[1] = c.v_rec;
+  a.dst_pos = dst_pos;
+  a.B = B;
+  a.Hkv = c.Hkv;
+  a.per_seq = c.per_seq_params;
+  a.t_new = t_new;
+  a.T_cap = c.T_cap;
+  const long long warps = 2LL * B * c.Hkv * t_new;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  if (dtype == KV_DTYPE_BF16)
+    encode_warp_kernel<true><<<blocks, 256, 0, s>>>(P, a);
+  else
+    encode_warp_kernel<false><<<blocks, 256, 0, s>>>(P, a);
+  return launch_check("encode_warp_kernel");
+}
+
+// ======================================================================================================
+// decode over packed records
+// ======================================================================================================
+constexpr int DT = 64;         // tokens per pipeline stage
+constexpr int DSTAGES = 4;     // stages in flight per CTA
+constexpr int DTHREADS = 128;  // 4 warps, 16 tokens each per stage
+constexpr int PSTR = 132;      // floats per (split, head) partial: M, L, Z, -, A[128]
+constexpr int KC_PITCH_MAX = 272;  // bytes per token row of an unpacked tile (odd multiple of 16)
+
+struct DecArgs {
+  const uint32_t* rec[2];
+  const __nv_bfloat16* q;
+  const int32_t* seq_lens;
+  __half* qa;       // [B*Hkv][16][128]
+  float* qc;        // [B*Hkv][16]: C0 of heads 0..7, C1 of heads 0..7
+  unsigned* cnt;    // [B*Hkv]
+  float* part;      // [B*Hkv][splits][8][PSTR]
+  float* out;       // [B][Hq][128]
+  long long T_cap;
+  long long wait_ns;
+  int B, Hkv, Hq, g, per_seq, splits, chunk;
+  float scale_log2;
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(256) qprep_kernel(ParamsDev P, DecArgs a) {
+  pdl_launch_dependents();
+  __shared__ float qs[MAX_G][D];
+  __shared__ float qt[MAX_G][D];
+  const int kh = blockIdx.x, b = blockIdx.y;
+  const int bh = b * a.Hkv + kh;
+  const int set = a.per_seq ? bh : kh;
+  const int g = a.g, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const TensorDev& tk = P.t[0];
+  for (int i = tid; i < g * D; i += 256) {
+    const int h = i >> 7, k = i & (D - 1);
+    qs[h][k] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k]);
+  }
+  __syncthreads();
+  const int nz = tk.nz[set];
+  const float* T = tk.T + (size_t)set * D * D;
+  for (int j = warp; j < nz; j += 8) {
+    const float4 t4 = __ldg(reinterpret_cast<const float4*>(T + (size_t)j * D) + lane);
+    for (int h = 0; h < g; ++h) {
+      const float4 q4 = *reinterpret_cast<const float4*>(&qs[h][4 * lane]);
+      float sacc = t4.x * q4.x + t4.y * q4.y + t4.z * q4.z + t4.w * q4.w;
+      sacc = warp_sum(sacc);
+      if (lane == 0) qt[h][j] = sacc;
+    }
+  }
+  __syncthreads();
+  const float* sig = tk.sigma + (size_t)set * D;
+  const uint8_t* wd = tk.widths + (size_t)set * D;
+  __half* qa = a.qa + (size_t)bh * 16 * D;
+  for (int i = tid; i < 16 * D; i += 256) {
+    const int r = i >> 7, j = i & (D - 1), h = r >> 1, hl = r & 1;
+    __half v = __float2half_rn(0.f);
+    if (h < g && j < nz) {
+      const float qp = a.scale_log2 * qt[h][j] * sig[j] * exp2i(-(int)wd[j]);
+      const __half hi = __float2half_rn(qp);
+      v = hl ? __float2half_rn(qp - __half2float(hi)) : hi;
+    }
+    qa[i] = v;
+  }
+  if (warp < g) {
+    const float* base = tk.base + (size_t)set * D;
+    float c0 = 0.f, c1 = 0.f;
+    for (int k = lane; k < D; k += 32) c0 += base[k] * qs[warp][k];
+    for (int j = lane; j < nz; j += 32) c1 += qt[warp][j] * sig[j];
+    c0 = warp_sum(c0);
+    c1 = warp_sum(c1);
+    if (lane == 0) {
+      a.qc[bh * 16 + warp] = a.scale_log2 * c0;
+      a.qc[bh * 16 + 8 + warp] = a.scale_log2 * c1;
+    }
+  }
+  if (tid == 0) a.cnt[bh] = 0u;
+}
+
+__host__ __device__ __forceinline__ int unpacked_pitch(int nblk16) {  // bytes, odd multiple of 16
+  return ((nblk16 * 2) | 1) * 16;
+}
+
+static size_t decode_smem_bytes(int RK, int RV) {
+  const size_t stage = (size_t)DT * (RK + RV) * 4;
+  size_t off = DSTAGES * stage + 16;
+  off = (off + 127) / 128 * 128;
+  off += 4 * (size_t)DT * KC_PITCH_MAX;       // Kc[2], Vc[2]
+  off += 2 * 2 * (size_t)DT * sizeof(float2); // zsK[2], zsV[2]
+  off += DSTAGES * 8;                         // mbarriers
+  return off + 128;
+}
+
+template <int NB>
+__global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  const int bh = b * a.Hkv + kh;
+  const int set = a.per_seq ? bh : kh;
+  const TensorDev& TK = P.t[0];
+  const TensorDev& TV = P.t[1];
+  const int RK = TK.r_words, RV = TV.r_words;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  const int g = a.g;
+
+  const int nzK = TK.nz[set], nzV = TV.nz[set];
+  const int nkb = (nzK + 15) >> 4, nmb = (nzV + 15) >> 4;
+  const int pitchK = unpacked_pitch(nkb), pitchV = unpacked_pitch(nmb);
+
+  const size_t stage_bytes = (size_t)DT * (RK + RV) * 4;
+  uint8_t* stage0 = smem;
+  size_t off = DSTAGES * stage_bytes + 16;
+  off = (off + 127) / 128 * 128;
+  uint8_t* kc0 = smem + off;
+  uint8_t* vc0 = kc0 + 2 * DT * KC_PITCH_MAX;
+  float2* zsK = reinterpret_cast<float2*>(vc0 + 2 * DT * KC_PITCH_MAX);
+  float2* zsV = zsK + 2 * DT;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(zsV + 2 * DT);
+  __shared__ int s_last;
+
+  const long long L = min((long long)a.seq_lens[b], a.T_cap);
+  const long long t0 = (long long)split * a.chunk;
+  const long long t1 = min(t0 + (long long)a.chunk, L);
+  const int ntiles = t1 > t0 ? (int)((t1 - t0 + DT - 1) / DT) : 0;
+  const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
+  const uint32_t* vrec = a.rec[1] + (size_t)bh * a.T_cap * RV;
+
+  auto issue = [&](int i) {
+    const int s = i % DSTAGES;
+    const long long tb = t0 + (long long)i * DT;
+    long long n = min((long long)DT, t1 - tb);
+    n = min((n + 3) & ~3LL, a.T_cap - tb);
+    const uint32_t kb = (uint32_t)(n * RK * 4), vb = (uint32_t)(n * RV * 4);
+    const uint32_t bar = smem_u32(&bars[s]);
+    const uint32_t dst = smem_u32(stage0 + s * stage_bytes);
+    mbar_expect_tx(bar, kb + vb);
+    bulk_g2s(dst, krec + tb * RK, kb, bar);
+    bulk_g2s(dst + DT * RK * 4, vrec + tb * RV, vb, bar);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < DSTAGES; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int i = 0; i < min(DSTAGES, ntiles); ++i) issue(i);
+
+  const QuadMap mk = quad_map(nkb * 4, tid, DTHREADS);
+  const QuadMap mv = quad_map(nmb * 4, tid, DTHREADS);
+  QuadDesc dk = {}, dv = {};
+  if (mk.active) dk = load_quad(TK, set, mk.q);
+  if (mv.active) dv = load_quad(TV, set, mv.q);
+
+  // q' operand and folded constants come from qprep_kernel
+  pdl_wait();
+  uint32_t qa[8][4];
+  {
+    const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(a.qa + (size_t)bh * 16 * D);
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      if (kb < nkb) {
+        qa[kb][0] = qa32[(gid * D + kb * 16 + 2 * tig) >> 1];
+        qa[kb][1] = qa32[((gid + 8) * D + kb * 16 + 2 * tig) >> 1];
+        qa[kb][2] = qa32[(gid * D + kb * 16 + 8 + 2 * tig) >> 1];
+        qa[kb][3] = qa32[((gid + 8) * D + kb * 16 + 8 + 2 * tig) >> 1];
+      } else {
+        qa[kb][0] = qa[kb][1] = qa[kb][2] = qa[kb][3] = 0u;
+      }
+    }
+  }
+  const int hA = gid >> 1, hB = 4 + (gid >> 1);
+  const float c0A = a.qc[bh * 16 + hA], c1A = a.qc[bh * 16 + 8 + hA];
+  const float c0B = NB == 2 ? a.qc[bh * 16 + hB] : 0.f, c1B = NB == 2 ? a.qc[bh * 16 + 8 + hB] : 0.f;
+
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, z_run[2] = {0.f, 0.f};
+  float acc_o[8][NB][4];
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc_o[mb][nb][i] = 0.f;
+
+  const int lrow = (lane & 7) + ((lane >> 4) << 3);  // ldmatrix row within a 16-token group
+  const int lcol = ((lane >> 3) & 1) * 16;            // byte offset of the second 8-channel half
+  const int hl = gid & 1;
+  int consumed = 0;
+  bool aborted = false;
+  for (int i = 0; i < ntiles; ++i) {
+    const int s = i % DSTAGES;
+    const uint32_t par = (uint32_t)((i / DSTAGES) & 1);
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), par, a.wait_ns);
+    const int buf = i & 1;
+    const uint32_t* sk = reinterpret_cast<const uint32_t*>(stage0 + s * stage_bytes);
+    const uint32_t* sv = sk + DT * RK;
+    uint8_t* kc = kc0 + buf * DT * KC_PITCH_MAX;
+    uint8_t* vc = vc0 + buf * DT * KC_PITCH_MAX;
+    if (mk.active)
+      for (int t = mk.r0; t < DT; t += mk.rstep)
+        *reinterpret_cast<uint2*>(kc + t * pitchK + 8 * mk.q) = unpack_quad(sk + t * RK, dk);
+    if (mv.active)
+      for (int t = mv.r0; t < DT; t += mv.rstep)
+        *reinterpret_cast<uint2*>(vc + t * pitchV + 8 * mv.q) = unpack_quad(sv + t * RV, dv);
+    if (tid < DT) {
+      const uint32_t w = sk[tid * RK];
+      zsK[buf * DT + tid] = make_float2(half_bits_to_float(w), half_bits_to_float(w >> 16));
+    } else {
+      const uint32_t w = sv[(tid - DT) * RV];
+      zsV[buf * DT + tid - DT] = make_float2(half_bits_to_float(w), half_bits_to_float(w >> 16));
+    }
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      consumed = i;
+      break;
+    }
+    consumed = i + 1;
+    if (tid == 0 && i + DSTAGES < ntiles) {
+      fence_proxy_async_smem();
+      issue(i + DSTAGES);
+    }
+    const long long tile_t0 = t0 + (long long)i * DT;
+    const int lt = warp * 16;
+    if (tile_t0 + lt >= t1) continue;  // this warp's 16 tokens are past the end
+
+    // ---- logits: rows 2h / 2h+1 = q' hi / lo of head h, columns = 16 tokens ----
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const uint32_t ka = smem_u32(kc + (lt + lrow) * pitchK + lcol);
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      if (kb < nkb) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(ka + kb * 32, r0, r1, r2, r3);
+        mma_f16(acc[0], qa[kb], r0, r1);
+        mma_f16(acc[1], qa[kb], r2, r3);
+      }
+    }
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nb][e] += __shfl_xor_sync(0xffffffffu, acc[nb][e], 4);
+
+    const int tl[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
+    bool valid[4];
+    float2 zk[4], zv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      valid[e] = tile_t0 + lt + tl[e] < t1;
+      zk[e] = zsK[buf * DT + lt + tl[e]];
+      zv[e] = zsV[buf * DT + lt + tl[e]];
+    }
+    uint32_t bp[NB][2];
+    float corr[2];
+#pragma unroll
+    for (int hb = 0; hb < NB; ++hb) {
+      const float c0 = hb ? c0B : c0A, c1 = hb ? c1B : c1A;
+      float lg[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float raw = acc[e >> 1][(e & 1) + 2 * hb];
+        lg[e] = valid[e] ? c0 + zk[e].x * c1 + zk[e].y * raw : -INFINITY;
+      }
+      float mt = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+      const float m_new = fmaxf(m_run[hb], mt);
+      const float cr = (m_run[hb] == m_new) ? 1.f : exp2f(m_run[hb] - m_new);
+      float p[4], psum = 0.f, zsum = 0.f;
+      __half pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        p[e] = valid[e] ? exp2f(lg[e] - m_new) : 0.f;
+        psum += p[e];
+        zsum += valid[e] ? p[e] * zv[e].x : 0.f;
+        const float w = valid[e] ? p[e] * zv[e].y : 0.f;
+        const __half whi = __float2half_rn(w);
+        pv[e] = hl ? __float2half_rn(w - __half2float(whi)) : whi;
+      }
+      l_run[hb] = l_run[hb] * cr + psum;
+      z_run[hb] = z_run[hb] * cr + zsum;
+      m_run[hb] = m_new;
+      corr[hb] = cr;
+      bp[hb][0] = pack_half2(pv[0], pv[1]);
+      bp[hb][1] = pack_half2(pv[2], pv[3]);
+    }
+    // rescale the value accumulators: columns 2tig / 2tig+1 belong to head tig (+4 for the second block)
+#pragma unroll
+    for (int hb = 0; hb < NB; ++hb) {
+      const float c = __shfl_sync(0xffffffffu, corr[hb], 8 * tig);
+      if (__any_sync(0xffffffffu, c != 1.f)) {
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc_o[mb][hb][e] *= c;
+      }
+    }
+    // ---- P.V in the rotated basis: rows = channels, k = 16 tokens, columns = head hi/lo ----
+    const uint32_t va = smem_u32(vc + (lt + lrow) * pitchV + lcol);
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      if (mb < nmb) {
+        uint32_t af[4];
+        ldsm_x4_t(va + mb * 32, af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int hb = 0; hb < NB; ++hb) mma_f16(acc_o[mb][hb], af, bp[hb][0], bp[hb][1]);
+      }
+    }
+  }
+
+  if (aborted) {  // drain copies still in flight into this CTA's shared memory, then leave
+    if (tid == 0)
+      for (int i = consumed; i < min(consumed + DSTAGES, ntiles); ++i)
+        mbar_wait_bounded(smem_u32(&bars[i % DSTAGES]), (uint32_t)((i / DSTAGES) & 1), a.wait_ns);
+    __syncthreads();
+    return;
+  }
+
+  // ---- merge the 4 warps of this CTA ----
+  __syncthreads();
+  float* ws = reinterpret_cast<float*>(kc0);  // [4][8][PSTR]
+#pragma unroll
+  for (int hb = 0; hb < NB; ++hb) {
+    float l = l_run[hb], z = z_run[hb];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+    z += __shfl_xor_sync(0xffffffffu, z, 2);
+    const int h = (gid >> 1) + 4 * hb;
+    if (tig == 0 && hl == 0 && h < g) {
+      float* w = ws + (warp * 8 + h) * PSTR;
+      w[0] = m_run[hb];
+      w[1] = l;
+      w[2] = z;
+    }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const int hcol = tig + 4 * hb;
+      if (mb < nmb && hcol < g) {
+        float* w = ws + (warp * 8 + hcol) * PSTR + 4 + mb * 16;
+        w[gid] = acc_o[mb][hb][0] + acc_o[mb][hb][1];
+        w[gid + 8] = acc_o[mb][hb][2] + acc_o[mb][hb][3];
+      }
+    }
+  }
+  __syncthreads();
+  float* part = a.part + ((size_t)bh * a.splits + split) * 8 * PSTR;
+  const int acols = nmb * 16;
+  for (int idx = tid; idx < g * PSTR; idx += DTHREADS) {
+    const int h = idx / PSTR, cidx = idx - h * PSTR;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
+    float val = 0.f;
+    if (cidx == 0) {
+      val = M;
+    } else if (cidx == 1 || cidx == 2 || (cidx >= 4 && cidx - 4 < acols)) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float mw = ws[(w * 8 + h) * PSTR];
+        const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        val += e * ws[(w * 8 + h) * PSTR + cidx];
+      }
+    }
+    part[idx] = val;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&a.cnt[bh], 1u) == (unsigned)(a.splits - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- last CTA of (b, kh): merge splits, reconstruct o^ - mu, inverse-rotate ----
+  float* delta = reinterpret_cast<float*>(kc0);  // [8][128]
+  __shared__ float s_have[MAX_G];
+  const float* pb = a.part + (size_t)bh * a.splits * 8 * PSTR;
+  const float* sigV = TV.sigma + (size_t)set * D;
+  const uint8_t* wV = TV.widths + (size_t)set * D;
+  const int j = tid;
+  for (int h = 0; h < g; ++h) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, __ldcg(pb + ((size_t)sp * 8 + h) * PSTR));
+    float Ls = 0.f, Zs = 0.f, As = 0.f;
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float* pp = pb + ((size_t)sp * 8 + h) * PSTR;
+      const float ms = __ldcg(pp);
+      const float e = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      Ls += e * __ldcg(pp + 1);
+      Zs += e * __ldcg(pp + 2);
+      if (j < nzV) As += e * __ldcg(pp + 4 + j);
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    delta[h * D + j] = j < nzV ? sigV[j] * (Zs * inv + exp2i(-(int)wV[j]) * As * inv) : 0.f;
+    if (j == 0) s_have[h] = Ls > 0.f ? 1.f : 0.f;
+  }
+  __syncthreads();
+  {
+    const int k = tid;
+    const float* Tv = TV.T + (size_t)set * D * D;
+    const float bk = TV.base[(size_t)set * D + k];
+    float o[MAX_G];
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) o[h] = bk;
+    for (int jj = 0; jj < nzV; ++jj) {
+      const float t = __ldg(Tv + (size_t)jj * D + k);
+#pragma unroll
+      for (int h = 0; h < MAX_G; ++h)
+        if (h < g) o[h] = fmaf(t, delta[h * D + jj], o[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h)
+      if (h < g) a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] = s_have[h] != 0.f ? o[h] : 0.f;
+  }
+  if (tid == 0) a.cnt[bh] = 0u;
+}
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+static int sm_count(int device) {
+  int n = 148;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
+  return n > 0 ? n : 148;
+}
+
+static void split_plan(int B, int Hkv, int64_t T_cap, int device, int tile, int per_sm, int* splits, int* chunk) {
+  const long long bh = (long long)B * Hkv;
+  const long long tiles = (T_cap + tile - 1) / tile;
+  long long sp = ((long long)per_sm * sm_count(device) + bh - 1) / bh;
+  sp = std::max(1LL, std::min(sp, tiles));
+  const long long ct = (tiles + sp - 1) / sp;
+  *splits = (int)((tiles + ct - 1) / ct);
+  *chunk = (int)(ct * tile);
+}
+
+DecodeLayout decode_layout(int B, int Hkv, int64_t T_cap, int device) {
+  DecodeLayout L{};
+  split_plan(B, Hkv, T_cap, device, DT, 2, &L.splits, &L.chunk);
+  const size_t bh = (size_t)B * Hkv;
+  size_t o = 0;
+  L.off_qa = o;
+  o = align256(o + bh * 16 * D * sizeof(__half));
+  L.off_qc = o;
+  o = align256(o + bh * 16 * sizeof(float));
+  L.off_cnt = o;
+  o = align256(o + bh * sizeof(unsigned));
+  L.off_part = o;
+  o = align256(o + bh * (size_t)L.splits * 8 * PSTR * sizeof(float));
+  L.total = o;
+  return L;
+}
+
+kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
+                        const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
+                        cudaStream_t s) {
+  DecArgs a;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.rec[0] = c.k_rec;
+  a.rec[1] = c.v_rec;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.seq_lens = seq_lens;
+  a.qa = reinterpret_cast<__half*>(w + L.off_qa);
+  a.qc = reinterpret_cast<float*>(w + L.off_qc);
+  a.cnt = reinterpret_cast<unsigned*>(w + L.off_cnt);
+  a.part = reinterpret_cast<float*>(w + L.off_part);
+  a.out = out;
+  a.T_cap = c.T_cap;
+  a.wait_ns = g_wait_limit_ns;
+  a.B = B;
+  a.Hkv = c.Hkv;
+  a.Hq = Hq;
+  a.g = Hq / c.Hkv;
+  a.per_seq = c.per_seq_params;
+  a.splits = L.splits;
+  a.chunk = L.chunk;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  qprep_kernel<<<dim3(c.Hkv, B), 256, 0, s>>>(P, a);
+  kv_status st = launch_check("qprep_kernel");
+  if (st != KV_OK) return st;
+  const size_t smem = decode_smem_bytes(P.t[0].r_words, P.t[1].r_words);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.splits, c.Hkv, B);
+  cfg.blockDim = dim3(DTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (a.g <= 4) {
+    cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<1>, P, a);
+  } else {
+    cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<2>, P, a);
+  }
+  if (e != cudaSuccess) {
+    set_error("decode_kernel launch: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
+  return launch_check("decode_kernel");
+}
+
+// ======================================================================================================
+// uncompressed bf16 split-K flash-decode (comparator)
+// ======================================================================================================
+constexpr int BDT = 64;
+constexpr int BSTAGES = 3;
+constexpr int BPITCH = 272;  // bytes per token row in shared memory (256 + 16: conflict-free ldmatrix)
+
+struct DecBf16Args {
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* q;
+  const int32_t* seq_lens;
+  unsigned* cnt;
+  float* part;
+  float* out;
+  long long T_cap;
+  long long wait_ns;
+  int B, Hkv, Hq, g, splits, chunk;
+  float scale_log2;
+};
+
+static size_t decode_bf16_smem_bytes() { return (size_t)BSTAGES * 2 * BDT * BPITCH + BSTAGES * 8 + 128; }
+
+__global__ void __launch_bounds__(DTHREADS, 2) decode_bf16_kernel(DecBf16Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  const int bh = b * a.Hkv + kh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  const int g = a.g;
+  const size_t stage_bytes = (size_t)2 * BDT * BPITCH;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BSTAGES * stage_bytes);
+  __shared__ int s_last;
+
+  const long long L = min((long long)a.seq_lens[b], a.T_cap);
+  const long long t0 = (long long)split * a.chunk;
+  const long long t1 = min(t0 + (long long)a.chunk, L);
+  const int ntiles = t1 > t0 ? (int)((t1 - t0 + BDT - 1) / BDT) : 0;
+  const __nv_bfloat16* kg = a.k + (size_t)bh * a.T_cap * D;
+  const __nv_bfloat16* vg = a.v + (size_t)bh * a.T_cap * D;
+
+  auto issue = [&](int i) {  // warp 0, all lanes
+    const int s = i % BSTAGES;
+    const long long tb = t0 + (long long)i * BDT;
+    const int n = (int)min((long long)BDT, t1 - tb);
+    const uint32_t bar = smem_u32(&bars[s]);
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)n * 2 * D * 2);
+    __syncwarp();
+    const uint32_t dk = smem_u32(smem + s * stage_bytes), dv = dk + BDT * BPITCH;
+    for (int r = lane; r < n; r += 32) {
+      bulk_g2s(dk + r * BPITCH, kg + (tb + r) * D, D * 2, bar);
+      bulk_g2s(dv + r * BPITCH, vg + (tb + r) * D, D * 2, bar);
+    }
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < BSTAGES; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0)
+    for (int i = 0; i < min(BSTAGES, ntiles); ++i) issue(i);
+
+  // q rows (bf16, exact): row h = head h (h < g), others zero; 8 k-blocks of 16 channels
+  uint32_t qa[8][4];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.Hq + (size_t)kh * g) * D);
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      qa[kb][0] = gid < g ? q32[(gid * D + kb * 16 + 2 * tig) >> 1] : 0u;
+      qa[kb][1] = 0u;
+      qa[kb][2] = gid < g ? q32[(gid * D + kb * 16 + 8 + 2 * tig) >> 1] : 0u;
+      qa[kb][3] = 0u;
+    }
+  }
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc_o[8][2][4];
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] = 0.f;
+  const int lrow = (lane & 7) + ((lane >> 4) << 3);
+  const int lcol = ((lane >> 3) & 1) * 16;
+  int consumed = 0;
+  bool aborted = false;
+  for (int i = 0; i < ntiles; ++i) {
+    const int s = i % BSTAGES;
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)((i / BSTAGES) & 1), a.wait_ns);
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      consumed = i;
+      break;
+    }
+    consumed = i + 1;
+    uint8_t* ks = smem + s * stage_bytes;
+    uint8_t* vs = ks + BDT * BPITCH;
+    const long long tile_t0 = t0 + (long long)i * BDT;
+    const int lt = warp * 16;
+    const bool warp_live = tile_t0 + lt < t1;
+    if (warp_live) {
+      // rows of this warp's 16 tokens that were not loaded hold stale bytes: zero the value rows so that
+      // P = 0 times them stays 0
+      for (int r = 0; r < 16; ++r)
+        if (tile_t0 + lt + r >= t1) reinterpret_cast<uint2*>(vs + (lt + r) * BPITCH)[lane] = make_uint2(0u, 0u);
+      __syncwarp();
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint32_t ka = smem_u32(ks + (lt + lrow) * BPITCH + lcol);
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(ka + kb * 32, r0, r1, r2, r3);
+        mma_bf16(acc[0], qa[kb], r0, r1);
+        mma_bf16(acc[1], qa[kb], r2, r3);
+      }
+      const int tl[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
+      float lg[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool valid = tile_t0 + lt + tl[e] < t1;
+        lg[e] = valid ? a.scale_log2 * acc[e >> 1][e & 1] : -INFINITY;
+      }
+      float mt = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+      const float m_new = fmaxf(m_run, mt);
+      const float cr = (m_run == m_new) ? 1.f : exp2f(m_run - m_new);
+      float p[4], psum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        p[e] = lg[e] == -INFINITY ? 0.f : exp2f(lg[e] - m_new);
+        psum += p[e];
+      }
+      l_run = l_run * cr + psum;
+      m_run = m_new;
+      __nv_bfloat16 ph[4], pl[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ph[e] = __float2bfloat16_rn(p[e]);
+        pl[e] = __float2bfloat16_rn(p[e] - __bfloat162float(ph[e]));
+      }
+      const uint32_t bh0 = pack_bf162(ph[0], ph[1]), bh1 = pack_bf162(ph[2], ph[3]);
+      const uint32_t bl0 = pack_bf162(pl[0], pl[1]), bl1 = pack_bf162(pl[2], pl[3]);
+      // accumulator columns 2tig, 2tig+1 = heads 2tig, 2tig+1; their maxima live at lanes 8tig, 8tig+4
+      const float c_lo = __shfl_sync(0xffffffffu, cr, 8 * tig);
+      const float c_hi = __shfl_sync(0xffffffffu, cr, 8 * tig + 4);
+      if (__any_sync(0xffffffffu, c_lo != 1.f || c_hi != 1.f)) {
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            acc_o[mb][nb][0] *= c_lo;
+            acc_o[mb][nb][1] *= c_hi;
+            acc_o[mb][nb][2] *= c_lo;
+            acc_o[mb][nb][3] *= c_hi;
+          }
+      }
+      const uint32_t va = smem_u32(vs + (lt + lrow) * BPITCH + lcol);
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        uint32_t af[4];
+        ldsm_x4_t(va + mb * 32, af[0], af[1], af[2], af[3]);
+        mma_bf16(acc_o[mb][0], af, bh0, bh1);
+        mma_bf16(acc_o[mb][1], af, bl0, bl1);
+      }
+    }
+    __syncthreads();  // every warp is done with stage s before it is refilled
+    if (warp == 0 && i + BSTAGES < ntiles) {
+      if (lane == 0) fence_proxy_async_smem();
+      __syncwarp();
+      issue(i + BSTAGES);
+    }
+  }
+  if (aborted) {
+    if (tid == 0)
+      for (int i = consumed; i < min(consumed + BSTAGES, ntiles); ++i)
+        mbar_wait_bounded(smem_u32(&bars[i % BSTAGES]), (uint32_t)((i / BSTAGES) & 1), a.wait_ns);
+    __syncthreads();
+    return;
+  }
+  __syncthreads();
+  float* ws = reinterpret_cast<float*>(smem);  // [4][8][PSTR]
+  {
+    float l = l_run;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (tig == 0 && gid < g) {
+      ws[(warp * 8 + gid) * PSTR + 0] = m_run;
+      ws[(warp * 8 + gid) * PSTR + 1] = l;
+    }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const int h0 = 2 * tig, h1 = 2 * tig + 1;
+      if (h0 < g) {
+        ws[(warp * 8 + h0) * PSTR + 4 + mb * 16 + gid] = acc_o[mb][0][0] + acc_o[mb][1][0];
+        ws[(warp * 8 + h0) * PSTR + 4 + mb * 16 + gid + 8] = acc_o[mb][0][2] + acc_o[mb][1][2];
+      }
+      if (h1 < g) {
+        ws[(warp * 8 + h1) * PSTR + 4 + mb * 16 + gid] = acc_o[mb][0][1] + acc_o[mb][1][1];
+        ws[(warp * 8 + h1) * PSTR + 4 + mb * 16 + gid + 8] = acc_o[mb][0][3] + acc_o[mb][1][3];
+      }
+    }
+  }
+  __syncthreads();
+  float* part = a.part + ((size_t)bh * a.splits + split) * 8 * PSTR;
+  for (int idx = tid; idx < g * PSTR; idx += DTHREADS) {
+    const int h = idx / PSTR, cidx = idx - h * PSTR;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
+    float val = 0.f;
+    if (cidx == 0) {
+      val = M;
+    } else if (cidx == 1 || cidx >= 4) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float mw = ws[(w * 8 + h) * PSTR];
+        const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        val += e * ws[(w * 8 + h) * PSTR + cidx];
+      }
+    }
+    part[idx] = val;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&a.cnt[bh], 1u) == (unsigned)(a.splits - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* pb = a.part + (size_t)bh * a.splits * 8 * PSTR;
+  const int k = tid;
+  for (int h = 0; h < g; ++h) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, __ldcg(pb + ((size_t)sp * 8 + h) * PSTR));
+    float Ls = 0.f, As = 0.f;
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float* pp = pb + ((size_t)sp * 8 + h) * PSTR;
+      const float ms = __ldcg(pp);
+      const float e = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      Ls += e * __ldcg(pp + 1);
+      As += e * __ldcg(pp + 4 + k);
+    }
+    a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] = Ls > 0.f ? As / Ls : 0.f;
+  }
+  if (tid == 0) a.cnt[bh] = 0u;
+}
+
+DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device) {
+  DecodeLayout L{};
+  split_plan(B, Hkv, T_cap, device, BDT, 2, &L.splits, &L.chunk);
+  const size_t bh = (size_t)B * Hkv;
+  size_t o = 0;
+  L.off_qa = L.off_qc = 0;
+  L.off_cnt = o;
+  o = align256(o + bh * sizeof(unsigned));
+  L.off_part = o;
+  o = align256(o + bh * (size_t)L.splits * 8 * PSTR * sizeof(float));
+  L.total = o;
+  return L;
+}
+
+__global__ void zero_u32_kernel(unsigned* p, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = 0u;
+}
+
+kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap, const void* q,
+                             const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
+                             cudaStream_t s) {
+  DecBf16Args a;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.seq_lens = seq_lens;
+  a.cnt = reinterpret_cast<unsigned*>(w + L.off_cnt);
+  a.part = reinterpret_cast<float*>(w + L.off_part);
+  a.out = out;
+  a.T_cap = T_cap;
+  a.wait_ns = g_wait_limit_ns;
+  a.B = B;
+  a.Hkv = Hkv;
+  a.Hq = Hq;
+  a.g = Hq / Hkv;
+  a.splits = L.splits;
+  a.chunk = L.chunk;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int nbh = B * Hkv;
+  zero_u32_kernel<<<(nbh + 255) / 256, 256, 0, s>>>(a.cnt, nbh);
+  kv_status st = launch_check("zero counters");
+  if (st != KV_OK) return st;
+  const size_t smem = decode_bf16_smem_bytes();
+  cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  decode_bf16_kernel<<<dim3(L.splits, Hkv, B), DTHREADS, smem, s>>>(a);
+  return launch_check("decode_bf16_kernel");
+}
+
+// ======================================================================================================
+// parity and self-test kernels
+// ======================================================================================================
+__global__ void __launch_bounds__(256) debug_qp_warp_kernel(ParamsDev P, int set, int tensor, const float* y,
+                                                            long long n, uint32_t* rec) {
+  __shared__ uint32_t rec_s[8][MAX_RW + 3];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long t = (long long)blockIdx.x * 8 + warp;
+  if (t >= n) return;
+  const TensorDev& td = P.t[tensor];
+  const float4 v = *reinterpret_cast<const float4*>(y + (size_t)t * D + 4 * lane);
+  const float yy[4] = {v.x, v.y, v.z, v.w};
+  quantize_pack_warp(td, set, yy, lane, rec_s[warp], rec + (size_t)t * td.r_words);
+}
+
+__global__ void __launch_bounds__(128) debug_qp_thread_kernel(ParamsDev P, int set, int tensor, const float* y,
+                                                              long long n, uint32_t* rec) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n) return;
+  const TensorDev& td = P.t[tensor];
+  const float* yr = y + (size_t)t * D;
+  uint32_t* out = rec + (size_t)t * td.r_words;
+  quantize_pack_thread(td, set, [&](int j) { return yr[j]; }, [&](int w, uint32_t val) { out[w] = val; });
+}
+
+kv_status launch_debug_quantize_pack(const ParamsDev& P, int set, int tensor, const float* y, int64_t n,
+                                     uint32_t* rec, int variant, cudaStream_t s) {
+  if (variant == 0)
+    debug_qp_warp_kernel<<<(unsigned)((n + 7) / 8), 256, 0, s>>>(P, set, tensor, y, n, rec);
+  else
+    debug_qp_thread_kernel<<<(unsigned)((n + 127) / 128), 128, 0, s>>>(P, set, tensor, y, n, rec);
+  return launch_check("debug quantize/pack");
+}
+
+// Runs the decode kernel's cooperative unpacker over 64-record tiles and writes integer codes.
+__global__ void __launch_bounds__(DTHREADS) debug_unpack_kernel(ParamsDev P, int set, int tensor,
+                                                                const uint32_t* rec, long long n,
+                                                                uint16_t* codes) {
+  __shared__ uint32_t srec[DT * MAX_RW + 4];
+  __shared__ __align__(16) uint8_t tile[DT * KC_PITCH_MAX];
+  const TensorDev& td = P.t[tensor];
+  const int R = td.r_words, tid = threadIdx.x;
+  const long long t0 = (long long)blockIdx.x * DT;
+  const int cnt = (int)min((long long)DT, n - t0);
+  for (int i = tid; i < DT * R + 4; i += DTHREADS) srec[i] = i < cnt * R ? rec[t0 * R + i] : 0u;
+  __syncthreads();
+  const int nz = td.nz[set], nblk = (nz + 15) >> 4, pitch = unpacked_pitch(nblk);
+  const QuadMap m = quad_map(nblk * 4, tid, DTHREADS);
+  if (m.active) {
+    const QuadDesc dq = load_quad(td, set, m.q);
+    for (int t = m.r0; t < DT; t += m.rstep)
+      *reinterpret_cast<uint2*>(tile + t * pitch + 8 * m.q) = unpack_quad(srec + t * R, dq);
+  }
+  __syncthreads();
+  for (int i = tid; i < cnt * D; i += DTHREADS) {
+    const int t = i / D, j = i % D;
+    uint16_t c = 0;
+    if (j < nz) {
+      const __half hv = *reinterpret_cast<const __half*>(tile + t * pitch + 2 * j);
+      c = (uint16_t)(__half2float(hv) - 0.5f);
+    }
+    codes[(t0 + t) * D + j] = c;
+  }
+}
+
+kv_status launch_debug_unpack(const ParamsDev& P, int set, int tensor, const uint32_t* rec, int64_t n,
+                              uint16_t* codes, cudaStream_t s) {
+  debug_unpack_kernel<<<(unsigned)((n + DT - 1) / DT), DTHREADS, 0, s>>>(P, set, tensor, rec, n, codes);
+  return launch_check("debug unpack");
+}
+
+__global__ void wait_selftest_kernel(long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait_bounded(smem_u32(&bar), 0u, limit_ns);  // no arrival will ever come
+  __syncthreads();
+}
+
+kv_status launch_wait_selftest(cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(g_wait_limit_ns);
+  return launch_check("wait self-test");
+}
+
+}  // namespace kvtc
