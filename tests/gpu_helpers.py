@@ -106,7 +106,8 @@ def rel_l2_rows(a, b):
 
 def code_diff(rec_a, rec_b, p):
     """Compare two record sets: (fraction of tokens whose z or s differ, max |dz| and |ds| in fp16 ulps,
-    fraction of code entries that differ, max |code difference|)."""
+    fraction of code entries that differ, max |code difference|, fraction of all record entries - z, s and
+    the codes of the nonzero-width channels - that differ)."""
     za, sa, ca = O.unpack(rec_a, p)
     zb, sb, cb = O.unpack(rec_b, p)
     zi = lambda h: h.view(np.uint16).astype(np.int64)
@@ -114,5 +115,7 @@ def code_diff(rec_a, rec_b, p):
     ds = np.abs(zi(sa) - zi(sb))
     nz = p.widths > 0
     dc = np.abs(ca[:, nz] - cb[:, nz])
+    n_entries = dc.size + 2 * dz.size
+    entry_frac = float((np.count_nonzero(dc) + np.count_nonzero(dz) + np.count_nonzero(ds)) / max(n_entries, 1))
     return (float(np.mean((dz > 0) | (ds > 0))), int(dz.max(initial=0)), int(ds.max(initial=0)),
-            float(np.mean(dc > 0)), int(dc.max(initial=0)))
+            float(np.mean(dc > 0)), int(dc.max(initial=0)), entry_frac)

@@ -92,32 +92,37 @@ def _encode_gpu(P, k_st, v_st, per_seq, T_cap=None, dst0=0):
 
 
 def _check_end_to_end(rk_gpu, rv_gpu, k, v, sets, per_seq):
+    """End-to-end encode against the oracle: every record entry (fp16 z, fp16 s, and the code of each
+    nonzero-width channel) within 1 LSB, and at most 1e-4 of all entries different. The rotation's fp32
+    rounding on the device differs from the oracle's single rounding of an fp64 product, so a value that
+    lands within an ulp of a quantiser bin edge or an fp16 rounding boundary can move by one step."""
     B, Hkv, T, _ = k.shape
-    tok_frac, code_frac, max_dc, max_dz = 0.0, 0.0, 0, 0
+    tok_frac, code_frac, entry_frac, max_dc, max_dz = 0.0, 0.0, 0.0, 0, 0
     n = 0
     for b in range(B):
         for h in range(Hkv):
             pk, pv = sets[G.set_index(b, h, Hkv, per_seq)]
             for rec, x, p in ((rk_gpu[b, h, :T], k[b, h], pk), (rv_gpu[b, h, :T], v[b, h], pv)):
                 ref = O.encode(x, p)
-                tf, dz, ds, cf, dc = G.code_diff(rec, ref, p)
+                tf, dz, ds, cf, dc, ef = G.code_diff(rec, ref, p)
                 tok_frac += tf
                 code_frac += cf
+                entry_frac += ef
                 max_dc = max(max_dc, dc)
                 max_dz = max(max_dz, dz, ds)
                 n += 1
     tok_frac /= n
     code_frac /= n
+    entry_frac /= n
     assert max_dc <= 1 and max_dz <= 1, (max_dc, max_dz)
-    assert code_frac <= 1e-4, code_frac
-    assert tok_frac <= 1e-3, tok_frac
-    return code_frac, tok_frac
+    assert entry_frac <= 1e-4, (entry_frac, code_frac, tok_frac)
+    return entry_frac, code_frac, tok_frac
 
 
 def test_encode_end_to_end_tiny_fp32(tiny):
     w, L, sets, P = tiny
     rk, rv = _encode_gpu(P, L.k, L.v, False)
-    print("code mismatch fraction %.2e, token z/s mismatch fraction %.2e" %
+    print("entry mismatch fraction %.2e, code mismatch fraction %.2e, token z/s mismatch fraction %.2e" %
           _check_end_to_end(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, False))
 
 
@@ -158,7 +163,7 @@ def test_encode_out_of_range_position_is_reported(tiny):
     kvtc.kv_encode(P, cache, G.to_dev_storage(k), G.to_dev_storage(v), kvtc.KV_DTYPE_F32, 1, 4, pos)
     assert kvtc.kv_check_status() == kvtc.KV_ERR_DEVICE
     ref = O.encode(synth.as_float(L.k[0, 0, :2]), sets[0][0])
-    tok, dz, ds, cf, dc = G.code_diff(G.u32(rk)[0, 0, 62:64], ref, sets[0][0])
+    tok, dz, ds, cf, dc, ef = G.code_diff(G.u32(rk)[0, 0, 62:64], ref, sets[0][0])
     assert dc <= 1 and dz <= 1 and ds <= 1
     assert kvtc.kv_check_status() == kvtc.KV_OK  # cleared
 
