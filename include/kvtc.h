@@ -162,6 +162,26 @@ kv_status kv_attend_decode(const kv_params* p, const kv_cache* cache, const void
                            const int32_t* seq_lens_dev, float softmax_scale, float* out,
                            void* workspace, size_t ws_bytes, kv_stream_t stream);
 
+/* Decode attention without a caller-provided workspace. No page has a counterpart; this entry point serves
+ * callers that cannot allocate device memory around the call: a serving engine whose memory planner owns
+ * all of the GPU's memory and hands a kernel library only pointers and a stream, or code that runs while a
+ * stream is being captured into a CUDA graph, where cudaMalloc is not allowed.
+ *   Same arguments, results and errors as kv_attend_decode, minus workspace and ws_bytes: the split
+ *   partials, q operands and arrival counters live in one static device array of KV_NOALLOC_SCRATCH_BYTES
+ *   bytes compiled into the library (every GPU that loads the library holds it until the process exits).
+ *   A shape whose workspace (kv_decode_workspace_bytes) exceeds that size is rejected with
+ *   KV_ERR_INVALID_ARG before any launch. The call allocates nothing: no cudaMalloc, cudaFree or
+ *   allocating library routine.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ *   current; make that first call before any stream capture.
+ *   Every call shares the one array and leaves its contents behind; each call resets the arrival counters
+ *   it needs before using them. Calls whose kernels overlap on the GPU (other streams, other host threads)
+ *   race on the array: serialise them. */
+#define KV_NOALLOC_SCRATCH_BYTES (4u << 20)
+kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache* cache, const void* q, int B, int Hq,
+                                   const int32_t* seq_lens_dev, float softmax_scale, float* out,
+                                   kv_stream_t stream);
+
 /* Uncompressed bf16 split-K flash-decode over k, v: device bf16 [B][Hkv][T_cap][d]; same q, seq_lens,
  * out conventions. The measurement comparator for the packed path (no page counterpart beyond the
  * full-cache FlashAttention-2 decoding that RDKV compares against). */

@@ -753,19 +753,29 @@ extern "C" kv_status kv_encode(const kv_params* p, const kv_cache* c, const void
   return kvtc::launch_encode(p->dev, *c, k, v, dtype, B, t_new, dst_pos_dev, g_encode_path, (cudaStream_t)stream);
 }
 
+namespace kvtc {
+// Argument checks shared by the decode entry points (everything except the workspace).
+kv_status check_decode_args(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
+                            const int32_t* seq_lens_dev, float softmax_scale, const float* out) {
+  kv_status st;
+  if ((st = check_params_on_device(p)) != KV_OK) return st;
+  if ((st = check_cache(p, c, B)) != KV_OK) return st;
+  KV_REQUIRE(q && seq_lens_dev && out, KV_ERR_INVALID_ARG, "null q, seq_lens or out");
+  KV_REQUIRE(Hq >= c->Hkv && Hq % c->Hkv == 0, KV_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, c->Hkv);
+  KV_REQUIRE(Hq / c->Hkv <= MAX_G, KV_ERR_UNSUPPORTED, "g = Hq/Hkv = %d > 8", Hq / c->Hkv);
+  KV_REQUIRE(aligned16(q) && aligned16(out), KV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  KV_REQUIRE(std::isfinite(softmax_scale), KV_ERR_INVALID_ARG, "non-finite softmax scale");
+  return KV_OK;
+}
+}  // namespace kvtc
+
 extern "C" kv_status kv_attend_decode(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
                                       const int32_t* seq_lens_dev, float softmax_scale, float* out,
                                       void* workspace, size_t ws_bytes, kv_stream_t stream) {
   clear_error();
   kv_status st;
-  if ((st = check_params_on_device(p)) != KV_OK) return st;
-  if ((st = check_cache(p, c, B)) != KV_OK) return st;
-  KV_REQUIRE(q && seq_lens_dev && out && workspace, KV_ERR_INVALID_ARG, "null q, seq_lens, out or workspace");
-  KV_REQUIRE(Hq >= c->Hkv && Hq % c->Hkv == 0, KV_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, c->Hkv);
-  KV_REQUIRE(Hq / c->Hkv <= MAX_G, KV_ERR_UNSUPPORTED, "g = Hq/Hkv = %d > 8", Hq / c->Hkv);
-  KV_REQUIRE(aligned16(q) && aligned16(out) && aligned16(workspace), KV_ERR_INVALID_ARG,
-             "q, out and workspace must be 16-byte aligned");
-  KV_REQUIRE(std::isfinite(softmax_scale), KV_ERR_INVALID_ARG, "non-finite softmax scale");
+  if ((st = kvtc::check_decode_args(p, c, q, B, Hq, seq_lens_dev, softmax_scale, out)) != KV_OK) return st;
+  KV_REQUIRE(workspace && aligned16(workspace), KV_ERR_INVALID_ARG, "workspace null or not 16-byte aligned");
   const DecodeLayout L = kvtc::decode_layout(B, c->Hkv, c->T_cap, current_device());
   KV_REQUIRE(ws_bytes >= L.total, KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
   return kvtc::launch_decode(p->dev, *c, q, B, Hq, seq_lens_dev, softmax_scale, out, workspace, L,

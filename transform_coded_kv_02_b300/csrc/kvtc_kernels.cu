@@ -26,6 +26,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kvtc_codec.cuh"
 #include "kvtc_internal.h"
@@ -1045,4 +1046,63 @@ kv_status launch_wait_selftest(cudaStream_t s) {
   return launch_check("wait self-test");
 }
 
+// ======================================================================================================
+// decode with the library's own fixed scratch (no allocation on the call path)
+// ======================================================================================================
+// The scratch array. Host code must not use its name as an address (on the host it is only a stand-in);
+// the device address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KV_NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_addr[NOALLOC_MAX_DEVICES] = {};
+
+static kv_status noalloc_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) {
+    set_error("device %d beyond the %d devices the static scratch table covers", dev, NOALLOC_MAX_DEVICES);
+    return KV_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      set_error("cudaGetSymbolAddress(static scratch) on device %d: %s", dev, cudaGetErrorString(e));
+      return KV_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return KV_OK;
+}
+
 }  // namespace kvtc
+
+extern "C" kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
+                                              const int32_t* seq_lens_dev, float softmax_scale, float* out,
+                                              kv_stream_t stream) {
+  kvtc::clear_error();
+  kv_status st = kvtc::check_decode_args(p, c, q, B, Hq, seq_lens_dev, softmax_scale, out);
+  if (st != KV_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    kvtc::set_error("cudaGetDevice failed");
+    return KV_ERR_CUDA;
+  }
+  const kvtc::DecodeLayout L = kvtc::decode_layout(B, c->Hkv, c->T_cap, dev);
+  if (L.total > (size_t)KV_NOALLOC_SCRATCH_BYTES) {
+    kvtc::set_error("decode of B=%d Hkv=%d T_cap=%lld needs %zu bytes of scratch, more than the library's fixed "
+                    "%u bytes; use kv_attend_decode with a workspace", B, c->Hkv, (long long)c->T_cap, L.total,
+                    (unsigned)KV_NOALLOC_SCRATCH_BYTES);
+    return KV_ERR_INVALID_ARG;
+  }
+  void* ws = nullptr;
+  if ((st = kvtc::noalloc_scratch_address(&ws)) != KV_OK) return st;
+  return kvtc::launch_decode(p->dev, *c, q, B, Hq, seq_lens_dev, softmax_scale, out, ws, L, (cudaStream_t)stream);
+}

@@ -65,6 +65,7 @@ _sig("kv_cache_bytes", c_size_t, [_P, c_int, c_int, c_int, c_int64])
 _sig("kv_encode", c_int, [_P, ctypes.POINTER(kv_cache), _P, _P, c_int, c_int, c_int64, _P, _P])
 _sig("kv_decode_workspace_bytes", c_size_t, [_P, c_int, c_int, c_int, c_int64])
 _sig("kv_attend_decode", c_int, [_P, ctypes.POINTER(kv_cache), _P, c_int, c_int, _P, c_float, _P, _P, c_size_t, _P])
+_sig("kv_attend_decode_noalloc", c_int, [_P, ctypes.POINTER(kv_cache), _P, c_int, c_int, _P, c_float, _P, _P])
 _sig("kv_decode_bf16_workspace_bytes", c_size_t, [c_int, c_int, c_int, c_int64])
 _sig("kv_attend_decode_bf16", c_int, [_P, _P, c_int, c_int, c_int, c_int64, _P, _P, c_float, _P, _P, c_size_t, _P])
 _sig("kv_check_status", c_int, [_P])
@@ -220,6 +221,17 @@ def kv_attend_decode(params, cache, q, B, Hq, seq_lens, softmax_scale, out, work
     _check("kv_attend_decode", _lib.kv_attend_decode(params.handle, ctypes.byref(cache), _ptr(q), B, Hq,
                                                      _ptr(seq_lens), softmax_scale, _ptr(out), _ptr(workspace),
                                                      nbytes, _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def kv_attend_decode_noalloc(params, cache, q, B, Hq, seq_lens, softmax_scale, out, stream=None):
+    """Decode attention using the library's fixed static scratch instead of a caller workspace (for callers
+    that cannot allocate device memory). Calls that overlap on the GPU race on that scratch."""
+    _check("kv_attend_decode_noalloc", _lib.kv_attend_decode_noalloc(params.handle, ctypes.byref(cache), _ptr(q), B,
+                                                                     Hq, _ptr(seq_lens), softmax_scale, _ptr(out),
+                                                                     _stream(stream)))
 
 
 def kv_decode_bf16_workspace_bytes(B, Hkv, Hq, T_cap):
