@@ -27,13 +27,20 @@ attention; IEEE fp32 for the quantiser, whose op sequence is part of the record 
       above B_max).
  5. Storage order: channels sorted by (width desc, lambda desc, eigen index asc); T = rows of U^T in
     that order; mu_j = rotated mean, sigma_j = sqrt(lambda_j) (fp32), inv_sigma_j = fp32(1/sigma_j).
+    Fixed-width layout [NOVA-KV: the allocation has to meet a fixed-width layout]: storage channels
+    (2k, 2k+1) form pair k and share one slot, at the same bit position in the low and the high 16-bit
+    half of one code word; a pair's slot is as wide as its wider channel. The narrower channel of a pair
+    is raised to the slot width (the layout reserves those bits anyway); slots are placed first-fit in
+    pair order (lowest code word with room, lowest free bit); while a pair finds no room, the pair with
+    the smallest distortion cost 3 (lambda_2k + lambda_2k+1) 4^-w of losing one bit (compared through
+    log2 at 1e-9 resolution; ties: the later pair) loses one bit and the placement restarts.
  6. Per-token quantiser (fixed fp32 op sequence, no fused multiply-add):
       y'_j = (y_j - mu_j) * inv_sigma_j                 (channels with b_j > 0)
       m, M = min/max of y'_j over b_j > 0;  z = fp16(m), s = fp16(M - z) (round-to-nearest-even, saturated)
       c_j = clamp(floor(((y'_j - z) / s) * 2^b_j), 0, 2^b_j - 1);  all codes 0 when s == 0.
  7. Fixed-width record [NOVA-KV: "a fixed per-token bit count"]: R_w 32-bit words per token; word 0 holds
-    z (bits 0-15) and s (bits 16-31); codes follow LSB-first from bit 0 of word 1 in storage order;
-    unused bits are 0.
+    z (bits 0-15) and s (bits 16-31); pair k's codes sit in code word 1 + u_k: channel 2k at bits
+    [r_k, r_k + b_2k), channel 2k+1 at bits [16 + r_k, 16 + r_k + b_2k+1); unused bits are 0.
  8. Decode attention over the records: y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j) for b_j > 0, else
     mu_j; k^ = T^T y^ (and v^); o_h = softmax_t(alpha q_h . k^_t) v^ over t < seq_len, all in fp64.
 
@@ -168,14 +175,64 @@ def storage_order(widths, lam):
     return sorted(range(d), key=lambda i: (-int(widths[i]), -float(lam[i]), i))
 
 
-def bit_offsets(widths):
+HALF = 16   # bits per half of a code word
+
+
+def slot_layout(widths, r_words: int):
+    """First-fit placement of the pair slots: pair k = storage channels (2k, 2k+1), slot width
+    max(b_2k, b_2k+1), placed in pair order into the lowest code word (0 .. R_w - 2) whose halves have
+    that many free bits, at the lowest free bit. Returns (word [d/2], pos [d/2]) with -1 for empty slots,
+    or None when some slot finds no room."""
     w = np.asarray(widths, np.int64)
-    return np.concatenate([[0], np.cumsum(w)[:-1]]).astype(np.int64)
+    if w.shape[0] % 2:
+        w = np.concatenate([w, [0]])
+    n_words = r_words - 1
+    used = [0] * max(n_words, 0)
+    word = np.full(w.shape[0] // 2, -1, np.int64)
+    pos = np.full(w.shape[0] // 2, -1, np.int64)
+    for k in range(w.shape[0] // 2):
+        sw = int(max(w[2 * k], w[2 * k + 1]))
+        if sw == 0:
+            continue
+        for u in range(n_words):
+            if used[u] + sw <= HALF:
+                word[k], pos[k] = u, used[u]
+                used[u] += sw
+                break
+        else:
+            return None
+    return word, pos
+
+
+def fit_cost_key(pair_importance: float, width: int) -> int:
+    """Integer key ordering the cost 3 (lambda_2k + lambda_2k+1) 4^-w of taking one bit from a pair of
+    width w: log2 of the cost (less the common log2 3) at 1e-9 resolution, so that costs equal in exact
+    arithmetic compare equal after rounding noise of the statistics."""
+    if pair_importance <= 0:
+        return -(1 << 62)
+    return int(np.rint(np.log2(pair_importance) * 1e9)) - 2_000_000_000 * int(width)
+
+
+def fit_layout(widths, importance, r_words: int):
+    """Widths (storage order) that the pair layout can hold: each pair's narrower channel raised to the
+    pair's slot width, then single bits taken from the cheapest pair (smallest cost key; ties to the later
+    pair) until first-fit placement succeeds."""
+    b = np.asarray(widths, np.int64)
+    lam = np.asarray(importance, F64)
+    d = b.shape[0]
+    assert d % 2 == 0
+    w = [int(max(b[2 * k], b[2 * k + 1])) for k in range(d // 2)]
+    plam = [float(lam[2 * k] + lam[2 * k + 1]) for k in range(d // 2)]
+    while slot_layout(np.repeat(w, 2), r_words) is None:
+        _, negk = min((fit_cost_key(plam[k], w[k]), -k) for k in range(d // 2) if w[k] > 0)
+        w[-negk] -= 1
+    return np.repeat(np.asarray(w, np.int64), 2)
 
 
 class TensorParams:
     """One tensor's (K or V) codec parameters in storage order. T: fp32 [d, d] (rows = storage channels);
-    mu, sigma, inv_sigma: fp32 [d]; widths: int [d]; r_words: record length in 32-bit words."""
+    mu, sigma, inv_sigma: fp32 [d]; widths: int [d]; r_words: record length in 32-bit words; slot_word /
+    slot_pos: first-fit placement of each channel pair."""
 
     def __init__(self, T, mu, sigma, widths, r_words, eigvals=None, importance=None):
         self.T = np.ascontiguousarray(T, F32)
@@ -187,11 +244,12 @@ class TensorParams:
         self.inv_sigma = np.where(self.sigma > 0, (1.0 / np.where(self.sigma > 0, self.sigma, 1)
                                                    .astype(F64)), 0.0).astype(F32)
         self.r_words = int(r_words)
-        self.offsets = bit_offsets(self.widths)
         self.eigvals = eigvals
         self.importance = importance
-        if int(self.widths.sum()) > code_bits(self.r_words):
-            raise ValueError("widths exceed the record's code bits")
+        lay = slot_layout(self.widths, self.r_words)
+        if lay is None:
+            raise ValueError("widths do not fit the record's pair layout")
+        self.slot_word, self.slot_pos = lay
 
     @property
     def d(self):
@@ -201,11 +259,13 @@ class TensorParams:
 def build_tensor_params(mu_raw, lam, u, importance, r_words: int, max_bits: int) -> TensorParams:
     widths_eig = water_fill_integer(importance, code_bits(r_words), max_bits)
     order = storage_order(widths_eig, importance)
+    imp_st = np.asarray(importance)[order]
+    widths = fit_layout(widths_eig[order], imp_st, r_words)
     T = u[:, order].T                                   # rows: storage channels
     mu_rot = T @ np.asarray(mu_raw, F64)
     sigma = np.sqrt(np.maximum(lam[order], 0.0))
-    return TensorParams(T=T, mu=mu_rot, sigma=sigma, widths=widths_eig[order], r_words=r_words,
-                        eigvals=lam[order], importance=np.asarray(importance)[order])
+    return TensorParams(T=T, mu=mu_rot, sigma=sigma, widths=widths, r_words=r_words,
+                        eigvals=lam[order], importance=imp_st)
 
 
 def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8):
@@ -266,6 +326,12 @@ def quantize(y32, p: TensorParams):
 # ----------------------------------------------------------------------------------------------------
 # 7. record packing
 # ----------------------------------------------------------------------------------------------------
+def _slot_of(p: TensorParams, j: int):
+    """(code word index within the record, bit shift) of storage channel j."""
+    k = j // 2
+    return 1 + int(p.slot_word[k]), int(p.slot_pos[k]) + HALF * (j % 2)
+
+
 def pack(z16, s16, codes, p: TensorParams):
     """-> uint32 records [n, R_w]."""
     codes = np.asarray(codes, np.int64)
@@ -275,15 +341,10 @@ def pack(z16, s16, codes, p: TensorParams):
     sb = np.asarray(s16, np.float16).view(np.uint16).astype(np.uint64)
     rec[:, 0] = zb | (sb << np.uint64(16))
     for j in range(d):
-        b = int(p.widths[j])
-        if b == 0:
+        if int(p.widths[j]) == 0:
             continue
-        o = int(p.offsets[j])
-        w, sh = 1 + o // 32, o % 32
-        c = codes[:, j].astype(np.uint64)
-        rec[:, w] |= (c << np.uint64(sh)) & np.uint64(0xFFFFFFFF)
-        if sh + b > 32:
-            rec[:, w + 1] |= c >> np.uint64(32 - sh)
+        w, sh = _slot_of(p, j)
+        rec[:, w] |= codes[:, j].astype(np.uint64) << np.uint64(sh)
     return rec.astype(np.uint32)
 
 
@@ -298,12 +359,8 @@ def unpack(rec, p: TensorParams):
         b = int(p.widths[j])
         if b == 0:
             continue
-        o = int(p.offsets[j])
-        w, sh = 1 + o // 32, o % 32
-        val = rec[:, w] >> np.uint64(sh)
-        if sh + b > 32:
-            val |= rec[:, w + 1] << np.uint64(32 - sh)
-        codes[:, j] = (val & np.uint64((1 << b) - 1)).astype(np.int64)
+        w, sh = _slot_of(p, j)
+        codes[:, j] = ((rec[:, w] >> np.uint64(sh)) & np.uint64((1 << b) - 1)).astype(np.int64)
     return z16, s16, codes
 
 

@@ -261,12 +261,22 @@ def pin_quantize_pack_golden():
         assert np.allclose(yh[0], _floats(yhat), atol=1e-12), (name, yh)
 
 
+def _words_needed(widths):
+    """Smallest record length whose pair layout holds the widths (first-fit), for test set-up."""
+    r = 2
+    while O.slot_layout(widths, r) is None:
+        r += 1
+    return r
+
+
 def pin_pack_roundtrip():
+    """Random widths 0..16 in any order: pack then unpack returns the codes, z and s; every bit outside the
+    channels' slots is zero; the slots of one code word never overlap."""
     rng = np.random.default_rng(6)
     for trial in range(40):
         d = int(rng.integers(1, 130))
         widths = rng.integers(0, 17, d)
-        r_words = 1 + (int(widths.sum()) + 31) // 32 + int(rng.integers(0, 2))
+        r_words = _words_needed(widths) + int(rng.integers(0, 2))
         p = _params_from_row(widths, np.zeros(d), np.ones(d), r_words)
         n = 7
         codes = np.stack([rng.integers(0, 2 ** int(b), n) if b > 0 else np.zeros(n, np.int64)
@@ -278,13 +288,59 @@ def pin_pack_roundtrip():
         assert np.array_equal(c2, codes)
         assert np.array_equal(z2.view(np.uint16), z.view(np.uint16))
         assert np.array_equal(s2.view(np.uint16), s.view(np.uint16))
-        used = int(widths.sum())
-        for wi in range(1, r_words):   # bits past the last code are zero
-            lo = 32 * (wi - 1)
-            if used <= lo:
-                assert np.all(rec[:, wi] == 0)
-            elif used < lo + 32:
-                assert np.all((rec[:, wi].astype(np.uint64) >> np.uint64(used - lo)) == 0)
+        owned = np.zeros(r_words, np.uint64)
+        for j in range(d):
+            b = int(widths[j])
+            if b == 0:
+                continue
+            k = j // 2
+            w = 1 + int(p.slot_word[k])
+            sh = int(p.slot_pos[k]) + 16 * (j % 2)
+            assert int(p.slot_pos[k]) + b <= 16
+            m = np.uint64(((1 << b) - 1) << sh)
+            assert (owned[w] & m) == 0            # no two channels share a bit
+            owned[w] |= m
+        for w in range(1, r_words):
+            assert np.all((rec[:, w].astype(np.uint64) & ~owned[w] & np.uint64(0xFFFFFFFF)) == 0)
+
+
+def pin_layout_fit_golden():
+    """Hand-solved fits of water-filling widths to the pair layout (tests/golden/layout_fit_small.txt)."""
+    for widths, imp, rw, fitted, words, pos in read_golden("layout_fit_small.txt"):
+        f = O.fit_layout(_ints(widths), _floats(imp), int(rw))
+        assert f.tolist() == _ints(fitted).tolist(), (widths, f)
+        lay = O.slot_layout(f, int(rw))
+        assert lay is not None
+        assert lay[0].tolist() == _ints(words).tolist() and lay[1].tolist() == _ints(pos).tolist(), lay
+
+
+def pin_layout_fit_properties():
+    """On the workloads' calibrations: the fitted widths fit the record, both channels of a pair share one
+    width no larger than the pair's wider water-filling width, and the white-noise distortion
+    sum_j lambda_j 4^-b_j grows by at most 2% over the unconstrained integer allocation."""
+    worst = 1.0
+    for name, bits in (("tiny", 2.75), ("llama_long_128k", 1.33), ("qwen_batched_8k", 2.0),
+                       ("qwen_batched_8k", 4.0)):
+        L = synth.make_layer(synth.WORKLOADS[name], T=64, B=1, steps=1)
+        mu_k, s_k, mu_v, s_v, m_q = O.calib_statistics(L.calib_k[0], L.calib_v[0], L.calib_q[0])
+        for lam_u, imp_fn in ((O.klt(s_k), lambda l, u: O.key_importance(l, u, m_q)),
+                              (O.klt(s_v), lambda l, u: O.value_importance(l))):
+            lam, u = lam_u
+            imp = imp_fn(lam, u)
+            r = O.record_words(bits, 128)
+            b = O.water_fill_integer(imp, O.code_bits(r), 8)
+            order = O.storage_order(b, imp)
+            b, imp = b[order], np.asarray(imp)[order]
+            f = O.fit_layout(b, imp, r)
+            assert O.slot_layout(f, r) is not None
+            assert np.array_equal(f[0::2], f[1::2])
+            assert np.all(f[0::2] <= np.maximum(b[0::2], b[1::2]))
+            assert f.sum() <= O.code_bits(r)
+            d0 = float(np.sum(imp * 4.0 ** (-b.astype(np.float64))))
+            d1 = float(np.sum(imp * 4.0 ** (-f.astype(np.float64))))
+            worst = max(worst, d1 / d0)
+    assert worst <= 1.02, worst
+    return worst
 
 
 def pin_quantizer_error_bound():
@@ -340,18 +396,24 @@ def brute_force_decode(q, rec_k, rec_v, pk, pv, seq_len, scale):
         word0 = int(rec[0])
         z = float(np.array([word0 & 0xFFFF], np.uint16).view(np.float16)[0])
         s = float(np.array([word0 >> 16], np.uint16).view(np.float16)[0])
-        bits = 0
-        for i in range(1, len(rec)):
-            bits |= int(rec[i]) << (32 * (i - 1))
+        # pair slots, placed first-fit by hand: pair k = channels (2k, 2k+1), slot width = the wider one
+        free = [16] * (len(rec) - 1)
+        where = {}
+        for k in range(d // 2):
+            sw = max(int(p.widths[2 * k]), int(p.widths[2 * k + 1]))
+            if sw == 0:
+                continue
+            u = next(i for i in range(len(free)) if free[i] >= sw)
+            where[k] = (u, 16 - free[u])
+            free[u] -= sw
         y = []
-        off = 0
         for j in range(d):
             b = int(p.widths[j])
             if b == 0:
                 y.append(float(p.mu[j]))
                 continue
-            c = (bits >> off) & ((1 << b) - 1)
-            off += b
+            u, r = where[j // 2]
+            c = (int(rec[1 + u]) >> (r + 16 * (j % 2))) & ((1 << b) - 1)
             y.append(float(p.mu[j]) + float(p.sigma[j]) * (z + (c + 0.5) * s / (2 ** b)))
         x = []
         for col in range(d):
@@ -388,15 +450,17 @@ def pin_decode_brute_force():
 
 
 def pin_calibrate_structure():
-    """Calibrated sets: orthogonal T, widths non-increasing in storage order and summing to the budget,
-    mu = T mu_raw, sigma^2 = eigenvalues."""
+    """Calibrated sets: orthogonal T; both channels of a pair share one width; the widths fit the record's
+    pair layout and use at most the budget and at least all but one code word of it; mu = T mu_raw,
+    sigma^2 = eigenvalues."""
     L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
     ck, cv, cq = L.calib_k[0], L.calib_v[0], L.calib_q[0]
     pk, pv = O.calibrate(ck, cv, cq, 2.75, 2.75)
     for p, x in ((pk, ck), (pv, cv)):
         t = p.T.astype(np.float64)
         assert np.linalg.norm(t @ t.T - np.eye(128)) < 1e-5
-        assert np.all(np.diff(p.widths) <= 0)
-        assert p.widths.sum() == O.code_bits(11)
+        assert np.array_equal(p.widths[0::2], p.widths[1::2])
+        assert O.code_bits(11) - 32 < p.widths.sum() <= O.code_bits(11)
+        assert O.slot_layout(p.widths, 11) is not None
         assert np.allclose(p.mu, t @ np.asarray(x, np.float64).mean(0), atol=1e-5)
         assert np.allclose(p.sigma.astype(np.float64) ** 2, p.eigvals, rtol=1e-5)

@@ -191,7 +191,9 @@ def test_decode_ragged_lengths(tiny, seq_len):
 
 
 def test_decode_split_count_invariance(tiny):
-    """Different cache capacities give different split plans over the same 1000 tokens."""
+    """Different cache capacities give different split plans over the same 1000 tokens. The results differ
+    only by rounding: fp32 merge order, and the fp16 hi/lo split of p*s taken against each split's running
+    maximum (about 1e-5 relative); a merge mistake would be of order one."""
     w, L, sets, P = tiny
     k, v = synth.as_float(L.k), synth.as_float(L.v)
     outs = []
@@ -199,7 +201,7 @@ def test_decode_split_count_invariance(tiny):
         rk, rv = G.oracle_cache(k, v, sets, False, T_cap)
         outs.append(G.run_decode(P, rk, rv, L.q[0], [1000], w.Hq, False))
     for o in outs[1:]:
-        assert G.rel_l2_rows(o, outs[0]).max() <= 1e-5
+        assert G.rel_l2_rows(o, outs[0]).max() <= 1e-4
 
 
 @pytest.mark.parametrize("bits", [2.0, 3.0, 4.0])

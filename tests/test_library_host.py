@@ -141,10 +141,18 @@ def test_params_from_arrays_validation():
         kvtc.kv_params_from_arrays(T, mu, sg, w, 10, T, mu, sg, w, 11)
     assert e.value.status == kvtc.KV_ERR_BUDGET
     w2 = np.zeros((1, d), np.int32)
-    w2[0, 5] = 3  # not a prefix
+    w2[0, :48] = 6  # 288 bits fit the budget, but 24 six-bit slots need 12 code words (2 per word)
     with pytest.raises(kvtc.KvError) as e:
         kvtc.kv_params_from_arrays(T, mu, sg, w2, 11, T, mu, sg, w2, 11)
+    assert e.value.status == kvtc.KV_ERR_BUDGET
+    w3 = np.zeros((1, d), np.int32)
+    w3[0, 5] = 9  # wider than 8 bits
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_params_from_arrays(T, mu, sg, w3, 11, T, mu, sg, w3, 11)
     assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+    w4 = np.zeros((1, d), np.int32)
+    w4[0, 5] = 3  # zero-width channels before a nonzero one are allowed (a pair may lose all its bits)
+    kvtc.kv_params_from_arrays(T, mu, sg, w4, 11, T, mu, sg, w4, 11)
     P = kvtc.kv_params_from_arrays(T, mu, sg, w, 11, T, mu, sg, w, 11)
     assert P.record_words(0) == 11 and P.info(0, 0)["widths"].sum() == 320
 

@@ -8,7 +8,8 @@ from oracle import kvtc_oracle as O
 
 _orig = {name: getattr(O, name) for name in
          ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
-          "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat"]}
+          "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat",
+          "slot_layout", "fit_layout"]}
 
 
 def _klt_transposed(sigma):
@@ -118,6 +119,55 @@ def _half_truncate(x):
     return np.where(over, np.nextafter(h, np.float16(0)), h).astype(np.float16)
 
 
+def _slot_layout_next_fit(widths, r_words):
+    """Never returns to an earlier code word."""
+    w = np.asarray(widths, np.int64)
+    if w.shape[0] % 2:
+        w = np.concatenate([w, [0]])
+    word = np.full(w.shape[0] // 2, -1, np.int64)
+    pos = np.full(w.shape[0] // 2, -1, np.int64)
+    u, used = 0, 0
+    for k in range(w.shape[0] // 2):
+        sw = int(max(w[2 * k], w[2 * k + 1]))
+        if sw == 0:
+            continue
+        if used + sw > 16:
+            u, used = u + 1, 0
+        if u >= r_words - 1:
+            return None
+        word[k], pos[k] = u, used
+        used += sw
+    return word, pos
+
+
+def _fit_ties_to_earlier(widths, importance, r_words):
+    b = np.asarray(widths, np.int64)
+    lam = np.asarray(importance, np.float64)
+    w = [int(max(b[2 * k], b[2 * k + 1])) for k in range(len(b) // 2)]
+    plam = [float(lam[2 * k] + lam[2 * k + 1]) for k in range(len(b) // 2)]
+    while O.slot_layout(np.repeat(w, 2), r_words) is None:
+        _, k = min((O.fit_cost_key(plam[k], w[k]), k) for k in range(len(w)) if w[k] > 0)
+        w[k] -= 1
+    return np.repeat(np.asarray(w, np.int64), 2)
+
+
+def _fit_cost_ignores_width(widths, importance, r_words):
+    b = np.asarray(widths, np.int64)
+    lam = np.asarray(importance, np.float64)
+    w = [int(max(b[2 * k], b[2 * k + 1])) for k in range(len(b) // 2)]
+    plam = [float(lam[2 * k] + lam[2 * k + 1]) for k in range(len(b) // 2)]
+    while O.slot_layout(np.repeat(w, 2), r_words) is None:
+        _, negk = min((plam[k], -k) for k in range(len(w)) if w[k] > 0)
+        w[-negk] -= 1
+    return np.repeat(np.asarray(w, np.int64), 2)
+
+
+def _fit_no_promotion(widths, importance, r_words):
+    f = _orig["fit_layout"](widths, importance, r_words)
+    b = np.asarray(widths, np.int64)
+    return np.minimum(f, b)
+
+
 MUTATIONS = [
     ("klt", _klt_transposed, P.pin_klt_known_spectrum),
     ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
@@ -134,6 +184,10 @@ MUTATIONS = [
     ("reconstruct", _reconstruct_transposed, P.pin_decode_brute_force),
     ("attention", _attention_unscaled, P.pin_decode_brute_force),
     ("half_rn_sat", _half_truncate, P.pin_half_conversion),
+    ("slot_layout", _slot_layout_next_fit, P.pin_layout_fit_golden),
+    ("fit_layout", _fit_ties_to_earlier, P.pin_layout_fit_golden),
+    ("fit_layout", _fit_cost_ignores_width, P.pin_layout_fit_golden),
+    ("fit_layout", _fit_no_promotion, P.pin_layout_fit_golden),
 ]
 
 

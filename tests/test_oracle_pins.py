@@ -59,6 +59,15 @@ def test_pack_roundtrip():
     P.pin_pack_roundtrip()
 
 
+def test_layout_fit_golden():
+    P.pin_layout_fit_golden()
+
+
+def test_layout_fit_properties():
+    worst = P.pin_layout_fit_properties()
+    print(f"worst distortion ratio of the fitted layout vs the unconstrained allocation: {worst:.4f}")
+
+
 def test_quantizer_error_bound():
     P.pin_quantizer_error_bound()
 

@@ -1,8 +1,9 @@
 // Per-token codec on the device: quantiser and record packer (encode side), record unpacker (decode side).
 //
 // Record of one token and tensor [NOVA-KV, third abstract of the "SPHERICAL KV" page: "a fixed per-token
-// bit count"]: r_words 32-bit words; word 0 = fp16 zero point z | fp16 scale s << 16; channel codes
-// LSB-first from bit 0 of word 1 in storage order (widths non-increasing, zero-width channels last).
+// bit count", fixed-width layout]: r_words 32-bit words; word 0 = fp16 zero point z | fp16 scale s << 16;
+// storage channels (2k, 2k+1) share slot k: code word 1 + u_k, channel 2k at bits [r_k, r_k + b_2k),
+// channel 2k+1 at bits [16 + r_k, 16 + r_k + b_2k+1) (slots placed first-fit by the host).
 //
 // Quantiser, one fixed fp32 op sequence (explicit _rn intrinsics, nothing fused), channels with b_j > 0:
 //   y'_j = (y_j - mu_j) * inv_sigma_j;  m = min y', M = max y';  z = fp16_rn(sat(m + 0)),
@@ -66,15 +67,15 @@ __device__ __forceinline__ void quantize_pack_warp(const TensorDev& td, int set,
   const int R = td.r_words;
   for (int i = lane; i < R; i += 32) rec_s[i] = 0u;
   __syncwarp();
-  const int nbits = b[0] + b[1] + b[2] + b[3];
-  if (nbits > 0) {
-    const uint64_t chunk = (uint64_t)c[0] | ((uint64_t)c[1] << b[0]) | ((uint64_t)c[2] << (b[0] + b[1])) |
-                           ((uint64_t)c[3] << (b[0] + b[1] + b[2]));
-    const int o = td.offs[so];
-    const uint64_t v = chunk << (o & 31);
-    atomicOr(&rec_s[1 + (o >> 5)], (uint32_t)v);
-    const uint32_t hi = (uint32_t)(v >> 32);
-    if (hi) atomicOr(&rec_s[2 + (o >> 5)], hi);
+  // lane holds pairs 2 lane and 2 lane + 1
+  const uint2 sd = *reinterpret_cast<const uint2*>(td.slots + (size_t)set * (D / 2) + 2 * lane);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t desc = i ? sd.y : sd.x;
+    if (desc) {
+      const uint32_t u = desc & 255u, r = (desc >> 8) & 255u;
+      atomicOr(&rec_s[1 + u], (c[2 * i] << r) | (c[2 * i + 1] << (16 + r)));
+    }
   }
   __syncwarp();
   if (lane == 0) rec_s[0] = (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
@@ -105,60 +106,61 @@ __device__ __forceinline__ void quantize_pack_thread(const TensorDev& td, int se
     sh = half_sat_rn(__fsub_rn(M, __half2float(zh)));
   }
   const float zf = __half2float(zh), sf = __half2float(sh);
-  emit(0, (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16));
-  uint64_t buf = 0;
-  int nb = 0, w = 1;
-  for (int j = 0; j < nz; ++j) {
-    const int b = __ldg(wd + j);
-    uint32_t c = 0;
-    if (sf != 0.f) c = quantize_code(__fmul_rn(__fsub_rn(gy(j), __ldg(mu + j)), __ldg(inv + j)), zf, sf, b);
-    buf |= (uint64_t)c << nb;
-    nb += b;
-    if (nb >= 32) {
-      emit(w++, (uint32_t)buf);
-      buf >>= 32;
-      nb -= 32;
+  uint32_t acc[MAX_RW];
+  for (int w = 0; w < td.r_words; ++w) acc[w] = 0u;
+  acc[0] = (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
+  const uint32_t* sl = td.slots + (size_t)set * (D / 2);
+  for (int k = 0; 2 * k < nz; ++k) {
+    const uint32_t desc = __ldg(sl + k);
+    if (!desc || sf == 0.f) continue;
+    uint32_t c[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = 2 * k + i, b = __ldg(wd + j);
+      if (b > 0) c[i] = quantize_code(__fmul_rn(__fsub_rn(gy(j), __ldg(mu + j)), __ldg(inv + j)), zf, sf, b);
     }
+    const uint32_t u = desc & 255u, r = (desc >> 8) & 255u;
+    acc[1 + u] |= (c[0] << r) | (c[1] << (16 + r));
   }
-  if (nb > 0) emit(w++, (uint32_t)buf);
-  for (; w < td.r_words; ++w) emit(w, 0u);
+  for (int w = 0; w < td.r_words; ++w) emit(w, acc[w]);
 }
 
 // ------------------------------------------------------------------------------------------------------
-// decode-side unpacker: channels 4q..4q+3 of one record -> two fp16 pairs holding (c + 1/2) exactly.
-// Codes are OR-ed under the fp16 exponent of 1024 (0x6400: value 1024 + c for c < 1024), then 1023.5 is
-// subtracted, which is exact for c < 1024.
+// decode-side unpacker: channels 4q..4q+3 (slots 2q, 2q+1) of one record -> two fp16 pairs holding (c + 1/2)
+// exactly. A slot's code word shifted right by the slot's bit leaves channel 2k at bit 0 and channel 2k+1 at
+// bit 16; both are masked and OR-ed under the fp16 exponent of 1024 (0x6400: value 1024 + c for c < 1024),
+// then 1023.5 is subtracted, which is exact.
 // ------------------------------------------------------------------------------------------------------
 struct QuadDesc {
-  uint32_t wq, sh, s1, s2, s3, m0, m1, m2, m3;
+  uint32_t w0, r0, m0, w1, r1, m1;
 };
 
+__device__ __forceinline__ uint32_t slot_mask(uint32_t desc) {
+  const uint32_t b0 = (desc >> 16) & 255u, b1 = desc >> 24;
+  return ((1u << b0) - 1u) | (((1u << b1) - 1u) << 16);
+}
+
 __device__ __forceinline__ QuadDesc load_quad(const TensorDev& td, int set, int q) {
-  const uint4 a = __ldg(td.quads + ((size_t)set * 32 + q) * 2);
-  const uint4 b = __ldg(td.quads + ((size_t)set * 32 + q) * 2 + 1);
+  const uint2 sd = __ldg(reinterpret_cast<const uint2*>(td.slots + (size_t)set * (D / 2)) + q);
   QuadDesc d;
-  d.wq = a.x & 255u;
-  d.sh = (a.x >> 8) & 255u;
-  d.s1 = (a.x >> 16) & 255u;
-  d.s2 = a.x >> 24;
-  d.m0 = a.y;
-  d.m1 = a.z;
-  d.s3 = a.w;
-  d.m2 = b.x;
-  d.m3 = b.y;
+  d.w0 = sd.x & 255u;
+  d.r0 = (sd.x >> 8) & 255u;
+  d.m0 = slot_mask(sd.x);
+  d.w1 = sd.y & 255u;
+  d.r1 = (sd.y >> 8) & 255u;
+  d.m1 = slot_mask(sd.y);
   return d;
 }
 
-__device__ __forceinline__ uint2 unpack_quad(const uint32_t* rec, const QuadDesc& d) {
-  const uint32_t w0 = rec[1 + d.wq], w1 = rec[2 + d.wq];
-  const uint32_t x = __funnelshift_r(w0, w1, d.sh);
-  const uint32_t h01 = (x & d.m0) | ((x << d.s1) & d.m1) | 0x64006400u;
-  const uint32_t y = x >> d.s2;
-  const uint32_t h23 = (y & d.m2) | ((y << d.s3) & d.m3) | 0x64006400u;
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t word, uint32_t r, uint32_t m) {
+  const uint32_t h = ((word >> r) & m) | 0x64006400u;
   const __half2 off = __halves2half2(__ushort_as_half(0x63FF), __ushort_as_half(0x63FF));  // 1023.5
-  const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&h01), off);
-  const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&h23), off);
-  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), off);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint2 unpack_quad(const uint32_t* rec, const QuadDesc& d) {
+  return make_uint2(unpack_pair(rec[1 + d.w0], d.r0, d.m0), unpack_pair(rec[1 + d.w1], d.r1, d.m1));
 }
 
 // thread -> (quad, first row, row step) of a cooperative unpack over a tile of records

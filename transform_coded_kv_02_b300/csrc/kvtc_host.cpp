@@ -224,6 +224,65 @@ static void moments(const float* x, int64_t n, int d, bool centre, std::vector<d
     }
 }
 
+// ------------------------------------------------------------------------------------------------------
+// fixed-width record layout [NOVA-KV: fixed per-token bit count, fixed-width layout]: storage channels
+// (2k, 2k+1) share a slot of width max(b_2k, b_2k+1) at the same bit of the low and the high half of one
+// code word; slots are placed first-fit in pair order.
+// ------------------------------------------------------------------------------------------------------
+bool kvtc::slot_layout(const int32_t* w, int d, int rw, int* word, int* pos) {
+  int used[MAX_RW] = {0};
+  const int nw = rw - 1;
+  for (int k = 0; k < d / 2; ++k) {
+    const int sw = std::max(w[2 * k], w[2 * k + 1]);
+    word[k] = pos[k] = -1;
+    if (sw == 0) continue;
+    int u = 0;
+    while (u < nw && used[u] + sw > 16) ++u;
+    if (u >= nw) return false;
+    word[k] = u;
+    pos[k] = used[u];
+    used[u] += sw;
+  }
+  return true;
+}
+
+// Order of the cost 3 (lambda_2k + lambda_2k+1) 4^-w of taking one bit from a pair: log2 at 1e-9
+// resolution (less the common log2 3), so that costs equal in exact arithmetic compare equal.
+static long long fit_cost_key(double pair_importance, int width) {
+  if (!(pair_importance > 0.0)) return -(1LL << 62);
+  return (long long)std::nearbyint(std::log2(pair_importance) * 1e9) - 2000000000LL * width;
+}
+
+// Raise the narrower channel of each pair to the slot width, then take single bits from the cheapest pair
+// (ties: the later pair) until the first-fit placement succeeds.
+static void fit_layout(int32_t* w, const double* imp, int d, int rw) {
+  const int np = d / 2;
+  std::vector<int32_t> sw(np), wide(d);
+  std::vector<double> plam(np);
+  for (int k = 0; k < np; ++k) {
+    sw[k] = std::max(w[2 * k], w[2 * k + 1]);
+    plam[k] = imp[2 * k] + imp[2 * k + 1];
+  }
+  std::vector<int> word(np), pos(np);
+  for (;;) {
+    for (int k = 0; k < np; ++k) wide[2 * k] = wide[2 * k + 1] = sw[k];
+    if (kvtc::slot_layout(wide.data(), d, rw, word.data(), pos.data())) break;
+    int best = -1;
+    long long best_key = 0;
+    for (int k = 0; k < np; ++k) {
+      if (sw[k] <= 0) continue;
+      const long long key = fit_cost_key(plam[k], sw[k]);
+      if (best < 0 || key <= best_key) {
+        best = k;
+        best_key = key;
+      }
+    }
+    if (best < 0) break;  // nothing left to take (cannot happen for rw >= 1)
+    --sw[best];
+  }
+  for (int j = 0; j < d; ++j) w[j] = wide[j];
+}
+
 static void build_tensor(const std::vector<double>& mu_raw, const std::vector<double>& lam,
                          const std::vector<double>& U, const std::vector<double>& imp, int rw, int bmax,
                          int d, SetResult& r, int t) {
@@ -236,6 +295,13 @@ static void build_tensor(const std::vector<double>& mu_raw, const std::vector<do
     if (imp[a] != imp[b]) return imp[a] > imp[b];
     return a < b;
   });
+  std::vector<int32_t> ws(d);
+  std::vector<double> imps(d);
+  for (int j = 0; j < d; ++j) {
+    ws[j] = w[order[j]];
+    imps[j] = imp[order[j]];
+  }
+  fit_layout(ws.data(), imps.data(), d, rw);
   r.T[t].resize((size_t)d * d);
   r.mu[t].resize(d);
   r.sigma[t].resize(d);
@@ -252,9 +318,9 @@ static void build_tensor(const std::vector<double>& mu_raw, const std::vector<do
     }
     r.mu[t][j] = (float)m;
     r.sigma[t][j] = (float)sqrt(std::max(lam[e], 0.0));
-    r.widths[t][j] = r.sigma[t][j] > 0.f ? w[e] : 0;
+    r.widths[t][j] = r.sigma[t][j] > 0.f ? ws[j] : 0;
     r.eig[t][j] = lam[e];
-    r.imp[t][j] = imp[e];
+    r.imp[t][j] = imps[j];
   }
 }
 
@@ -383,7 +449,6 @@ extern "C" kv_status kv_params_from_arrays(int d, int n_sets, const float* T_k, 
     p->eig[t].resize(n);
     p->imp[t].assign(n, 0.0);
     for (int s = 0; s < n_sets; ++s) {
-      long long sum = 0;
       for (int j = 0; j < d; ++j) {
         const size_t i = (size_t)s * d + j;
         if (!(p->sigma[t][i] > 0.f)) p->widths[t][i] = 0;
@@ -391,17 +456,13 @@ extern "C" kv_status kv_params_from_arrays(int d, int n_sets, const float* T_k, 
           delete p;
           KV_REQUIRE(false, KV_ERR_INVALID_ARG, "set %d channel %d: width out of range 0..8", s, j);
         }
-        if (j > 0 && p->widths[t][i] > 0 && p->widths[t][i - 1] == 0) {
-          delete p;
-          KV_REQUIRE(false, KV_ERR_INVALID_ARG,
-                     "set %d: channels with width > 0 must form a prefix of the storage order", s);
-        }
-        sum += p->widths[t][i];
         p->eig[t][i] = (double)p->sigma[t][i] * p->sigma[t][i];
       }
-      if (sum > 32LL * rws[t] - 32) {
+      int word[D / 2], pos[D / 2];
+      if (!kvtc::slot_layout(&p->widths[t][(size_t)s * d], d, rws[t], word, pos)) {
         delete p;
-        KV_REQUIRE(false, KV_ERR_BUDGET, "set %d: widths use %lld bits > %d", s, sum, 32 * rws[t] - 32);
+        KV_REQUIRE(false, KV_ERR_BUDGET, "set %d tensor %d: widths do not fit the %d-word record's pair layout", s,
+                   t, rws[t]);
       }
     }
   }
@@ -425,18 +486,11 @@ static float bf16_to_f32(uint16_t h) {
   return f;
 }
 
-// Unpack descriptor of channels 4q..4q+3 (storage order): the decode kernel extracts the four codes with
-// one funnel shift of record words (1+wq, 2+wq) by sh, then builds two fp16 pairs:
-//   pair01 = (x & m0) | ((x << s1) & m1hi),  pair23 = (y & m2) | ((y << s3) & m3hi),  y = x >> s2.
-static void quad_descriptor(const int32_t* w, const uint16_t* off, int q, uint4* out2) {
-  const int j = 4 * q;
-  const int b0 = w[j], b1 = w[j + 1], b2 = w[j + 2], b3 = w[j + 3];
-  const int o = (b0 + b1 + b2 + b3) ? off[j] : 0;
-  const uint32_t wq = (uint32_t)(o / 32), sh = (uint32_t)(o % 32);
-  const uint32_t s1 = 16 - b0, s2 = b0 + b1, s3 = 16 - b2;
-  auto m = [](int b) { return b ? ((1u << b) - 1u) : 0u; };
-  out2[0] = make_uint4(wq | (sh << 8) | (s1 << 16) | (s2 << 24), m(b0), m(b1) << 16, s3);
-  out2[1] = make_uint4(m(b2), m(b3) << 16, 0u, 0u);
+// Slot descriptor of pair k: code word u (0-based within the code words), bit r, widths of its two channels:
+//   u | r << 8 | b_2k << 16 | b_2k+1 << 24   (all zero for an empty slot).
+static uint32_t slot_descriptor(int u, int r, int b0, int b1) {
+  if (u < 0 || (b0 == 0 && b1 == 0)) return 0u;
+  return (uint32_t)u | ((uint32_t)r << 8) | ((uint32_t)b0 << 16) | ((uint32_t)b1 << 24);
 }
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -460,7 +514,7 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     blob.resize(off + bytes);
     return Piece{off, bytes};
   };
-  Piece pT[2], pTT[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], poff[2], pnz[2], pq[2];
+  Piece pT[2], pTT[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], pnz[2], psl[2];
   for (int t = 0; t < 2; ++t) {
     pT[t] = reserve((size_t)S * d * d * 4);
     pTT[t] = reserve((size_t)S * d * d * 4);
@@ -470,9 +524,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     pinv[t] = reserve((size_t)S * d * 4);
     pbase[t] = reserve((size_t)S * d * 4);
     pw[t] = reserve((size_t)S * d);
-    poff[t] = reserve((size_t)S * d * 2);
     pnz[t] = reserve((size_t)S * 4);
-    pq[t] = reserve((size_t)S * 32 * 2 * sizeof(uint4));
+    psl[t] = reserve((size_t)S * (d / 2) * 4);
   }
   for (int t = 0; t < 2; ++t) {
     float* T = (float*)&blob[pT[t].off];
@@ -483,9 +536,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     float* inv = (float*)&blob[pinv[t].off];
     float* base = (float*)&blob[pbase[t].off];
     uint8_t* w8 = (uint8_t*)&blob[pw[t].off];
-    uint16_t* of = (uint16_t*)&blob[poff[t].off];
     int32_t* nz = (int32_t*)&blob[pnz[t].off];
-    uint4* qd = (uint4*)&blob[pq[t].off];
+    uint32_t* sl = (uint32_t*)&blob[psl[t].off];
     for (int s = 0; s < S; ++s) {
       const float* Tsrc = &p->T[t][(size_t)s * d * d];
       for (int j = 0; j < d; ++j)
@@ -502,9 +554,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
           Ts[((size_t)s * 3 + 1) * d * d + (size_t)j * d + k] = mid;
           Ts[((size_t)s * 3 + 2) * d * d + (size_t)j * d + k] = lo;
         }
-      int n_nz = 0, bitpos = 0;
+      int n_nz = 0;
       std::vector<int32_t> wv(d);
-      std::vector<uint16_t> ov(d);
       for (int j = 0; j < d; ++j) {
         const size_t i = (size_t)s * d + j;
         mu[i] = p->mu[t][i];
@@ -513,9 +564,6 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
         inv[i] = w > 0 ? (float)(1.0 / (double)p->sigma[t][i]) : 0.f;
         w8[i] = (uint8_t)w;
         wv[j] = w;
-        of[i] = (uint16_t)bitpos;
-        ov[j] = (uint16_t)bitpos;
-        bitpos += w;
         if (w > 0) n_nz = j + 1;
       }
       nz[s] = n_nz;
@@ -524,7 +572,10 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
         for (int j = 0; j < d; ++j) acc += (double)Tsrc[(size_t)j * d + k] * (double)p->mu[t][(size_t)s * d + j];
         base[(size_t)s * d + k] = (float)acc;
       }
-      for (int q = 0; q < 32; ++q) quad_descriptor(wv.data(), ov.data(), q, &qd[((size_t)s * 32 + q) * 2]);
+      int word[D / 2], pos[D / 2];
+      kvtc::slot_layout(wv.data(), d, p->r_words[t], word, pos);
+      for (int k = 0; k < d / 2; ++k)
+        sl[(size_t)s * (d / 2) + k] = slot_descriptor(word[k], pos[k], wv[2 * k], wv[2 * k + 1]);
     }
   }
   void* dblob = nullptr;
@@ -550,9 +601,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     td.inv_sigma = (const float*)(b + pinv[t].off);
     td.base = (const float*)(b + pbase[t].off);
     td.widths = (const uint8_t*)(b + pw[t].off);
-    td.offs = (const uint16_t*)(b + poff[t].off);
     td.nz = (const int32_t*)(b + pnz[t].off);
-    td.quads = (const uint4*)(b + pq[t].off);
+    td.slots = (const uint32_t*)(b + psl[t].off);
     td.r_words = p->r_words[t];
   }
   p->dev.n_sets = S;

@@ -30,9 +30,8 @@ struct TensorDev {
   const float* inv_sigma;          // [S][D]  fp32(1/sigma) computed in double; 0 for zero-width
   const float* base;               // [S][D]  T^T mu (original-basis vector of the all-mean record)
   const uint8_t* widths;           // [S][D]
-  const uint16_t* offs;            // [S][D]  bit offset of each channel's code in the code area
-  const int32_t* nz;               // [S]     number of channels with width > 0 (a prefix)
-  const uint4* quads;              // [S][32][2] unpack descriptors of channel quads (see kernels)
+  const int32_t* nz;               // [S]     1 + last storage channel with width > 0
+  const uint32_t* slots;           // [S][D/2] pair slots: code word | bit << 8 | b_2k << 16 | b_2k+1 << 24
   int r_words;                     // record words per token (same for every set)
 };
 
@@ -40,6 +39,10 @@ struct ParamsDev {
   TensorDev t[2];
   int n_sets;
 };
+
+// First-fit placement of the pair slots of widths w[d] in a record of rw words (word/pos [d/2], -1 = empty);
+// false when a slot finds no room.
+bool slot_layout(const int32_t* w, int d, int rw, int* word, int* pos);
 
 // host-side error message of the calling thread
 void set_error(const char* fmt, ...);
