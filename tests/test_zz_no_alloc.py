@@ -62,7 +62,7 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     w, L, P, rk, rv, _ = _case("llama_long_128k", 64, 1, 1.33, [64])
-    B, Hkv, T_cap = 64, w.Hkv, 64
+    B, Hkv, T_cap = 256, w.Hkv, 64
     assert kvtc.kv_decode_workspace_bytes(P, B, Hkv, w.Hq, T_cap) > kvtc.NOALLOC_SCRATCH_BYTES
     tk = torch.zeros((B, Hkv, T_cap, P.record_words(0)), dtype=torch.int32, device="cuda")
     tv = torch.zeros((B, Hkv, T_cap, P.record_words(1)), dtype=torch.int32, device="cuda")

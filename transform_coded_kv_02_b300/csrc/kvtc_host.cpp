@@ -748,7 +748,7 @@ static int current_device() {
 
 extern "C" size_t kv_decode_workspace_bytes(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap) {
   if (!p || B < 1 || Hkv < 1 || Hq < Hkv || T_cap < 1) return 0;
-  return kvtc::decode_layout(B, Hkv, T_cap, current_device()).total;
+  return kvtc::decode_layout(B, Hkv, Hq, T_cap, current_device()).total;
 }
 
 extern "C" size_t kv_decode_bf16_workspace_bytes(int B, int Hkv, int Hq, int64_t T_cap) {
@@ -826,7 +826,7 @@ extern "C" kv_status kv_attend_decode(const kv_params* p, const kv_cache* c, con
   kv_status st;
   if ((st = kvtc::check_decode_args(p, c, q, B, Hq, seq_lens_dev, softmax_scale, out)) != KV_OK) return st;
   KV_REQUIRE(workspace && aligned16(workspace), KV_ERR_INVALID_ARG, "workspace null or not 16-byte aligned");
-  const DecodeLayout L = kvtc::decode_layout(B, c->Hkv, c->T_cap, current_device());
+  const DecodeLayout L = kvtc::decode_layout(B, c->Hkv, Hq, c->T_cap, current_device());
   KV_REQUIRE(ws_bytes >= L.total, KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
   return kvtc::launch_decode(p->dev, *c, q, B, Hq, seq_lens_dev, softmax_scale, out, workspace, L,
                              (cudaStream_t)stream);

@@ -56,7 +56,7 @@ struct DecodeLayout {
   int chunk;                  // tokens per split, multiple of the decode tile
   size_t off_qa, off_qc, off_cnt, off_part, total;
 };
-DecodeLayout decode_layout(int B, int Hkv, int64_t T_cap, int device);
+DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device);
 DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device);
 kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
                         const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,

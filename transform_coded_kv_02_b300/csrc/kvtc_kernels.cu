@@ -156,24 +156,30 @@ kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, co
 // ======================================================================================================
 // decode over packed records
 // ======================================================================================================
-constexpr int DT = 64;         // tokens per pipeline stage
-constexpr int DSTAGES = 4;     // stages in flight per CTA
-constexpr int DTHREADS = 128;  // 4 warps, 16 tokens each per stage
-constexpr int PSTR = 132;      // floats per (split, head) partial: M, L, Z, -, A[128]
+constexpr int PSTR = 132;          // floats per (split, head) partial: m, l, z, -, A[128]
+constexpr int DWARPS = 4;          // consumer warps per decode CTA
+constexpr int DT = 16 * DWARPS;    // tokens per ring stage (16 per consumer warp)
+constexpr int DTHREADS = 32 * (DWARPS + 1);
+constexpr int RING_BUDGET = 48 * 1024;
+constexpr int MAX_STAGES = 8;
+constexpr int MAX_SPLITS = 256;
+constexpr int TAIL_RESERVE = MAX_G * D * 4 + MAX_SPLITS * MAX_G * 4 + 2 * MAX_G * 4;  // delta, e, L/Z
+constexpr int TAIL_MIN = 64 * 1024 + MAX_G * PSTR * 4;   // T_V rows, or one split's partials
+constexpr int UNPACK_T = 64;       // tokens per tile of the parity unpacker
 constexpr int KC_PITCH_MAX = 272;  // bytes per token row of an unpacked tile (odd multiple of 16)
 
 struct DecArgs {
   const uint32_t* rec[2];
   const __nv_bfloat16* q;
   const int32_t* seq_lens;
-  __half* qa;       // [B*Hkv][16][128]
-  float* qc;        // [B*Hkv][16]: C0 of heads 0..7, C1 of heads 0..7
-  unsigned* cnt;    // [B*Hkv]
-  float* part;      // [B*Hkv][splits][8][PSTR]
+  __half* qa;       // [B*Hkv][16][128]: row 2h (+1) = fp16 hi (lo) part of q' of head h
+  float* qc;        // [B*Hkv][16]: C0 of heads 0..7, C1 of heads 0..7 (base-2 logit units)
+  unsigned* cnt;    // [B*Hkv] arrival counters
+  float* part;      // [B*Hkv][splits][g][PSTR] split partials
   float* out;       // [B][Hq][128]
   long long T_cap;
   long long wait_ns;
-  int B, Hkv, Hq, g, per_seq, splits, chunk;
+  int B, Hkv, Hq, g, per_seq, splits, chunk, stages;
   float scale_log2;
 };
 
@@ -183,342 +189,436 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__global__ void __launch_bounds__(256) qprep_kernel(ParamsDev P, DecArgs a) {
+// ---- q preparation: one CTA per (sequence, KV head) ---------------------------------------------------
+// q~ = T_K q for the g query heads (T_K rows staged in shared memory by one bulk copy);
+// q'_j = a log2(e) q~_j sigma_j 2^-b_j as fp16 hi + lo; C0 = a log2(e) q.(T_K^T mu); C1 = a log2(e) sum q~_j sigma_j.
+constexpr int QP_THREADS = 256;
+static size_t qprep_smem_bytes() { return (size_t)D * D * 4 + (size_t)MAX_G * D * 4; }
+
+__global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs a) {
   pdl_launch_dependents();
-  __shared__ float qs[MAX_G][D];
-  __shared__ float qt[MAX_G][D];
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* Ts = reinterpret_cast<float*>(smem);    // [nz][128]
+  float* qs = Ts + D * D;                        // [g][128]
+  __shared__ uint64_t bar;
+  __shared__ float red[4][MAX_G];
   const int kh = blockIdx.x, b = blockIdx.y;
   const int bh = b * a.Hkv + kh;
   const int set = a.per_seq ? bh : kh;
-  const int g = a.g, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const TensorDev& tk = P.t[0];
-  for (int i = tid; i < g * D; i += 256) {
-    const int h = i >> 7, k = i & (D - 1);
-    qs[h][k] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k]);
+  const int nz = tk.nz[set], g = a.g, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
   }
   __syncthreads();
-  const int nz = tk.nz[set];
-  const float* T = tk.T + (size_t)set * D * D;
-  for (int j = warp; j < nz; j += 8) {
-    const float4 t4 = __ldg(reinterpret_cast<const float4*>(T + (size_t)j * D) + lane);
-    for (int h = 0; h < g; ++h) {
-      const float4 q4 = *reinterpret_cast<const float4*>(&qs[h][4 * lane]);
-      float sacc = t4.x * q4.x + t4.y * q4.y + t4.z * q4.z + t4.w * q4.w;
-      sacc = warp_sum(sacc);
-      if (lane == 0) qt[h][j] = sacc;
+  if (tid == 0 && nz > 0) {
+    mbar_expect_tx(smem_u32(&bar), (uint32_t)nz * D * 4);
+    bulk_g2s(smem_u32(Ts), tk.T + (size_t)set * D * D, (uint32_t)nz * D * 4, smem_u32(&bar));
+  }
+  const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kh * g) * D;
+  for (int i = tid; i < g * D; i += QP_THREADS) qs[i] = __bfloat162float(qg[i]);
+  bool ok = true;
+  if (nz > 0) ok = mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);
+  if (!ok && tid == 0) mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);  // drain before leaving
+  __syncthreads();
+  if (__syncthreads_or(!ok)) return;
+
+  float qt[MAX_G];
+#pragma unroll
+  for (int h = 0; h < MAX_G; ++h) qt[h] = 0.f;
+  const int j = tid;
+  if (j < D && j < nz) {
+    const float4* Trow = reinterpret_cast<const float4*>(Ts + (size_t)j * D);
+#pragma unroll 4
+    for (int k4 = 0; k4 < D / 4; ++k4) {
+      const int kk = (k4 + j) & (D / 4 - 1);   // rotated start: conflict-free row reads
+      const float4 t = Trow[kk];
+#pragma unroll
+      for (int h = 0; h < MAX_G; ++h) {
+        if (h < g) {
+          const float4 qv = reinterpret_cast<const float4*>(qs + h * D)[kk];
+          qt[h] = fmaf(t.x, qv.x, fmaf(t.y, qv.y, fmaf(t.z, qv.z, fmaf(t.w, qv.w, qt[h]))));
+        }
+      }
     }
   }
-  __syncthreads();
-  const float* sig = tk.sigma + (size_t)set * D;
-  const uint8_t* wd = tk.widths + (size_t)set * D;
-  __half* qa = a.qa + (size_t)bh * 16 * D;
-  for (int i = tid; i < 16 * D; i += 256) {
-    const int r = i >> 7, j = i & (D - 1), h = r >> 1, hl = r & 1;
-    __half v = __float2half_rn(0.f);
-    if (h < g && j < nz) {
-      const float qp = a.scale_log2 * qt[h][j] * sig[j] * exp2i(-(int)wd[j]);
+  float c1[MAX_G];
+  if (j < D) {
+    const float sg = tk.sigma[(size_t)set * D + j];
+    const int bw = tk.widths[(size_t)set * D + j];
+    __half* qa = a.qa + (size_t)bh * 16 * D;
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) {
+      const bool on = h < g && bw > 0;
+      const float qp = on ? a.scale_log2 * qt[h] * sg * exp2i(-bw) : 0.f;
       const __half hi = __float2half_rn(qp);
-      v = hl ? __float2half_rn(qp - __half2float(hi)) : hi;
+      const __half lo = __float2half_rn(qp - __half2float(hi));
+      qa[(2 * h) * D + j] = hi;
+      qa[(2 * h + 1) * D + j] = lo;
+      c1[h] = on ? qt[h] * sg : 0.f;
     }
-    qa[i] = v;
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) {
+      const float s = warp_sum(c1[h]);
+      if (lane == 0) red[warp][h] = s;
+    }
   }
-  if (warp < g) {
+  __syncthreads();
+  if (warp < g) {  // C0 of head `warp`: q . (T_K^T mu) over the original basis
     const float* base = tk.base + (size_t)set * D;
-    float c0 = 0.f, c1 = 0.f;
-    for (int k = lane; k < D; k += 32) c0 += base[k] * qs[warp][k];
-    for (int j = lane; j < nz; j += 32) c1 += qt[warp][j] * sig[j];
+    float c0 = 0.f;
+    for (int k = lane; k < D; k += 32) c0 = fmaf(base[k], qs[warp * D + k], c0);
     c0 = warp_sum(c0);
-    c1 = warp_sum(c1);
     if (lane == 0) {
       a.qc[bh * 16 + warp] = a.scale_log2 * c0;
-      a.qc[bh * 16 + 8 + warp] = a.scale_log2 * c1;
+      a.qc[bh * 16 + 8 + warp] = a.scale_log2 * (red[0][warp] + red[1][warp] + red[2][warp] + red[3][warp]);
     }
   }
   if (tid == 0) a.cnt[bh] = 0u;
 }
 
+// ---- split-K decode ----------------------------------------------------------------------------------
 __host__ __device__ __forceinline__ int unpacked_pitch(int nblk16) {  // bytes, odd multiple of 16
   return ((nblk16 * 2) | 1) * 16;
 }
 
-static size_t decode_smem_bytes(int RK, int RV) {
-  const size_t stage = (size_t)DT * (RK + RV) * 4;
-  size_t off = DSTAGES * stage + 16;
-  off = (off + 127) / 128 * 128;
-  off += 4 * (size_t)DT * KC_PITCH_MAX;       // Kc[2], Vc[2]
-  off += 2 * 2 * (size_t)DT * sizeof(float2); // zsK[2], zsV[2]
-  off += DSTAGES * 8;                         // mbarriers
-  return off + 128;
+struct DecSmem {  // byte offsets into the dynamic shared memory of decode_kernel
+  uint32_t stage_bytes, tiles, warp_tile, ps, bars, tail_reserve, total;
+};
+
+__host__ __device__ __forceinline__ uint32_t align128u(uint32_t x) { return (x + 127u) & ~127u; }
+
+__host__ __device__ inline DecSmem decode_smem(int RK, int RV, int nkb, int nmb, int stages, int nb) {
+  DecSmem s;
+  s.stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
+  s.tiles = align128u(stages * s.stage_bytes);
+  s.warp_tile = 16u * (uint32_t)(unpacked_pitch(nkb) + unpacked_pitch(nmb));
+  s.ps = align128u(s.tiles + DWARPS * s.warp_tile);
+  s.bars = align128u(s.ps + DWARPS * 16u * 8u * nb * 2u);
+  uint32_t end = s.bars + (2u * MAX_STAGES + 1u) * 8u;
+  if (end < (uint32_t)TAIL_MIN) end = TAIL_MIN;
+  s.tail_reserve = align128u(end);
+  s.total = s.tail_reserve + TAIL_RESERVE;
+  return s;
 }
 
 template <int NB>
 __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_abort, s_last, s_issued;
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int bh = b * a.Hkv + kh;
   const int set = a.per_seq ? bh : kh;
   const TensorDev& TK = P.t[0];
   const TensorDev& TV = P.t[1];
-  const int RK = TK.r_words, RV = TV.r_words;
+  const int RK = TK.r_words, RV = TV.r_words, NS = a.stages, g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-  const int g = a.g;
-
   const int nzK = TK.nz[set], nzV = TV.nz[set];
   const int nkb = (nzK + 15) >> 4, nmb = (nzV + 15) >> 4;
   const int pitchK = unpacked_pitch(nkb), pitchV = unpacked_pitch(nmb);
+  const DecSmem L = decode_smem(RK, RV, nkb, nmb, NS, NB);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* tbar = empty + MAX_STAGES;
 
-  const size_t stage_bytes = (size_t)DT * (RK + RV) * 4;
-  uint8_t* stage0 = smem;
-  size_t off = DSTAGES * stage_bytes + 16;
-  off = (off + 127) / 128 * 128;
-  uint8_t* kc0 = smem + off;
-  uint8_t* vc0 = kc0 + 2 * DT * KC_PITCH_MAX;
-  float2* zsK = reinterpret_cast<float2*>(vc0 + 2 * DT * KC_PITCH_MAX);
-  float2* zsV = zsK + 2 * DT;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(zsV + 2 * DT);
-  __shared__ int s_last;
-
-  const long long L = min((long long)a.seq_lens[b], a.T_cap);
+  const long long Lseq = min((long long)a.seq_lens[b], a.T_cap);
   const long long t0 = (long long)split * a.chunk;
-  const long long t1 = min(t0 + (long long)a.chunk, L);
+  const long long t1 = min(t0 + (long long)a.chunk, Lseq);
   const int ntiles = t1 > t0 ? (int)((t1 - t0 + DT - 1) / DT) : 0;
-  const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
-  const uint32_t* vrec = a.rec[1] + (size_t)bh * a.T_cap * RV;
-
-  auto issue = [&](int i) {
-    const int s = i % DSTAGES;
-    const long long tb = t0 + (long long)i * DT;
-    long long n = min((long long)DT, t1 - tb);
-    n = min((n + 3) & ~3LL, a.T_cap - tb);
-    const uint32_t kb = (uint32_t)(n * RK * 4), vb = (uint32_t)(n * RV * 4);
-    const uint32_t bar = smem_u32(&bars[s]);
-    const uint32_t dst = smem_u32(stage0 + s * stage_bytes);
-    mbar_expect_tx(bar, kb + vb);
-    bulk_g2s(dst, krec + tb * RK, kb, bar);
-    bulk_g2s(dst + DT * RK * 4, vrec + tb * RV, vb, bar);
-  };
 
   if (tid == 0) {
-    for (int s = 0; s < DSTAGES; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), DWARPS);
+    }
+    mbar_init(smem_u32(tbar), 1);
     fence_mbar_init();
+    s_abort = 0;
+    s_issued = 0;
   }
   __syncthreads();
-  if (tid == 0)
-    for (int i = 0; i < min(DSTAGES, ntiles); ++i) issue(i);
 
-  const QuadMap mk = quad_map(nkb * 4, tid, DTHREADS);
-  const QuadMap mv = quad_map(nmb * 4, tid, DTHREADS);
-  QuadDesc dk = {}, dv = {};
-  if (mk.active) dk = load_quad(TK, set, mk.q);
-  if (mv.active) dv = load_quad(TV, set, mv.q);
-
-  // q' operand and folded constants come from qprep_kernel
-  pdl_wait();
-  uint32_t qa[8][4];
-  {
-    const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(a.qa + (size_t)bh * 16 * D);
-#pragma unroll
-    for (int kb = 0; kb < 8; ++kb) {
-      if (kb < nkb) {
-        qa[kb][0] = qa32[(gid * D + kb * 16 + 2 * tig) >> 1];
-        qa[kb][1] = qa32[((gid + 8) * D + kb * 16 + 2 * tig) >> 1];
-        qa[kb][2] = qa32[(gid * D + kb * 16 + 8 + 2 * tig) >> 1];
-        qa[kb][3] = qa32[((gid + 8) * D + kb * 16 + 8 + 2 * tig) >> 1];
-      } else {
-        qa[kb][0] = qa[kb][1] = qa[kb][2] = qa[kb][3] = 0u;
-      }
-    }
-  }
-  const int hA = gid >> 1, hB = 4 + (gid >> 1);
-  const float c0A = a.qc[bh * 16 + hA], c1A = a.qc[bh * 16 + 8 + hA];
-  const float c0B = NB == 2 ? a.qc[bh * 16 + hB] : 0.f, c1B = NB == 2 ? a.qc[bh * 16 + 8 + hB] : 0.f;
-
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, z_run[2] = {0.f, 0.f};
+  float m_run[NB], l_run[NB], z_run[NB];
   float acc_o[8][NB][4];
 #pragma unroll
-  for (int mb = 0; mb < 8; ++mb)
+  for (int nb = 0; nb < NB; ++nb) {
+    m_run[nb] = -INFINITY;
+    l_run[nb] = 0.f;
+    z_run[nb] = 0.f;
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb)
+    for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc_o[mb][nb][i] = 0.f;
+      for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] = 0.f;
+  }
 
-  const int lrow = (lane & 7) + ((lane >> 4) << 3);  // ldmatrix row within a 16-token group
-  const int lcol = ((lane >> 3) & 1) * 16;            // byte offset of the second 8-channel half
-  const int hl = gid & 1;
-  int consumed = 0;
-  bool aborted = false;
-  for (int i = 0; i < ntiles; ++i) {
-    const int s = i % DSTAGES;
-    const uint32_t par = (uint32_t)((i / DSTAGES) & 1);
-    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), par, a.wait_ns);
-    const int buf = i & 1;
-    const uint32_t* sk = reinterpret_cast<const uint32_t*>(stage0 + s * stage_bytes);
-    const uint32_t* sv = sk + DT * RK;
-    uint8_t* kc = kc0 + buf * DT * KC_PITCH_MAX;
-    uint8_t* vc = vc0 + buf * DT * KC_PITCH_MAX;
-    if (mk.active)
-      for (int t = mk.r0; t < DT; t += mk.rstep)
-        *reinterpret_cast<uint2*>(kc + t * pitchK + 8 * mk.q) = unpack_quad(sk + t * RK, dk);
-    if (mv.active)
-      for (int t = mv.r0; t < DT; t += mv.rstep)
-        *reinterpret_cast<uint2*>(vc + t * pitchV + 8 * mv.q) = unpack_quad(sv + t * RV, dv);
-    if (tid < DT) {
-      const uint32_t w = sk[tid * RK];
-      zsK[buf * DT + tid] = make_float2(half_bits_to_float(w), half_bits_to_float(w >> 16));
-    } else {
-      const uint32_t w = sv[(tid - DT) * RV];
-      zsV[buf * DT + tid - DT] = make_float2(half_bits_to_float(w), half_bits_to_float(w >> 16));
+  if (warp == DWARPS) {
+    // ================= producer: one elected lane streams record tiles into the ring =================
+    if (lane == 0) {
+      if (split == 0 && nzV > 0)  // the last CTA's inverse rotation reads T_V rows: warm L2 now
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(TV.T + (size_t)set * D * D),
+                     "r"((uint32_t)nzV * D * 4)
+                     : "memory");
+      const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
+      const uint32_t* vrec = a.rec[1] + (size_t)bh * a.T_cap * RV;
+      int i = 0;
+      for (; i < ntiles; ++i) {
+        const int s = i % NS;
+        if (i >= NS && !mbar_wait_bounded(smem_u32(&empty[s]), (uint32_t)((i / NS - 1) & 1), a.wait_ns)) {
+          s_abort = 1;
+          break;
+        }
+        if (*(volatile int*)&s_abort) break;
+        const long long tb = t0 + (long long)i * DT;
+        long long n = min((long long)DT, t1 - tb);
+        n = min((n + 3) & ~3LL, a.T_cap - tb);
+        const uint32_t kb = (uint32_t)(n * RK * 4), vb = (uint32_t)(n * RV * 4);
+        const uint32_t bar = smem_u32(&full[s]);
+        const uint32_t dst = smem_u32(smem + (size_t)s * L.stage_bytes);
+        mbar_expect_tx(bar, kb + vb);
+        bulk_g2s(dst, krec + tb * RK, kb, bar);
+        bulk_g2s(dst + DT * RK * 4, vrec + tb * RV, vb, bar);
+      }
+      s_issued = i;
     }
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      consumed = i;
-      break;
+  } else {
+    // ================= consumers: warp w owns tokens [16w, 16w + 16) of every tile =================
+    // unpack task of this lane: group gi (4 slot pairs = 8 channels) of token sub + TPP * p
+    const int GK = 2 * nkb, G = 2 * (nkb + nmb);
+    const int GP = G <= 4 ? 4 : G <= 8 ? 8 : G <= 16 ? 16 : 32;
+    const int TPP = 32 / GP, passes = 16 / TPP;
+    const int gi = lane & (GP - 1), sub = lane / GP;
+    const bool active = gi < G;
+    const bool isV = gi >= GK;
+    const int grp = isV ? gi - GK : gi;
+    uint32_t wo[4] = {0u, 0u, 0u, 0u}, sh[4] = {0u, 0u, 0u, 0u}, mk[4] = {0u, 0u, 0u, 0u};
+    if (active) {
+      const uint32_t* sl = (isV ? TV.slots : TK.slots) + (size_t)set * (D / 2) + 4 * grp;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t desc = __ldg(sl + i);
+        wo[i] = 4u * (1u + (desc & 255u));
+        sh[i] = (desc >> 8) & 255u;
+        mk[i] = slot_mask(desc);
+      }
     }
-    consumed = i + 1;
-    if (tid == 0 && i + DSTAGES < ntiles) {
-      fence_proxy_async_smem();
-      issue(i + DSTAGES);
-    }
-    const long long tile_t0 = t0 + (long long)i * DT;
-    const int lt = warp * 16;
-    if (tile_t0 + lt >= t1) continue;  // this warp's 16 tokens are past the end
+    const uint32_t src_off = isV ? (uint32_t)DT * RK * 4 : 0u;
+    const uint32_t R4 = (uint32_t)(isV ? RV : RK) * 4u;
+    const int upitch = isV ? pitchV : pitchK;
+    uint8_t* wtile = smem + L.tiles + (size_t)warp * L.warp_tile;
+    uint8_t* udst = wtile + (isV ? 16 * pitchK : 0) + grp * 16 + sub * upitch;
+    __half* ps = reinterpret_cast<__half*>(smem + L.ps) + (size_t)warp * 16 * 8 * NB;
 
-    // ---- logits: rows 2h / 2h+1 = q' hi / lo of head h, columns = 16 tokens ----
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    const uint32_t ka = smem_u32(kc + (lt + lrow) * pitchK + lcol);
+    // q' (B operand of the logits MMA) and the folded constants come from qprep_kernel
+    pdl_wait();
+    uint32_t qb[8][NB][2];
+    {
+      const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(a.qa + (size_t)bh * 16 * D);
 #pragma unroll
-    for (int kb = 0; kb < 8; ++kb) {
-      if (kb < nkb) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(ka + kb * 32, r0, r1, r2, r3);
-        mma_f16(acc[0], qa[kb], r0, r1);
-        mma_f16(acc[1], qa[kb], r2, r3);
-      }
+      for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const int col = nb * 8 + gid;
+          qb[kb][nb][0] = kb < nkb ? qa32[(col * D + kb * 16 + 2 * tig) >> 1] : 0u;
+          qb[kb][nb][1] = kb < nkb ? qa32[(col * D + kb * 16 + 8 + 2 * tig) >> 1] : 0u;
+        }
     }
+    float c0[NB], c1[NB];
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nb][e] += __shfl_xor_sync(0xffffffffu, acc[nb][e], 4);
+    for (int nb = 0; nb < NB; ++nb) {
+      const int h = tig + 4 * nb;
+      c0[nb] = h < g ? a.qc[bh * 16 + h] : 0.f;
+      c1[nb] = h < g ? a.qc[bh * 16 + 8 + h] : 0.f;
+    }
+    const uint32_t ka = smem_u32(wtile + (lane & 15) * pitchK + (lane >> 4) * 16);
+    const uint32_t va = smem_u32(wtile + 16 * pitchK + ((lane & 7) + ((lane >> 4) << 3)) * pitchV +
+                                 ((lane >> 3) & 1) * 16);
+    const uint32_t pa = smem_u32(ps + (lane & 15) * 8 * NB);
 
-    const int tl[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
-    bool valid[4];
-    float2 zk[4], zv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      valid[e] = tile_t0 + lt + tl[e] < t1;
-      zk[e] = zsK[buf * DT + lt + tl[e]];
-      zv[e] = zsV[buf * DT + lt + tl[e]];
-    }
-    uint32_t bp[NB][2];
-    float corr[2];
-#pragma unroll
-    for (int hb = 0; hb < NB; ++hb) {
-      const float c0 = hb ? c0B : c0A, c1 = hb ? c1B : c1A;
-      float lg[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float raw = acc[e >> 1][(e & 1) + 2 * hb];
-        lg[e] = valid[e] ? c0 + zk[e].x * c1 + zk[e].y * raw : -INFINITY;
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % NS;
+      // every lane takes the stage's data through its own wait; the verdict is made warp-uniform
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
       }
-      float mt = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-      const float m_new = fmaxf(m_run[hb], mt);
-      const float cr = (m_run[hb] == m_new) ? 1.f : exp2f(m_run[hb] - m_new);
-      float p[4], psum = 0.f, zsum = 0.f;
-      __half pv[4];
+      const uint8_t* st = smem + (size_t)s * L.stage_bytes;
+      const long long my_t0 = t0 + (long long)i * DT + 16 * warp;
+      const bool live = my_t0 < t1;
+      uint32_t kzs[2] = {0u, 0u}, vzs[2] = {0u, 0u};
+      if (live) {
+        kzs[0] = *reinterpret_cast<const uint32_t*>(st + (16 * warp + gid) * RK * 4);
+        kzs[1] = *reinterpret_cast<const uint32_t*>(st + (16 * warp + gid + 8) * RK * 4);
+        vzs[0] = *reinterpret_cast<const uint32_t*>(st + DT * RK * 4 + (16 * warp + gid) * RV * 4);
+        vzs[1] = *reinterpret_cast<const uint32_t*>(st + DT * RK * 4 + (16 * warp + gid + 8) * RV * 4);
+        if (active) {
+          // four passes per batch: all 16 words are loaded before any unpacked tile row is stored, so the
+          // loads of a batch are in flight together
+          const uint8_t* row = st + src_off + (16 * warp + sub) * R4;
+          uint8_t* drow = udst;
+          for (int p = 0; p < passes; p += 4) {
+            uint32_t x[4][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        p[e] = valid[e] ? exp2f(lg[e] - m_new) : 0.f;
-        psum += p[e];
-        zsum += valid[e] ? p[e] * zv[e].x : 0.f;
-        const float w = valid[e] ? p[e] * zv[e].y : 0.f;
-        const __half whi = __float2half_rn(w);
-        pv[e] = hl ? __float2half_rn(w - __half2float(whi)) : whi;
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                x[u][i] = (p + u < passes) ? *reinterpret_cast<const uint32_t*>(row + u * TPP * R4 + wo[i]) : 0u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (p + u < passes) {
+                uint4 v;
+                v.x = unpack_pair(x[u][0], sh[0], mk[0]);
+                v.y = unpack_pair(x[u][1], sh[1], mk[1]);
+                v.z = unpack_pair(x[u][2], sh[2], mk[2]);
+                v.w = unpack_pair(x[u][3], sh[3], mk[3]);
+                *reinterpret_cast<uint4*>(drow + u * TPP * upitch) = v;
+              }
+            }
+            row += 4 * TPP * R4;
+            drow += 4 * TPP * upitch;
+          }
+        }
       }
-      l_run[hb] = l_run[hb] * cr + psum;
-      z_run[hb] = z_run[hb] * cr + zsum;
-      m_run[hb] = m_new;
-      corr[hb] = cr;
-      bp[hb][0] = pack_half2(pv[0], pv[1]);
-      bp[hb][1] = pack_half2(pv[2], pv[3]);
-    }
-    // rescale the value accumulators: columns 2tig / 2tig+1 belong to head tig (+4 for the second block)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // this warp is done with the stage
+      if (!live) continue;
+
+      // ---- logits: A = codes (16 tokens x 16 channels), B = q' (16 channels x 8 columns) ----
+      // two accumulators (even / odd channel blocks) halve the dependent MMA chain
+      float acc2[2][NB][4];
 #pragma unroll
-    for (int hb = 0; hb < NB; ++hb) {
-      const float c = __shfl_sync(0xffffffffu, corr[hb], 8 * tig);
-      if (__any_sync(0xffffffffu, c != 1.f)) {
+      for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int mb = 0; mb < 8; ++mb)
+        for (int nb = 0; nb < NB; ++nb) acc2[u][nb][0] = acc2[u][nb][1] = acc2[u][nb][2] = acc2[u][nb][3] = 0.f;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc_o[mb][hb][e] *= c;
+      for (int kb = 0; kb < 8; ++kb) {
+        if (kb < nkb) {
+          uint32_t af[4];
+          ldsm_x4(ka + kb * 32, af[0], af[1], af[2], af[3]);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(acc2[kb & 1][nb], af, qb[kb][nb][0], qb[kb][nb][1]);
+        }
       }
+      float acc[NB][4];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nb][e] = acc2[0][nb][e] + acc2[1][nb][e];
+      const bool valid0 = my_t0 + gid < t1, valid1 = my_t0 + gid + 8 < t1;
+      const float zk0 = half_bits_to_float(kzs[0]), sk0 = half_bits_to_float(kzs[0] >> 16);
+      const float zk1 = half_bits_to_float(kzs[1]), sk1 = half_bits_to_float(kzs[1] >> 16);
+      const float zv0 = half_bits_to_float(vzs[0]), sv0 = half_bits_to_float(vzs[0] >> 16);
+      const float zv1 = half_bits_to_float(vzs[1]), sv1 = half_bits_to_float(vzs[1] >> 16);
+      float corr[NB];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const float l0 = valid0 ? fmaf(sk0, acc[nb][0] + acc[nb][1], fmaf(zk0, c1[nb], c0[nb])) : -INFINITY;
+        const float l1 = valid1 ? fmaf(sk1, acc[nb][2] + acc[nb][3], fmaf(zk1, c1[nb], c0[nb])) : -INFINITY;
+        float mt = fmaxf(l0, l1);
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        const float m_new = fmaxf(m_run[nb], mt);
+        corr[nb] = (m_run[nb] == m_new) ? 1.f : exp2f(m_run[nb] - m_new);
+        const float p0 = valid0 ? exp2f(l0 - m_new) : 0.f;
+        const float p1 = valid1 ? exp2f(l1 - m_new) : 0.f;
+        l_run[nb] = fmaf(l_run[nb], corr[nb], p0 + p1);
+        z_run[nb] = fmaf(z_run[nb], corr[nb], (valid0 ? p0 * zv0 : 0.f) + (valid1 ? p1 * zv1 : 0.f));
+        m_run[nb] = m_new;
+        const float w0 = valid0 ? p0 * sv0 : 0.f, w1 = valid1 ? p1 * sv1 : 0.f;
+        const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
+        const uint32_t e0 = pack_half2(h0, __float2half_rn(w0 - __half2float(h0)));
+        const uint32_t e1 = pack_half2(h1, __float2half_rn(w1 - __half2float(h1)));
+        reinterpret_cast<uint32_t*>(ps)[(gid * 8 * NB + nb * 8 + 2 * tig) >> 1] = e0;
+        reinterpret_cast<uint32_t*>(ps)[((gid + 8) * 8 * NB + nb * 8 + 2 * tig) >> 1] = e1;
+      }
+      __syncwarp();
+      uint32_t bp[NB][2];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) ldsm_x2_t(pa + nb * 16, bp[nb][0], bp[nb][1]);
+      // accumulator columns 2tig, 2tig+1 are head tig (+4 nb): rescale with this lane's own factor
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        if (__any_sync(0xffffffffu, corr[nb] != 1.f)) {
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] *= corr[nb];
+        }
+      }
+      // ---- P.V in the rotated basis: A = V^T (16 channels x 16 tokens), B = P (16 tokens x 8 columns) ----
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        if (mb < nmb) {
+          uint32_t af[4];
+          ldsm_x4_t(va + mb * 32, af[0], af[1], af[2], af[3]);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(acc_o[mb][nb], af, bp[nb][0], bp[nb][1]);
+        }
+      }
+      __syncwarp();  // the P tile and this warp's unpacked tiles are rewritten next iteration
     }
-    // ---- P.V in the rotated basis: rows = channels, k = 16 tokens, columns = head hi/lo ----
-    const uint32_t va = smem_u32(vc + (lt + lrow) * pitchV + lcol);
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb) {
-      if (mb < nmb) {
-        uint32_t af[4];
-        ldsm_x4_t(va + mb * 32, af[0], af[1], af[2], af[3]);
+    for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
-        for (int hb = 0; hb < NB; ++hb) mma_f16(acc_o[mb][hb], af, bp[hb][0], bp[hb][1]);
+      for (int o = 4; o < 32; o <<= 1) {
+        l_run[nb] += __shfl_xor_sync(0xffffffffu, l_run[nb], o);
+        z_run[nb] += __shfl_xor_sync(0xffffffffu, z_run[nb], o);
       }
     }
   }
 
-  if (aborted) {  // drain copies still in flight into this CTA's shared memory, then leave
-    if (tid == 0)
-      for (int i = consumed; i < min(consumed + DSTAGES, ntiles); ++i)
-        mbar_wait_bounded(smem_u32(&bars[i % DSTAGES]), (uint32_t)((i / DSTAGES) & 1), a.wait_ns);
+  __syncthreads();
+  if (s_abort) {  // drain the copies this CTA may still have in flight, then leave
+    if (tid == 0) {
+      const int issued = s_issued;
+      for (int i = max(0, issued - NS); i < issued; ++i)
+        mbar_wait_bounded(smem_u32(&full[i % NS]), (uint32_t)((i / NS) & 1), a.wait_ns);
+    }
     __syncthreads();
     return;
   }
 
-  // ---- merge the 4 warps of this CTA ----
-  __syncthreads();
-  float* ws = reinterpret_cast<float*>(kc0);  // [4][8][PSTR]
+  // ---- merge the consumer warps of this CTA (ring memory is free now) ----
+  float* ws = reinterpret_cast<float*>(smem);  // [DWARPS][8][PSTR]
+  if (warp < DWARPS) {
 #pragma unroll
-  for (int hb = 0; hb < NB; ++hb) {
-    float l = l_run[hb], z = z_run[hb];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    z += __shfl_xor_sync(0xffffffffu, z, 1);
-    z += __shfl_xor_sync(0xffffffffu, z, 2);
-    const int h = (gid >> 1) + 4 * hb;
-    if (tig == 0 && hl == 0 && h < g) {
-      float* w = ws + (warp * 8 + h) * PSTR;
-      w[0] = m_run[hb];
-      w[1] = l;
-      w[2] = z;
-    }
+    for (int nb = 0; nb < NB; ++nb) {
+      const int h = tig + 4 * nb;
+      if (h < g) {
+        float* w = ws + (warp * 8 + h) * PSTR;
+        if (gid == 0) {
+          w[0] = m_run[nb];
+          w[1] = l_run[nb];
+          w[2] = z_run[nb];
+        }
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb) {
-      const int hcol = tig + 4 * hb;
-      if (mb < nmb && hcol < g) {
-        float* w = ws + (warp * 8 + hcol) * PSTR + 4 + mb * 16;
-        w[gid] = acc_o[mb][hb][0] + acc_o[mb][hb][1];
-        w[gid + 8] = acc_o[mb][hb][2] + acc_o[mb][hb][3];
+        for (int mb = 0; mb < 8; ++mb) {
+          if (mb < nmb) {
+            w[4 + mb * 16 + gid] = acc_o[mb][nb][0] + acc_o[mb][nb][1];
+            w[4 + mb * 16 + gid + 8] = acc_o[mb][nb][2] + acc_o[mb][nb][3];
+          }
+        }
       }
     }
   }
   __syncthreads();
-  float* part = a.part + ((size_t)bh * a.splits + split) * 8 * PSTR;
-  const int acols = nmb * 16;
+  float* part = a.part + ((size_t)bh * a.splits + split) * g * PSTR;
+  const int acols = 4 + nmb * 16;
   for (int idx = tid; idx < g * PSTR; idx += DTHREADS) {
     const int h = idx / PSTR, cidx = idx - h * PSTR;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
+    for (int w = 0; w < DWARPS; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
     float val = 0.f;
     if (cidx == 0) {
       val = M;
-    } else if (cidx == 1 || cidx == 2 || (cidx >= 4 && cidx - 4 < acols)) {
+    } else if (cidx != 3 && cidx < acols) {
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
+      for (int w = 0; w < DWARPS; ++w) {
         const float mw = ws[(w * 8 + h) * PSTR];
         const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        val += e * ws[(w * 8 + h) * PSTR + cidx];
+        val = fmaf(e, ws[(w * 8 + h) * PSTR + cidx], val);
       }
     }
     part[idx] = val;
@@ -530,46 +630,111 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   if (!s_last) return;
   __threadfence();
 
-  // ---- last CTA of (b, kh): merge splits, reconstruct o^ - mu, inverse-rotate ----
-  float* delta = reinterpret_cast<float*>(kc0);  // [8][128]
-  __shared__ float s_have[MAX_G];
-  const float* pb = a.part + (size_t)bh * a.splits * 8 * PSTR;
-  const float* sigV = TV.sigma + (size_t)set * D;
-  const uint8_t* wV = TV.widths + (size_t)set * D;
-  const int j = tid;
-  for (int h = 0; h < g; ++h) {
+  // ======== last CTA of (b, kh): merge the splits, reconstruct o^ - mu, inverse-rotate once ========
+  float* delta = reinterpret_cast<float*>(smem + L.tail_reserve);   // [8][128]
+  float* esc = delta + MAX_G * D;                                   // [splits][g]
+  float* LZ = esc + MAX_SPLITS * MAX_G;                             // [2][8]
+  const float* pb = a.part + (size_t)bh * a.splits * g * PSTR;
+  const int S = a.splits;
+  // per-head maximum, split weights, L and Z (one warp per head)
+  for (int h = warp; h < g; h += DWARPS + 1) {
     float M = -INFINITY;
-    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, __ldcg(pb + ((size_t)sp * 8 + h) * PSTR));
-    float Ls = 0.f, Zs = 0.f, As = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float* pp = pb + ((size_t)sp * 8 + h) * PSTR;
+    for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, __ldcg(pb + ((size_t)sp * g + h) * PSTR));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Ls = 0.f, Zs = 0.f;
+    for (int sp = lane; sp < S; sp += 32) {
+      const float* pp = pb + ((size_t)sp * g + h) * PSTR;
       const float ms = __ldcg(pp);
       const float e = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      Ls += e * __ldcg(pp + 1);
-      Zs += e * __ldcg(pp + 2);
-      if (j < nzV) As += e * __ldcg(pp + 4 + j);
+      esc[sp * MAX_G + h] = e;
+      Ls = fmaf(e, __ldcg(pp + 1), Ls);
+      Zs = fmaf(e, __ldcg(pp + 2), Zs);
     }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    delta[h * D + j] = j < nzV ? sigV[j] * (Zs * inv + exp2i(-(int)wV[j]) * As * inv) : 0.f;
-    if (j == 0) s_have[h] = Ls > 0.f ? 1.f : 0.f;
+    Ls = warp_sum(Ls);
+    Zs = warp_sum(Zs);
+    if (lane == 0) {
+      LZ[h] = Ls;
+      LZ[MAX_G + h] = Zs;
+    }
+  }
+  // A_{h,j} = sum_s e_{s,h} A_{s,h,j}: partials streamed through shared memory by bulk copies
+  const uint32_t per_split = (uint32_t)g * PSTR * 4;
+  const int chunk_splits = max(1, min(S, (int)(L.tail_reserve / per_split)));
+  const int items = g * nzV;
+  float accA[7];
+#pragma unroll
+  for (int r = 0; r < 7; ++r) accA[r] = 0.f;
+  uint32_t tphase = 0;
+  bool ok = true;
+  fence_proxy_async_global();
+  for (int c0s = 0; c0s < S; c0s += chunk_splits) {
+    const int n = min(chunk_splits, S - c0s);
+    __syncthreads();  // previous chunk consumed (and the merge scratch above is dead)
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      mbar_expect_tx(smem_u32(tbar), (uint32_t)n * per_split);
+      bulk_g2s(smem_u32(smem), pb + (size_t)c0s * g * PSTR, (uint32_t)n * per_split, smem_u32(tbar));
+    }
+    const bool okw = mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);
+    if (!okw && tid == 0) mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);  // drain before leaving
+    ok = __syncthreads_and(okw);
+    tphase ^= 1u;
+    if (!ok) break;
+    const float* cp = reinterpret_cast<const float*>(smem);
+#pragma unroll
+    for (int r = 0; r < 7; ++r) {
+      const int it = tid + r * DTHREADS;
+      if (it < items) {
+        const int h = it / nzV, jj = it - h * nzV;
+        float s = accA[r];
+        for (int sp = 0; sp < n; ++sp) s = fmaf(esc[(c0s + sp) * MAX_G + h], cp[(sp * g + h) * PSTR + 4 + jj], s);
+        accA[r] = s;
+      }
+    }
+  }
+  if (__syncthreads_or(!ok)) return;
+  const float* sigV = TV.sigma + (size_t)set * D;
+  const uint8_t* wV = TV.widths + (size_t)set * D;
+  for (int it = tid; it < g * D; it += DTHREADS) delta[it] = 0.f;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 7; ++r) {
+    const int it = tid + r * DTHREADS;
+    if (it < items) {
+      const int h = it / nzV, jj = it - h * nzV;
+      const float Lh = LZ[h];
+      const int bw = wV[jj];
+      if (Lh > 0.f && bw > 0) delta[h * D + jj] = sigV[jj] * (LZ[MAX_G + h] + exp2i(-bw) * accA[r]) / Lh;
+    }
+  }
+  // T_V rows [0, nzV) into shared memory (one bulk copy, warm in L2)
+  __syncthreads();  // the last chunk of partials has been read
+  if (tid == 0 && nzV > 0) {
+    fence_proxy_async_smem();
+    mbar_expect_tx(smem_u32(tbar), (uint32_t)nzV * D * 4);
+    bulk_g2s(smem_u32(smem), TV.T + (size_t)set * D * D, (uint32_t)nzV * D * 4, smem_u32(tbar));
   }
   __syncthreads();
-  {
+  if (nzV > 0) ok = mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);
+  if (!ok && tid == 0) mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);  // drain before leaving
+  if (__syncthreads_or(!ok)) return;
+  if (tid < D) {
     const int k = tid;
-    const float* Tv = TV.T + (size_t)set * D * D;
+    const float* Ts = reinterpret_cast<const float*>(smem);
     const float bk = TV.base[(size_t)set * D + k];
     float o[MAX_G];
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h) o[h] = bk;
     for (int jj = 0; jj < nzV; ++jj) {
-      const float t = __ldg(Tv + (size_t)jj * D + k);
+      const float t = Ts[jj * D + k];
 #pragma unroll
       for (int h = 0; h < MAX_G; ++h)
         if (h < g) o[h] = fmaf(t, delta[h * D + jj], o[h]);
     }
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h)
-      if (h < g) a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] = s_have[h] != 0.f ? o[h] : 0.f;
+      if (h < g) a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] = LZ[h] > 0.f ? o[h] : 0.f;
   }
   if (tid == 0) a.cnt[bh] = 0u;
 }
@@ -582,20 +747,22 @@ static int sm_count(int device) {
   return n > 0 ? n : 148;
 }
 
-static void split_plan(int B, int Hkv, int64_t T_cap, int device, int tile, int per_sm, int* splits, int* chunk) {
+static void split_plan(int B, int Hkv, int64_t T_cap, int device, int tile, int per_sm, int max_splits,
+                       int* splits, int* chunk) {
   const long long bh = (long long)B * Hkv;
   const long long tiles = (T_cap + tile - 1) / tile;
   long long sp = ((long long)per_sm * sm_count(device) + bh - 1) / bh;
-  sp = std::max(1LL, std::min(sp, tiles));
+  sp = std::max(1LL, std::min(std::min(sp, tiles), (long long)max_splits));
   const long long ct = (tiles + sp - 1) / sp;
   *splits = (int)((tiles + ct - 1) / ct);
   *chunk = (int)(ct * tile);
 }
 
-DecodeLayout decode_layout(int B, int Hkv, int64_t T_cap, int device) {
+DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device) {
   DecodeLayout L{};
-  split_plan(B, Hkv, T_cap, device, DT, 2, &L.splits, &L.chunk);
+  split_plan(B, Hkv, T_cap, device, DT, 2, MAX_SPLITS, &L.splits, &L.chunk);
   const size_t bh = (size_t)B * Hkv;
+  const int g = Hq / Hkv;
   size_t o = 0;
   L.off_qa = o;
   o = align256(o + bh * 16 * D * sizeof(__half));
@@ -604,9 +771,14 @@ DecodeLayout decode_layout(int B, int Hkv, int64_t T_cap, int device) {
   L.off_cnt = o;
   o = align256(o + bh * sizeof(unsigned));
   L.off_part = o;
-  o = align256(o + bh * (size_t)L.splits * 8 * PSTR * sizeof(float));
+  o = align256(o + bh * (size_t)L.splits * g * PSTR * sizeof(float));
   L.total = o;
   return L;
+}
+
+static int ring_stages(int RK, int RV) {
+  const int stage = DT * (RK + RV) * 4;
+  return std::max(2, std::min(MAX_STAGES, RING_BUDGET / stage));
 }
 
 kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
@@ -632,11 +804,16 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   a.per_seq = c.per_seq_params;
   a.splits = L.splits;
   a.chunk = L.chunk;
+  a.stages = ring_stages(P.t[0].r_words, P.t[1].r_words);
   a.scale_log2 = scale * 1.4426950408889634f;
-  qprep_kernel<<<dim3(c.Hkv, B), 256, 0, s>>>(P, a);
+  const size_t qsm = qprep_smem_bytes();
+  cudaFuncSetAttribute(qprep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qsm);
+  qprep_kernel<<<dim3(c.Hkv, B), QP_THREADS, qsm, s>>>(P, a);
   kv_status st = launch_check("qprep_kernel");
   if (st != KV_OK) return st;
-  const size_t smem = decode_smem_bytes(P.t[0].r_words, P.t[1].r_words);
+  // shared memory sized for the widest parameter set (8 channel blocks each for K and V)
+  const int nb = a.g <= 4 ? 1 : 2;
+  const size_t smem = decode_smem(P.t[0].r_words, P.t[1].r_words, 8, 8, a.stages, nb).total;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.splits, c.Hkv, B);
   cfg.blockDim = dim3(DTHREADS);
@@ -648,7 +825,7 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (a.g <= 4) {
+  if (nb == 1) {
     cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     e = cudaLaunchKernelEx(&cfg, decode_kernel<1>, P, a);
   } else {
@@ -666,6 +843,7 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
 // uncompressed bf16 split-K flash-decode (comparator)
 // ======================================================================================================
 constexpr int BDT = 64;
+constexpr int BTHREADS = 128;
 constexpr int BSTAGES = 3;
 constexpr int BPITCH = 272;  // bytes per token row in shared memory (256 + 16: conflict-free ldmatrix)
 
@@ -685,7 +863,7 @@ struct DecBf16Args {
 
 static size_t decode_bf16_smem_bytes() { return (size_t)BSTAGES * 2 * BDT * BPITCH + BSTAGES * 8 + 128; }
 
-__global__ void __launch_bounds__(DTHREADS, 2) decode_bf16_kernel(DecBf16Args a) {
+__global__ void __launch_bounds__(BTHREADS, 2) decode_bf16_kernel(DecBf16Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int bh = b * a.Hkv + kh;
@@ -867,7 +1045,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_bf16_kernel(DecBf16Args a)
   }
   __syncthreads();
   float* part = a.part + ((size_t)bh * a.splits + split) * 8 * PSTR;
-  for (int idx = tid; idx < g * PSTR; idx += DTHREADS) {
+  for (int idx = tid; idx < g * PSTR; idx += BTHREADS) {
     const int h = idx / PSTR, cidx = idx - h * PSTR;
     float M = -INFINITY;
 #pragma unroll
@@ -911,7 +1089,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_bf16_kernel(DecBf16Args a)
 
 DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device) {
   DecodeLayout L{};
-  split_plan(B, Hkv, T_cap, device, BDT, 2, &L.splits, &L.chunk);
+  split_plan(B, Hkv, T_cap, device, BDT, 2, 1 << 20, &L.splits, &L.chunk);
   const size_t bh = (size_t)B * Hkv;
   size_t o = 0;
   L.off_qa = L.off_qc = 0;
@@ -955,7 +1133,7 @@ kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int H
   if (st != KV_OK) return st;
   const size_t smem = decode_bf16_smem_bytes();
   cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  decode_bf16_kernel<<<dim3(L.splits, Hkv, B), DTHREADS, smem, s>>>(a);
+  decode_bf16_kernel<<<dim3(L.splits, Hkv, B), BTHREADS, smem, s>>>(a);
   return launch_check("decode_bf16_kernel");
 }
 
@@ -993,27 +1171,27 @@ kv_status launch_debug_quantize_pack(const ParamsDev& P, int set, int tensor, co
   return launch_check("debug quantize/pack");
 }
 
-// Runs the decode kernel's cooperative unpacker over 64-record tiles and writes integer codes.
-__global__ void __launch_bounds__(DTHREADS) debug_unpack_kernel(ParamsDev P, int set, int tensor,
+// Runs the decoder's record unpacker (unpack_pair) over 64-record tiles and writes integer codes.
+__global__ void __launch_bounds__(128) debug_unpack_kernel(ParamsDev P, int set, int tensor,
                                                                 const uint32_t* rec, long long n,
                                                                 uint16_t* codes) {
-  __shared__ uint32_t srec[DT * MAX_RW + 4];
-  __shared__ __align__(16) uint8_t tile[DT * KC_PITCH_MAX];
+  __shared__ uint32_t srec[UNPACK_T * MAX_RW + 4];
+  __shared__ __align__(16) uint8_t tile[UNPACK_T * KC_PITCH_MAX];
   const TensorDev& td = P.t[tensor];
   const int R = td.r_words, tid = threadIdx.x;
-  const long long t0 = (long long)blockIdx.x * DT;
-  const int cnt = (int)min((long long)DT, n - t0);
-  for (int i = tid; i < DT * R + 4; i += DTHREADS) srec[i] = i < cnt * R ? rec[t0 * R + i] : 0u;
+  const long long t0 = (long long)blockIdx.x * UNPACK_T;
+  const int cnt = (int)min((long long)UNPACK_T, n - t0);
+  for (int i = tid; i < UNPACK_T * R + 4; i += 128) srec[i] = i < cnt * R ? rec[t0 * R + i] : 0u;
   __syncthreads();
   const int nz = td.nz[set], nblk = (nz + 15) >> 4, pitch = unpacked_pitch(nblk);
-  const QuadMap m = quad_map(nblk * 4, tid, DTHREADS);
+  const QuadMap m = quad_map(nblk * 4, tid, 128);
   if (m.active) {
     const QuadDesc dq = load_quad(td, set, m.q);
-    for (int t = m.r0; t < DT; t += m.rstep)
+    for (int t = m.r0; t < UNPACK_T; t += m.rstep)
       *reinterpret_cast<uint2*>(tile + t * pitch + 8 * m.q) = unpack_quad(srec + t * R, dq);
   }
   __syncthreads();
-  for (int i = tid; i < cnt * D; i += DTHREADS) {
+  for (int i = tid; i < cnt * D; i += 128) {
     const int t = i / D, j = i % D;
     uint16_t c = 0;
     if (j < nz) {
@@ -1026,7 +1204,7 @@ __global__ void __launch_bounds__(DTHREADS) debug_unpack_kernel(ParamsDev P, int
 
 kv_status launch_debug_unpack(const ParamsDev& P, int set, int tensor, const uint32_t* rec, int64_t n,
                               uint16_t* codes, cudaStream_t s) {
-  debug_unpack_kernel<<<(unsigned)((n + DT - 1) / DT), DTHREADS, 0, s>>>(P, set, tensor, rec, n, codes);
+  debug_unpack_kernel<<<(unsigned)((n + UNPACK_T - 1) / UNPACK_T), 128, 0, s>>>(P, set, tensor, rec, n, codes);
   return launch_check("debug unpack");
 }
 
@@ -1095,7 +1273,7 @@ extern "C" kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache
     kvtc::set_error("cudaGetDevice failed");
     return KV_ERR_CUDA;
   }
-  const kvtc::DecodeLayout L = kvtc::decode_layout(B, c->Hkv, c->T_cap, dev);
+  const kvtc::DecodeLayout L = kvtc::decode_layout(B, c->Hkv, Hq, c->T_cap, dev);
   if (L.total > (size_t)KV_NOALLOC_SCRATCH_BYTES) {
     kvtc::set_error("decode of B=%d Hkv=%d T_cap=%lld needs %zu bytes of scratch, more than the library's fixed "
                     "%u bytes; use kv_attend_decode with a workspace", B, c->Hkv, (long long)c->T_cap, L.total,
