@@ -514,7 +514,7 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     blob.resize(off + bytes);
     return Piece{off, bytes};
   };
-  Piece pT[2], pTT[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], pnz[2], psl[2];
+  Piece pT[2], pTT[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], pnz[2], psl[2], psc[2], pws[2];
   for (int t = 0; t < 2; ++t) {
     pT[t] = reserve((size_t)S * d * d * 4);
     pTT[t] = reserve((size_t)S * d * d * 4);
@@ -523,6 +523,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     psg[t] = reserve((size_t)S * d * 4);
     pinv[t] = reserve((size_t)S * d * 4);
     pbase[t] = reserve((size_t)S * d * 4);
+    psc[t] = reserve((size_t)S * d * d * 4);
+    pws[t] = reserve((size_t)S * d * 4);
     pw[t] = reserve((size_t)S * d);
     pnz[t] = reserve((size_t)S * 4);
     psl[t] = reserve((size_t)S * (d / 2) * 4);
@@ -535,6 +537,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     float* sg = (float*)&blob[psg[t].off];
     float* inv = (float*)&blob[pinv[t].off];
     float* base = (float*)&blob[pbase[t].off];
+    float* tsc = (float*)&blob[psc[t].off];
+    float* wsum = (float*)&blob[pws[t].off];
     uint8_t* w8 = (uint8_t*)&blob[pw[t].off];
     int32_t* nz = (int32_t*)&blob[pnz[t].off];
     uint32_t* sl = (uint32_t*)&blob[psl[t].off];
@@ -572,6 +576,19 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
         for (int j = 0; j < d; ++j) acc += (double)Tsrc[(size_t)j * d + k] * (double)p->mu[t][(size_t)s * d + j];
         base[(size_t)s * d + k] = (float)acc;
       }
+      // scaled rows T'[j][k] = T[j][k] sigma_j 2^-b_j and w_k = sum_{b_j > 0} T[j][k] sigma_j: the decode maps a
+      // split's rotated-basis value sums into the original basis with them
+      for (int k = 0; k < d; ++k) {
+        double wacc = 0.0;
+        for (int j = 0; j < d; ++j) {
+          const double tj = (double)Tsrc[(size_t)j * d + k];
+          const double sj = (double)p->sigma[t][(size_t)s * d + j];
+          const int bj = wv[j];
+          tsc[(size_t)s * d * d + (size_t)j * d + k] = bj > 0 ? (float)(tj * sj * std::ldexp(1.0, -bj)) : 0.f;
+          if (bj > 0) wacc += tj * sj;
+        }
+        wsum[(size_t)s * d + k] = (float)wacc;
+      }
       int word[D / 2], pos[D / 2];
       kvtc::slot_layout(wv.data(), d, p->r_words[t], word, pos);
       for (int k = 0; k < d / 2; ++k)
@@ -600,6 +617,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     td.sigma = (const float*)(b + psg[t].off);
     td.inv_sigma = (const float*)(b + pinv[t].off);
     td.base = (const float*)(b + pbase[t].off);
+    td.Tsc = (const float*)(b + psc[t].off);
+    td.wsum = (const float*)(b + pws[t].off);
     td.widths = (const uint8_t*)(b + pw[t].off);
     td.nz = (const int32_t*)(b + pnz[t].off);
     td.slots = (const uint32_t*)(b + psl[t].off);

@@ -29,6 +29,8 @@ struct TensorDev {
   const float* sigma;              // [S][D]
   const float* inv_sigma;          // [S][D]  fp32(1/sigma) computed in double; 0 for zero-width
   const float* base;               // [S][D]  T^T mu (original-basis vector of the all-mean record)
+  const float* Tsc;                // [S][D][D]  T[j][k] sigma_j 2^-b_j (0 for zero-width rows)
+  const float* wsum;               // [S][D]  sum over b_j > 0 of T[j][k] sigma_j
   const uint8_t* widths;           // [S][D]
   const int32_t* nz;               // [S]     1 + last storage channel with width > 0
   const uint32_t* slots;           // [S][D/2] pair slots: code word | bit << 8 | b_2k << 16 | b_2k+1 << 24

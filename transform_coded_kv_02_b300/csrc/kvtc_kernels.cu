@@ -163,8 +163,7 @@ constexpr int DTHREADS = 32 * (DWARPS + 1);
 constexpr int RING_BUDGET = 48 * 1024;
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_SPLITS = 256;
-constexpr int TAIL_RESERVE = MAX_G * D * 4 + MAX_SPLITS * MAX_G * 4 + 2 * MAX_G * 4;  // delta, e, L/Z
-constexpr int TAIL_MIN = 64 * 1024 + MAX_G * PSTR * 4;   // T_V rows, or one split's partials
+constexpr int TAIL_RESERVE = MAX_SPLITS * MAX_G * 4 + 4 * MAX_G * 4;  // split weights, head state
 constexpr int UNPACK_T = 64;       // tokens per tile of the parity unpacker
 constexpr int KC_PITCH_MAX = 272;  // bytes per token row of an unpacked tile (odd multiple of 16)
 
@@ -190,23 +189,27 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---- q preparation: one CTA per (sequence, KV head) ---------------------------------------------------
-// q~ = T_K q for the g query heads (T_K rows staged in shared memory by one bulk copy);
-// q'_j = a log2(e) q~_j sigma_j 2^-b_j as fp16 hi + lo; C0 = a log2(e) q.(T_K^T mu); C1 = a log2(e) sum q~_j sigma_j.
+// q~ = T_K q for the g query heads (T_K rows staged in shared memory by one bulk copy, every other input
+// fetched while it flies); q'_j = a log2(e) q~_j sigma_j 2^-b_j as fp16 hi + lo; C0 = a log2(e) q.(T_K^T mu);
+// C1 = a log2(e) sum_{b_j > 0} q~_j sigma_j. 256 threads: channel j = tid % 128, half of the k range = tid / 128.
 constexpr int QP_THREADS = 256;
-static size_t qprep_smem_bytes() { return (size_t)D * D * 4 + (size_t)MAX_G * D * 4; }
+static size_t qprep_smem_bytes() { return (size_t)D * D * 4 + 2 * (size_t)MAX_G * D * 4; }
 
 __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs a) {
   pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   float* Ts = reinterpret_cast<float*>(smem);    // [nz][128]
   float* qs = Ts + D * D;                        // [g][128]
+  float* hs = qs + MAX_G * D;                    // [8][128] upper-half partial sums
   __shared__ uint64_t bar;
-  __shared__ float red[4][MAX_G];
+  __shared__ float red[4][2][MAX_G];
   const int kh = blockIdx.x, b = blockIdx.y;
   const int bh = b * a.Hkv + kh;
   const int set = a.per_seq ? bh : kh;
   const TensorDev& tk = P.t[0];
-  const int nz = tk.nz[set], g = a.g, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = a.g, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j = tid & (D - 1), hf = tid >> 7;
+  const int nz = tk.nz[set];
   if (tid == 0) {
     mbar_init(smem_u32(&bar), 1);
     fence_mbar_init();
@@ -216,64 +219,69 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs 
     mbar_expect_tx(smem_u32(&bar), (uint32_t)nz * D * 4);
     bulk_g2s(smem_u32(Ts), tk.T + (size_t)set * D * D, (uint32_t)nz * D * 4, smem_u32(&bar));
   }
+  // everything else is fetched while T_K is in flight
+  const float sg = tk.sigma[(size_t)set * D + j];
+  const int bw = tk.widths[(size_t)set * D + j];
+  const float bk = tk.base[(size_t)set * D + j];
   const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kh * g) * D;
   for (int i = tid; i < g * D; i += QP_THREADS) qs[i] = __bfloat162float(qg[i]);
   bool ok = true;
   if (nz > 0) ok = mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);
   if (!ok && tid == 0) mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);  // drain before leaving
-  __syncthreads();
   if (__syncthreads_or(!ok)) return;
 
   float qt[MAX_G];
 #pragma unroll
   for (int h = 0; h < MAX_G; ++h) qt[h] = 0.f;
-  const int j = tid;
-  if (j < D && j < nz) {
-    const float4* Trow = reinterpret_cast<const float4*>(Ts + (size_t)j * D);
+  if (j < nz) {
+    const float4* Trow = reinterpret_cast<const float4*>(Ts + (size_t)j * D) + 16 * hf;
 #pragma unroll 4
-    for (int k4 = 0; k4 < D / 4; ++k4) {
-      const int kk = (k4 + j) & (D / 4 - 1);   // rotated start: conflict-free row reads
+    for (int k4 = 0; k4 < 16; ++k4) {
+      const int kk = (k4 + j) & 15;   // rotated start: conflict-free row reads
       const float4 t = Trow[kk];
 #pragma unroll
       for (int h = 0; h < MAX_G; ++h) {
         if (h < g) {
-          const float4 qv = reinterpret_cast<const float4*>(qs + h * D)[kk];
+          const float4 qv = reinterpret_cast<const float4*>(qs + h * D)[16 * hf + kk];
           qt[h] = fmaf(t.x, qv.x, fmaf(t.y, qv.y, fmaf(t.z, qv.z, fmaf(t.w, qv.w, qt[h]))));
         }
       }
     }
   }
-  float c1[MAX_G];
-  if (j < D) {
-    const float sg = tk.sigma[(size_t)set * D + j];
-    const int bw = tk.widths[(size_t)set * D + j];
+  if (hf == 1) {
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) hs[h * D + j] = qt[h];
+  }
+  __syncthreads();
+  if (hf == 0) {
     __half* qa = a.qa + (size_t)bh * 16 * D;
+    float c0p[MAX_G], c1p[MAX_G];
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h) {
+      const float q_t = qt[h] + hs[h * D + j];
       const bool on = h < g && bw > 0;
-      const float qp = on ? a.scale_log2 * qt[h] * sg * exp2i(-bw) : 0.f;
+      const float qp = on ? a.scale_log2 * q_t * sg * exp2i(-bw) : 0.f;
       const __half hi = __float2half_rn(qp);
       const __half lo = __float2half_rn(qp - __half2float(hi));
       qa[(2 * h) * D + j] = hi;
       qa[(2 * h + 1) * D + j] = lo;
-      c1[h] = on ? qt[h] * sg : 0.f;
+      c1p[h] = on ? q_t * sg : 0.f;
+      c0p[h] = h < g ? bk * qs[h * D + j] : 0.f;
     }
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h) {
-      const float s = warp_sum(c1[h]);
-      if (lane == 0) red[warp][h] = s;
+      const float s0 = warp_sum(c0p[h]), s1 = warp_sum(c1p[h]);
+      if (lane == 0) {
+        red[warp][0][h] = s0;
+        red[warp][1][h] = s1;
+      }
     }
   }
   __syncthreads();
-  if (warp < g) {  // C0 of head `warp`: q . (T_K^T mu) over the original basis
-    const float* base = tk.base + (size_t)set * D;
-    float c0 = 0.f;
-    for (int k = lane; k < D; k += 32) c0 = fmaf(base[k], qs[warp * D + k], c0);
-    c0 = warp_sum(c0);
-    if (lane == 0) {
-      a.qc[bh * 16 + warp] = a.scale_log2 * c0;
-      a.qc[bh * 16 + 8 + warp] = a.scale_log2 * (red[0][warp] + red[1][warp] + red[2][warp] + red[3][warp]);
-    }
+  if (tid < g) {
+    const int h = tid;
+    a.qc[bh * 16 + h] = a.scale_log2 * (red[0][0][h] + red[1][0][h] + red[2][0][h] + red[3][0][h]);
+    a.qc[bh * 16 + 8 + h] = a.scale_log2 * (red[0][1][h] + red[1][1][h] + red[2][1][h] + red[3][1][h]);
   }
   if (tid == 0) a.cnt[bh] = 0u;
 }
@@ -284,21 +292,26 @@ __host__ __device__ __forceinline__ int unpacked_pitch(int nblk16) {  // bytes, 
 }
 
 struct DecSmem {  // byte offsets into the dynamic shared memory of decode_kernel
-  uint32_t stage_bytes, tiles, warp_tile, ps, bars, tail_reserve, total;
+  uint32_t stage_bytes, tiles, warp_tile, ps, bars, epi_ws, epi_merged, tail_reserve, total;
 };
 
 __host__ __device__ __forceinline__ uint32_t align128u(uint32_t x) { return (x + 127u) & ~127u; }
 
+// main loop: ring | per-warp unpacked tiles | per-warp P tiles
+// epilogue (ring and tiles dead): T'_V rows [0, 64 KB) | per-warp partials | merged partial
+// tail: split partial chunks from 0 | per-split weights and per-head state in the reserve at the end
 __host__ __device__ inline DecSmem decode_smem(int RK, int RV, int nkb, int nmb, int stages, int nb) {
   DecSmem s;
   s.stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
   s.tiles = align128u(stages * s.stage_bytes);
   s.warp_tile = 16u * (uint32_t)(unpacked_pitch(nkb) + unpacked_pitch(nmb));
   s.ps = align128u(s.tiles + DWARPS * s.warp_tile);
-  s.bars = align128u(s.ps + DWARPS * 16u * 8u * nb * 2u);
-  uint32_t end = s.bars + (2u * MAX_STAGES + 1u) * 8u;
-  if (end < (uint32_t)TAIL_MIN) end = TAIL_MIN;
-  s.tail_reserve = align128u(end);
+  s.bars = 0;
+  const uint32_t main_end = s.ps + DWARPS * 16u * 8u * nb * 2u;
+  s.epi_ws = D * D * 4u;
+  s.epi_merged = s.epi_ws + DWARPS * 8u * PSTR * 4u;
+  const uint32_t epi_end = s.epi_merged + (MAX_G * D + 4 * MAX_G) * 4u;
+  s.tail_reserve = align128u(main_end > epi_end ? main_end : epi_end);
   s.total = s.tail_reserve + TAIL_RESERVE;
   return s;
 }
@@ -306,6 +319,8 @@ __host__ __device__ inline DecSmem decode_smem(int RK, int RV, int nkb, int nmb,
 template <int NB>
 __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // barriers live outside the dynamic region, which the epilogue and the tail reuse wholesale
+  __shared__ __align__(8) uint64_t full[MAX_STAGES], empty[MAX_STAGES], tbar_s;
   __shared__ int s_abort, s_last, s_issued;
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int bh = b * a.Hkv + kh;
@@ -318,9 +333,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   const int nkb = (nzK + 15) >> 4, nmb = (nzV + 15) >> 4;
   const int pitchK = unpacked_pitch(nkb), pitchV = unpacked_pitch(nmb);
   const DecSmem L = decode_smem(RK, RV, nkb, nmb, NS, NB);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + MAX_STAGES;
-  uint64_t* tbar = empty + MAX_STAGES;
+  uint64_t* tbar = &tbar_s;
 
   const long long Lseq = min((long long)a.seq_lens[b], a.T_cap);
   const long long t0 = (long long)split * a.chunk;
@@ -579,8 +592,18 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
     return;
   }
 
-  // ---- merge the consumer warps of this CTA (ring memory is free now) ----
-  float* ws = reinterpret_cast<float*>(smem);  // [DWARPS][8][PSTR]
+  // ================= epilogue: this split's partial, mapped to the original basis =================
+  // N_h[k] = Z_h w_k + sum_j T'[j][k] A_h[j] with T'[j][k] = T_V[j][k] sigma_j 2^-b_j and w_k = sum_{b_j>0} T_V[j][k]
+  // sigma_j, so that o_h[k] = base_k + (sum over splits e_s N_s,h[k]) / (sum over splits e_s L_s,h).
+  float* Tsc = reinterpret_cast<float*>(smem);                           // [nzV][128]
+  float* ws = reinterpret_cast<float*>(smem + L.epi_ws);                 // [DWARPS][8][PSTR]
+  float* mA = reinterpret_cast<float*>(smem + L.epi_merged);             // [8][128]
+  float* mS = mA + MAX_G * D;                                            // M[8], L[8], Z[8]
+  if (tid == 0 && nzV > 0) {
+    fence_proxy_async_smem();
+    mbar_expect_tx(smem_u32(tbar), (uint32_t)nzV * D * 4);
+    bulk_g2s(smem_u32(Tsc), TV.Tsc + (size_t)set * D * D, (uint32_t)nzV * D * 4, smem_u32(tbar));
+  }
   if (warp < DWARPS) {
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
@@ -603,25 +626,54 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
     }
   }
   __syncthreads();
-  float* part = a.part + ((size_t)bh * a.splits + split) * g * PSTR;
-  const int acols = 4 + nmb * 16;
-  for (int idx = tid; idx < g * PSTR; idx += DTHREADS) {
-    const int h = idx / PSTR, cidx = idx - h * PSTR;
-    float M = -INFINITY;
+  {
+    const int acols = 4 + nmb * 16;
+    for (int idx = tid; idx < g * acols; idx += DTHREADS) {
+      const int h = idx / acols, cidx = idx - h * acols;
+      if (cidx == 3) continue;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < DWARPS; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
-    float val = 0.f;
-    if (cidx == 0) {
-      val = M;
-    } else if (cidx != 3 && cidx < acols) {
+      for (int w = 0; w < DWARPS; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
+      if (cidx == 0) {
+        mS[h] = M;
+        continue;
+      }
+      float val = 0.f;
 #pragma unroll
       for (int w = 0; w < DWARPS; ++w) {
         const float mw = ws[(w * 8 + h) * PSTR];
         const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
         val = fmaf(e, ws[(w * 8 + h) * PSTR + cidx], val);
       }
+      if (cidx == 1) mS[MAX_G + h] = val;
+      else if (cidx == 2) mS[2 * MAX_G + h] = val;
+      else mA[h * D + cidx - 4] = val;
     }
-    part[idx] = val;
+  }
+  bool okw = true;
+  if (nzV > 0) okw = mbar_wait_bounded(smem_u32(tbar), 0u, a.wait_ns);
+  if (!okw && tid == 0) mbar_wait_bounded(smem_u32(tbar), 0u, a.wait_ns);  // drain before leaving
+  if (__syncthreads_or(!okw)) return;
+  float* part = a.part + ((size_t)bh * a.splits + split) * g * PSTR;
+  if (tid < D) {
+    const int k = tid;
+    const float wk = TV.wsum[(size_t)set * D + k];
+    float n[MAX_G];
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) n[h] = h < g ? mS[2 * MAX_G + h] * wk : 0.f;
+    for (int jj = 0; jj < nzV; ++jj) {
+      const float t = Tsc[jj * D + k];
+#pragma unroll
+      for (int h = 0; h < MAX_G; ++h)
+        if (h < g) n[h] = fmaf(t, mA[h * D + jj], n[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h)
+      if (h < g) part[h * PSTR + 4 + k] = n[h];
+  } else if (tid < D + g) {
+    const int h = tid - D;
+    part[h * PSTR + 0] = mS[h];
+    part[h * PSTR + 1] = mS[MAX_G + h];
   }
   __threadfence();
   __syncthreads();
@@ -630,111 +682,79 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   if (!s_last) return;
   __threadfence();
 
-  // ======== last CTA of (b, kh): merge the splits, reconstruct o^ - mu, inverse-rotate once ========
-  float* delta = reinterpret_cast<float*>(smem + L.tail_reserve);   // [8][128]
-  float* esc = delta + MAX_G * D;                                   // [splits][g]
-  float* LZ = esc + MAX_SPLITS * MAX_G;                             // [2][8]
+  // ======== last CTA of (b, kh): weighted sum of the split partials (streamed by bulk copies) ========
+  float* esc = reinterpret_cast<float*>(smem + L.tail_reserve);   // [MAX_SPLITS][8] split weights of a chunk
+  float* hst = esc + MAX_SPLITS * MAX_G;                          // Mrun[8], Lrun[8], Mnew[8], scale[8]
   const float* pb = a.part + (size_t)bh * a.splits * g * PSTR;
   const int S = a.splits;
-  // per-head maximum, split weights, L and Z (one warp per head)
-  for (int h = warp; h < g; h += DWARPS + 1) {
-    float M = -INFINITY;
-    for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, __ldcg(pb + ((size_t)sp * g + h) * PSTR));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Ls = 0.f, Zs = 0.f;
-    for (int sp = lane; sp < S; sp += 32) {
-      const float* pp = pb + ((size_t)sp * g + h) * PSTR;
-      const float ms = __ldcg(pp);
-      const float e = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      esc[sp * MAX_G + h] = e;
-      Ls = fmaf(e, __ldcg(pp + 1), Ls);
-      Zs = fmaf(e, __ldcg(pp + 2), Zs);
-    }
-    Ls = warp_sum(Ls);
-    Zs = warp_sum(Zs);
-    if (lane == 0) {
-      LZ[h] = Ls;
-      LZ[MAX_G + h] = Zs;
-    }
-  }
-  // A_{h,j} = sum_s e_{s,h} A_{s,h,j}: partials streamed through shared memory by bulk copies
   const uint32_t per_split = (uint32_t)g * PSTR * 4;
-  const int chunk_splits = max(1, min(S, (int)(L.tail_reserve / per_split)));
-  const int items = g * nzV;
-  float accA[7];
+  const int chunk_splits = max(1, min(S, min((int)(L.tail_reserve / per_split), MAX_SPLITS)));
+  const int items = g * D;
+  float accN[7];
 #pragma unroll
-  for (int r = 0; r < 7; ++r) accA[r] = 0.f;
-  uint32_t tphase = 0;
-  bool ok = true;
+  for (int r = 0; r < 7; ++r) accN[r] = 0.f;
+  if (tid < g) {
+    hst[tid] = -INFINITY;
+    hst[MAX_G + tid] = 0.f;
+  }
+  uint32_t tphase = nzV > 0 ? 1u : 0u;  // phase 0 of tbar went to the T' copy when there was one
   fence_proxy_async_global();
+  const float* cp = reinterpret_cast<const float*>(smem);
   for (int c0s = 0; c0s < S; c0s += chunk_splits) {
     const int n = min(chunk_splits, S - c0s);
-    __syncthreads();  // previous chunk consumed (and the merge scratch above is dead)
+    __syncthreads();  // previous chunk consumed
     if (tid == 0) {
       fence_proxy_async_smem();
       mbar_expect_tx(smem_u32(tbar), (uint32_t)n * per_split);
       bulk_g2s(smem_u32(smem), pb + (size_t)c0s * g * PSTR, (uint32_t)n * per_split, smem_u32(tbar));
     }
-    const bool okw = mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);
-    if (!okw && tid == 0) mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);  // drain before leaving
-    ok = __syncthreads_and(okw);
+    const bool okc = mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);
+    if (!okc && tid == 0) mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);  // drain before leaving
     tphase ^= 1u;
-    if (!ok) break;
-    const float* cp = reinterpret_cast<const float*>(smem);
+    if (!__syncthreads_and(okc)) return;
+    if (tid < g) {  // running maximum of head tid over the splits seen so far
+      const int h = tid;
+      float cm = -INFINITY;
+      for (int sp = 0; sp < n; ++sp) cm = fmaxf(cm, cp[(sp * g + h) * PSTR]);
+      const float Mo = hst[h], Mn = fmaxf(Mo, cm);
+      hst[2 * MAX_G + h] = Mn;
+      hst[3 * MAX_G + h] = (Mo == Mn) ? 1.f : exp2f(Mo - Mn);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < n * g; idx += DTHREADS) {
+      const int sp = idx / g, h = idx - sp * g;
+      const float ms = cp[(sp * g + h) * PSTR];
+      esc[sp * MAX_G + h] = (ms == -INFINITY) ? 0.f : exp2f(ms - hst[2 * MAX_G + h]);
+    }
+    __syncthreads();
+    if (tid < g) {
+      const int h = tid;
+      float l = hst[MAX_G + h] * hst[3 * MAX_G + h];
+      for (int sp = 0; sp < n; ++sp) l = fmaf(esc[sp * MAX_G + h], cp[(sp * g + h) * PSTR + 1], l);
+      hst[MAX_G + h] = l;
+      hst[h] = hst[2 * MAX_G + h];
+    }
 #pragma unroll
     for (int r = 0; r < 7; ++r) {
       const int it = tid + r * DTHREADS;
       if (it < items) {
-        const int h = it / nzV, jj = it - h * nzV;
-        float s = accA[r];
-        for (int sp = 0; sp < n; ++sp) s = fmaf(esc[(c0s + sp) * MAX_G + h], cp[(sp * g + h) * PSTR + 4 + jj], s);
-        accA[r] = s;
+        const int h = it >> 7, k = it & (D - 1);
+        float acc = accN[r] * hst[3 * MAX_G + h];
+        for (int sp = 0; sp < n; ++sp) acc = fmaf(esc[sp * MAX_G + h], cp[(sp * g + h) * PSTR + 4 + k], acc);
+        accN[r] = acc;
       }
     }
   }
-  if (__syncthreads_or(!ok)) return;
-  const float* sigV = TV.sigma + (size_t)set * D;
-  const uint8_t* wV = TV.widths + (size_t)set * D;
-  for (int it = tid; it < g * D; it += DTHREADS) delta[it] = 0.f;
   __syncthreads();
 #pragma unroll
   for (int r = 0; r < 7; ++r) {
     const int it = tid + r * DTHREADS;
     if (it < items) {
-      const int h = it / nzV, jj = it - h * nzV;
-      const float Lh = LZ[h];
-      const int bw = wV[jj];
-      if (Lh > 0.f && bw > 0) delta[h * D + jj] = sigV[jj] * (LZ[MAX_G + h] + exp2i(-bw) * accA[r]) / Lh;
+      const int h = it >> 7, k = it & (D - 1);
+      const float Lh = hst[MAX_G + h];
+      a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] =
+          Lh > 0.f ? TV.base[(size_t)set * D + k] + accN[r] / Lh : 0.f;
     }
-  }
-  // T_V rows [0, nzV) into shared memory (one bulk copy, warm in L2)
-  __syncthreads();  // the last chunk of partials has been read
-  if (tid == 0 && nzV > 0) {
-    fence_proxy_async_smem();
-    mbar_expect_tx(smem_u32(tbar), (uint32_t)nzV * D * 4);
-    bulk_g2s(smem_u32(smem), TV.T + (size_t)set * D * D, (uint32_t)nzV * D * 4, smem_u32(tbar));
-  }
-  __syncthreads();
-  if (nzV > 0) ok = mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);
-  if (!ok && tid == 0) mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);  // drain before leaving
-  if (__syncthreads_or(!ok)) return;
-  if (tid < D) {
-    const int k = tid;
-    const float* Ts = reinterpret_cast<const float*>(smem);
-    const float bk = TV.base[(size_t)set * D + k];
-    float o[MAX_G];
-#pragma unroll
-    for (int h = 0; h < MAX_G; ++h) o[h] = bk;
-    for (int jj = 0; jj < nzV; ++jj) {
-      const float t = Ts[jj * D + k];
-#pragma unroll
-      for (int h = 0; h < MAX_G; ++h)
-        if (h < g) o[h] = fmaf(t, delta[h * D + jj], o[h]);
-    }
-#pragma unroll
-    for (int h = 0; h < MAX_G; ++h)
-      if (h < g) a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] = LZ[h] > 0.f ? o[h] : 0.f;
   }
   if (tid == 0) a.cnt[bh] = 0u;
 }
