@@ -278,7 +278,7 @@ def run_ours(args, rank, world, local_rank):
     P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), BITS, BITS).upload()
     rk_w, rv_w = P.record_words(0), P.record_words(1)
     rec_k = torch.zeros((B, Hkv, T_cap, rk_w), dtype=torch.int32, device=dev)
-    rec_v = torch.zeros((B, Hkv, T_cap, rv_w), dtype=torch.int32, device=dev)
+    rec_v = torch.zeros((B, Hkv, T_cap // 2, 2 * rv_w), dtype=torch.int32, device=dev)  # two-token records
     cache = kvtc.make_cache(rec_k, rec_v, B, Hkv, T_cap)
 
     k_all = bf16_tensor(L.k, dev)                         # [B, Hkv, T + n_new, d]

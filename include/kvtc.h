@@ -96,7 +96,9 @@ typedef struct {
 kv_status kv_calibrate(int n_sets, const kv_calib_set* sets, const kv_calib_opts* opts, kv_params** out);
 
 /* Build a parameter table from explicit arrays (host, fp32, set-major): T_* [n_sets][d][d] (rows =
- * storage channels), mu_* / sigma_* [n_sets][d], widths_* [n_sets][d] (0..max 8, sum <= 32*r_words-32).
+ * storage channels), mu_* / sigma_* [n_sets][d], widths_* [n_sets][d] (0..8; the key widths must fit the
+ * key record's first-fit pair slots, the value widths the value record's first-fit channel slots, else
+ * KV_ERR_BUDGET).
  * Channels with sigma == 0 get width 0. Used to feed externally computed parameters (e.g. by a reference
  * implementation) to the codec. */
 kv_status kv_params_from_arrays(int d, int n_sets,
@@ -123,13 +125,19 @@ kv_status kv_params_load(const char* path, kv_params** out);
 void kv_params_free(kv_params* p);
 
 /* ------------------------------------------------------------------------------------------------------
- * Packed cache (device, caller-owned).  [NOVA-KV: fixed per-token bit count]
- * Record of one token and tensor: r_words 32-bit words; word 0 = fp16 zero point z (bits 0-15) | fp16
- * scale s (bits 16-31); channel codes LSB-first from bit 0 of word 1 in storage order; unused bits 0.
+ * Packed cache (device, caller-owned).  [NOVA-KV: fixed per-token bit count and fixed-width layout]
+ * z/s word of a token = fp16 zero point z (bits 0-15) | fp16 scale s (bits 16-31); unused bits are 0.
+ * Key record (one token, r_words_k words): word 0 = z/s; storage channels (2k, 2k+1) share slot k at bit r_k
+ *   of code word 1 + u_k: channel 2k in the low half, channel 2k+1 in the high half.
+ * Value record (tokens 2p and 2p+1, 2 r_words_v words): words 0 and 1 = their z/s words; channel j has slot j
+ *   at bit r_j of code word 2 + u_j: token 2p's code in the low half, token 2p+1's in the high half. (Decode
+ *   contracts values over tokens; this puts the two codes one tensor-core operand register needs into one
+ *   word.) Slots are placed first-fit by kv_calibrate / kv_params_from_arrays.
  * ------------------------------------------------------------------------------------------------------ */
 typedef struct {
   uint32_t* k_rec;      /* [B][Hkv][T_cap][r_words_k], 16-byte aligned                                 */
-  uint32_t* v_rec;      /* [B][Hkv][T_cap][r_words_v], 16-byte aligned                                 */
+  uint32_t* v_rec;      /* [B][Hkv][T_cap / 2][2 r_words_v] (same bytes as T_cap one-token records),
+                           16-byte aligned                                                              */
   int B;
   int Hkv;
   int64_t T_cap;        /* token capacity per (sequence, head); multiple of 16                          */
@@ -144,7 +152,9 @@ size_t kv_cache_bytes(const kv_params* p, int tensor, int B, int Hkv, int64_t T_
  *   dst_pos_dev: device int64 [B], token i of sequence b is written at position dst_pos[b] + i, which must
  *   be <= T_cap - t_new (checked on the device: violations are skipped and reported as KV_ERR_DEVICE).
  * Rotation y = T x, then per token y'_j = (y_j - mu_j) * (1/sigma_j), z = fp16(min y'), s = fp16(max y' - z),
- * c_j = clamp(floor(((y'_j - z)/s) * 2^b_j), 0, 2^b_j - 1), packed as above. */
+ * c_j = clamp(floor(((y'_j - z)/s) * 2^b_j), 0, 2^b_j - 1), packed as above.
+ * A value token writes only its own halves (16-bit stores), so a token appended at an odd position leaves
+ * the record's earlier token intact. */
 kv_status kv_encode(const kv_params* p, const kv_cache* cache, const void* k, const void* v, int dtype,
                     int B, int64_t t_new, const int64_t* dst_pos_dev, kv_stream_t stream);
 
@@ -199,13 +209,14 @@ int kv_version(void);
 /* ------------------------------------------------------------------------------------------------------
  * Parity and test entry points (same kernels' device code; no separate math).
  * ------------------------------------------------------------------------------------------------------ */
-/* Quantise + pack n rotated fp32 vectors y_dev [n][d] (storage order) of one set/tensor into rec_dev
- * [n][r_words], running the encode kernels' quantiser. variant 0: warp-per-token (append / fp32 path);
- * variant 1: thread-per-token (tensor-core prefill epilogue). */
+/* Quantise + pack n rotated fp32 vectors y_dev [n][d] (storage order) of one set/tensor into rec_dev (keys:
+ * [n][r_words]; values: [ceil(n/2)][2 r_words], a missing second token's half left as it was), running the
+ * encode kernels' quantiser. variant 0: warp-per-token; variant 1: thread-per-token. */
 kv_status kv_debug_quantize_pack(const kv_params* p, int set, int tensor, const float* y_dev, int64_t n,
                                  uint32_t* rec_dev, int variant, kv_stream_t stream);
-/* Run the decode kernel's record unpacker over n records rec_dev [n][r_words] of one set/tensor and write
- * codes_dev [n][d] (uint16, channels in storage order; 0 for zero-width channels). */
+/* Run the decoder's slot extraction over the records of n tokens (keys [n][r_words], values
+ * [ceil(n/2)][2 r_words]) of one set/tensor and write codes_dev [n][d] (uint16, storage order; 0 for
+ * zero-width channels). */
 kv_status kv_debug_unpack(const kv_params* p, int set, int tensor, const uint32_t* rec_dev, int64_t n,
                           uint16_t* codes_dev, kv_stream_t stream);
 /* Host water-filling used by kv_calibrate: integer widths for importances lam [d] and budget bits. */

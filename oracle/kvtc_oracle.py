@@ -33,14 +33,22 @@ attention; IEEE fp32 for the quantiser, whose op sequence is part of the record 
     is raised to the slot width (the layout reserves those bits anyway); slots are placed first-fit in
     pair order (lowest code word with room, lowest free bit); while a pair finds no room, the pair with
     the smallest distortion cost 3 (lambda_2k + lambda_2k+1) 4^-w of losing one bit (compared through
-    log2 at 1e-9 resolution; ties: the later pair) loses one bit and the placement restarts.
+    log2 at 1e-9 resolution; ties: the later pair) loses one bit and the placement restarts. That is the
+    key layout ("channel pairs"). Values use a "token pairs" layout instead, because decode contracts
+    values over tokens: a record holds two consecutive tokens, and each channel j has one slot at the same
+    bit of the low half (earlier token) and the high half (later token) of one code word; slots are
+    placed first-fit in storage order, and while a channel finds no room the channel with the smallest
+    cost 3 lambda_j 4^-b_j (same comparison, ties to the later channel) loses one bit.
  6. Per-token quantiser (fixed fp32 op sequence, no fused multiply-add):
       y'_j = (y_j - mu_j) * inv_sigma_j                 (channels with b_j > 0)
       m, M = min/max of y'_j over b_j > 0;  z = fp16(m), s = fp16(M - z) (round-to-nearest-even, saturated)
       c_j = clamp(floor(((y'_j - z) / s) * 2^b_j), 0, 2^b_j - 1);  all codes 0 when s == 0.
- 7. Fixed-width record [NOVA-KV: "a fixed per-token bit count"]: R_w 32-bit words per token; word 0 holds
-    z (bits 0-15) and s (bits 16-31); pair k's codes sit in code word 1 + u_k: channel 2k at bits
-    [r_k, r_k + b_2k), channel 2k+1 at bits [16 + r_k, 16 + r_k + b_2k+1); unused bits are 0.
+ 7. Fixed-width records [NOVA-KV: "a fixed per-token bit count"]. Keys: R_w 32-bit words per token;
+    word 0 holds z (bits 0-15) and s (bits 16-31); pair k's codes sit in code word 1 + u_k: channel 2k
+    at bits [r_k, r_k + b_2k), channel 2k+1 at bits [16 + r_k, 16 + r_k + b_2k+1). Values: 2 R_w words
+    per pair of tokens (2p, 2p+1); words 0 and 1 hold their z/s words, channel j's codes sit in code word
+    2 + u_j at bits [r_j, r_j + b_j) (token 2p) and [16 + r_j, 16 + r_j + b_j) (token 2p+1). The budget per
+    token is the same. Unused bits are 0.
  8. Decode attention over the records: y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j) for b_j > 0, else
     mu_j; k^ = T^T y^ (and v^); o_h = softmax_t(alpha q_h . k^_t) v^ over t < seq_len, all in fp64.
 
@@ -229,12 +237,49 @@ def fit_layout(widths, importance, r_words: int):
     return np.repeat(np.asarray(w, np.int64), 2)
 
 
+def token_slot_layout(widths, r_words: int):
+    """First-fit placement of single channels for the token-pair layout: channel j (width b_j) goes, in
+    storage order, to the lowest of the 2 R_w - 2 code words of a two-token record whose 16-bit halves have
+    b_j free bits, at the lowest free bit. Returns (word [d], pos [d]) with -1 for zero widths, or None
+    when a channel finds no room."""
+    w = np.asarray(widths, np.int64)
+    n_words = 2 * r_words - 2
+    used = [0] * max(n_words, 0)
+    word = np.full(w.shape[0], -1, np.int64)
+    pos = np.full(w.shape[0], -1, np.int64)
+    for j in range(w.shape[0]):
+        b = int(w[j])
+        if b == 0:
+            continue
+        for u in range(n_words):
+            if used[u] + b <= HALF:
+                word[j], pos[j] = u, used[u]
+                used[u] += b
+                break
+        else:
+            return None
+    return word, pos
+
+
+def fit_token_layout(widths, importance, r_words: int):
+    """Widths (storage order) that the token-pair layout can hold: single bits taken from the cheapest
+    channel (smallest cost key of lambda_j, ties to the later channel) until first-fit placement succeeds."""
+    w = [int(x) for x in np.asarray(widths, np.int64)]
+    lam = [float(x) for x in np.asarray(importance, F64)]
+    while token_slot_layout(w, r_words) is None:
+        _, negj = min((fit_cost_key(lam[j], w[j]), -j) for j in range(len(w)) if w[j] > 0)
+        w[-negj] -= 1
+    return np.asarray(w, np.int64)
+
+
 class TensorParams:
     """One tensor's (K or V) codec parameters in storage order. T: fp32 [d, d] (rows = storage channels);
-    mu, sigma, inv_sigma: fp32 [d]; widths: int [d]; r_words: record length in 32-bit words; slot_word /
-    slot_pos: first-fit placement of each channel pair."""
+    mu, sigma, inv_sigma: fp32 [d]; widths: int [d]; r_words: record length in 32-bit words per token;
+    pairing: "channels" (key records, one token each, channel pairs share slots) or "tokens" (value
+    records, two tokens each, one slot per channel); slot_word / slot_pos: the first-fit placement (per
+    channel pair, resp. per channel)."""
 
-    def __init__(self, T, mu, sigma, widths, r_words, eigvals=None, importance=None):
+    def __init__(self, T, mu, sigma, widths, r_words, eigvals=None, importance=None, pairing="channels"):
         self.T = np.ascontiguousarray(T, F32)
         self.mu = np.ascontiguousarray(mu, F32)
         self.sigma = np.ascontiguousarray(sigma, F32)
@@ -246,26 +291,42 @@ class TensorParams:
         self.r_words = int(r_words)
         self.eigvals = eigvals
         self.importance = importance
-        lay = slot_layout(self.widths, self.r_words)
+        if pairing not in ("channels", "tokens"):
+            raise ValueError(pairing)
+        self.pairing = pairing
+        lay = (slot_layout if pairing == "channels" else token_slot_layout)(self.widths, self.r_words)
         if lay is None:
-            raise ValueError("widths do not fit the record's pair layout")
+            raise ValueError("widths do not fit the record layout")
         self.slot_word, self.slot_pos = lay
 
     @property
     def d(self):
         return self.T.shape[0]
 
+    @property
+    def tokens_per_record(self):
+        return 1 if self.pairing == "channels" else 2
 
-def build_tensor_params(mu_raw, lam, u, importance, r_words: int, max_bits: int) -> TensorParams:
+    @property
+    def record_len(self):
+        """32-bit words per record."""
+        return self.r_words * self.tokens_per_record
+
+
+def build_tensor_params(mu_raw, lam, u, importance, r_words: int, max_bits: int,
+                        pairing: str = "channels") -> TensorParams:
     widths_eig = water_fill_integer(importance, code_bits(r_words), max_bits)
     order = storage_order(widths_eig, importance)
     imp_st = np.asarray(importance)[order]
-    widths = fit_layout(widths_eig[order], imp_st, r_words)
+    if pairing == "channels":
+        widths = fit_layout(widths_eig[order], imp_st, r_words)
+    else:
+        widths = fit_token_layout(widths_eig[order], imp_st, r_words)
     T = u[:, order].T                                   # rows: storage channels
     mu_rot = T @ np.asarray(mu_raw, F64)
     sigma = np.sqrt(np.maximum(lam[order], 0.0))
     return TensorParams(T=T, mu=mu_rot, sigma=sigma, widths=widths, r_words=r_words,
-                        eigvals=lam[order], importance=imp_st)
+                        eigvals=lam[order], importance=imp_st, pairing=pairing)
 
 
 def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8):
@@ -276,8 +337,8 @@ def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8):
     lam_v, u_v = klt(s_v)
     imp_k = key_importance(lam_k, u_k, m_q)
     imp_v = value_importance(lam_v)
-    pk = build_tensor_params(mu_k, lam_k, u_k, imp_k, record_words(bits_k, d), max_bits)
-    pv = build_tensor_params(mu_v, lam_v, u_v, imp_v, record_words(bits_v, d), max_bits)
+    pk = build_tensor_params(mu_k, lam_k, u_k, imp_k, record_words(bits_k, d), max_bits, "channels")
+    pv = build_tensor_params(mu_v, lam_v, u_v, imp_v, record_words(bits_v, d), max_bits, "tokens")
     return pk, pv
 
 
@@ -326,46 +387,66 @@ def quantize(y32, p: TensorParams):
 # ----------------------------------------------------------------------------------------------------
 # 7. record packing
 # ----------------------------------------------------------------------------------------------------
-def _slot_of(p: TensorParams, j: int):
-    """(code word index within the record, bit shift) of storage channel j."""
-    k = j // 2
-    return 1 + int(p.slot_word[k]), int(p.slot_pos[k]) + HALF * (j % 2)
+def _slot_of(p: TensorParams, j: int, t_in_record: int = 0):
+    """(word index within the record, bit shift) of storage channel j of the record's token t_in_record."""
+    if p.pairing == "channels":
+        k = j // 2
+        return 1 + int(p.slot_word[k]), int(p.slot_pos[k]) + HALF * (j % 2)
+    return 2 + int(p.slot_word[j]), int(p.slot_pos[j]) + HALF * t_in_record
 
 
 def pack(z16, s16, codes, p: TensorParams):
-    """-> uint32 records [n, R_w]."""
+    """-> uint32 records [n_records, record_len]: one token per record for keys, two for values (a missing
+    second token leaves its words 0)."""
     codes = np.asarray(codes, np.int64)
     n, d = codes.shape
-    rec = np.zeros((n, p.r_words), np.uint64)
+    tpr = p.tokens_per_record
+    nrec = (n + tpr - 1) // tpr
+    rec = np.zeros((nrec, p.record_len), np.uint64)
     zb = np.asarray(z16, np.float16).view(np.uint16).astype(np.uint64)
     sb = np.asarray(s16, np.float16).view(np.uint16).astype(np.uint64)
-    rec[:, 0] = zb | (sb << np.uint64(16))
-    for j in range(d):
-        if int(p.widths[j]) == 0:
-            continue
-        w, sh = _slot_of(p, j)
-        rec[:, w] |= codes[:, j].astype(np.uint64) << np.uint64(sh)
+    for t in range(tpr):
+        rows = slice(t, n, tpr)
+        m = codes[rows].shape[0]
+        rec[:m, t] = zb[rows] | (sb[rows] << np.uint64(16))
+        for j in range(d):
+            if int(p.widths[j]) == 0:
+                continue
+            w, sh = _slot_of(p, j, t)
+            rec[:m, w] |= codes[rows, j].astype(np.uint64) << np.uint64(sh)
     return rec.astype(np.uint32)
 
 
 def unpack(rec, p: TensorParams):
-    """uint32 records [n, R_w] -> (z fp16 [n], s fp16 [n], codes int64 [n, d])."""
+    """uint32 records -> (z fp16 [n], s fp16 [n], codes int64 [n, d]) for every token slot of the records
+    (n = records x tokens per record)."""
     rec = np.asarray(rec, np.uint32).astype(np.uint64)
-    n = rec.shape[0]
-    z16 = (rec[:, 0] & np.uint64(0xFFFF)).astype(np.uint16).view(np.float16)
-    s16 = (rec[:, 0] >> np.uint64(16)).astype(np.uint16).view(np.float16)
+    tpr = p.tokens_per_record
+    nrec = rec.shape[0]
+    n = nrec * tpr
+    z16 = np.zeros(n, np.float16)
+    s16 = np.zeros(n, np.float16)
     codes = np.zeros((n, p.d), np.int64)
-    for j in range(p.d):
-        b = int(p.widths[j])
-        if b == 0:
-            continue
-        w, sh = _slot_of(p, j)
-        codes[:, j] = ((rec[:, w] >> np.uint64(sh)) & np.uint64((1 << b) - 1)).astype(np.int64)
+    for t in range(tpr):
+        z16[t::tpr] = (rec[:, t] & np.uint64(0xFFFF)).astype(np.uint16).view(np.float16)
+        s16[t::tpr] = (rec[:, t] >> np.uint64(16)).astype(np.uint16).view(np.float16)
+        for j in range(p.d):
+            b = int(p.widths[j])
+            if b == 0:
+                continue
+            w, sh = _slot_of(p, j, t)
+            codes[t::tpr, j] = ((rec[:, w] >> np.uint64(sh)) & np.uint64((1 << b) - 1)).astype(np.int64)
     return z16, s16, codes
 
 
+def records_for(rec, p: TensorParams, n_tokens: int):
+    """The leading records that hold the first n_tokens tokens."""
+    tpr = p.tokens_per_record
+    return np.asarray(rec)[:(n_tokens + tpr - 1) // tpr]
+
+
 def encode(x, p: TensorParams):
-    """Raw vectors x [n, d] -> records [n, R_w]."""
+    """Raw vectors x [n, d] -> records (one per token for keys, one per token pair for values)."""
     z, s, c = quantize(rotate(x, p), p)
     return pack(z, s, c, p)
 
@@ -385,7 +466,7 @@ def dequantize(z16, s16, codes, p: TensorParams):
 
 
 def reconstruct(rec, p: TensorParams):
-    """Records -> original-basis vectors x^ = T^T y^ [n, d] (fp64)."""
+    """Records -> original-basis vectors x^ = T^T y^ [n, d] (fp64), one row per token slot."""
     y = dequantize(*unpack(rec, p), p)
     return y @ p.T.astype(F64)
 
@@ -401,7 +482,7 @@ def attention(q, k, v, scale: float):
 
 
 def attend_decode(q, rec_k, rec_v, pk: TensorParams, pv: TensorParams, seq_len: int, scale: float):
-    """Decode attention of the g query heads q [g, d] over the first seq_len records of one KV head."""
-    kh = reconstruct(np.asarray(rec_k)[:seq_len], pk)
-    vh = reconstruct(np.asarray(rec_v)[:seq_len], pv)
+    """Decode attention of the g query heads q [g, d] over the first seq_len tokens of one KV head."""
+    kh = reconstruct(records_for(rec_k, pk, seq_len), pk)[:seq_len]
+    vh = reconstruct(records_for(rec_v, pv, seq_len), pv)[:seq_len]
     return attention(q, kh, vh, scale)

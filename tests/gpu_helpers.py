@@ -46,18 +46,24 @@ def set_index(b, h, Hkv, per_seq):
     return b * Hkv + h if per_seq else h
 
 
+def value_cache_shape(B, Hkv, T_cap, r_words):
+    """Value cache: two-token records of 2 R words, [B, Hkv, T_cap / 2, 2 R]."""
+    return (B, Hkv, T_cap // 2, 2 * r_words)
+
+
 def oracle_cache(k, v, sets, per_seq, T_cap=None):
-    """Oracle-encoded records for k, v [B, Hkv, T, d] (float64) -> numpy uint32 [B, Hkv, T_cap, R]."""
+    """Oracle-encoded records for k, v [B, Hkv, T, d] (float64) -> numpy uint32 key cache [B, Hkv, T_cap, R]
+    and value cache [B, Hkv, T_cap / 2, 2 R] (T_cap even)."""
     B, Hkv, T, d = k.shape
-    T_cap = T_cap or T
+    T_cap = T_cap or (T + T % 2)
     Rk, Rv = sets[0][0].r_words, sets[0][1].r_words
     rk = np.zeros((B, Hkv, T_cap, Rk), np.uint32)
-    rv = np.zeros((B, Hkv, T_cap, Rv), np.uint32)
+    rv = np.zeros(value_cache_shape(B, Hkv, T_cap, Rv), np.uint32)
     for b in range(B):
         for h in range(Hkv):
             pk, pv = sets[set_index(b, h, Hkv, per_seq)]
             rk[b, h, :T] = O.encode(k[b, h], pk)
-            rv[b, h, :T] = O.encode(v[b, h], pv)
+            rv[b, h, :(T + 1) // 2] = O.encode(v[b, h], pv)
     return rk, rv
 
 
@@ -66,7 +72,8 @@ def dev_u32(a):
 
 
 def run_decode(P, rk, rv, q_bits, seq_lens, Hq, per_seq, scale=None, T_cap=None):
-    """rk, rv: numpy uint32 [B, Hkv, T_cap, R]; q_bits: bf16 bits [B, Hq, d]; returns fp32 [B, Hq, d]."""
+    """rk: numpy uint32 [B, Hkv, T_cap, R]; rv: [B, Hkv, T_cap / 2, 2 R]; q_bits: bf16 bits [B, Hq, d];
+    returns fp32 [B, Hq, d]."""
     B, Hkv, Tc, _ = rk.shape
     d = 128
     scale = scale if scale is not None else 1.0 / math.sqrt(d)
@@ -104,12 +111,14 @@ def rel_l2_rows(a, b):
     return num / np.maximum(den, 1e-30)
 
 
-def code_diff(rec_a, rec_b, p):
+def code_diff(rec_a, rec_b, p, n=None):
     """Compare two record sets: (fraction of tokens whose z or s differ, max |dz| and |ds| in fp16 ulps,
     fraction of code entries that differ, max |code difference|, fraction of all record entries - z, s and
     the codes of the nonzero-width channels - that differ)."""
     za, sa, ca = O.unpack(rec_a, p)
     zb, sb, cb = O.unpack(rec_b, p)
+    if n is not None:
+        za, sa, ca, zb, sb, cb = za[:n], sa[:n], ca[:n], zb[:n], sb[:n], cb[:n]
     zi = lambda h: h.view(np.uint16).astype(np.int64)
     dz = np.abs(zi(za) - zi(zb))
     ds = np.abs(zi(sa) - zi(sb))

@@ -261,47 +261,84 @@ def pin_quantize_pack_golden():
         assert np.allclose(yh[0], _floats(yhat), atol=1e-12), (name, yh)
 
 
-def _words_needed(widths):
-    """Smallest record length whose pair layout holds the widths (first-fit), for test set-up."""
+def _words_needed(widths, pairing="channels"):
+    """Smallest record length whose layout holds the widths (first-fit), for test set-up."""
+    lay = O.slot_layout if pairing == "channels" else O.token_slot_layout
     r = 2
-    while O.slot_layout(widths, r) is None:
+    while lay(widths, r) is None:
         r += 1
     return r
 
 
 def pin_pack_roundtrip():
-    """Random widths 0..16 in any order: pack then unpack returns the codes, z and s; every bit outside the
-    channels' slots is zero; the slots of one code word never overlap."""
+    """Random widths 0..16 in any order, both layouts: pack then unpack returns the codes, z and s; every
+    bit outside the channels' slots is zero; no two channels share a bit."""
     rng = np.random.default_rng(6)
     for trial in range(40):
+        pairing = ("channels", "tokens")[trial % 2]
         d = int(rng.integers(1, 130))
         widths = rng.integers(0, 17, d)
-        r_words = _words_needed(widths) + int(rng.integers(0, 2))
-        p = _params_from_row(widths, np.zeros(d), np.ones(d), r_words)
+        r_words = _words_needed(widths, pairing) + int(rng.integers(0, 2))
+        p = O.TensorParams(T=np.eye(d), mu=np.zeros(d), sigma=np.ones(d), widths=widths, r_words=r_words,
+                           pairing=pairing)
         n = 7
         codes = np.stack([rng.integers(0, 2 ** int(b), n) if b > 0 else np.zeros(n, np.int64)
                           for b in widths], axis=1)
         z = rng.normal(size=n).astype(np.float16)
         s = np.abs(rng.normal(size=n)).astype(np.float16)
         rec = O.pack(z, s, codes, p)
+        assert rec.shape == ((n + p.tokens_per_record - 1) // p.tokens_per_record, p.record_len)
         z2, s2, c2 = O.unpack(rec, p)
-        assert np.array_equal(c2, codes)
-        assert np.array_equal(z2.view(np.uint16), z.view(np.uint16))
-        assert np.array_equal(s2.view(np.uint16), s.view(np.uint16))
-        owned = np.zeros(r_words, np.uint64)
-        for j in range(d):
-            b = int(widths[j])
-            if b == 0:
-                continue
-            k = j // 2
-            w = 1 + int(p.slot_word[k])
-            sh = int(p.slot_pos[k]) + 16 * (j % 2)
-            assert int(p.slot_pos[k]) + b <= 16
-            m = np.uint64(((1 << b) - 1) << sh)
-            assert (owned[w] & m) == 0            # no two channels share a bit
-            owned[w] |= m
-        for w in range(1, r_words):
+        assert np.array_equal(c2[:n], codes)
+        assert np.array_equal(z2[:n].view(np.uint16), z.view(np.uint16))
+        assert np.array_equal(s2[:n].view(np.uint16), s.view(np.uint16))
+        owned = np.zeros(p.record_len, np.uint64)
+        for t in range(p.tokens_per_record):
+            owned[t] = np.uint64(0xFFFFFFFF)
+            for j in range(d):
+                b = int(widths[j])
+                if b == 0:
+                    continue
+                if pairing == "channels":
+                    k = j // 2
+                    w, r0, hi = 1 + int(p.slot_word[k]), int(p.slot_pos[k]), j % 2
+                else:
+                    w, r0, hi = 2 + int(p.slot_word[j]), int(p.slot_pos[j]), t
+                assert r0 + b <= 16
+                m = np.uint64(((1 << b) - 1) << (r0 + 16 * hi))
+                assert (owned[w] & m) == 0            # no two channels share a bit
+                owned[w] |= m
+        for w in range(p.tokens_per_record, p.record_len):
             assert np.all((rec[:, w].astype(np.uint64) & ~owned[w] & np.uint64(0xFFFFFFFF)) == 0)
+
+
+def pin_token_pack_golden():
+    """Hand-computed value records in the token-pair layout (tests/golden/quantize_pack_token_pairs.txt)."""
+    for name, widths, mu, sigma, ys, rw, codes, recs, yhats in read_golden("quantize_pack_token_pairs.txt"):
+        w = _ints(widths)
+        p = O.TensorParams(T=np.eye(len(w)), mu=_floats(mu), sigma=_floats(sigma), widths=w, r_words=int(rw),
+                           pairing="tokens")
+        y32 = np.array([_floats(r) for r in ys.split(";")], np.float32)
+        z, s_, c = O.quantize(y32, p)
+        assert np.array_equal(c, np.array([_ints(r) for r in codes.split(";")])), (name, c)
+        rec = O.pack(z, s_, c, p)
+        want = [[int(x, 16) for x in r.split()] for r in recs.split(";")]
+        assert rec.astype(np.int64).tolist() == want, (name, [[hex(x) for x in r] for r in rec])
+        z2, s2, c2 = O.unpack(rec, p)
+        n = y32.shape[0]
+        assert np.array_equal(c2[:n], c)
+        yh = O.dequantize(z2[:n], s2[:n], c2[:n], p)
+        assert np.allclose(yh, np.array([_floats(r) for r in yhats.split(";")]), atol=1e-12), (name, yh)
+
+
+def pin_token_layout_fit_golden():
+    """Hand-solved fits of value widths to the token-pair layout (tests/golden/layout_fit_token_pairs.txt)."""
+    for widths, imp, rw, fitted, words, pos in read_golden("layout_fit_token_pairs.txt"):
+        f = O.fit_token_layout(_ints(widths), _floats(imp), int(rw))
+        assert f.tolist() == _ints(fitted).tolist(), (widths, f)
+        lay = O.token_slot_layout(f, int(rw))
+        assert lay is not None
+        assert lay[0].tolist() == _ints(words).tolist() and lay[1].tolist() == _ints(pos).tolist(), lay
 
 
 def pin_layout_fit_golden():
@@ -315,26 +352,33 @@ def pin_layout_fit_golden():
 
 
 def pin_layout_fit_properties():
-    """On the workloads' calibrations: the fitted widths fit the record, both channels of a pair share one
-    width no larger than the pair's wider water-filling width, and the white-noise distortion
-    sum_j lambda_j 4^-b_j grows by at most 2% over the unconstrained integer allocation."""
+    """On the workloads' calibrations (their own calibration sizes; the batched workload calibrates on a
+    sequence's first 1024 tokens): the fitted widths fit the record (key: channel pairs sharing one width no
+    larger than the pair's wider water-filling width; value: each channel no wider than its water-filling
+    width), and the white-noise distortion sum_j lambda_j 4^-b_j grows by at most 2% over the unconstrained
+    integer allocation."""
     worst = 1.0
     for name, bits in (("tiny", 2.75), ("llama_long_128k", 1.33), ("qwen_batched_8k", 2.0),
-                       ("qwen_batched_8k", 4.0)):
-        L = synth.make_layer(synth.WORKLOADS[name], T=64, B=1, steps=1)
+                       ("qwen_batched_8k", 3.0), ("qwen_batched_8k", 4.0)):
+        L = synth.make_layer(synth.WORKLOADS[name], T=1024, B=1, steps=1)
         mu_k, s_k, mu_v, s_v, m_q = O.calib_statistics(L.calib_k[0], L.calib_v[0], L.calib_q[0])
-        for lam_u, imp_fn in ((O.klt(s_k), lambda l, u: O.key_importance(l, u, m_q)),
-                              (O.klt(s_v), lambda l, u: O.value_importance(l))):
+        for lam_u, imp_fn, pairing in ((O.klt(s_k), lambda l, u: O.key_importance(l, u, m_q), "channels"),
+                                       (O.klt(s_v), lambda l, u: O.value_importance(l), "tokens")):
             lam, u = lam_u
             imp = imp_fn(lam, u)
             r = O.record_words(bits, 128)
             b = O.water_fill_integer(imp, O.code_bits(r), 8)
             order = O.storage_order(b, imp)
             b, imp = b[order], np.asarray(imp)[order]
-            f = O.fit_layout(b, imp, r)
-            assert O.slot_layout(f, r) is not None
-            assert np.array_equal(f[0::2], f[1::2])
-            assert np.all(f[0::2] <= np.maximum(b[0::2], b[1::2]))
+            if pairing == "channels":
+                f = O.fit_layout(b, imp, r)
+                assert O.slot_layout(f, r) is not None
+                assert np.array_equal(f[0::2], f[1::2])
+                assert np.all(f[0::2] <= np.maximum(b[0::2], b[1::2]))
+            else:
+                f = O.fit_token_layout(b, imp, r)
+                assert O.token_slot_layout(f, r) is not None
+                assert np.all(f <= b)
             assert f.sum() <= O.code_bits(r)
             d0 = float(np.sum(imp * 4.0 ** (-b.astype(np.float64))))
             d1 = float(np.sum(imp * 4.0 ** (-f.astype(np.float64))))
@@ -390,30 +434,42 @@ def pin_half_conversion():
 
 # --- decode ------------------------------------------------------------------------------------------
 def brute_force_decode(q, rec_k, rec_v, pk, pv, seq_len, scale):
-    """Explicit per-element loops: unpack bits, dequantise, rotate back, softmax, weighted sum."""
-    def rec_to_vec(rec, p):
+    """Explicit per-element loops: unpack bits, dequantise, rotate back, softmax, weighted sum. Key records
+    hold one token with channel pairs sharing slots; value records hold two tokens, one slot per channel."""
+    def rec_to_vec(rec, p, t_in=0):
         d = p.d
-        word0 = int(rec[0])
+        two = p.pairing == "tokens"
+        word0 = int(rec[t_in])
         z = float(np.array([word0 & 0xFFFF], np.uint16).view(np.float16)[0])
         s = float(np.array([word0 >> 16], np.uint16).view(np.float16)[0])
-        # pair slots, placed first-fit by hand: pair k = channels (2k, 2k+1), slot width = the wider one
-        free = [16] * (len(rec) - 1)
+        first_code = 2 if two else 1
+        free = [16] * (len(rec) - first_code)
         where = {}
-        for k in range(d // 2):
-            sw = max(int(p.widths[2 * k]), int(p.widths[2 * k + 1]))
-            if sw == 0:
-                continue
-            u = next(i for i in range(len(free)) if free[i] >= sw)
-            where[k] = (u, 16 - free[u])
-            free[u] -= sw
+        if two:      # one slot per channel, first-fit by hand
+            for j in range(d):
+                b = int(p.widths[j])
+                if b == 0:
+                    continue
+                u = next(i for i in range(len(free)) if free[i] >= b)
+                where[j] = (u, 16 - free[u], 16 * t_in)
+                free[u] -= b
+        else:        # pair k = channels (2k, 2k+1), slot width = the wider one
+            for k in range(d // 2):
+                sw = max(int(p.widths[2 * k]), int(p.widths[2 * k + 1]))
+                if sw == 0:
+                    continue
+                u = next(i for i in range(len(free)) if free[i] >= sw)
+                where[2 * k] = (u, 16 - free[u], 0)
+                where[2 * k + 1] = (u, 16 - free[u], 16)
+                free[u] -= sw
         y = []
         for j in range(d):
             b = int(p.widths[j])
             if b == 0:
                 y.append(float(p.mu[j]))
                 continue
-            u, r = where[j // 2]
-            c = (int(rec[1 + u]) >> (r + 16 * (j % 2))) & ((1 << b) - 1)
+            u, r, half = where[j]
+            c = (int(rec[first_code + u]) >> (r + half)) & ((1 << b) - 1)
             y.append(float(p.mu[j]) + float(p.sigma[j]) * (z + (c + 0.5) * s / (2 ** b)))
         x = []
         for col in range(d):
@@ -423,8 +479,13 @@ def brute_force_decode(q, rec_k, rec_v, pk, pv, seq_len, scale):
             x.append(acc)
         return x
 
-    ks = [rec_to_vec(rec_k[t], pk) for t in range(seq_len)]
-    vs = [rec_to_vec(rec_v[t], pv) for t in range(seq_len)]
+    def token_vec(recs, p, t):
+        if p.pairing == "tokens":
+            return rec_to_vec(recs[t // 2], p, t % 2)
+        return rec_to_vec(recs[t], p)
+
+    ks = [token_vec(rec_k, pk, t) for t in range(seq_len)]
+    vs = [token_vec(rec_v, pv, t) for t in range(seq_len)]
     out = []
     for h in range(q.shape[0]):
         logits = [scale * sum(float(q[h, i]) * ks[t][i] for i in range(len(ks[t]))) for t in range(seq_len)]
@@ -456,11 +517,15 @@ def pin_calibrate_structure():
     L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
     ck, cv, cq = L.calib_k[0], L.calib_v[0], L.calib_q[0]
     pk, pv = O.calibrate(ck, cv, cq, 2.75, 2.75)
+    assert pk.pairing == "channels" and pv.pairing == "tokens"
     for p, x in ((pk, ck), (pv, cv)):
         t = p.T.astype(np.float64)
         assert np.linalg.norm(t @ t.T - np.eye(128)) < 1e-5
-        assert np.array_equal(p.widths[0::2], p.widths[1::2])
+        if p.pairing == "channels":
+            assert np.array_equal(p.widths[0::2], p.widths[1::2])
+            assert O.slot_layout(p.widths, 11) is not None
+        else:
+            assert O.token_slot_layout(p.widths, 11) is not None
         assert O.code_bits(11) - 32 < p.widths.sum() <= O.code_bits(11)
-        assert O.slot_layout(p.widths, 11) is not None
         assert np.allclose(p.mu, t @ np.asarray(x, np.float64).mean(0), atol=1e-5)
         assert np.allclose(p.sigma.astype(np.float64) ** 2, p.eigvals, rtol=1e-5)

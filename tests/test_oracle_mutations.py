@@ -9,7 +9,7 @@ from oracle import kvtc_oracle as O
 _orig = {name: getattr(O, name) for name in
          ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
           "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat",
-          "slot_layout", "fit_layout"]}
+          "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout"]}
 
 
 def _klt_transposed(sigma):
@@ -168,6 +168,44 @@ def _fit_no_promotion(widths, importance, r_words):
     return np.minimum(f, b)
 
 
+def _token_layout_next_fit(widths, r_words):
+    w = np.asarray(widths, np.int64)
+    word = np.full(w.shape[0], -1, np.int64)
+    pos = np.full(w.shape[0], -1, np.int64)
+    u, used = 0, 0
+    for j in range(w.shape[0]):
+        b = int(w[j])
+        if b == 0:
+            continue
+        if used + b > 16:
+            u, used = u + 1, 0
+        if u >= 2 * r_words - 2:
+            return None
+        word[j], pos[j] = u, used
+        used += b
+    return word, pos
+
+
+def _token_fit_ties_to_earlier(widths, importance, r_words):
+    w = [int(x) for x in np.asarray(widths, np.int64)]
+    lam = [float(x) for x in np.asarray(importance, np.float64)]
+    while O.token_slot_layout(w, r_words) is None:
+        _, j = min((O.fit_cost_key(lam[j], w[j]), j) for j in range(len(w)) if w[j] > 0)
+        w[j] -= 1
+    return np.asarray(w, np.int64)
+
+
+def _token_pack_swapped_halves(z16, s16, codes, p):
+    rec = _orig["pack"](z16, s16, codes, p)
+    if p.pairing != "tokens":
+        return rec
+    out = rec.copy()
+    for w in range(2, rec.shape[1]):
+        x = rec[:, w].astype(np.uint64)
+        out[:, w] = (((x & np.uint64(0xFFFF)) << np.uint64(16)) | (x >> np.uint64(16))).astype(np.uint32)
+    return out
+
+
 MUTATIONS = [
     ("klt", _klt_transposed, P.pin_klt_known_spectrum),
     ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
@@ -188,6 +226,9 @@ MUTATIONS = [
     ("fit_layout", _fit_ties_to_earlier, P.pin_layout_fit_golden),
     ("fit_layout", _fit_cost_ignores_width, P.pin_layout_fit_golden),
     ("fit_layout", _fit_no_promotion, P.pin_layout_fit_golden),
+    ("token_slot_layout", _token_layout_next_fit, P.pin_token_layout_fit_golden),
+    ("fit_token_layout", _token_fit_ties_to_earlier, P.pin_token_layout_fit_golden),
+    ("pack", _token_pack_swapped_halves, P.pin_token_pack_golden),
 ]
 
 

@@ -63,6 +63,14 @@ def test_layout_fit_golden():
     P.pin_layout_fit_golden()
 
 
+def test_token_pack_golden():
+    P.pin_token_pack_golden()
+
+
+def test_token_layout_fit_golden():
+    P.pin_token_layout_fit_golden()
+
+
 def test_layout_fit_properties():
     worst = P.pin_layout_fit_properties()
     print(f"worst distortion ratio of the fitted layout vs the unconstrained allocation: {worst:.4f}")

@@ -65,7 +65,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     B, Hkv, T_cap = 256, w.Hkv, 64
     assert kvtc.kv_decode_workspace_bytes(P, B, Hkv, w.Hq, T_cap) > kvtc.NOALLOC_SCRATCH_BYTES
     tk = torch.zeros((B, Hkv, T_cap, P.record_words(0)), dtype=torch.int32, device="cuda")
-    tv = torch.zeros((B, Hkv, T_cap, P.record_words(1)), dtype=torch.int32, device="cuda")
+    tv = torch.zeros(G.value_cache_shape(B, Hkv, T_cap, P.record_words(1)), dtype=torch.int32, device="cuda")
     cache = kvtc.make_cache(tk, tv, B, Hkv, T_cap)
     q = torch.zeros((B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
     sl = torch.full((B,), T_cap, dtype=torch.int32, device="cuda")

@@ -246,6 +246,25 @@ bool kvtc::slot_layout(const int32_t* w, int d, int rw, int* word, int* pos) {
   return true;
 }
 
+// Value records hold two tokens: channel j has one slot of width b_j at the same bit of the low half (earlier
+// token) and the high half (later token) of one of the 2 rw - 2 code words; slots are placed first-fit in
+// storage order.
+bool kvtc::token_slot_layout(const int32_t* w, int d, int rw, int* word, int* pos) {
+  int used[2 * MAX_RW] = {0};
+  const int nw = 2 * rw - 2;
+  for (int j = 0; j < d; ++j) {
+    word[j] = pos[j] = -1;
+    if (w[j] == 0) continue;
+    int u = 0;
+    while (u < nw && used[u] + w[j] > 16) ++u;
+    if (u >= nw) return false;
+    word[j] = u;
+    pos[j] = used[u];
+    used[u] += w[j];
+  }
+  return true;
+}
+
 // Order of the cost 3 (lambda_2k + lambda_2k+1) 4^-w of taking one bit from a pair: log2 at 1e-9
 // resolution (less the common log2 3), so that costs equal in exact arithmetic compare equal.
 static long long fit_cost_key(double pair_importance, int width) {
@@ -283,6 +302,25 @@ static void fit_layout(int32_t* w, const double* imp, int d, int rw) {
   for (int j = 0; j < d; ++j) w[j] = wide[j];
 }
 
+// Take single bits from the cheapest channel (ties: the later channel) until the token-pair layout holds.
+static void fit_token_layout(int32_t* w, const double* imp, int d, int rw) {
+  std::vector<int> word(d), pos(d);
+  while (!kvtc::token_slot_layout(w, d, rw, word.data(), pos.data())) {
+    int best = -1;
+    long long best_key = 0;
+    for (int j = 0; j < d; ++j) {
+      if (w[j] <= 0) continue;
+      const long long key = fit_cost_key(imp[j], w[j]);
+      if (best < 0 || key <= best_key) {
+        best = j;
+        best_key = key;
+      }
+    }
+    if (best < 0) break;
+    --w[best];
+  }
+}
+
 static void build_tensor(const std::vector<double>& mu_raw, const std::vector<double>& lam,
                          const std::vector<double>& U, const std::vector<double>& imp, int rw, int bmax,
                          int d, SetResult& r, int t) {
@@ -301,7 +339,10 @@ static void build_tensor(const std::vector<double>& mu_raw, const std::vector<do
     ws[j] = w[order[j]];
     imps[j] = imp[order[j]];
   }
-  fit_layout(ws.data(), imps.data(), d, rw);
+  if (t == 0)
+    fit_layout(ws.data(), imps.data(), d, rw);  // keys: channel pairs share slots
+  else
+    fit_token_layout(ws.data(), imps.data(), d, rw);  // values: token pairs share slots
   r.T[t].resize((size_t)d * d);
   r.mu[t].resize(d);
   r.sigma[t].resize(d);
@@ -458,11 +499,12 @@ extern "C" kv_status kv_params_from_arrays(int d, int n_sets, const float* T_k, 
         }
         p->eig[t][i] = (double)p->sigma[t][i] * p->sigma[t][i];
       }
-      int word[D / 2], pos[D / 2];
-      if (!kvtc::slot_layout(&p->widths[t][(size_t)s * d], d, rws[t], word, pos)) {
+      int word[D], pos[D];
+      const int32_t* wt = &p->widths[t][(size_t)s * d];
+      if (!(t == 0 ? kvtc::slot_layout(wt, d, rws[t], word, pos) : kvtc::token_slot_layout(wt, d, rws[t], word, pos))) {
         delete p;
-        KV_REQUIRE(false, KV_ERR_BUDGET, "set %d tensor %d: widths do not fit the %d-word record's pair layout", s,
-                   t, rws[t]);
+        KV_REQUIRE(false, KV_ERR_BUDGET, "set %d tensor %d: widths do not fit the %d-word record layout", s, t,
+                   rws[t]);
       }
     }
   }
@@ -486,8 +528,9 @@ static float bf16_to_f32(uint16_t h) {
   return f;
 }
 
-// Slot descriptor of pair k: code word u (0-based within the code words), bit r, widths of its two channels:
-//   u | r << 8 | b_2k << 16 | b_2k+1 << 24   (all zero for an empty slot).
+// Slot descriptor: code word u (0-based within the record's code words), bit r, width of the low-half and of
+// the high-half code: u | r << 8 | b_lo << 16 | b_hi << 24 (all zero for an empty slot). Key slots hold the
+// channel pair (2k, 2k+1) of one token; value slots hold channel j of the record's two tokens.
 static uint32_t slot_descriptor(int u, int r, int b0, int b1) {
   if (u < 0 || (b0 == 0 && b1 == 0)) return 0u;
   return (uint32_t)u | ((uint32_t)r << 8) | ((uint32_t)b0 << 16) | ((uint32_t)b1 << 24);
@@ -527,7 +570,7 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     pws[t] = reserve((size_t)S * d * 4);
     pw[t] = reserve((size_t)S * d);
     pnz[t] = reserve((size_t)S * 4);
-    psl[t] = reserve((size_t)S * (d / 2) * 4);
+    psl[t] = reserve((size_t)S * d * 4);
   }
   for (int t = 0; t < 2; ++t) {
     float* T = (float*)&blob[pT[t].off];
@@ -589,10 +632,16 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
         }
         wsum[(size_t)s * d + k] = (float)wacc;
       }
-      int word[D / 2], pos[D / 2];
-      kvtc::slot_layout(wv.data(), d, p->r_words[t], word, pos);
-      for (int k = 0; k < d / 2; ++k)
-        sl[(size_t)s * (d / 2) + k] = slot_descriptor(word[k], pos[k], wv[2 * k], wv[2 * k + 1]);
+      int word[D], pos[D];
+      uint32_t* sls = sl + (size_t)s * d;
+      if (t == 0) {  // key slots: one per channel pair (entries d/2 .. d-1 unused)
+        kvtc::slot_layout(wv.data(), d, p->r_words[t], word, pos);
+        for (int k = 0; k < d / 2; ++k) sls[k] = slot_descriptor(word[k], pos[k], wv[2 * k], wv[2 * k + 1]);
+        for (int k = d / 2; k < d; ++k) sls[k] = 0u;
+      } else {       // value slots: one per channel, the same width for both tokens of a record
+        kvtc::token_slot_layout(wv.data(), d, p->r_words[t], word, pos);
+        for (int j = 0; j < d; ++j) sls[j] = slot_descriptor(word[j], pos[j], wv[j], wv[j]);
+      }
     }
   }
   void* dblob = nullptr;

@@ -33,7 +33,9 @@ struct TensorDev {
   const float* wsum;               // [S][D]  sum over b_j > 0 of T[j][k] sigma_j
   const uint8_t* widths;           // [S][D]
   const int32_t* nz;               // [S]     1 + last storage channel with width > 0
-  const uint32_t* slots;           // [S][D/2] pair slots: code word | bit << 8 | b_2k << 16 | b_2k+1 << 24
+  const uint32_t* slots;           // [S][D] slots: code word | bit << 8 | b_lo << 16 | b_hi << 24; keys: entry k =
+                                   // channel pair (2k, 2k+1) of a one-token record (k < D/2); values: entry j =
+                                   // channel j of a two-token record (code words start at record word 2)
   int r_words;                     // record words per token (same for every set)
 };
 
@@ -45,6 +47,8 @@ struct ParamsDev {
 // First-fit placement of the pair slots of widths w[d] in a record of rw words (word/pos [d/2], -1 = empty);
 // false when a slot finds no room.
 bool slot_layout(const int32_t* w, int d, int rw, int* word, int* pos);
+// First-fit placement of single channels in a two-token value record (word/pos [d]).
+bool token_slot_layout(const int32_t* w, int d, int rw, int* word, int* pos);
 
 // host-side error message of the calling thread
 void set_error(const char* fmt, ...);

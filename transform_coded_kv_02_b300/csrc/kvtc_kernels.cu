@@ -74,7 +74,7 @@ struct EncArgs {
 
 template <bool BF16>
 __global__ void __launch_bounds__(256) encode_warp_kernel(ParamsDev P, EncArgs a) {
-  __shared__ uint32_t rec_s[8][MAX_RW + 3];
+  __shared__ uint32_t rec_s[8][2 * MAX_RW + 4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long per_tensor = (long long)a.B * a.Hkv * a.t_new;
   const long long idx = (long long)blockIdx.x * 8 + warp;
@@ -120,11 +120,13 @@ __global__ void __launch_bounds__(256) encode_warp_kernel(ParamsDev P, EncArgs a
   const long long pos = a.dst_pos[b] + t;
   uint32_t* out = nullptr;
   if (pos >= 0 && pos < a.T_cap) {
-    out = a.dst[tensor] + (((size_t)b * a.Hkv + h) * (size_t)a.T_cap + (size_t)pos) * td.r_words;
+    const size_t bh = (size_t)b * a.Hkv + h;
+    out = tensor == 0 ? a.dst[0] + (bh * (size_t)a.T_cap + (size_t)pos) * td.r_words
+                      : a.dst[1] + (bh * (size_t)(a.T_cap / 2) + (size_t)(pos >> 1)) * 2 * td.r_words;
   } else if (lane == 0) {
     atomicOr(&g_status, ST_BAD_INDEX);
   }
-  quantize_pack_warp(td, set, y, lane, rec_s[warp], out);
+  quantize_pack_warp(td, set, y, lane, rec_s[warp], out, tensor == 1, (int)(pos & 1));
 }
 
 kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, const void* v, int dtype, int B,
@@ -159,13 +161,11 @@ kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, co
 constexpr int PSTR = 132;          // floats per (split, head) partial: m, l, z, -, A[128]
 constexpr int DWARPS = 4;          // consumer warps per decode CTA
 constexpr int DT = 16 * DWARPS;    // tokens per ring stage (16 per consumer warp)
-constexpr int DTHREADS = 32 * (DWARPS + 1);
+constexpr int DTHREADS = 32 * DWARPS;   // all warps consume; lane 0 of warp 0 also issues the copies
 constexpr int RING_BUDGET = 48 * 1024;
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_SPLITS = 256;
 constexpr int TAIL_RESERVE = MAX_SPLITS * MAX_G * 4 + 4 * MAX_G * 4;  // split weights, head state
-constexpr int UNPACK_T = 64;       // tokens per tile of the parity unpacker
-constexpr int KC_PITCH_MAX = 272;  // bytes per token row of an unpacked tile (odd multiple of 16)
 
 struct DecArgs {
   const uint32_t* rec[2];
@@ -287,26 +287,19 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs 
 }
 
 // ---- split-K decode ----------------------------------------------------------------------------------
-__host__ __device__ __forceinline__ int unpacked_pitch(int nblk16) {  // bytes, odd multiple of 16
-  return ((nblk16 * 2) | 1) * 16;
-}
-
 struct DecSmem {  // byte offsets into the dynamic shared memory of decode_kernel
-  uint32_t stage_bytes, tiles, warp_tile, ps, bars, epi_ws, epi_merged, tail_reserve, total;
+  uint32_t stage_bytes, ps, epi_ws, epi_merged, tail_reserve, total;
 };
 
 __host__ __device__ __forceinline__ uint32_t align128u(uint32_t x) { return (x + 127u) & ~127u; }
 
-// main loop: ring | per-warp unpacked tiles | per-warp P tiles
-// epilogue (ring and tiles dead): T'_V rows [0, 64 KB) | per-warp partials | merged partial
+// main loop: ring | per-warp P tiles
+// epilogue (ring dead): T'_V rows [0, 64 KB) | per-warp partials | merged partial
 // tail: split partial chunks from 0 | per-split weights and per-head state in the reserve at the end
-__host__ __device__ inline DecSmem decode_smem(int RK, int RV, int nkb, int nmb, int stages, int nb) {
+__host__ __device__ inline DecSmem decode_smem(int RK, int RV, int stages, int nb) {
   DecSmem s;
   s.stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
-  s.tiles = align128u(stages * s.stage_bytes);
-  s.warp_tile = 16u * (uint32_t)(unpacked_pitch(nkb) + unpacked_pitch(nmb));
-  s.ps = align128u(s.tiles + DWARPS * s.warp_tile);
-  s.bars = 0;
+  s.ps = align128u(stages * s.stage_bytes);
   const uint32_t main_end = s.ps + DWARPS * 16u * 8u * nb * 2u;
   s.epi_ws = D * D * 4u;
   s.epi_merged = s.epi_ws + DWARPS * 8u * PSTR * 4u;
@@ -316,7 +309,21 @@ __host__ __device__ inline DecSmem decode_smem(int RK, int RV, int nkb, int nmb,
   return s;
 }
 
-template <int NB>
+__host__ __device__ constexpr int ring_stages_for(int RK, int RV) {
+  return (RING_BUDGET / (DT * (RK + RV) * 4)) > MAX_STAGES ? MAX_STAGES
+         : (RING_BUDGET / (DT * (RK + RV) * 4)) < 2      ? 2
+                                                          : RING_BUDGET / (DT * (RK + RV) * 4);
+}
+
+// plain shared-memory word load (byte offset into the dynamic region): the compiler is free to schedule it
+template <class T>
+__device__ __forceinline__ uint32_t ldsw(const T* base, uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(base) + off);
+}
+
+// RT > 0: keys and values both use records of RT words; the ring stage size and count and the offsets between
+// a lane's two tokens (two records) are compile-time, so each staged-record address is one add away.
+template <int NB, int RT>
 __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   // barriers live outside the dynamic region, which the epilogue and the tail reuse wholesale
@@ -327,12 +334,14 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   const int set = a.per_seq ? bh : kh;
   const TensorDev& TK = P.t[0];
   const TensorDev& TV = P.t[1];
-  const int RK = TK.r_words, RV = TV.r_words, NS = a.stages, g = a.g;
+  const int RK = RT ? RT : TK.r_words, RV = RT ? RT : TV.r_words;
+  constexpr int NS_CT = RT ? ring_stages_for(RT, RT) : 0;
+  const int NS = RT ? NS_CT : a.stages, g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   const int nzK = TK.nz[set], nzV = TV.nz[set];
   const int nkb = (nzK + 15) >> 4, nmb = (nzV + 15) >> 4;
-  const int pitchK = unpacked_pitch(nkb), pitchV = unpacked_pitch(nmb);
-  const DecSmem L = decode_smem(RK, RV, nkb, nmb, NS, NB);
+  const DecSmem L = decode_smem(RK, RV, NS, NB);
+  const uint32_t stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
   uint64_t* tbar = &tbar_s;
 
   const long long Lseq = min((long long)a.seq_lens[b], a.T_cap);
@@ -365,61 +374,77 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
       for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] = 0.f;
   }
 
-  if (warp == DWARPS) {
-    // ================= producer: one elected lane streams record tiles into the ring =================
-    if (lane == 0) {
-      if (split == 0 && nzV > 0)  // the last CTA's inverse rotation reads T_V rows: warm L2 now
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(TV.T + (size_t)set * D * D),
-                     "r"((uint32_t)nzV * D * 4)
-                     : "memory");
-      const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
-      const uint32_t* vrec = a.rec[1] + (size_t)bh * a.T_cap * RV;
-      int i = 0;
-      for (; i < ntiles; ++i) {
-        const int s = i % NS;
-        if (i >= NS && !mbar_wait_bounded(smem_u32(&empty[s]), (uint32_t)((i / NS - 1) & 1), a.wait_ns)) {
-          s_abort = 1;
-          break;
+  // ---- record tiles stream into the ring by bulk copies that lane 0 of warp 0 issues ----
+  const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
+  const uint32_t* vrec = a.rec[1] + (size_t)bh * a.T_cap * RV;  // two-token records: same bytes per token
+  const bool issuer = tid == 0;
+  int next_issue = 0;  // meaningful in the issuing thread only
+  auto issue_tile = [&](int i) {
+    const int s = i % NS;
+    const long long tb = t0 + (long long)i * DT;
+    long long n = min((long long)DT, t1 - tb);
+    n = min((n + 3) & ~3LL, a.T_cap - tb);
+    const uint32_t kbytes = (uint32_t)(n * RK * 4), vbytes = (uint32_t)(n * RV * 4);
+    const uint32_t bar = smem_u32(&full[s]);
+    const uint32_t dst = smem_u32(smem + (size_t)s * stage_bytes);
+    mbar_expect_tx(bar, kbytes + vbytes);
+    bulk_g2s(dst, krec + tb * RK, kbytes, bar);
+    bulk_g2s(dst + DT * RK * 4, vrec + tb * RV, vbytes, bar);
+  };
+  // issue tiles up to `upto`; blocking: wait for each ring slot to be released, else stop at the first busy one
+  auto issue_until = [&](int upto, bool blocking) {
+    while (next_issue <= upto && next_issue < ntiles) {
+      if (next_issue >= NS) {
+        const uint32_t eb = smem_u32(&empty[next_issue % NS]), par = (uint32_t)((next_issue / NS - 1) & 1);
+        if (blocking) {
+          if (!mbar_wait_bounded(eb, par, a.wait_ns)) {
+            s_abort = 1;
+            return;
+          }
+        } else if (!mbar_test(eb, par)) {
+          return;
         }
-        if (*(volatile int*)&s_abort) break;
-        const long long tb = t0 + (long long)i * DT;
-        long long n = min((long long)DT, t1 - tb);
-        n = min((n + 3) & ~3LL, a.T_cap - tb);
-        const uint32_t kb = (uint32_t)(n * RK * 4), vb = (uint32_t)(n * RV * 4);
-        const uint32_t bar = smem_u32(&full[s]);
-        const uint32_t dst = smem_u32(smem + (size_t)s * L.stage_bytes);
-        mbar_expect_tx(bar, kb + vb);
-        bulk_g2s(dst, krec + tb * RK, kb, bar);
-        bulk_g2s(dst + DT * RK * 4, vrec + tb * RV, vb, bar);
       }
-      s_issued = i;
+      issue_tile(next_issue);
+      ++next_issue;
     }
-  } else {
+  };
+  if (issuer) {
+    if (split == 0 && nzV > 0)  // every split's epilogue reads the scaled T_V rows: warm L2 now
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(TV.Tsc + (size_t)set * D * D),
+                   "r"((uint32_t)nzV * D * 4)
+                   : "memory");
+    issue_until(NS - 1, false);
+  }
+  {
     // ================= consumers: warp w owns tokens [16w, 16w + 16) of every tile =================
-    // unpack task of this lane: group gi (4 slot pairs = 8 channels) of token sub + TPP * p
-    const int GK = 2 * nkb, G = 2 * (nkb + nmb);
-    const int GP = G <= 4 ? 4 : G <= 8 ? 8 : G <= 16 ? 16 : 32;
-    const int TPP = 32 / GP, passes = 16 / TPP;
-    const int gi = lane & (GP - 1), sub = lane / GP;
-    const bool active = gi < G;
-    const bool isV = gi >= GK;
-    const int grp = isV ? gi - GK : gi;
-    uint32_t wo[4] = {0u, 0u, 0u, 0u}, sh[4] = {0u, 0u, 0u, 0u}, mk[4] = {0u, 0u, 0u, 0u};
-    if (active) {
-      const uint32_t* sl = (isV ? TV.slots : TK.slots) + (size_t)set * (D / 2) + 4 * grp;
+    // Codes go from the staged records straight into MMA operand registers.
+    //  keys, logits A operand (16 tokens x 16 channels of block kb): key slot 8kb + tig holds channels
+    //    (16kb + 2tig, +1), slot 8kb + 4 + tig channels (16kb + 8 + 2tig, +1); rows gid, gid + 8 = tokens gid,
+    //    gid + 8 of this warp.
+    //  values, P.V A operand (16 channels x 16 tokens): value slot 16mb + gid (+ 8) holds that channel for the
+    //    two tokens of a value record; this warp's records tig and tig + 4 hold tokens (2tig, 2tig+1) and
+    //    (2tig + 8, 2tig + 9).
+    const uint32_t krow = (uint32_t)(16 * warp + gid) * RK * 4;
+    const uint32_t vrow = (uint32_t)DT * RK * 4 + (uint32_t)(8 * warp + tig) * 2 * RV * 4;
+    const uint32_t kstep = 8u * RK * 4, vstep = 4u * 2 * RV * 4;
+    uint32_t ka[8][2], ks[8][2], km[8][2], va[8][2], vsh[8][2], vm[8][2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t desc = __ldg(sl + i);
-        wo[i] = 4u * (1u + (desc & 255u));
-        sh[i] = (desc >> 8) & 255u;
-        mk[i] = slot_mask(desc);
+    for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t dk = kb < nkb ? __ldg(TK.slots + (size_t)set * D + 8 * kb + 4 * i + tig) : 0u;
+        ka[kb][i] = krow + 4u * (1u + (dk & 255u));
+        ks[kb][i] = (dk >> 8) & 255u;
+        km[kb][i] = slot_mask(dk);
+        const uint32_t dv = kb < nmb ? __ldg(TV.slots + (size_t)set * D + 16 * kb + 8 * i + gid) : 0u;
+        va[kb][i] = vrow + 4u * (2u + (dv & 255u));
+        vsh[kb][i] = (dv >> 8) & 255u;
+        vm[kb][i] = slot_mask(dv);
       }
-    }
-    const uint32_t src_off = isV ? (uint32_t)DT * RK * 4 : 0u;
-    const uint32_t R4 = (uint32_t)(isV ? RV : RK) * 4u;
-    const int upitch = isV ? pitchV : pitchK;
-    uint8_t* wtile = smem + L.tiles + (size_t)warp * L.warp_tile;
-    uint8_t* udst = wtile + (isV ? 16 * pitchK : 0) + grp * 16 + sub * upitch;
+    // z/s words: key record of token gid; value record (gid >> 1), half gid & 1; tokens gid + 8 one step on
+    const uint32_t kz = krow;
+    const uint32_t vz = (uint32_t)DT * RK * 4 + (uint32_t)(8 * warp + (gid >> 1)) * 2 * RV * 4 + 4u * (gid & 1);
     __half* ps = reinterpret_cast<__half*>(smem + L.ps) + (size_t)warp * 16 * 8 * NB;
 
     // q' (B operand of the logits MMA) and the folded constants come from qprep_kernel
@@ -443,134 +468,114 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
       c0[nb] = h < g ? a.qc[bh * 16 + h] : 0.f;
       c1[nb] = h < g ? a.qc[bh * 16 + 8 + h] : 0.f;
     }
-    const uint32_t ka = smem_u32(wtile + (lane & 15) * pitchK + (lane >> 4) * 16);
-    const uint32_t va = smem_u32(wtile + 16 * pitchK + ((lane & 7) + ((lane >> 4) << 3)) * pitchV +
-                                 ((lane >> 3) & 1) * 16);
     const uint32_t pa = smem_u32(ps + (lane & 15) * 8 * NB);
+    constexpr int UNR = 1;  // unrolling over the ring outgrows the instruction cache
 
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i % NS;
-      // every lane takes the stage's data through its own wait; the verdict is made warp-uniform
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
-        s_abort = 1;
-        break;
-      }
-      const uint8_t* st = smem + (size_t)s * L.stage_bytes;
-      const long long my_t0 = t0 + (long long)i * DT + 16 * warp;
-      const bool live = my_t0 < t1;
-      uint32_t kzs[2] = {0u, 0u}, vzs[2] = {0u, 0u};
-      if (live) {
-        kzs[0] = *reinterpret_cast<const uint32_t*>(st + (16 * warp + gid) * RK * 4);
-        kzs[1] = *reinterpret_cast<const uint32_t*>(st + (16 * warp + gid + 8) * RK * 4);
-        vzs[0] = *reinterpret_cast<const uint32_t*>(st + DT * RK * 4 + (16 * warp + gid) * RV * 4);
-        vzs[1] = *reinterpret_cast<const uint32_t*>(st + DT * RK * 4 + (16 * warp + gid + 8) * RV * 4);
-        if (active) {
-          // four passes per batch: all 16 words are loaded before any unpacked tile row is stored, so the
-          // loads of a batch are in flight together
-          const uint8_t* row = st + src_off + (16 * warp + sub) * R4;
-          uint8_t* drow = udst;
-          for (int p = 0; p < passes; p += 4) {
-            uint32_t x[4][4];
+    for (int i0 = 0; i0 < ntiles; i0 += UNR) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+      for (int uu = 0; uu < UNR; ++uu) {
+        const int i = i0 + uu;
+        if (i >= ntiles) break;
+        const int s = i % NS;
+        const uint8_t* st = smem + (size_t)s * stage_bytes;
+        if (issuer) issue_until(i, true);
+        // every lane takes the stage's data through its own wait; the verdict is made warp-uniform
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
+          s_abort = 1;
+          break;
+        }
+        const long long my_t0 = t0 + (long long)i * DT + 16 * warp;
+        if (my_t0 >= t1) {  // this warp's tokens are past the end: release the stage and move on
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+          if (issuer) issue_until(i + NS - 1, false);
+          continue;
+        }
+        const uint32_t kzw0 = ldsw(st, kz), kzw1 = ldsw(st, kz + kstep);
+        const uint32_t vzw0 = ldsw(st, vz), vzw1 = ldsw(st, vz + vstep);
+
+        // ---- logits: A = key codes (16 tokens x 16 channels), B = q' (16 channels x 8 columns) ----
+        float acc2[2][NB][4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                x[u][i] = (p + u < passes) ? *reinterpret_cast<const uint32_t*>(row + u * TPP * R4 + wo[i]) : 0u;
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if (p + u < passes) {
-                uint4 v;
-                v.x = unpack_pair(x[u][0], sh[0], mk[0]);
-                v.y = unpack_pair(x[u][1], sh[1], mk[1]);
-                v.z = unpack_pair(x[u][2], sh[2], mk[2]);
-                v.w = unpack_pair(x[u][3], sh[3], mk[3]);
-                *reinterpret_cast<uint4*>(drow + u * TPP * upitch) = v;
-              }
-            }
-            row += 4 * TPP * R4;
-            drow += 4 * TPP * upitch;
+          for (int nb = 0; nb < NB; ++nb) acc2[u][nb][0] = acc2[u][nb][1] = acc2[u][nb][2] = acc2[u][nb][3] = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          if (kb < nkb) {
+            uint32_t af[4];
+            af[0] = unpack_pair(ldsw(st, ka[kb][0]), ks[kb][0], km[kb][0]);
+            af[1] = unpack_pair(ldsw(st, ka[kb][0] + kstep), ks[kb][0], km[kb][0]);
+            af[2] = unpack_pair(ldsw(st, ka[kb][1]), ks[kb][1], km[kb][1]);
+            af[3] = unpack_pair(ldsw(st, ka[kb][1] + kstep), ks[kb][1], km[kb][1]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_f16(acc2[kb & 1][nb], af, qb[kb][nb][0], qb[kb][nb][1]);
           }
         }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // this warp is done with the stage
-      if (!live) continue;
-
-      // ---- logits: A = codes (16 tokens x 16 channels), B = q' (16 channels x 8 columns) ----
-      // two accumulators (even / odd channel blocks) halve the dependent MMA chain
-      float acc2[2][NB][4];
+        const bool valid0 = my_t0 + gid < t1, valid1 = my_t0 + gid + 8 < t1;
+        const float zk0 = half_bits_to_float(kzw0), sk0 = half_bits_to_float(kzw0 >> 16);
+        const float zk1 = half_bits_to_float(kzw1), sk1 = half_bits_to_float(kzw1 >> 16);
+        const float zv0 = half_bits_to_float(vzw0), sv0 = half_bits_to_float(vzw0 >> 16);
+        const float zv1 = half_bits_to_float(vzw1), sv1 = half_bits_to_float(vzw1 >> 16);
+        float corr[NB];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) acc2[u][nb][0] = acc2[u][nb][1] = acc2[u][nb][2] = acc2[u][nb][3] = 0.f;
-#pragma unroll
-      for (int kb = 0; kb < 8; ++kb) {
-        if (kb < nkb) {
-          uint32_t af[4];
-          ldsm_x4(ka + kb * 32, af[0], af[1], af[2], af[3]);
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_f16(acc2[kb & 1][nb], af, qb[kb][nb][0], qb[kb][nb][1]);
+        for (int nb = 0; nb < NB; ++nb) {
+          const float r0 = (acc2[0][nb][0] + acc2[1][nb][0]) + (acc2[0][nb][1] + acc2[1][nb][1]);
+          const float r1 = (acc2[0][nb][2] + acc2[1][nb][2]) + (acc2[0][nb][3] + acc2[1][nb][3]);
+          const float l0 = valid0 ? fmaf(sk0, r0, fmaf(zk0, c1[nb], c0[nb])) : -INFINITY;
+          const float l1 = valid1 ? fmaf(sk1, r1, fmaf(zk1, c1[nb], c0[nb])) : -INFINITY;
+          float mt = fmaxf(l0, l1);
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+          const float m_new = fmaxf(m_run[nb], mt);
+          corr[nb] = (m_run[nb] == m_new) ? 1.f : exp2f(m_run[nb] - m_new);
+          const float p0 = valid0 ? exp2f(l0 - m_new) : 0.f;
+          const float p1 = valid1 ? exp2f(l1 - m_new) : 0.f;
+          l_run[nb] = fmaf(l_run[nb], corr[nb], p0 + p1);
+          z_run[nb] = fmaf(z_run[nb], corr[nb], (valid0 ? p0 * zv0 : 0.f) + (valid1 ? p1 * zv1 : 0.f));
+          m_run[nb] = m_new;
+          const float w0 = valid0 ? p0 * sv0 : 0.f, w1 = valid1 ? p1 * sv1 : 0.f;
+          const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
+          const uint32_t e0 = pack_half2(h0, __float2half_rn(w0 - __half2float(h0)));
+          const uint32_t e1 = pack_half2(h1, __float2half_rn(w1 - __half2float(h1)));
+          reinterpret_cast<uint32_t*>(ps)[(gid * 8 * NB + nb * 8 + 2 * tig) >> 1] = e0;
+          reinterpret_cast<uint32_t*>(ps)[((gid + 8) * 8 * NB + nb * 8 + 2 * tig) >> 1] = e1;
         }
-      }
-      float acc[NB][4];
+        __syncwarp();
+        uint32_t bp[NB][2];
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
+        for (int nb = 0; nb < NB; ++nb) ldsm_x2_t(pa + nb * 16, bp[nb][0], bp[nb][1]);
+        // accumulator columns 2tig, 2tig+1 are head tig (+4 nb): rescale with this lane's own factor
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nb][e] = acc2[0][nb][e] + acc2[1][nb][e];
-      const bool valid0 = my_t0 + gid < t1, valid1 = my_t0 + gid + 8 < t1;
-      const float zk0 = half_bits_to_float(kzs[0]), sk0 = half_bits_to_float(kzs[0] >> 16);
-      const float zk1 = half_bits_to_float(kzs[1]), sk1 = half_bits_to_float(kzs[1] >> 16);
-      const float zv0 = half_bits_to_float(vzs[0]), sv0 = half_bits_to_float(vzs[0] >> 16);
-      const float zv1 = half_bits_to_float(vzs[1]), sv1 = half_bits_to_float(vzs[1] >> 16);
-      float corr[NB];
+        for (int nb = 0; nb < NB; ++nb) {
+          if (__any_sync(0xffffffffu, corr[nb] != 1.f)) {
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const float l0 = valid0 ? fmaf(sk0, acc[nb][0] + acc[nb][1], fmaf(zk0, c1[nb], c0[nb])) : -INFINITY;
-        const float l1 = valid1 ? fmaf(sk1, acc[nb][2] + acc[nb][3], fmaf(zk1, c1[nb], c0[nb])) : -INFINITY;
-        float mt = fmaxf(l0, l1);
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-        const float m_new = fmaxf(m_run[nb], mt);
-        corr[nb] = (m_run[nb] == m_new) ? 1.f : exp2f(m_run[nb] - m_new);
-        const float p0 = valid0 ? exp2f(l0 - m_new) : 0.f;
-        const float p1 = valid1 ? exp2f(l1 - m_new) : 0.f;
-        l_run[nb] = fmaf(l_run[nb], corr[nb], p0 + p1);
-        z_run[nb] = fmaf(z_run[nb], corr[nb], (valid0 ? p0 * zv0 : 0.f) + (valid1 ? p1 * zv1 : 0.f));
-        m_run[nb] = m_new;
-        const float w0 = valid0 ? p0 * sv0 : 0.f, w1 = valid1 ? p1 * sv1 : 0.f;
-        const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
-        const uint32_t e0 = pack_half2(h0, __float2half_rn(w0 - __half2float(h0)));
-        const uint32_t e1 = pack_half2(h1, __float2half_rn(w1 - __half2float(h1)));
-        reinterpret_cast<uint32_t*>(ps)[(gid * 8 * NB + nb * 8 + 2 * tig) >> 1] = e0;
-        reinterpret_cast<uint32_t*>(ps)[((gid + 8) * 8 * NB + nb * 8 + 2 * tig) >> 1] = e1;
-      }
-      __syncwarp();
-      uint32_t bp[NB][2];
+            for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) ldsm_x2_t(pa + nb * 16, bp[nb][0], bp[nb][1]);
-      // accumulator columns 2tig, 2tig+1 are head tig (+4 nb): rescale with this lane's own factor
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        if (__any_sync(0xffffffffu, corr[nb] != 1.f)) {
-#pragma unroll
-          for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] *= corr[nb];
+              for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] *= corr[nb];
+          }
         }
-      }
-      // ---- P.V in the rotated basis: A = V^T (16 channels x 16 tokens), B = P (16 tokens x 8 columns) ----
+        // ---- P.V in the rotated basis: A = V^T (16 channels x 16 tokens), B = P (16 tokens x 8 columns) ----
 #pragma unroll
-      for (int mb = 0; mb < 8; ++mb) {
-        if (mb < nmb) {
-          uint32_t af[4];
-          ldsm_x4_t(va + mb * 32, af[0], af[1], af[2], af[3]);
+        for (int mb = 0; mb < 8; ++mb) {
+          if (mb < nmb) {
+            uint32_t af[4];
+            af[0] = unpack_pair(ldsw(st, va[mb][0]), vsh[mb][0], vm[mb][0]);
+            af[1] = unpack_pair(ldsw(st, va[mb][1]), vsh[mb][1], vm[mb][1]);
+            af[2] = unpack_pair(ldsw(st, va[mb][0] + vstep), vsh[mb][0], vm[mb][0]);
+            af[3] = unpack_pair(ldsw(st, va[mb][1] + vstep), vsh[mb][1], vm[mb][1]);
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_f16(acc_o[mb][nb], af, bp[nb][0], bp[nb][1]);
+            for (int nb = 0; nb < NB; ++nb) mma_f16(acc_o[mb][nb], af, bp[nb][0], bp[nb][1]);
+          }
         }
+        __syncwarp();  // every lane is done with the stage and with the P tile
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (issuer) issue_until(i + NS - 1, false);
       }
-      __syncwarp();  // the P tile and this warp's unpacked tiles are rewritten next iteration
+      if (*(volatile int*)&s_abort) break;
     }
+    if (issuer) s_issued = next_issue;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
@@ -670,10 +675,10 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h)
       if (h < g) part[h * PSTR + 4 + k] = n[h];
-  } else if (tid < D + g) {
-    const int h = tid - D;
-    part[h * PSTR + 0] = mS[h];
-    part[h * PSTR + 1] = mS[MAX_G + h];
+  }
+  if (tid < g) {
+    part[tid * PSTR + 0] = mS[tid];
+    part[tid * PSTR + 1] = mS[MAX_G + tid];
   }
   __threadfence();
   __syncthreads();
@@ -690,9 +695,10 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   const uint32_t per_split = (uint32_t)g * PSTR * 4;
   const int chunk_splits = max(1, min(S, min((int)(L.tail_reserve / per_split), MAX_SPLITS)));
   const int items = g * D;
-  float accN[7];
+  constexpr int ITEMS_PER_THREAD = MAX_G * D / DTHREADS;
+  float accN[ITEMS_PER_THREAD];
 #pragma unroll
-  for (int r = 0; r < 7; ++r) accN[r] = 0.f;
+  for (int r = 0; r < ITEMS_PER_THREAD; ++r) accN[r] = 0.f;
   if (tid < g) {
     hst[tid] = -INFINITY;
     hst[MAX_G + tid] = 0.f;
@@ -735,7 +741,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
       hst[h] = hst[2 * MAX_G + h];
     }
 #pragma unroll
-    for (int r = 0; r < 7; ++r) {
+    for (int r = 0; r < ITEMS_PER_THREAD; ++r) {
       const int it = tid + r * DTHREADS;
       if (it < items) {
         const int h = it >> 7, k = it & (D - 1);
@@ -747,7 +753,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   }
   __syncthreads();
 #pragma unroll
-  for (int r = 0; r < 7; ++r) {
+  for (int r = 0; r < ITEMS_PER_THREAD; ++r) {
     const int it = tid + r * DTHREADS;
     if (it < items) {
       const int h = it >> 7, k = it & (D - 1);
@@ -796,9 +802,31 @@ DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device) {
   return L;
 }
 
-static int ring_stages(int RK, int RV) {
-  const int stage = DT * (RK + RV) * 4;
-  return std::max(2, std::min(MAX_STAGES, RING_BUDGET / stage));
+// record lengths with a compile-time decode kernel (equal key and value budgets of 1.25 - 4 bits/element)
+static int compile_time_record_words(int RK, int RV) {
+  if (RK != RV) return 0;
+  switch (RK) {
+    case 5: case 8: case 11: case 12: case 16: return RK;
+    default: return 0;
+  }
+}
+
+template <int NB, int RT>
+static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a) {
+  cudaFuncSetAttribute(decode_kernel<NB, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RT>, P, a);
+}
+
+template <int NB>
+static cudaError_t launch_decode_nb(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a, int rt) {
+  switch (rt) {
+    case 5: return launch_decode_kernel<NB, 5>(cfg, P, a);
+    case 8: return launch_decode_kernel<NB, 8>(cfg, P, a);
+    case 11: return launch_decode_kernel<NB, 11>(cfg, P, a);
+    case 12: return launch_decode_kernel<NB, 12>(cfg, P, a);
+    case 16: return launch_decode_kernel<NB, 16>(cfg, P, a);
+    default: return launch_decode_kernel<NB, 0>(cfg, P, a);
+  }
 }
 
 kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
@@ -824,16 +852,16 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   a.per_seq = c.per_seq_params;
   a.splits = L.splits;
   a.chunk = L.chunk;
-  a.stages = ring_stages(P.t[0].r_words, P.t[1].r_words);
+  const int rt = compile_time_record_words(P.t[0].r_words, P.t[1].r_words);
+  a.stages = ring_stages_for(P.t[0].r_words, P.t[1].r_words);
   a.scale_log2 = scale * 1.4426950408889634f;
   const size_t qsm = qprep_smem_bytes();
   cudaFuncSetAttribute(qprep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qsm);
   qprep_kernel<<<dim3(c.Hkv, B), QP_THREADS, qsm, s>>>(P, a);
   kv_status st = launch_check("qprep_kernel");
   if (st != KV_OK) return st;
-  // shared memory sized for the widest parameter set (8 channel blocks each for K and V)
   const int nb = a.g <= 4 ? 1 : 2;
-  const size_t smem = decode_smem(P.t[0].r_words, P.t[1].r_words, 8, 8, a.stages, nb).total;
+  const size_t smem = decode_smem(P.t[0].r_words, P.t[1].r_words, a.stages, nb).total;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.splits, c.Hkv, B);
   cfg.blockDim = dim3(DTHREADS);
@@ -844,14 +872,7 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e;
-  if (nb == 1) {
-    cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    e = cudaLaunchKernelEx(&cfg, decode_kernel<1>, P, a);
-  } else {
-    cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    e = cudaLaunchKernelEx(&cfg, decode_kernel<2>, P, a);
-  }
+  const cudaError_t e = nb == 1 ? launch_decode_nb<1>(cfg, P, a, rt) : launch_decode_nb<2>(cfg, P, a, rt);
   if (e != cudaSuccess) {
     set_error("decode_kernel launch: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;
@@ -1162,14 +1183,15 @@ kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int H
 // ======================================================================================================
 __global__ void __launch_bounds__(256) debug_qp_warp_kernel(ParamsDev P, int set, int tensor, const float* y,
                                                             long long n, uint32_t* rec) {
-  __shared__ uint32_t rec_s[8][MAX_RW + 3];
+  __shared__ uint32_t rec_s[8][2 * MAX_RW + 4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long t = (long long)blockIdx.x * 8 + warp;
   if (t >= n) return;
   const TensorDev& td = P.t[tensor];
   const float4 v = *reinterpret_cast<const float4*>(y + (size_t)t * D + 4 * lane);
   const float yy[4] = {v.x, v.y, v.z, v.w};
-  quantize_pack_warp(td, set, yy, lane, rec_s[warp], rec + (size_t)t * td.r_words);
+  uint32_t* out = tensor == 0 ? rec + (size_t)t * td.r_words : rec + (size_t)(t >> 1) * 2 * td.r_words;
+  quantize_pack_warp(td, set, yy, lane, rec_s[warp], out, tensor == 1, (int)(t & 1));
 }
 
 __global__ void __launch_bounds__(128) debug_qp_thread_kernel(ParamsDev P, int set, int tensor, const float* y,
@@ -1178,8 +1200,19 @@ __global__ void __launch_bounds__(128) debug_qp_thread_kernel(ParamsDev P, int s
   if (t >= n) return;
   const TensorDev& td = P.t[tensor];
   const float* yr = y + (size_t)t * D;
-  uint32_t* out = rec + (size_t)t * td.r_words;
-  quantize_pack_thread(td, set, [&](int j) { return yr[j]; }, [&](int w, uint32_t val) { out[w] = val; });
+  if (tensor == 0) {
+    uint32_t* out = rec + (size_t)t * td.r_words;
+    quantize_pack_thread(td, set, false, [&](int j) { return yr[j]; }, [&](int w, uint32_t val) { out[w] = val; });
+  } else {
+    uint32_t* out = rec + (size_t)(t >> 1) * 2 * td.r_words;
+    const int half = (int)(t & 1);
+    quantize_pack_thread(td, set, true, [&](int j) { return yr[j]; }, [&](int w, uint32_t val) {
+      if (w == 0)
+        out[half] = val;
+      else
+        reinterpret_cast<uint16_t*>(out)[2 * w + half] = (uint16_t)val;
+    });
+  }
 }
 
 kv_status launch_debug_quantize_pack(const ParamsDev& P, int set, int tensor, const float* y, int64_t n,
@@ -1191,40 +1224,38 @@ kv_status launch_debug_quantize_pack(const ParamsDev& P, int set, int tensor, co
   return launch_check("debug quantize/pack");
 }
 
-// Runs the decoder's record unpacker (unpack_pair) over 64-record tiles and writes integer codes.
-__global__ void __launch_bounds__(128) debug_unpack_kernel(ParamsDev P, int set, int tensor,
-                                                                const uint32_t* rec, long long n,
-                                                                uint16_t* codes) {
-  __shared__ uint32_t srec[UNPACK_T * MAX_RW + 4];
-  __shared__ __align__(16) uint8_t tile[UNPACK_T * KC_PITCH_MAX];
+// The decoder's slot extraction (unpack_pair) over records: one thread per (record, slot); writes integer
+// codes [n tokens][128]. Keys: slot k of token t gives channels 2k, 2k+1; values: slot j of record p gives
+// channel j of tokens 2p, 2p+1.
+__global__ void __launch_bounds__(128) debug_unpack_kernel(ParamsDev P, int set, int tensor, const uint32_t* rec,
+                                                           long long n, uint16_t* codes) {
   const TensorDev& td = P.t[tensor];
-  const int R = td.r_words, tid = threadIdx.x;
-  const long long t0 = (long long)blockIdx.x * UNPACK_T;
-  const int cnt = (int)min((long long)UNPACK_T, n - t0);
-  for (int i = tid; i < UNPACK_T * R + 4; i += 128) srec[i] = i < cnt * R ? rec[t0 * R + i] : 0u;
-  __syncthreads();
-  const int nz = td.nz[set], nblk = (nz + 15) >> 4, pitch = unpacked_pitch(nblk);
-  const QuadMap m = quad_map(nblk * 4, tid, 128);
-  if (m.active) {
-    const QuadDesc dq = load_quad(td, set, m.q);
-    for (int t = m.r0; t < UNPACK_T; t += m.rstep)
-      *reinterpret_cast<uint2*>(tile + t * pitch + 8 * m.q) = unpack_quad(srec + t * R, dq);
-  }
-  __syncthreads();
-  for (int i = tid; i < cnt * D; i += 128) {
-    const int t = i / D, j = i % D;
-    uint16_t c = 0;
-    if (j < nz) {
-      const __half hv = *reinterpret_cast<const __half*>(tile + t * pitch + 2 * j);
-      c = (uint16_t)(__half2float(hv) - 0.5f);
-    }
-    codes[(t0 + t) * D + j] = c;
+  const int R = td.r_words;
+  const long long n_rec = tensor == 0 ? n : (n + 1) / 2;
+  const int n_slot = tensor == 0 ? D / 2 : D;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_rec * n_slot) return;
+  const long long r = idx / n_slot;
+  const int k = (int)(idx - r * n_slot);
+  const uint32_t desc = td.slots[(size_t)set * D + k];
+  const uint32_t u = desc & 255u, sh = (desc >> 8) & 255u;
+  if (tensor == 0) {
+    const uint32_t h2 = unpack_pair(rec[r * R + 1 + u], sh, slot_mask(desc));
+    const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+    codes[r * D + 2 * k] = (uint16_t)(__low2float(hv) - 0.5f);
+    codes[r * D + 2 * k + 1] = (uint16_t)(__high2float(hv) - 0.5f);
+  } else {
+    const uint32_t h2 = unpack_pair(rec[r * 2 * R + 2 + u], sh, slot_mask(desc));
+    const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+    codes[(2 * r) * D + k] = (uint16_t)(__low2float(hv) - 0.5f);
+    if (2 * r + 1 < n) codes[(2 * r + 1) * D + k] = (uint16_t)(__high2float(hv) - 0.5f);
   }
 }
 
 kv_status launch_debug_unpack(const ParamsDev& P, int set, int tensor, const uint32_t* rec, int64_t n,
                               uint16_t* codes, cudaStream_t s) {
-  debug_unpack_kernel<<<(unsigned)((n + UNPACK_T - 1) / UNPACK_T), 128, 0, s>>>(P, set, tensor, rec, n, codes);
+  const long long work = (tensor == 0 ? n : (n + 1) / 2) * (long long)(tensor == 0 ? D / 2 : D);
+  debug_unpack_kernel<<<(unsigned)((work + 127) / 128), 128, 0, s>>>(P, set, tensor, rec, n, codes);
   return launch_check("debug unpack");
 }
 
