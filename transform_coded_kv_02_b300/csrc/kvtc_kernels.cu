@@ -159,9 +159,9 @@ kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, co
 // decode over packed records
 // ======================================================================================================
 constexpr int PSTR = 132;          // floats per (split, head) partial: m, l, z, -, A[128]
-constexpr int DWARPS = 4;          // consumer warps per decode CTA
-constexpr int DT = 16 * DWARPS;    // tokens per ring stage (16 per consumer warp)
-constexpr int DTHREADS = 32 * DWARPS;   // all warps consume; lane 0 of warp 0 also issues the copies
+constexpr int DWARPS = 4;          // token groups per tile: a key warp and a value warp each
+constexpr int DT = 16 * DWARPS;    // tokens per ring stage (16 per warp pair)
+constexpr int DTHREADS = 64 * DWARPS;  // key warps 0..3, value warps 4..7; lane 0 of warp 0 issues the copies
 constexpr int RING_BUDGET = 48 * 1024;
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_SPLITS = 256;
@@ -287,20 +287,22 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs 
 }
 
 // ---- split-K decode ----------------------------------------------------------------------------------
+constexpr uint32_t PAIR_BYTES_PER_NB = 16u * 8u * 2u + 4u * 4u;  // P tile (16 tokens x 8 columns) + 4 factors
+
 struct DecSmem {  // byte offsets into the dynamic shared memory of decode_kernel
   uint32_t stage_bytes, ps, epi_ws, epi_merged, tail_reserve, total;
 };
 
 __host__ __device__ __forceinline__ uint32_t align128u(uint32_t x) { return (x + 127u) & ~127u; }
 
-// main loop: ring | per-warp P tiles
+// main loop: ring | per-pair P tiles and rescale factors
 // epilogue (ring dead): T'_V rows [0, 64 KB) | per-warp partials | merged partial
 // tail: split partial chunks from 0 | per-split weights and per-head state in the reserve at the end
 __host__ __device__ inline DecSmem decode_smem(int RK, int RV, int stages, int nb) {
   DecSmem s;
   s.stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
   s.ps = align128u(stages * s.stage_bytes);
-  const uint32_t main_end = s.ps + DWARPS * 16u * 8u * nb * 2u;
+  const uint32_t main_end = s.ps + DWARPS * PAIR_BYTES_PER_NB * nb;
   s.epi_ws = D * D * 4u;
   s.epi_merged = s.epi_ws + DWARPS * 8u * PSTR * 4u;
   const uint32_t epi_end = s.epi_merged + (MAX_G * D + 4 * MAX_G) * 4u;
@@ -327,7 +329,7 @@ template <int NB, int RT>
 __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   // barriers live outside the dynamic region, which the epilogue and the tail reuse wholesale
-  __shared__ __align__(8) uint64_t full[MAX_STAGES], empty[MAX_STAGES], tbar_s;
+  __shared__ __align__(8) uint64_t full[MAX_STAGES], empty[MAX_STAGES], pF[DWARPS], pE[DWARPS], tbar_s;
   __shared__ int s_abort, s_last, s_issued;
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int bh = b * a.Hkv + kh;
@@ -352,7 +354,11 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), DWARPS);
+      mbar_init(smem_u32(&empty[s]), 2 * DWARPS);  // every key and value warp releases each stage
+    }
+    for (int p = 0; p < DWARPS; ++p) {
+      mbar_init(smem_u32(&pF[p]), 1);
+      mbar_init(smem_u32(&pE[p]), 1);
     }
     mbar_init(smem_u32(tbar), 1);
     fence_mbar_init();
@@ -360,19 +366,6 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
     s_issued = 0;
   }
   __syncthreads();
-
-  float m_run[NB], l_run[NB], z_run[NB];
-  float acc_o[8][NB][4];
-#pragma unroll
-  for (int nb = 0; nb < NB; ++nb) {
-    m_run[nb] = -INFINITY;
-    l_run[nb] = 0.f;
-    z_run[nb] = 0.f;
-#pragma unroll
-    for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] = 0.f;
-  }
 
   // ---- record tiles stream into the ring by bulk copies that lane 0 of warp 0 issues ----
   const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
@@ -416,19 +409,24 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
                    : "memory");
     issue_until(NS - 1, false);
   }
-  {
-    // ================= consumers: warp w owns tokens [16w, 16w + 16) of every tile =================
-    // Codes go from the staged records straight into MMA operand registers.
-    //  keys, logits A operand (16 tokens x 16 channels of block kb): key slot 8kb + tig holds channels
-    //    (16kb + 2tig, +1), slot 8kb + 4 + tig channels (16kb + 8 + 2tig, +1); rows gid, gid + 8 = tokens gid,
-    //    gid + 8 of this warp.
-    //  values, P.V A operand (16 channels x 16 tokens): value slot 16mb + gid (+ 8) holds that channel for the
-    //    two tokens of a value record; this warp's records tig and tig + 4 hold tokens (2tig, 2tig+1) and
-    //    (2tig + 8, 2tig + 9).
-    const uint32_t krow = (uint32_t)(16 * warp + gid) * RK * 4;
-    const uint32_t vrow = (uint32_t)DT * RK * 4 + (uint32_t)(8 * warp + tig) * 2 * RV * 4;
-    const uint32_t kstep = 8u * RK * 4, vstep = 4u * 2 * RV * 4;
-    uint32_t ka[8][2], ks[8][2], km[8][2], va[8][2], vsh[8][2], vm[8][2];
+  // ============ warp pairs: key warp pw and value warp pw + 4 own tokens [16 pw, 16 pw + 16) of every tile ============
+  // Codes go from the staged records straight into MMA operand registers.
+  //  key warp, logits A operand (16 tokens x 16 channels of block kb): key slot 8kb + tig holds channels
+  //    (16kb + 2tig, +1), slot 8kb + 4 + tig channels (16kb + 8 + 2tig, +1); rows gid, gid + 8 = tokens gid, gid + 8.
+  //  value warp, P.V A operand (16 channels x 16 tokens): value slot 16mb + gid (+ 8) holds that channel for the
+  //    two tokens of a value record; the pair's records tig and tig + 4 hold tokens (2tig, 2tig+1), (2tig+8, 2tig+9).
+  // The key warp hands P (fp16 hi/lo of p s_V) and the heads' rescale factors to the value warp through shared
+  // memory, guarded by two mbarriers per pair (filled / emptied), whose waits are bounded like every other.
+  const int pw = warp & 3;
+  const bool kwarp = warp < 4;
+  uint8_t* pair_smem = smem + L.ps + (size_t)pw * PAIR_BYTES_PER_NB * NB;
+  __half* ps = reinterpret_cast<__half*>(pair_smem);                          // [16 tokens][8 NB columns]
+  float* pcorr = reinterpret_cast<float*>(pair_smem + 16 * 8 * NB * 2);       // [NB][4]
+  float* ws = reinterpret_cast<float*>(smem + L.epi_ws);                       // [DWARPS][8][PSTR]
+  const uint32_t kstep = 8u * RK * 4, vstep = 4u * 2 * RV * 4;
+  if (kwarp) {
+    const uint32_t krow = (uint32_t)(16 * pw + gid) * RK * 4;
+    uint32_t ka[8][2], ks[8][2], km[8][2];
 #pragma unroll
     for (int kb = 0; kb < 8; ++kb)
 #pragma unroll
@@ -437,16 +435,17 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
         ka[kb][i] = krow + 4u * (1u + (dk & 255u));
         ks[kb][i] = (dk >> 8) & 255u;
         km[kb][i] = slot_mask(dk);
-        const uint32_t dv = kb < nmb ? __ldg(TV.slots + (size_t)set * D + 16 * kb + 8 * i + gid) : 0u;
-        va[kb][i] = vrow + 4u * (2u + (dv & 255u));
-        vsh[kb][i] = (dv >> 8) & 255u;
-        vm[kb][i] = slot_mask(dv);
       }
     // z/s words: key record of token gid; value record (gid >> 1), half gid & 1; tokens gid + 8 one step on
     const uint32_t kz = krow;
-    const uint32_t vz = (uint32_t)DT * RK * 4 + (uint32_t)(8 * warp + (gid >> 1)) * 2 * RV * 4 + 4u * (gid & 1);
-    __half* ps = reinterpret_cast<__half*>(smem + L.ps) + (size_t)warp * 16 * 8 * NB;
-
+    const uint32_t vz = (uint32_t)DT * RK * 4 + (uint32_t)(8 * pw + (gid >> 1)) * 2 * RV * 4 + 4u * (gid & 1);
+    float m_run[NB], l_run[NB], z_run[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      m_run[nb] = -INFINITY;
+      l_run[nb] = 0.f;
+      z_run[nb] = 0.f;
+    }
     // q' (B operand of the logits MMA) and the folded constants come from qprep_kernel
     pdl_wait();
     uint32_t qb[8][NB][2];
@@ -468,120 +467,216 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
       c0[nb] = h < g ? a.qc[bh * 16 + h] : 0.f;
       c1[nb] = h < g ? a.qc[bh * 16 + 8 + h] : 0.f;
     }
-    const uint32_t pa = smem_u32(ps + (lane & 15) * 8 * NB);
-    constexpr int UNR = 1;  // unrolling over the ring outgrows the instruction cache
-
-    for (int i0 = 0; i0 < ntiles; i0 += UNR) {
-#pragma unroll
-      for (int uu = 0; uu < UNR; ++uu) {
-        const int i = i0 + uu;
-        if (i >= ntiles) break;
-        const int s = i % NS;
-        const uint8_t* st = smem + (size_t)s * stage_bytes;
-        if (issuer) issue_until(i, true);
-        // every lane takes the stage's data through its own wait; the verdict is made warp-uniform
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
-          s_abort = 1;
-          break;
-        }
-        const long long my_t0 = t0 + (long long)i * DT + 16 * warp;
-        if (my_t0 >= t1) {  // this warp's tokens are past the end: release the stage and move on
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-          if (issuer) issue_until(i + NS - 1, false);
-          continue;
-        }
-        const uint32_t kzw0 = ldsw(st, kz), kzw1 = ldsw(st, kz + kstep);
-        const uint32_t vzw0 = ldsw(st, vz), vzw1 = ldsw(st, vz + vstep);
-
-        // ---- logits: A = key codes (16 tokens x 16 channels), B = q' (16 channels x 8 columns) ----
-        float acc2[2][NB][4];
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) acc2[u][nb][0] = acc2[u][nb][1] = acc2[u][nb][2] = acc2[u][nb][3] = 0.f;
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          if (kb < nkb) {
-            uint32_t af[4];
-            af[0] = unpack_pair(ldsw(st, ka[kb][0]), ks[kb][0], km[kb][0]);
-            af[1] = unpack_pair(ldsw(st, ka[kb][0] + kstep), ks[kb][0], km[kb][0]);
-            af[2] = unpack_pair(ldsw(st, ka[kb][1]), ks[kb][1], km[kb][1]);
-            af[3] = unpack_pair(ldsw(st, ka[kb][1] + kstep), ks[kb][1], km[kb][1]);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_f16(acc2[kb & 1][nb], af, qb[kb][nb][0], qb[kb][nb][1]);
-          }
-        }
-        const bool valid0 = my_t0 + gid < t1, valid1 = my_t0 + gid + 8 < t1;
-        const float zk0 = half_bits_to_float(kzw0), sk0 = half_bits_to_float(kzw0 >> 16);
-        const float zk1 = half_bits_to_float(kzw1), sk1 = half_bits_to_float(kzw1 >> 16);
-        const float zv0 = half_bits_to_float(vzw0), sv0 = half_bits_to_float(vzw0 >> 16);
-        const float zv1 = half_bits_to_float(vzw1), sv1 = half_bits_to_float(vzw1 >> 16);
-        float corr[NB];
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const float r0 = (acc2[0][nb][0] + acc2[1][nb][0]) + (acc2[0][nb][1] + acc2[1][nb][1]);
-          const float r1 = (acc2[0][nb][2] + acc2[1][nb][2]) + (acc2[0][nb][3] + acc2[1][nb][3]);
-          const float l0 = valid0 ? fmaf(sk0, r0, fmaf(zk0, c1[nb], c0[nb])) : -INFINITY;
-          const float l1 = valid1 ? fmaf(sk1, r1, fmaf(zk1, c1[nb], c0[nb])) : -INFINITY;
-          float mt = fmaxf(l0, l1);
-          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-          const float m_new = fmaxf(m_run[nb], mt);
-          corr[nb] = (m_run[nb] == m_new) ? 1.f : exp2f(m_run[nb] - m_new);
-          const float p0 = valid0 ? exp2f(l0 - m_new) : 0.f;
-          const float p1 = valid1 ? exp2f(l1 - m_new) : 0.f;
-          l_run[nb] = fmaf(l_run[nb], corr[nb], p0 + p1);
-          z_run[nb] = fmaf(z_run[nb], corr[nb], (valid0 ? p0 * zv0 : 0.f) + (valid1 ? p1 * zv1 : 0.f));
-          m_run[nb] = m_new;
-          const float w0 = valid0 ? p0 * sv0 : 0.f, w1 = valid1 ? p1 * sv1 : 0.f;
-          const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
-          const uint32_t e0 = pack_half2(h0, __float2half_rn(w0 - __half2float(h0)));
-          const uint32_t e1 = pack_half2(h1, __float2half_rn(w1 - __half2float(h1)));
-          reinterpret_cast<uint32_t*>(ps)[(gid * 8 * NB + nb * 8 + 2 * tig) >> 1] = e0;
-          reinterpret_cast<uint32_t*>(ps)[((gid + 8) * 8 * NB + nb * 8 + 2 * tig) >> 1] = e1;
-        }
+    int hand = 0;  // handoffs to the value warp so far
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % NS;
+      const uint8_t* st = smem + (size_t)s * stage_bytes;
+      if (issuer) issue_until(i, true);
+      // every lane takes the stage's data through its own wait; the verdict is made warp-uniform
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
+      }
+      const long long my_t0 = t0 + (long long)i * DT + 16 * pw;
+      if (my_t0 >= t1) {  // this pair's tokens are past the end
         __syncwarp();
-        uint32_t bp[NB][2];
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (issuer) issue_until(i + NS - 1, false);
+        continue;
+      }
+      const uint32_t kzw0 = ldsw(st, kz), kzw1 = ldsw(st, kz + kstep);
+      const uint32_t vzw0 = ldsw(st, vz), vzw1 = ldsw(st, vz + vstep);
+      // ---- logits: A = key codes (16 tokens x 16 channels), B = q' (16 channels x 8 columns) ----
+      float acc2[2][NB][4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) ldsm_x2_t(pa + nb * 16, bp[nb][0], bp[nb][1]);
-        // accumulator columns 2tig, 2tig+1 are head tig (+4 nb): rescale with this lane's own factor
+      for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          if (__any_sync(0xffffffffu, corr[nb] != 1.f)) {
+        for (int nb = 0; nb < NB; ++nb) acc2[u][nb][0] = acc2[u][nb][1] = acc2[u][nb][2] = acc2[u][nb][3] = 0.f;
 #pragma unroll
-            for (int mb = 0; mb < 8; ++mb)
+      for (int kb = 0; kb < 8; ++kb) {
+        if (kb < nkb) {
+          uint32_t af[4];
+          af[0] = unpack_pair(ldsw(st, ka[kb][0]), ks[kb][0], km[kb][0]);
+          af[1] = unpack_pair(ldsw(st, ka[kb][0] + kstep), ks[kb][0], km[kb][0]);
+          af[2] = unpack_pair(ldsw(st, ka[kb][1]), ks[kb][1], km[kb][1]);
+          af[3] = unpack_pair(ldsw(st, ka[kb][1] + kstep), ks[kb][1], km[kb][1]);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] *= corr[nb];
-          }
+          for (int nb = 0; nb < NB; ++nb) mma_f16(acc2[kb & 1][nb], af, qb[kb][nb][0], qb[kb][nb][1]);
         }
-        // ---- P.V in the rotated basis: A = V^T (16 channels x 16 tokens), B = P (16 tokens x 8 columns) ----
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // the key warp is done with the stage
+      if (issuer) issue_until(i + NS - 1, false);
+      const bool valid0 = my_t0 + gid < t1, valid1 = my_t0 + gid + 8 < t1;
+      const float zk0 = half_bits_to_float(kzw0), sk0 = half_bits_to_float(kzw0 >> 16);
+      const float zk1 = half_bits_to_float(kzw1), sk1 = half_bits_to_float(kzw1 >> 16);
+      const float zv0 = half_bits_to_float(vzw0), sv0 = half_bits_to_float(vzw0 >> 16);
+      const float zv1 = half_bits_to_float(vzw1), sv1 = half_bits_to_float(vzw1 >> 16);
+      uint32_t e0[NB], e1[NB];
+      float corr[NB];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const float r0 = (acc2[0][nb][0] + acc2[1][nb][0]) + (acc2[0][nb][1] + acc2[1][nb][1]);
+        const float r1 = (acc2[0][nb][2] + acc2[1][nb][2]) + (acc2[0][nb][3] + acc2[1][nb][3]);
+        const float l0 = valid0 ? fmaf(sk0, r0, fmaf(zk0, c1[nb], c0[nb])) : -INFINITY;
+        const float l1 = valid1 ? fmaf(sk1, r1, fmaf(zk1, c1[nb], c0[nb])) : -INFINITY;
+        float mt = fmaxf(l0, l1);
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        const float m_new = fmaxf(m_run[nb], mt);
+        corr[nb] = (m_run[nb] == m_new) ? 1.f : exp2f(m_run[nb] - m_new);
+        const float p0 = valid0 ? exp2f(l0 - m_new) : 0.f;
+        const float p1 = valid1 ? exp2f(l1 - m_new) : 0.f;
+        l_run[nb] = fmaf(l_run[nb], corr[nb], p0 + p1);
+        z_run[nb] = fmaf(z_run[nb], corr[nb], (valid0 ? p0 * zv0 : 0.f) + (valid1 ? p1 * zv1 : 0.f));
+        m_run[nb] = m_new;
+        const float w0 = valid0 ? p0 * sv0 : 0.f, w1 = valid1 ? p1 * sv1 : 0.f;
+        const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
+        e0[nb] = pack_half2(h0, __float2half_rn(w0 - __half2float(h0)));
+        e1[nb] = pack_half2(h1, __float2half_rn(w1 - __half2float(h1)));
+      }
+      // ---- hand P and the rescale factors to the value warp ----
+      if (hand > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&pE[pw]), (uint32_t)((hand - 1) & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
+      }
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        reinterpret_cast<uint32_t*>(ps)[(gid * 8 * NB + nb * 8 + 2 * tig) >> 1] = e0[nb];
+        reinterpret_cast<uint32_t*>(ps)[((gid + 8) * 8 * NB + nb * 8 + 2 * tig) >> 1] = e1[nb];
+        if (gid == 0) pcorr[nb * 4 + tig] = corr[nb];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&pF[pw]));
+      ++hand;
+    }
+    if (issuer) s_issued = next_issue;
+    // this pair's softmax state into the per-pair partial (the region lies past the ring)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      l_run[nb] += __shfl_xor_sync(0xffffffffu, l_run[nb], 4);
+      l_run[nb] += __shfl_xor_sync(0xffffffffu, l_run[nb], 8);
+      l_run[nb] += __shfl_xor_sync(0xffffffffu, l_run[nb], 16);
+      z_run[nb] += __shfl_xor_sync(0xffffffffu, z_run[nb], 4);
+      z_run[nb] += __shfl_xor_sync(0xffffffffu, z_run[nb], 8);
+      z_run[nb] += __shfl_xor_sync(0xffffffffu, z_run[nb], 16);
+      const int h = tig + 4 * nb;
+      if (h < g && gid == 0) {
+        float* w = ws + (pw * 8 + h) * PSTR;
+        w[0] = m_run[nb];
+        w[1] = l_run[nb];
+        w[2] = z_run[nb];
+      }
+    }
+  } else {
+    const uint32_t vrow = (uint32_t)DT * RK * 4 + (uint32_t)(8 * pw + tig) * 2 * RV * 4;
+    uint32_t va[8][2], vsh[8][2], vm[8][2];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t dv = mb < nmb ? __ldg(TV.slots + (size_t)set * D + 16 * mb + 8 * i + gid) : 0u;
+        va[mb][i] = vrow + 4u * (2u + (dv & 255u));
+        vsh[mb][i] = (dv >> 8) & 255u;
+        vm[mb][i] = slot_mask(dv);
+      }
+    float acc_o[8][NB][4];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] = 0.f;
+    const uint32_t pa = smem_u32(ps + (lane & 15) * 8 * NB);
+    int hand = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % NS;
+      const uint8_t* st = smem + (size_t)s * stage_bytes;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
+      }
+      const long long my_t0 = t0 + (long long)i * DT + 16 * pw;
+      if (my_t0 >= t1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        continue;
+      }
+      // value codes of this pair's 16 tokens: with one column block they are taken while the key warp works on
+      // the logits (and the stage released early); with two, registers are short and they go straight to the MMA
+      uint32_t vf[NB == 1 ? 8 : 1][4];
+      if constexpr (NB == 1) {
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) {
           if (mb < nmb) {
-            uint32_t af[4];
+            vf[mb][0] = unpack_pair(ldsw(st, va[mb][0]), vsh[mb][0], vm[mb][0]);
+            vf[mb][1] = unpack_pair(ldsw(st, va[mb][1]), vsh[mb][1], vm[mb][1]);
+            vf[mb][2] = unpack_pair(ldsw(st, va[mb][0] + vstep), vsh[mb][0], vm[mb][0]);
+            vf[mb][3] = unpack_pair(ldsw(st, va[mb][1] + vstep), vsh[mb][1], vm[mb][1]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // the value warp is done with the stage
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&pF[pw]), (uint32_t)(hand & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
+      }
+      uint32_t bp[NB][2];
+      float corr[NB];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        ldsm_x2_t(pa + nb * 16, bp[nb][0], bp[nb][1]);
+        corr[nb] = pcorr[nb * 4 + tig];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&pE[pw]));
+      ++hand;
+      // accumulator columns 2tig, 2tig+1 are head tig (+4 nb)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        if (__any_sync(0xffffffffu, corr[nb] != 1.f)) {
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] *= corr[nb];
+        }
+      }
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        if (mb < nmb) {
+          uint32_t af[4];
+          if constexpr (NB == 1) {
+            af[0] = vf[mb][0], af[1] = vf[mb][1], af[2] = vf[mb][2], af[3] = vf[mb][3];
+          } else {
             af[0] = unpack_pair(ldsw(st, va[mb][0]), vsh[mb][0], vm[mb][0]);
             af[1] = unpack_pair(ldsw(st, va[mb][1]), vsh[mb][1], vm[mb][1]);
             af[2] = unpack_pair(ldsw(st, va[mb][0] + vstep), vsh[mb][0], vm[mb][0]);
             af[3] = unpack_pair(ldsw(st, va[mb][1] + vstep), vsh[mb][1], vm[mb][1]);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_f16(acc_o[mb][nb], af, bp[nb][0], bp[nb][1]);
           }
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(acc_o[mb][nb], af, bp[nb][0], bp[nb][1]);
         }
-        __syncwarp();  // every lane is done with the stage and with the P tile
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-        if (issuer) issue_until(i + NS - 1, false);
       }
-      if (*(volatile int*)&s_abort) break;
+      if constexpr (NB != 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // the value warp is done with the stage
+      }
     }
-    if (issuer) s_issued = next_issue;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
+      const int h = tig + 4 * nb;
+      if (h < g) {
+        float* w = ws + (pw * 8 + h) * PSTR;
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        l_run[nb] += __shfl_xor_sync(0xffffffffu, l_run[nb], o);
-        z_run[nb] += __shfl_xor_sync(0xffffffffu, z_run[nb], o);
+        for (int mb = 0; mb < 8; ++mb) {
+          if (mb < nmb) {
+            w[4 + mb * 16 + gid] = acc_o[mb][nb][0] + acc_o[mb][nb][1];
+            w[4 + mb * 16 + gid + 8] = acc_o[mb][nb][2] + acc_o[mb][nb][3];
+          }
+        }
       }
     }
   }
@@ -601,34 +696,12 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   // N_h[k] = Z_h w_k + sum_j T'[j][k] A_h[j] with T'[j][k] = T_V[j][k] sigma_j 2^-b_j and w_k = sum_{b_j>0} T_V[j][k]
   // sigma_j, so that o_h[k] = base_k + (sum over splits e_s N_s,h[k]) / (sum over splits e_s L_s,h).
   float* Tsc = reinterpret_cast<float*>(smem);                           // [nzV][128]
-  float* ws = reinterpret_cast<float*>(smem + L.epi_ws);                 // [DWARPS][8][PSTR]
   float* mA = reinterpret_cast<float*>(smem + L.epi_merged);             // [8][128]
   float* mS = mA + MAX_G * D;                                            // M[8], L[8], Z[8]
   if (tid == 0 && nzV > 0) {
     fence_proxy_async_smem();
     mbar_expect_tx(smem_u32(tbar), (uint32_t)nzV * D * 4);
     bulk_g2s(smem_u32(Tsc), TV.Tsc + (size_t)set * D * D, (uint32_t)nzV * D * 4, smem_u32(tbar));
-  }
-  if (warp < DWARPS) {
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const int h = tig + 4 * nb;
-      if (h < g) {
-        float* w = ws + (warp * 8 + h) * PSTR;
-        if (gid == 0) {
-          w[0] = m_run[nb];
-          w[1] = l_run[nb];
-          w[2] = z_run[nb];
-        }
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-          if (mb < nmb) {
-            w[4 + mb * 16 + gid] = acc_o[mb][nb][0] + acc_o[mb][nb][1];
-            w[4 + mb * 16 + gid + 8] = acc_o[mb][nb][2] + acc_o[mb][nb][3];
-          }
-        }
-      }
-    }
   }
   __syncthreads();
   {
