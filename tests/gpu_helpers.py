@@ -119,6 +119,13 @@ def code_diff(rec_a, rec_b, p, n=None):
     zb, sb, cb = O.unpack(rec_b, p)
     if n is not None:
         za, sa, ca, zb, sb, cb = za[:n], sa[:n], ca[:n], zb[:n], sb[:n], cb[:n]
+    return token_diff((za, sa, ca), (zb, sb, cb), p)
+
+
+def token_diff(a, b, p):
+    """code_diff on per-token unpacked records (z, s, codes) as O.unpack returns them."""
+    za, sa, ca = a
+    zb, sb, cb = b
     zi = lambda h: h.view(np.uint16).astype(np.int64)
     dz = np.abs(zi(za) - zi(zb))
     ds = np.abs(zi(sa) - zi(sb))
@@ -128,3 +135,10 @@ def code_diff(rec_a, rec_b, p, n=None):
     entry_frac = float((np.count_nonzero(dc) + np.count_nonzero(dz) + np.count_nonzero(ds)) / max(n_entries, 1))
     return (float(np.mean((dz > 0) | (ds > 0))), int(dz.max(initial=0)), int(ds.max(initial=0)),
             float(np.mean(dc > 0)), int(dc.max(initial=0)), entry_frac)
+
+
+def tokens_of(rec, p, start, n):
+    """Per-token (z, s, codes) of tokens start .. start + n - 1 of a cache row (keys [T_cap, R], values
+    [T_cap / 2, 2 R]); the value record of an odd start is shared with the token before it."""
+    z, s, c = O.unpack(rec, p)
+    return z[start:start + n], s[start:start + n], c[start:start + n]

@@ -137,6 +137,115 @@ def test_encode_end_to_end_bf16_per_sequence():
         _check_end_to_end(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, True)
 
 
+@pytest.fixture(scope="module")
+def llama_300():
+    """Llama-shaped layer (8 KV heads, bf16, RoPE on keys, one parameter set per head) with 300 new tokens:
+    two full 128-token tiles and a ragged one per head."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    L = synth.make_layer(w, T=300, steps=1)
+    sets = G.calibrate_oracle(L, 2.75, 2.75)
+    return w, L, sets, G.lib_params(sets)
+
+
+def _check_tokens(rk, rv, k, v, sets, per_seq, dst0, T):
+    """Every token's record entries at cache positions dst0 .. dst0 + T - 1 against the oracle encode of the
+    same vectors: each entry within 1 LSB, at most 1e-4 of all the entries checked different, and nothing
+    written outside those positions."""
+    B, Hkv = k.shape[:2]
+    n_diff, n_all = 0.0, 0
+    for b in range(B):
+        for h in range(Hkv):
+            pk, pv = sets[G.set_index(b, h, Hkv, per_seq)]
+            for rec, x, p in ((rk[b, h], k[b, h], pk), (rv[b, h], v[b, h], pv)):
+                got = G.tokens_of(rec, p, dst0, T)
+                ref = G.tokens_of(O.encode(x, p), p, 0, T)
+                tf, dz, ds, cf, dc, ef = G.token_diff(got, ref, p)
+                assert dc <= 1 and dz <= 1 and ds <= 1, (b, h, dz, ds, dc)
+                n = T * (int(np.count_nonzero(p.widths)) + 2)
+                n_diff += ef * n
+                n_all += n
+                z, s, c = O.unpack(rec, p)
+                outside = np.r_[0:dst0, dst0 + T:len(z)]
+                assert not np.any(z.view(np.uint16)[outside]) and not np.any(s.view(np.uint16)[outside])
+                assert not np.any(c[outside])
+    frac = n_diff / n_all
+    assert frac <= 1e-4, (frac, round(n_diff), n_all)
+    return frac
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("dst0", [0, 5])
+def test_encode_paths_bf16_llama_shape(llama_300, path, dst0):
+    """The CUDA-core path and the tensor-core path against the oracle on 8 bf16 heads with a ragged last tile;
+    an odd write offset makes value records straddle tile edges and share a record with an unwritten token."""
+    w, L, sets, P = llama_300
+    kvtc.kv_debug_set_encode_path(path)
+    try:
+        rk, rv = _encode_gpu(P, L.k, L.v, False, T_cap=320, dst0=dst0)
+    finally:
+        kvtc.kv_debug_set_encode_path(0)
+    _check_tokens(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, False, dst0, L.k.shape[2])
+
+
+@pytest.mark.parametrize("bits", [1.33, 4.0, 8.0])
+def test_encode_tensor_core_budgets_per_sequence(bits):
+    """Tensor-core encode at 5, 16 and 33 record words (the last with two accumulator groups, for shared
+    memory), one parameter set per (sequence, head)."""
+    w = synth.WORKLOADS["qwen_batched_8k"]
+    L = synth.make_layer(w, T=200, B=2, steps=1)
+    sets = G.calibrate_oracle(L, bits, bits)
+    P = G.lib_params(sets)
+    kvtc.kv_debug_set_encode_path(2)
+    try:
+        rk, rv = _encode_gpu(P, L.k, L.v, True, T_cap=208, dst0=3)
+    finally:
+        kvtc.kv_debug_set_encode_path(0)
+    _check_tokens(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, True, 3, 200)
+
+
+def test_encode_tensor_core_rejects_fp32(tiny):
+    w, L, sets, P = tiny
+    kvtc.kv_debug_set_encode_path(2)
+    try:
+        k, v = np.ascontiguousarray(L.k[:, :, :128]), np.ascontiguousarray(L.v[:, :, :128])
+        rk = torch.zeros((1, 1, 128, P.record_words(0)), dtype=torch.int32, device="cuda")
+        rv = torch.zeros(G.value_cache_shape(1, 1, 128, P.record_words(1)), dtype=torch.int32, device="cuda")
+        cache = kvtc.make_cache(rk, rv, 1, 1, 128, False)
+        pos = torch.zeros((1,), dtype=torch.int64, device="cuda")
+        with pytest.raises(kvtc.KvError) as e:
+            kvtc.kv_encode(P, cache, G.to_dev_storage(k), G.to_dev_storage(v), kvtc.KV_DTYPE_F32, 1, 128, pos)
+        assert e.value.status == kvtc.KV_ERR_UNSUPPORTED
+    finally:
+        kvtc.kv_debug_set_encode_path(0)
+
+
+def test_encode_full_size_llama_32k_sampled():
+    """Prefill of the 32K-token Llama-shaped layer through kv_encode in its default configuration (the
+    tensor-core path): 1024 sampled token pairs per head against the oracle encode of the same vectors."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    L = synth.make_layer(w, steps=1)
+    sets = G.calibrate_oracle(L, 2.75, 2.75)
+    P = G.lib_params(sets)
+    T = w.T
+    rk, rv = _encode_gpu(P, L.k, L.v, False, T_cap=T + 512)
+    rng = np.random.default_rng(7)
+    n_diff, n_all = 0.0, 0
+    for h in range(w.Hkv):
+        pk, pv = sets[h]
+        pairs = np.sort(rng.choice(T // 2, 1024, replace=False))
+        toks = np.stack([2 * pairs, 2 * pairs + 1], 1).reshape(-1)
+        kx, vx = synth.as_float(L.k[0, h, toks]), synth.as_float(L.v[0, h, toks])
+        ga = O.unpack(rk[0, h, toks], pk)
+        gv = O.unpack(rv[0, h, pairs], pv)
+        for got, ref, p in ((ga, O.unpack(O.encode(kx, pk), pk), pk), (gv, O.unpack(O.encode(vx, pv), pv), pv)):
+            tf, dz, ds, cf, dc, ef = G.token_diff(got, ref, p)
+            assert dc <= 1 and dz <= 1 and ds <= 1, (h, dz, ds, dc)
+            n = len(toks) * (int(np.count_nonzero(p.widths)) + 2)
+            n_diff += ef * n
+            n_all += n
+    assert n_diff / n_all <= 1e-4, (n_diff / n_all, round(n_diff), n_all)
+
+
 def test_append_matches_prefill(tiny):
     w, L, sets, P = tiny
     T = 200

@@ -14,7 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libkvtc.so")
 SOURCES = ["kvtc_host.cpp", "kvtc_kernels.cu"]
-HEADERS = ["kvtc_internal.h", "kvtc_ptx.cuh", "kvtc_codec.cuh"]
+HEADERS = ["kvtc_internal.h", "kvtc_ptx.cuh", "kvtc_codec.cuh", "kvtc_tc.cuh", "kvtc_encode.cuh",
+           "kvtc_encode_tc.cuh", "kvtc_decode.cuh", "kvtc_bf16.cuh", "kvtc_debug.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

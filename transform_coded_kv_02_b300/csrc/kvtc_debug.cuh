@@ -1,0 +1,104 @@
+// Parity and self-test kernels behind the kv_debug_* entry points.
+// Part of the single CUDA translation unit of the library (included once by kvtc_kernels.cu).
+#pragma once
+
+namespace kvtc {
+
+// ======================================================================================================
+// parity and self-test kernels
+// ======================================================================================================
+__global__ void __launch_bounds__(256) debug_qp_warp_kernel(ParamsDev P, int set, int tensor, const float* y,
+                                                            long long n, uint32_t* rec) {
+  __shared__ uint32_t rec_s[8][2 * MAX_RW + 4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long t = (long long)blockIdx.x * 8 + warp;
+  if (t >= n) return;
+  const TensorDev& td = P.t[tensor];
+  const float4 v = *reinterpret_cast<const float4*>(y + (size_t)t * D + 4 * lane);
+  const float yy[4] = {v.x, v.y, v.z, v.w};
+  uint32_t* out = tensor == 0 ? rec + (size_t)t * td.r_words : rec + (size_t)(t >> 1) * 2 * td.r_words;
+  quantize_pack_warp(td, set, yy, lane, rec_s[warp], out, tensor == 1, (int)(t & 1));
+}
+
+__global__ void __launch_bounds__(128) debug_qp_thread_kernel(ParamsDev P, int set, int tensor, const float* y,
+                                                              long long n, uint32_t* rec) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n) return;
+  const TensorDev& td = P.t[tensor];
+  const float* yr = y + (size_t)t * D;
+  if (tensor == 0) {
+    uint32_t* out = rec + (size_t)t * td.r_words;
+    quantize_pack_thread(td, set, false, [&](int j) { return yr[j]; }, [&](int w, uint32_t val) { out[w] = val; });
+  } else {
+    uint32_t* out = rec + (size_t)(t >> 1) * 2 * td.r_words;
+    const int half = (int)(t & 1);
+    quantize_pack_thread(td, set, true, [&](int j) { return yr[j]; }, [&](int w, uint32_t val) {
+      if (w == 0)
+        out[half] = val;
+      else
+        reinterpret_cast<uint16_t*>(out)[2 * w + half] = (uint16_t)val;
+    });
+  }
+}
+
+kv_status launch_debug_quantize_pack(const ParamsDev& P, int set, int tensor, const float* y, int64_t n,
+                                     uint32_t* rec, int variant, cudaStream_t s) {
+  if (variant == 0)
+    debug_qp_warp_kernel<<<(unsigned)((n + 7) / 8), 256, 0, s>>>(P, set, tensor, y, n, rec);
+  else
+    debug_qp_thread_kernel<<<(unsigned)((n + 127) / 128), 128, 0, s>>>(P, set, tensor, y, n, rec);
+  return launch_check("debug quantize/pack");
+}
+
+// The decoder's slot extraction (unpack_pair) over records: one thread per (record, slot); writes integer
+// codes [n tokens][128]. Keys: slot k of token t gives channels 2k, 2k+1; values: slot j of record p gives
+// channel j of tokens 2p, 2p+1.
+__global__ void __launch_bounds__(128) debug_unpack_kernel(ParamsDev P, int set, int tensor, const uint32_t* rec,
+                                                           long long n, uint16_t* codes) {
+  const TensorDev& td = P.t[tensor];
+  const int R = td.r_words;
+  const long long n_rec = tensor == 0 ? n : (n + 1) / 2;
+  const int n_slot = tensor == 0 ? D / 2 : D;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_rec * n_slot) return;
+  const long long r = idx / n_slot;
+  const int k = (int)(idx - r * n_slot);
+  const uint32_t desc = td.slots[(size_t)set * D + k];
+  const uint32_t u = desc & 255u, sh = (desc >> 8) & 255u;
+  if (tensor == 0) {
+    const uint32_t h2 = unpack_pair(rec[r * R + 1 + u], sh, slot_mask(desc));
+    const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+    codes[r * D + 2 * k] = (uint16_t)(__low2float(hv) - 0.5f);
+    codes[r * D + 2 * k + 1] = (uint16_t)(__high2float(hv) - 0.5f);
+  } else {
+    const uint32_t h2 = unpack_pair(rec[r * 2 * R + 2 + u], sh, slot_mask(desc));
+    const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+    codes[(2 * r) * D + k] = (uint16_t)(__low2float(hv) - 0.5f);
+    if (2 * r + 1 < n) codes[(2 * r + 1) * D + k] = (uint16_t)(__high2float(hv) - 0.5f);
+  }
+}
+
+kv_status launch_debug_unpack(const ParamsDev& P, int set, int tensor, const uint32_t* rec, int64_t n,
+                              uint16_t* codes, cudaStream_t s) {
+  const long long work = (tensor == 0 ? n : (n + 1) / 2) * (long long)(tensor == 0 ? D / 2 : D);
+  debug_unpack_kernel<<<(unsigned)((work + 127) / 128), 128, 0, s>>>(P, set, tensor, rec, n, codes);
+  return launch_check("debug unpack");
+}
+
+__global__ void wait_selftest_kernel(long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait_bounded(smem_u32(&bar), 0u, limit_ns);  // no arrival will ever come
+  __syncthreads();
+}
+
+kv_status launch_wait_selftest(cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(g_wait_limit_ns);
+  return launch_check("wait self-test");
+}
+
+}  // namespace kvtc

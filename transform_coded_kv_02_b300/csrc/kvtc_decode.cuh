@@ -1,0 +1,797 @@
+// Decode over packed records: q preparation and the split-K flash-decode kernel with its launcher.
+// Part of the single CUDA translation unit of the library (included once by kvtc_kernels.cu).
+#pragma once
+
+namespace kvtc {
+
+// ======================================================================================================
+// decode over packed records
+// ======================================================================================================
+constexpr int PSTR = 132;          // floats per (split, head) partial: m, l, z, -, A[128]
+constexpr int DWARPS = 4;          // token groups per tile: a key warp and a value warp each
+constexpr int DT = 16 * DWARPS;    // tokens per ring stage (16 per warp pair)
+constexpr int DTHREADS = 64 * DWARPS;  // key warps 0..3, value warps 4..7; lane 0 of warp 0 issues the copies
+constexpr int RING_BUDGET = 48 * 1024;
+constexpr int MAX_STAGES = 8;
+constexpr int MAX_SPLITS = 256;
+constexpr int TAIL_RESERVE = MAX_SPLITS * MAX_G * 4 + 4 * MAX_G * 4;  // split weights, head state
+
+struct DecArgs {
+  const uint32_t* rec[2];
+  const __nv_bfloat16* q;
+  const int32_t* seq_lens;
+  __half* qa;       // [B*Hkv][16][128]: row 2h (+1) = fp16 hi (lo) part of q' of head h
+  float* qc;        // [B*Hkv][16]: C0 of heads 0..7, C1 of heads 0..7 (base-2 logit units)
+  unsigned* cnt;    // [B*Hkv] arrival counters
+  float* part;      // [B*Hkv][splits][g][PSTR] split partials
+  float* out;       // [B][Hq][128]
+  long long T_cap;
+  long long wait_ns;
+  int B, Hkv, Hq, g, per_seq, splits, chunk, stages;
+  float scale_log2;
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---- q preparation: one CTA per (sequence, KV head) ---------------------------------------------------
+// q~ = T_K q for the g query heads (T_K rows staged in shared memory by one bulk copy, every other input
+// fetched while it flies); q'_j = a log2(e) q~_j sigma_j 2^-b_j as fp16 hi + lo; C0 = a log2(e) q.(T_K^T mu);
+// C1 = a log2(e) sum_{b_j > 0} q~_j sigma_j. 256 threads: channel j = tid % 128, half of the k range = tid / 128.
+constexpr int QP_THREADS = 256;
+static size_t qprep_smem_bytes() { return (size_t)D * D * 4 + 2 * (size_t)MAX_G * D * 4; }
+
+__global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs a) {
+  pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* Ts = reinterpret_cast<float*>(smem);    // [nz][128]
+  float* qs = Ts + D * D;                        // [g][128]
+  float* hs = qs + MAX_G * D;                    // [8][128] upper-half partial sums
+  __shared__ uint64_t bar;
+  __shared__ float red[4][2][MAX_G];
+  const int kh = blockIdx.x, b = blockIdx.y;
+  const int bh = b * a.Hkv + kh;
+  const int set = a.per_seq ? bh : kh;
+  const TensorDev& tk = P.t[0];
+  const int g = a.g, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j = tid & (D - 1), hf = tid >> 7;
+  const int nz = tk.nz[set];
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0 && nz > 0) {
+    mbar_expect_tx(smem_u32(&bar), (uint32_t)nz * D * 4);
+    bulk_g2s(smem_u32(Ts), tk.T + (size_t)set * D * D, (uint32_t)nz * D * 4, smem_u32(&bar));
+  }
+  // everything else is fetched while T_K is in flight
+  const float sg = tk.sigma[(size_t)set * D + j];
+  const int bw = tk.widths[(size_t)set * D + j];
+  const float bk = tk.base[(size_t)set * D + j];
+  const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kh * g) * D;
+  for (int i = tid; i < g * D; i += QP_THREADS) qs[i] = __bfloat162float(qg[i]);
+  bool ok = true;
+  if (nz > 0) ok = mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);
+  if (!ok && tid == 0) mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);  // drain before leaving
+  if (__syncthreads_or(!ok)) return;
+
+  float qt[MAX_G];
+#pragma unroll
+  for (int h = 0; h < MAX_G; ++h) qt[h] = 0.f;
+  if (j < nz) {
+    const float4* Trow = reinterpret_cast<const float4*>(Ts + (size_t)j * D) + 16 * hf;
+#pragma unroll 4
+    for (int k4 = 0; k4 < 16; ++k4) {
+      const int kk = (k4 + j) & 15;   // rotated start: conflict-free row reads
+      const float4 t = Trow[kk];
+#pragma unroll
+      for (int h = 0; h < MAX_G; ++h) {
+        if (h < g) {
+          const float4 qv = reinterpret_cast<const float4*>(qs + h * D)[16 * hf + kk];
+          qt[h] = fmaf(t.x, qv.x, fmaf(t.y, qv.y, fmaf(t.z, qv.z, fmaf(t.w, qv.w, qt[h]))));
+        }
+      }
+    }
+  }
+  if (hf == 1) {
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) hs[h * D + j] = qt[h];
+  }
+  __syncthreads();
+  if (hf == 0) {
+    __half* qa = a.qa + (size_t)bh * 16 * D;
+    float c0p[MAX_G], c1p[MAX_G];
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) {
+      const float q_t = qt[h] + hs[h * D + j];
+      const bool on = h < g && bw > 0;
+      const float qp = on ? a.scale_log2 * q_t * sg * exp2i(-bw) : 0.f;
+      const __half hi = __float2half_rn(qp);
+      const __half lo = __float2half_rn(qp - __half2float(hi));
+      qa[(2 * h) * D + j] = hi;
+      qa[(2 * h + 1) * D + j] = lo;
+      c1p[h] = on ? q_t * sg : 0.f;
+      c0p[h] = h < g ? bk * qs[h * D + j] : 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) {
+      const float s0 = warp_sum(c0p[h]), s1 = warp_sum(c1p[h]);
+      if (lane == 0) {
+        red[warp][0][h] = s0;
+        red[warp][1][h] = s1;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < g) {
+    const int h = tid;
+    a.qc[bh * 16 + h] = a.scale_log2 * (red[0][0][h] + red[1][0][h] + red[2][0][h] + red[3][0][h]);
+    a.qc[bh * 16 + 8 + h] = a.scale_log2 * (red[0][1][h] + red[1][1][h] + red[2][1][h] + red[3][1][h]);
+  }
+  if (tid == 0) a.cnt[bh] = 0u;
+}
+
+// ---- split-K decode ----------------------------------------------------------------------------------
+constexpr uint32_t PAIR_BYTES_PER_NB = 16u * 8u * 2u + 4u * 4u;  // P tile (16 tokens x 8 columns) + 4 factors
+
+struct DecSmem {  // byte offsets into the dynamic shared memory of decode_kernel
+  uint32_t stage_bytes, ps, epi_ws, epi_merged, tail_reserve, total;
+};
+
+__host__ __device__ __forceinline__ uint32_t align128u(uint32_t x) { return (x + 127u) & ~127u; }
+
+// main loop: ring | per-pair P tiles and rescale factors
+// epilogue (ring dead): T'_V rows [0, 64 KB) | per-warp partials | merged partial
+// tail: split partial chunks from 0 | per-split weights and per-head state in the reserve at the end
+__host__ __device__ inline DecSmem decode_smem(int RK, int RV, int stages, int nb) {
+  DecSmem s;
+  s.stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
+  s.ps = align128u(stages * s.stage_bytes);
+  const uint32_t main_end = s.ps + DWARPS * PAIR_BYTES_PER_NB * nb;
+  s.epi_ws = D * D * 4u;
+  s.epi_merged = s.epi_ws + DWARPS * 8u * PSTR * 4u;
+  const uint32_t epi_end = s.epi_merged + (MAX_G * D + 4 * MAX_G) * 4u;
+  s.tail_reserve = align128u(main_end > epi_end ? main_end : epi_end);
+  s.total = s.tail_reserve + TAIL_RESERVE;
+  return s;
+}
+
+__host__ __device__ constexpr int ring_stages_for(int RK, int RV) {
+  return (RING_BUDGET / (DT * (RK + RV) * 4)) > MAX_STAGES ? MAX_STAGES
+         : (RING_BUDGET / (DT * (RK + RV) * 4)) < 2      ? 2
+                                                          : RING_BUDGET / (DT * (RK + RV) * 4);
+}
+
+// plain shared-memory word load (byte offset into the dynamic region): the compiler is free to schedule it
+template <class T>
+__device__ __forceinline__ uint32_t ldsw(const T* base, uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(base) + off);
+}
+
+// RT > 0: keys and values both use records of RT words; the ring stage size and count and the offsets between
+// a lane's two tokens (two records) are compile-time, so each staged-record address is one add away.
+template <int NB, int RT>
+__global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  // barriers live outside the dynamic region, which the epilogue and the tail reuse wholesale
+  __shared__ __align__(8) uint64_t full[MAX_STAGES], empty[MAX_STAGES], pF[DWARPS], pE[DWARPS], tbar_s;
+  __shared__ int s_abort, s_last, s_issued;
+  const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  const int bh = b * a.Hkv + kh;
+  const int set = a.per_seq ? bh : kh;
+  const TensorDev& TK = P.t[0];
+  const TensorDev& TV = P.t[1];
+  const int RK = RT ? RT : TK.r_words, RV = RT ? RT : TV.r_words;
+  constexpr int NS_CT = RT ? ring_stages_for(RT, RT) : 0;
+  const int NS = RT ? NS_CT : a.stages, g = a.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  const int nzK = TK.nz[set], nzV = TV.nz[set];
+  const int nkb = (nzK + 15) >> 4, nmb = (nzV + 15) >> 4;
+  const DecSmem L = decode_smem(RK, RV, NS, NB);
+  const uint32_t stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
+  uint64_t* tbar = &tbar_s;
+
+  const long long Lseq = min((long long)a.seq_lens[b], a.T_cap);
+  const long long t0 = (long long)split * a.chunk;
+  const long long t1 = min(t0 + (long long)a.chunk, Lseq);
+  const int ntiles = t1 > t0 ? (int)((t1 - t0 + DT - 1) / DT) : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 2 * DWARPS);  // every key and value warp releases each stage
+    }
+    for (int p = 0; p < DWARPS; ++p) {
+      mbar_init(smem_u32(&pF[p]), 1);
+      mbar_init(smem_u32(&pE[p]), 1);
+    }
+    mbar_init(smem_u32(tbar), 1);
+    fence_mbar_init();
+    s_abort = 0;
+    s_issued = 0;
+  }
+  __syncthreads();
+
+  // ---- record tiles stream into the ring by bulk copies that lane 0 of warp 0 issues ----
+  const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
+  const uint32_t* vrec = a.rec[1] + (size_t)bh * a.T_cap * RV;  // two-token records: same bytes per token
+  const bool issuer = tid == 0;
+  int next_issue = 0;  // meaningful in the issuing thread only
+  auto issue_tile = [&](int i) {
+    const int s = i % NS;
+    const long long tb = t0 + (long long)i * DT;
+    long long n = min((long long)DT, t1 - tb);
+    n = min((n + 3) & ~3LL, a.T_cap - tb);
+    const uint32_t kbytes = (uint32_t)(n * RK * 4), vbytes = (uint32_t)(n * RV * 4);
+    const uint32_t bar = smem_u32(&full[s]);
+    const uint32_t dst = smem_u32(smem + (size_t)s * stage_bytes);
+    mbar_expect_tx(bar, kbytes + vbytes);
+    bulk_g2s(dst, krec + tb * RK, kbytes, bar);
+    bulk_g2s(dst + DT * RK * 4, vrec + tb * RV, vbytes, bar);
+  };
+  // issue tiles up to `upto`; blocking: wait for each ring slot to be released, else stop at the first busy one
+  auto issue_until = [&](int upto, bool blocking) {
+    while (next_issue <= upto && next_issue < ntiles) {
+      if (next_issue >= NS) {
+        const uint32_t eb = smem_u32(&empty[next_issue % NS]), par = (uint32_t)((next_issue / NS - 1) & 1);
+        if (blocking) {
+          if (!mbar_wait_bounded(eb, par, a.wait_ns)) {
+            s_abort = 1;
+            return;
+          }
+        } else if (!mbar_test(eb, par)) {
+          return;
+        }
+      }
+      issue_tile(next_issue);
+      ++next_issue;
+    }
+  };
+  if (issuer) {
+    if (split == 0 && nzV > 0)  // every split's epilogue reads the scaled T_V rows: warm L2 now
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(TV.Tsc + (size_t)set * D * D),
+                   "r"((uint32_t)nzV * D * 4)
+                   : "memory");
+    issue_until(NS - 1, false);
+  }
+  // ============ warp pairs: key warp pw and value warp pw + 4 own tokens [16 pw, 16 pw + 16) of every tile ============
+  // Codes go from the staged records straight into MMA operand registers.
+  //  key warp, logits A operand (16 tokens x 16 channels of block kb): key slot 8kb + tig holds channels
+  //    (16kb + 2tig, +1), slot 8kb + 4 + tig channels (16kb + 8 + 2tig, +1); rows gid, gid + 8 = tokens gid, gid + 8.
+  //  value warp, P.V A operand (16 channels x 16 tokens): value slot 16mb + gid (+ 8) holds that channel for the
+  //    two tokens of a value record; the pair's records tig and tig + 4 hold tokens (2tig, 2tig+1), (2tig+8, 2tig+9).
+  // The key warp hands P (fp16 hi/lo of p s_V) and the heads' rescale factors to the value warp through shared
+  // memory, guarded by two mbarriers per pair (filled / emptied), whose waits are bounded like every other.
+  const int pw = warp & 3;
+  const bool kwarp = warp < 4;
+  uint8_t* pair_smem = smem + L.ps + (size_t)pw * PAIR_BYTES_PER_NB * NB;
+  __half* ps = reinterpret_cast<__half*>(pair_smem);                          // [16 tokens][8 NB columns]
+  float* pcorr = reinterpret_cast<float*>(pair_smem + 16 * 8 * NB * 2);       // [NB][4]
+  float* ws = reinterpret_cast<float*>(smem + L.epi_ws);                       // [DWARPS][8][PSTR]
+  const uint32_t kstep = 8u * RK * 4, vstep = 4u * 2 * RV * 4;
+  if (kwarp) {
+    const uint32_t krow = (uint32_t)(16 * pw + gid) * RK * 4;
+    uint32_t ka[8][2], ks[8][2], km[8][2];
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t dk = kb < nkb ? __ldg(TK.slots + (size_t)set * D + 8 * kb + 4 * i + tig) : 0u;
+        ka[kb][i] = krow + 4u * (1u + (dk & 255u));
+        ks[kb][i] = (dk >> 8) & 255u;
+        km[kb][i] = slot_mask(dk);
+      }
+    // z/s words: key record of token gid; value record (gid >> 1), half gid & 1; tokens gid + 8 one step on
+    const uint32_t kz = krow;
+    const uint32_t vz = (uint32_t)DT * RK * 4 + (uint32_t)(8 * pw + (gid >> 1)) * 2 * RV * 4 + 4u * (gid & 1);
+    float m_run[NB], l_run[NB], z_run[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      m_run[nb] = -INFINITY;
+      l_run[nb] = 0.f;
+      z_run[nb] = 0.f;
+    }
+    // q' (B operand of the logits MMA) and the folded constants come from qprep_kernel
+    pdl_wait();
+    uint32_t qb[8][NB][2];
+    {
+      const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(a.qa + (size_t)bh * 16 * D);
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const int col = nb * 8 + gid;
+          qb[kb][nb][0] = kb < nkb ? qa32[(col * D + kb * 16 + 2 * tig) >> 1] : 0u;
+          qb[kb][nb][1] = kb < nkb ? qa32[(col * D + kb * 16 + 8 + 2 * tig) >> 1] : 0u;
+        }
+    }
+    float c0[NB], c1[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const int h = tig + 4 * nb;
+      c0[nb] = h < g ? a.qc[bh * 16 + h] : 0.f;
+      c1[nb] = h < g ? a.qc[bh * 16 + 8 + h] : 0.f;
+    }
+    int hand = 0;  // handoffs to the value warp so far
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % NS;
+      const uint8_t* st = smem + (size_t)s * stage_bytes;
+      if (issuer) issue_until(i, true);
+      // every lane takes the stage's data through its own wait; the verdict is made warp-uniform
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
+      }
+      const long long my_t0 = t0 + (long long)i * DT + 16 * pw;
+      if (my_t0 >= t1) {  // this pair's tokens are past the end
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (issuer) issue_until(i + NS - 1, false);
+        continue;
+      }
+      const uint32_t kzw0 = ldsw(st, kz), kzw1 = ldsw(st, kz + kstep);
+      const uint32_t vzw0 = ldsw(st, vz), vzw1 = ldsw(st, vz + vstep);
+      // ---- logits: A = key codes (16 tokens x 16 channels), B = q' (16 channels x 8 columns) ----
+      float acc2[2][NB][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) acc2[u][nb][0] = acc2[u][nb][1] = acc2[u][nb][2] = acc2[u][nb][3] = 0.f;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        if (kb < nkb) {
+          uint32_t af[4];
+          af[0] = unpack_pair(ldsw(st, ka[kb][0]), ks[kb][0], km[kb][0]);
+          af[1] = unpack_pair(ldsw(st, ka[kb][0] + kstep), ks[kb][0], km[kb][0]);
+          af[2] = unpack_pair(ldsw(st, ka[kb][1]), ks[kb][1], km[kb][1]);
+          af[3] = unpack_pair(ldsw(st, ka[kb][1] + kstep), ks[kb][1], km[kb][1]);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(acc2[kb & 1][nb], af, qb[kb][nb][0], qb[kb][nb][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // the key warp is done with the stage
+      if (issuer) issue_until(i + NS - 1, false);
+      const bool valid0 = my_t0 + gid < t1, valid1 = my_t0 + gid + 8 < t1;
+      const float zk0 = half_bits_to_float(kzw0), sk0 = half_bits_to_float(kzw0 >> 16);
+      const float zk1 = half_bits_to_float(kzw1), sk1 = half_bits_to_float(kzw1 >> 16);
+      const float zv0 = half_bits_to_float(vzw0), sv0 = half_bits_to_float(vzw0 >> 16);
+      const float zv1 = half_bits_to_float(vzw1), sv1 = half_bits_to_float(vzw1 >> 16);
+      uint32_t e0[NB], e1[NB];
+      float corr[NB];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const float r0 = (acc2[0][nb][0] + acc2[1][nb][0]) + (acc2[0][nb][1] + acc2[1][nb][1]);
+        const float r1 = (acc2[0][nb][2] + acc2[1][nb][2]) + (acc2[0][nb][3] + acc2[1][nb][3]);
+        const float l0 = valid0 ? fmaf(sk0, r0, fmaf(zk0, c1[nb], c0[nb])) : -INFINITY;
+        const float l1 = valid1 ? fmaf(sk1, r1, fmaf(zk1, c1[nb], c0[nb])) : -INFINITY;
+        float mt = fmaxf(l0, l1);
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        const float m_new = fmaxf(m_run[nb], mt);
+        corr[nb] = (m_run[nb] == m_new) ? 1.f : exp2f(m_run[nb] - m_new);
+        const float p0 = valid0 ? exp2f(l0 - m_new) : 0.f;
+        const float p1 = valid1 ? exp2f(l1 - m_new) : 0.f;
+        l_run[nb] = fmaf(l_run[nb], corr[nb], p0 + p1);
+        z_run[nb] = fmaf(z_run[nb], corr[nb], (valid0 ? p0 * zv0 : 0.f) + (valid1 ? p1 * zv1 : 0.f));
+        m_run[nb] = m_new;
+        const float w0 = valid0 ? p0 * sv0 : 0.f, w1 = valid1 ? p1 * sv1 : 0.f;
+        const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
+        e0[nb] = pack_half2(h0, __float2half_rn(w0 - __half2float(h0)));
+        e1[nb] = pack_half2(h1, __float2half_rn(w1 - __half2float(h1)));
+      }
+      // ---- hand P and the rescale factors to the value warp ----
+      if (hand > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&pE[pw]), (uint32_t)((hand - 1) & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
+      }
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        reinterpret_cast<uint32_t*>(ps)[(gid * 8 * NB + nb * 8 + 2 * tig) >> 1] = e0[nb];
+        reinterpret_cast<uint32_t*>(ps)[((gid + 8) * 8 * NB + nb * 8 + 2 * tig) >> 1] = e1[nb];
+        if (gid == 0) pcorr[nb * 4 + tig] = corr[nb];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&pF[pw]));
+      ++hand;
+    }
+    if (issuer) s_issued = next_issue;
+    // this pair's softmax state into the per-pair partial (the region lies past the ring)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      l_run[nb] += __shfl_xor_sync(0xffffffffu, l_run[nb], 4);
+      l_run[nb] += __shfl_xor_sync(0xffffffffu, l_run[nb], 8);
+      l_run[nb] += __shfl_xor_sync(0xffffffffu, l_run[nb], 16);
+      z_run[nb] += __shfl_xor_sync(0xffffffffu, z_run[nb], 4);
+      z_run[nb] += __shfl_xor_sync(0xffffffffu, z_run[nb], 8);
+      z_run[nb] += __shfl_xor_sync(0xffffffffu, z_run[nb], 16);
+      const int h = tig + 4 * nb;
+      if (h < g && gid == 0) {
+        float* w = ws + (pw * 8 + h) * PSTR;
+        w[0] = m_run[nb];
+        w[1] = l_run[nb];
+        w[2] = z_run[nb];
+      }
+    }
+  } else {
+    const uint32_t vrow = (uint32_t)DT * RK * 4 + (uint32_t)(8 * pw + tig) * 2 * RV * 4;
+    uint32_t va[8][2], vsh[8][2], vm[8][2];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t dv = mb < nmb ? __ldg(TV.slots + (size_t)set * D + 16 * mb + 8 * i + gid) : 0u;
+        va[mb][i] = vrow + 4u * (2u + (dv & 255u));
+        vsh[mb][i] = (dv >> 8) & 255u;
+        vm[mb][i] = slot_mask(dv);
+      }
+    float acc_o[8][NB][4];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] = 0.f;
+    const uint32_t pa = smem_u32(ps + (lane & 15) * 8 * NB);
+    int hand = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % NS;
+      const uint8_t* st = smem + (size_t)s * stage_bytes;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
+      }
+      const long long my_t0 = t0 + (long long)i * DT + 16 * pw;
+      if (my_t0 >= t1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        continue;
+      }
+      // value codes of this pair's 16 tokens: with one column block they are taken while the key warp works on
+      // the logits (and the stage released early); with two, registers are short and they go straight to the MMA
+      uint32_t vf[NB == 1 ? 8 : 1][4];
+      if constexpr (NB == 1) {
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+          if (mb < nmb) {
+            vf[mb][0] = unpack_pair(ldsw(st, va[mb][0]), vsh[mb][0], vm[mb][0]);
+            vf[mb][1] = unpack_pair(ldsw(st, va[mb][1]), vsh[mb][1], vm[mb][1]);
+            vf[mb][2] = unpack_pair(ldsw(st, va[mb][0] + vstep), vsh[mb][0], vm[mb][0]);
+            vf[mb][3] = unpack_pair(ldsw(st, va[mb][1] + vstep), vsh[mb][1], vm[mb][1]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // the value warp is done with the stage
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&pF[pw]), (uint32_t)(hand & 1), a.wait_ns))) {
+        s_abort = 1;
+        break;
+      }
+      uint32_t bp[NB][2];
+      float corr[NB];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        ldsm_x2_t(pa + nb * 16, bp[nb][0], bp[nb][1]);
+        corr[nb] = pcorr[nb * 4 + tig];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&pE[pw]));
+      ++hand;
+      // accumulator columns 2tig, 2tig+1 are head tig (+4 nb)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        if (__any_sync(0xffffffffu, corr[nb] != 1.f)) {
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] *= corr[nb];
+        }
+      }
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        if (mb < nmb) {
+          uint32_t af[4];
+          if constexpr (NB == 1) {
+            af[0] = vf[mb][0], af[1] = vf[mb][1], af[2] = vf[mb][2], af[3] = vf[mb][3];
+          } else {
+            af[0] = unpack_pair(ldsw(st, va[mb][0]), vsh[mb][0], vm[mb][0]);
+            af[1] = unpack_pair(ldsw(st, va[mb][1]), vsh[mb][1], vm[mb][1]);
+            af[2] = unpack_pair(ldsw(st, va[mb][0] + vstep), vsh[mb][0], vm[mb][0]);
+            af[3] = unpack_pair(ldsw(st, va[mb][1] + vstep), vsh[mb][1], vm[mb][1]);
+          }
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(acc_o[mb][nb], af, bp[nb][0], bp[nb][1]);
+        }
+      }
+      if constexpr (NB != 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // the value warp is done with the stage
+      }
+    }
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const int h = tig + 4 * nb;
+      if (h < g) {
+        float* w = ws + (pw * 8 + h) * PSTR;
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+          if (mb < nmb) {
+            w[4 + mb * 16 + gid] = acc_o[mb][nb][0] + acc_o[mb][nb][1];
+            w[4 + mb * 16 + gid + 8] = acc_o[mb][nb][2] + acc_o[mb][nb][3];
+          }
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (s_abort) {  // drain the copies this CTA may still have in flight, then leave
+    if (tid == 0) {
+      const int issued = s_issued;
+      for (int i = max(0, issued - NS); i < issued; ++i)
+        mbar_wait_bounded(smem_u32(&full[i % NS]), (uint32_t)((i / NS) & 1), a.wait_ns);
+    }
+    __syncthreads();
+    return;
+  }
+
+  // ================= epilogue: this split's partial, mapped to the original basis =================
+  // N_h[k] = Z_h w_k + sum_j T'[j][k] A_h[j] with T'[j][k] = T_V[j][k] sigma_j 2^-b_j and w_k = sum_{b_j>0} T_V[j][k]
+  // sigma_j, so that o_h[k] = base_k + (sum over splits e_s N_s,h[k]) / (sum over splits e_s L_s,h).
+  float* Tsc = reinterpret_cast<float*>(smem);                           // [nzV][128]
+  float* mA = reinterpret_cast<float*>(smem + L.epi_merged);             // [8][128]
+  float* mS = mA + MAX_G * D;                                            // M[8], L[8], Z[8]
+  if (tid == 0 && nzV > 0) {
+    fence_proxy_async_smem();
+    mbar_expect_tx(smem_u32(tbar), (uint32_t)nzV * D * 4);
+    bulk_g2s(smem_u32(Tsc), TV.Tsc + (size_t)set * D * D, (uint32_t)nzV * D * 4, smem_u32(tbar));
+  }
+  __syncthreads();
+  {
+    const int acols = 4 + nmb * 16;
+    for (int idx = tid; idx < g * acols; idx += DTHREADS) {
+      const int h = idx / acols, cidx = idx - h * acols;
+      if (cidx == 3) continue;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < DWARPS; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
+      if (cidx == 0) {
+        mS[h] = M;
+        continue;
+      }
+      float val = 0.f;
+#pragma unroll
+      for (int w = 0; w < DWARPS; ++w) {
+        const float mw = ws[(w * 8 + h) * PSTR];
+        const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        val = fmaf(e, ws[(w * 8 + h) * PSTR + cidx], val);
+      }
+      if (cidx == 1) mS[MAX_G + h] = val;
+      else if (cidx == 2) mS[2 * MAX_G + h] = val;
+      else mA[h * D + cidx - 4] = val;
+    }
+  }
+  bool okw = true;
+  if (nzV > 0) okw = mbar_wait_bounded(smem_u32(tbar), 0u, a.wait_ns);
+  if (!okw && tid == 0) mbar_wait_bounded(smem_u32(tbar), 0u, a.wait_ns);  // drain before leaving
+  if (__syncthreads_or(!okw)) return;
+  float* part = a.part + ((size_t)bh * a.splits + split) * g * PSTR;
+  if (tid < D) {
+    const int k = tid;
+    const float wk = TV.wsum[(size_t)set * D + k];
+    float n[MAX_G];
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h) n[h] = h < g ? mS[2 * MAX_G + h] * wk : 0.f;
+    for (int jj = 0; jj < nzV; ++jj) {
+      const float t = Tsc[jj * D + k];
+#pragma unroll
+      for (int h = 0; h < MAX_G; ++h)
+        if (h < g) n[h] = fmaf(t, mA[h * D + jj], n[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h)
+      if (h < g) part[h * PSTR + 4 + k] = n[h];
+  }
+  if (tid < g) {
+    part[tid * PSTR + 0] = mS[tid];
+    part[tid * PSTR + 1] = mS[MAX_G + tid];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&a.cnt[bh], 1u) == (unsigned)(a.splits - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ======== last CTA of (b, kh): weighted sum of the split partials (streamed by bulk copies) ========
+  float* esc = reinterpret_cast<float*>(smem + L.tail_reserve);   // [MAX_SPLITS][8] split weights of a chunk
+  float* hst = esc + MAX_SPLITS * MAX_G;                          // Mrun[8], Lrun[8], Mnew[8], scale[8]
+  const float* pb = a.part + (size_t)bh * a.splits * g * PSTR;
+  const int S = a.splits;
+  const uint32_t per_split = (uint32_t)g * PSTR * 4;
+  const int chunk_splits = max(1, min(S, min((int)(L.tail_reserve / per_split), MAX_SPLITS)));
+  const int items = g * D;
+  constexpr int ITEMS_PER_THREAD = MAX_G * D / DTHREADS;
+  float accN[ITEMS_PER_THREAD];
+#pragma unroll
+  for (int r = 0; r < ITEMS_PER_THREAD; ++r) accN[r] = 0.f;
+  if (tid < g) {
+    hst[tid] = -INFINITY;
+    hst[MAX_G + tid] = 0.f;
+  }
+  uint32_t tphase = nzV > 0 ? 1u : 0u;  // phase 0 of tbar went to the T' copy when there was one
+  fence_proxy_async_global();
+  const float* cp = reinterpret_cast<const float*>(smem);
+  for (int c0s = 0; c0s < S; c0s += chunk_splits) {
+    const int n = min(chunk_splits, S - c0s);
+    __syncthreads();  // previous chunk consumed
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      mbar_expect_tx(smem_u32(tbar), (uint32_t)n * per_split);
+      bulk_g2s(smem_u32(smem), pb + (size_t)c0s * g * PSTR, (uint32_t)n * per_split, smem_u32(tbar));
+    }
+    const bool okc = mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);
+    if (!okc && tid == 0) mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);  // drain before leaving
+    tphase ^= 1u;
+    if (!__syncthreads_and(okc)) return;
+    if (tid < g) {  // running maximum of head tid over the splits seen so far
+      const int h = tid;
+      float cm = -INFINITY;
+      for (int sp = 0; sp < n; ++sp) cm = fmaxf(cm, cp[(sp * g + h) * PSTR]);
+      const float Mo = hst[h], Mn = fmaxf(Mo, cm);
+      hst[2 * MAX_G + h] = Mn;
+      hst[3 * MAX_G + h] = (Mo == Mn) ? 1.f : exp2f(Mo - Mn);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < n * g; idx += DTHREADS) {
+      const int sp = idx / g, h = idx - sp * g;
+      const float ms = cp[(sp * g + h) * PSTR];
+      esc[sp * MAX_G + h] = (ms == -INFINITY) ? 0.f : exp2f(ms - hst[2 * MAX_G + h]);
+    }
+    __syncthreads();
+    if (tid < g) {
+      const int h = tid;
+      float l = hst[MAX_G + h] * hst[3 * MAX_G + h];
+      for (int sp = 0; sp < n; ++sp) l = fmaf(esc[sp * MAX_G + h], cp[(sp * g + h) * PSTR + 1], l);
+      hst[MAX_G + h] = l;
+      hst[h] = hst[2 * MAX_G + h];
+    }
+#pragma unroll
+    for (int r = 0; r < ITEMS_PER_THREAD; ++r) {
+      const int it = tid + r * DTHREADS;
+      if (it < items) {
+        const int h = it >> 7, k = it & (D - 1);
+        float acc = accN[r] * hst[3 * MAX_G + h];
+        for (int sp = 0; sp < n; ++sp) acc = fmaf(esc[sp * MAX_G + h], cp[(sp * g + h) * PSTR + 4 + k], acc);
+        accN[r] = acc;
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < ITEMS_PER_THREAD; ++r) {
+    const int it = tid + r * DTHREADS;
+    if (it < items) {
+      const int h = it >> 7, k = it & (D - 1);
+      const float Lh = hst[MAX_G + h];
+      a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] =
+          Lh > 0.f ? TV.base[(size_t)set * D + k] + accN[r] / Lh : 0.f;
+    }
+  }
+  if (tid == 0) a.cnt[bh] = 0u;
+}
+
+static void split_plan(int B, int Hkv, int64_t T_cap, int device, int tile, int per_sm, int max_splits,
+                       int* splits, int* chunk) {
+  const long long bh = (long long)B * Hkv;
+  const long long tiles = (T_cap + tile - 1) / tile;
+  long long sp = ((long long)per_sm * sm_count(device) + bh - 1) / bh;
+  sp = std::max(1LL, std::min(std::min(sp, tiles), (long long)max_splits));
+  const long long ct = (tiles + sp - 1) / sp;
+  *splits = (int)((tiles + ct - 1) / ct);
+  *chunk = (int)(ct * tile);
+}
+
+DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device) {
+  DecodeLayout L{};
+  split_plan(B, Hkv, T_cap, device, DT, 2, MAX_SPLITS, &L.splits, &L.chunk);
+  const size_t bh = (size_t)B * Hkv;
+  const int g = Hq / Hkv;
+  size_t o = 0;
+  L.off_qa = o;
+  o = align256(o + bh * 16 * D * sizeof(__half));
+  L.off_qc = o;
+  o = align256(o + bh * 16 * sizeof(float));
+  L.off_cnt = o;
+  o = align256(o + bh * sizeof(unsigned));
+  L.off_part = o;
+  o = align256(o + bh * (size_t)L.splits * g * PSTR * sizeof(float));
+  L.total = o;
+  return L;
+}
+
+// record lengths with a compile-time decode kernel (equal key and value budgets of 1.25 - 4 bits/element)
+static int compile_time_record_words(int RK, int RV) {
+  if (RK != RV) return 0;
+  switch (RK) {
+    case 5: case 8: case 11: case 12: case 16: return RK;
+    default: return 0;
+  }
+}
+
+template <int NB, int RT>
+static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a) {
+  cudaFuncSetAttribute(decode_kernel<NB, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RT>, P, a);
+}
+
+template <int NB>
+static cudaError_t launch_decode_nb(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a, int rt) {
+  switch (rt) {
+    case 5: return launch_decode_kernel<NB, 5>(cfg, P, a);
+    case 8: return launch_decode_kernel<NB, 8>(cfg, P, a);
+    case 11: return launch_decode_kernel<NB, 11>(cfg, P, a);
+    case 12: return launch_decode_kernel<NB, 12>(cfg, P, a);
+    case 16: return launch_decode_kernel<NB, 16>(cfg, P, a);
+    default: return launch_decode_kernel<NB, 0>(cfg, P, a);
+  }
+}
+
+kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
+                        const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
+                        cudaStream_t s) {
+  DecArgs a;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.rec[0] = c.k_rec;
+  a.rec[1] = c.v_rec;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.seq_lens = seq_lens;
+  a.qa = reinterpret_cast<__half*>(w + L.off_qa);
+  a.qc = reinterpret_cast<float*>(w + L.off_qc);
+  a.cnt = reinterpret_cast<unsigned*>(w + L.off_cnt);
+  a.part = reinterpret_cast<float*>(w + L.off_part);
+  a.out = out;
+  a.T_cap = c.T_cap;
+  a.wait_ns = g_wait_limit_ns;
+  a.B = B;
+  a.Hkv = c.Hkv;
+  a.Hq = Hq;
+  a.g = Hq / c.Hkv;
+  a.per_seq = c.per_seq_params;
+  a.splits = L.splits;
+  a.chunk = L.chunk;
+  const int rt = compile_time_record_words(P.t[0].r_words, P.t[1].r_words);
+  a.stages = ring_stages_for(P.t[0].r_words, P.t[1].r_words);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const size_t qsm = qprep_smem_bytes();
+  cudaFuncSetAttribute(qprep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qsm);
+  qprep_kernel<<<dim3(c.Hkv, B), QP_THREADS, qsm, s>>>(P, a);
+  kv_status st = launch_check("qprep_kernel");
+  if (st != KV_OK) return st;
+  const int nb = a.g <= 4 ? 1 : 2;
+  const size_t smem = decode_smem(P.t[0].r_words, P.t[1].r_words, a.stages, nb).total;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.splits, c.Hkv, B);
+  cfg.blockDim = dim3(DTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = nb == 1 ? launch_decode_nb<1>(cfg, P, a, rt) : launch_decode_nb<2>(cfg, P, a, rt);
+  if (e != cudaSuccess) {
+    set_error("decode_kernel launch: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
+  return launch_check("decode_kernel");
+}
+
+}  // namespace kvtc

@@ -1,0 +1,476 @@
+// Encode on the tensor cores: 128-token tiles, rotation y = X T^T by tcgen05 MMAs, thread-per-token quantiser.
+// Part of the single CUDA translation unit of the library (included once by kvtc_kernels.cu).
+//
+// Method: "KV Cache Compression Through the Lens of Transform Coding" (AATC), Key points (a decorrelating
+// orthogonal transform per head, then scalar quantisation of each rotated channel at its allocated width);
+// "SPHERICAL KV ..." page, third abstract (NOVA-KV: a fixed per-token bit count).
+//
+// Work unit = (tensor, sequence, KV head, tile of 128 new tokens). A persistent CTA owns a contiguous run of
+// units, so the transform of a (tensor, set) is staged once per run:
+//   TMA warp   T = T_hi + T_mid + T_lo (three bf16 matrices [128 channels][128 inputs]) and the bf16 token
+//              tile X [128 tokens][128 inputs], all by tiled TMA with 128-byte swizzling, X double-buffered;
+//   MMA warp   one thread issues 8 K-steps x 3 splits of tcgen05.mma (M = 128 tokens, N = 128 channels,
+//              K = 16) into an fp32 accumulator of 128 tensor-memory columns; NACC accumulators rotate;
+//   epilogue   NACC groups of four warps; group g takes every NACC-th unit: thread = token row of the
+//              accumulator (tcgen05.ld 32x32b), two passes over the channels (min/max, then codes), the same
+//              fp32 op sequence as every other quantiser of the library, record words assembled in shared
+//              memory, then copied out row by row.
+// bf16 inputs are exact in bf16, and the three-way split represents T to about 24 significant bits, so the
+// only difference from an fp32 CUDA-core rotation is the order of the fp32 accumulation.
+#pragma once
+#include <cudaTypedefs.h>
+
+#include "kvtc_tc.cuh"
+
+namespace kvtc {
+
+constexpr int TC_TILE = 128;           // tokens per unit
+constexpr int TC_NSPLIT = 3;           // bf16 terms of T
+constexpr int TC_NST = 2;              // X stages
+constexpr uint32_t TC_OP_BYTES = 128u * 128u * 2u;   // one 128 x 128 bf16 operand (two 64-column boxes)
+constexpr uint32_t TC_BOX_BYTES = 128u * 128u;       // one 128-row x 128-byte box
+
+struct EncTcArgs {
+  const int64_t* dst_pos;
+  uint32_t* dst[2];
+  int B, Hkv, per_seq, n_sets;
+  long long t_new, T_cap;
+  int units, tiles_per_head;
+  long long wait_ns;
+};
+
+struct EncTcSmem {  // byte offsets from the 1024-byte-aligned base of the dynamic shared memory
+  uint32_t x, epi, epi_group, par, bits, stage, total;
+};
+
+__host__ __device__ inline EncTcSmem enc_tc_smem(int RK, int RV, int nacc) {
+  EncTcSmem s;
+  s.x = TC_NSPLIT * TC_OP_BYTES;
+  s.epi = s.x + TC_NST * TC_OP_BYTES;
+  const uint32_t kw = (uint32_t)TC_TILE * (uint32_t)(RK | 1);
+  const uint32_t vw = (uint32_t)(TC_TILE / 2 + 1) * (uint32_t)(2 * RV + 1);
+  const uint32_t stage_words = kw > vw ? kw : vw;
+  s.par = 0;                                   // float4 [128]: mu, 1/sigma (NaN if zero width), 2^b, 2^b - 1
+  s.bits = D * 16;                             // uint32 [128]: record word | bit << 8
+  s.stage = s.bits + D * 4;                    // record staging
+  s.epi_group = (s.stage + stage_words * 4 + 127) & ~127u;
+  s.total = 1024 + s.epi + (uint32_t)nacc * s.epi_group;  // 1024: alignment slack of the base
+  return s;
+}
+
+// Same verdict for the 128 threads of an epilogue group (named barrier 1 + group).
+__device__ __forceinline__ bool group_all(int group, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(1 + group)
+      : "memory");
+  return r != 0;
+}
+
+template <int NACC>
+__global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
+    encode_tc_kernel(ParamsDev P, EncTcArgs a, const __grid_constant__ CUtensorMap mx_k,
+                     const __grid_constant__ CUtensorMap mx_v, const __grid_constant__ CUtensorMap mt_k,
+                     const __grid_constant__ CUtensorMap mt_v) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t x_full[TC_NST], x_empty[TC_NST], acc_full[NACC], acc_empty[NACC];
+  __shared__ __align__(8) uint64_t t_full, t_free, mma_fin;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - smem_u32(smem_raw));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int RK = P.t[0].r_words, RV = P.t[1].r_words;
+  const EncTcSmem L = enc_tc_smem(RK, RV, NACC);
+  const int tma_warp = 4 * NACC, mma_warp = 4 * NACC + 1;
+
+  // contiguous run of units of this CTA
+  const long long U = a.units;
+  const int u0 = (int)(U * blockIdx.x / gridDim.x), u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
+  const int per_tensor = a.B * a.Hkv * a.tiles_per_head;
+  // unit -> (tensor, bh, tile); the transform key (tensor, set) decides when T is restaged
+  auto unit_tensor = [&](int u) { return u / per_tensor; };
+  auto unit_bh = [&](int u) { return (u - unit_tensor(u) * per_tensor) / a.tiles_per_head; };
+  auto unit_tile = [&](int u) { return (u - unit_tensor(u) * per_tensor) % a.tiles_per_head; };
+  auto unit_set = [&](int u) { const int bh = unit_bh(u); return a.per_seq ? bh : bh % a.Hkv; };
+  auto unit_tkey = [&](int u) { return unit_tensor(u) * a.n_sets + unit_set(u); };
+
+  if (tid == 0) {
+    for (int s = 0; s < TC_NST; ++s) {
+      mbar_init(smem_u32(&x_full[s]), 1);
+      mbar_init(smem_u32(&x_empty[s]), 1);
+    }
+    for (int g = 0; g < NACC; ++g) {
+      mbar_init(smem_u32(&acc_full[g]), 1);
+      mbar_init(smem_u32(&acc_empty[g]), 4);  // lane 0 of each warp of the group
+    }
+    mbar_init(smem_u32(&t_full), 1);
+    mbar_init(smem_u32(&t_free), 1);
+    mbar_init(smem_u32(&mma_fin), 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == mma_warp) {
+    tmem_alloc(smem_u32(&s_tmem), 128u * NACC);
+    tmem_relinquish();
+  }
+  // record staging starts zeroed; the epilogue re-zeroes it after every copy-out
+  for (uint32_t g = 0; g < NACC; ++g) {
+    uint32_t* st = reinterpret_cast<uint32_t*>(gbase + L.epi + g * L.epi_group + L.stage);
+    for (uint32_t i = tid; i < (L.epi_group - L.stage) / 4; i += blockDim.x) st[i] = 0u;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == tma_warp) {
+    // ================= TMA producer (one thread) =================
+    if (lane == 0 && u0 < u1) {
+      tma_prefetch_map(&mx_k);
+      tma_prefetch_map(&mx_v);
+      tma_prefetch_map(&mt_k);
+      tma_prefetch_map(&mt_v);
+      int tloads = 0, issued = 0;
+      for (int u = u0; u < u1 && !s_abort; ++u) {
+        const int li = u - u0, s = li % TC_NST;
+        const int tensor = unit_tensor(u);
+        if (u == u0 || unit_tkey(u) != unit_tkey(u - 1)) {
+          if (tloads > 0 && !mbar_wait_bounded(smem_u32(&t_free), (uint32_t)((tloads - 1) & 1), a.wait_ns)) {
+            s_abort = 1;
+            break;
+          }
+          const CUtensorMap* mt = tensor == 0 ? &mt_k : &mt_v;
+          const uint32_t tb = smem_u32(&t_full);
+          mbar_expect_tx(tb, TC_NSPLIT * TC_OP_BYTES);
+          for (int p = 0; p < TC_NSPLIT; ++p)
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_2d(base + p * TC_OP_BYTES + hf * TC_BOX_BYTES, mt, 64 * hf, (unit_set(u) * TC_NSPLIT + p) * D,
+                          tb);
+          ++tloads;
+        }
+        if (li >= TC_NST &&
+            !mbar_wait_bounded(smem_u32(&x_empty[s]), (uint32_t)((li / TC_NST - 1) & 1), a.wait_ns)) {
+          s_abort = 1;
+          break;
+        }
+        const CUtensorMap* mx = tensor == 0 ? &mx_k : &mx_v;
+        const int row0 = (int)((long long)unit_bh(u) * a.t_new + (long long)unit_tile(u) * TC_TILE);
+        const uint32_t xb = smem_u32(&x_full[s]);
+        mbar_expect_tx(xb, TC_OP_BYTES);
+        tma_load_2d(base + L.x + s * TC_OP_BYTES, mx, 0, row0, xb);
+        tma_load_2d(base + L.x + s * TC_OP_BYTES + TC_BOX_BYTES, mx, 64, row0, xb);
+        ++issued;
+      }
+      // leave no copy in flight: the last loads of every stage and of T complete before the CTA can exit
+      for (int i = (issued > TC_NST ? issued - TC_NST : 0); i < issued; ++i)
+        mbar_wait_bounded(smem_u32(&x_full[i % TC_NST]), (uint32_t)((i / TC_NST) & 1), a.wait_ns);
+      if (tloads > 0) mbar_wait_bounded(smem_u32(&t_full), (uint32_t)((tloads - 1) & 1), a.wait_ns);
+    }
+  } else if (warp == mma_warp) {
+    // ================= MMA issuer (one thread) =================
+    if (lane == 0 && u0 < u1) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+      int tloads = 0;
+      for (int u = u0; u < u1 && !s_abort; ++u) {
+        const int li = u - u0, s = li % TC_NST, g = li % NACC;
+        if (u == u0 || unit_tkey(u) != unit_tkey(u - 1)) {
+          if (!mbar_wait_bounded(smem_u32(&t_full), (uint32_t)(tloads & 1), a.wait_ns)) {
+            s_abort = 1;
+            break;
+          }
+          ++tloads;
+        }
+        if (!mbar_wait_bounded(smem_u32(&x_full[s]), (uint32_t)((li / TC_NST) & 1), a.wait_ns)) {
+          s_abort = 1;
+          break;
+        }
+        if (li >= NACC &&
+            !mbar_wait_bounded(smem_u32(&acc_empty[g]), (uint32_t)((li / NACC - 1) & 1), a.wait_ns)) {
+          s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(g * 128);
+        const uint32_t xs = base + L.x + s * TC_OP_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t koff = (uint32_t)(kk >> 2) * TC_BOX_BYTES + (uint32_t)(kk & 3) * 32u;
+          const uint64_t adesc = smem_desc_k128(xs + koff);
+#pragma unroll
+          for (int p = 0; p < TC_NSPLIT; ++p)
+            tc_mma_bf16(d, adesc, smem_desc_k128(base + p * TC_OP_BYTES + koff), IDESC, (kk | p) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&x_empty[s]));
+        tc_commit(smem_u32(&acc_full[g]));
+        if (u + 1 < u1 && unit_tkey(u + 1) != unit_tkey(u)) tc_commit(smem_u32(&t_free));
+      }
+      // every MMA issued has completed before tensor memory is released
+      tc_commit(smem_u32(&mma_fin));
+      mbar_wait_bounded(smem_u32(&mma_fin), 0u, a.wait_ns);
+    }
+  } else {
+    // ================= epilogue groups =================
+    const int g = warp >> 2, q = warp & 3;
+    const int row = 32 * q + lane;  // accumulator lane = token row of the tile
+    uint8_t* eg = gbase + L.epi + g * L.epi_group;
+    float4* par = reinterpret_cast<float4*>(eg + L.par);
+    uint32_t* pbits = reinterpret_cast<uint32_t*>(eg + L.bits);
+    uint32_t* stage = reinterpret_cast<uint32_t*>(eg + L.stage);
+    int cached_key = -1, k = 0;
+    for (int u = u0 + g; u < u1; u += NACC, ++k) {
+      const int tensor = unit_tensor(u), bh = unit_bh(u), tile = unit_tile(u), set = unit_set(u);
+      const TensorDev& td = P.t[tensor];
+      const int R = td.r_words;
+      const int b = bh / a.Hkv;
+      if (unit_tkey(u) != cached_key) {  // this group's channel parameters (the group is idle here)
+        const int j = row;
+        const size_t so = (size_t)set * D;
+        const int w = td.widths[so + j];
+        float4 pv;
+        pv.x = td.mu[so + j];
+        pv.y = w > 0 ? td.inv_sigma[so + j] : __int_as_float(0x7fc00000);  // NaN: left out of min/max, code 0
+        pv.z = exp2i(w);
+        pv.w = (float)((1 << w) - 1);
+        uint32_t word, bit;
+        if (tensor == 0) {
+          const uint32_t dsc = td.slots[so + (j >> 1)];
+          word = 1u + (dsc & 255u);
+          bit = ((dsc >> 8) & 255u) + 16u * (uint32_t)(j & 1);
+        } else {
+          const uint32_t dsc = td.slots[so + j];
+          word = 2u + (dsc & 255u);
+          bit = (dsc >> 8) & 255u;
+        }
+        if (w == 0) bit = 0u;
+        par[j] = pv;
+        pbits[j] = word | (bit << 8);
+        cached_key = unit_tkey(u);
+        named_bar(1 + g, 128);
+      }
+      const int nz = td.nz[set];
+      const int nch = (nz + 31) >> 5;
+      const bool ok = group_all(g, mbar_wait_bounded(smem_u32(&acc_full[g]), (uint32_t)(k & 1), a.wait_ns));
+      if (!ok) {
+        s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
+      // ---- pass 1: min / max of y'_j over the channels with b_j > 0 ----
+      float m = INFINITY, M = -INFINITY;
+      for (int c = 0; c < nch; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tacc + 32u * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * c + jj;
+          if (j < nz) {
+            const float4 p = par[j];
+            const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
+            m = fminf(m, yp);
+            M = fmaxf(M, yp);
+          }
+        }
+      }
+      __half zh = __ushort_as_half(0), sh = __ushort_as_half(0);
+      if (nz > 0) {
+        zh = half_sat_rn(__fadd_rn(m, 0.f));
+        sh = half_sat_rn(__fsub_rn(M, __half2float(zh)));
+      }
+      const float zf = __half2float(zh), sf = __half2float(sh);
+      const bool coded = sf != 0.f;
+      const uint32_t zs = (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
+      // ---- pass 2: codes into this token's record words ----
+      const long long pos0 = a.dst_pos[b] + (long long)tile * TC_TILE;
+      const int half = (int)((pos0 + row) & 1);
+      const int lr = (row + (int)(pos0 & 1)) >> 1;  // local two-token record of a value token
+      const int PK = R | 1, PV = 2 * R + 1;
+      uint32_t* krow = stage + row * PK;
+      uint16_t* vrow16 = reinterpret_cast<uint16_t*>(stage + lr * PV) + half;
+      for (int c = 0; c < nch; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tacc + 32u * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * c + jj;
+          if (j < nz) {
+            const float4 p = par[j];
+            const uint32_t wb = pbits[j];
+            const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
+            const float t = __fdiv_rn(__fsub_rn(yp, zf), sf);
+            const float f = fminf(fmaxf(floorf(__fmul_rn(t, p.z)), 0.f), p.w);
+            const uint32_t code = coded ? (uint32_t)f : 0u;
+            if (tensor == 0)
+              krow[wb & 255u] |= code << (wb >> 8);
+            else
+              vrow16[2 * (wb & 255u)] |= (uint16_t)(code << (wb >> 8));
+          }
+        }
+      }
+      // the accumulator is free for the next unit of this group
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[g]));
+      if (tensor == 0)
+        krow[0] = zs;
+      else
+        stage[lr * PV + half] = zs;
+      named_bar(1 + g, 128);
+      // ---- copy-out: one warp per record, lanes over its words ----
+      const long long n_valid = min((long long)TC_TILE, a.t_new - (long long)tile * TC_TILE);
+      if (tensor == 0) {
+        uint32_t* dst = a.dst[0] + (size_t)bh * a.T_cap * R;
+        for (int r = q; r < n_valid; r += 4) {
+          const long long pos = pos0 + r;
+          if (pos < 0 || pos >= a.T_cap) {
+            if (lane == 0) atomicOr(&g_status, ST_BAD_INDEX);
+            continue;
+          }
+          for (int w = lane; w < R; w += 32) dst[pos * R + w] = stage[r * PK + w];
+        }
+      } else {
+        uint32_t* dst = a.dst[1] + (size_t)bh * (a.T_cap / 2) * 2 * R;
+        const int odd = (int)(pos0 & 1);
+        const int nrec = (int)((n_valid - 1 + odd) >> 1) + 1;
+        for (int r = q; r < nrec; r += 4) {
+          const long long gr = (pos0 >> 1) + r;  // global record (pos0 >> 1 rounds toward minus infinity)
+          const int t_lo = 2 * r - odd;            // tile row of the record's first token
+          bool has[2];
+          for (int hh = 0; hh < 2; ++hh) {
+            const int tr = t_lo + hh;
+            const long long pos = 2 * gr + hh;
+            has[hh] = tr >= 0 && tr < n_valid;
+            if (has[hh] && (pos < 0 || pos >= a.T_cap)) {
+              if (lane == 0) atomicOr(&g_status, ST_BAD_INDEX);
+              has[hh] = false;
+            }
+          }
+          const uint32_t* src = stage + r * PV;
+          uint32_t* drec = dst + gr * 2 * R;
+          if (has[0] && has[1]) {
+            for (int w = lane; w < 2 * R; w += 32) drec[w] = src[w];
+          } else {
+            for (int hh = 0; hh < 2; ++hh) {
+              if (!has[hh]) continue;
+              if (lane == 0) drec[hh] = src[hh];
+              const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+              uint16_t* d16 = reinterpret_cast<uint16_t*>(drec);
+              for (int w = 2 + lane; w < 2 * R; w += 32) d16[2 * w + hh] = s16[2 * w + hh];
+            }
+          }
+        }
+      }
+      named_bar(1 + g, 128);
+      // zero the staging words this unit used, for the next one
+      {
+        const int words = tensor == 0 ? TC_TILE * PK : (TC_TILE / 2 + 1) * PV;
+        for (int i = row; i < words; i += 128) stage[i] = 0u;
+      }
+      named_bar(1 + g, 128);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == mma_warp) tmem_dealloc(tmem, 128u * NACC);
+}
+
+// ---- host side: tensor maps and launch ---------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 matrix [rows][128] (256-byte rows), boxes of 128 rows x 64 columns, 128-byte swizzle, zero fill
+static bool make_bf16_map(CUtensorMap* m, const void* ptr, unsigned long long rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NACC>
+static cudaError_t launch_encode_tc_n(const ParamsDev& P, const EncTcArgs& a, const CUtensorMap* maps,
+                                      uint32_t smem, cudaStream_t s, int grid) {
+  cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel<NACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  encode_tc_kernel<NACC><<<grid, (4 * NACC + 2) * 32, smem, s>>>(P, a, maps[0], maps[1], maps[2], maps[3]);
+  return cudaGetLastError();
+}
+
+// Tensor-core encode of bf16 tokens. Returns KV_ERR_UNSUPPORTED (nothing launched) when the shapes fall outside
+// what the kernel handles, so the caller can take the CUDA-core path.
+static kv_status launch_encode_tc(const ParamsDev& P, const kv_cache& c, const void* k, const void* v, int B,
+                                  int64_t t_new, const int64_t* dst_pos, cudaStream_t s) {
+  const long long rows = (long long)B * c.Hkv * t_new;
+  if (rows + TC_TILE >= (1LL << 31) || P.n_sets * TC_NSPLIT * D >= (1 << 30)) {
+    set_error("tensor-core encode: %lld token rows exceed the kernel's 32-bit tile coordinates", rows);
+    return KV_ERR_UNSUPPORTED;
+  }
+  const int RK = P.t[0].r_words, RV = P.t[1].r_words;
+  int nacc = 4;
+  if (enc_tc_smem(RK, RV, 4).total > 227u * 1024u) nacc = 2;
+  const uint32_t smem = enc_tc_smem(RK, RV, nacc).total;
+  if (smem > 227u * 1024u) {
+    set_error("tensor-core encode: %u bytes of shared memory needed", smem);
+    return KV_ERR_UNSUPPORTED;
+  }
+  CUtensorMap maps[4];
+  if (!make_bf16_map(&maps[0], k, (unsigned long long)rows) || !make_bf16_map(&maps[1], v, (unsigned long long)rows) ||
+      !make_bf16_map(&maps[2], P.t[0].Tsplit, (unsigned long long)P.n_sets * TC_NSPLIT * D) ||
+      !make_bf16_map(&maps[3], P.t[1].Tsplit, (unsigned long long)P.n_sets * TC_NSPLIT * D)) {
+    set_error("tensor-core encode: tensor map encoding failed");
+    return KV_ERR_UNSUPPORTED;
+  }
+  EncTcArgs a;
+  a.dst_pos = dst_pos;
+  a.dst[0] = c.k_rec;
+  a.dst[1] = c.v_rec;
+  a.B = B;
+  a.Hkv = c.Hkv;
+  a.per_seq = c.per_seq_params;
+  a.n_sets = P.n_sets;
+  a.t_new = t_new;
+  a.T_cap = c.T_cap;
+  a.tiles_per_head = (int)((t_new + TC_TILE - 1) / TC_TILE);
+  const long long units = 2LL * B * c.Hkv * a.tiles_per_head;
+  if (units >= (1LL << 31)) {
+    set_error("tensor-core encode: too many tiles");
+    return KV_ERR_UNSUPPORTED;
+  }
+  a.units = (int)units;
+  a.wait_ns = g_wait_limit_ns;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int grid = (int)std::min<long long>(units, sm_count(dev));
+  const cudaError_t e = nacc == 4 ? launch_encode_tc_n<4>(P, a, maps, smem, s, grid)
+                                  : launch_encode_tc_n<2>(P, a, maps, smem, s, grid);
+  if (e != cudaSuccess) {
+    set_error("encode_tc_kernel launch: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
+  return KV_OK;
+}
+
+}  // namespace kvtc
