@@ -147,9 +147,9 @@ def llama_300():
     return w, L, sets, G.lib_params(sets)
 
 
-def _check_tokens(rk, rv, k, v, sets, per_seq, dst0, T):
+def _check_tokens(rk, rv, k, v, sets, per_seq, dst0, T, frac_bar=1e-4):
     """Every token's record entries at cache positions dst0 .. dst0 + T - 1 against the oracle encode of the
-    same vectors: each entry within 1 LSB, at most 1e-4 of all the entries checked different, and nothing
+    same vectors: each entry within 1 LSB, at most frac_bar of all the entries checked different, and nothing
     written outside those positions."""
     B, Hkv = k.shape[:2]
     n_diff, n_all = 0.0, 0
@@ -169,7 +169,7 @@ def _check_tokens(rk, rv, k, v, sets, per_seq, dst0, T):
                 assert not np.any(z.view(np.uint16)[outside]) and not np.any(s.view(np.uint16)[outside])
                 assert not np.any(c[outside])
     frac = n_diff / n_all
-    assert frac <= 1e-4, (frac, round(n_diff), n_all)
+    assert frac <= frac_bar, (frac, round(n_diff), n_all)
     return frac
 
 
@@ -189,8 +189,13 @@ def test_encode_paths_bf16_llama_shape(llama_300, path, dst0):
 
 @pytest.mark.parametrize("bits", [1.33, 4.0, 8.0])
 def test_encode_tensor_core_budgets_per_sequence(bits):
-    """Tensor-core encode at 5, 16 and 33 record words (the last with two accumulator groups, for shared
-    memory), one parameter set per (sequence, head)."""
+    """Tensor-core encode at 5, 16 and 32 record words (the last one's record staging is the largest in
+    shared memory), one parameter set per (sequence, head).
+
+    The 1e-4 mismatch bar belongs to the workloads' budgets (at most 4 bits per element). A code flips when the
+    fp32 rotation's rounding error carries a value across a bin edge, so the flip rate scales with 1 / bin
+    width: at 8 bits per element the channels get 7-8 bits instead of 3-4, bins 16 times narrower than at
+    4 bits, and the bar scales to 16e-4. Every entry must still be within 1 LSB."""
     w = synth.WORKLOADS["qwen_batched_8k"]
     L = synth.make_layer(w, T=200, B=2, steps=1)
     sets = G.calibrate_oracle(L, bits, bits)
@@ -200,7 +205,8 @@ def test_encode_tensor_core_budgets_per_sequence(bits):
         rk, rv = _encode_gpu(P, L.k, L.v, True, T_cap=208, dst0=3)
     finally:
         kvtc.kv_debug_set_encode_path(0)
-    _check_tokens(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, True, 3, 200)
+    _check_tokens(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, True, 3, 200,
+                  frac_bar=1.6e-3 if bits > 4 else 1e-4)
 
 
 def test_encode_tensor_core_rejects_fp32(tiny):

@@ -582,21 +582,30 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   if (!okw && tid == 0) mbar_wait_bounded(smem_u32(tbar), 0u, a.wait_ns);  // drain before leaving
   if (__syncthreads_or(!okw)) return;
   float* part = a.part + ((size_t)bh * a.splits + split) * g * PSTR;
-  if (tid < D) {
-    const int k = tid;
+  static_assert(DTHREADS == 2 * D, "two threads per channel of the original basis");
+  {  // thread: channel k of the original basis for the heads of one parity
+    const int k = tid & (D - 1), hp = tid >> 7;
     const float wk = TV.wsum[(size_t)set * D + k];
-    float n[MAX_G];
+    float n[MAX_G / 2];
 #pragma unroll
-    for (int h = 0; h < MAX_G; ++h) n[h] = h < g ? mS[2 * MAX_G + h] * wk : 0.f;
+    for (int i = 0; i < MAX_G / 2; ++i) {
+      const int h = hp + 2 * i;
+      n[i] = h < g ? mS[2 * MAX_G + h] * wk : 0.f;
+    }
+#pragma unroll 4
     for (int jj = 0; jj < nzV; ++jj) {
       const float t = Tsc[jj * D + k];
 #pragma unroll
-      for (int h = 0; h < MAX_G; ++h)
-        if (h < g) n[h] = fmaf(t, mA[h * D + jj], n[h]);
+      for (int i = 0; i < MAX_G / 2; ++i) {
+        const int h = hp + 2 * i;
+        if (h < g) n[i] = fmaf(t, mA[h * D + jj], n[i]);
+      }
     }
 #pragma unroll
-    for (int h = 0; h < MAX_G; ++h)
-      if (h < g) part[h * PSTR + 4 + k] = n[h];
+    for (int i = 0; i < MAX_G / 2; ++i) {
+      const int h = hp + 2 * i;
+      if (h < g) part[h * PSTR + 4 + k] = n[i];
+    }
   }
   if (tid < g) {
     part[tid * PSTR + 0] = mS[tid];

@@ -12,9 +12,9 @@
 //   MMA warp   one thread issues 8 K-steps x 3 splits of tcgen05.mma (M = 128 tokens, N = 128 channels,
 //              K = 16) into an fp32 accumulator of 128 tensor-memory columns; NACC accumulators rotate;
 //   epilogue   NACC groups of four warps; group g takes every NACC-th unit: thread = token row of the
-//              accumulator (tcgen05.ld 32x32b), two passes over the channels (min/max, then codes), the same
-//              fp32 op sequence as every other quantiser of the library, record words assembled in shared
-//              memory, then copied out row by row.
+//              accumulator (tcgen05.ld 32x32b), two passes over the channels (min/max, then codes), codes equal
+//              to those of every other quantiser of the library, record words assembled in shared memory by
+//              atomic ORs, then copied out row by row.
 // bf16 inputs are exact in bf16, and the three-way split represents T to about 24 significant bits, so the
 // only difference from an fp32 CUDA-core rotation is the order of the fp32 accumulation.
 #pragma once
@@ -27,6 +27,7 @@ namespace kvtc {
 constexpr int TC_TILE = 128;           // tokens per unit
 constexpr int TC_NSPLIT = 3;           // bf16 terms of T
 constexpr int TC_NST = 2;              // X stages
+constexpr int TC_NACC = 3;             // tensor-memory accumulators = epilogue groups
 constexpr uint32_t TC_OP_BYTES = 128u * 128u * 2u;   // one 128 x 128 bf16 operand (two 64-column boxes)
 constexpr uint32_t TC_BOX_BYTES = 128u * 128u;       // one 128-row x 128-byte box
 
@@ -50,8 +51,8 @@ __host__ __device__ inline EncTcSmem enc_tc_smem(int RK, int RV, int nacc) {
   const uint32_t kw = (uint32_t)TC_TILE * (uint32_t)(RK | 1);
   const uint32_t vw = (uint32_t)(TC_TILE / 2 + 1) * (uint32_t)(2 * RV + 1);
   const uint32_t stage_words = kw > vw ? kw : vw;
-  s.par = 0;                                   // float4 [128]: mu, 1/sigma (NaN if zero width), 2^b, 2^b - 1
-  s.bits = D * 16;                             // uint32 [128]: record word | bit << 8
+  s.par = 0;      // float4 [128]: mu, 1/sigma (NaN if zero width), 2^b, 2^b - 1/2
+  s.bits = D * 16;  // uint32 [128]: byte offset of the code word in the record | bit << 16
   s.stage = s.bits + D * 4;                    // record staging
   s.epi_group = (s.stage + stage_words * 4 + 127) & ~127u;
   s.total = 1024 + s.epi + (uint32_t)nacc * s.epi_group;  // 1024: alignment slack of the base
@@ -113,8 +114,9 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
     fence_mbar_init();
     s_abort = 0;
   }
+  constexpr uint32_t TMEM_COLS = NACC <= 2 ? 256u : 512u;  // 128 columns per accumulator, a power of two
   if (warp == mma_warp) {
-    tmem_alloc(smem_u32(&s_tmem), 128u * NACC);
+    tmem_alloc(smem_u32(&s_tmem), TMEM_COLS);
     tmem_relinquish();
   }
   // record staging starts zeroed; the epilogue re-zeroes it after every copy-out
@@ -232,9 +234,9 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
         const int w = td.widths[so + j];
         float4 pv;
         pv.x = td.mu[so + j];
-        pv.y = w > 0 ? td.inv_sigma[so + j] : __int_as_float(0x7fc00000);  // NaN: left out of min/max, code 0
+        pv.y = w > 0 ? td.inv_sigma[so + j] : __int_as_float(0x7fc00000);  // NaN: out of min/max, code 0
         pv.z = exp2i(w);
-        pv.w = (float)((1 << w) - 1);
+        pv.w = (float)((1 << w) - 1) + 0.5f;
         uint32_t word, bit;
         if (tensor == 0) {
           const uint32_t dsc = td.slots[so + (j >> 1)];
@@ -247,12 +249,12 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
         }
         if (w == 0) bit = 0u;
         par[j] = pv;
-        pbits[j] = word | (bit << 8);
+        pbits[j] = (4u * word) | (bit << 16);
         cached_key = unit_tkey(u);
         named_bar(1 + g, 128);
       }
       const int nz = td.nz[set];
-      const int nch = (nz + 31) >> 5;
+      const int nblk = (nz + 15) >> 4;  // 16-column blocks; channels past nz have width 0
       const bool ok = group_all(g, mbar_wait_bounded(smem_u32(&acc_full[g]), (uint32_t)(k & 1), a.wait_ns));
       if (!ok) {
         s_abort = 1;
@@ -260,21 +262,18 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       }
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
-      // ---- pass 1: min / max of y'_j over the channels with b_j > 0 ----
+      // ---- pass 1: min / max of y'_j over the channels with b_j > 0 (the others give NaN, which min/max skip) ----
       float m = INFINITY, M = -INFINITY;
-      for (int c = 0; c < nch; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tacc + 32u * c, v);
+      for (int cb = 0; cb < nblk; ++cb) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tacc + 16u * cb, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * c + jj;
-          if (j < nz) {
-            const float4 p = par[j];
-            const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
-            m = fminf(m, yp);
-            M = fmaxf(M, yp);
-          }
+        for (int jj = 0; jj < 16; ++jj) {
+          const float2 p = *reinterpret_cast<const float2*>(&par[16 * cb + jj]);
+          const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
+          m = fminf(m, yp);
+          M = fmaxf(M, yp);
         }
       }
       __half zh = __ushort_as_half(0), sh = __ushort_as_half(0);
@@ -286,30 +285,55 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       const bool coded = sf != 0.f;
       const uint32_t zs = (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
       // ---- pass 2: codes into this token's record words ----
+      // The quantiser's code clamp(floor(RN((y' - z) / s) 2^b), 0, 2^b - 1) is formed from
+      // u = RN((y' - z) * (RN(1/s) 2^b)), which differs from RN((y' - z) / s) 2^b by at most 3 units of 2^-24
+      // relative, i.e. by less than 2^(b-21) where it matters (|u| <= 2^b). u is clamped to [1/2, 2^b - 1/2]
+      // first, so floor() yields the clamped code and the clamp ends, being half-integers, are never ties. Only
+      // a clamped u within 2^(b-21) of an integer can give a different floor: such tokens are redone below with
+      // the IEEE division.
       const long long pos0 = a.dst_pos[b] + (long long)tile * TC_TILE;
       const int half = (int)((pos0 + row) & 1);
       const int lr = (row + (int)(pos0 & 1)) >> 1;  // local two-token record of a value token
       const int PK = R | 1, PV = 2 * R + 1;
-      uint32_t* krow = stage + row * PK;
-      uint16_t* vrow16 = reinterpret_cast<uint16_t*>(stage + lr * PV) + half;
-      for (int c = 0; c < nch; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tacc + 32u * c, v);
+      uint32_t* const rec = tensor == 0 ? stage + row * PK : stage + lr * PV;
+      const uint32_t rec_s = smem_u32(rec);
+      const uint32_t hsh = tensor == 0 ? 0u : 16u * (uint32_t)half;  // value token: its half of each code word
+      const float rs = coded ? __frcp_rn(sf) : 0.f;
+      bool near = false;
+      for (int cb = 0; cb < nblk; ++cb) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tacc + 16u * cb, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * c + jj;
-          if (j < nz) {
-            const float4 p = par[j];
-            const uint32_t wb = pbits[j];
-            const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
-            const float t = __fdiv_rn(__fsub_rn(yp, zf), sf);
-            const float f = fminf(fmaxf(floorf(__fmul_rn(t, p.z)), 0.f), p.w);
-            const uint32_t code = coded ? (uint32_t)f : 0u;
-            if (tensor == 0)
-              krow[wb & 255u] |= code << (wb >> 8);
-            else
-              vrow16[2 * (wb & 255u)] |= (uint16_t)(code << (wb >> 8));
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j = 16 * cb + jj;
+          const float4 p = par[j];
+          const uint32_t pb = pbits[j];
+          const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
+          const float uq = fminf(fmaxf(__fmul_rn(__fsub_rn(yp, zf), __fmul_rn(rs, p.z)), 0.5f), p.w);
+          const float fl = floorf(uq);
+          near |= fabsf(__fsub_rn(__fsub_rn(uq, fl), 0.5f)) > fmaf(p.z, -0x1p-21f, 0.5f);
+          red_or_shared(rec_s + (pb & 0xFFFFu), (uint32_t)fl << ((pb >> 16) + hsh));
+        }
+      }
+      near = near && coded;
+      if (__any_sync(0xffffffffu, near)) {  // rare: exact quotients for the near-tie tokens of this warp
+        for (int cb = 0; cb < nblk; ++cb) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tacc + 16u * cb, v);
+          tmem_ld_wait();
+          if (near) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = 16 * cb + jj;
+              const float4 p = par[j];
+              const uint32_t pb = pbits[j];
+              const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
+              const float dq = __fsub_rn(yp, zf);
+              const uint32_t fast = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(dq, __fmul_rn(rs, p.z)), 0.5f), p.w));
+              const uint32_t exact = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(__fdiv_rn(dq, sf), p.z), 0.5f), p.w));
+              if (fast != exact) red_xor_shared(rec_s + (pb & 0xFFFFu), (fast ^ exact) << ((pb >> 16) + hsh));
+            }
           }
         }
       }
@@ -317,51 +341,77 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[g]));
-      if (tensor == 0)
-        krow[0] = zs;
-      else
-        stage[lr * PV + half] = zs;
+      rec[tensor == 0 ? 0 : half] = zs;
       named_bar(1 + g, 128);
-      // ---- copy-out: one warp per record, lanes over its words ----
-      const long long n_valid = min((long long)TC_TILE, a.t_new - (long long)tile * TC_TILE);
+      // ---- copy-out: the tile's records are contiguous in the cache; the group copies them word by word ----
+      const int n_valid = (int)min((long long)TC_TILE, a.t_new - (long long)tile * TC_TILE);
+      const int gt = tid & 127;  // thread index within the group
       if (tensor == 0) {
         uint32_t* dst = a.dst[0] + (size_t)bh * a.T_cap * R;
-        for (int r = q; r < n_valid; r += 4) {
-          const long long pos = pos0 + r;
-          if (pos < 0 || pos >= a.T_cap) {
-            if (lane == 0) atomicOr(&g_status, ST_BAD_INDEX);
-            continue;
+        if (pos0 >= 0 && pos0 + n_valid <= a.T_cap) {
+          const uint32_t mR = 0xFFFFFFFFu / (uint32_t)R + 1u;  // i / R = umulhi(i, mR) for i < 2^16
+          uint32_t* d0 = dst + pos0 * R;
+          for (int i = gt; i < n_valid * R; i += 128) {
+            const int r = (int)__umulhi((uint32_t)i, mR);
+            d0[i] = stage[r * PK + (i - r * R)];
           }
-          for (int w = lane; w < R; w += 32) dst[pos * R + w] = stage[r * PK + w];
+        } else {
+          for (int r = gt; r < n_valid; r += 128) {
+            const long long pos = pos0 + r;
+            if (pos < 0 || pos >= a.T_cap) {
+              atomicOr(&g_status, ST_BAD_INDEX);
+              continue;
+            }
+            for (int w = 0; w < R; ++w) dst[pos * R + w] = stage[r * PK + w];
+          }
         }
       } else {
+        // local record r holds tokens 2r - odd and 2r - odd + 1 of the tile; the first and the last record may
+        // hold only one of this tile's tokens (their other halves belong to neighbouring writes)
         uint32_t* dst = a.dst[1] + (size_t)bh * (a.T_cap / 2) * 2 * R;
         const int odd = (int)(pos0 & 1);
-        const int nrec = (int)((n_valid - 1 + odd) >> 1) + 1;
-        for (int r = q; r < nrec; r += 4) {
-          const long long gr = (pos0 >> 1) + r;  // global record (pos0 >> 1 rounds toward minus infinity)
-          const int t_lo = 2 * r - odd;            // tile row of the record's first token
-          bool has[2];
-          for (int hh = 0; hh < 2; ++hh) {
-            const int tr = t_lo + hh;
-            const long long pos = 2 * gr + hh;
-            has[hh] = tr >= 0 && tr < n_valid;
-            if (has[hh] && (pos < 0 || pos >= a.T_cap)) {
-              if (lane == 0) atomicOr(&g_status, ST_BAD_INDEX);
-              has[hh] = false;
+        const int nrec = ((n_valid - 1 + odd) >> 1) + 1;
+        const int f0 = odd, f1 = ((n_valid + odd) & 1) ? nrec - 1 : nrec;  // full records [f0, f1)
+        const long long gr0 = pos0 >> 1;  // global record of local record 0 (rounds toward minus infinity)
+        if (pos0 >= 0 && pos0 + n_valid <= a.T_cap) {
+          const int W2 = 2 * R;
+          const uint32_t mW = 0xFFFFFFFFu / (uint32_t)W2 + 1u;
+          uint32_t* d0 = dst + (gr0 + f0) * W2;
+          for (int i = gt; i < (f1 - f0) * W2; i += 128) {
+            const int r = (int)__umulhi((uint32_t)i, mW);
+            d0[i] = stage[(f0 + r) * PV + (i - r * W2)];
+          }
+          // partial records (never the same one): the first holds only its later token when pos0 is odd, the
+          // last only its earlier token when the tile ends on an even position; copy this tile's half of each
+          // code word and its z/s word
+          for (int e = 0; e < 2; ++e) {
+            if (e == 0 ? odd == 0 : f1 != nrec - 1) continue;
+            const int r = e == 0 ? 0 : nrec - 1, hh = e == 0 ? 1 : 0;
+            const uint32_t* src = stage + r * PV;
+            uint32_t* drec = dst + (gr0 + r) * W2;
+            for (int w = gt; w < W2; w += 128) {
+              if (w < 2) {
+                if (w == hh) drec[w] = src[w];
+              } else {
+                reinterpret_cast<uint16_t*>(drec)[2 * w + hh] = reinterpret_cast<const uint16_t*>(src)[2 * w + hh];
+              }
             }
           }
-          const uint32_t* src = stage + r * PV;
-          uint32_t* drec = dst + gr * 2 * R;
-          if (has[0] && has[1]) {
-            for (int w = lane; w < 2 * R; w += 32) drec[w] = src[w];
-          } else {
+        } else {
+          for (int r = gt; r < nrec; r += 128) {
             for (int hh = 0; hh < 2; ++hh) {
-              if (!has[hh]) continue;
-              if (lane == 0) drec[hh] = src[hh];
-              const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
-              uint16_t* d16 = reinterpret_cast<uint16_t*>(drec);
-              for (int w = 2 + lane; w < 2 * R; w += 32) d16[2 * w + hh] = s16[2 * w + hh];
+              const int tr = 2 * r - odd + hh;
+              if (tr < 0 || tr >= n_valid) continue;
+              const long long pos = pos0 + tr;
+              if (pos < 0 || pos >= a.T_cap) {
+                atomicOr(&g_status, ST_BAD_INDEX);
+                continue;
+              }
+              const uint32_t* src = stage + r * PV;
+              uint32_t* drec = dst + (pos >> 1) * 2 * R;
+              drec[hh] = src[hh];
+              for (int w = 2; w < 2 * R; ++w)
+                reinterpret_cast<uint16_t*>(drec)[2 * w + hh] = reinterpret_cast<const uint16_t*>(src)[2 * w + hh];
             }
           }
         }
@@ -379,7 +429,10 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == mma_warp) tmem_dealloc(tmem, 128u * NACC);
+  if (warp == mma_warp) {
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
 }
 
 // ---- host side: tensor maps and launch ---------------------------------------------------------------
@@ -429,9 +482,9 @@ static kv_status launch_encode_tc(const ParamsDev& P, const kv_cache& c, const v
     return KV_ERR_UNSUPPORTED;
   }
   const int RK = P.t[0].r_words, RV = P.t[1].r_words;
-  int nacc = 4;
-  if (enc_tc_smem(RK, RV, 4).total > 227u * 1024u) nacc = 2;
-  const uint32_t smem = enc_tc_smem(RK, RV, nacc).total;
+  // three epilogue groups: 14 warps, i.e. at most four per SM sub-partition, leave 128 registers a thread;
+  // their shared memory fits for every record length up to 33 words
+  const uint32_t smem = enc_tc_smem(RK, RV, TC_NACC).total;
   if (smem > 227u * 1024u) {
     set_error("tensor-core encode: %u bytes of shared memory needed", smem);
     return KV_ERR_UNSUPPORTED;
@@ -464,8 +517,7 @@ static kv_status launch_encode_tc(const ParamsDev& P, const kv_cache& c, const v
   int dev = 0;
   cudaGetDevice(&dev);
   const int grid = (int)std::min<long long>(units, sm_count(dev));
-  const cudaError_t e = nacc == 4 ? launch_encode_tc_n<4>(P, a, maps, smem, s, grid)
-                                  : launch_encode_tc_n<2>(P, a, maps, smem, s, grid);
+  const cudaError_t e = launch_encode_tc_n<TC_NACC>(P, a, maps, smem, s, grid);
   if (e != cudaSuccess) {
     set_error("encode_tc_kernel launch: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;
