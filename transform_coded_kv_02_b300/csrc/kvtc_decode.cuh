@@ -15,6 +15,7 @@ constexpr int RING_BUDGET = 48 * 1024;
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_SPLITS = 256;
 constexpr int TAIL_RESERVE = MAX_SPLITS * MAX_G * 4 + 4 * MAX_G * 4;  // split weights, head state
+static_assert(DTHREADS / 32 >= MAX_G, "one warp per query head of a group in the split merge");
 
 struct DecArgs {
   const uint32_t* rec[2];
@@ -45,7 +46,6 @@ constexpr int QP_THREADS = 256;
 static size_t qprep_smem_bytes() { return (size_t)D * D * 4 + 2 * (size_t)MAX_G * D * 4; }
 
 __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs a) {
-  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   float* Ts = reinterpret_cast<float*>(smem);    // [nz][128]
   float* qs = Ts + D * D;                        // [g][128]
@@ -72,6 +72,11 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs 
   const float sg = tk.sigma[(size_t)set * D + j];
   const int bw = tk.widths[(size_t)set * D + j];
   const float bk = tk.base[(size_t)set * D + j];
+  // This kernel may start while the previous kernel of the stream (an append, say) still runs: wait for it
+  // before reading q, and only then release decode_kernel, whose record copies must see every record written
+  // before this call. The transform above is already in flight.
+  pdl_wait();
+  pdl_launch_dependents();
   const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kh * g) * D;
   for (int i = tid; i < g * D; i += QP_THREADS) qs[i] = __bfloat162float(qg[i]);
   bool ok = true;
@@ -618,23 +623,23 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   if (!s_last) return;
   __threadfence();
 
-  // ======== last CTA of (b, kh): weighted sum of the split partials (streamed by bulk copies) ========
-  float* esc = reinterpret_cast<float*>(smem + L.tail_reserve);   // [MAX_SPLITS][8] split weights of a chunk
-  float* hst = esc + MAX_SPLITS * MAX_G;                          // Mrun[8], Lrun[8], Mnew[8], scale[8]
+  // ======== last CTA of (b, kh): weighted sum of the split partials ========
+  // The partials arrive in shared memory by bulk copies (chunks of splits); warp h (< g) keeps head h's running
+  // maximum M_h and L_h = sum e_s l_s with the weights e_s = 2^(m_s - M_h) (lanes over the chunk's splits,
+  // shuffle reductions); every thread then adds its outputs' sum e_s N_s from shared memory.
+  float* esc = reinterpret_cast<float*>(smem + L.tail_reserve);  // [MAX_SPLITS][8] weights of the chunk
+  float* hst = esc + MAX_SPLITS * MAX_G;                         // L[8], rescale of the running sums[8]
   const float* pb = a.part + (size_t)bh * a.splits * g * PSTR;
   const int S = a.splits;
   const uint32_t per_split = (uint32_t)g * PSTR * 4;
   const int chunk_splits = max(1, min(S, min((int)(L.tail_reserve / per_split), MAX_SPLITS)));
-  const int items = g * D;
   constexpr int ITEMS_PER_THREAD = MAX_G * D / DTHREADS;
+  constexpr int SPL = MAX_SPLITS / 32;  // splits per lane within a chunk
   float accN[ITEMS_PER_THREAD];
 #pragma unroll
   for (int r = 0; r < ITEMS_PER_THREAD; ++r) accN[r] = 0.f;
-  if (tid < g) {
-    hst[tid] = -INFINITY;
-    hst[MAX_G + tid] = 0.f;
-  }
-  uint32_t tphase = nzV > 0 ? 1u : 0u;  // phase 0 of tbar went to the T' copy when there was one
+  float M_run = -INFINITY, L_run = 0.f;  // warp h's running state of head h
+  uint32_t tphase = nzV > 0 ? 1u : 0u;   // phase 0 of tbar went to the T' copy when there was one
   fence_proxy_async_global();
   const float* cp = reinterpret_cast<const float*>(smem);
   for (int c0s = 0; c0s < S; c0s += chunk_splits) {
@@ -649,34 +654,44 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
     if (!okc && tid == 0) mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);  // drain before leaving
     tphase ^= 1u;
     if (!__syncthreads_and(okc)) return;
-    if (tid < g) {  // running maximum of head tid over the splits seen so far
-      const int h = tid;
+    if (warp < g) {
+      const int h = warp;
+      float ms[SPL];
       float cm = -INFINITY;
-      for (int sp = 0; sp < n; ++sp) cm = fmaxf(cm, cp[(sp * g + h) * PSTR]);
-      const float Mo = hst[h], Mn = fmaxf(Mo, cm);
-      hst[2 * MAX_G + h] = Mn;
-      hst[3 * MAX_G + h] = (Mo == Mn) ? 1.f : exp2f(Mo - Mn);
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) {
+        const int sp = lane + 32 * i;
+        ms[i] = sp < n ? cp[(sp * g + h) * PSTR] : -INFINITY;
+        cm = fmaxf(cm, ms[i]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+      const float Mn = fmaxf(M_run, cm);
+      const float sc = (M_run == Mn) ? 1.f : exp2f(M_run - Mn);
+      float l = 0.f;
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) {
+        const int sp = lane + 32 * i;
+        if (sp < n) {
+          const float e = ms[i] == -INFINITY ? 0.f : exp2f(ms[i] - Mn);
+          esc[sp * MAX_G + h] = e;
+          l = fmaf(e, cp[(sp * g + h) * PSTR + 1], l);
+        }
+      }
+      L_run = fmaf(L_run, sc, warp_sum(l));
+      M_run = Mn;
+      if (lane == 0) {
+        hst[h] = L_run;
+        hst[MAX_G + h] = sc;
+      }
     }
     __syncthreads();
-    for (int idx = tid; idx < n * g; idx += DTHREADS) {
-      const int sp = idx / g, h = idx - sp * g;
-      const float ms = cp[(sp * g + h) * PSTR];
-      esc[sp * MAX_G + h] = (ms == -INFINITY) ? 0.f : exp2f(ms - hst[2 * MAX_G + h]);
-    }
-    __syncthreads();
-    if (tid < g) {
-      const int h = tid;
-      float l = hst[MAX_G + h] * hst[3 * MAX_G + h];
-      for (int sp = 0; sp < n; ++sp) l = fmaf(esc[sp * MAX_G + h], cp[(sp * g + h) * PSTR + 1], l);
-      hst[MAX_G + h] = l;
-      hst[h] = hst[2 * MAX_G + h];
-    }
 #pragma unroll
     for (int r = 0; r < ITEMS_PER_THREAD; ++r) {
       const int it = tid + r * DTHREADS;
-      if (it < items) {
+      if (it < g * D) {
         const int h = it >> 7, k = it & (D - 1);
-        float acc = accN[r] * hst[3 * MAX_G + h];
+        float acc = accN[r] * hst[MAX_G + h];
         for (int sp = 0; sp < n; ++sp) acc = fmaf(esc[sp * MAX_G + h], cp[(sp * g + h) * PSTR + 4 + k], acc);
         accN[r] = acc;
       }
@@ -686,9 +701,9 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
 #pragma unroll
   for (int r = 0; r < ITEMS_PER_THREAD; ++r) {
     const int it = tid + r * DTHREADS;
-    if (it < items) {
+    if (it < g * D) {
       const int h = it >> 7, k = it & (D - 1);
-      const float Lh = hst[MAX_G + h];
+      const float Lh = hst[h];
       a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] =
           Lh > 0.f ? TV.base[(size_t)set * D + k] + accN[r] / Lh : 0.f;
     }
@@ -780,7 +795,23 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   a.scale_log2 = scale * 1.4426950408889634f;
   const size_t qsm = qprep_smem_bytes();
   cudaFuncSetAttribute(qprep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qsm);
-  qprep_kernel<<<dim3(c.Hkv, B), QP_THREADS, qsm, s>>>(P, a);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    cudaLaunchConfig_t qc = {};
+    qc.gridDim = dim3(c.Hkv, B);
+    qc.blockDim = dim3(QP_THREADS);
+    qc.dynamicSmemBytes = qsm;
+    qc.stream = s;
+    qc.attrs = pdl;
+    qc.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&qc, qprep_kernel, P, a);
+    if (e != cudaSuccess) {
+      set_error("qprep_kernel launch: %s", cudaGetErrorString(e));
+      return KV_ERR_CUDA;
+    }
+  }
   kv_status st = launch_check("qprep_kernel");
   if (st != KV_OK) return st;
   const int nb = a.g <= 4 ? 1 : 2;
@@ -790,10 +821,7 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   cfg.blockDim = dim3(DTHREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
+  cfg.attrs = pdl;
   cfg.numAttrs = 1;
   const cudaError_t e = nb == 1 ? launch_decode_nb<1>(cfg, P, a, rt) : launch_decode_nb<2>(cfg, P, a, rt);
   if (e != cudaSuccess) {

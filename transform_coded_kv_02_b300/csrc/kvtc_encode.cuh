@@ -89,6 +89,9 @@ __global__ void __launch_bounds__(AP_THREADS) encode_append_kernel(ParamsDev P, 
   float* ys = xs + D;
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t rec_s[2 * MAX_RW + 4];
+  // a decode call that follows may start preparing (its q-preparation waits for this grid before it reads q
+  // or lets the decode kernel copy records)
+  pdl_launch_dependents();
   const int tensor = blockIdx.y, bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const int b = bh / a.Hkv, h = bh - b * a.Hkv;
   const int set = a.per_seq ? bh : h;
