@@ -375,6 +375,19 @@ def test_decode_bf16_comparator_matches_exact_attention():
     assert err.max() <= 1e-4, err
 
 
+@pytest.mark.parametrize("seq_len", [1, 63, 1000, 2048])
+def test_decode_llama_shape_all_key_blocks(seq_len):
+    """Llama-shaped keys fill all eight 16-channel blocks, which selects the software-pipelined key loop; ragged
+    lengths exercise its partial last tile."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    L = synth.make_layer(w, T=2048, steps=1)
+    sets = G.calibrate_oracle(L, 2.75, 2.75)
+    assert min(int(np.max(np.nonzero(s[0].widths)[0])) + 1 for s in sets) > 96
+    P = G.lib_params(sets)
+    err = _decode_case(L, sets, P, w.Hq, False, [seq_len], 2048)
+    assert err.max() <= DEC_TOL, (seq_len, err)
+
+
 def test_decode_full_size_llama_32k():
     """The 32K-token Llama-shaped layer (32 q / 8 KV heads, 2.75 bits) in the bench's launch configuration:
     every output row against the oracle on the same records."""

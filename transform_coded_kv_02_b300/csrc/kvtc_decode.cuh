@@ -179,8 +179,10 @@ __device__ __forceinline__ uint32_t ldsw(const T* base, uint32_t off) {
 
 // RT > 0: keys and values both use records of RT words; the ring stage size and count and the offsets between
 // a lane's two tokens (two records) are compile-time, so each staged-record address is one add away.
-template <int NB, int RT>
+// PIPE: the key warps run the software-pipelined loop (one column block, all eight key channel blocks).
+template <int NB, int RT, bool PIPE>
 __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArgs a) {
+  static_assert(!PIPE || NB == 1, "the pipelined key loop handles one column block");
   extern __shared__ __align__(128) uint8_t smem[];
   // barriers live outside the dynamic region, which the epilogue and the tail reuse wholesale
   __shared__ __align__(8) uint64_t full[MAX_STAGES], empty[MAX_STAGES], pF[DWARPS], pE[DWARPS], tbar_s;
@@ -322,6 +324,88 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
       c1[nb] = h < g ? a.qc[bh * 16 + 8 + h] : 0.f;
     }
     int hand = 0;  // handoffs to the value warp so far
+    if constexpr (PIPE) {
+      // Software pipeline: tile i + 1's record loads, code extraction and logit MMAs are issued in the same
+      // straight-line block as tile i's softmax, so that the two interleave. All eight channel blocks are
+      // processed (blocks past the last nonzero-width channel hold zero descriptors and meet a zero q').
+      const int n_in = (int)(t1 - t0);  // tokens of this split
+      float accC[4] = {0.f, 0.f, 0.f, 0.f}, accN[4];
+      uint32_t zC[4] = {0u, 0u, 0u, 0u}, zN[4];
+      auto tile_logits = [&](int j, float (&acc)[4], uint32_t (&zw)[4]) -> bool {
+        const int sj = j % NS;
+        const uint8_t* st = smem + (size_t)sj * stage_bytes;
+        if (issuer) issue_until(j, true);
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[sj]), (uint32_t)((j / NS) & 1), a.wait_ns)))
+          return false;
+        zw[0] = ldsw(st, kz);
+        zw[1] = ldsw(st, kz + kstep);
+        zw[2] = ldsw(st, vz);
+        zw[3] = ldsw(st, vz + vstep);
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          uint32_t af[4];
+          af[0] = unpack_pair(ldsw(st, ka[kb][0]), ks[kb][0], km[kb][0]);
+          af[1] = unpack_pair(ldsw(st, ka[kb][0] + kstep), ks[kb][0], km[kb][0]);
+          af[2] = unpack_pair(ldsw(st, ka[kb][1]), ks[kb][1], km[kb][1]);
+          af[3] = unpack_pair(ldsw(st, ka[kb][1] + kstep), ks[kb][1], km[kb][1]);
+          mma_f16(acc, af, qb[kb][0][0], qb[kb][0][1]);
+        }
+        return true;
+      };
+      bool ok = ntiles == 0 || tile_logits(0, accC, zC);
+      if (!ok) s_abort = 1;
+      for (int i = 0; ok && i < ntiles; ++i) {
+        // tile i's codes are in registers: release its stage before waiting for the next one
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[i % NS]));
+        if (issuer) issue_until(i + NS - 1, false);
+        if (i + 1 < ntiles && !tile_logits(i + 1, accN, zN)) {
+          s_abort = 1;
+          break;
+        }
+        const int my0 = i * DT + 16 * pw;
+        const bool valid0 = my0 + gid < n_in, valid1 = my0 + gid + 8 < n_in;
+        const float zk0 = half_bits_to_float(zC[0]), sk0 = half_bits_to_float(zC[0] >> 16);
+        const float zk1 = half_bits_to_float(zC[1]), sk1 = half_bits_to_float(zC[1] >> 16);
+        const float zv0 = half_bits_to_float(zC[2]), sv0 = half_bits_to_float(zC[2] >> 16);
+        const float zv1 = half_bits_to_float(zC[3]), sv1 = half_bits_to_float(zC[3] >> 16);
+        const float r0 = accC[0] + accC[1], r1 = accC[2] + accC[3];
+        const float l0 = valid0 ? fmaf(sk0, r0, fmaf(zk0, c1[0], c0[0])) : -INFINITY;
+        const float l1 = valid1 ? fmaf(sk1, r1, fmaf(zk1, c1[0], c0[0])) : -INFINITY;
+        float mt = fmaxf(l0, l1);
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        const float m_new = fmaxf(m_run[0], mt);
+        const float corr = (m_run[0] == m_new) ? 1.f : exp2f(m_run[0] - m_new);
+        const float p0 = valid0 ? exp2f(l0 - m_new) : 0.f;
+        const float p1 = valid1 ? exp2f(l1 - m_new) : 0.f;
+        l_run[0] = fmaf(l_run[0], corr, p0 + p1);
+        z_run[0] = fmaf(z_run[0], corr, (valid0 ? p0 * zv0 : 0.f) + (valid1 ? p1 * zv1 : 0.f));
+        m_run[0] = m_new;
+        const float w0 = valid0 ? p0 * sv0 : 0.f, w1 = valid1 ? p1 * sv1 : 0.f;
+        const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
+        const uint32_t e0 = pack_half2(h0, __float2half_rn(w0 - __half2float(h0)));
+        const uint32_t e1 = pack_half2(h1, __float2half_rn(w1 - __half2float(h1)));
+        if (hand > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&pE[pw]), (uint32_t)((hand - 1) & 1), a.wait_ns))) {
+          s_abort = 1;
+          break;
+        }
+        reinterpret_cast<uint32_t*>(ps)[(gid * 8 + 2 * tig) >> 1] = e0;
+        reinterpret_cast<uint32_t*>(ps)[((gid + 8) * 8 + 2 * tig) >> 1] = e1;
+        if (gid == 0) pcorr[tig] = corr;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&pF[pw]));
+        ++hand;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          accC[e] = accN[e];
+          zC[e] = zN[e];
+        }
+      }
+    } else {
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % NS;
       const uint8_t* st = smem + (size_t)s * stage_bytes;
@@ -405,6 +489,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&pF[pw]));
       ++hand;
+    }
     }
     if (issuer) s_issued = next_issue;
     // this pair's softmax state into the per-pair partial (the region lies past the ring)
@@ -749,21 +834,22 @@ static int compile_time_record_words(int RK, int RV) {
   }
 }
 
-template <int NB, int RT>
+template <int NB, int RT, bool PIPE>
 static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a) {
-  cudaFuncSetAttribute(decode_kernel<NB, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RT>, P, a);
+  cudaFuncSetAttribute(decode_kernel<NB, RT, PIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)cfg.dynamicSmemBytes);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RT, PIPE>, P, a);
 }
 
-template <int NB>
+template <int NB, bool PIPE>
 static cudaError_t launch_decode_nb(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a, int rt) {
   switch (rt) {
-    case 5: return launch_decode_kernel<NB, 5>(cfg, P, a);
-    case 8: return launch_decode_kernel<NB, 8>(cfg, P, a);
-    case 11: return launch_decode_kernel<NB, 11>(cfg, P, a);
-    case 12: return launch_decode_kernel<NB, 12>(cfg, P, a);
-    case 16: return launch_decode_kernel<NB, 16>(cfg, P, a);
-    default: return launch_decode_kernel<NB, 0>(cfg, P, a);
+    case 5: return launch_decode_kernel<NB, 5, PIPE>(cfg, P, a);
+    case 8: return launch_decode_kernel<NB, 8, PIPE>(cfg, P, a);
+    case 11: return launch_decode_kernel<NB, 11, PIPE>(cfg, P, a);
+    case 12: return launch_decode_kernel<NB, 12, PIPE>(cfg, P, a);
+    case 16: return launch_decode_kernel<NB, 16, PIPE>(cfg, P, a);
+    default: return launch_decode_kernel<NB, 0, PIPE>(cfg, P, a);
   }
 }
 
@@ -823,7 +909,10 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  const cudaError_t e = nb == 1 ? launch_decode_nb<1>(cfg, P, a, rt) : launch_decode_nb<2>(cfg, P, a, rt);
+  // the pipelined key loop processes all eight key channel blocks: taken when every set needs at least seven
+  const bool pipe = nb == 1 && P.t[0].min_nz > 6 * 16;
+  const cudaError_t e = nb == 1 ? (pipe ? launch_decode_nb<1, true>(cfg, P, a, rt) : launch_decode_nb<1, false>(cfg, P, a, rt))
+                                : launch_decode_nb<2, false>(cfg, P, a, rt);
   if (e != cudaSuccess) {
     set_error("decode_kernel launch: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;

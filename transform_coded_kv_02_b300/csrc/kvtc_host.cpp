@@ -672,6 +672,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     td.nz = (const int32_t*)(b + pnz[t].off);
     td.slots = (const uint32_t*)(b + psl[t].off);
     td.r_words = p->r_words[t];
+    const int32_t* nzh = (const int32_t*)&blob[pnz[t].off];
+    td.min_nz = S > 0 ? *std::min_element(nzh, nzh + S) : 0;
   }
   p->dev.n_sets = S;
   return KV_OK;

@@ -37,6 +37,7 @@ struct TensorDev {
                                    // channel pair (2k, 2k+1) of a one-token record (k < D/2); values: entry j =
                                    // channel j of a two-token record (code words start at record word 2)
   int r_words;                     // record words per token (same for every set)
+  int min_nz;                      // smallest nz over the sets
 };
 
 struct ParamsDev {
