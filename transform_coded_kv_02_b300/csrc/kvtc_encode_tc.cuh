@@ -51,8 +51,11 @@ __host__ __device__ inline EncTcSmem enc_tc_smem(int RK, int RV, int nacc) {
   const uint32_t kw = (uint32_t)TC_TILE * (uint32_t)(RK | 1);
   const uint32_t vw = (uint32_t)(TC_TILE / 2 + 1) * (uint32_t)(2 * RV + 1);
   const uint32_t stage_words = kw > vw ? kw : vw;
-  s.par = 0;      // float4 [128]: mu, 1/sigma (NaN if zero width), 2^b, 2^b - 1/2
-  s.bits = D * 16;  // uint32 [128]: byte offset of the code word in the record | bit << 16
+  // per channel pair (2i, 2i + 1): pmi float4 {mu, mu', 1/sigma, 1/sigma'} (1/sigma NaN at zero width),
+  // ptc float4 {2^b, 2^b', 2^b - 1/2, 2^b' - 1/2}, phh float2 {1/2 - 2^(b-21), ...}, pbits uint2 {byte offset of
+  // the code word in the record | bit << 16, ...}
+  s.par = 0;
+  s.bits = D * 8 + D * 8 + D * 4;
   s.stage = s.bits + D * 4;                    // record staging
   s.epi_group = (s.stage + stage_words * 4 + 127) & ~127u;
   s.total = 1024 + s.epi + (uint32_t)nacc * s.epi_group;  // 1024: alignment slack of the base
@@ -219,8 +222,10 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
     const int g = warp >> 2, q = warp & 3;
     const int row = 32 * q + lane;  // accumulator lane = token row of the tile
     uint8_t* eg = gbase + L.epi + g * L.epi_group;
-    float4* par = reinterpret_cast<float4*>(eg + L.par);
-    uint32_t* pbits = reinterpret_cast<uint32_t*>(eg + L.bits);
+    float* const pmi = reinterpret_cast<float*>(eg + L.par);       // [64][4]
+    float* const ptc = pmi + 4 * (D / 2);                            // [64][4]
+    float* const phh = ptc + 4 * (D / 2);                            // [64][2]
+    uint32_t* const pbits = reinterpret_cast<uint32_t*>(eg + L.bits);  // [64][2]
     uint32_t* stage = reinterpret_cast<uint32_t*>(eg + L.stage);
     int cached_key = -1, k = 0;
     for (int u = u0 + g; u < u1; u += NACC, ++k) {
@@ -232,11 +237,12 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
         const int j = row;
         const size_t so = (size_t)set * D;
         const int w = td.widths[so + j];
-        float4 pv;
-        pv.x = td.mu[so + j];
-        pv.y = w > 0 ? td.inv_sigma[so + j] : __int_as_float(0x7fc00000);  // NaN: out of min/max, code 0
-        pv.z = exp2i(w);
-        pv.w = (float)((1 << w) - 1) + 0.5f;
+        const int jp = j >> 1, jo = j & 1;
+        pmi[4 * jp + jo] = td.mu[so + j];
+        pmi[4 * jp + 2 + jo] = w > 0 ? td.inv_sigma[so + j] : __int_as_float(0x7fc00000);  // NaN: out of min/max
+        ptc[4 * jp + jo] = exp2i(w);
+        ptc[4 * jp + 2 + jo] = (float)((1 << w) - 1) + 0.5f;
+        phh[j] = 0.5f - exp2i(w - 21);
         uint32_t word, bit;
         if (tensor == 0) {
           const uint32_t dsc = td.slots[so + (j >> 1)];
@@ -248,7 +254,6 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
           bit = (dsc >> 8) & 255u;
         }
         if (w == 0) bit = 0u;
-        par[j] = pv;
         pbits[j] = (4u * word) | (bit << 16);
         cached_key = unit_tkey(u);
         named_bar(1 + g, 128);
@@ -262,20 +267,27 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       }
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
-      // ---- pass 1: min / max of y'_j over the channels with b_j > 0 (the others give NaN, which min/max skip) ----
+      // ---- pass 1: y'_j = (y_j - mu_j) / sigma_j two channels at a time, min / max over b_j > 0 (the others are
+      // NaN, which min and max skip); y' goes back to tensor memory for pass 2 ----
       float m = INFINITY, M = -INFINITY;
       for (int cb = 0; cb < nblk; ++cb) {
         uint32_t v[16];
         tmem_ld_32x32b_x16(tacc + 16u * cb, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const float2 p = *reinterpret_cast<const float2*>(&par[16 * cb + jj]);
-          const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
-          m = fminf(m, yp);
-          M = fmaxf(M, yp);
+        for (int jp = 0; jp < 8; ++jp) {
+          const float4 mi = reinterpret_cast<const float4*>(pmi)[8 * cb + jp];
+          const float2 yp = f2unpack(f2mul(f2sub(f2pack(__uint_as_float(v[2 * jp]), __uint_as_float(v[2 * jp + 1])),
+                                                 f2pack(mi.x, mi.y)),
+                                           f2pack(mi.z, mi.w)));
+          m = fminf(m, fminf(yp.x, yp.y));
+          M = fmaxf(M, fmaxf(yp.x, yp.y));
+          v[2 * jp] = __float_as_uint(yp.x);
+          v[2 * jp + 1] = __float_as_uint(yp.y);
         }
+        tmem_st_32x32b_x16(tacc + 16u * cb, v);
       }
+      tmem_st_wait();
       __half zh = __ushort_as_half(0), sh = __ushort_as_half(0);
       if (nz > 0) {
         zh = half_sat_rn(__fadd_rn(m, 0.f));
@@ -299,21 +311,26 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       const uint32_t rec_s = smem_u32(rec);
       const uint32_t hsh = tensor == 0 ? 0u : 16u * (uint32_t)half;  // value token: its half of each code word
       const float rs = coded ? __frcp_rn(sf) : 0.f;
+      const uint64_t zz = f2pack(zf, zf), rr = f2pack(rs, rs), hv = f2pack(0.5f, 0.5f);
       bool near = false;
       for (int cb = 0; cb < nblk; ++cb) {
         uint32_t v[16];
-        tmem_ld_32x32b_x16(tacc + 16u * cb, v);
+        tmem_ld_32x32b_x16(tacc + 16u * cb, v);  // y'
         tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int j = 16 * cb + jj;
-          const float4 p = par[j];
-          const uint32_t pb = pbits[j];
-          const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
-          const float uq = fminf(fmaxf(__fmul_rn(__fsub_rn(yp, zf), __fmul_rn(rs, p.z)), 0.5f), p.w);
-          const float fl = floorf(uq);
-          near |= fabsf(__fsub_rn(__fsub_rn(uq, fl), 0.5f)) > fmaf(p.z, -0x1p-21f, 0.5f);
-          red_or_shared(rec_s + (pb & 0xFFFFu), (uint32_t)fl << ((pb >> 16) + hsh));
+        for (int jp = 0; jp < 8; ++jp) {
+          const float4 tc = reinterpret_cast<const float4*>(ptc)[8 * cb + jp];
+          const float2 hh = reinterpret_cast<const float2*>(phh)[8 * cb + jp];
+          const uint2 pb = reinterpret_cast<const uint2*>(pbits)[8 * cb + jp];
+          float2 u = f2unpack(f2mul(f2sub(f2pack(__uint_as_float(v[2 * jp]), __uint_as_float(v[2 * jp + 1])), zz),
+                                    f2mul(rr, f2pack(tc.x, tc.y))));
+          u.x = fminf(fmaxf(u.x, 0.5f), tc.z);
+          u.y = fminf(fmaxf(u.y, 0.5f), tc.w);
+          const float flx = floorf(u.x), fly = floorf(u.y);
+          const float2 t = f2unpack(f2sub(f2sub(f2pack(u.x, u.y), f2pack(flx, fly)), hv));
+          near |= (fabsf(t.x) > hh.x) | (fabsf(t.y) > hh.y);
+          red_or_shared(rec_s + (pb.x & 0xFFFFu), (uint32_t)flx << ((pb.x >> 16) + hsh));
+          red_or_shared(rec_s + (pb.y & 0xFFFFu), (uint32_t)fly << ((pb.y >> 16) + hsh));
         }
       }
       near = near && coded;
@@ -326,12 +343,11 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int j = 16 * cb + jj;
-              const float4 p = par[j];
+              const float tb = ptc[4 * (j >> 1) + (j & 1)], cm = ptc[4 * (j >> 1) + 2 + (j & 1)];
               const uint32_t pb = pbits[j];
-              const float yp = __fmul_rn(__fsub_rn(__uint_as_float(v[jj]), p.x), p.y);
-              const float dq = __fsub_rn(yp, zf);
-              const uint32_t fast = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(dq, __fmul_rn(rs, p.z)), 0.5f), p.w));
-              const uint32_t exact = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(__fdiv_rn(dq, sf), p.z), 0.5f), p.w));
+              const float dq = __fsub_rn(__uint_as_float(v[jj]), zf);
+              const uint32_t fast = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(dq, __fmul_rn(rs, tb)), 0.5f), cm));
+              const uint32_t exact = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(__fdiv_rn(dq, sf), tb), 0.5f), cm));
               if (fast != exact) red_xor_shared(rec_s + (pb & 0xFFFFu), (fast ^ exact) << ((pb >> 16) + hsh));
             }
           }
