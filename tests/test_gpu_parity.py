@@ -189,8 +189,8 @@ def test_encode_paths_bf16_llama_shape(llama_300, path, dst0):
 
 @pytest.mark.parametrize("bits", [1.33, 4.0, 8.0])
 def test_encode_tensor_core_budgets_per_sequence(bits):
-    """Tensor-core encode at 5, 16 and 32 record words (the last one's record staging is the largest in
-    shared memory), one parameter set per (sequence, head).
+    """Tensor-core encode at 5, 16 and 32 record words (four epilogue groups at 5 and 16 words; at 32 the record
+    staging only fits three), one parameter set per (sequence, head).
 
     The 1e-4 mismatch bar belongs to the workloads' budgets (at most 4 bits per element). A code flips when the
     fp32 rotation's rounding error carries a value across a bin edge, so the flip rate scales with 1 / bin

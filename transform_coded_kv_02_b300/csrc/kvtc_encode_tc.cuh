@@ -27,7 +27,7 @@ namespace kvtc {
 constexpr int TC_TILE = 128;           // tokens per unit
 constexpr int TC_NSPLIT = 3;           // bf16 terms of T
 constexpr int TC_NST = 2;              // X stages
-constexpr int TC_NACC = 3;             // tensor-memory accumulators = epilogue groups
+constexpr int TC_NACC_MAX = 4;         // tensor-memory accumulators = epilogue groups (4, or 3 for long records)
 constexpr uint32_t TC_OP_BYTES = 128u * 128u * 2u;   // one 128 x 128 bf16 operand (two 64-column boxes)
 constexpr uint32_t TC_BOX_BYTES = 128u * 128u;       // one 128-row x 128-byte box
 
@@ -117,6 +117,7 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
     fence_mbar_init();
     s_abort = 0;
   }
+  static_assert(NACC >= 1 && NACC <= 4, "128 tensor-memory columns per accumulator, 512 in all");
   constexpr uint32_t TMEM_COLS = NACC <= 2 ? 256u : 512u;  // 128 columns per accumulator, a power of two
   if (warp == mma_warp) {
     tmem_alloc(smem_u32(&s_tmem), TMEM_COLS);
@@ -498,9 +499,10 @@ static kv_status launch_encode_tc(const ParamsDev& P, const kv_cache& c, const v
     return KV_ERR_UNSUPPORTED;
   }
   const int RK = P.t[0].r_words, RV = P.t[1].r_words;
-  // three epilogue groups: 14 warps, i.e. at most four per SM sub-partition, leave 128 registers a thread;
-  // their shared memory fits for every record length up to 33 words
-  const uint32_t smem = enc_tc_smem(RK, RV, TC_NACC).total;
+  // four epilogue groups (18 warps, 96 registers a thread) where their record staging fits in shared memory,
+  // else three (14 warps), which fit for every record length up to 33 words
+  const int nacc = enc_tc_smem(RK, RV, TC_NACC_MAX).total <= 227u * 1024u ? TC_NACC_MAX : TC_NACC_MAX - 1;
+  const uint32_t smem = enc_tc_smem(RK, RV, nacc).total;
   if (smem > 227u * 1024u) {
     set_error("tensor-core encode: %u bytes of shared memory needed", smem);
     return KV_ERR_UNSUPPORTED;
@@ -533,7 +535,8 @@ static kv_status launch_encode_tc(const ParamsDev& P, const kv_cache& c, const v
   int dev = 0;
   cudaGetDevice(&dev);
   const int grid = (int)std::min<long long>(units, sm_count(dev));
-  const cudaError_t e = launch_encode_tc_n<TC_NACC>(P, a, maps, smem, s, grid);
+  const cudaError_t e = nacc == TC_NACC_MAX ? launch_encode_tc_n<TC_NACC_MAX>(P, a, maps, smem, s, grid)
+                                            : launch_encode_tc_n<TC_NACC_MAX - 1>(P, a, maps, smem, s, grid);
   if (e != cudaSuccess) {
     set_error("encode_tc_kernel launch: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;
