@@ -64,6 +64,11 @@ def make_workload(n_new: int):
     return w, L
 
 
+def workload_name(w, rk_w: int, rv_w: int) -> str:
+    return (f"llama3.1-8b layer decode: {w.Hq} q / {w.Hkv} kv heads, d={w.d}, batch {w.B}, {w.T} cached tokens growing "
+            f"by 1 per step, {BITS} bits/elem (K {rk_w} + V {rv_w} words/token), append-encode + decode per step")
+
+
 def step_bytes(T_ctx: int, w, rk: int, rv: int) -> int:
     """Algorithmic bytes of one step at context length T_ctx (after the append)."""
     B, Hkv, Hq, d = w.B, w.Hkv, w.Hq, w.d
@@ -254,8 +259,7 @@ def run_reference(args, rank, world):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": "llama3.1-8b layer decode: 32 q / 8 kv heads, d=128, batch 1, 32768 cached "
-                                   "tokens, 2.75 bits/elem, append + decode per step", "l2": "n/a (host)"},
+            "config": {"workload": workload_name(w, 11, 11), "l2": "n/a (host)", "parallelism": "single host"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -456,9 +460,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": total / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u32-packed codes, f16 mma / f32 accumulate", "data": "synthetic",
-        "config": {"workload": f"llama3.1-8b layer decode: {Hq} q / {Hkv} kv heads, d={d}, batch {B}, {T} cached "
-                               f"tokens growing by 1 per step, {BITS} bits/elem (K {rk_w} + V {rv_w} words/token), "
-                               f"append-encode + decode per step",
+        "config": {"workload": workload_name(w, rk_w, rv_w),
                    "l2": "flushed before every timed step (2 x L2 buffer written, outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single gpu"},
         "roofline": {"bound": "hbm", "kernel": "kv_attend_decode (qprep_kernel + decode_kernel)",
