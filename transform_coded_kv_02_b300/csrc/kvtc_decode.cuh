@@ -672,30 +672,23 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   if (!okw && tid == 0) mbar_wait_bounded(smem_u32(tbar), 0u, a.wait_ns);  // drain before leaving
   if (__syncthreads_or(!okw)) return;
   float* part = a.part + ((size_t)bh * a.splits + split) * g * PSTR;
-  static_assert(DTHREADS == 2 * D, "two threads per channel of the original basis");
-  {  // thread: channel k of the original basis for the heads of one parity
-    const int k = tid & (D - 1), hp = tid >> 7;
-    const float wk = TV.wsum[(size_t)set * D + k];
-    float n[MAX_G / 2];
-#pragma unroll
-    for (int i = 0; i < MAX_G / 2; ++i) {
-      const int h = hp + 2 * i;
-      n[i] = h < g ? mS[2 * MAX_G + h] * wk : 0.f;
-    }
+  static_assert(DTHREADS / 32 >= MAX_G && 4 * 32 == D, "a warp per query head, four original channels a lane");
+  if (warp < g) {  // warp h: N_h[k] for k = 4 lane .. 4 lane + 3, one 128-bit row segment of T' per rotated channel
+    const int h = warp;
+    const float4 w4 = reinterpret_cast<const float4*>(TV.wsum + (size_t)set * D)[lane];
+    const float zh = mS[2 * MAX_G + h];
+    float4 n = make_float4(zh * w4.x, zh * w4.y, zh * w4.z, zh * w4.w);
+    const float* ah = mA + h * D;
 #pragma unroll 4
     for (int jj = 0; jj < nzV; ++jj) {
-      const float t = Tsc[jj * D + k];
-#pragma unroll
-      for (int i = 0; i < MAX_G / 2; ++i) {
-        const int h = hp + 2 * i;
-        if (h < g) n[i] = fmaf(t, mA[h * D + jj], n[i]);
-      }
+      const float4 t = reinterpret_cast<const float4*>(Tsc + jj * D)[lane];
+      const float aj = ah[jj];
+      n.x = fmaf(t.x, aj, n.x);
+      n.y = fmaf(t.y, aj, n.y);
+      n.z = fmaf(t.z, aj, n.z);
+      n.w = fmaf(t.w, aj, n.w);
     }
-#pragma unroll
-    for (int i = 0; i < MAX_G / 2; ++i) {
-      const int h = hp + 2 * i;
-      if (h < g) part[h * PSTR + 4 + k] = n[i];
-    }
+    reinterpret_cast<float4*>(part + h * PSTR + 4)[lane] = n;
   }
   if (tid < g) {
     part[tid * PSTR + 0] = mS[tid];
