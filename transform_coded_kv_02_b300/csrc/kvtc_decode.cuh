@@ -22,7 +22,7 @@ struct DecArgs {
   const __nv_bfloat16* q;
   const int32_t* seq_lens;
   __half* qa;       // [B*Hkv][16][128]: row 2h (+1) = fp16 hi (lo) part of q' of head h
-  float* qc;        // [B*Hkv][16]: C0 of heads 0..7, C1 of heads 0..7 (base-2 logit units)
+  float* qc;        // [B*Hkv][QP_PARTS][16]: partial C0 of heads 0..7, partial C1 of heads 0..7 (base-2 logits)
   unsigned* cnt;    // [B*Hkv] arrival counters
   float* part;      // [B*Hkv][splits][g][PSTR] split partials
   float* out;       // [B][Hq][128]
@@ -38,106 +38,73 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// ---- q preparation: one CTA per (sequence, KV head) ---------------------------------------------------
-// q~ = T_K q for the g query heads (T_K rows staged in shared memory by one bulk copy, every other input
-// fetched while it flies); q'_j = a log2(e) q~_j sigma_j 2^-b_j as fp16 hi + lo; C0 = a log2(e) q.(T_K^T mu);
-// C1 = a log2(e) sum_{b_j > 0} q~_j sigma_j. 256 threads: channel j = tid % 128, half of the k range = tid / 128.
+// ---- q preparation: QP_PARTS CTAs per (sequence, KV head), 32 rotated channels each ---------------------
+// q~ = T_K q for the g query heads, read from the transposed transform (T^T row k holds T[j][k] for all j, so the
+// 32 lanes of a warp load one coalesced line per k); q'_j = a log2(e) q~_j sigma_j 2^-b_j as fp16 hi + lo;
+// partial sums per part of C0 = a log2(e) q.(T_K^T mu) and C1 = a log2(e) sum_{b_j > 0} q~_j sigma_j, which
+// the decode kernel adds up. Thread: channel j0 + (tid % 32), k slice 16 (tid / 32) .. + 16.
 constexpr int QP_THREADS = 256;
-static size_t qprep_smem_bytes() { return (size_t)D * D * 4 + 2 * (size_t)MAX_G * D * 4; }
+constexpr int QP_PARTS = D / 32;
 
 __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  float* Ts = reinterpret_cast<float*>(smem);    // [nz][128]
-  float* qs = Ts + D * D;                        // [g][128]
-  float* hs = qs + MAX_G * D;                    // [8][128] upper-half partial sums
-  __shared__ uint64_t bar;
-  __shared__ float red[4][2][MAX_G];
-  const int kh = blockIdx.x, b = blockIdx.y;
+  __shared__ float qs[MAX_G][D];
+  __shared__ float red[QP_THREADS / 32][MAX_G][33];
+  const int kh = blockIdx.x, b = blockIdx.y, part = blockIdx.z;
   const int bh = b * a.Hkv + kh;
   const int set = a.per_seq ? bh : kh;
   const TensorDev& tk = P.t[0];
   const int g = a.g, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = tid & (D - 1), hf = tid >> 7;
-  const int nz = tk.nz[set];
-  if (tid == 0) {
-    mbar_init(smem_u32(&bar), 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0 && nz > 0) {
-    mbar_expect_tx(smem_u32(&bar), (uint32_t)nz * D * 4);
-    bulk_g2s(smem_u32(Ts), tk.T + (size_t)set * D * D, (uint32_t)nz * D * 4, smem_u32(&bar));
-  }
-  // everything else is fetched while T_K is in flight
+  const int j = 32 * part + lane, k0 = 16 * warp;
+  // the transform, sigma, widths and the base vector do not depend on earlier kernels: fetch them first
+  float t[16];
+  const float* TTc = tk.TT + (size_t)set * D * D + j;
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) t[kk] = __ldg(TTc + (size_t)(k0 + kk) * D);
   const float sg = tk.sigma[(size_t)set * D + j];
   const int bw = tk.widths[(size_t)set * D + j];
   const float bk = tk.base[(size_t)set * D + j];
   // This kernel may start while the previous kernel of the stream (an append, say) still runs: wait for it
   // before reading q, and only then release decode_kernel, whose record copies must see every record written
-  // before this call. The transform above is already in flight.
+  // before this call.
   pdl_wait();
   pdl_launch_dependents();
   const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kh * g) * D;
-  for (int i = tid; i < g * D; i += QP_THREADS) qs[i] = __bfloat162float(qg[i]);
-  bool ok = true;
-  if (nz > 0) ok = mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);
-  if (!ok && tid == 0) mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);  // drain before leaving
-  if (__syncthreads_or(!ok)) return;
-
-  float qt[MAX_G];
+  for (int i = tid; i < g * D; i += QP_THREADS) qs[i / D][i % D] = __bfloat162float(qg[i]);
+  __syncthreads();
 #pragma unroll
-  for (int h = 0; h < MAX_G; ++h) qt[h] = 0.f;
-  if (j < nz) {
-    const float4* Trow = reinterpret_cast<const float4*>(Ts + (size_t)j * D) + 16 * hf;
-#pragma unroll 4
-    for (int k4 = 0; k4 < 16; ++k4) {
-      const int kk = (k4 + j) & 15;   // rotated start: conflict-free row reads
-      const float4 t = Trow[kk];
+  for (int h = 0; h < MAX_G; ++h) {
+    float acc = 0.f;
+    if (h < g) {
 #pragma unroll
-      for (int h = 0; h < MAX_G; ++h) {
-        if (h < g) {
-          const float4 qv = reinterpret_cast<const float4*>(qs + h * D)[16 * hf + kk];
-          qt[h] = fmaf(t.x, qv.x, fmaf(t.y, qv.y, fmaf(t.z, qv.z, fmaf(t.w, qv.w, qt[h]))));
-        }
-      }
+      for (int kk = 0; kk < 16; ++kk) acc = fmaf(t[kk], qs[h][k0 + kk], acc);
     }
-  }
-  if (hf == 1) {
-#pragma unroll
-    for (int h = 0; h < MAX_G; ++h) hs[h * D + j] = qt[h];
+    red[warp][h][lane] = acc;
   }
   __syncthreads();
-  if (hf == 0) {
+  if (warp == 0) {
     __half* qa = a.qa + (size_t)bh * 16 * D;
-    float c0p[MAX_G], c1p[MAX_G];
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h) {
-      const float q_t = qt[h] + hs[h * D + j];
+      float q_t = 0.f;
+#pragma unroll
+      for (int w = 0; w < QP_THREADS / 32; ++w) q_t += red[w][h][lane];
       const bool on = h < g && bw > 0;
       const float qp = on ? a.scale_log2 * q_t * sg * exp2i(-bw) : 0.f;
       const __half hi = __float2half_rn(qp);
       const __half lo = __float2half_rn(qp - __half2float(hi));
       qa[(2 * h) * D + j] = hi;
       qa[(2 * h + 1) * D + j] = lo;
-      c1p[h] = on ? q_t * sg : 0.f;
-      c0p[h] = h < g ? bk * qs[h * D + j] : 0.f;
+      const float c1 = warp_sum(on ? q_t * sg : 0.f);
+      if (lane == 0 && h < g) a.qc[(bh * QP_PARTS + part) * 16 + 8 + h] = a.scale_log2 * c1;
     }
+  } else if (warp == 1) {  // C0 over the query entries k = j0 .. j0 + 31 (the base vector is indexed like q)
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h) {
-      const float s0 = warp_sum(c0p[h]), s1 = warp_sum(c1p[h]);
-      if (lane == 0) {
-        red[warp][0][h] = s0;
-        red[warp][1][h] = s1;
-      }
+      const float c0 = warp_sum(h < g ? bk * qs[h][j] : 0.f);
+      if (lane == 0 && h < g) a.qc[(bh * QP_PARTS + part) * 16 + h] = a.scale_log2 * c0;
     }
   }
-  __syncthreads();
-  if (tid < g) {
-    const int h = tid;
-    a.qc[bh * 16 + h] = a.scale_log2 * (red[0][0][h] + red[1][0][h] + red[2][0][h] + red[3][0][h]);
-    a.qc[bh * 16 + 8 + h] = a.scale_log2 * (red[0][1][h] + red[1][1][h] + red[2][1][h] + red[3][1][h]);
-  }
-  if (tid == 0) a.cnt[bh] = 0u;
+  if (tid == 0 && part == 0) a.cnt[bh] = 0u;
 }
 
 // ---- split-K decode ----------------------------------------------------------------------------------
@@ -320,8 +287,14 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       const int h = tig + 4 * nb;
-      c0[nb] = h < g ? a.qc[bh * 16 + h] : 0.f;
-      c1[nb] = h < g ? a.qc[bh * 16 + 8 + h] : 0.f;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int pt = 0; pt < QP_PARTS; ++pt) {
+        s0 += h < g ? a.qc[(bh * QP_PARTS + pt) * 16 + h] : 0.f;
+        s1 += h < g ? a.qc[(bh * QP_PARTS + pt) * 16 + 8 + h] : 0.f;
+      }
+      c0[nb] = s0;
+      c1[nb] = s1;
     }
     int hand = 0;  // handoffs to the value warp so far
     if constexpr (PIPE) {
@@ -809,7 +782,7 @@ DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device) {
   L.off_qa = o;
   o = align256(o + bh * 16 * D * sizeof(__half));
   L.off_qc = o;
-  o = align256(o + bh * 16 * sizeof(float));
+  o = align256(o + bh * QP_PARTS * 16 * sizeof(float));
   L.off_cnt = o;
   o = align256(o + bh * sizeof(unsigned));
   L.off_part = o;
@@ -872,16 +845,14 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   const int rt = compile_time_record_words(P.t[0].r_words, P.t[1].r_words);
   a.stages = ring_stages_for(P.t[0].r_words, P.t[1].r_words);
   a.scale_log2 = scale * 1.4426950408889634f;
-  const size_t qsm = qprep_smem_bytes();
-  cudaFuncSetAttribute(qprep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qsm);
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   {
     cudaLaunchConfig_t qc = {};
-    qc.gridDim = dim3(c.Hkv, B);
+    qc.gridDim = dim3(c.Hkv, B, QP_PARTS);
     qc.blockDim = dim3(QP_THREADS);
-    qc.dynamicSmemBytes = qsm;
+    qc.dynamicSmemBytes = 0;
     qc.stream = s;
     qc.attrs = pdl;
     qc.numAttrs = 1;
