@@ -32,8 +32,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = "llama_decode_32k"
+WORKLOAD = "llama_decode_32k"   # the headline workload; --workload selects another layer shape for reports
 BITS = 2.75
+DESCRIPTION = {"llama_decode_32k": "llama3.1-8b layer decode", "qwen_batched_8k": "qwen2.5-7b batched layer decode",
+               "llama_long_128k": "llama3.1-8b long-context layer decode"}
 METRIC = "decode_attn_packed_kv_hbm_gbs"
 UNIT = "GB/s"
 # the decode kernel and the device headers it is built from: the recorded traffic is valid while they are unchanged
@@ -50,6 +52,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(DESCRIPTION),
+                    help="layer shape (the default is the headline workload)")
+    ap.add_argument("--bits", type=float, default=None, help="bits per element (default: the workload's first)")
     return ap.parse_args()
 
 
@@ -65,8 +70,14 @@ def make_workload(n_new: int):
 
 
 def workload_name(w, rk_w: int, rv_w: int) -> str:
-    return (f"llama3.1-8b layer decode: {w.Hq} q / {w.Hkv} kv heads, d={w.d}, batch {w.B}, {w.T} cached tokens growing "
-            f"by 1 per step, {BITS} bits/elem (K {rk_w} + V {rv_w} words/token), append-encode + decode per step")
+    calib = "per-sequence calibration, " if w.calib == "own_prefix" else ""
+    return (f"{DESCRIPTION[WORKLOAD]}: {w.Hq} q / {w.Hkv} kv heads, d={w.d}, batch {w.B}, {w.T} cached tokens "
+            f"growing by 1 per step, {calib}{BITS} bits/elem (K {rk_w} + V {rv_w} words/token), append-encode + "
+            f"decode per step")
+
+
+def record_words(bits: float, d: int = 128) -> int:
+    return int(math.floor(bits * d / 32 + 1e-9))
 
 
 def step_bytes(T_ctx: int, w, rk: int, rv: int) -> int:
@@ -252,14 +263,15 @@ def run_reference(args, rank, world):
         secs += s
         nbytes += b
     value = nbytes / secs / 1e9
-    full_step = step_bytes(w.T + 1, w, 11, 11)
+    rw = record_words(BITS)
+    full_step = step_bytes(w.T + 1, w, rw, rw)
     ms_per_step = full_step / (value * 1e9) * 1e3
     sample = (f"per step: one KV head (cycling over {w.Hkv}), append-encode of one token + decode of its {w.g} "
               f"query heads over {n_tok} of the {w.T} cached records")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": workload_name(w, 11, 11), "l2": "n/a (host)", "parallelism": "single host"},
+            "config": {"workload": workload_name(w, rw, rw), "l2": "n/a (host)", "parallelism": "single host"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -288,7 +300,7 @@ def run_ours(args, rank, world, local_rank):
     rk_w, rv_w = P.record_words(0), P.record_words(1)
     rec_k = torch.zeros((B, Hkv, T_cap, rk_w), dtype=torch.int32, device=dev)
     rec_v = torch.zeros((B, Hkv, T_cap // 2, 2 * rv_w), dtype=torch.int32, device=dev)  # two-token records
-    cache = kvtc.make_cache(rec_k, rec_v, B, Hkv, T_cap)
+    cache = kvtc.make_cache(rec_k, rec_v, B, Hkv, T_cap, L.per_seq_params)
 
     k_all = bf16_tensor(L.k, dev)                         # [B, Hkv, T + n_new, d]
     v_all = bf16_tensor(L.v, dev)
@@ -487,7 +499,11 @@ def run_ours(args, rank, world, local_rank):
 
 
 def main():
+    global WORKLOAD, BITS
     args = parse_args()
+    from transform_coded_kv_02_b300 import synth
+    WORKLOAD = args.workload
+    BITS = args.bits if args.bits is not None else synth.WORKLOADS[WORKLOAD].bits[0]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
