@@ -154,7 +154,13 @@ size_t kv_cache_bytes(const kv_params* p, int tensor, int B, int Hkv, int64_t T_
  * Rotation y = T x, then per token y'_j = (y_j - mu_j) * (1/sigma_j), z = fp16(min y'), s = fp16(max y' - z),
  * c_j = clamp(floor(((y'_j - z)/s) * 2^b_j), 0, 2^b_j - 1), packed as above.
  * A value token writes only its own halves (16-bit stores), so a token appended at an odd position leaves
- * the record's earlier token intact. */
+ * the record's earlier token intact.
+ * Kernels: bf16 tokens with t_new >= 128 go to the tensor cores (rotation by tcgen05 MMAs against the bf16
+ * three-way split of T, fp32 accumulation); fp32 tokens and short appends to CUDA cores (fp32 FMAs). The codes
+ * of a given rotated vector are identical on every path; the rotations themselves differ by fp32 rounding
+ * order, so the paths agree with each other and with the oracle to the end-to-end bar (1 LSB, rare).
+ * Asynchronous on `stream`; a following kv_attend_decode on the same stream may begin preparing while the
+ * append kernel finishes (programmatic dependent launch), and waits for it before reading any record. */
 kv_status kv_encode(const kv_params* p, const kv_cache* cache, const void* k, const void* v, int dtype,
                     int B, int64_t t_new, const int64_t* dst_pos_dev, kv_stream_t stream);
 
@@ -164,7 +170,10 @@ kv_status kv_encode(const kv_params* p, const kv_cache* cache, const void* k, co
  *   out: device fp32 [B][Hq][d]; softmax_scale (alpha) typically 1/sqrt(d).
  *   o_h = sum_t softmax_t(alpha q_h . k^_t) v^_t, k^ = T_K^T y^ with y^_j = mu_j + sigma_j (z + (c_j + 1/2)
  *   s 2^-b_j) for b_j > 0 and mu_j otherwise (v^ likewise). Computed in the rotated bases: q is rotated
- *   once, the output once inverse-rotated.
+ *   once per call; each split of the tokens maps its partial sum back to the original basis (T_V^T, folded
+ *   with sigma and 2^-b), and the splits are merged with their softmax weights. Kernels: a q-preparation kernel
+ *   (which waits for the previous kernel of the stream, e.g. an append, before reading q) and the split-K
+ *   decode kernel, launched as its programmatic dependant. */
  *   workspace: device, at least kv_decode_workspace_bytes(...) bytes, 16-byte aligned, reused across
  *   calls (no initialisation needed); calls that share a workspace must not overlap on the device. */
 size_t kv_decode_workspace_bytes(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap);
@@ -224,7 +233,9 @@ kv_status kv_debug_water_fill(const double* lam, int d, int budget_bits, int max
 /* Host Jacobi eigensolver used by kv_calibrate: sym [d][d] -> eigenvalues descending [d] and eigenvectors
  * as columns evecs [d][d] (row-major), sign-normalised. */
 kv_status kv_debug_eigh(const double* sym, int d, double* evals, double* evecs);
-/* Encode path selection for tests: 0 auto, 1 warp-per-token, 2 tensor-core tiles (bf16 only). */
+/* Encode path selection for tests: 0 automatic (bf16 with at least 128 new tokens per head: tensor cores;
+ * otherwise CUDA cores), 1 CUDA cores (one CTA per head for up to 16 new tokens, else one warp per token; the
+ * two write identical records), 2 tensor-core tiles (bf16 only; KV_ERR_UNSUPPORTED for fp32). */
 kv_status kv_debug_set_encode_path(int path);
 /* Device wait limit in nanoseconds for the bounded mbarrier waits (default 2e9). */
 kv_status kv_debug_set_wait_limit_ns(long long ns);
