@@ -173,7 +173,7 @@ kv_status kv_encode(const kv_params* p, const kv_cache* cache, const void* k, co
  *   once per call; each split of the tokens maps its partial sum back to the original basis (T_V^T, folded
  *   with sigma and 2^-b), and the splits are merged with their softmax weights. Kernels: a q-preparation kernel
  *   (which waits for the previous kernel of the stream, e.g. an append, before reading q) and the split-K
- *   decode kernel, launched as its programmatic dependant. */
+ *   decode kernel, launched as its programmatic dependant.
  *   workspace: device, at least kv_decode_workspace_bytes(...) bytes, 16-byte aligned, reused across
  *   calls (no initialisation needed); calls that share a workspace must not overlap on the device. */
 size_t kv_decode_workspace_bytes(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap);
