@@ -339,10 +339,13 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
         }
         const int my0 = i * DT + 16 * pw;
         const bool valid0 = my0 + gid < n_in, valid1 = my0 + gid + 8 < n_in;
-        const float zk0 = half_bits_to_float(zC[0]), sk0 = half_bits_to_float(zC[0] >> 16);
-        const float zk1 = half_bits_to_float(zC[1]), sk1 = half_bits_to_float(zC[1] >> 16);
-        const float zv0 = half_bits_to_float(zC[2]), sv0 = half_bits_to_float(zC[2] >> 16);
-        const float zv1 = half_bits_to_float(zC[3]), sv1 = half_bits_to_float(zC[3] >> 16);
+        // z/s words: fp16 z in the low half, s in the high half
+        const float2 zsk0 = __half22float2(*reinterpret_cast<const __half2*>(&zC[0]));
+        const float2 zsk1 = __half22float2(*reinterpret_cast<const __half2*>(&zC[1]));
+        const float2 zsv0 = __half22float2(*reinterpret_cast<const __half2*>(&zC[2]));
+        const float2 zsv1 = __half22float2(*reinterpret_cast<const __half2*>(&zC[3]));
+        const float zk0 = zsk0.x, sk0 = zsk0.y, zk1 = zsk1.x, sk1 = zsk1.y;
+        const float zv0 = zsv0.x, sv0 = zsv0.y, zv1 = zsv1.x, sv1 = zsv1.y;
         const float r0 = accC[0] + accC[1], r1 = accC[2] + accC[3];
         const float l0 = valid0 ? fmaf(sk0, r0, fmaf(zk0, c1[0], c0[0])) : -INFINITY;
         const float l1 = valid1 ? fmaf(sk1, r1, fmaf(zk1, c1[0], c0[0])) : -INFINITY;
@@ -351,9 +354,9 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
         const float m_new = fmaxf(m_run[0], mt);
-        const float corr = (m_run[0] == m_new) ? 1.f : exp2f(m_run[0] - m_new);
-        const float p0 = valid0 ? exp2f(l0 - m_new) : 0.f;
-        const float p1 = valid1 ? exp2f(l1 - m_new) : 0.f;
+        const float corr = (m_run[0] == m_new) ? 1.f : ex2_approx(m_run[0] - m_new);
+        const float p0 = valid0 ? ex2_approx(l0 - m_new) : 0.f;
+        const float p1 = valid1 ? ex2_approx(l1 - m_new) : 0.f;
         l_run[0] = fmaf(l_run[0], corr, p0 + p1);
         z_run[0] = fmaf(z_run[0], corr, (valid0 ? p0 * zv0 : 0.f) + (valid1 ? p1 * zv1 : 0.f));
         m_run[0] = m_new;
