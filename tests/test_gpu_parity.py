@@ -408,3 +408,145 @@ def test_wait_timeout_is_reported_not_hung():
         assert kvtc.kv_check_status() == kvtc.KV_OK
     finally:
         kvtc.kv_debug_set_wait_limit_ns(2_000_000_000)
+
+
+# ---- full sizes, at the cache capacity of bench.py's default run (8 warm-up + 256 timed steps, one appended
+# token each), which fixes the decode's split plan ----
+BENCH_APPENDED = 8 + 256
+
+
+def _bench_T_cap(T):
+    return (T + BENCH_APPENDED + 15) // 16 * 16
+
+
+def _compare_records(got, ref, p, T):
+    """Device records against the oracle's for the first T tokens of one cache row (keys [T_cap, R], values
+    [T_cap / 2, 2 R]): identical words are equal records; records with any different word are unpacked and
+    compared entry by entry. Returns (entries that differ, entries compared); asserts every entry within 1 LSB
+    and nothing written past token T."""
+    n_rec = (T + p.tokens_per_record - 1) // p.tokens_per_record
+    assert not np.any(got[n_rec:]), "records written past the last token"
+    if T % p.tokens_per_record:  # the unused token of the last value record stays zero
+        z, s, c = O.unpack(got[n_rec - 1:n_rec], p)
+        assert not (z.view(np.uint16)[1] or s.view(np.uint16)[1] or np.any(c[1])), "token T written"
+    rows = np.nonzero(np.any(got[:n_rec] != ref[:n_rec], axis=1))[0]
+    n_entries = T * (int(np.count_nonzero(p.widths)) + 2)
+    if rows.size == 0:
+        return 0, n_entries
+    tf, dz, ds, cf, dc, ef = G.token_diff(O.unpack(got[rows], p), O.unpack(ref[rows], p), p)
+    assert dc <= 1 and dz <= 1 and ds <= 1, (dz, ds, dc)
+    n_rows_entries = rows.size * p.tokens_per_record * (int(np.count_nonzero(p.widths)) + 2)
+    return ef * n_rows_entries, n_entries
+
+
+def _full_size_case(w, L, bits):
+    """kv_encode of the whole prefill (default path: tensor cores) against the oracle's records, every entry;
+    then kv_attend_decode over the oracle's records against the oracle decode, every output row."""
+    sets = G.calibrate_oracle(L, bits, bits)
+    P = G.lib_params(sets)
+    per_seq = L.per_seq_params
+    B, Hkv, T, _ = L.k.shape
+    T_cap = _bench_T_cap(T)
+    ork, orv = G.oracle_cache(synth.as_float(L.k), synth.as_float(L.v), sets, per_seq, T_cap)
+    rk, rv = _encode_gpu(P, L.k, L.v, per_seq, T_cap=T_cap)
+    n_diff, n_all = 0.0, 0
+    for b in range(B):
+        for h in range(Hkv):
+            pk, pv = sets[G.set_index(b, h, Hkv, per_seq)]
+            for got, ref, p in ((rk[b, h], ork[b, h], pk), (rv[b, h], orv[b, h], pv)):
+                nd, na = _compare_records(got, ref, p, T)
+                n_diff += nd
+                n_all += na
+    assert n_diff / n_all <= 1e-4, (n_diff / n_all, round(n_diff), n_all)
+    seq = [T] * B
+    got = G.run_decode(P, ork, orv, L.q[0], seq, w.Hq, per_seq)
+    ref = G.oracle_decode(ork, orv, L.q[0], seq, sets, w.Hq, per_seq)
+    err = G.rel_l2_rows(got, ref)
+    assert err.max() <= DEC_TOL, err.max()
+    return n_diff / n_all, err.max()
+
+
+@pytest.fixture(scope="module")
+def qwen_full():
+    w = synth.WORKLOADS["qwen_batched_8k"]
+    return w, synth.make_layer(w, steps=1)
+
+
+@pytest.mark.parametrize("bits", [2.0, 3.0, 4.0])
+def test_full_size_qwen_batched_8k(qwen_full, bits):
+    """The batched Qwen-shaped workload at full size: 16 sequences x 4 KV heads x 8192 Student-t keys, 7 query
+    heads per KV head, one parameter set per (sequence, head) from the sequence's own first 1024 tokens."""
+    w, L = qwen_full
+    print("entry mismatch %.2e, decode rel-L2 max %.2e" % _full_size_case(w, L, bits))
+
+
+def test_full_size_llama_long_128k():
+    """The long-context workload at full size: 131072 tokens x 8 KV heads at 1.33 bits per element (5-word
+    records, most channels at zero width)."""
+    w = synth.WORKLOADS["llama_long_128k"]
+    L = synth.make_layer(w, steps=1)
+    print("entry mismatch %.2e, decode rel-L2 max %.2e" % _full_size_case(w, L, 1.33))
+
+
+def test_prefill_stack_full_size_sampled():
+    """The 32-layer prefill workload at full size. Per layer: tokens drawn on the device (4 sequences x 8 KV
+    heads x 65536 bf16 tokens), oracle parameters calibrated on tokens 0..4095 of sequence 0, one kv_encode of
+    the whole layer (the tensor-core path), 64 sampled token pairs of every (sequence, head) against the oracle
+    encode; then one decode step over the layer's cache. On every fourth layer one (sequence, head)'s records
+    are replaced by the oracle's records of all its tokens, and that pair's decode rows are checked against the
+    oracle decode."""
+    w = synth.WORKLOADS["llama_prefill_32l"]
+    B, Hkv, Hq, T, g, d = w.B, w.Hkv, w.Hq, w.T, w.g, w.d
+    rng = np.random.default_rng(11)
+    scale = 1.0 / math.sqrt(d)
+    n_diff, n_all, worst = 0.0, 0, 0.0
+    for layer in range(w.layers):
+        Ld = synth.make_layer_device(w, layer, "cuda")
+        sets = G.calibrate_oracle(Ld, 2.75, 2.75)
+        P = G.lib_params(sets)
+        Rk, Rv = P.record_words(0), P.record_words(1)
+        rk = torch.zeros((B, Hkv, T, Rk), dtype=torch.int32, device="cuda")
+        rv = torch.zeros(G.value_cache_shape(B, Hkv, T, Rv), dtype=torch.int32, device="cuda")
+        cache = kvtc.make_cache(rk, rv, B, Hkv, T, False)
+        kvtc.kv_encode(P, cache, Ld.k, Ld.v, kvtc.KV_DTYPE_BF16, B, T, torch.zeros(B, dtype=torch.int64,
+                                                                                      device="cuda"))
+        assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
+        for b in range(B):
+            for h in range(Hkv):
+                pk, pv = sets[h]
+                pairs = np.sort(rng.choice(T // 2, 64, replace=False))
+                toks = np.stack([2 * pairs, 2 * pairs + 1], 1).reshape(-1)
+                ti, pi = torch.from_numpy(toks).cuda(), torch.from_numpy(pairs).cuda()
+                kx = Ld.k[b, h, ti].double().cpu().numpy()
+                vx = Ld.v[b, h, ti].double().cpu().numpy()
+                for got, x, p in ((G.u32(rk[b, h, ti]), kx, pk), (G.u32(rv[b, h, pi]), vx, pv)):
+                    tf, dz, ds, cf, dc, ef = G.token_diff(O.unpack(got, p), O.unpack(O.encode(x, p), p), p)
+                    assert dc <= 1 and dz <= 1 and ds <= 1, (layer, b, h, dz, ds, dc)
+                    n = len(toks) * (int(np.count_nonzero(p.widths)) + 2)
+                    n_diff += ef * n
+                    n_all += n
+        check = layer % 4 == 0
+        if check:
+            bc, hc = int(rng.integers(B)), int(rng.integers(Hkv))
+            pk, pv = sets[hc]
+            ork = O.encode(Ld.k[bc, hc].double().cpu().numpy(), pk)
+            orv = O.encode(Ld.v[bc, hc].double().cpu().numpy(), pv)
+            rk[bc, hc] = G.dev_u32(ork)
+            rv[bc, hc] = G.dev_u32(orv)
+        q = G.to_dev_storage(Ld.q[0])
+        sl = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
+        ws = torch.empty(kvtc.kv_decode_workspace_bytes(P, B, Hkv, Hq, T), dtype=torch.uint8, device="cuda")
+        kvtc.kv_attend_decode(P, cache, q, B, Hq, sl, scale, out, ws)
+        assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
+        o = out.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(o))
+        if check:
+            qf = synth.as_float(Ld.q[0])
+            ref = O.attend_decode(qf[bc, hc * g:(hc + 1) * g], ork, orv, pk, pv, T, scale)
+            err = G.rel_l2_rows(o[bc, hc * g:(hc + 1) * g], ref)
+            assert err.max() <= DEC_TOL, (layer, bc, hc, err)
+            worst = max(worst, float(err.max()))
+        del Ld, rk, rv, cache
+    assert n_diff / n_all <= 1e-4, (n_diff / n_all, round(n_diff), n_all)
+    print("sampled entry mismatch %.2e, decode rel-L2 max %.2e" % (n_diff / n_all, worst))

@@ -549,16 +549,10 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&pE[pw]));
       ++hand;
-      // accumulator columns 2tig, 2tig+1 are head tig (+4 nb)
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        if (__any_sync(0xffffffffu, corr[nb] != 1.f)) {
-#pragma unroll
-          for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] *= corr[nb];
-        }
-      }
+      // accumulator columns 2tig, 2tig+1 are head tig (+4 nb). Each tile's products are summed by the MMA from
+      // zero and folded into the running sums by round-to-nearest FMAs (acc = acc * corr + tile): accumulating
+      // inside the MMA across tiles biases the sums of these positive terms by about 2^-23 per tile, which the
+      // near-cancellation of Z and A in the output can magnify a hundredfold.
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb) {
         if (mb < nmb) {
@@ -572,7 +566,12 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
             af[3] = unpack_pair(ldsw(st, va[mb][1] + vstep), vsh[mb][1], vm[mb][1]);
           }
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_f16(acc_o[mb][nb], af, bp[nb][0], bp[nb][1]);
+          for (int nb = 0; nb < NB; ++nb) {
+            float tile[4];
+            mma_f16_zero(tile, af, bp[nb][0], bp[nb][1]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] = fmaf(acc_o[mb][nb][e], corr[nb], tile[e]);
+          }
         }
       }
       if constexpr (NB != 1) {

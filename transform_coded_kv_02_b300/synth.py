@@ -224,3 +224,73 @@ def as_float(x: np.ndarray) -> np.ndarray:
     if x.dtype == np.uint16:
         return bf16_bits_to_f32(x).astype(np.float64)
     return np.asarray(x, dtype=np.float64)
+
+
+def torch_seed(seed: int, layer: int, seq: int, head: int, stream: int) -> int:
+    """A 63-bit seed for torch's generator, derived from the same stream key as rng_for."""
+    s = np.random.SeedSequence([seed, layer, seq, head, stream]).generate_state(1, np.uint64)[0]
+    return int(s) & ((1 << 63) - 1)
+
+
+@dataclasses.dataclass
+class DeviceLayerData:
+    """One layer drawn on a torch device. k, v: bf16 device tensors [B, Hkv, T, d]; q: bf16 bits [1, B, Hq, d]
+    (host); calibration sets as in LayerData (host fp32, the stored values)."""
+    k: object
+    v: object
+    q: np.ndarray
+    calib_k: list
+    calib_v: list
+    calib_q: list
+    per_seq_params: bool
+
+
+def make_layer_device(w: Workload, layer: int, device, T: int | None = None,
+                      B: int | None = None) -> DeviceLayerData:
+    """Workload `w`'s recipe with the token streams drawn by torch's generator on `device`, for layers too
+    large to draw on the host (the prefill stack: 4 x 8 x 65536 tokens per layer, 32 layers). The bases,
+    outlier channels, spectra and queries are the host recipe's; the Gaussian latents of keys and values come
+    from torch (one generator per stream, seeded by torch_seed) and are mixed in fp32, the rotary angles are
+    taken in fp64 on the host. One parameter set per KV head, calibrated on tokens 0 .. n_calib - 1 of
+    sequence 0 (the prefix shared by the batch). Gaussian keys only."""
+    import torch
+
+    if w.key_dist != "gauss" or w.calib != "own_prefix":
+        raise ValueError("device draws cover Gaussian keys with a shared calibration prefix")
+    T = w.T if T is None else T
+    B = w.B if B is None else B
+    d, g = w.d, w.g
+    k = torch.empty((B, w.Hkv, T, d), dtype=torch.bfloat16, device=device)
+    v = torch.empty((B, w.Hkv, T, d), dtype=torch.bfloat16, device=device)
+    q = np.empty((1, B, w.Hq, d))
+    if w.rope:
+        half = d // 2
+        inv = 500000.0 ** (-np.arange(half, dtype=np.float64) * 2.0 / d)
+        ang = np.arange(T, dtype=np.float64)[:, None] * inv[None, :]
+        cos = torch.from_numpy(np.cos(ang).astype(np.float32)).to(device)
+        sin = torch.from_numpy(np.sin(ang).astype(np.float32)).to(device)
+    ck, cv, cq = [], [], []
+    for h in range(w.Hkv):
+        hd = HeadDist(w.seed, layer, 0, h, d, g, w.key_dist)
+        spec = torch.from_numpy(hd.sqrt_spec.astype(np.float32)).to(device)
+        kb = torch.from_numpy(hd.k_basis.T.astype(np.float32)).to(device)
+        vb = torch.from_numpy(hd.v_basis.T.astype(np.float32)).to(device)
+        ks = torch.from_numpy(hd.k_scale.astype(np.float32)).to(device)
+        for b in range(B):
+            gen = torch.Generator(device=device)
+            gen.manual_seed(torch_seed(w.seed, layer, b, h, _S_KTOK))
+            x = (torch.randn((T, d), generator=gen, device=device) * spec) @ kb * ks
+            if w.rope:
+                a, c = x[:, :d // 2], x[:, d // 2:]
+                x = torch.cat([a * cos - c * sin, a * sin + c * cos], dim=1)
+            k[b, h] = x.to(torch.bfloat16)
+            gen.manual_seed(torch_seed(w.seed, layer, b, h, _S_VTOK))
+            v[b, h] = ((torch.randn((T, d), generator=gen, device=device) * spec) @ vb).to(torch.bfloat16)
+            qq = hd.queries(1, rng_for(w.seed, layer, b, h, _S_QTOK))  # [g, 1, d]
+            q[0, b, h * g:(h + 1) * g] = qq[:, 0]
+        n = min(w.n_calib, T)
+        ck.append(k[0, h, :n].float().cpu().numpy())
+        cv.append(v[0, h, :n].float().cpu().numpy())
+        cq.append(np.asarray(hd.queries(n, rng_for(w.seed, layer, 0, h, _S_QCAL)).reshape(-1, d), np.float32))
+    return DeviceLayerData(k=k, v=v, q=round_to(q, "bf16"), calib_k=ck, calib_v=cv, calib_q=cq,
+                           per_seq_params=False)
