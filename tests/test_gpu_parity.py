@@ -388,6 +388,23 @@ def test_decode_llama_shape_all_key_blocks(seq_len):
     assert err.max() <= DEC_TOL, (seq_len, err)
 
 
+@pytest.mark.parametrize("wl,bits", [("llama_decode_32k", 8.0), ("qwen_batched_8k", 6.0)])
+def test_decode_runtime_record_length(wl, bits):
+    """Record lengths without a compile-time kernel (32 words at 8 bits per element, 24 at 6) run the decode with
+    run-time record strides: one column block and the pipelined key loop on the Llama shape, two column blocks
+    on the Qwen shape, ragged lengths. The wide codes also give the smallest q' entries (sigma_j 2^-b_j near
+    1e-6), which the per-head power-of-two scaling of q' keeps out of the fp16 subnormal range."""
+    w = synth.WORKLOADS[wl]
+    L = synth.make_layer(w, T=1000, B=min(w.B, 2), steps=1)
+    sets = G.calibrate_oracle(L, bits, bits)
+    assert sets[0][0].r_words not in (5, 8, 11, 12, 16)
+    P = G.lib_params(sets)
+    seq = [1000, 777][:L.k.shape[0]]
+    err = _decode_case(L, sets, P, w.Hq, L.per_seq_params, seq, 1024)
+    print("decode rel-L2 max %.2e" % err.max())
+    assert err.max() <= DEC_TOL, err
+
+
 def test_decode_full_size_llama_32k():
     """The 32K-token Llama-shaped layer (32 q / 8 KV heads, 2.75 bits) in the bench's launch configuration:
     every output row against the oracle on the same records."""

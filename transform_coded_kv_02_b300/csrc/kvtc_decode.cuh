@@ -22,7 +22,8 @@ struct DecArgs {
   const __nv_bfloat16* q;
   const int32_t* seq_lens;
   __half* qa;       // [B*Hkv][16][128]: row 2h (+1) = fp16 hi (lo) part of q' of head h
-  float* qc;        // [B*Hkv][QP_PARTS][16]: partial C0 of heads 0..7, partial C1 of heads 0..7 (base-2 logits)
+  float* qc;        // [B*Hkv][QP_PARTS][QPC]: partial C0 of heads 0..7, partial C1 of heads 0..7 (base-2 logits),
+                    // the factor 2^-e_h that undoes the scaling of q'_h (the same in every part)
   unsigned* cnt;    // [B*Hkv] arrival counters
   float* part;      // [B*Hkv][splits][g][PSTR] split partials
   float* out;       // [B][Hq][128]
@@ -39,10 +40,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---- q preparation: QP_PARTS CTAs per (sequence, KV head), 32 rotated channels each ---------------------
+constexpr int QPC = 24;  // floats per (sequence, KV head, part) in DecArgs::qc
 // q~ = T_K q for the g query heads, read from the transposed transform (T^T row k holds T[j][k] for all j, so the
 // 32 lanes of a warp load one coalesced line per k); q'_j = a log2(e) q~_j sigma_j 2^-b_j as fp16 hi + lo;
 // partial sums per part of C0 = a log2(e) q.(T_K^T mu) and C1 = a log2(e) sum_{b_j > 0} q~_j sigma_j, which
 // the decode kernel adds up. Thread: channel j0 + (tid % 32), k slice 16 (tid / 32) .. + 16.
+// q'_h is stored times 2^e_h, e_h = 14 - ceil(log2 B_h) with B_h = |a log2(e)| ||q_h|| max_j sigma_j 2^-b_j >= max_j
+// |q'_h,j|: the largest entries then sit near 2^12..2^14, so that the fp16 hi + lo pair keeps about 22 bits for
+// every channel that matters instead of sinking into fp16 subnormals when sigma_j 2^-b_j is small; the decode
+// multiplies the logit sum by 2^-e_h. Every part computes B_h from the same inputs in the same order.
 constexpr int QP_THREADS = 256;
 constexpr int QP_PARTS = D / 32;
 
@@ -63,6 +69,17 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs 
   const float sg = tk.sigma[(size_t)set * D + j];
   const int bw = tk.widths[(size_t)set * D + j];
   const float bk = tk.base[(size_t)set * D + j];
+  float sig_step = 0.f;  // max over the nonzero-width channels of sigma_j 2^-b_j (warp 0)
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+      const int jj = 32 * i + lane;
+      const int b2 = tk.widths[(size_t)set * D + jj];
+      if (b2 > 0) sig_step = fmaxf(sig_step, tk.sigma[(size_t)set * D + jj] * exp2i(-b2));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sig_step = fmaxf(sig_step, __shfl_xor_sync(0xffffffffu, sig_step, o));
+  }
   // This kernel may start while the previous kernel of the stream (an append, say) still runs: wait for it
   // before reading q, and only then release decode_kernel, whose record copies must see every record written
   // before this call.
@@ -88,20 +105,36 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(ParamsDev P, DecArgs 
       float q_t = 0.f;
 #pragma unroll
       for (int w = 0; w < QP_THREADS / 32; ++w) q_t += red[w][h][lane];
+      float n2 = 0.f;
+      if (h < g) {  // warp-uniform
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) n2 = fmaf(qs[h][32 * i + lane], qs[h][32 * i + lane], n2);
+        n2 = warp_sum(n2);
+      }
+      const float bound = fabsf(a.scale_log2) * sqrtf(n2) * sig_step;
+      int e = 0;
+      if (bound > 0.f && bound <= 3.0e38f) {
+        int ex;
+        frexpf(bound, &ex);  // bound < 2^ex
+        e = min(max(14 - ex, -120), 120);
+      }
       const bool on = h < g && bw > 0;
-      const float qp = on ? a.scale_log2 * q_t * sg * exp2i(-bw) : 0.f;
+      const float qp = on ? a.scale_log2 * q_t * sg * exp2i(-bw) * exp2i(e) : 0.f;
       const __half hi = __float2half_rn(qp);
       const __half lo = __float2half_rn(qp - __half2float(hi));
       qa[(2 * h) * D + j] = hi;
       qa[(2 * h + 1) * D + j] = lo;
       const float c1 = warp_sum(on ? q_t * sg : 0.f);
-      if (lane == 0 && h < g) a.qc[(bh * QP_PARTS + part) * 16 + 8 + h] = a.scale_log2 * c1;
+      if (lane == 0 && h < g) {
+        a.qc[(bh * QP_PARTS + part) * QPC + 8 + h] = a.scale_log2 * c1;
+        a.qc[(bh * QP_PARTS + part) * QPC + 16 + h] = exp2i(-e);
+      }
     }
   } else if (warp == 1) {  // C0 over the query entries k = j0 .. j0 + 31 (the base vector is indexed like q)
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h) {
       const float c0 = warp_sum(h < g ? bk * qs[h][j] : 0.f);
-      if (lane == 0 && h < g) a.qc[(bh * QP_PARTS + part) * 16 + h] = a.scale_log2 * c0;
+      if (lane == 0 && h < g) a.qc[(bh * QP_PARTS + part) * QPC + h] = a.scale_log2 * c0;
     }
   }
   if (tid == 0 && part == 0) a.cnt[bh] = 0u;
@@ -283,18 +316,19 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
           qb[kb][nb][1] = kb < nkb ? qa32[(col * D + kb * 16 + 8 + 2 * tig) >> 1] : 0u;
         }
     }
-    float c0[NB], c1[NB];
+    float c0[NB], c1[NB], qsc[NB];  // qsc: 2^-e_h, undoing the scaling of q'
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       const int h = tig + 4 * nb;
       float s0 = 0.f, s1 = 0.f;
 #pragma unroll
       for (int pt = 0; pt < QP_PARTS; ++pt) {
-        s0 += h < g ? a.qc[(bh * QP_PARTS + pt) * 16 + h] : 0.f;
-        s1 += h < g ? a.qc[(bh * QP_PARTS + pt) * 16 + 8 + h] : 0.f;
+        s0 += h < g ? a.qc[(bh * QP_PARTS + pt) * QPC + h] : 0.f;
+        s1 += h < g ? a.qc[(bh * QP_PARTS + pt) * QPC + 8 + h] : 0.f;
       }
       c0[nb] = s0;
       c1[nb] = s1;
+      qsc[nb] = h < g ? a.qc[(size_t)bh * QP_PARTS * QPC + 16 + h] : 0.f;
     }
     int hand = 0;  // handoffs to the value warp so far
     if constexpr (PIPE) {
@@ -346,7 +380,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
         const float2 zsv1 = __half22float2(*reinterpret_cast<const __half2*>(&zC[3]));
         const float zk0 = zsk0.x, sk0 = zsk0.y, zk1 = zsk1.x, sk1 = zsk1.y;
         const float zv0 = zsv0.x, sv0 = zsv0.y, zv1 = zsv1.x, sv1 = zsv1.y;
-        const float r0 = accC[0] + accC[1], r1 = accC[2] + accC[3];
+        const float r0 = (accC[0] + accC[1]) * qsc[0], r1 = (accC[2] + accC[3]) * qsc[0];
         const float l0 = valid0 ? fmaf(sk0, r0, fmaf(zk0, c1[0], c0[0])) : -INFINITY;
         const float l1 = valid1 ? fmaf(sk1, r1, fmaf(zk1, c1[0], c0[0])) : -INFINITY;
         float mt = fmaxf(l0, l1);
@@ -430,8 +464,8 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
       float corr[NB];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
-        const float r0 = (acc2[0][nb][0] + acc2[1][nb][0]) + (acc2[0][nb][1] + acc2[1][nb][1]);
-        const float r1 = (acc2[0][nb][2] + acc2[1][nb][2]) + (acc2[0][nb][3] + acc2[1][nb][3]);
+        const float r0 = ((acc2[0][nb][0] + acc2[1][nb][0]) + (acc2[0][nb][1] + acc2[1][nb][1])) * qsc[nb];
+        const float r1 = ((acc2[0][nb][2] + acc2[1][nb][2]) + (acc2[0][nb][3] + acc2[1][nb][3])) * qsc[nb];
         const float l0 = valid0 ? fmaf(sk0, r0, fmaf(zk0, c1[nb], c0[nb])) : -INFINITY;
         const float l1 = valid1 ? fmaf(sk1, r1, fmaf(zk1, c1[nb], c0[nb])) : -INFINITY;
         float mt = fmaxf(l0, l1);
@@ -784,7 +818,7 @@ DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device) {
   L.off_qa = o;
   o = align256(o + bh * 16 * D * sizeof(__half));
   L.off_qc = o;
-  o = align256(o + bh * QP_PARTS * 16 * sizeof(float));
+  o = align256(o + bh * QP_PARTS * QPC * sizeof(float));
   L.off_cnt = o;
   o = align256(o + bh * sizeof(unsigned));
   L.off_part = o;
