@@ -61,12 +61,30 @@ def parse_args():
 # ------------------------------------------------------------------------------------------------------
 # workload
 # ------------------------------------------------------------------------------------------------------
-def make_workload(n_new: int):
-    """Synthetic layer with T + n_new tokens: the first T are prefilled, the rest appended one per step."""
+def make_workload(n_new: int, layer: int = 0):
+    """Synthetic layer with T + n_new tokens: the first T are prefilled, the rest appended one per step. Rank r
+    of a multi-GPU run takes layer r of the model: its own data, the same shapes."""
     from transform_coded_kv_02_b300 import synth
     w = synth.WORKLOADS[WORKLOAD]
-    L = synth.make_layer(w, T=w.T + n_new, steps=n_new)
+    L = synth.make_layer(w, layer=layer, T=w.T + n_new, steps=n_new)
     return w, L
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over the ranks (the job's time is its slowest rank's); x itself when world == 1."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: float, seconds: float, world: int) -> float:
+    """Whole-job throughput: every rank processes the same amount of work (its own layer), and the job takes
+    the slowest rank's time."""
+    return world * bytes_per_rank / seconds / 1e9
 
 
 def workload_name(w, rk_w: int, rv_w: int) -> str:
@@ -290,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     K, W = args.steps, args.warmup
     n_new = K + W
-    w, L = make_workload(n_new)
+    w, L = make_workload(n_new, layer=rank)
     B, Hkv, Hq, d, T = w.B, w.Hkv, w.Hq, w.d, w.T
     T_cap = (T + n_new + 15) // 16 * 16
     stream = torch.cuda.current_stream(dev)
@@ -392,14 +410,10 @@ def run_ours(args, rank, world, local_rank):
     t_dec = timed([[g_dec[W + j].replay] for j in range(K)])[:, 0]
     t_app = timed([[g_enc[W + j].replay] for j in range(K)])[:, 0]
     assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
-    total = float(np.sum(t_step))
-    if world > 1:
-        tt = torch.tensor([total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total = float(tt.item())
+    total = max_over_ranks(float(np.sum(t_step)), world, dev)
     ctx = [T + W + j + 1 for j in range(K)]
     bytes_steps = sum(step_bytes(c, w, rk_w, rv_w) for c in ctx)
-    value = world * bytes_steps / total / 1e9
+    value = job_gbs(bytes_steps, total, world)
     dec_bytes_avg = float(np.mean([decode_bytes(c, w, rk_w, rv_w) for c in ctx]))
     dec_avg = float(np.mean(t_dec))
     peak, peak_kind = measured_peaks()
@@ -459,7 +473,7 @@ def run_ours(args, rank, world, local_rank):
         te.append(e0.elapsed_time(e1) * 1e-3)
     assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
     e2e_bytes = float(np.mean([step_bytes(T + W + j + 1, w, rk_w, rv_w) for j in range(ne)]))
-    e2e_val = world * e2e_bytes / float(np.mean(te)) / 1e9
+    e2e_val = job_gbs(e2e_bytes, max_over_ranks(float(np.mean(te)), world, dev), world)
     h2d = (k_d.numel() + v_d.numel() + q_d.numel()) * 2
     d2h = out_h.numel() * 4
 
