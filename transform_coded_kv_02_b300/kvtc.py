@@ -104,14 +104,21 @@ def _ptr(x):
     raise TypeError(type(x))
 
 
+_torch = None  # the torch module once looked up (False when it is not installed)
+
+
 def _stream(stream):
     if stream is None:
-        try:
-            import torch
-            if torch.cuda.is_available():
-                return torch.cuda.current_stream().cuda_stream
-        except ImportError:
-            pass
+        global _torch
+        if _torch is None:
+            try:
+                import torch
+                _torch = torch
+            except ImportError:
+                _torch = False
+        # before CUDA is initialised in this process the current stream is the default stream
+        if _torch and _torch.cuda.is_initialized():
+            return _torch.cuda.current_stream().cuda_stream
         return None
     if isinstance(stream, int):
         return stream
