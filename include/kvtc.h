@@ -174,6 +174,11 @@ kv_status kv_encode(const kv_params* p, const kv_cache* cache, const void* k, co
  *   with sigma and 2^-b), and the splits are merged with their softmax weights. Kernels: a q-preparation kernel
  *   (which waits for the previous kernel of the stream, e.g. an append, before reading q) and the split-K
  *   decode kernel, launched as its programmatic dependant.
+ *   Arithmetic: codes enter fp16 tensor-core MMAs exactly (c + 1/2); q' (scaled per head by a power of two so
+ *   that it stays clear of fp16 subnormals) is carried as an fp16 hi + lo pair, p s_V likewise; each 16-token
+ *   product sum starts from zero and the running sums are kept in fp32 with round-to-nearest arithmetic; the
+ *   softmax runs in base 2 on the hardware exponential. Result: within 2e-3 relative L2 of the exact decode
+ *   of the same records (measured 1e-5 to 2e-5 on the workloads' full-size layers).
  *   workspace: device, at least kv_decode_workspace_bytes(...) bytes, 16-byte aligned, reused across
  *   calls (no initialisation needed); calls that share a workspace must not overlap on the device. */
 size_t kv_decode_workspace_bytes(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap);
