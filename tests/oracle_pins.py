@@ -510,6 +510,21 @@ def pin_decode_brute_force():
         assert np.allclose(o, ref, rtol=1e-11, atol=1e-11), T
 
 
+def pin_storage_order():
+    """Storage order sorts channels by width (descending), then importance (descending), then eigen-index. The
+    value channels of a calibrated set lose no bits to the record layout here, so along storage order their
+    widths do not increase, and within each run of equal widths their importances (the variances) do not
+    increase either."""
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    for bits in (1.33, 2.75, 4.0):
+        pk, pv = O.calibrate(L.calib_k[0], L.calib_v[0], L.calib_q[0], bits, bits)
+        w = np.asarray(pv.widths)
+        lam = np.asarray(pv.importance, np.float64)
+        assert np.all(np.diff(w) <= 0), bits
+        same = np.diff(w) == 0
+        assert same.sum() > 10 and np.all(np.diff(lam)[same] <= 0), bits
+
+
 def pin_calibrate_structure():
     """Calibrated sets: orthogonal T; both channels of a pair share one width; the widths fit the record's
     pair layout and use at most the budget and at least all but one code word of it; mu = T mu_raw,

@@ -9,7 +9,7 @@ from oracle import kvtc_oracle as O
 _orig = {name: getattr(O, name) for name in
          ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
           "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat",
-          "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout"]}
+          "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout", "storage_order", "attend_decode"]}
 
 
 def _klt_transposed(sigma):
@@ -206,6 +206,18 @@ def _token_pack_swapped_halves(z16, s16, codes, p):
     return out
 
 
+def _storage_ties_ascending(widths, lam):
+    return sorted(range(len(widths)), key=lambda i: (-int(widths[i]), float(lam[i]), i))
+
+
+def _attend_ignores_length(q, rec_k, rec_v, pk, pv, seq_len, scale):
+    return _orig["attend_decode"](q, rec_k, rec_v, pk, pv, len(rec_k), scale)
+
+
+def _attend_one_token_short(q, rec_k, rec_v, pk, pv, seq_len, scale):
+    return _orig["attend_decode"](q, rec_k, rec_v, pk, pv, max(1, seq_len - 1), scale)
+
+
 MUTATIONS = [
     ("klt", _klt_transposed, P.pin_klt_known_spectrum),
     ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
@@ -229,6 +241,9 @@ MUTATIONS = [
     ("token_slot_layout", _token_layout_next_fit, P.pin_token_layout_fit_golden),
     ("fit_token_layout", _token_fit_ties_to_earlier, P.pin_token_layout_fit_golden),
     ("pack", _token_pack_swapped_halves, P.pin_token_pack_golden),
+    ("storage_order", _storage_ties_ascending, P.pin_storage_order),
+    ("attend_decode", _attend_ignores_length, P.pin_decode_brute_force),
+    ("attend_decode", _attend_one_token_short, P.pin_decode_brute_force),
 ]
 
 

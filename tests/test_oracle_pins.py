@@ -94,3 +94,7 @@ def test_decode_brute_force():
 
 def test_calibrate_structure():
     P.pin_calibrate_structure()
+
+
+def test_storage_order():
+    P.pin_storage_order()
