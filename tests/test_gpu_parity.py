@@ -3,6 +3,7 @@
 Bars: quantise+pack and unpack bit-exact given the same fp32 rotated input; end-to-end codes differ by at most
 1 LSB on at most 1e-4 of entries (rounding ties of the rotation); decode within 2e-3 relative L2 of the oracle
 run on the same records."""
+import dataclasses
 import math
 
 import numpy as np
@@ -402,6 +403,58 @@ def test_decode_runtime_record_length(wl, bits):
     seq = [1000, 777][:L.k.shape[0]]
     err = _decode_case(L, sets, P, w.Hq, L.per_seq_params, seq, 1024)
     print("decode rel-L2 max %.2e" % err.max())
+    assert err.max() <= DEC_TOL, err
+
+
+def test_encode_zero_tokens_is_a_no_op(tiny):
+    """t_new = 0 returns at once, before any pointer is looked at, and writes nothing."""
+    w, L, sets, P = tiny
+    rk = torch.full((1, 1, 64, P.record_words(0)), 7, dtype=torch.int32, device="cuda")
+    rv = torch.full(G.value_cache_shape(1, 1, 64, P.record_words(1)), 7, dtype=torch.int32, device="cuda")
+    cache = kvtc.make_cache(rk, rv, 1, 1, 64, False)
+    kvtc.kv_encode(P, cache, None, None, kvtc.KV_DTYPE_F32, 1, 0, None)
+    assert kvtc.kv_check_status() == kvtc.KV_OK
+    assert bool(torch.all(rk == 7)) and bool(torch.all(rv == 7))
+
+
+def test_decode_empty_sequence_gives_zeros():
+    """A batch whose first sequence is empty (seq_len 0): its rows are zeros, as the header states; the other
+    sequence's rows match the oracle."""
+    w = synth.WORKLOADS["qwen_batched_8k"]
+    L = synth.make_layer(w, T=300, B=2, steps=1)
+    sets = G.calibrate_oracle(L, 3.0, 3.0)
+    P = G.lib_params(sets)
+    rk, rv = G.oracle_cache(synth.as_float(L.k), synth.as_float(L.v), sets, True, 320)
+    got = G.run_decode(P, rk, rv, L.q[0], [0, 300], w.Hq, True)
+    assert np.all(got[0] == 0)
+    ref = G.oracle_decode(rk[1:2], rv[1:2], L.q[0][1:2], [300], sets[w.Hkv:], w.Hq, True)
+    assert G.rel_l2_rows(got[1:2], ref).max() <= DEC_TOL
+
+
+def test_all_channels_at_zero_width():
+    """The degenerate budget: 1-word records (0.25 bits per element) leave no code bits, so every channel has
+    width 0. The tensor-core encode writes all-zero records like the oracle, and the decode returns the mean
+    value T_V^T mu_V for every head (every key reconstructs to the same mean, so the softmax is uniform)."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    L = synth.make_layer(w, T=300, steps=1)
+    sets = G.calibrate_oracle(L, 0.25, 0.25)
+    assert all(s[0].r_words == 1 and not s[0].widths.any() and not s[1].widths.any() for s in sets)
+    P = G.lib_params(sets)
+    rk, rv = _encode_gpu(P, L.k, L.v, False, T_cap=320)
+    assert not rk.any() and not rv.any()
+    ork, orv = G.oracle_cache(synth.as_float(L.k), synth.as_float(L.v), sets, False, 320)
+    got = G.run_decode(P, ork, orv, L.q[0], [300], w.Hq, False)
+    ref = G.oracle_decode(ork, orv, L.q[0], [300], sets, w.Hq, False)
+    assert G.rel_l2_rows(got, ref).max() <= DEC_TOL
+
+
+def test_decode_largest_group():
+    """g = 8 query heads per KV head, the library's largest group (two full column blocks)."""
+    w = dataclasses.replace(synth.WORKLOADS["llama_decode_32k"], Hq=64)
+    L = synth.make_layer(w, T=700, steps=1)
+    sets = G.calibrate_oracle(L, 2.75, 2.75)
+    P = G.lib_params(sets)
+    err = _decode_case(L, sets, P, w.Hq, False, [700], 704)
     assert err.max() <= DEC_TOL, err
 
 
