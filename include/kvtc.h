@@ -84,12 +84,23 @@ typedef struct {
   float bits_v;   /* same for values                                                                */
   int max_bits;   /* largest channel width, 1..8 (8)                                                 */
   int n_threads;  /* host threads for calibration; 0 = all hardware threads                         */
+  int joint;      /* 0: keys and values each get their own budget (R_wK from bits_k, R_wV from bits_v).
+                   * 1: the table keeps R_wK + R_wV words per token but splits them between keys and values
+                   *    jointly (see kv_calibrate)                                                      */
 } kv_calib_opts;
 
 /* Calibrate n_sets sets: fp64 mean/covariance of K and V, query second moment M_Q, Jacobi
  * eigendecomposition (eigenvalues descending, largest-|.| component of each eigenvector positive),
  * importances lambda_K = sigma^2 * (u^T M_Q u), lambda_V = sigma^2, reverse water-filling to
  * C = 32*R_w - 32 code bits with R_w = floor(bits*d/32), storage order (width desc, lambda desc, index asc).
+ * joint = 1 (one rate trade-off between keys and values, [AATC] Key points, first bullet: the attention-aware
+ * distortion is a sum of a key and a value part): to first order the output error is
+ * sum_t p_t^2 (alpha^2 |v_t - o|^2 sum_i w_i D^K_i + sum_i D^V_i), so with |v_t - o|^2 taken at tr(Sigma_V) and
+ * alpha = 1/sqrt(d) the key importances weigh rho = tr(Sigma_V)/d against the value importances. The split
+ * R_wK of the table's R_wK + R_wV record words minimises sum over sets of rho sum_i lambda_K,i 4^-b_i +
+ * sum_j lambda_V,j 4^-b_j (each tensor water-filled at its own budget); objectives within a relative 1e-9 tie,
+ * ties go to the split nearest the separate one, then to fewer key words. The record lengths then differ
+ * between keys and values (kv_params_record_words).
  * The result lives on the host; call kv_params_upload before encoding or decoding.
  * Errors: KV_ERR_INVALID_ARG (null, n_tok < 2, n_q < 1), KV_ERR_UNSUPPORTED (d), KV_ERR_BUDGET,
  * KV_ERR_NUMERIC (non-finite input). */

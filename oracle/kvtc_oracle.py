@@ -343,6 +343,61 @@ def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8):
 
 
 # ----------------------------------------------------------------------------------------------------
+# 5b. joint key/value allocation (one rate trade-off between the two tensors)
+# ----------------------------------------------------------------------------------------------------
+def exchange_rate(lam_v, d: int) -> float:
+    """Weight of key distortion against value distortion in the attention output. To first order a key error
+    e_t moves logit t by alpha q.e_t and the output by p_t alpha (q.e_t)(v_t - o); with white noise of
+    variances D^K_i (key basis) and D^V_i (value basis), independent across tokens,
+        E|do|^2 = sum_t p_t^2 (alpha^2 |v_t - o|^2 sum_i w_i D^K_i + sum_i D^V_i),
+    additive in keys and values and factored over tokens and channels ([AATC] Key points, first bullet).
+    Taking |v_t - o|^2 at its mean over tokens, tr(Sigma_V), with alpha = 1/sqrt(d) (the softmax scale the
+    decode uses by default): rho = tr(Sigma_V) / d multiplies the key importances sigma_i^2 w_i."""
+    return float(np.sum(np.maximum(np.asarray(lam_v, F64), 0.0))) / d
+
+
+def joint_objective(imp_k, imp_v, rho: float, rwk: int, rwv: int, max_bits: int) -> float:
+    """sum_i rho imp_k,i 4^-b_i + sum_j imp_v,j 4^-b_j with each tensor's integer water-filling at its own
+    budget (the white-noise distortion of a b-bit channel is proportional to sigma^2 4^-b)."""
+    bk = water_fill_integer(imp_k, code_bits(rwk), max_bits)
+    bv = water_fill_integer(imp_v, code_bits(rwv), max_bits)
+    return float(rho * np.sum(np.asarray(imp_k, F64) * 4.0 ** -bk.astype(F64)) +
+                 np.sum(np.asarray(imp_v, F64) * 4.0 ** -bv.astype(F64)))
+
+
+def joint_split(per_set, r_total: int, rwk_sep: int, max_bits: int, d: int) -> int:
+    """Key record words R_wK (values get r_total - R_wK) minimising the sum over the parameter sets of
+    joint_objective; per_set holds (imp_k, imp_v, rho) of each set. Candidates keep both tensors within
+    1 .. 1 + max_bits d / 32 words. Objectives within a relative 1e-9 of the minimum tie; ties go to the split
+    nearest rwk_sep (the separate allocation's), then to fewer key words."""
+    cands = [r for r in range(1, r_total) if code_bits(r) <= max_bits * d and code_bits(r_total - r) <= max_bits * d]
+    J = {r: sum(joint_objective(ik, iv, rho, r, r_total - r, max_bits) for ik, iv, rho in per_set) for r in cands}
+    jmin = min(J.values())
+    ties = [r for r in cands if J[r] <= jmin * (1.0 + 1e-9)]
+    return min(ties, key=lambda r: (abs(r - rwk_sep), r))
+
+
+def calibrate_joint(sets, bits_k: float, bits_v: float, max_bits: int = 8):
+    """Calibration of a table of sets [(k, v, q), ...] with the key/value split of the record chosen jointly:
+    the table keeps R_wK + R_wV = record_words(bits_k) + record_words(bits_v) words per token, split as
+    joint_split decides (one split for the table, since the cache holds one record length per tensor); each
+    tensor is then allocated and laid out as in calibrate. Returns [(TensorParams K, TensorParams V), ...]."""
+    d = np.asarray(sets[0][0]).shape[1]
+    prep = []
+    for k, v, q in sets:
+        mu_k, s_k, mu_v, s_v, m_q = calib_statistics(k, v, q)
+        lam_k, u_k = klt(s_k)
+        lam_v, u_v = klt(s_v)
+        prep.append((mu_k, lam_k, u_k, key_importance(lam_k, u_k, m_q), mu_v, lam_v, u_v, value_importance(lam_v),
+                     exchange_rate(lam_v, d)))
+    rwk_sep, rwv_sep = record_words(bits_k, d), record_words(bits_v, d)
+    rwk = joint_split([(p[3], p[7], p[8]) for p in prep], rwk_sep + rwv_sep, rwk_sep, max_bits, d)
+    rwv = rwk_sep + rwv_sep - rwk
+    return [(build_tensor_params(p[0], p[1], p[2], p[3], rwk, max_bits, "channels"),
+             build_tensor_params(p[4], p[5], p[6], p[7], rwv, max_bits, "tokens")) for p in prep]
+
+
+# ----------------------------------------------------------------------------------------------------
 # 6. quantiser (fp32, fixed op order)
 # ----------------------------------------------------------------------------------------------------
 def half_rn_sat(x):

@@ -161,6 +161,72 @@ def pin_additive_key_value_distortion():
     assert abs(diff.mean()) <= 4 * diff.std() / math.sqrt(trials) + 1e-3 * both.mean()
 
 
+def pin_exchange_rate_monte_carlo():
+    """The weight of key against value distortion in the joint allocation. Many tokens, values independent of
+    the attention weights, small white key noise in the key basis: the output error energy through exact
+    attention, divided by sum_t p_t^2 sum_i w_i D_i (w_i = (u_i.q)^2 for the query used), equals
+    rho = alpha^2 tr(Sigma_V) with alpha = 1/sqrt(d) to within the model's approximation (|v_t - o|^2 averages
+    to tr(Sigma_V) + |mu_V - o|^2, a few per cent here)."""
+    rng = np.random.default_rng(14)
+    d, n = 128, 512
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=n, steps=1)
+    k = synth.as_float(L.k[0, 0])
+    v_basis = synth.random_orthogonal(d, rng)
+    lam_v = 0.9 ** np.arange(d)
+    v = (rng.standard_normal((n, d)) * np.sqrt(lam_v)) @ v_basis.T
+    q = synth.as_float(L.q[0, 0])[:1]
+    _, s_k, _, _, _ = O.calib_statistics(k, v, q)
+    _, u = O.klt(s_k)
+    scale = 1.0 / math.sqrt(d)
+    o = O.attention(q, k, v, scale)
+    logits = scale * (q @ k.T)[0]
+    p = np.exp(logits - logits.max())
+    p /= p.sum()
+    D = 1e-8 * (1.0 + (np.arange(d) % 3))
+    w = (u.T @ q[0]) ** 2
+    trials = 3000
+    x = np.empty(trials)
+    for i in range(trials):
+        e = (rng.standard_normal((n, d)) * np.sqrt(D)) @ u.T
+        x[i] = np.sum((O.attention(q, k + e, v, scale) - o) ** 2)
+    measured = x.mean() / (np.sum(p ** 2) * float(w @ D))
+    rho = O.exchange_rate(lam_v, d)
+    assert abs(measured / rho - 1) < 0.15, (measured, rho)
+
+
+def pin_joint_split_by_enumeration():
+    """The joint split against an enumeration written here: every word split of the record, each tensor at
+    its own integer water-filling, the summed weighted white-noise distortion rho sum lambda_K 4^-b +
+    sum lambda_V 4^-b; the chosen split attains the minimum. Limits: keys weighted a million times heavier
+    take every word they can use, a million times lighter the fewest; equal importances and weights keep the
+    even split (the tie rule)."""
+    L = synth.make_layer(synth.WORKLOADS["llama_decode_32k"], T=16, steps=1)
+    per_set = []
+    for ck, cv, cq in list(zip(L.calib_k, L.calib_v, L.calib_q))[:3]:
+        _, s_k, _, s_v, m_q = O.calib_statistics(ck, cv, cq)
+        lk, uk = O.klt(s_k)
+        lv, _ = O.klt(s_v)
+        per_set.append((O.key_importance(lk, uk, m_q), O.value_importance(lv), O.exchange_rate(lv, 128)))
+    r_total = 22
+
+    def total(r):
+        acc = 0.0
+        for ik, iv, rho in per_set:
+            bk = O.water_fill_integer(ik, 32 * r - 32, 8)
+            bv = O.water_fill_integer(iv, 32 * (r_total - r) - 32, 8)
+            acc += rho * float(np.sum(ik * 0.25 ** bk)) + float(np.sum(iv * 0.25 ** bv))
+        return acc
+
+    costs = {r: total(r) for r in range(1, r_total)}
+    chosen = O.joint_split(per_set, r_total, 11, 8, 128)
+    assert costs[chosen] <= min(costs.values()) * (1 + 1e-9)
+    heavy = O.joint_split([(ik, iv, rho * 1e6) for ik, iv, rho in per_set], r_total, 11, 8, 128)
+    light = O.joint_split([(ik, iv, rho * 1e-6) for ik, iv, rho in per_set], r_total, 11, 8, 128)
+    assert heavy > 11 and light < 11 and heavy > light
+    same = O.joint_split([(iv, iv, 1.0) for _, iv, _ in per_set], r_total, 11, 8, 128)
+    assert same == 11
+
+
 # --- water-filling -----------------------------------------------------------------------------------
 def pin_water_fill_golden():
     for lam, C, bmax, b_real, b_int in read_golden("water_fill_small.txt"):

@@ -458,6 +458,20 @@ def test_decode_largest_group():
     assert err.max() <= DEC_TOL, err
 
 
+def test_joint_split_unequal_record_lengths():
+    """The joint key/value split gives the Llama-shaped layer 14 key and 8 value words per token: the
+    tensor-core encode and the decode with different record lengths for the two tensors, against the oracle."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    L = synth.make_layer(w, T=500, steps=1)
+    sets = O.calibrate_joint(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75)
+    assert (sets[0][0].r_words, sets[0][1].r_words) == (14, 8)
+    P = G.lib_params(sets)
+    rk, rv = _encode_gpu(P, L.k, L.v, False, T_cap=512)
+    _check_tokens(rk, rv, synth.as_float(L.k), synth.as_float(L.v), sets, False, 0, 500)
+    err = _decode_case(L, sets, P, w.Hq, False, [500], 512)
+    assert err.max() <= DEC_TOL, err
+
+
 def test_decode_full_size_llama_32k():
     """The 32K-token Llama-shaped layer (32 q / 8 KV heads, 2.75 bits) in the bench's launch configuration:
     every output row against the oracle on the same records."""

@@ -1,0 +1,35 @@
+"""The joint key/value split of the record, measured with the oracle: at the same bytes per token, on the
+Llama-shaped layer (outlier key channels, rotary keys) it moves record words to the keys and lowers the
+decode's error against exact attention on the unquantised tokens."""
+import numpy as np
+
+from oracle import kvtc_oracle as O
+from transform_coded_kv_02_b300 import synth
+
+
+def _decode_error(L, sets, w, T, steps):
+    k, v = synth.as_float(L.k), synth.as_float(L.v)
+    num = den = 0.0
+    for h in range(w.Hkv):
+        pk, pv = sets[h]
+        rk, rv = O.encode(k[0, h], pk), O.encode(v[0, h], pv)
+        for s in range(steps):
+            q = synth.as_float(L.q[s, 0, h * w.g:(h + 1) * w.g])
+            o = O.attend_decode(q, rk, rv, pk, pv, T, 1 / np.sqrt(w.d))
+            ex = O.attention(q, k[0, h], v[0, h], 1 / np.sqrt(w.d))
+            num += np.sum((o - ex) ** 2)
+            den += np.sum(ex ** 2)
+    return float(np.sqrt(num / den))
+
+
+def test_joint_split_lowers_attention_error_llama_shape():
+    w = synth.WORKLOADS["llama_decode_32k"]
+    T, steps = 1024, 4
+    L = synth.make_layer(w, T=T, steps=steps)
+    sets_in = list(zip(L.calib_k, L.calib_v, L.calib_q))
+    sep = [O.calibrate(k, v, q, 2.75, 2.75) for k, v, q in sets_in]
+    jnt = O.calibrate_joint(sets_in, 2.75, 2.75)
+    assert (jnt[0][0].r_words, jnt[0][1].r_words) == (14, 8)       # same 22 words per token, keys get more
+    e_sep, e_jnt = _decode_error(L, sep, w, T, steps), _decode_error(L, jnt, w, T, steps)
+    print("relative L2 error against exact attention: separate %.4f, joint %.4f" % (e_sep, e_jnt))
+    assert e_jnt < 0.9 * e_sep

@@ -83,6 +83,34 @@ def test_host_calibration_matches_oracle(name):
                 assert np.allclose(info["importance"], po.importance, rtol=1e-8)
 
 
+@pytest.mark.parametrize("name,bits", [("llama_decode_32k", 2.75), ("llama_long_128k", 1.33), ("qwen_batched_8k", 3.0)])
+def test_host_joint_calibration_matches_oracle(name, bits):
+    """The joint key/value split: the library picks the oracle's split for the table, then allocates and lays
+    out each tensor as the oracle does."""
+    w = synth.WORKLOADS[name]
+    # sequences calibrated on their own prefix need more tokens than channels for a full-rank covariance
+    # (unique eigenvectors)
+    L = synth.make_layer(w, T=256, B=2 if w.calib == "own_prefix" else 1, steps=1)
+    sets = list(zip(L.calib_k, L.calib_v, L.calib_q))
+    P = kvtc.kv_calibrate(sets, bits, bits, joint=True)
+    ref = O.calibrate_joint(sets, bits, bits)
+    assert P.record_words(0) + P.record_words(1) == 2 * O.record_words(bits, 128)
+    for s, (pk, pv) in enumerate(ref):
+        for t, po in ((0, pk), (1, pv)):
+            info = P.info(s, t)
+            assert info["r_words"] == po.r_words
+            assert np.array_equal(info["widths"], po.widths)
+            assert np.max(np.abs(info["T"].astype(np.float64) - po.T.astype(np.float64))) < 1e-5
+
+
+def test_joint_flag_is_checked():
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    sets = list(zip(L.calib_k, L.calib_v, L.calib_q))
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_calibrate(sets, 2.75, 2.75, joint=2)
+    assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+
+
 def test_params_save_load_roundtrip(tmp_path):
     L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
     P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75)

@@ -9,7 +9,8 @@ from oracle import kvtc_oracle as O
 _orig = {name: getattr(O, name) for name in
          ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
           "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat",
-          "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout", "storage_order", "attend_decode"]}
+          "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout", "storage_order", "attend_decode",
+          "exchange_rate", "joint_split"]}
 
 
 def _klt_transposed(sigma):
@@ -218,6 +219,14 @@ def _attend_one_token_short(q, rec_k, rec_v, pk, pv, seq_len, scale):
     return _orig["attend_decode"](q, rec_k, rec_v, pk, pv, max(1, seq_len - 1), scale)
 
 
+def _rate_alpha_not_squared(lam_v, d):
+    return float(np.sum(np.maximum(np.asarray(lam_v, np.float64), 0.0))) / np.sqrt(d)
+
+
+def _split_ignores_rho(per_set, r_total, rwk_sep, max_bits, d):
+    return _orig["joint_split"]([(ik, iv, 1.0) for ik, iv, _ in per_set], r_total, rwk_sep, max_bits, d)
+
+
 MUTATIONS = [
     ("klt", _klt_transposed, P.pin_klt_known_spectrum),
     ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
@@ -244,6 +253,8 @@ MUTATIONS = [
     ("storage_order", _storage_ties_ascending, P.pin_storage_order),
     ("attend_decode", _attend_ignores_length, P.pin_decode_brute_force),
     ("attend_decode", _attend_one_token_short, P.pin_decode_brute_force),
+    ("exchange_rate", _rate_alpha_not_squared, P.pin_exchange_rate_monte_carlo),
+    ("joint_split", _split_ignores_rho, P.pin_joint_split_by_enumeration),
 ]
 
 

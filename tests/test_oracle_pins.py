@@ -98,3 +98,11 @@ def test_calibrate_structure():
 
 def test_storage_order():
     P.pin_storage_order()
+
+
+def test_exchange_rate_monte_carlo():
+    P.pin_exchange_rate_monte_carlo()
+
+
+def test_joint_split_by_enumeration():
+    P.pin_joint_split_by_enumeration()

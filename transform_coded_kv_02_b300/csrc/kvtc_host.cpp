@@ -365,7 +365,13 @@ static void build_tensor(const std::vector<double>& mu_raw, const std::vector<do
   }
 }
 
-static void calibrate_one(const kv_calib_set& s, const kv_calib_opts& o, SetResult& r) {
+// Statistics, transforms and importances of one set (everything before the record budget is applied).
+struct SetPrep {
+  std::vector<double> mk, lk, uk, ik, mv, lv, uv, iv;
+  double rho = 0.0;  // weight of key against value distortion (joint allocation)
+};
+
+static void prepare_one(const kv_calib_set& s, const kv_calib_opts& o, SetPrep& P, SetResult& r) {
   const int d = o.d;
   if (!finite_all(s.k, (size_t)s.n_tok * d) || !finite_all(s.v, (size_t)s.n_tok * d) ||
       !finite_all(s.q, (size_t)s.n_q * d)) {
@@ -373,15 +379,21 @@ static void calibrate_one(const kv_calib_set& s, const kv_calib_opts& o, SetResu
     r.err = "non-finite calibration data";
     return;
   }
-  std::vector<double> mk, ck, mv, cv, mq, cq;
+  std::vector<double> ck, cv, mq, cq;
+  std::vector<double>&mk = P.mk, &mv = P.mv, &lk = P.lk, &lv = P.lv, &uk = P.uk, &uv = P.uv, &ik = P.ik, &iv = P.iv;
   moments(s.k, s.n_tok, d, true, mk, ck);
   moments(s.v, s.n_tok, d, true, mv, cv);
   moments(s.q, s.n_q, d, false, mq, cq);
-  std::vector<double> lk(d), uk((size_t)d * d), lv(d), uv((size_t)d * d);
+  lk.assign(d, 0.0);
+  lv.assign(d, 0.0);
+  uk.assign((size_t)d * d, 0.0);
+  uv.assign((size_t)d * d, 0.0);
   jacobi_eigh(ck.data(), d, lk.data(), uk.data());
   jacobi_eigh(cv.data(), d, lv.data(), uv.data());
   // key importances: sigma_i^2 * u_i^T M_Q u_i; value importances: sigma_i^2
-  std::vector<double> ik(d), iv(d), tmp(d);
+  ik.assign(d, 0.0);
+  iv.assign(d, 0.0);
+  std::vector<double> tmp(d);
   for (int i = 0; i < d; ++i) {
     for (int a = 0; a < d; ++a) {
       double acc = 0.0;
@@ -399,8 +411,28 @@ static void calibrate_one(const kv_calib_set& s, const kv_calib_opts& o, SetResu
       r.err = "non-finite statistics";
       return;
     }
-  build_tensor(mk, lk, uk, ik, record_words(o.bits_k, d), o.max_bits, d, r, 0);
-  build_tensor(mv, lv, uv, iv, record_words(o.bits_v, d), o.max_bits, d, r, 1);
+  // Key against value distortion in the attention output: to first order a key error e_t moves the output by
+  // p_t alpha (q.e_t)(v_t - o), so with white noise E|do|^2 = sum_t p_t^2 (alpha^2 |v_t - o|^2 sum_i w_i D^K_i
+  // + sum_i D^V_i) (additive, factored over tokens and channels: [AATC] Key points, first bullet). With
+  // |v_t - o|^2 at its mean tr(Sigma_V) and alpha = 1/sqrt(d): rho = tr(Sigma_V) / d.
+  double tr = 0.0;
+  for (int i = 0; i < d; ++i) tr += std::max(lv[i], 0.0);
+  P.rho = tr / d;
+}
+
+// Integer water-filling of imp at 32 rw - 32 code bits; returns sum_i imp_i 4^-b_i (the white-noise distortion
+// of a b-bit channel is proportional to sigma^2 4^-b).
+static double budget_distortion(const std::vector<double>& imp, int rw, int bmax, int d) {
+  std::vector<int32_t> w(d);
+  water_fill(imp.data(), d, 32 * rw - 32, bmax, w.data());
+  double acc = 0.0;
+  for (int i = 0; i < d; ++i) acc += imp[i] * ldexp(1.0, -2 * w[i]);
+  return acc;
+}
+
+static void build_one(const SetPrep& P, int rwk, int rwv, const kv_calib_opts& o, SetResult& r) {
+  build_tensor(P.mk, P.lk, P.uk, P.ik, rwk, o.max_bits, o.d, r, 0);
+  build_tensor(P.mv, P.lv, P.uv, P.iv, rwv, o.max_bits, o.d, r, 1);
 }
 
 static kv_status check_budget(float bits, int d, int bmax, int* rw_out) {
@@ -425,19 +457,56 @@ extern "C" kv_status kv_calibrate(int n_sets, const kv_calib_set* sets, const kv
     KV_REQUIRE(sets[i].k && sets[i].v && sets[i].q, KV_ERR_INVALID_ARG, "set %d: null pointer", i);
     KV_REQUIRE(sets[i].n_tok >= 2 && sets[i].n_q >= 1, KV_ERR_INVALID_ARG, "set %d: need n_tok >= 2, n_q >= 1", i);
   }
+  KV_REQUIRE(opts->joint == 0 || opts->joint == 1, KV_ERR_INVALID_ARG, "joint must be 0 or 1");
   std::vector<SetResult> res(n_sets);
+  std::vector<SetPrep> prep(n_sets);
   int nth = opts->n_threads > 0 ? opts->n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
   nth = std::min(nth, n_sets);
-  std::atomic<int> next{0};
-  auto worker = [&]() {
-    for (int i; (i = next.fetch_add(1)) < n_sets;) calibrate_one(sets[i], *opts, res[i]);
+  auto parallel = [&](auto&& fn) {  // fn(i) for every set, on nth host threads
+    std::atomic<int> next{0};
+    auto worker = [&]() {
+      for (int i; (i = next.fetch_add(1)) < n_sets;) fn(i);
+    };
+    std::vector<std::thread> pool;
+    for (int t = 1; t < nth; ++t) pool.emplace_back(worker);
+    worker();
+    for (auto& th : pool) th.join();
   };
-  std::vector<std::thread> pool;
-  for (int t = 1; t < nth; ++t) pool.emplace_back(worker);
-  worker();
-  for (auto& th : pool) th.join();
+  parallel([&](int i) { prepare_one(sets[i], *opts, prep[i], res[i]); });
   for (int i = 0; i < n_sets; ++i)
     KV_REQUIRE(res[i].ok, KV_ERR_NUMERIC, "set %d: %s", i, res[i].err.c_str());
+  if (opts->joint) {
+    // one split of the record between keys and values for the whole table (the cache holds one record length
+    // per tensor): the split that minimises the summed distortion; objectives within a relative 1e-9 of the
+    // minimum tie, ties go to the split nearest the separate allocation's, then to fewer key words
+    const int r_total = rwk + rwv, rmax = 1 + opts->max_bits * opts->d / 32;
+    std::vector<int> cands;
+    for (int r = 1; r < r_total; ++r)
+      if (r <= rmax && r_total - r <= rmax) cands.push_back(r);
+    std::vector<double> J(cands.size() * (size_t)n_sets);
+    parallel([&](int i) {
+      for (size_t c = 0; c < cands.size(); ++c)
+        J[c * n_sets + i] = prep[i].rho * budget_distortion(prep[i].ik, cands[c], opts->max_bits, opts->d) +
+                            budget_distortion(prep[i].iv, r_total - cands[c], opts->max_bits, opts->d);
+    });
+    std::vector<double> Jc(cands.size(), 0.0);
+    double jmin = INFINITY;
+    for (size_t c = 0; c < cands.size(); ++c) {
+      for (int i = 0; i < n_sets; ++i) Jc[c] += J[c * n_sets + i];
+      jmin = std::min(jmin, Jc[c]);
+    }
+    int best = -1;
+    for (size_t c = 0; c < cands.size(); ++c) {
+      if (!(Jc[c] <= jmin * (1.0 + 1e-9))) continue;
+      if (best < 0 || std::abs(cands[c] - rwk) < std::abs(best - rwk) ||
+          (std::abs(cands[c] - rwk) == std::abs(best - rwk) && cands[c] < best))
+        best = cands[c];
+    }
+    KV_REQUIRE(best >= 1, KV_ERR_NUMERIC, "joint allocation: no finite split");
+    rwv = r_total - best;
+    rwk = best;
+  }
+  parallel([&](int i) { build_one(prep[i], rwk, rwv, *opts, res[i]); });
   kv_params* p = new kv_params();
   p->d = opts->d;
   p->n_sets = n_sets;
