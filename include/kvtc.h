@@ -87,6 +87,7 @@ typedef struct {
   int joint;      /* 0: keys and values each get their own budget (R_wK from bits_k, R_wV from bits_v).
                    * 1: the table keeps R_wK + R_wV words per token but splits them between keys and values
                    *    jointly (see kv_calibrate)                                                      */
+  int key_basis;  /* 0: the KLT of Sigma_K. 1: the attention-aware orthogonal key basis (see kv_calibrate) */
 } kv_calib_opts;
 
 /* Calibrate n_sets sets: fp64 mean/covariance of K and V, query second moment M_Q, Jacobi
@@ -101,6 +102,12 @@ typedef struct {
  * sum_j lambda_V,j 4^-b_j (each tensor water-filled at its own budget); objectives within a relative 1e-9 tie,
  * ties go to the split nearest the separate one, then to fewer key words. The record lengths then differ
  * between keys and values (kv_params_record_words).
+ * key_basis = 1 ([NOVA-KV]: derive the key transform from the attention-aware distortion, here kept
+ * orthogonal): with white noise in basis U the key distortion is sum_i w_i D_i, and water-filling against the
+ * coefficient variances s_i = u_i^T Sigma_K u_i makes it proportional to (prod_i s_i w_i)^(1/d) at high rate.
+ * Starting from the KLT, 8 cyclic Jacobi sweeps rotate each pair (i < j) by the angle on a 48-point grid over
+ * [-pi/4, pi/4) that minimises the pair's log s_i + log s_j + log w_i + log w_j (rotating only when that gains
+ * more than 1e-10); the key importances are then s_i w_i and the stored variances s_i.
  * The result lives on the host; call kv_params_upload before encoding or decoding.
  * Errors: KV_ERR_INVALID_ARG (null, n_tok < 2, n_q < 1), KV_ERR_UNSUPPORTED (d), KV_ERR_BUDGET,
  * KV_ERR_NUMERIC (non-finite input). */

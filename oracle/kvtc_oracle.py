@@ -104,6 +104,52 @@ def klt(sigma):
 # ----------------------------------------------------------------------------------------------------
 # 3. importances
 # ----------------------------------------------------------------------------------------------------
+def attention_aware_key_basis(sigma_k, m_q, u0, sweeps: int = 8, grid: int = 48):
+    """Orthogonal key basis for the attention-aware distortion. With white quantisation noise of variances
+    D_i in basis U the key distortion is sum_i w_i D_i, w_i = u_i^T M_Q u_i, and water-filling against the
+    coefficient variances s_i = u_i^T Sigma_K u_i makes it proportional (high-rate model) to
+    (prod_i s_i w_i)^(1/d); the KLT minimises prod s_i alone (Hadamard) and ignores w. [NOVA-KV] derives the
+    key transform from the attention-aware distortion (its optimum is not orthogonal); this keeps the
+    transform orthogonal and minimises sum_i log s_i + log w_i by cyclic Jacobi sweeps from u0 (the KLT):
+    pairs (i, j), i < j in row order, each rotated by the angle phi on the grid -pi/4 + k pi/(2 grid),
+    k = 0 .. grid-1, that minimises the pair's four log terms (first such k), applied only when it beats
+    phi = 0 by more than 1e-10. Sigma_K and M_Q are regularised by 1e-12 tr/d on the diagonal."""
+    A = np.array(sigma_k, F64)
+    B = np.array(m_q, F64)
+    d = A.shape[0]
+    A += np.eye(d) * (1e-12 * np.trace(A) / d)
+    B += np.eye(d) * (1e-12 * np.trace(B) / d)
+    U = np.array(u0, F64)
+    a = U.T @ A @ U
+    b = U.T @ B @ U
+    phis = -np.pi / 4 + np.arange(grid) * (np.pi / 2 / grid)
+    c, s = np.cos(phis), np.sin(phis)
+    k0 = grid // 2                                            # phi = 0
+    for _ in range(sweeps):
+        for i in range(d - 1):
+            for j in range(i + 1, d):
+                f = (np.log(c * c * a[i, i] + 2 * c * s * a[i, j] + s * s * a[j, j]) +
+                     np.log(s * s * a[i, i] - 2 * c * s * a[i, j] + c * c * a[j, j]) +
+                     np.log(c * c * b[i, i] + 2 * c * s * b[i, j] + s * s * b[j, j]) +
+                     np.log(s * s * b[i, i] - 2 * c * s * b[i, j] + c * c * b[j, j]))
+                k = int(np.argmin(f))
+                if not f[k] < f[k0] - 1e-10:
+                    continue
+                R = np.array([[c[k], -s[k]], [s[k], c[k]]])    # u_i <- c u_i + s u_j, u_j <- -s u_i + c u_j
+                U[:, [i, j]] = U[:, [i, j]] @ R
+                for M in (a, b):
+                    M[:, [i, j]] = M[:, [i, j]] @ R
+                    M[[i, j], :] = R.T @ M[[i, j], :]
+    return U
+
+
+def basis_objective(u, sigma_k, m_q):
+    """sum_i log(u_i^T Sigma_K u_i) + log(u_i^T M_Q u_i): the log of prod_i s_i w_i."""
+    u = np.asarray(u, F64)
+    return float(np.sum(np.log(np.einsum("ji,jk,ki->i", u, sigma_k, u))) +
+                 np.sum(np.log(np.einsum("ji,jk,ki->i", u, m_q, u))))
+
+
 def key_weights(u, m_q):
     """w_i = u_i^T M_Q u_i for each eigenvector column u_i."""
     u = np.asarray(u, F64)
@@ -329,11 +375,20 @@ def build_tensor_params(mu_raw, lam, u, importance, r_words: int, max_bits: int,
                         eigvals=lam[order], importance=imp_st, pairing=pairing)
 
 
-def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8):
+def key_basis(s_k, m_q, attention_aware: bool):
+    """(coefficient variances, basis) of the keys: the KLT, or the attention-aware basis started from it."""
+    lam_k, u_k = klt(s_k)
+    if not attention_aware:
+        return lam_k, u_k
+    u = attention_aware_key_basis(s_k, m_q, u_k)
+    return np.einsum("ji,jk,ki->i", u, np.asarray(s_k, F64), u), u
+
+
+def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8, attention_aware_keys: bool = False):
     """Full calibration of one (layer, KV head) set -> (TensorParams K, TensorParams V)."""
     d = np.asarray(k).shape[1]
     mu_k, s_k, mu_v, s_v, m_q = calib_statistics(k, v, q)
-    lam_k, u_k = klt(s_k)
+    lam_k, u_k = key_basis(s_k, m_q, attention_aware_keys)
     lam_v, u_v = klt(s_v)
     imp_k = key_importance(lam_k, u_k, m_q)
     imp_v = value_importance(lam_v)
@@ -377,7 +432,7 @@ def joint_split(per_set, r_total: int, rwk_sep: int, max_bits: int, d: int) -> i
     return min(ties, key=lambda r: (abs(r - rwk_sep), r))
 
 
-def calibrate_joint(sets, bits_k: float, bits_v: float, max_bits: int = 8):
+def calibrate_joint(sets, bits_k: float, bits_v: float, max_bits: int = 8, attention_aware_keys: bool = False):
     """Calibration of a table of sets [(k, v, q), ...] with the key/value split of the record chosen jointly:
     the table keeps R_wK + R_wV = record_words(bits_k) + record_words(bits_v) words per token, split as
     joint_split decides (one split for the table, since the cache holds one record length per tensor); each
@@ -386,7 +441,7 @@ def calibrate_joint(sets, bits_k: float, bits_v: float, max_bits: int = 8):
     prep = []
     for k, v, q in sets:
         mu_k, s_k, mu_v, s_v, m_q = calib_statistics(k, v, q)
-        lam_k, u_k = klt(s_k)
+        lam_k, u_k = key_basis(s_k, m_q, attention_aware_keys)
         lam_v, u_v = klt(s_v)
         prep.append((mu_k, lam_k, u_k, key_importance(lam_k, u_k, m_q), mu_v, lam_v, u_v, value_importance(lam_v),
                      exchange_rate(lam_v, d)))

@@ -227,6 +227,63 @@ def pin_joint_split_by_enumeration():
     assert same == 11
 
 
+def pin_aware_basis_commuting():
+    """When Sigma_K and M_Q share an eigenbasis (distinct eigenvalues), the KLT already minimises
+    prod s_i w_i (Hadamard's inequality for each factor, equality only on the eigenbasis): no rotation is
+    taken and the basis comes back unchanged."""
+    rng = np.random.default_rng(15)
+    d = 16
+    q = synth.random_orthogonal(d, rng)
+    A = (q * (0.8 ** np.arange(d))) @ q.T
+    B = (q * (1.0 + rng.random(d))) @ q.T
+    assert np.array_equal(O.attention_aware_key_basis(A, B, q), q)
+
+
+def pin_aware_basis_two_channels():
+    """d = 2: every sweep rotates by a multiple of the grid step pi/96 from the start (2-D rotations compose
+    into one), so the result is the best of the 48 lattice angles of the start (enumerated here), and its angle
+    lies within one lattice step of the true optimum's (a 20000-point enumeration; the objective has period
+    pi/2 in the angle, which swaps the two channels)."""
+    rng = np.random.default_rng(16)
+    for _ in range(5):
+        x = rng.standard_normal((2, 2))
+        A = x @ x.T + 0.1 * np.eye(2)
+        y = rng.standard_normal((2, 2))
+        B = y @ y.T + 0.1 * np.eye(2)
+        u0 = np.eye(2)
+        u = O.attention_aware_key_basis(A, B, u0)
+
+        def obj(phi):
+            c, s = np.cos(phi), np.sin(phi)
+            return O.basis_objective(np.array([[c, -s], [s, c]]), A + 1e-12 * np.trace(A) / 2 * np.eye(2),
+                                     B + 1e-12 * np.trace(B) / 2 * np.eye(2))
+
+        lattice = min(obj(-np.pi / 4 + k * np.pi / 96) for k in range(48))
+        phis = np.linspace(-np.pi / 4, np.pi / 4, 20000, endpoint=False)
+        best = phis[int(np.argmin([obj(p) for p in phis]))]
+        got = O.basis_objective(u, A + 1e-12 * np.trace(A) / 2 * np.eye(2), B + 1e-12 * np.trace(B) / 2 * np.eye(2))
+        assert abs(got - lattice) <= 1e-9, (got, lattice)
+        phi = np.arctan2(u[1, 0], u[0, 0])
+        gap = abs((phi - best + np.pi / 4) % (np.pi / 2) - np.pi / 4)
+        assert gap <= np.pi / 96 + 1e-9, (phi, best)
+        assert np.allclose(u.T @ u, np.eye(2), atol=1e-14)
+
+
+def pin_aware_basis_bounds():
+    """On the Llama-shaped layer's statistics the attention-aware basis is orthogonal, its objective lies above
+    Hadamard's bound log det Sigma_K + log det M_Q (reached only when one basis diagonalises both) and at
+    least 20 nats below the KLT's; the coefficient variances it reports are diag(U^T Sigma_K U)."""
+    L = synth.make_layer(synth.WORKLOADS["llama_decode_32k"], T=16, steps=1)
+    _, s_k, _, _, m_q = O.calib_statistics(L.calib_k[0], L.calib_v[0], L.calib_q[0])
+    lam, u0 = O.klt(s_k)
+    var, u = O.key_basis(s_k, m_q, True)
+    assert np.abs(u.T @ u - np.eye(128)).max() < 1e-12
+    bound = np.linalg.slogdet(s_k)[1] + np.linalg.slogdet(m_q)[1]
+    got, klt_obj = O.basis_objective(u, s_k, m_q), O.basis_objective(u0, s_k, m_q)
+    assert bound < got < klt_obj - 20.0, (bound, got, klt_obj)
+    assert np.allclose(var, np.diag(u.T @ s_k @ u), rtol=1e-12)
+
+
 # --- water-filling -----------------------------------------------------------------------------------
 def pin_water_fill_golden():
     for lam, C, bmax, b_real, b_int in read_golden("water_fill_small.txt"):

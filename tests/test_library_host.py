@@ -103,6 +103,31 @@ def test_host_joint_calibration_matches_oracle(name, bits):
             assert np.max(np.abs(info["T"].astype(np.float64) - po.T.astype(np.float64))) < 1e-5
 
 
+@pytest.mark.parametrize("name", ["tiny", "llama_decode_32k", "qwen_batched_8k"])
+def test_host_attention_aware_key_basis_matches_oracle(name):
+    """The attention-aware key basis: the library's Jacobi sweeps take the oracle's rotations (same grid, same
+    order, same threshold), so the transforms, variances and widths agree; the value side is untouched."""
+    w = synth.WORKLOADS[name]
+    L = synth.make_layer(w, T=256, B=2 if w.calib == "own_prefix" else 1, steps=1)
+    sets = list(zip(L.calib_k, L.calib_v, L.calib_q))[:3]
+    bits = w.bits[0]
+    P = kvtc.kv_calibrate(sets, bits, bits, attention_aware_keys=True)
+    for s, (ck, cv, cq) in enumerate(sets):
+        pk, pv = O.calibrate(ck, cv, cq, bits, bits, attention_aware_keys=True)
+        for t, po in ((0, pk), (1, pv)):
+            info = P.info(s, t)
+            assert np.array_equal(info["widths"], po.widths)
+            assert np.max(np.abs(info["T"].astype(np.float64) - po.T.astype(np.float64))) < 1e-5
+            assert np.allclose(info["eigvals"], po.eigvals, rtol=1e-9, atol=1e-12 * np.abs(po.eigvals).max())
+
+
+def test_key_basis_flag_is_checked():
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75, attention_aware_keys=2)
+    assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+
+
 def test_joint_flag_is_checked():
     L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
     sets = list(zip(L.calib_k, L.calib_v, L.calib_q))

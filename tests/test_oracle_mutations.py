@@ -10,7 +10,7 @@ _orig = {name: getattr(O, name) for name in
          ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
           "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat",
           "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout", "storage_order", "attend_decode",
-          "exchange_rate", "joint_split"]}
+          "exchange_rate", "joint_split", "attention_aware_key_basis"]}
 
 
 def _klt_transposed(sigma):
@@ -227,6 +227,37 @@ def _split_ignores_rho(per_set, r_total, rwk_sep, max_bits, d):
     return _orig["joint_split"]([(ik, iv, 1.0) for ik, iv, _ in per_set], r_total, rwk_sep, max_bits, d)
 
 
+def _aware_ignores_queries(sigma_k, m_q, u0, sweeps=8, grid=48):
+    return _orig["attention_aware_key_basis"](sigma_k, np.eye(np.asarray(sigma_k).shape[0]), u0, sweeps, grid)
+
+
+def _aware_rotates_u_backwards(sigma_k, m_q, u0, sweeps=8, grid=48):
+    """Tracks the rotated matrices correctly but turns the basis the other way."""
+    A = np.array(sigma_k, np.float64) + np.eye(len(sigma_k)) * (1e-12 * np.trace(sigma_k) / len(sigma_k))
+    B = np.array(m_q, np.float64) + np.eye(len(m_q)) * (1e-12 * np.trace(m_q) / len(m_q))
+    U = np.array(u0, np.float64)
+    a, b = U.T @ A @ U, U.T @ B @ U
+    phis = -np.pi / 4 + np.arange(grid) * (np.pi / 2 / grid)
+    c, s = np.cos(phis), np.sin(phis)
+    d = len(A)
+    for _ in range(sweeps):
+        for i in range(d - 1):
+            for j in range(i + 1, d):
+                f = (np.log(c * c * a[i, i] + 2 * c * s * a[i, j] + s * s * a[j, j]) +
+                     np.log(s * s * a[i, i] - 2 * c * s * a[i, j] + c * c * a[j, j]) +
+                     np.log(c * c * b[i, i] + 2 * c * s * b[i, j] + s * s * b[j, j]) +
+                     np.log(s * s * b[i, i] - 2 * c * s * b[i, j] + c * c * b[j, j]))
+                k = int(np.argmin(f))
+                if not f[k] < f[grid // 2] - 1e-10:
+                    continue
+                R = np.array([[c[k], -s[k]], [s[k], c[k]]])
+                U[:, [i, j]] = U[:, [i, j]] @ R.T
+                for M in (a, b):
+                    M[:, [i, j]] = M[:, [i, j]] @ R
+                    M[[i, j], :] = R.T @ M[[i, j], :]
+    return U
+
+
 MUTATIONS = [
     ("klt", _klt_transposed, P.pin_klt_known_spectrum),
     ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
@@ -255,6 +286,8 @@ MUTATIONS = [
     ("attend_decode", _attend_one_token_short, P.pin_decode_brute_force),
     ("exchange_rate", _rate_alpha_not_squared, P.pin_exchange_rate_monte_carlo),
     ("joint_split", _split_ignores_rho, P.pin_joint_split_by_enumeration),
+    ("attention_aware_key_basis", _aware_ignores_queries, P.pin_aware_basis_bounds),
+    ("attention_aware_key_basis", _aware_rotates_u_backwards, P.pin_aware_basis_two_channels),
 ]
 
 

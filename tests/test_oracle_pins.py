@@ -106,3 +106,15 @@ def test_exchange_rate_monte_carlo():
 
 def test_joint_split_by_enumeration():
     P.pin_joint_split_by_enumeration()
+
+
+def test_aware_basis_commuting():
+    P.pin_aware_basis_commuting()
+
+
+def test_aware_basis_two_channels():
+    P.pin_aware_basis_two_channels()
+
+
+def test_aware_basis_bounds():
+    P.pin_aware_basis_bounds()

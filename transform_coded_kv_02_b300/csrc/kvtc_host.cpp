@@ -365,6 +365,90 @@ static void build_tensor(const std::vector<double>& mu_raw, const std::vector<do
   }
 }
 
+// Attention-aware orthogonal key basis, from the KLT U (columns; replaced in place). With white quantisation
+// noise in basis U the key distortion is sum_i w_i D_i (w_i = u_i^T M_Q u_i); water-filling against the
+// coefficient variances s_i = u_i^T Sigma_K u_i makes it proportional (high-rate model) to (prod_i s_i w_i)^(1/d),
+// of which the KLT minimises only prod s_i. [NOVA-KV] derives the key transform from this distortion (its optimum
+// is not orthogonal); here the transform stays orthogonal and sum_i log s_i + log w_i falls by cyclic Jacobi
+// sweeps: each pair (i < j, row order) is rotated by the grid angle -pi/4 + k pi/(2 grid) that minimises its four
+// log terms (the first such k), when that beats no rotation by more than 1e-10. Both matrices get 1e-12 tr/d
+// added on the diagonal.
+static void attention_aware_basis(const std::vector<double>& sk, const std::vector<double>& mq, int d,
+                                  std::vector<double>& U) {
+  constexpr int SWEEPS = 8, GRID = 48;
+  std::vector<double> A(sk), B(mq);
+  double ta = 0.0, tb = 0.0;
+  for (int i = 0; i < d; ++i) {
+    ta += A[(size_t)i * d + i];
+    tb += B[(size_t)i * d + i];
+  }
+  for (int i = 0; i < d; ++i) {
+    A[(size_t)i * d + i] += 1e-12 * ta / d;
+    B[(size_t)i * d + i] += 1e-12 * tb / d;
+  }
+  // a = U^T A U, b = U^T B U
+  auto congruence = [&](const std::vector<double>& M, std::vector<double>& out) {
+    std::vector<double> MU((size_t)d * d, 0.0);
+    for (int r = 0; r < d; ++r)
+      for (int c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int k = 0; k < d; ++k) acc += M[(size_t)r * d + k] * U[(size_t)k * d + c];
+        MU[(size_t)r * d + c] = acc;
+      }
+    out.assign((size_t)d * d, 0.0);
+    for (int r = 0; r < d; ++r)
+      for (int c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int k = 0; k < d; ++k) acc += U[(size_t)k * d + r] * MU[(size_t)k * d + c];
+        out[(size_t)r * d + c] = acc;
+      }
+  };
+  std::vector<double> a, b;
+  congruence(A, a);
+  congruence(B, b);
+  double cs[GRID], sn[GRID], f[GRID];
+  for (int k = 0; k < GRID; ++k) {
+    const double phi = -M_PI / 4 + k * (M_PI / 2 / GRID);
+    cs[k] = cos(phi);
+    sn[k] = sin(phi);
+  }
+  const int k0 = GRID / 2;  // phi = 0
+  auto rotate = [&](std::vector<double>& M, int i, int j, double c, double s) {
+    for (int r = 0; r < d; ++r) {  // columns i, j
+      const double mi = M[(size_t)r * d + i], mj = M[(size_t)r * d + j];
+      M[(size_t)r * d + i] = mi * c + mj * s;
+      M[(size_t)r * d + j] = mi * -s + mj * c;
+    }
+    for (int col = 0; col < d; ++col) {  // rows i, j
+      const double mi = M[(size_t)i * d + col], mj = M[(size_t)j * d + col];
+      M[(size_t)i * d + col] = c * mi + s * mj;
+      M[(size_t)j * d + col] = -s * mi + c * mj;
+    }
+  };
+  for (int sweep = 0; sweep < SWEEPS; ++sweep)
+    for (int i = 0; i < d - 1; ++i)
+      for (int j = i + 1; j < d; ++j) {
+        const double aii = a[(size_t)i * d + i], ajj = a[(size_t)j * d + j], aij = a[(size_t)i * d + j];
+        const double bii = b[(size_t)i * d + i], bjj = b[(size_t)j * d + j], bij = b[(size_t)i * d + j];
+        int kb = 0;
+        for (int k = 0; k < GRID; ++k) {
+          const double c = cs[k], s = sn[k];
+          f[k] = log(c * c * aii + 2 * c * s * aij + s * s * ajj) + log(s * s * aii - 2 * c * s * aij + c * c * ajj) +
+                 log(c * c * bii + 2 * c * s * bij + s * s * bjj) + log(s * s * bii - 2 * c * s * bij + c * c * bjj);
+          if (f[k] < f[kb]) kb = k;
+        }
+        if (!(f[kb] < f[k0] - 1e-10)) continue;
+        const double c = cs[kb], s = sn[kb];
+        for (int r = 0; r < d; ++r) {  // U columns i, j
+          const double ui = U[(size_t)r * d + i], uj = U[(size_t)r * d + j];
+          U[(size_t)r * d + i] = ui * c + uj * s;
+          U[(size_t)r * d + j] = ui * -s + uj * c;
+        }
+        rotate(a, i, j, c, s);
+        rotate(b, i, j, c, s);
+      }
+}
+
 // Statistics, transforms and importances of one set (everything before the record budget is applied).
 struct SetPrep {
   std::vector<double> mk, lk, uk, ik, mv, lv, uv, iv;
@@ -390,6 +474,18 @@ static void prepare_one(const kv_calib_set& s, const kv_calib_opts& o, SetPrep& 
   uv.assign((size_t)d * d, 0.0);
   jacobi_eigh(ck.data(), d, lk.data(), uk.data());
   jacobi_eigh(cv.data(), d, lv.data(), uv.data());
+  if (o.key_basis == 1) {  // attention-aware key basis; the variances are then the diagonal of U^T Sigma_K U
+    attention_aware_basis(ck, cq, d, uk);
+    for (int i = 0; i < d; ++i) {
+      double acc = 0.0;
+      for (int a = 0; a < d; ++a) {
+        double row = 0.0;
+        for (int b = 0; b < d; ++b) row += ck[(size_t)a * d + b] * uk[(size_t)b * d + i];
+        acc += uk[(size_t)a * d + i] * row;
+      }
+      lk[i] = acc;
+    }
+  }
   // key importances: sigma_i^2 * u_i^T M_Q u_i; value importances: sigma_i^2
   ik.assign(d, 0.0);
   iv.assign(d, 0.0);
@@ -458,6 +554,7 @@ extern "C" kv_status kv_calibrate(int n_sets, const kv_calib_set* sets, const kv
     KV_REQUIRE(sets[i].n_tok >= 2 && sets[i].n_q >= 1, KV_ERR_INVALID_ARG, "set %d: need n_tok >= 2, n_q >= 1", i);
   }
   KV_REQUIRE(opts->joint == 0 || opts->joint == 1, KV_ERR_INVALID_ARG, "joint must be 0 or 1");
+  KV_REQUIRE(opts->key_basis == 0 || opts->key_basis == 1, KV_ERR_INVALID_ARG, "key_basis must be 0 or 1");
   std::vector<SetResult> res(n_sets);
   std::vector<SetPrep> prep(n_sets);
   int nth = opts->n_threads > 0 ? opts->n_threads : (int)std::max(1u, std::thread::hardware_concurrency());

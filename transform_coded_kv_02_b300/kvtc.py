@@ -37,7 +37,7 @@ class kv_calib_set(ctypes.Structure):
 
 class kv_calib_opts(ctypes.Structure):
     _fields_ = [("d", c_int), ("bits_k", c_float), ("bits_v", c_float), ("max_bits", c_int), ("n_threads", c_int),
-                ("joint", c_int)]
+                ("joint", c_int), ("key_basis", c_int)]
 
 
 class kv_cache(ctypes.Structure):
@@ -172,9 +172,10 @@ class Params:
         _check("kv_params_save", _lib.kv_params_save(self.handle, path.encode()))
 
 
-def kv_calibrate(sets, bits_k, bits_v, max_bits=8, n_threads=0, d=128, joint=False):
+def kv_calibrate(sets, bits_k, bits_v, max_bits=8, n_threads=0, d=128, joint=False, attention_aware_keys=False):
     """sets: list of (k [n, d], v [n, d], q [m, d]) host arrays (converted to contiguous fp32); joint: split the
-    record words between keys and values jointly instead of by bits_k and bits_v."""
+    record words between keys and values jointly instead of by bits_k and bits_v; attention_aware_keys: the
+    attention-aware orthogonal key basis instead of the KLT."""
     keep = []
     arr = (kv_calib_set * len(sets))()
     for i, (k, v, q) in enumerate(sets):
@@ -183,7 +184,7 @@ def kv_calibrate(sets, bits_k, bits_v, max_bits=8, n_threads=0, d=128, joint=Fal
         q = np.ascontiguousarray(q, np.float32)
         keep += [k, v, q]
         arr[i] = kv_calib_set(_ptr(k), _ptr(v), _ptr(q), k.shape[0], q.shape[0])
-    opts = kv_calib_opts(d, bits_k, bits_v, max_bits, n_threads, int(joint))
+    opts = kv_calib_opts(d, bits_k, bits_v, max_bits, n_threads, int(joint), int(attention_aware_keys))
     h = c_void_p()
     _check("kv_calibrate", _lib.kv_calibrate(len(sets), arr, ctypes.byref(opts), ctypes.byref(h)))
     return Params(h.value)
