@@ -143,6 +143,28 @@ def attention_aware_key_basis(sigma_k, m_q, u0, sweeps: int = 8, grid: int = 48)
     return U
 
 
+def whitened_key_transform(sigma_k, m_q):
+    """[NOVA-KV]'s key transform under the high-resolution model, which is not orthogonal: T = c V^T M_Q^(1/2)
+    with V the eigenvectors (KLT) of M_Q^(1/2) Sigma_K M_Q^(1/2). The key distortion E_q[(q.e)^2] = e^T M_Q e
+    then equals |T e|^2 / c^2, a mean-squared error in the transform domain (the pages' generalised Parseval
+    relation), and the coefficients T k are uncorrelated with variances c^2 x the eigenvalues, so plain
+    reverse water-filling on those variances allocates the bits. c is the largest column norm of
+    (V^T M_Q^(1/2))^-1, so every column of T^-1 has norm <= 1 and |(T^-T q)_j| <= |q|. M_Q gets 1e-12 tr/d on
+    the diagonal. Returns (variances, T with rows = channels, T^-1)."""
+    A = np.asarray(sigma_k, F64)
+    M = np.array(m_q, F64)
+    d = M.shape[0]
+    M += np.eye(d) * (1e-12 * np.trace(M) / d)
+    lq, Q = np.linalg.eigh(M)
+    m_half = (Q * np.sqrt(lq)) @ Q.T
+    m_ihalf = (Q / np.sqrt(lq)) @ Q.T
+    lam, V = klt(m_half @ A @ m_half)
+    T = V.T @ m_half
+    T_inv = m_ihalf @ V
+    c = float(np.linalg.norm(T_inv, axis=0).max())
+    return np.maximum(lam, 0.0) * c * c, T * c, T_inv / c
+
+
 def basis_objective(u, sigma_k, m_q):
     """sum_i log(u_i^T Sigma_K u_i) + log(u_i^T M_Q u_i): the log of prod_i s_i w_i."""
     u = np.asarray(u, F64)
@@ -325,8 +347,11 @@ class TensorParams:
     records, two tokens each, one slot per channel); slot_word / slot_pos: the first-fit placement (per
     channel pair, resp. per channel)."""
 
-    def __init__(self, T, mu, sigma, widths, r_words, eigvals=None, importance=None, pairing="channels"):
+    def __init__(self, T, mu, sigma, widths, r_words, eigvals=None, importance=None, pairing="channels",
+                 T_inv=None):
         self.T = np.ascontiguousarray(T, F32)
+        # inverse of a non-orthogonal transform (fp64; None: T is orthogonal and T^T is its inverse)
+        self.T_inv = None if T_inv is None else np.asarray(T_inv, F64)
         self.mu = np.ascontiguousarray(mu, F32)
         self.sigma = np.ascontiguousarray(sigma, F32)
         w = np.asarray(widths, np.int64).copy()
@@ -360,7 +385,7 @@ class TensorParams:
 
 
 def build_tensor_params(mu_raw, lam, u, importance, r_words: int, max_bits: int,
-                        pairing: str = "channels") -> TensorParams:
+                        pairing: str = "channels", u_inv=None) -> TensorParams:
     widths_eig = water_fill_integer(importance, code_bits(r_words), max_bits)
     order = storage_order(widths_eig, importance)
     imp_st = np.asarray(importance)[order]
@@ -371,8 +396,10 @@ def build_tensor_params(mu_raw, lam, u, importance, r_words: int, max_bits: int,
     T = u[:, order].T                                   # rows: storage channels
     mu_rot = T @ np.asarray(mu_raw, F64)
     sigma = np.sqrt(np.maximum(lam[order], 0.0))
+    # u_inv: the inverse of a non-orthogonal u^T; column i pairs with channel i, so it follows the storage order
+    T_inv = None if u_inv is None else np.asarray(u_inv, F64)[:, order]
     return TensorParams(T=T, mu=mu_rot, sigma=sigma, widths=widths, r_words=r_words,
-                        eigvals=lam[order], importance=imp_st, pairing=pairing)
+                        eigvals=lam[order], importance=imp_st, pairing=pairing, T_inv=T_inv)
 
 
 def key_basis(s_k, m_q, attention_aware: bool):
@@ -384,10 +411,21 @@ def key_basis(s_k, m_q, attention_aware: bool):
     return np.einsum("ji,jk,ki->i", u, np.asarray(s_k, F64), u), u
 
 
-def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8, attention_aware_keys: bool = False):
-    """Full calibration of one (layer, KV head) set -> (TensorParams K, TensorParams V)."""
+def calibrate(k, v, q, bits_k: float, bits_v: float, max_bits: int = 8, attention_aware_keys: bool = False,
+              whitened_keys: bool = False):
+    """Full calibration of one (layer, KV head) set -> (TensorParams K, TensorParams V). whitened_keys: the
+    non-orthogonal key transform of whitened_key_transform (the key importances are then the coefficient
+    variances: the distortion is already mean-squared in that domain)."""
     d = np.asarray(k).shape[1]
     mu_k, s_k, mu_v, s_v, m_q = calib_statistics(k, v, q)
+    if whitened_keys:
+        lam_k, t_k, t_inv = whitened_key_transform(s_k, m_q)
+        lam_v, u_v = klt(s_v)
+        pk = build_tensor_params(mu_k, lam_k, t_k.T, lam_k, record_words(bits_k, d), max_bits, "channels",
+                                 u_inv=t_inv)
+        pv = build_tensor_params(mu_v, lam_v, u_v, value_importance(lam_v), record_words(bits_v, d), max_bits,
+                                 "tokens")
+        return pk, pv
     lam_k, u_k = key_basis(s_k, m_q, attention_aware_keys)
     lam_v, u_v = klt(s_v)
     imp_k = key_importance(lam_k, u_k, m_q)
@@ -576,8 +614,11 @@ def dequantize(z16, s16, codes, p: TensorParams):
 
 
 def reconstruct(rec, p: TensorParams):
-    """Records -> original-basis vectors x^ = T^T y^ [n, d] (fp64), one row per token slot."""
+    """Records -> original-basis vectors x^ = T^-1 y^ [n, d] (fp64; T^-1 = T^T for an orthogonal T), one row per
+    token slot."""
     y = dequantize(*unpack(rec, p), p)
+    if p.T_inv is not None:
+        return y @ p.T_inv.T
     return y @ p.T.astype(F64)
 
 

@@ -284,6 +284,31 @@ def pin_aware_basis_bounds():
     assert np.allclose(var, np.diag(u.T @ s_k @ u), rtol=1e-12)
 
 
+def pin_whitened_key_transform():
+    """The non-orthogonal key transform: T^-1 T = I; the generalised Parseval relation e^T M_Q e = |T e|^2 / c^2
+    for every e (one constant c); uncorrelated coefficients, T Sigma_K T^T diagonal with the returned variances
+    on the diagonal; every column of T^-1 of norm at most 1 (one of them exactly 1); and with M_Q = I the rows
+    are the KLT's up to sign and one common scale."""
+    L = synth.make_layer(synth.WORKLOADS["llama_decode_32k"], T=16, steps=1)
+    _, s_k, _, _, m_q = O.calib_statistics(L.calib_k[0], L.calib_v[0], L.calib_q[0])
+    var, T, T_inv = O.whitened_key_transform(s_k, m_q)
+    d = T.shape[0]
+    assert np.abs(T_inv @ T - np.eye(d)).max() < 1e-9
+    m = m_q + np.eye(d) * (1e-12 * np.trace(m_q) / d)
+    e = np.random.default_rng(17).standard_normal((64, d))
+    ratio = np.einsum("nd,dk,nk->n", e, m, e) / np.sum((e @ T.T) ** 2, axis=1)
+    assert np.std(ratio) <= 1e-9 * np.mean(ratio)
+    c = T @ s_k @ T.T
+    assert np.abs(c - np.diag(np.diag(c))).max() <= 1e-9 * np.abs(np.diag(c)).max()
+    assert np.allclose(np.diag(c), var, rtol=1e-9, atol=1e-12 * var.max())
+    norms = np.linalg.norm(T_inv, axis=0)
+    assert norms.max() <= 1 + 1e-12 and abs(norms.max() - 1) < 1e-12
+    _, T1, _ = O.whitened_key_transform(s_k, np.eye(d))
+    _, u = O.klt(s_k)
+    cos = np.abs(np.sum(T1 * u.T, axis=1)) / np.linalg.norm(T1, axis=1)
+    assert np.all(cos > 1 - 1e-9)
+
+
 # --- water-filling -----------------------------------------------------------------------------------
 def pin_water_fill_golden():
     for lam, C, bmax, b_real, b_int in read_golden("water_fill_small.txt"):

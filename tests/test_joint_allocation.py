@@ -48,3 +48,17 @@ def test_attention_aware_keys_lower_attention_error_llama_shape():
     print("relative L2 error against exact attention: KLT %.4f, attention-aware keys %.4f, both options %.4f"
           % (e_klt, e_aware, e_both))
     assert e_aware < 0.9 * e_klt and e_both < e_aware
+
+
+def test_whitened_keys_lower_attention_error_llama_shape():
+    """The non-orthogonal key transform (the attention-aware distortion is mean-squared in its domain) against
+    the KLT and the attention-aware orthogonal basis, same bytes per token."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    T, steps = 1024, 4
+    L = synth.make_layer(w, T=T, steps=steps)
+    sets_in = list(zip(L.calib_k, L.calib_v, L.calib_q))
+    klt = [O.calibrate(k, v, q, 2.75, 2.75) for k, v, q in sets_in]
+    white = [O.calibrate(k, v, q, 2.75, 2.75, whitened_keys=True) for k, v, q in sets_in]
+    e_klt, e_white = _decode_error(L, klt, w, T, steps), _decode_error(L, white, w, T, steps)
+    print("relative L2 error against exact attention: KLT %.4f, whitened keys %.4f" % (e_klt, e_white))
+    assert e_white < 0.85 * e_klt

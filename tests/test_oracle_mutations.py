@@ -10,7 +10,7 @@ _orig = {name: getattr(O, name) for name in
          ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
           "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat",
           "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout", "storage_order", "attend_decode",
-          "exchange_rate", "joint_split", "attention_aware_key_basis"]}
+          "exchange_rate", "joint_split", "attention_aware_key_basis", "whitened_key_transform"]}
 
 
 def _klt_transposed(sigma):
@@ -258,6 +258,21 @@ def _aware_rotates_u_backwards(sigma_k, m_q, u0, sweeps=8, grid=48):
     return U
 
 
+def _whitened_full_power(sigma_k, m_q):
+    """Whitens with M_Q instead of its square root."""
+    A = np.asarray(sigma_k, np.float64)
+    M = np.array(m_q, np.float64) + np.eye(len(m_q)) * (1e-12 * np.trace(m_q) / len(m_q))
+    lam, V = O.klt(M @ A @ M)
+    T = V.T @ M
+    T_inv = np.linalg.inv(T)
+    c = float(np.linalg.norm(T_inv, axis=0).max())
+    return lam * c * c, T * c, T_inv / c
+
+
+def _whitened_ignores_queries(sigma_k, m_q):
+    return _orig["whitened_key_transform"](sigma_k, np.eye(len(m_q)))
+
+
 MUTATIONS = [
     ("klt", _klt_transposed, P.pin_klt_known_spectrum),
     ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
@@ -288,6 +303,8 @@ MUTATIONS = [
     ("joint_split", _split_ignores_rho, P.pin_joint_split_by_enumeration),
     ("attention_aware_key_basis", _aware_ignores_queries, P.pin_aware_basis_bounds),
     ("attention_aware_key_basis", _aware_rotates_u_backwards, P.pin_aware_basis_two_channels),
+    ("whitened_key_transform", _whitened_full_power, P.pin_whitened_key_transform),
+    ("whitened_key_transform", _whitened_ignores_queries, P.pin_whitened_key_transform),
 ]
 
 

@@ -118,3 +118,7 @@ def test_aware_basis_two_channels():
 
 def test_aware_basis_bounds():
     P.pin_aware_basis_bounds()
+
+
+def test_whitened_key_transform():
+    P.pin_whitened_key_transform()
