@@ -470,7 +470,8 @@ def joint_split(per_set, r_total: int, rwk_sep: int, max_bits: int, d: int) -> i
     return min(ties, key=lambda r: (abs(r - rwk_sep), r))
 
 
-def calibrate_joint(sets, bits_k: float, bits_v: float, max_bits: int = 8, attention_aware_keys: bool = False):
+def calibrate_joint(sets, bits_k: float, bits_v: float, max_bits: int = 8, attention_aware_keys: bool = False,
+                    whitened_keys: bool = False):
     """Calibration of a table of sets [(k, v, q), ...] with the key/value split of the record chosen jointly:
     the table keeps R_wK + R_wV = record_words(bits_k) + record_words(bits_v) words per token, split as
     joint_split decides (one split for the table, since the cache holds one record length per tensor); each
@@ -479,15 +480,19 @@ def calibrate_joint(sets, bits_k: float, bits_v: float, max_bits: int = 8, atten
     prep = []
     for k, v, q in sets:
         mu_k, s_k, mu_v, s_v, m_q = calib_statistics(k, v, q)
-        lam_k, u_k = key_basis(s_k, m_q, attention_aware_keys)
         lam_v, u_v = klt(s_v)
-        prep.append((mu_k, lam_k, u_k, key_importance(lam_k, u_k, m_q), mu_v, lam_v, u_v, value_importance(lam_v),
-                     exchange_rate(lam_v, d)))
+        if whitened_keys:   # importances: the coefficient variances (the distortion is mean-squared there)
+            lam_k, t_k, t_inv = whitened_key_transform(s_k, m_q)
+            key = (mu_k, lam_k, t_k.T, lam_k, t_inv)
+        else:
+            lam_k, u_k = key_basis(s_k, m_q, attention_aware_keys)
+            key = (mu_k, lam_k, u_k, key_importance(lam_k, u_k, m_q), None)
+        prep.append(key + (mu_v, lam_v, u_v, value_importance(lam_v), exchange_rate(lam_v, d)))
     rwk_sep, rwv_sep = record_words(bits_k, d), record_words(bits_v, d)
-    rwk = joint_split([(p[3], p[7], p[8]) for p in prep], rwk_sep + rwv_sep, rwk_sep, max_bits, d)
+    rwk = joint_split([(p[3], p[8], p[9]) for p in prep], rwk_sep + rwv_sep, rwk_sep, max_bits, d)
     rwv = rwk_sep + rwv_sep - rwk
-    return [(build_tensor_params(p[0], p[1], p[2], p[3], rwk, max_bits, "channels"),
-             build_tensor_params(p[4], p[5], p[6], p[7], rwv, max_bits, "tokens")) for p in prep]
+    return [(build_tensor_params(p[0], p[1], p[2], p[3], rwk, max_bits, "channels", u_inv=p[4]),
+             build_tensor_params(p[5], p[6], p[7], p[8], rwv, max_bits, "tokens")) for p in prep]
 
 
 # ----------------------------------------------------------------------------------------------------
