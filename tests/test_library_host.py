@@ -121,6 +121,22 @@ def test_host_attention_aware_key_basis_matches_oracle(name):
             assert np.allclose(info["eigvals"], po.eigvals, rtol=1e-9, atol=1e-12 * np.abs(po.eigvals).max())
 
 
+def test_host_both_calibration_options_match_oracle():
+    """The attention-aware key basis and the joint split together: the library's split, widths and transforms
+    are the oracle's."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    L = synth.make_layer(w, T=256, steps=1)
+    sets = list(zip(L.calib_k, L.calib_v, L.calib_q))[:3]
+    P = kvtc.kv_calibrate(sets, 2.75, 2.75, joint=True, attention_aware_keys=True)
+    ref = O.calibrate_joint(sets, 2.75, 2.75, attention_aware_keys=True)
+    assert (P.record_words(0), P.record_words(1)) == (ref[0][0].r_words, ref[0][1].r_words) == (14, 8)
+    for s, (pk, pv) in enumerate(ref):
+        for t, po in ((0, pk), (1, pv)):
+            info = P.info(s, t)
+            assert np.array_equal(info["widths"], po.widths)
+            assert np.max(np.abs(info["T"].astype(np.float64) - po.T.astype(np.float64))) < 1e-5
+
+
 def test_key_basis_flag_is_checked():
     L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
     with pytest.raises(kvtc.KvError) as e:
