@@ -177,6 +177,24 @@ def test_params_save_load_roundtrip(tmp_path):
     assert e.value.status == kvtc.KV_ERR_IO
 
 
+def test_params_save_load_unequal_record_lengths(tmp_path):
+    """A table from the joint split (14 key and 8 value words on the Llama-shaped statistics) keeps both
+    record lengths and every array through save and load."""
+    L = synth.make_layer(synth.WORKLOADS["llama_decode_32k"], T=16, steps=1)
+    sets = list(zip(L.calib_k, L.calib_v, L.calib_q))[:2]
+    P = kvtc.kv_calibrate(sets, 2.75, 2.75, joint=True, attention_aware_keys=True)
+    assert (P.record_words(0), P.record_words(1)) == (14, 8)
+    path = str(tmp_path / "joint.kvtc")
+    P.save(path)
+    Q = kvtc.kv_params_load(path)
+    assert (Q.record_words(0), Q.record_words(1)) == (14, 8)
+    for s in range(2):
+        for t in (0, 1):
+            a, b = P.info(s, t), Q.info(s, t)
+            for key in a:
+                assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), (s, t, key)
+
+
 def test_calibrate_argument_errors():
     rng = np.random.default_rng(0)
     k = rng.normal(size=(64, 128)).astype(np.float32)
