@@ -206,8 +206,8 @@ kv_status kv_attend_decode(const kv_params* p, const kv_cache* cache, const void
 
 /* Decode attention without a caller-provided workspace. No page has a counterpart; this entry point serves
  * callers that cannot allocate device memory around the call: a serving engine whose memory planner owns
- * all of the GPU's memory and hands a kernel library only pointers and a stream, or code that runs while a
- * stream is being captured into a CUDA graph, where cudaMalloc is not allowed.
+ * all of the GPU's memory and hands a kernel library only pointers and a stream, or code that runs inside an
+ * allocator or memory-pool callback, where calling cudaMalloc would re-enter the allocator.
  *   Same arguments, results and errors as kv_attend_decode, minus workspace and ws_bytes: the split
  *   partials, q operands and arrival counters live in one static device array of KV_NOALLOC_SCRATCH_BYTES
  *   bytes compiled into the library (every GPU that loads the library holds it until the process exits).
@@ -243,7 +243,9 @@ int kv_version(void);
  * ------------------------------------------------------------------------------------------------------ */
 /* Quantise + pack n rotated fp32 vectors y_dev [n][d] (storage order) of one set/tensor into rec_dev (keys:
  * [n][r_words]; values: [ceil(n/2)][2 r_words], a missing second token's half left as it was), running the
- * encode kernels' quantiser. variant 0: warp-per-token; variant 1: thread-per-token. */
+ * encode kernels' quantiser. variant 0: warp-per-token (CUDA-core encode); variant 1: thread-per-token;
+ * variant 2: the tensor-core encode's epilogue (coefficients staged in tensor memory, reciprocal quotient with the
+ * exact redo of near-ties), 128 tokens per CTA. */
 kv_status kv_debug_quantize_pack(const kv_params* p, int set, int tensor, const float* y_dev, int64_t n,
                                  uint32_t* rec_dev, int variant, kv_stream_t stream);
 /* Run the decoder's slot extraction over the records of n tokens (keys [n][r_words], values

@@ -52,9 +52,10 @@ attention; IEEE fp32 for the quantiser, whose op sequence is part of the record 
  8. Decode attention over the records: y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j) for b_j > 0, else
     mu_j; k^ = T^T y^ (and v^); o_h = softmax_t(alpha q_h . k^_t) v^ over t < seq_len, all in fp64.
 
-Readings where the pages are silent are listed in the repository's design notes (same bits/element for
-keys and values, orthogonal key KLT with query weighting in the allocation, mid-rise quantiser with bin
-centres, fp16 round-to-nearest-even, budget counting the scale/zero word, alpha = 1/sqrt(d)).
+Where the pages are silent this module takes the plainest reading the rest of them supports: the same
+bits/element for keys and values, an orthogonal key KLT with the query weighting in the allocation, a
+mid-rise quantiser with bin centres, fp16 round-to-nearest-even, a budget that counts the scale/zero word, and
+alpha = 1/sqrt(d).
 """
 from __future__ import annotations
 

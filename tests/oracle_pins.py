@@ -571,13 +571,65 @@ def pin_zero_bit_channels_are_the_mean():
     assert np.array_equal(yh[:, 6:], np.broadcast_to(mu[6:].astype(np.float64), (20, 10)))
 
 
+def half_rn_sat_bits(x32):
+    """Independent fp32 -> saturated fp16 conversion written from the IEEE 754 binary16 definition on the bit
+    patterns, with integer arithmetic only: the value of |x| counted in units of the binary16 quantum at its
+    exponent (2^(e - 10) for normal results, 2^-24 for subnormal ones), rounded to the nearest integer with ties
+    to even, the sign put back; magnitudes >= 65504 give +-65504 (saturation instead of infinity). Returns the
+    values as float64."""
+    u = np.asarray(x32, np.float32).view(np.uint32).astype(np.int64)
+    sign = np.where(u >> 31, -1.0, 1.0)
+    ex = (u >> 23) & 0xFF
+    frac = u & 0x7FFFFF
+    sig = np.where(ex > 0, frac | (1 << 23), frac)            # significand, value = sig 2^(e32 - 150)
+    e_unb = np.where(ex > 0, ex - 127, -126)                  # exponent of the leading bit position 23
+    lead = np.where(sig > 0, np.floor(np.log2(np.maximum(sig, 1))).astype(np.int64), 0)
+    e_val = e_unb + lead - 23                                 # floor(log2 |x|)
+    q_exp = np.maximum(e_val, -14) - 10                       # binary16 quantum exponent at that magnitude
+    shift = q_exp - (np.where(ex > 0, ex, 1) - 150)           # sig 2^(e32 - 150) / 2^q_exp = sig >> shift
+    out = np.empty(u.shape, np.float64)
+    for i in range(u.size):
+        s_i, sh, sg = int(shift.flat[i]), int(shift.flat[i]), int(sig.flat[i])
+        if sh <= 0:
+            n = sg << (-sh)
+        elif sh >= 62:
+            n = 0
+        else:
+            n, rem, half = sg >> sh, sg & ((1 << sh) - 1), 1 << (sh - 1)
+            if rem > half or (rem == half and n & 1):
+                n += 1
+        mag = float(n) * 2.0 ** int(q_exp.flat[i])
+        out.flat[i] = sign.flat[i] * min(mag, 65504.0)
+    return out
+
+
 def pin_half_conversion():
-    """fp32 -> fp16 round-to-nearest-even with saturation, per IEEE 754 binary16 (hand-picked values)."""
+    """fp32 -> fp16 round-to-nearest-even with saturation, per IEEE 754 binary16: hand-picked values; then the
+    oracle's converter against half_rn_sat_bits (written from the binary16 definition, integer arithmetic on the
+    bit patterns) on every one of the 2^16 binary16 values, every midpoint between neighbouring finite binary16
+    values (the ties) with the fp32 values one ulp either side of it, and a sweep of 2^17 fp32 bit patterns
+    spread over the whole range."""
     cases = [(1.0 + 2.0 ** -11, 1.0), (1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -9), (65519.0, 65504.0),
              (65520.0, 65504.0), (1e9, 65504.0), (-1e9, -65504.0), (2.0 ** -25, 0.0),
              (3 * 2.0 ** -26, 2.0 ** -24), (0.1, 0.0999755859375)]
     for x, want in cases:
         assert float(O.half_rn_sat(np.float32(x))) == want, (x, want)
+        assert float(half_rn_sat_bits(np.float32(x))) == want, (x, want)
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    fin = h[np.isfinite(h)].astype(np.float64)
+    allh = fin.astype(np.float32)                              # exact in fp32
+    srt = np.unique(fin)
+    mids = ((srt[1:] + srt[:-1]) / 2).astype(np.float32)       # exact in fp32 (one more bit than binary16)
+    assert np.array_equal((srt[1:] + srt[:-1]) / 2, mids.astype(np.float64))
+    mb = mids.view(np.uint32)
+    near = np.concatenate([mb - 1, mb + 1]).view(np.float32)
+    sweep = (np.arange(1 << 17, dtype=np.uint64) * 32749 % (1 << 32)).astype(np.uint32).view(np.float32)
+    sweep = sweep[np.isfinite(sweep)]
+    for xs in (allh, mids, near, sweep):
+        want = half_rn_sat_bits(xs)
+        got = O.half_rn_sat(xs).astype(np.float64)
+        bad = np.nonzero(got != want)[0]
+        assert bad.size == 0, (xs[bad[:5]], got[bad[:5]], want[bad[:5]])
 
 
 # --- decode ------------------------------------------------------------------------------------------

@@ -42,17 +42,74 @@ def _special_rows(p, rng, n=64):
     return rows.astype(np.float32)
 
 
-@pytest.mark.parametrize("variant", [0, 1])
+def _near_tie_rows(p, rng, n_rows=24):
+    """Rotated fp32 rows whose normalised coefficients sit on a quantiser bin edge or a few fp32 ulps from one.
+    In each row every coded channel other than the row's extremes (which fix z and s) is aimed at
+    y' = z + s k 2^-b_j for a random interior edge k, then moved ulp by ulp (17 candidates) to the y whose
+    quotient (y' - z) / s 2^b_j lands closest to k from the side the row asks for: just below, as close as fp32
+    gets, or just above."""
+    nz = np.nonzero(p.widths > 0)[0]
+    mu, inv, sg = p.mu, p.inv_sigma, p.sigma
+    rows = []
+    for r in range(n_rows):
+        y = (mu + sg * rng.normal(size=p.d).astype(np.float32) * 2).astype(np.float32)
+        yp = (y[nz] - mu[nz]) * inv[nz]
+        jmin, jmax = nz[np.argmin(yp)], nz[np.argmax(yp)]
+        z = np.float64(O.half_rn_sat(yp.min()))
+        s = np.float64(O.half_rn_sat(np.float32(yp.max() - np.float32(z))))
+        side = r % 3
+        for j in nz:
+            if j in (jmin, jmax):
+                continue
+            b = int(p.widths[j])
+            k = int(rng.integers(1, 2 ** b))
+            y0 = np.float32((z + s * k / 2.0 ** b) / np.float64(inv[j]) + np.float64(mu[j]))
+            bits0 = np.array([y0], np.float32).view(np.int32)[0]
+            best, bestd = y0, None
+            for step in range(-8, 9):
+                c = np.array([bits0 + step], np.int32).view(np.float32)[0]
+                d = (np.float64((c - mu[j]) * inv[j]) - z) / s * 2.0 ** b - k
+                ok, key = ((d < 0, -d), (True, abs(d)), (d >= 0, d))[side]
+                if ok and (bestd is None or key < bestd):
+                    best, bestd = c, key
+            y[j] = best
+        rows.append(y)
+    return np.array(rows, np.float32)
+
+
+def _reciprocal_only_codes(y, p):
+    """Codes of the coded channels as the reciprocal quotient alone would give them (u = (y' - z) (RN(1/s) 2^b),
+    clamped to [1/2, 2^b - 1/2], floored), i.e. without the tensor-core epilogue's exact redo of near-ties."""
+    nz = p.widths > 0
+    yp = (y[:, nz] - p.mu[nz]) * p.inv_sigma[nz]
+    z = O.half_rn_sat(yp.min(1)).astype(np.float32)
+    s = O.half_rn_sat(yp.max(1) - z).astype(np.float32)
+    tb = np.ldexp(np.ones(int(nz.sum()), np.float32), p.widths[nz].astype(np.int32))
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        u = (yp - z[:, None]) * ((np.float32(1) / s)[:, None] * tb[None, :])
+        c = np.floor(np.minimum(np.maximum(u, np.float32(0.5)), tb - np.float32(0.5)))
+    c[s == 0] = 0
+    return c.astype(np.int64)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
 @pytest.mark.parametrize("bits", [2.75, 1.33, 4.0, 8.0])
 def test_quantize_pack_bitexact(tiny, variant, bits):
+    """The three device quantisers (variant 0: warp per token, CUDA-core encode; 1: thread per token; 2: the
+    tensor-core encode's epilogue, run on coefficients stored into tensor memory) against the oracle's
+    quantiser and packer on the same fp32 rotated rows: bit-exact records. Rows: the tiny layer's rotated tokens,
+    the codec's corner cases (s = 0, saturation, subnormal z and s, -0, exact bin edges on a coarse grid) and
+    rows of near-ties; 1024 + 159 rows, so variant 2 also ends on a ragged tile."""
     w, L, _, _ = tiny
     sets = G.calibrate_oracle(L, bits, bits)
     P = G.lib_params(sets)
     rng = np.random.default_rng(100)
     for t, p in ((0, sets[0][0]), (1, sets[0][1])):
         x = synth.as_float(L.k[0, 0] if t == 0 else L.v[0, 0])
-        y = np.vstack([O.rotate(x, p), _special_rows(p, rng)])
+        y = np.vstack([O.rotate(x, p), _special_rows(p, rng), _near_tie_rows(p, rng)])
         ref = O.pack(*O.quantize(y, p), p)
+        if variant == 2:  # the near-tie rows do reach the exact redo: the reciprocal alone differs somewhere
+            assert np.count_nonzero(_reciprocal_only_codes(y, p) != O.quantize(y, p)[2][:, p.widths > 0]) > 0
         yd = torch.from_numpy(y).cuda()
         rec = torch.zeros(ref.shape, dtype=torch.int32, device="cuda")
         kvtc.kv_debug_quantize_pack(P, 0, t, yd, y.shape[0], rec, variant)
@@ -268,6 +325,61 @@ def test_append_matches_prefill(tiny):
                        kvtc.KV_DTYPE_F32, 1, 1, pos)
     assert kvtc.kv_check_status() == kvtc.KV_OK
     assert np.array_equal(G.u32(rk), rk_all) and np.array_equal(G.u32(rv), rv_all)
+
+
+def _value_token_raw(rec, t):
+    """Raw bits of token t in a value cache row [T_cap / 2, 2 R]: its z/s word (word t & 1 of its record) and
+    its 16-bit half (t & 1) of every code word."""
+    r = rec[t >> 1]
+    return np.concatenate([[r[t & 1]], (r[2:].astype(np.uint32) >> (16 * (t & 1))) & 0xFFFF])
+
+
+@pytest.mark.parametrize("wl,bits", [("llama_decode_32k", 2.75), ("qwen_batched_8k", 3.0)])
+def test_append_bf16_one_token_per_call_matches_oracle(wl, bits):
+    """The bf16 append kernel (t_new = 1 per call: the encode of every decode step) against the oracle. Two
+    sequences, 70 tokens each, appended one call at a time into a cache pre-filled with the oracle's records of
+    other tokens; sequence 0 starts at an even position and sequence 1 at an odd one, so the first and the last
+    value records are shared with a background token. Every appended token's record entries are within 1 LSB of
+    the oracle's with at most 1e-4 of them different; every other token of the cache, including the other half
+    of each shared value record, keeps its bits."""
+    w = synth.WORKLOADS[wl]
+    n_bg, n_app, T_cap, starts = 96, 70, 96, (4, 9)
+    L = synth.make_layer(w, T=n_bg + n_app, B=2, steps=1)
+    sets = G.calibrate_oracle(L, bits, bits)
+    P = G.lib_params(sets)
+    per_seq = L.per_seq_params
+    kf, vf = synth.as_float(L.k), synth.as_float(L.v)
+    bg_k, bg_v = G.oracle_cache(kf[:, :, :n_bg], vf[:, :, :n_bg], sets, per_seq, T_cap)
+    rk, rv = G.dev_u32(bg_k), G.dev_u32(bg_v)
+    cache = kvtc.make_cache(rk, rv, 2, w.Hkv, T_cap, per_seq)
+    kn = G.to_dev_storage(np.ascontiguousarray(L.k[:, :, n_bg:]))
+    vn = G.to_dev_storage(np.ascontiguousarray(L.v[:, :, n_bg:]))
+    for i in range(n_app):
+        pos = torch.tensor([starts[0] + i, starts[1] + i], dtype=torch.int64, device="cuda")
+        kvtc.kv_encode(P, cache, kn[:, :, i:i + 1].contiguous(), vn[:, :, i:i + 1].contiguous(), kvtc.KV_DTYPE_BF16,
+                       2, 1, pos)
+    assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
+    got_k, got_v = G.u32(rk), G.u32(rv)
+    n_diff, n_all = 0.0, 0
+    for b in range(2):
+        s0 = starts[b]
+        keep = [t for t in range(T_cap) if not s0 <= t < s0 + n_app]
+        for h in range(w.Hkv):
+            pk, pv = sets[G.set_index(b, h, w.Hkv, per_seq)]
+            for got, bg, x, p in ((got_k[b, h], bg_k[b, h], kf[b, h, n_bg:], pk),
+                                  (got_v[b, h], bg_v[b, h], vf[b, h, n_bg:], pv)):
+                z, s, c = O.unpack(got, p)
+                ref = O.unpack(O.encode(x, p), p)
+                tf, dz, ds, cf, dc, ef = G.token_diff((z[s0:s0 + n_app], s[s0:s0 + n_app], c[s0:s0 + n_app]),
+                                                      tuple(a[:n_app] for a in ref), p)
+                assert dc <= 1 and dz <= 1 and ds <= 1, (b, h, p.pairing, dz, ds, dc)
+                n = n_app * (int(np.count_nonzero(p.widths)) + 2)
+                n_diff += ef * n
+                n_all += n
+                raw = (lambda r, t: r[t]) if p.pairing == "channels" else _value_token_raw
+                for t in keep:
+                    assert np.array_equal(raw(got, t), raw(bg, t)), (b, h, p.pairing, t)
+    assert n_diff / n_all <= 1e-4, (n_diff / n_all, round(n_diff), n_all)
 
 
 def test_encode_out_of_range_position_is_reported(tiny):

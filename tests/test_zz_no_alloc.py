@@ -1,8 +1,10 @@
-"""kv_attend_decode_noalloc: decode attention for callers that cannot allocate device memory (a serving
-engine whose memory planner owns the whole GPU and only passes pointers and a stream, or code running under
-CUDA graph stream capture, where cudaMalloc is refused). It keeps its scratch in one static device array of
-the library, so its results must equal those of kv_attend_decode with a caller workspace, call after call,
-whatever a previous call left in that array.
+"""kv_attend_decode_noalloc: decode attention for callers that cannot allocate device memory around a call. One
+example is a serving engine whose memory planner owns the whole GPU and hands a kernel library only pointers
+and a stream. Another is code that runs inside an allocator or memory-pool callback, where calling cudaMalloc
+again would re-enter the allocator. The entry point keeps its scratch in one static device array of the library.
+Its split plan and its kernels are those of kv_attend_decode, so its results must equal those of
+kv_attend_decode with a caller workspace bit for bit, call after call, whatever a previous call left in that
+array; both must also match the oracle.
 
 This file is collected last so that a failure here stops a `-x` run only after every other test ran."""
 import math
@@ -28,12 +30,13 @@ def _case(name, T, B, bits, seq_lens):
     sets = G.calibrate_oracle(L, bits, bits)
     P = G.lib_params(sets)
     rk, rv = G.oracle_cache(synth.as_float(L.k), synth.as_float(L.v), sets, L.per_seq_params, T)
-    return w, L, P, rk, rv, seq_lens
+    return w, L, P, rk, rv, seq_lens, sets
 
 
 def _both(case):
-    """Output of the workspace entry point and of the no-allocation entry point on the same inputs."""
-    w, L, P, rk, rv, seq_lens = case
+    """Output of the workspace entry point and of the no-allocation entry point on the same inputs, and the
+    oracle's decode of the same records."""
+    w, L, P, rk, rv, seq_lens, sets = case
     B, Hkv, T_cap, _ = rk.shape
     tk, tv = G.dev_u32(rk), G.dev_u32(rv)
     cache = kvtc.make_cache(tk, tv, B, Hkv, T_cap, L.per_seq_params)
@@ -46,7 +49,8 @@ def _both(case):
     got = torch.full_like(ref, float("nan"))
     kvtc.kv_attend_decode_noalloc(P, cache, q, B, w.Hq, sl, scale, got)
     assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
-    return got.cpu().numpy().astype(np.float64), ref.cpu().numpy().astype(np.float64)
+    ora = G.oracle_decode(rk, rv, L.q[0], seq_lens, sets, w.Hq, L.per_seq_params)
+    return got.cpu().numpy(), ref.cpu().numpy(), ora
 
 
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
@@ -54,14 +58,15 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
     cases = [_case("llama_long_128k", 2048, 1, 1.33, [2000]),
              _case("qwen_batched_8k", 512, 2, 3.0, [512, 301])]
     for case in cases + cases[:1]:
-        got, ref = _both(case)
+        got, ref, ora = _both(case)
         assert np.all(np.isfinite(got))
-        err = G.rel_l2_rows(got, ref)
+        assert np.array_equal(got, ref), np.abs(got - ref).max()
+        err = G.rel_l2_rows(got.astype(np.float64), ora)
         assert err.max() <= DEC_TOL, err
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    w, L, P, rk, rv, _ = _case("llama_long_128k", 64, 1, 1.33, [64])
+    w, L, P, rk, rv, _, _ = _case("llama_long_128k", 64, 1, 1.33, [64])
     B, Hkv, T_cap = 256, w.Hkv, 64
     assert kvtc.kv_decode_workspace_bytes(P, B, Hkv, w.Hq, T_cap) > kvtc.NOALLOC_SCRATCH_BYTES
     tk = torch.zeros((B, Hkv, T_cap, P.record_words(0)), dtype=torch.int32, device="cuda")

@@ -297,7 +297,11 @@ kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int H
   kv_status st = launch_check("zero counters");
   if (st != KV_OK) return st;
   const size_t smem = decode_bf16_smem_bytes();
-  cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = ensure_dyn_smem((const void*)decode_bf16_kernel, smem);
+  if (e != cudaSuccess) {
+    set_error("decode_bf16_kernel shared memory: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
   decode_bf16_kernel<<<dim3(L.splits, Hkv, B), BTHREADS, smem, s>>>(a);
   return launch_check("decode_bf16_kernel");
 }

@@ -41,12 +41,76 @@ __global__ void __launch_bounds__(128) debug_qp_thread_kernel(ParamsDev P, int s
   }
 }
 
+// The tensor-core encode's quantiser and packer (tc_stage_channel + tc_quantize_pack_row, the functions
+// encode_tc_kernel's epilogue runs) on given fp32 rotated rows: one CTA of four warps per 128 tokens; thread = token
+// row, its coefficients stored into its tensor-memory lane by tcgen05.st where the encode's MMA would leave them.
+// Records as the other variants: keys [n][R]; values [ceil(n / 2)][2 R], token t in half t & 1, and a missing
+// second token's half left as it was.
+constexpr int DQ_TC_SMEM = 100 * 1024;  // also keeps at most two CTAs (256 tensor-memory columns) per SM
+__global__ void __launch_bounds__(128, 1) debug_qp_tc_kernel(ParamsDev P, int set, int tensor, const float* y,
+                                                             long long n, uint32_t* rec) {
+  extern __shared__ __align__(16) uint32_t stage[];
+  __shared__ __align__(16) float pmi[4 * (D / 2)], ptc[4 * (D / 2)], phh[D];
+  __shared__ __align__(16) uint32_t pbits[D];
+  __shared__ uint32_t s_tmem;
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid;
+  const TensorDev& td = P.t[tensor];
+  const int R = td.r_words, PK = R | 1, PV = 2 * R + 1;
+  const int words = tensor == 0 ? TC_TILE * PK : (TC_TILE / 2) * PV;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&s_tmem), 128);
+    tmem_relinquish();
+  }
+  tc_stage_channel(td, tensor, set, row, pmi, ptc, phh, pbits);
+  for (int i = tid; i < words; i += 128) stage[i] = 0u;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tacc = s_tmem + ((uint32_t)(32 * warp) << 16);
+  const long long t = (long long)blockIdx.x * TC_TILE + row;
+#pragma unroll 1
+  for (int cb = 0; cb < D / 16; ++cb) {
+    uint32_t v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = t < n ? __float_as_uint(y[(size_t)t * D + 16 * cb + i]) : 0u;
+    tmem_st_32x32b_x16(tacc + 16u * cb, v);
+  }
+  tmem_st_wait();
+  const int nz = td.nz[set];
+  uint32_t* const r = tensor == 0 ? stage + row * PK : stage + (row >> 1) * PV;
+  const uint32_t hsh = tensor == 0 ? 0u : 16u * (uint32_t)(row & 1);
+  const uint32_t zs = tc_quantize_pack_row(tacc, (nz + 15) >> 4, nz, pmi, ptc, phh, pbits, smem_u32(r), hsh);
+  r[tensor == 0 ? 0 : (row & 1)] = zs;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (t < n) {
+    if (tensor == 0) {
+      for (int w = 0; w < R; ++w) rec[(size_t)t * R + w] = r[w];
+    } else {
+      uint32_t* out = rec + (size_t)(t >> 1) * 2 * R;
+      const int hf = (int)(t & 1);
+      out[hf] = r[hf];
+      for (int w = 2; w < 2 * R; ++w)
+        reinterpret_cast<uint16_t*>(out)[2 * w + hf] = reinterpret_cast<const uint16_t*>(r)[2 * w + hf];
+    }
+  }
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(s_tmem, 128);
+}
+
 kv_status launch_debug_quantize_pack(const ParamsDev& P, int set, int tensor, const float* y, int64_t n,
                                      uint32_t* rec, int variant, cudaStream_t s) {
-  if (variant == 0)
+  if (variant == 0) {
     debug_qp_warp_kernel<<<(unsigned)((n + 7) / 8), 256, 0, s>>>(P, set, tensor, y, n, rec);
-  else
+  } else if (variant == 1) {
     debug_qp_thread_kernel<<<(unsigned)((n + 127) / 128), 128, 0, s>>>(P, set, tensor, y, n, rec);
+  } else {
+    static_assert(TC_TILE * (MAX_RW | 1) * 4 <= DQ_TC_SMEM && (TC_TILE / 2) * (2 * MAX_RW + 1) * 4 <= DQ_TC_SMEM,
+                  "record staging of one tile");
+    ensure_dyn_smem((const void*)debug_qp_tc_kernel, DQ_TC_SMEM);
+    debug_qp_tc_kernel<<<(unsigned)((n + TC_TILE - 1) / TC_TILE), 128, DQ_TC_SMEM, s>>>(P, set, tensor, y, n, rec);
+  }
   return launch_check("debug quantize/pack");
 }
 

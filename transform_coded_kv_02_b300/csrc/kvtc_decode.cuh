@@ -202,9 +202,12 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(ParamsDev P, DecArg
   const uint32_t stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
   uint64_t* tbar = &tbar_s;
 
-  const long long Lseq = min((long long)a.seq_lens[b], a.T_cap);
-  const long long t0 = (long long)split * a.chunk;
-  const long long t1 = min(t0 + (long long)a.chunk, Lseq);
+  // this sequence's tokens spread over all the splits: chunks of whole tiles sized from its own length, so a
+  // short sequence in a long cache (or in a ragged batch) keeps every split busy
+  const long long Lseq = max(0LL, min((long long)a.seq_lens[b], a.T_cap));
+  const long long chunk = ((Lseq + a.splits - 1) / a.splits + DT - 1) / DT * DT;
+  const long long t0 = (long long)split * chunk;
+  const long long t1 = min(t0 + chunk, Lseq);
   const int ntiles = t1 > t0 ? (int)((t1 - t0 + DT - 1) / DT) : 0;
 
   if (tid == 0) {
@@ -838,8 +841,8 @@ static int compile_time_record_words(int RK, int RV) {
 
 template <int NB, int RT, bool PIPE>
 static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a) {
-  cudaFuncSetAttribute(decode_kernel<NB, RT, PIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)cfg.dynamicSmemBytes);
+  const cudaError_t e = ensure_dyn_smem((const void*)decode_kernel<NB, RT, PIPE>, cfg.dynamicSmemBytes);
+  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RT, PIPE>, P, a);
 }
 

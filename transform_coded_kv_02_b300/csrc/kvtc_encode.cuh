@@ -164,13 +164,17 @@ kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, co
   if (t_new <= AP_MAX_TOKENS) {
     const size_t smem = append_smem_bytes();
     const dim3 grid((unsigned)(B * c.Hkv), 2);
-    if (dtype == KV_DTYPE_BF16) {
-      cudaFuncSetAttribute(encode_append_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      encode_append_kernel<true><<<grid, AP_THREADS, smem, s>>>(P, a);
-    } else {
-      cudaFuncSetAttribute(encode_append_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      encode_append_kernel<false><<<grid, AP_THREADS, smem, s>>>(P, a);
+    const void* fn = dtype == KV_DTYPE_BF16 ? (const void*)encode_append_kernel<true>
+                                            : (const void*)encode_append_kernel<false>;
+    const cudaError_t e = ensure_dyn_smem(fn, smem);
+    if (e != cudaSuccess) {
+      set_error("encode_append_kernel shared memory: %s", cudaGetErrorString(e));
+      return KV_ERR_CUDA;
     }
+    if (dtype == KV_DTYPE_BF16)
+      encode_append_kernel<true><<<grid, AP_THREADS, smem, s>>>(P, a);
+    else
+      encode_append_kernel<false><<<grid, AP_THREADS, smem, s>>>(P, a);
     return launch_check("encode_append_kernel");
   }
   const long long warps = 2LL * B * c.Hkv * t_new;

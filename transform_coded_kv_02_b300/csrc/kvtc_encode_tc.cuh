@@ -74,6 +74,122 @@ __device__ __forceinline__ bool group_all(int group, bool ok) {
   return r != 0;
 }
 
+// Channel parameters of one (tensor, set) for the epilogue, channel j = the calling thread's row: pmi float4 per
+// pair {mu, mu', 1/sigma, 1/sigma'} (1/sigma NaN at zero width, which min and max skip), ptc float4 per pair
+// {2^b, 2^b', 2^b - 1/2, 2^b' - 1/2}, phh {1/2 - 2^(b-21)}, pbits {byte offset of the code word in the record |
+// bit << 16} (keys: pair slot, the odd channel in the high half; values: channel slot of the record's earlier
+// token).
+__device__ __forceinline__ void tc_stage_channel(const TensorDev& td, int tensor, int set, int j, float* pmi,
+                                                 float* ptc, float* phh, uint32_t* pbits) {
+  const size_t so = (size_t)set * D;
+  const int w = td.widths[so + j];
+  const int jp = j >> 1, jo = j & 1;
+  pmi[4 * jp + jo] = td.mu[so + j];
+  pmi[4 * jp + 2 + jo] = w > 0 ? td.inv_sigma[so + j] : __int_as_float(0x7fc00000);  // NaN: out of min/max
+  ptc[4 * jp + jo] = exp2i(w);
+  ptc[4 * jp + 2 + jo] = (float)((1 << w) - 1) + 0.5f;
+  phh[j] = 0.5f - exp2i(w - 21);
+  uint32_t word, bit;
+  if (tensor == 0) {
+    const uint32_t dsc = td.slots[so + (j >> 1)];
+    word = 1u + (dsc & 255u);
+    bit = ((dsc >> 8) & 255u) + 16u * (uint32_t)(j & 1);
+  } else {
+    const uint32_t dsc = td.slots[so + j];
+    word = 2u + (dsc & 255u);
+    bit = (dsc >> 8) & 255u;
+  }
+  if (w == 0) bit = 0u;
+  pbits[j] = (4u * word) | (bit << 16);
+}
+
+// Quantise and pack one token whose rotated coefficients y_j sit in this thread's tensor-memory lane, columns
+// [0, 16 nblk) (the columns past nz hold zero-width channels). Whole warps call it (one token per thread).
+// Codes are OR-ed into the record at shared address rec_s (shifted by hsh: 16 for the later token of a value
+// record); returns the token's z/s word. Tensor memory is left holding y'.
+//   pass 1: y'_j = (y_j - mu_j) * (1/sigma_j), two channels at a time; min / max over b_j > 0; y' back to
+//           tensor memory; z = fp16(min), s = fp16(max - z).
+//   pass 2: the quantiser's code clamp(floor(RN((y' - z) / s) 2^b), 0, 2^b - 1) formed from
+//           u = RN((y' - z) * (RN(1/s) 2^b)), which differs from RN((y' - z) / s) 2^b by at most 3 units of
+//           2^-24 relative, i.e. by less than 2^(b-21) where it matters (|u| <= 2^b). u is clamped to
+//           [1/2, 2^b - 1/2] first, so floor() yields the clamped code and the clamp ends, being half-integers,
+//           are never ties. Only a clamped u within 2^(b-21) of an integer can give a different floor: such
+//           tokens are redone with the IEEE division, so the codes equal the quantiser's for the given y.
+__device__ __forceinline__ uint32_t tc_quantize_pack_row(uint32_t tacc, int nblk, int nz, const float* pmi,
+                                                         const float* ptc, const float* phh, const uint32_t* pbits,
+                                                         uint32_t rec_s, uint32_t hsh) {
+  float m = INFINITY, M = -INFINITY;
+  for (int cb = 0; cb < nblk; ++cb) {
+    uint32_t v[16];
+    tmem_ld_32x32b_x16(tacc + 16u * cb, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+      const float4 mi = reinterpret_cast<const float4*>(pmi)[8 * cb + jp];
+      const float2 yp = f2unpack(f2mul(f2sub(f2pack(__uint_as_float(v[2 * jp]), __uint_as_float(v[2 * jp + 1])),
+                                             f2pack(mi.x, mi.y)),
+                                       f2pack(mi.z, mi.w)));
+      m = fminf(m, fminf(yp.x, yp.y));
+      M = fmaxf(M, fmaxf(yp.x, yp.y));
+      v[2 * jp] = __float_as_uint(yp.x);
+      v[2 * jp + 1] = __float_as_uint(yp.y);
+    }
+    tmem_st_32x32b_x16(tacc + 16u * cb, v);
+  }
+  tmem_st_wait();
+  __half zh = __ushort_as_half(0), sh = __ushort_as_half(0);
+  if (nz > 0) {
+    zh = half_sat_rn(__fadd_rn(m, 0.f));
+    sh = half_sat_rn(__fsub_rn(M, __half2float(zh)));
+  }
+  const float zf = __half2float(zh), sf = __half2float(sh);
+  const bool coded = sf != 0.f;
+  const float rs = coded ? __frcp_rn(sf) : 0.f;
+  const uint64_t zz = f2pack(zf, zf), rr = f2pack(rs, rs), hv = f2pack(0.5f, 0.5f);
+  bool near = false;
+  for (int cb = 0; cb < nblk; ++cb) {
+    uint32_t v[16];
+    tmem_ld_32x32b_x16(tacc + 16u * cb, v);  // y'
+    tmem_ld_wait();
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+      const float4 tc = reinterpret_cast<const float4*>(ptc)[8 * cb + jp];
+      const float2 hh = reinterpret_cast<const float2*>(phh)[8 * cb + jp];
+      const uint2 pb = reinterpret_cast<const uint2*>(pbits)[8 * cb + jp];
+      float2 u = f2unpack(f2mul(f2sub(f2pack(__uint_as_float(v[2 * jp]), __uint_as_float(v[2 * jp + 1])), zz),
+                                f2mul(rr, f2pack(tc.x, tc.y))));
+      u.x = fminf(fmaxf(u.x, 0.5f), tc.z);
+      u.y = fminf(fmaxf(u.y, 0.5f), tc.w);
+      const float flx = floorf(u.x), fly = floorf(u.y);
+      const float2 t = f2unpack(f2sub(f2sub(f2pack(u.x, u.y), f2pack(flx, fly)), hv));
+      near |= (fabsf(t.x) > hh.x) | (fabsf(t.y) > hh.y);
+      red_or_shared(rec_s + (pb.x & 0xFFFFu), (uint32_t)flx << ((pb.x >> 16) + hsh));
+      red_or_shared(rec_s + (pb.y & 0xFFFFu), (uint32_t)fly << ((pb.y >> 16) + hsh));
+    }
+  }
+  near = near && coded;
+  if (__any_sync(0xffffffffu, near)) {  // rare: exact quotients for the near-tie tokens of this warp
+    for (int cb = 0; cb < nblk; ++cb) {
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(tacc + 16u * cb, v);
+      tmem_ld_wait();
+      if (near) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j = 16 * cb + jj;
+          const float tb = ptc[4 * (j >> 1) + (j & 1)], cm = ptc[4 * (j >> 1) + 2 + (j & 1)];
+          const uint32_t pb = pbits[j];
+          const float dq = __fsub_rn(__uint_as_float(v[jj]), zf);
+          const uint32_t fast = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(dq, __fmul_rn(rs, tb)), 0.5f), cm));
+          const uint32_t exact = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(__fdiv_rn(dq, sf), tb), 0.5f), cm));
+          if (fast != exact) red_xor_shared(rec_s + (pb & 0xFFFFu), (fast ^ exact) << ((pb >> 16) + hsh));
+        }
+      }
+    }
+  }
+  return (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
+}
+
 template <int NACC>
 __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
     encode_tc_kernel(ParamsDev P, EncTcArgs a, const __grid_constant__ CUtensorMap mx_k,
@@ -235,27 +351,7 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       const int R = td.r_words;
       const int b = bh / a.Hkv;
       if (unit_tkey(u) != cached_key) {  // this group's channel parameters (the group is idle here)
-        const int j = row;
-        const size_t so = (size_t)set * D;
-        const int w = td.widths[so + j];
-        const int jp = j >> 1, jo = j & 1;
-        pmi[4 * jp + jo] = td.mu[so + j];
-        pmi[4 * jp + 2 + jo] = w > 0 ? td.inv_sigma[so + j] : __int_as_float(0x7fc00000);  // NaN: out of min/max
-        ptc[4 * jp + jo] = exp2i(w);
-        ptc[4 * jp + 2 + jo] = (float)((1 << w) - 1) + 0.5f;
-        phh[j] = 0.5f - exp2i(w - 21);
-        uint32_t word, bit;
-        if (tensor == 0) {
-          const uint32_t dsc = td.slots[so + (j >> 1)];
-          word = 1u + (dsc & 255u);
-          bit = ((dsc >> 8) & 255u) + 16u * (uint32_t)(j & 1);
-        } else {
-          const uint32_t dsc = td.slots[so + j];
-          word = 2u + (dsc & 255u);
-          bit = (dsc >> 8) & 255u;
-        }
-        if (w == 0) bit = 0u;
-        pbits[j] = (4u * word) | (bit << 16);
+        tc_stage_channel(td, tensor, set, row, pmi, ptc, phh, pbits);
         cached_key = unit_tkey(u);
         named_bar(1 + g, 128);
       }
@@ -268,92 +364,13 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       }
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
-      // ---- pass 1: y'_j = (y_j - mu_j) / sigma_j two channels at a time, min / max over b_j > 0 (the others are
-      // NaN, which min and max skip); y' goes back to tensor memory for pass 2 ----
-      float m = INFINITY, M = -INFINITY;
-      for (int cb = 0; cb < nblk; ++cb) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tacc + 16u * cb, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int jp = 0; jp < 8; ++jp) {
-          const float4 mi = reinterpret_cast<const float4*>(pmi)[8 * cb + jp];
-          const float2 yp = f2unpack(f2mul(f2sub(f2pack(__uint_as_float(v[2 * jp]), __uint_as_float(v[2 * jp + 1])),
-                                                 f2pack(mi.x, mi.y)),
-                                           f2pack(mi.z, mi.w)));
-          m = fminf(m, fminf(yp.x, yp.y));
-          M = fmaxf(M, fmaxf(yp.x, yp.y));
-          v[2 * jp] = __float_as_uint(yp.x);
-          v[2 * jp + 1] = __float_as_uint(yp.y);
-        }
-        tmem_st_32x32b_x16(tacc + 16u * cb, v);
-      }
-      tmem_st_wait();
-      __half zh = __ushort_as_half(0), sh = __ushort_as_half(0);
-      if (nz > 0) {
-        zh = half_sat_rn(__fadd_rn(m, 0.f));
-        sh = half_sat_rn(__fsub_rn(M, __half2float(zh)));
-      }
-      const float zf = __half2float(zh), sf = __half2float(sh);
-      const bool coded = sf != 0.f;
-      const uint32_t zs = (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
-      // ---- pass 2: codes into this token's record words ----
-      // The quantiser's code clamp(floor(RN((y' - z) / s) 2^b), 0, 2^b - 1) is formed from
-      // u = RN((y' - z) * (RN(1/s) 2^b)), which differs from RN((y' - z) / s) 2^b by at most 3 units of 2^-24
-      // relative, i.e. by less than 2^(b-21) where it matters (|u| <= 2^b). u is clamped to [1/2, 2^b - 1/2]
-      // first, so floor() yields the clamped code and the clamp ends, being half-integers, are never ties. Only
-      // a clamped u within 2^(b-21) of an integer can give a different floor: such tokens are redone below with
-      // the IEEE division.
       const long long pos0 = a.dst_pos[b] + (long long)tile * TC_TILE;
       const int half = (int)((pos0 + row) & 1);
       const int lr = (row + (int)(pos0 & 1)) >> 1;  // local two-token record of a value token
       const int PK = R | 1, PV = 2 * R + 1;
       uint32_t* const rec = tensor == 0 ? stage + row * PK : stage + lr * PV;
-      const uint32_t rec_s = smem_u32(rec);
       const uint32_t hsh = tensor == 0 ? 0u : 16u * (uint32_t)half;  // value token: its half of each code word
-      const float rs = coded ? __frcp_rn(sf) : 0.f;
-      const uint64_t zz = f2pack(zf, zf), rr = f2pack(rs, rs), hv = f2pack(0.5f, 0.5f);
-      bool near = false;
-      for (int cb = 0; cb < nblk; ++cb) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tacc + 16u * cb, v);  // y'
-        tmem_ld_wait();
-#pragma unroll
-        for (int jp = 0; jp < 8; ++jp) {
-          const float4 tc = reinterpret_cast<const float4*>(ptc)[8 * cb + jp];
-          const float2 hh = reinterpret_cast<const float2*>(phh)[8 * cb + jp];
-          const uint2 pb = reinterpret_cast<const uint2*>(pbits)[8 * cb + jp];
-          float2 u = f2unpack(f2mul(f2sub(f2pack(__uint_as_float(v[2 * jp]), __uint_as_float(v[2 * jp + 1])), zz),
-                                    f2mul(rr, f2pack(tc.x, tc.y))));
-          u.x = fminf(fmaxf(u.x, 0.5f), tc.z);
-          u.y = fminf(fmaxf(u.y, 0.5f), tc.w);
-          const float flx = floorf(u.x), fly = floorf(u.y);
-          const float2 t = f2unpack(f2sub(f2sub(f2pack(u.x, u.y), f2pack(flx, fly)), hv));
-          near |= (fabsf(t.x) > hh.x) | (fabsf(t.y) > hh.y);
-          red_or_shared(rec_s + (pb.x & 0xFFFFu), (uint32_t)flx << ((pb.x >> 16) + hsh));
-          red_or_shared(rec_s + (pb.y & 0xFFFFu), (uint32_t)fly << ((pb.y >> 16) + hsh));
-        }
-      }
-      near = near && coded;
-      if (__any_sync(0xffffffffu, near)) {  // rare: exact quotients for the near-tie tokens of this warp
-        for (int cb = 0; cb < nblk; ++cb) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(tacc + 16u * cb, v);
-          tmem_ld_wait();
-          if (near) {
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int j = 16 * cb + jj;
-              const float tb = ptc[4 * (j >> 1) + (j & 1)], cm = ptc[4 * (j >> 1) + 2 + (j & 1)];
-              const uint32_t pb = pbits[j];
-              const float dq = __fsub_rn(__uint_as_float(v[jj]), zf);
-              const uint32_t fast = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(dq, __fmul_rn(rs, tb)), 0.5f), cm));
-              const uint32_t exact = (uint32_t)floorf(fminf(fmaxf(__fmul_rn(__fdiv_rn(dq, sf), tb), 0.5f), cm));
-              if (fast != exact) red_xor_shared(rec_s + (pb & 0xFFFFu), (fast ^ exact) << ((pb >> 16) + hsh));
-            }
-          }
-        }
-      }
+      const uint32_t zs = tc_quantize_pack_row(tacc, nblk, nz, pmi, ptc, phh, pbits, smem_u32(rec), hsh);
       // the accumulator is free for the next unit of this group
       tc_fence_before();
       __syncwarp();
@@ -483,7 +500,7 @@ static bool make_bf16_map(CUtensorMap* m, const void* ptr, unsigned long long ro
 template <int NACC>
 static cudaError_t launch_encode_tc_n(const ParamsDev& P, const EncTcArgs& a, const CUtensorMap* maps,
                                       uint32_t smem, cudaStream_t s, int grid) {
-  cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel<NACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem((const void*)encode_tc_kernel<NACC>, smem);
   if (e != cudaSuccess) return e;
   encode_tc_kernel<NACC><<<grid, (4 * NACC + 2) * 32, smem, s>>>(P, a, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
@@ -532,9 +549,7 @@ static kv_status launch_encode_tc(const ParamsDev& P, const kv_cache& c, const v
   }
   a.units = (int)units;
   a.wait_ns = g_wait_limit_ns;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int grid = (int)std::min<long long>(units, sm_count(dev));
+  const int grid = (int)std::min<long long>(units, sm_count(current_device()));
   const cudaError_t e = nacc == TC_NACC_MAX ? launch_encode_tc_n<TC_NACC_MAX>(P, a, maps, smem, s, grid)
                                             : launch_encode_tc_n<TC_NACC_MAX - 1>(P, a, maps, smem, s, grid);
   if (e != cudaSuccess) {

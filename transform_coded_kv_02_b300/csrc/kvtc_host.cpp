@@ -997,11 +997,13 @@ extern "C" size_t kv_decode_bf16_workspace_bytes(int B, int Hkv, int Hq, int64_t
 // ------------------------------------------------------------------------------------------------------
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-static kv_status check_params_on_device(const kv_params* p) {
+static kv_status check_params_on_device(const kv_params* p, int* dev_out = nullptr) {
   KV_REQUIRE(p, KV_ERR_INVALID_ARG, "null parameter table");
   KV_REQUIRE(p->dev_blob, KV_ERR_INVALID_ARG, "parameter table not uploaded (kv_params_upload)");
-  KV_REQUIRE(p->device == current_device(), KV_ERR_INVALID_ARG,
-             "parameter table uploaded to device %d, current device is %d", p->device, current_device());
+  const int dev = current_device();
+  KV_REQUIRE(p->device == dev, KV_ERR_INVALID_ARG, "parameter table uploaded to device %d, current device is %d",
+             p->device, dev);
+  if (dev_out) *dev_out = dev;
   return KV_OK;
 }
 
@@ -1042,9 +1044,9 @@ extern "C" kv_status kv_encode(const kv_params* p, const kv_cache* c, const void
 namespace kvtc {
 // Argument checks shared by the decode entry points (everything except the workspace).
 kv_status check_decode_args(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
-                            const int32_t* seq_lens_dev, float softmax_scale, const float* out) {
+                            const int32_t* seq_lens_dev, float softmax_scale, const float* out, int* dev) {
   kv_status st;
-  if ((st = check_params_on_device(p)) != KV_OK) return st;
+  if ((st = check_params_on_device(p, dev)) != KV_OK) return st;
   if ((st = check_cache(p, c, B)) != KV_OK) return st;
   KV_REQUIRE(q && seq_lens_dev && out, KV_ERR_INVALID_ARG, "null q, seq_lens or out");
   KV_REQUIRE(Hq >= c->Hkv && Hq % c->Hkv == 0, KV_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, c->Hkv);
@@ -1060,9 +1062,10 @@ extern "C" kv_status kv_attend_decode(const kv_params* p, const kv_cache* c, con
                                       void* workspace, size_t ws_bytes, kv_stream_t stream) {
   clear_error();
   kv_status st;
-  if ((st = kvtc::check_decode_args(p, c, q, B, Hq, seq_lens_dev, softmax_scale, out)) != KV_OK) return st;
+  int dev = 0;
+  if ((st = kvtc::check_decode_args(p, c, q, B, Hq, seq_lens_dev, softmax_scale, out, &dev)) != KV_OK) return st;
   KV_REQUIRE(workspace && aligned16(workspace), KV_ERR_INVALID_ARG, "workspace null or not 16-byte aligned");
-  const DecodeLayout L = kvtc::decode_layout(B, c->Hkv, Hq, c->T_cap, current_device());
+  const DecodeLayout L = kvtc::decode_layout(B, c->Hkv, Hq, c->T_cap, dev);
   KV_REQUIRE(ws_bytes >= L.total, KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
   return kvtc::launch_decode(p->dev, *c, q, B, Hq, seq_lens_dev, softmax_scale, out, workspace, L,
                              (cudaStream_t)stream);
@@ -1108,7 +1111,7 @@ extern "C" kv_status kv_debug_quantize_pack(const kv_params* p, int set, int ten
   clear_error();
   kv_status st;
   if ((st = check_params_on_device(p)) != KV_OK) return st;
-  KV_REQUIRE(set >= 0 && set < p->n_sets && (tensor == 0 || tensor == 1) && n >= 0 && (variant == 0 || variant == 1),
+  KV_REQUIRE(set >= 0 && set < p->n_sets && (tensor == 0 || tensor == 1) && n >= 0 && variant >= 0 && variant <= 2,
              KV_ERR_INVALID_ARG, "kv_debug_quantize_pack: bad argument");
   if (n == 0) return KV_OK;
   KV_REQUIRE(y_dev && rec_dev, KV_ERR_INVALID_ARG, "null buffer");

@@ -68,8 +68,9 @@ DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device);
 kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
                         const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
                         cudaStream_t s);
+// (dev: receives the current device, which holds the parameter table)
 kv_status check_decode_args(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
-                            const int32_t* seq_lens_dev, float softmax_scale, const float* out);
+                            const int32_t* seq_lens_dev, float softmax_scale, const float* out, int* dev);
 kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap,
                              const void* q, const int32_t* seq_lens, float scale, float* out, void* ws,
                              const DecodeLayout& L, cudaStream_t s);

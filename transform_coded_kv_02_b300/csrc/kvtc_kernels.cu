@@ -24,7 +24,10 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "kvtc_codec.cuh"
 #include "kvtc_internal.h"
@@ -61,10 +64,39 @@ __device__ __forceinline__ float bf16_bits_f(uint32_t b) { return __uint_as_floa
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// SM count of a device, queried once per device.
 static int sm_count(int device) {
+  static std::atomic<int> cached[64];
+  const bool slot = device >= 0 && device < 64;
+  if (slot) {
+    const int v = cached[device].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
   int n = 148;
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
-  return n > 0 ? n : 148;
+  n = n > 0 ? n : 148;
+  if (slot) cached[device].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+static int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+
+// Raise a kernel's dynamic shared-memory ceiling on the current device, once: cudaFuncSetAttribute runs only
+// when a launch asks for more than the value last set for that (kernel, device).
+static cudaError_t ensure_dyn_smem(const void* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> set_to;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& cur = set_to[{fn, dev}];
+  if (bytes <= cur) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
 }
 
 }  // namespace kvtc
@@ -88,13 +120,8 @@ constexpr int NOALLOC_MAX_DEVICES = 64;
 static std::mutex g_noalloc_mu;
 static void* g_noalloc_addr[NOALLOC_MAX_DEVICES] = {};
 
-static kv_status noalloc_scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    set_error("cudaGetDevice: %s", cudaGetErrorString(e));
-    return KV_ERR_CUDA;
-  }
+// dev: the current device (the lookup must run with it current)
+static kv_status noalloc_scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) {
     set_error("device %d beyond the %d devices the static scratch table covers", dev, NOALLOC_MAX_DEVICES);
     return KV_ERR_UNSUPPORTED;
@@ -102,7 +129,7 @@ static kv_status noalloc_scratch_address(void** out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_addr[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p) {
       set_error("cudaGetSymbolAddress(static scratch) on device %d: %s", dev, cudaGetErrorString(e));
       return KV_ERR_CUDA;
@@ -119,13 +146,9 @@ extern "C" kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache
                                               const int32_t* seq_lens_dev, float softmax_scale, float* out,
                                               kv_stream_t stream) {
   kvtc::clear_error();
-  kv_status st = kvtc::check_decode_args(p, c, q, B, Hq, seq_lens_dev, softmax_scale, out);
-  if (st != KV_OK) return st;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    kvtc::set_error("cudaGetDevice failed");
-    return KV_ERR_CUDA;
-  }
+  kv_status st = kvtc::check_decode_args(p, c, q, B, Hq, seq_lens_dev, softmax_scale, out, &dev);
+  if (st != KV_OK) return st;
   const kvtc::DecodeLayout L = kvtc::decode_layout(B, c->Hkv, Hq, c->T_cap, dev);
   if (L.total > (size_t)KV_NOALLOC_SCRATCH_BYTES) {
     kvtc::set_error("decode of B=%d Hkv=%d T_cap=%lld needs %zu bytes of scratch, more than the library's fixed "
@@ -134,7 +157,7 @@ extern "C" kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache
     return KV_ERR_INVALID_ARG;
   }
   void* ws = nullptr;
-  if ((st = kvtc::noalloc_scratch_address(&ws)) != KV_OK) return st;
+  if ((st = kvtc::noalloc_scratch_address(dev, &ws)) != KV_OK) return st;
   return kvtc::launch_decode(p->dev, *c, q, B, Hq, seq_lens_dev, softmax_scale, out, ws, L, (cudaStream_t)stream);
 }
 
