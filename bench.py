@@ -330,7 +330,7 @@ def run_ours(args, rank, world, local_rank):
     pos_all = (T + torch.arange(n_new, dtype=torch.int64, device=dev)).repeat_interleave(B).view(n_new, B)
     seq_all = (pos_all + 1).to(torch.int32)
     out = torch.zeros((B, Hq, d), dtype=torch.float32, device=dev)
-    ws = torch.empty(kvtc.kv_decode_workspace_bytes(P, B, Hkv, Hq, T_cap), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(kvtc.kv_decode_workspace_bytes(P, B, Hkv, Hq, T_cap), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(d)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
@@ -489,7 +489,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": workload_name(w, rk_w, rv_w),
                    "l2": "flushed before every timed step (2 x L2 buffer written, outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single gpu"},
-        "roofline": {"bound": "hbm", "kernel": "kv_attend_decode (qprep_kernel + decode_kernel)",
+        "roofline": {"bound": "hbm", "kernel": "kv_attend_decode (decode_kernel)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "frac_of_nominal_8tbs": achieved / 8000.0,
                      "traffic": recorded_traffic(), "algorithmic_bytes_per_launch": dec_bytes_avg,

@@ -187,18 +187,21 @@ kv_status kv_encode(const kv_params* p, const kv_cache* cache, const void* k, co
  *   q: device bf16 [B][Hq][d]; seq_lens_dev: device int32 [B], 1 <= seq_len <= T_cap (0 gives zeros);
  *   out: device fp32 [B][Hq][d]; softmax_scale (alpha) typically 1/sqrt(d).
  *   o_h = sum_t softmax_t(alpha q_h . k^_t) v^_t, k^ = T_K^T y^ with y^_j = mu_j + sigma_j (z + (c_j + 1/2)
- *   s 2^-b_j) for b_j > 0 and mu_j otherwise (v^ likewise). Computed in the rotated bases: q is rotated
- *   once per call; each split of the tokens maps its partial sum back to the original basis (T_V^T, folded
- *   with sigma and 2^-b), and the splits are merged with their softmax weights. Kernels: a q-preparation kernel
- *   (which waits for the previous kernel of the stream, e.g. an append, before reading q) and the split-K
- *   decode kernel, launched as its programmatic dependant.
- *   Arithmetic: codes enter fp16 tensor-core MMAs exactly (c + 1/2); q' (scaled per head by a power of two so
- *   that it stays clear of fp16 subnormals) is carried as an fp16 hi + lo pair, p s_V likewise; each 16-token
- *   product sum starts from zero and the running sums are kept in fp32 with round-to-nearest arithmetic; the
- *   softmax runs in base 2 on the hardware exponential. Result: within 2e-3 relative L2 of the exact decode
- *   of the same records (measured 1e-5 to 2e-5 on the workloads' full-size layers).
- *   workspace: device, at least kv_decode_workspace_bytes(...) bytes, 16-byte aligned, reused across
- *   calls (no initialisation needed); calls that share a workspace must not overlap on the device. */
+ *   s 2^-b_j) for b_j > 0 and mu_j otherwise (v^ likewise). Computed in the rotated bases: each CTA rotates
+ *   q for its (sequence, KV head) in its prologue; each split of the tokens maps its partial sum back to the
+ *   original basis (T_V^T folded with sigma), and the last split to finish merges the splits with their
+ *   softmax weights. One kernel launch, as a programmatic dependant of the previous kernel of the stream (an
+ *   append, say): it reads q and the records only after that kernel has completed.
+ *   Arithmetic: each code enters an fp16 tensor-core MMA exactly, as 1 + c 2^-w (w: its slot's width), and the
+ *   affine terms of the dequantisation are folded into per-head constants; q's coefficients (scaled per head
+ *   by a power of two so that they stay clear of fp16 subnormals) are carried as fp16 hi + lo pairs, p s_V
+ *   likewise; each 32-token product sum starts from zero and the running sums are kept in fp32 with
+ *   round-to-nearest arithmetic; the softmax runs in base 2 on the hardware exponential. Result: within 2e-3
+ *   relative L2 of the exact decode of the same records.
+ *   workspace: device, at least kv_decode_workspace_bytes(...) bytes, 16-byte aligned, zero-filled before its
+ *   first use (it holds one arrival counter per (sequence, KV head), which every call leaves at zero, so the
+ *   workspace is reused across calls without clearing); calls that share a workspace must not overlap on the
+ *   device. */
 size_t kv_decode_workspace_bytes(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap);
 kv_status kv_attend_decode(const kv_params* p, const kv_cache* cache, const void* q, int B, int Hq,
                            const int32_t* seq_lens_dev, float softmax_scale, float* out,
@@ -216,9 +219,10 @@ kv_status kv_attend_decode(const kv_params* p, const kv_cache* cache, const void
  *   allocating library routine.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
  *   current; make that first call before any stream capture.
- *   Every call shares the one array and leaves its contents behind; each call resets the arrival counters
- *   it needs before using them. Calls whose kernels overlap on the GPU (other streams, other host threads)
- *   race on the array: serialise them. */
+ *   Every call shares the one array and leaves its contents behind. The array starts zeroed (static device
+ *   storage) and every call leaves the arrival counters in it at zero, which is the state the next call
+ *   needs; the split partials are written before they are read. Calls whose kernels overlap on the GPU (other
+ *   streams, other host threads) race on the array: serialise them. */
 #define KV_NOALLOC_SCRATCH_BYTES (4u << 20)
 kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache* cache, const void* q, int B, int Hq,
                                    const int32_t* seq_lens_dev, float softmax_scale, float* out,

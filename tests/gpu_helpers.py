@@ -83,7 +83,7 @@ def run_decode(P, rk, rv, q_bits, seq_lens, Hq, per_seq, scale=None, T_cap=None)
     sl = torch.tensor(seq_lens, dtype=torch.int32, device=DEV)
     out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device=DEV)
     wsb = kvtc.kv_decode_workspace_bytes(P, B, Hkv, Hq, Tc)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)  # zero-filled before first use (arrival counters)
     kvtc.kv_attend_decode(P, cache, q, B, Hq, sl, scale, out, ws)
     assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
     return out.cpu().numpy().astype(np.float64)

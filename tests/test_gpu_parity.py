@@ -490,8 +490,8 @@ def test_decode_bf16_comparator_matches_exact_attention():
 
 @pytest.mark.parametrize("seq_len", [1, 63, 1000, 2048])
 def test_decode_llama_shape_all_key_blocks(seq_len):
-    """Llama-shaped keys fill all eight 16-channel blocks, which selects the software-pipelined key loop; ragged
-    lengths exercise its partial last tile."""
+    """Llama-shaped keys fill all eight 16-channel blocks (the decode's eight-block kernel); ragged lengths exercise
+    its partial last stage."""
     w = synth.WORKLOADS["llama_decode_32k"]
     L = synth.make_layer(w, T=2048, steps=1)
     sets = G.calibrate_oracle(L, 2.75, 2.75)
@@ -504,7 +504,7 @@ def test_decode_llama_shape_all_key_blocks(seq_len):
 @pytest.mark.parametrize("wl,bits", [("llama_decode_32k", 8.0), ("qwen_batched_8k", 6.0)])
 def test_decode_runtime_record_length(wl, bits):
     """Record lengths without a compile-time kernel (32 words at 8 bits per element, 24 at 6) run the decode with
-    run-time record strides: one column block and the pipelined key loop on the Llama shape, two column blocks
+    run-time record strides: one column block on the Llama shape, two column blocks
     on the Qwen shape, ragged lengths. The wide codes also give the smallest q' entries (sigma_j 2^-b_j near
     1e-6), which the per-head power-of-two scaling of q' keeps out of the fp16 subnormal range."""
     w = synth.WORKLOADS[wl]
@@ -732,7 +732,7 @@ def test_prefill_stack_full_size_sampled():
         q = G.to_dev_storage(Ld.q[0])
         sl = torch.full((B,), T, dtype=torch.int32, device="cuda")
         out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
-        ws = torch.empty(kvtc.kv_decode_workspace_bytes(P, B, Hkv, Hq, T), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(kvtc.kv_decode_workspace_bytes(P, B, Hkv, Hq, T), dtype=torch.uint8, device="cuda")
         kvtc.kv_attend_decode(P, cache, q, B, Hq, sl, scale, out, ws)
         assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
         o = out.cpu().numpy().astype(np.float64)

@@ -44,7 +44,7 @@ def _both(case):
     sl = torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
     scale = 1.0 / math.sqrt(w.d)
     ref = torch.full((B, w.Hq, w.d), float("nan"), dtype=torch.float32, device="cuda")
-    ws = torch.empty(kvtc.kv_decode_workspace_bytes(P, B, Hkv, w.Hq, T_cap), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(kvtc.kv_decode_workspace_bytes(P, B, Hkv, w.Hq, T_cap), dtype=torch.uint8, device="cuda")
     kvtc.kv_attend_decode(P, cache, q, B, w.Hq, sl, scale, ref, ws)
     got = torch.full_like(ref, float("nan"))
     kvtc.kv_attend_decode_noalloc(P, cache, q, B, w.Hq, sl, scale, got)

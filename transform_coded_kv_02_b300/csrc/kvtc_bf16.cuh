@@ -257,7 +257,6 @@ DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device) {
   split_plan(B, Hkv, T_cap, device, BDT, 2, 1 << 20, &L.splits, &L.chunk);
   const size_t bh = (size_t)B * Hkv;
   size_t o = 0;
-  L.off_qa = L.off_qc = 0;
   L.off_cnt = o;
   o = align256(o + bh * sizeof(unsigned));
   L.off_part = o;

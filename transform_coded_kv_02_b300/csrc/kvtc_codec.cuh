@@ -167,22 +167,4 @@ __device__ __forceinline__ void quantize_pack_thread(const TensorDev& td, int se
   for (int w = tokens ? 2 : 1; w < W; ++w) emit(w, acc[w]);
 }
 
-// ------------------------------------------------------------------------------------------------------
-// decode-side extraction of one slot -> an fp16 pair holding (c + 1/2) exactly: the slot's code word shifted
-// right by the slot's bit leaves the low-half code at bit 0 and the high-half code at bit 16 (key slot:
-// channels 2k, 2k+1 of a token; value slot: channel j of the record's two tokens); both are masked and OR-ed
-// under the fp16 exponent of 1024 (0x6400: value 1024 + c for c < 1024), then 1023.5 is subtracted, exactly.
-// ------------------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t slot_mask(uint32_t desc) {
-  const uint32_t b0 = (desc >> 16) & 255u, b1 = desc >> 24;
-  return ((1u << b0) - 1u) | (((1u << b1) - 1u) << 16);
-}
-
-__device__ __forceinline__ uint32_t unpack_pair(uint32_t word, uint32_t r, uint32_t m) {
-  const uint32_t h = ((word >> r) & m) | 0x64006400u;
-  const __half2 off = __halves2half2(__ushort_as_half(0x63FF), __ushort_as_half(0x63FF));  // 1023.5
-  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), off);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 }  // namespace kvtc

@@ -114,9 +114,9 @@ kv_status launch_debug_quantize_pack(const ParamsDev& P, int set, int tensor, co
   return launch_check("debug quantize/pack");
 }
 
-// The decoder's slot extraction (unpack_pair) over records: one thread per (record, slot); writes integer
-// codes [n tokens][128]. Keys: slot k of token t gives channels 2k, 2k+1; values: slot j of record p gives
-// channel j of tokens 2p, 2p+1.
+// The decoder's slot extraction (slot_f16x2) over records: one thread per (record, slot); writes integer codes
+// [n tokens][128], c = (A - 1) 2^w of each fp16 value A = 1 + c 2^-w. Keys: slot k of token t gives channels
+// 2k, 2k+1; values: slot j of record p gives channel j of tokens 2p, 2p+1.
 __global__ void __launch_bounds__(128) debug_unpack_kernel(ParamsDev P, int set, int tensor, const uint32_t* rec,
                                                            long long n, uint16_t* codes) {
   const TensorDev& td = P.t[tensor];
@@ -128,17 +128,20 @@ __global__ void __launch_bounds__(128) debug_unpack_kernel(ParamsDev P, int set,
   const long long r = idx / n_slot;
   const int k = (int)(idx - r * n_slot);
   const uint32_t desc = td.slots[(size_t)set * D + k];
-  const uint32_t u = desc & 255u, sh = (desc >> 8) & 255u;
+  const uint32_t u = desc & 255u, b0 = (desc >> 16) & 255u, b1 = desc >> 24, w = b0 > b1 ? b0 : b1;
+  uint32_t dd, mm;
+  slot_decode_desc(0u, (desc >> 8) & 255u, w, b0, b1, dd, mm);
+  const float sc = exp2i((int)w);
   if (tensor == 0) {
-    const uint32_t h2 = unpack_pair(rec[r * R + 1 + u], sh, slot_mask(desc));
+    const uint32_t h2 = slot_f16x2(rec[r * R + 1 + u], dd, mm);
     const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-    codes[r * D + 2 * k] = (uint16_t)(__low2float(hv) - 0.5f);
-    codes[r * D + 2 * k + 1] = (uint16_t)(__high2float(hv) - 0.5f);
+    codes[r * D + 2 * k] = (uint16_t)((__low2float(hv) - 1.f) * sc);
+    codes[r * D + 2 * k + 1] = (uint16_t)((__high2float(hv) - 1.f) * sc);
   } else {
-    const uint32_t h2 = unpack_pair(rec[r * 2 * R + 2 + u], sh, slot_mask(desc));
+    const uint32_t h2 = slot_f16x2(rec[r * 2 * R + 2 + u], dd, mm);
     const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-    codes[(2 * r) * D + k] = (uint16_t)(__low2float(hv) - 0.5f);
-    if (2 * r + 1 < n) codes[(2 * r + 1) * D + k] = (uint16_t)(__high2float(hv) - 0.5f);
+    codes[(2 * r) * D + k] = (uint16_t)((__low2float(hv) - 1.f) * sc);
+    if (2 * r + 1 < n) codes[(2 * r + 1) * D + k] = (uint16_t)((__high2float(hv) - 1.f) * sc);
   }
 }
 

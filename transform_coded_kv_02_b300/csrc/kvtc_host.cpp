@@ -723,7 +723,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     blob.resize(off + bytes);
     return Piece{off, bytes};
   };
-  Piece pT[2], pTT[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], pnz[2], psl[2], psc[2], pws[2];
+  Piece pT[2], pTT[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], pnz[2], psl[2], psc[2], pws[2], pws2[2],
+      psmx[2];
   for (int t = 0; t < 2; ++t) {
     pT[t] = reserve((size_t)S * d * d * 4);
     pTT[t] = reserve((size_t)S * d * d * 4);
@@ -734,6 +735,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     pbase[t] = reserve((size_t)S * d * 4);
     psc[t] = reserve((size_t)S * d * d * 4);
     pws[t] = reserve((size_t)S * d * 4);
+    pws2[t] = reserve((size_t)S * d * 4);
+    psmx[t] = reserve((size_t)S * 4);
     pw[t] = reserve((size_t)S * d);
     pnz[t] = reserve((size_t)S * 4);
     psl[t] = reserve((size_t)S * d * 4);
@@ -748,6 +751,8 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     float* base = (float*)&blob[pbase[t].off];
     float* tsc = (float*)&blob[psc[t].off];
     float* wsum = (float*)&blob[pws[t].off];
+    float* wsum2 = (float*)&blob[pws2[t].off];
+    float* smx = (float*)&blob[psmx[t].off];
     uint8_t* w8 = (uint8_t*)&blob[pw[t].off];
     int32_t* nz = (int32_t*)&blob[pnz[t].off];
     uint32_t* sl = (uint32_t*)&blob[psl[t].off];
@@ -785,18 +790,32 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
         for (int j = 0; j < d; ++j) acc += (double)Tsrc[(size_t)j * d + k] * (double)p->mu[t][(size_t)s * d + j];
         base[(size_t)s * d + k] = (float)acc;
       }
-      // scaled rows T'[j][k] = T[j][k] sigma_j 2^-b_j and w_k = sum_{b_j > 0} T[j][k] sigma_j: the decode maps a
-      // split's rotated-basis value sums into the original basis with them
+      // The decode's folded constants. Slot width w_j: the wider code width of a key channel pair (both channels
+      // share one slot), b_j itself for values. Scaled rows T'[j][k] = T[j][k] sigma_j (0 for zero-width rows);
+      // w_k = sum_{b_j > 0} T[j][k] sigma_j; w2_k = sum_{b_j > 0} T[j][k] sigma_j (2^(w_j - b_j) - 2^(-b_j - 1));
+      // smax = max_{b_j > 0} sigma_j 2^(w_j - b_j). Keys: q.w, q.w2 and smax give the logit constants and the
+      // scale of the q coefficients; values: the rows and vectors map rotated-basis sums to the original basis.
+      std::vector<int> slotw(d);
+      for (int j = 0; j < d; ++j) slotw[j] = t == 0 ? std::max(wv[j], wv[j ^ 1]) : wv[j];
+      double smax = 0.0;
+      for (int j = 0; j < d; ++j)
+        if (wv[j] > 0)
+          smax = std::max(smax, (double)p->sigma[t][(size_t)s * d + j] * std::ldexp(1.0, slotw[j] - wv[j]));
+      smx[s] = (float)smax;
       for (int k = 0; k < d; ++k) {
-        double wacc = 0.0;
+        double wacc = 0.0, wacc2 = 0.0;
         for (int j = 0; j < d; ++j) {
           const double tj = (double)Tsrc[(size_t)j * d + k];
           const double sj = (double)p->sigma[t][(size_t)s * d + j];
           const int bj = wv[j];
-          tsc[(size_t)s * d * d + (size_t)j * d + k] = bj > 0 ? (float)(tj * sj * std::ldexp(1.0, -bj)) : 0.f;
-          if (bj > 0) wacc += tj * sj;
+          tsc[(size_t)s * d * d + (size_t)j * d + k] = bj > 0 ? (float)(tj * sj) : 0.f;
+          if (bj > 0) {
+            wacc += tj * sj;
+            wacc2 += tj * sj * (std::ldexp(1.0, slotw[j] - bj) - std::ldexp(1.0, -bj - 1));
+          }
         }
         wsum[(size_t)s * d + k] = (float)wacc;
+        wsum2[(size_t)s * d + k] = (float)wacc2;
       }
       int word[D], pos[D];
       uint32_t* sls = sl + (size_t)s * d;
@@ -834,12 +853,15 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     td.base = (const float*)(b + pbase[t].off);
     td.Tsc = (const float*)(b + psc[t].off);
     td.wsum = (const float*)(b + pws[t].off);
+    td.wsum2 = (const float*)(b + pws2[t].off);
+    td.smax = (const float*)(b + psmx[t].off);
     td.widths = (const uint8_t*)(b + pw[t].off);
     td.nz = (const int32_t*)(b + pnz[t].off);
     td.slots = (const uint32_t*)(b + psl[t].off);
     td.r_words = p->r_words[t];
     const int32_t* nzh = (const int32_t*)&blob[pnz[t].off];
     td.min_nz = S > 0 ? *std::min_element(nzh, nzh + S) : 0;
+    td.max_nz = S > 0 ? *std::max_element(nzh, nzh + S) : 0;
   }
   p->dev.n_sets = S;
   return KV_OK;

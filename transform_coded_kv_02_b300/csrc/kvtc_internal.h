@@ -29,8 +29,11 @@ struct TensorDev {
   const float* sigma;              // [S][D]
   const float* inv_sigma;          // [S][D]  fp32(1/sigma) computed in double; 0 for zero-width
   const float* base;               // [S][D]  T^T mu (original-basis vector of the all-mean record)
-  const float* Tsc;                // [S][D][D]  T[j][k] sigma_j 2^-b_j (0 for zero-width rows)
+  const float* Tsc;                // [S][D][D]  T[j][k] sigma_j (0 for zero-width rows)
   const float* wsum;               // [S][D]  sum over b_j > 0 of T[j][k] sigma_j
+  const float* wsum2;              // [S][D]  sum over b_j > 0 of T[j][k] sigma_j (2^(w_j - b_j) - 2^(-b_j - 1)),
+                                   //         w_j = slot width (keys: the pair's wider width; values: b_j)
+  const float* smax;               // [S]     max over b_j > 0 of sigma_j 2^(w_j - b_j)
   const uint8_t* widths;           // [S][D]
   const int32_t* nz;               // [S]     1 + last storage channel with width > 0
   const uint32_t* slots;           // [S][D] slots: code word | bit << 8 | b_lo << 16 | b_hi << 24; keys: entry k =
@@ -38,6 +41,7 @@ struct TensorDev {
                                    // channel j of a two-token record (code words start at record word 2)
   int r_words;                     // record words per token (same for every set)
   int min_nz;                      // smallest nz over the sets
+  int max_nz;                      // largest nz over the sets
 };
 
 struct ParamsDev {
@@ -60,8 +64,8 @@ kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, co
                         int B, int64_t t_new, const int64_t* dst_pos, int path, cudaStream_t s);
 struct DecodeLayout {
   int splits;
-  int chunk;                  // tokens per split, multiple of the decode tile
-  size_t off_qa, off_qc, off_cnt, off_part, total;
+  int chunk;                  // tokens per split at full capacity, multiple of the decode tile
+  size_t off_cnt, off_part, total;
 };
 DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device);
 DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device);

@@ -3,8 +3,8 @@
 //                      FMAs, then the warp quantiser/packer (append and fp32 inputs)
 //  kvtc_encode_tc.cuh  encode_tc_kernel: 128-token tiles staged by TMA, y = X T^T on the tensor cores (tcgen05,
 //                      split-bf16 T, fp32 accumulators in tensor memory), thread-per-token quantiser/packer
-//  kvtc_decode.cuh     qprep_kernel (q~ = T_K q and the folded logit constants) and decode_kernel (split-K
-//                      flash-decode over the packed records: bulk-copy ring, codes unpacked straight into warp-MMA
+//  kvtc_decode.cuh     decode_kernel (split-K flash-decode over the packed records: q~ = T_K q and the folded
+//                      logit constants in the prologue, bulk-copy ring, codes unpacked straight into warp-MMA
 //                      operands, key warps for logits and softmax, value warps for P.V, per-split inverse
 //                      rotation, last-CTA merge of the splits)
 //  kvtc_bf16.cuh       decode_bf16_kernel: the same split-K structure over an uncompressed bf16 cache
@@ -17,7 +17,8 @@
 // Decode algebra (rotated domain). With y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j) for b_j > 0:
 //   a q.k^ = a (T q).y^ = C0 + z C1 + s sum_{b_j>0} q'_j (c_j + 1/2)
 //   sum_t p_t v^_t = T_V^T o^,  o^_j = mu_j + sigma_j (Z + 2^-b_j A_j) / l for b_j > 0 (mu_j otherwise),
-//   Z = sum_t p_t z_t, A_j = sum_t p_t s_t (c_tj + 1/2), l = sum_t p_t.
+//   Z = sum_t p_t z_t, A_j = sum_t p_t s_t (c_tj + 1/2), l = sum_t p_t;
+// kvtc_decode.cuh states the form the kernel evaluates (codes entering the MMA as 1 + c 2^-w).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

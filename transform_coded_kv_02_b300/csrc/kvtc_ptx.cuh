@@ -58,6 +58,21 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+// Wait for the phase with the given parity, polling with a sleep of sleep_ns between tests (a waiter that sleeps
+// leaves the issue slots to the other warps of its scheduler); gives up after limit_ns nanoseconds, records
+// ST_TIMEOUT in the device status word and returns false.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, long long limit_ns, uint32_t sleep_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_test(bar, parity)) return true;
+    if ((long long)(global_ns() - t0) > limit_ns) {
+      atomicOr(&g_status, 1u);
+      return false;
+    }
+  }
+}
 // Wait for the phase with the given parity; gives up after limit_ns nanoseconds, records ST_TIMEOUT in
 // the device status word and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns) {
