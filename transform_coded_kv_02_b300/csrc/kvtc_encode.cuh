@@ -74,28 +74,30 @@ __global__ void __launch_bounds__(256) encode_warp_kernel(ParamsDev P, EncArgs a
 }
 
 // ---- append: one CTA per (tensor, sequence, KV head), its few new tokens one after another ---------------
-// T^T arrives in shared memory by one bulk copy; thread j then forms y_j = sum_k T[j][k] x_k with the same FMA
-// chain, in the same k order, as encode_warp_kernel, so both kernels write identical records; warp 0 runs the
-// warp quantiser/packer. One launch costs one transform fetch per head instead of one per token.
+// T^T arrives in shared memory by one bulk copy while every thread fetches its channel's parameters and the write
+// position (one round of loads). Thread j then forms y_j = sum_k T[j][k] x_k with the same FMA chain, in the same k
+// order, as encode_warp_kernel, and quantises channel j with the same op sequence as the warp quantiser, so both
+// kernels write identical records; the block reduces min and max over the coded channels, and the codes meet in
+// the record by shared-memory ORs. One launch costs one transform fetch per head instead of one per token.
 constexpr int AP_THREADS = 128;
 constexpr int AP_MAX_TOKENS = 16;  // larger appends go to the token-parallel kernels
 static size_t append_smem_bytes() { return (size_t)D * D * 4 + 2 * D * 4; }
+static_assert(AP_THREADS == D, "one thread per channel");
 
 template <bool BF16>
 __global__ void __launch_bounds__(AP_THREADS) encode_append_kernel(ParamsDev P, EncArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   float* TTs = reinterpret_cast<float*>(smem);  // [k][j]
   float* xs = TTs + D * D;
-  float* ys = xs + D;
   __shared__ __align__(8) uint64_t bar;
+  __shared__ float red_m[AP_THREADS / 32], red_M[AP_THREADS / 32];
   __shared__ uint32_t rec_s[2 * MAX_RW + 4];
-  // a decode call that follows may start preparing (its q-preparation waits for this grid before it reads q
-  // or lets the decode kernel copy records)
+  // a decode call that follows may start preparing (it waits for this grid before it reads q or any record)
   pdl_launch_dependents();
-  const int tensor = blockIdx.y, bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  const int tensor = blockIdx.y, bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, j = tid;
   const int b = bh / a.Hkv, h = bh - b * a.Hkv;
   const int set = a.per_seq ? bh : h;
-  const TensorDev& td = P.t[tensor];
+  const TensorDev& td = tensor == 0 ? P.t[0] : P.t[1];
   if (tid == 0) {
     mbar_init(smem_u32(&bar), 1);
     fence_mbar_init();
@@ -105,31 +107,83 @@ __global__ void __launch_bounds__(AP_THREADS) encode_append_kernel(ParamsDev P, 
     mbar_expect_tx(smem_u32(&bar), D * D * 4);
     bulk_g2s(smem_u32(TTs), td.TT + (size_t)set * D * D, D * D * 4, smem_u32(&bar));
   }
+  // channel j's parameters and its code's place in the record; the first token's element j; the write position
+  const size_t so = (size_t)set * D;
+  const float mu = td.mu[so + j], inv = td.inv_sigma[so + j];
+  const int bw = td.widths[so + j];
+  const int nz = td.nz[set];
+  const int R = td.r_words, W = tensor == 0 ? R : 2 * R;
+  uint32_t cw = 0, cb = 0;  // code word of the record and bit (values: within this token's 16-bit half)
+  if (tensor == 0) {
+    const uint32_t dsc = td.slots[so + (j >> 1)];
+    cw = 1u + (dsc & 255u);
+    cb = ((dsc >> 8) & 255u) + 16u * (uint32_t)(j & 1);
+  } else {
+    const uint32_t dsc = td.slots[so + j];
+    cw = 2u + (dsc & 255u);
+    cb = (dsc >> 8) & 255u;
+  }
+  const long long p0 = a.dst_pos[b];
+  const void* src = tensor == 0 ? a.src[0] : a.src[1];
+  auto load_x = [&](long long t) {
+    const size_t xo = ((size_t)bh * a.t_new + t) * D + j;
+    return BF16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[xo]) : static_cast<const float*>(src)[xo];
+  };
+  float xn = load_x(0);
   bool ok = mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);
   if (!ok && tid == 0) mbar_wait_bounded(smem_u32(&bar), 0u, a.wait_ns);  // drain before leaving
   if (!__syncthreads_and(ok)) return;
   for (long long t = 0; t < a.t_new; ++t) {
-    const size_t xo = ((size_t)bh * a.t_new + t) * D + tid;
-    xs[tid] = BF16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.src[tensor])[xo])
-                   : static_cast<const float*>(a.src[tensor])[xo];
+    xs[j] = xn;
+    if (t + 1 < a.t_new) xn = load_x(t + 1);
+    for (int i = tid; i < W; i += AP_THREADS) rec_s[i] = 0u;
     __syncthreads();
     float acc = 0.f;
 #pragma unroll 16
-    for (int k = 0; k < D; ++k) acc = fmaf(TTs[k * D + tid], xs[k], acc);
-    ys[tid] = acc;
+    for (int k = 0; k < D; ++k) acc = fmaf(TTs[k * D + j], xs[k], acc);
+    // y'_j = (y_j - mu_j) * (1/sigma_j); z = fp16(min y'), s = fp16(max y' - z) over the coded channels
+    const float yp = __fmul_rn(__fsub_rn(acc, mu), inv);
+    float m = bw > 0 ? yp : INFINITY, M = bw > 0 ? yp : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    }
+    if (lane == 0) {
+      red_m[warp] = m;
+      red_M[warp] = M;
+    }
     __syncthreads();
-    if (tid < 32) {
-      const float4 y4 = reinterpret_cast<const float4*>(ys)[lane];
-      const float y[4] = {y4.x, y4.y, y4.z, y4.w};
-      const long long pos = a.dst_pos[b] + t;
-      uint32_t* out = nullptr;
-      if (pos >= 0 && pos < a.T_cap) {
-        out = tensor == 0 ? a.dst[0] + ((size_t)bh * a.T_cap + (size_t)pos) * td.r_words
-                          : a.dst[1] + ((size_t)bh * (a.T_cap / 2) + (size_t)(pos >> 1)) * 2 * td.r_words;
-      } else if (lane == 0) {
-        atomicOr(&g_status, ST_BAD_INDEX);
+    m = fminf(fminf(red_m[0], red_m[1]), fminf(red_m[2], red_m[3]));
+    M = fmaxf(fmaxf(red_M[0], red_M[1]), fmaxf(red_M[2], red_M[3]));
+    __half zh = __ushort_as_half(0), sh = __ushort_as_half(0);
+    if (nz > 0) {
+      zh = half_sat_rn(__fadd_rn(m, 0.f));
+      sh = half_sat_rn(__fsub_rn(M, __half2float(zh)));
+    }
+    const float zf = __half2float(zh), sf = __half2float(sh);
+    if (sf != 0.f && bw > 0) atomicOr(&rec_s[cw], quantize_code(yp, zf, sf, bw) << cb);
+    __syncthreads();
+    const long long pos = p0 + t;
+    const uint32_t zs = (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
+    if (pos >= 0 && pos < a.T_cap) {
+      if (tensor == 0) {
+        uint32_t* out = a.dst[0] + ((size_t)bh * a.T_cap + (size_t)pos) * R;
+        for (int i = tid; i < R; i += AP_THREADS) out[i] = i == 0 ? zs : rec_s[i];
+      } else {
+        // the token's half of its two-token record: its z/s word and its 16-bit half of every code word
+        uint32_t* out = a.dst[1] + ((size_t)bh * (a.T_cap / 2) + (size_t)(pos >> 1)) * 2 * R;
+        const int hf = (int)(pos & 1);
+        for (int i = tid; i < W; i += AP_THREADS) {
+          if (i < 2) {
+            if (i == hf) out[i] = zs;
+          } else {
+            reinterpret_cast<uint16_t*>(out)[2 * i + hf] = (uint16_t)rec_s[i];
+          }
+        }
       }
-      quantize_pack_warp(td, set, y, lane, rec_s, out, tensor == 1, (int)(pos & 1));
+    } else if (tid == 0) {
+      atomicOr(&g_status, ST_BAD_INDEX);
     }
     __syncthreads();
   }
