@@ -21,10 +21,15 @@
 // Values, per head, with weights p_t (unnormalised softmax) and W_t = p_t s_t (value slots have w_j = b_j):
 //   sum_t p_t y^_tj = l mu_j + sigma_j (Z - (1 - 2^(-b_j - 1)) S + M_j),  M_j = sum_t W_t A_tj,
 //   Z = sum_t p_t z_t, S = sum_t W_t, l = sum_t p_t,
-// so the original-basis output is o_k = (T_V^T mu)_k + (Z w_k - S w2_k + sum_j T'_jk M_j) / l with
-// T'_jk = T_V[j][k] sigma_j, w_k = sum_j T'_jk, w2_k = sum_j T'_jk (1 - 2^(-b_j - 1)) (sums over b_j > 0).
-// Each split leaves (m, l, Z, S, M) in the rotated basis; the last split to finish merges them with their softmax
-// weights and maps the result to the original basis once.
+// so the original-basis sum is U_k = l (T_V^T mu)_k + Z w_k - S w2_k + sum_j T'_jk M_j with T'_jk = T_V[j][k]
+// sigma_j, w_k = sum_j T'_jk, w2_k = sum_j T'_jk (1 - 2^(-b_j - 1)) (sums over b_j > 0), and o = U / l.
+//
+// Work split. A CTA owns one split (a token range) of one (sequence, KV head). Its warps are alike: each takes 32
+// tokens of every ring stage (two 16-token MMA tiles), forms their logits (A = key codes, B = the heads' q'
+// coefficients), runs the online softmax in the MMA's accumulator layout (a lane owns one head and four tokens),
+// hands the weights W = p s to the value MMA's operand layout by warp shuffles, and accumulates M with A = value
+// codes. At the end the warps' partials meet in shared memory, the CTA maps its merged sums to the original basis
+// (U above), and the last CTA of the (sequence, head) to finish adds the splits' U with their softmax weights.
 #pragma once
 #include <type_traits>
 
@@ -33,27 +38,25 @@ namespace kvtc {
 // ======================================================================================================
 // decode over packed records
 // ======================================================================================================
-constexpr int PSTR = 132;              // floats per (split, head) partial: m, l, Z, S, M[128]
-constexpr int WT = 32;                 // tokens of a warp pair per ring stage
-constexpr int RING_BUDGET = 128 * 1024;
+constexpr int PSTR = 132;              // floats per (warp or split, head) partial: m, l, Z, S | U or M [128]
+constexpr int WTOK = 32;               // tokens of one warp per ring stage
+constexpr int RING_BUDGET = 160 * 1024;
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_SPLITS = 256;
-constexpr int TAIL_RESERVE = MAX_SPLITS * MAX_G * 4 + 4 * MAX_G * 4;  // split weights, head state
 constexpr int HC = 4;                  // per-head constants: C0, C1, C2, 2^-e
 
-// warp pairs (a key warp and a value warp) per CTA: eight with one 8-column block (128 registers a thread, one
-// 16-warp CTA per SM), four with two (the heads' operands and sums need more registers)
-__host__ __device__ constexpr int dec_pairs(int nb) { return nb == 1 ? 8 : 4; }
-__host__ __device__ constexpr int dec_threads(int nb) { return 64 * dec_pairs(nb); }
-__host__ __device__ constexpr int dec_stage_tokens(int nb) { return WT * dec_pairs(nb); }
-static_assert(dec_threads(2) / 32 >= MAX_G, "one warp per query head of a group in the merge");
+// Warps per CTA: sixteen when the per-lane operand arrays fit 128 registers (one 8-column block of heads, at most
+// four 16-channel blocks), eight otherwise.
+__host__ __device__ constexpr int dec_warps(int nb, int nblk) { return (nb == 1 && nblk <= 4) ? 16 : 8; }
+__host__ __device__ constexpr int dec_threads(int nb, int nblk) { return 32 * dec_warps(nb, nblk); }
+__host__ __device__ constexpr int dec_stage_tokens(int nb, int nblk) { return WTOK * dec_warps(nb, nblk); }
 
 struct DecArgs {
   const uint32_t* rec[2];
   const __nv_bfloat16* q;
   const int32_t* seq_lens;
   unsigned* cnt;    // [B*Hkv] arrival counters: zero before a call, left at zero after it
-  float* part;      // [B*Hkv][splits][g][PSTR] split partials
+  float* part;      // [B*Hkv][splits][g][PSTR] split partials (m, l, -, -, U[128])
   float* out;       // [B][Hq][128]
   long long T_cap;
   long long wait_ns;
@@ -74,45 +77,143 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __host__ __device__ __forceinline__ uint32_t align128u(uint32_t x) { return (x + 127u) & ~127u; }
 
-// P hand-off buffer of one warp pair and one slot: the softmax weights p (fp32) [2 m-tiles][4 NB heads][24] (16
-// tokens, rows padded to 24 floats so that both the key warp's stores and the value warp's 64-bit loads are free
-// of bank conflicts), then the NB x 4 rescale factors.
-constexpr int PROW = 24;
-__host__ __device__ constexpr uint32_t pbuf_bytes(int nb) { return 2u * 4u * nb * PROW * 4u + 16u * nb; }
-
 struct DecSmem {  // byte offsets into the dynamic shared memory of decode_kernel
-  uint32_t stage_bytes, qa, hc, pbuf, epi, chunks, tail_reserve, total;
+  uint32_t stage_bytes, qa, hc, pro, tsl, total;
 };
+constexpr uint32_t SMEM_LIMIT = 227u * 1024u;   // dynamic shared memory a CTA may hold
+constexpr uint32_t SMEM_STATIC = 1024u;         // room left for the kernel's static shared variables
 
-// main loop: ring | q' operands [16][128] fp16 | per-head constants | P buffers (pairs x 2 slots)
-// prologue scratch from epi: q [8][128] f32, partial q~ [parts][8][128] f32, coefficient scales [8]
-// epilogue: per-warp-pair partials from epi
-// tail (last CTA): T'_V rows [0, 64 KB) | split partial chunks [64 KB, tail_reserve) | merged partial and the
-//   per-split weights and per-head state in the reserve at the end
-__host__ __device__ inline DecSmem decode_smem(int RK, int RV, int stages, int nb) {
+// Epilogue scratch (floats) in the ring's bytes once the ring is consumed: the warps' partials [NW][8][PSTR], the
+// CTA's merged partial [8][PSTR], the splits' merged M [8][128], the heads' merged l, Z, S [8][4], the splits'
+// weights [MAX_SPLITS][8], the row blocks' partial dot products [NT / KW][8][KW] and a chunk of split partials
+// [MERGE_CHUNK] (global merge); the last CTA of the global merge stages
+// T'_V [128][128] and T_V^T mu, w, w2 [3][128] at the start (over the warps' partials, dead by then).
+constexpr uint32_t MERGE_CHUNK = 12288;  // floats of split partials the global merge stages at once
+struct DecEpi {
+  uint32_t wpart, mrg, mg, hs, esw, rot, chunk, tfull, end;
+};
+__host__ __device__ inline DecEpi decode_epi(int nw, int nt) {
+  DecEpi e;
+  e.wpart = 0;
+  e.tfull = 0;
+  e.mrg = e.wpart + (uint32_t)nw * MAX_G * PSTR;
+  e.mg = e.mrg + MAX_G * PSTR;
+  e.hs = e.mg + MAX_G * D;
+  e.esw = e.hs + MAX_G * 4;
+  e.rot = e.esw + MAX_SPLITS * MAX_G;
+  e.chunk = e.rot + (uint32_t)MAX_G * nt;
+  e.end = e.chunk + MERGE_CHUNK;
+  const uint32_t tend = (uint32_t)(D + 3) * D;  // T'_V rows and the three column vectors
+  if (e.mrg < tend) {                           // keep the merge scratch clear of the staged T'_V
+    const uint32_t sh = tend - e.mrg;
+    e.mrg += sh, e.mg += sh, e.hs += sh, e.esw += sh, e.rot += sh, e.chunk += sh, e.end += sh;
+  }
+  return e;
+}
+
+// [0, qa): the ring of record stages, then the epilogue scratch above | qa: q' operands [16 columns][128] fp16 |
+// hc: per-head constants [8][HC] | pro: prologue scratch (q [8][128], partial q~ [QPARTS][8][128], coefficient
+// scales [8]) | tsl (cluster merge, cs > 0): this CTA's columns of T'_V [128][128 / cs] and of T_V^T mu, w, w2
+// [3][128 / cs]
+__host__ __device__ inline DecSmem decode_smem(int RK, int RV, int stages, int nb, int nblk, int cs) {
   DecSmem s;
-  const int pairs = dec_pairs(nb), parts = dec_threads(nb) / D;
-  s.stage_bytes = (uint32_t)dec_stage_tokens(nb) * (RK + RV) * 4u;
-  s.qa = align128u(stages * s.stage_bytes);
+  const int nt = dec_threads(nb, nblk), parts = nt / D, nw = nt / 32;
+  s.stage_bytes = (uint32_t)dec_stage_tokens(nb, nblk) * (RK + RV) * 4u;
+  const uint32_t ring = (uint32_t)stages * s.stage_bytes;
+  const uint32_t epi = decode_epi(nw, nt).end * 4u;
+  const uint32_t r = ring > epi ? ring : epi;
+  s.qa = align128u(r);
   s.hc = s.qa + 16u * D * 2u;
-  s.pbuf = align128u(s.hc + MAX_G * HC * 4u);
-  const uint32_t main_end = s.pbuf + pairs * 2u * pbuf_bytes(nb);
-  s.epi = align128u(main_end);
-  const uint32_t prologue_end = s.epi + (MAX_G * D + parts * MAX_G * D + MAX_G) * 4u;
-  const uint32_t epi_end = s.epi + pairs * 8u * PSTR * 4u;
-  s.chunks = (uint32_t)D * D * 4u;
-  uint32_t end = prologue_end > epi_end ? prologue_end : epi_end;
-  const uint32_t tail_min = s.chunks + 8u * MAX_G * PSTR * 4u;  // room for eight splits' partials at least
-  end = end > tail_min ? end : tail_min;
-  s.tail_reserve = align128u(end);
-  s.total = s.tail_reserve + (MAX_G * PSTR + 4 * MAX_G) * 4u + TAIL_RESERVE;
+  s.pro = align128u(s.hc + MAX_G * HC * 4u);
+  s.tsl = align128u(s.pro + (uint32_t)(MAX_G * D + parts * MAX_G * D + MAX_G) * 4u);
+  s.total = s.tsl + (cs > 0 ? (uint32_t)(D + 3) * (D / cs) * 4u : 0u);
   return s;
 }
 
-__host__ __device__ constexpr int ring_stages_for(int RK, int RV, int nb) {
-  return (RING_BUDGET / (dec_stage_tokens(nb) * (RK + RV) * 4)) > MAX_STAGES ? MAX_STAGES
-         : (RING_BUDGET / (dec_stage_tokens(nb) * (RK + RV) * 4)) < 2      ? 2
-                                                                          : RING_BUDGET / (dec_stage_tokens(nb) * (RK + RV) * 4);
+// ring stages: as many as RING_BUDGET (and the CTA's shared memory left beside the other regions) holds, 2 to 8
+__host__ __device__ inline int ring_stages_for(int RK, int RV, int nb, int nblk, int cs) {
+  const DecSmem z = decode_smem(RK, RV, 0, nb, nblk, cs);
+  const uint32_t other = z.total - z.qa;
+  uint32_t budget = SMEM_LIMIT - SMEM_STATIC - other;
+  budget = budget < (uint32_t)RING_BUDGET ? budget : (uint32_t)RING_BUDGET;
+  const int n = (int)(budget / z.stage_bytes);
+  return n > MAX_STAGES ? MAX_STAGES : (n < 2 ? 2 : n);
+}
+
+// The map of merged rotated-basis sums to the original basis for output columns [k0, k0 + KW) of every head:
+// o_k = (l base_k + Z w_k - S w2_k + sum_j T'[j][k] M_j) / l, with tsl = T' columns [128][KW], bsl = base, w, w2
+// columns [3][KW], mg = merged M [8][128], hs = merged (l, Z, S) [8][4]. Thread (row block, column) sums its rows
+// for every head (one T' element serves all heads); rot [NT / KW][8][KW] gathers the row blocks' sums.
+template <int NT>
+__device__ __forceinline__ void rotate_out(const float* tsl, const float* bsl, const float* mg, const float* hs,
+                                           float* rot, int g, int KW, int k0, int nzV, float* outp) {
+  const int tid = threadIdx.x;
+  const int JP = NT / KW, kl = tid % KW, jp = tid / KW;
+  const int j0 = nzV * jp / JP, j1 = nzV * (jp + 1) / JP;
+  float acc[MAX_G];
+#pragma unroll
+  for (int h = 0; h < MAX_G; ++h) acc[h] = 0.f;
+  int j = j0;
+  for (; j + 4 <= j1; j += 4) {  // four rows per step: their loads in flight together
+    float t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) t[u] = tsl[(j + u) * KW + kl];
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h)
+      if (h < g) {
+        const float* m = mg + h * D + j;
+        acc[h] = fmaf(t[0], m[0], fmaf(t[1], m[1], fmaf(t[2], m[2], fmaf(t[3], m[3], acc[h]))));
+      }
+  }
+  for (; j < j1; ++j) {
+    const float t = tsl[j * KW + kl];
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h)
+      if (h < g) acc[h] = fmaf(t, mg[h * D + j], acc[h]);
+  }
+#pragma unroll
+  for (int h = 0; h < MAX_G; ++h)
+    if (h < g) rot[(jp * MAX_G + h) * KW + kl] = acc[h];
+  __syncthreads();
+  for (int o = tid; o < g * KW; o += NT) {
+    const int h = o / KW, c = o - h * KW;
+    float sacc = 0.f;
+    for (int p = 0; p < JP; ++p) sacc += rot[(p * MAX_G + h) * KW + c];
+    const float l = hs[h * 4];
+    const float u = fmaf(l, bsl[c], fmaf(hs[h * 4 + 1], bsl[KW + c], fmaf(-hs[h * 4 + 2], bsl[2 * KW + c], sacc)));
+    outp[h * D + k0 + c] = l > 0.f ? u / l : 0.f;
+  }
+}
+
+// The cluster's merged M_j = sum_r e_r M_rj over its CSX splits (distributed shared memory): every thread's loads
+// for all its items and ranks are issued before the first is used (the item index clamped, so that none is
+// predicated).
+template <int CSX, int NT>
+__device__ __forceinline__ void cluster_merge_m(uint32_t mrg_a, const float* esw, float* mg, int g, int nzV) {
+  constexpr int IT = (MAX_G * D + NT - 1) / NT;
+  const int n = g * nzV;
+  if (n == 0) return;
+  float v[IT][CSX];
+  int hj[IT];
+#pragma unroll
+  for (int r = 0; r < IT; ++r) {
+    const int idx = min((int)threadIdx.x + NT * r, n - 1);
+    const int h = idx / nzV, j = idx - h * nzV;
+    hj[r] = h * D + j;
+    const uint32_t la = mrg_a + (uint32_t)(h * PSTR + 4 + j) * 4u;
+#pragma unroll
+    for (int c = 0; c < CSX; ++c) v[r][c] = ld_dsmem(dsmem_addr(la, c));
+  }
+#pragma unroll
+  for (int r = 0; r < IT; ++r) {
+    if ((int)threadIdx.x + NT * r < n) {
+      const int h = hj[r] / D;
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < CSX; ++c) acc = fmaf(esw[c * MAX_G + h], v[r][c], acc);
+      mg[hj[r]] = acc;
+    }
+  }
 }
 
 // Four shared-memory words at a 32-bit shared address and three further multiples of a byte stride (an immediate
@@ -150,15 +251,17 @@ __device__ __forceinline__ void slot_decode_desc(uint32_t stage_off, uint32_t r,
 }
 
 // RK_, RV_ > 0: compile-time record lengths (ring stage size and count, token row offsets as immediates).
-// NB: 8-column blocks of the MMA's n dimension (4 heads each, fp16 hi and lo columns). NBLK: 16-channel blocks
-// processed per tensor (blocks past a set's last nonzero-width channel hold zero masks and zero coefficients).
-template <int NB, int RK_, int RV_, int NBLK>
-__global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P, DecArgs a) {
-  constexpr int DW = dec_pairs(NB), DTHREADS = dec_threads(NB), DT = dec_stage_tokens(NB);
-  constexpr int QPARTS = DTHREADS / D, KQ = D / QPARTS;  // q preparation: threads per channel, k's per thread
+// NB: 8-column blocks of the logit MMA's n dimension (4 heads each, fp16 hi and lo columns). NBLK: 16-channel
+// blocks processed per tensor (blocks past a set's last nonzero-width channel hold zero masks and coefficients).
+// CL: the splits of a (sequence, head) form one thread-block cluster (gridDim.x = cluster size) and merge through
+// distributed shared memory; otherwise they merge through the workspace, the last to arrive doing the merge.
+template <int NB, int RK_, int RV_, int NBLK, bool CL>
+__global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(ParamsDev P, DecArgs a) {
+  constexpr int NW = dec_warps(NB, NBLK), NT = 32 * NW, ST = WTOK * NW;
+  constexpr int QPARTS = NT / D, KQ = D / QPARTS;  // q preparation: threads per channel, k's per thread
   extern __shared__ __align__(128) uint8_t smem[];
-  // barriers live outside the dynamic region, which the epilogue and the tail reuse wholesale
-  __shared__ __align__(8) uint64_t full[MAX_STAGES], pF[DW][2], pE[DW][2], tbar_s, vbar_s;
+  // barriers live outside the dynamic region, which the epilogue reuses wholesale
+  __shared__ __align__(8) uint64_t full[MAX_STAGES];
   __shared__ unsigned rel[MAX_STAGES];  // warps done with the stage in each ring slot
   __shared__ int s_abort, s_last, s_issued;
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
@@ -167,15 +270,12 @@ __global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P,
   const TensorDev& TK = P.t[0];
   const TensorDev& TV = P.t[1];
   const int RK = RK_ ? RK_ : TK.r_words, RV = RV_ ? RV_ : TV.r_words;
-  constexpr int NS_CT = RK_ ? ring_stages_for(RK_, RV_, NB) : 0;
-  const int NS = RK_ ? NS_CT : a.stages, g = a.g;
+  const int NS = a.stages, g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   const size_t so = (size_t)set * D;
-  const int nzK = TK.nz[set], nzV = TV.nz[set];
-  const int nkb = (nzK + 15) >> 4, nmb = (nzV + 15) >> 4;
-  const DecSmem L = decode_smem(RK, RV, NS, NB);
-  const uint32_t stage_bytes = (uint32_t)DT * (RK + RV) * 4u;
-  uint64_t* tbar = &tbar_s;
+  const int CS = CL ? a.splits : 0;  // cluster size
+  const DecSmem L = decode_smem(RK, RV, NS, NB, NBLK, CS);
+  const uint32_t stage_bytes = L.stage_bytes;
   __half* qa = reinterpret_cast<__half*>(smem + L.qa);  // [16 columns][128 channels]
   float* hc = reinterpret_cast<float*>(smem + L.hc);    // [8 heads][HC]
 
@@ -184,40 +284,32 @@ __global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P,
       mbar_init(smem_u32(&full[s]), 1);
       rel[s] = 0u;
     }
-    for (int p = 0; p < DW; ++p)
-      for (int sl = 0; sl < 2; ++sl) {
-        mbar_init(smem_u32(&pF[p][sl]), 1);
-        mbar_init(smem_u32(&pE[p][sl]), 1);
-      }
-    mbar_init(smem_u32(tbar), 1);
-    mbar_init(smem_u32(&vbar_s), 1);
     fence_mbar_init();
     s_abort = 0;
     s_issued = 0;
   }
-  // ---- parameters only (nothing a previous kernel writes), all in one round of loads ----
-  uint32_t sd[NBLK][2], sm[NBLK][2];  // slot descriptors of this warp's role
-  if (warp < DW) {  // key warp: pair 8 kb + 4 i + tig of token rows WT pw + gid (+ 8, 16, 24)
+  // ---- parameters only (nothing a previous kernel writes): one round of loads, left in flight while the kernel
+  // waits for its predecessor and fetches q ----
+  // key slots: pair 8 kb + 4 i + tig of token rows 32 warp + gid (+ 8, 16, 24); value slots: channel 16 mb + 8 i +
+  // gid of the two-token records 16 warp + tig (+ 4, 8, 12)
+  const int nzK = __ldg(TK.nz + set), nzV = __ldg(TV.nz + set);
+  uint32_t kd[NBLK][2], km[NBLK][2], vd[NBLK][2], vm[NBLK][2];  // raw slot entries first, descriptors later
 #pragma unroll
-    for (int kb = 0; kb < NBLK; ++kb)
+  for (int kb = 0; kb < NBLK; ++kb)
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint32_t dk = kb < nkb ? __ldg(TK.slots + so + 8 * kb + 4 * i + tig) : 0u;
-        const uint32_t b0 = (dk >> 16) & 255u, b1 = dk >> 24, w = b0 > b1 ? b0 : b1;
-        const uint32_t off = (uint32_t)(WT * warp + gid) * RK * 4u + 4u * (1u + (dk & 255u));
-        slot_decode_desc(off, (dk >> 8) & 255u, w, b0, b1, sd[kb][i], sm[kb][i]);
-      }
-  } else {          // value warp: channel 16 mb + 8 i + gid of token-pair records (WT/2) pw + tig (+ 4, 8, 12)
-#pragma unroll
-    for (int mb = 0; mb < NBLK; ++mb)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint32_t dv = mb < nmb ? __ldg(TV.slots + so + 16 * mb + 8 * i + gid) : 0u;
-        const uint32_t bw = (dv >> 16) & 255u;
-        const uint32_t off = (uint32_t)DT * RK * 4u + (uint32_t)((WT / 2) * (warp - DW) + tig) * 2u * RV * 4u +
-                             4u * (2u + (dv & 255u));
-        slot_decode_desc(off, (dv >> 8) & 255u, bw, bw, bw, sd[mb][i], sm[mb][i]);
-      }
+    for (int i = 0; i < 2; ++i) {
+      kd[kb][i] = __ldg(TK.slots + so + 8 * kb + 4 * i + tig);
+      vd[kb][i] = __ldg(TV.slots + so + 16 * kb + 8 * i + gid);
+    }
+  if constexpr (CL) {  // this CTA's output columns of T'_V and of T_V^T mu, w, w2, copied while the CTA works
+    const int KW = D / CS, k0 = split * KW, cpr = KW / 4;  // 16-byte chunks per row
+    const uint32_t tdst = smem_u32(smem + L.tsl);
+    for (int c = tid; c < (D + 3) * cpr; c += NT) {
+      const int row = c / cpr, cc = c - row * cpr;
+      const float* src = row < D ? TV.Tsc + (so + row) * D : (row == D ? TV.base : row == D + 1 ? TV.wsum : TV.wsum2) + so;
+      cp_async16(tdst + (uint32_t)(row * KW + 4 * cc) * 4u, src + k0 + 4 * cc);
+    }
+    cp_async_commit();
   }
   // q preparation: this thread's slice of T^T (rows KQ part .. KQ part + KQ - 1, column j), channel j's sigma and
   // widths; warp h < 8: the folded key vectors at its lane's four entries
@@ -240,35 +332,38 @@ __global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P,
   }
   __syncthreads();
 
-  // The previous kernel of the stream (an append, say) may still be running: q and the records are read only
-  // after it has completed.
+  // The previous kernel of the stream (an append, say) may still be running: q, the lengths and the records are
+  // read only after it has completed.
   pdl_wait();
-
-  // this sequence's tokens spread over all the splits: chunks of whole stages sized from its own length, so a
-  // short sequence in a long cache (or in a ragged batch) keeps every split busy
+  // q and the length first, so that their loads do not queue behind the ring's copies
+  uint2 qraw = make_uint2(0u, 0u);
+  if (warp < g) qraw = reinterpret_cast<const uint2*>(a.q + ((size_t)b * a.Hq + (size_t)kh * g + warp) * D)[lane];
   const long long Lseq = max(0LL, min((long long)a.seq_lens[b], a.T_cap));
-  const long long chunk = ((Lseq + a.splits - 1) / a.splits + DT - 1) / DT * DT;
+
+  // this sequence's tokens spread over all the splits in whole warp blocks, sized from its own length, so that a
+  // short sequence in a long cache (or in a ragged batch) keeps every split busy
+  const long long chunk = ((Lseq + a.splits - 1) / a.splits + WTOK - 1) / WTOK * WTOK;
   const long long t0 = min((long long)split * chunk, Lseq);
   const long long t1 = min(t0 + chunk, Lseq);
-  const int ntiles = (int)((t1 - t0 + DT - 1) / DT);
   const int n_in = (int)(t1 - t0);
+  const int ntiles = (n_in + ST - 1) / ST;
 
-  // ---- record stages stream into the ring by bulk copies: thread 0 fills the ring, then the last of the 2 DW warps
+  // ---- record stages stream into the ring by bulk copies: thread 0 fills the ring, then the last of the NW warps
   // to release a slot refills it at once with the stage NS further on ----
   const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
   const uint32_t* vrec = a.rec[1] + (size_t)bh * a.T_cap * RV;  // two-token records: same bytes per token
   const uint32_t ring = smem_u32(smem);
   auto issue_tile = [&](int i) {
     const int s = i % NS;
-    const long long tb = t0 + (long long)i * DT;
-    long long n = min((long long)DT, t1 - tb);
+    const long long tb = t0 + (long long)i * ST;
+    long long n = min((long long)ST, t1 - tb);
     n = min((n + 3) & ~3LL, a.T_cap - tb);
     const uint32_t kbytes = (uint32_t)(n * RK * 4), vbytes = (uint32_t)(n * RV * 4);
     const uint32_t bar = smem_u32(&full[s]);
     const uint32_t dst = ring + (uint32_t)s * stage_bytes;
     mbar_expect_tx(bar, kbytes + vbytes);
     bulk_g2s(dst, krec + tb * RK, kbytes, bar);
-    bulk_g2s(dst + DT * RK * 4, vrec + tb * RV, vbytes, bar);
+    bulk_g2s(dst + ST * RK * 4, vrec + tb * RV, vbytes, bar);
   };
   // this warp is done reading stage i: the last warp to say so issues stage i + NS into the same slot (its
   // acquire-release count orders every warp's reads of the slot before the refill's writes)
@@ -278,7 +373,7 @@ __global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P,
       const int s = i % NS;
       unsigned old;
       asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_u32(&rel[s])) : "memory");
-      if (old == 2u * DW - 1u) {
+      if (old == (unsigned)NW - 1u) {
         rel[s] = 0u;
         if (i + NS < ntiles) {
           fence_proxy_async_smem();
@@ -288,28 +383,47 @@ __global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P,
       }
     }
   };
-  if (tid == 0) {
-    if (split == 0 && nzV > 0)  // the merge of this (sequence, head) reads the scaled T_V rows: warm L2 now
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(TV.Tsc + so * D), "r"((uint32_t)nzV * D * 4)
-                   : "memory");
-    for (int i = 0; i < NS && i < ntiles; ++i) issue_tile(i);
-    s_issued = min(NS, ntiles);
+  if (warp == NW - 1) {  // the last warp fills the ring, a stage per lane (the q preparation runs meanwhile)
+    if (lane < NS && lane < ntiles) issue_tile(lane);
+    if (lane == 0) {
+      if (!CL && split == 0 && nzV > 0)  // the merging split reads the scaled T_V rows at its end
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(TV.Tsc + so * D), "r"((uint32_t)nzV * D * 4)
+                     : "memory");
+      s_issued = min(NS, ntiles);
+    }
   }
+  // slot descriptors (blocks past the set's last nonzero-width channel get zero masks)
+  const int nkb = (nzK + 15) >> 4, nmb = (nzV + 15) >> 4;
+#pragma unroll
+  for (int kb = 0; kb < NBLK; ++kb)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t dk = kb < nkb ? kd[kb][i] : 0u;
+      const uint32_t b0 = (dk >> 16) & 255u, b1 = dk >> 24, w = b0 > b1 ? b0 : b1;
+      const uint32_t off = (uint32_t)(WTOK * warp + gid) * RK * 4u + 4u * (1u + (dk & 255u));
+      slot_decode_desc(off, (dk >> 8) & 255u, w, b0, b1, kd[kb][i], km[kb][i]);
+      const uint32_t dv = kb < nmb ? vd[kb][i] : 0u;
+      const uint32_t bw = (dv >> 16) & 255u;
+      const uint32_t voff = (uint32_t)ST * RK * 4u + (uint32_t)((WTOK / 2) * warp + tig) * 2u * RV * 4u +
+                            4u * (2u + (dv & 255u));
+      slot_decode_desc(voff, (dv >> 8) & 255u, bw, bw, bw, vd[kb][i], vm[kb][i]);
+    }
 
   // ---- q preparation: per-head constants from dot products of q with the folded vectors, then
   // q~ = T_K q and the MMA coefficients Q_j 2^(w_j - b_j) 2^e_h as fp16 hi + lo pairs ----
   {
-    float* qs = reinterpret_cast<float*>(smem + L.epi);  // [8][128]
+    float* qs = reinterpret_cast<float*>(smem + L.pro);  // [8][128]
     float* red = qs + MAX_G * D;                          // [QPARTS][8][128]
     float* esc = red + QPARTS * MAX_G * D;                // [8] 2^e_h
-    if (warp < MAX_G) {  // warp h: head h's row of q, its norm and its three dot products
+    if (warp >= g && warp < MAX_G && lane == 0) {  // columns of no head: zero coefficients, unit scale
+      hc[warp * HC + 0] = hc[warp * HC + 1] = hc[warp * HC + 2] = 0.f;
+      hc[warp * HC + 3] = 1.f;
+      esc[warp] = 1.f;
+    }
+    if (warp < g) {  // warp h: head h's row of q, its norm and its three dot products
       const int h = warp;
-      float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (h < g) {
-        const uint2 u = reinterpret_cast<const uint2*>(a.q + ((size_t)b * a.Hq + (size_t)kh * g + h) * D)[lane];
-        qv = make_float4(bf16_bits_f(u.x & 0xFFFFu), bf16_bits_f(u.x >> 16), bf16_bits_f(u.y & 0xFFFFu),
-                         bf16_bits_f(u.y >> 16));
-      }
+      const float4 qv = make_float4(bf16_bits_f(qraw.x & 0xFFFFu), bf16_bits_f(qraw.x >> 16),
+                                    bf16_bits_f(qraw.y & 0xFFFFu), bf16_bits_f(qraw.y >> 16));
       reinterpret_cast<float4*>(qs + h * D)[lane] = qv;
       const float n2 = warp_sum(qv.x * qv.x + qv.y * qv.y + qv.z * qv.z + qv.w * qv.w);
       const float c0 = warp_sum(qv.x * kb4.x + qv.y * kb4.y + qv.z * kb4.z + qv.w * kb4.w);
@@ -336,19 +450,19 @@ __global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P,
     __syncthreads();
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h) {  // q~_h[j] over k in [KQ part, KQ part + KQ)
-      float acc = 0.f;
       if (h < g) {
+        float acc0 = 0.f, acc1 = 0.f;
         const float4* q4 = reinterpret_cast<const float4*>(qs + h * D + KQ * qpart);
 #pragma unroll
         for (int k4 = 0; k4 < KQ / 4; ++k4) {
           const float4 v = q4[k4];
-          acc = fmaf(tt[4 * k4], v.x, acc);
-          acc = fmaf(tt[4 * k4 + 1], v.y, acc);
-          acc = fmaf(tt[4 * k4 + 2], v.z, acc);
-          acc = fmaf(tt[4 * k4 + 3], v.w, acc);
+          acc0 = fmaf(tt[4 * k4], v.x, acc0);
+          acc1 = fmaf(tt[4 * k4 + 1], v.y, acc1);
+          acc0 = fmaf(tt[4 * k4 + 2], v.z, acc0);
+          acc1 = fmaf(tt[4 * k4 + 3], v.w, acc1);
         }
+        red[(qpart * MAX_G + h) * D + qj] = acc0 + acc1;
       }
-      red[(qpart * MAX_G + h) * D + qj] = acc;
     }
     __syncthreads();
     if (tid < D) {
@@ -356,10 +470,13 @@ __global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P,
       const float f = bj > 0 ? a.scale_log2 * q_sg * exp2i(wj - bj) : 0.f;
 #pragma unroll
       for (int h = 0; h < MAX_G; ++h) {
-        float qt = 0.f;
+        float c = 0.f;
+        if (h < g) {
+          float qt = 0.f;
 #pragma unroll
-        for (int p = 0; p < QPARTS; ++p) qt += red[(p * MAX_G + h) * D + j];
-        const float c = h < g ? qt * f * esc[h] : 0.f;
+          for (int p = 0; p < QPARTS; ++p) qt += red[(p * MAX_G + h) * D + j];
+          c = qt * f * esc[h];
+        }
         const __half hi = __float2half_rn(c);
         const __half lo = __float2half_rn(c - __half2float(hi));
         qa[(2 * h) * D + j] = hi;
@@ -369,487 +486,406 @@ __global__ void __launch_bounds__(dec_threads(NB), 1) decode_kernel(ParamsDev P,
     __syncthreads();
   }
 
-  // ============ warp pairs: key warp pw and value warp pw + DW own tokens [32 pw, 32 pw + 32) of every stage ============
-  const int pw = warp % DW;
-  uint8_t* const pbase = smem + L.pbuf + (size_t)pw * 2 * pbuf_bytes(NB);
-  float* ws = reinterpret_cast<float*>(smem + L.epi);  // [DW][8][PSTR] (the prologue scratch is dead)
-  constexpr uint32_t PCORR = 2u * 4u * NB * PROW * 4u;  // byte offset of the rescale factors in a P buffer
-  if (warp < DW) {
-    // ---------------- key warp: logits (MMA over the key codes), online softmax, p to the value warp ----------------
-    uint32_t qb[NBLK][NB][2];  // B operand: coefficients, k = channels 16 kb + 2 tig (+1, +8, +9), n = column gid
-    {
-      const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(qa);
+  // ============ main loop: warp w owns tokens [32 w, 32 w + 32) of every stage ============
+  // B operand of the logit MMA: coefficients, k = channels 16 kb + 2 tig (+1, +8, +9), n = column gid (head
+  // gid / 2 + 4 nb, fp16 hi part for even gid, lo part for odd gid)
+  uint32_t qb[NBLK][NB][2];
+  {
+    const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(qa);
 #pragma unroll
-      for (int kb = 0; kb < NBLK; ++kb)
+    for (int kb = 0; kb < NBLK; ++kb)
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const int col = nb * 8 + gid;
-          qb[kb][nb][0] = qa32[(col * D + kb * 16 + 2 * tig) >> 1];
-          qb[kb][nb][1] = qa32[(col * D + kb * 16 + 8 + 2 * tig) >> 1];
-        }
-    }
-    float C0[NB], C1[NB], C2[NB], qsc[NB], m_run[NB], l_run[NB];
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const int h = tig + 4 * nb;
-      C0[nb] = hc[h * HC + 0];
-      C1[nb] = hc[h * HC + 1];
-      C2[nb] = hc[h * HC + 2];
-      qsc[nb] = hc[h * HC + 3];
-      m_run[nb] = -INFINITY;
-      l_run[nb] = 0.f;
-    }
-    const uint32_t kzo = (uint32_t)(WT * pw + gid) * RK * 4u;
-    constexpr int KSTR = RK_ ? 8 * RK_ * 4 : 0;  // token rows +8
-    const uint32_t kstr = 8u * RK * 4u;
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i % NS;
-      const uint32_t sb = ring + (uint32_t)s * stage_bytes;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
-        s_abort = 1;
-        break;
+      for (int nb = 0; nb < NB; ++nb) {
+        const int col = nb * 8 + gid;
+        qb[kb][nb][0] = qa32[(col * D + kb * 16 + 2 * tig) >> 1];
+        qb[kb][nb][1] = qa32[(col * D + kb * 16 + 8 + 2 * tig) >> 1];
       }
-      // ---- logits: A = key codes (16 tokens x 16 channels) of m-tiles 0 (rows gid, gid + 8) and 1 (+16); two
-      // accumulators per m-tile (even and odd channel blocks) halve the MMA dependency chain ----
-      float acc[2][2][NB][4];
+  }
+  // this lane's softmax head in column block nb: tig + 4 nb, over the tokens 32 w + gid + 8 m (m = 0..3)
+  float C0[NB], C1[NB], C2[NB], qsc[NB], m_run[NB], l_run[NB], zsum[NB], ssum[NB];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+  for (int nb = 0; nb < NB; ++nb) {
+    const int h = tig + 4 * nb;
+    C0[nb] = hc[h * HC + 0];
+    C1[nb] = hc[h * HC + 1];
+    C2[nb] = hc[h * HC + 2];
+    qsc[nb] = hc[h * HC + 3];
+    m_run[nb] = -INFINITY;
+    l_run[nb] = zsum[nb] = ssum[nb] = 0.f;
+  }
+  // value sums M: channels 16 mb + gid (+8) x columns 2 tig, 2 tig + 1 (head tig + 4 nb, fp16 hi and lo parts of W)
+  float vacc[NBLK][NB][4];
 #pragma unroll
-        for (int pr = 0; pr < 2; ++pr)
+  for (int mb = 0; mb < NBLK; ++mb)
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb)
-            acc[mt][pr][nb][0] = acc[mt][pr][nb][1] = acc[mt][pr][nb][2] = acc[mt][pr][nb][3] = 0.f;
-#pragma unroll
-      for (int kb = 0; kb < NBLK; ++kb) {
-        uint32_t af[2][4];  // rows gid, gid + 8 (m-tile 0), gid + 16, gid + 24 (m-tile 1)
-        lds_x4<KSTR>(sb + (sd[kb][0] >> 5), kstr, af[0][0], af[0][1], af[1][0], af[1][1]);
-        lds_x4<KSTR>(sb + (sd[kb][1] >> 5), kstr, af[0][2], af[0][3], af[1][2], af[1][3]);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          af[mt][0] = slot_f16x2(af[mt][0], sd[kb][0], sm[kb][0]);
-          af[mt][1] = slot_f16x2(af[mt][1], sd[kb][0], sm[kb][0]);
-          af[mt][2] = slot_f16x2(af[mt][2], sd[kb][1], sm[kb][1]);
-          af[mt][3] = slot_f16x2(af[mt][3], sd[kb][1], sm[kb][1]);
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_f16(acc[mt][kb & 1][nb], af[mt], qb[kb][nb][0], qb[kb][nb][1]);
-        }
-      }
-      // z/s words of this lane's four tokens (rows gid + 8 m) of their key records
-      uint32_t kzw[4];
-      lds_x4<KSTR>(sb + kzo, kstr, kzw[0], kzw[1], kzw[2], kzw[3]);
+    for (int nb = 0; nb < NB; ++nb) vacc[mb][nb][0] = vacc[mb][nb][1] = vacc[mb][nb][2] = vacc[mb][nb][3] = 0.f;
+  // the value MMA's B operand: this lane holds column gid at tile tokens 2 tig, 2 tig + 1 (+8), which the logit
+  // layout keeps in lanes (2 tig) * 4 + gid / 2 and (2 tig + 1) * 4 + gid / 2, one packed (hi, lo) word per token
+  const int srcA = 8 * tig + (gid >> 1), srcB = srcA + 4;
+  const uint32_t psel = (gid & 1) ? 0x7632u : 0x5410u;
+  const uint32_t kzo = (uint32_t)(WTOK * warp + gid) * RK * 4u;  // key z/s word of token row gid
+  // value z/s word of token gid: record (gid / 2) of the warp's 16, word gid & 1
+  const uint32_t vzo = (uint32_t)ST * RK * 4u + (uint32_t)((WTOK / 2) * warp + (gid >> 1)) * 2u * RV * 4u +
+                       4u * (uint32_t)(gid & 1);
+  constexpr int KSTR = RK_ ? 8 * RK_ * 4 : 0;       // token rows +8
+  constexpr int VSTR = RV_ ? 4 * 2 * RV_ * 4 : 0;   // records +4
+  const uint32_t kstr = 8u * RK * 4u, vstr = 4u * 2u * RV * 4u;
+
+  for (int i = 0; i < ntiles; ++i) {
+    const int s = i % NS;
+    const uint32_t sb = ring + (uint32_t)s * stage_bytes;
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
+      s_abort = 1;
+      break;
+    }
+    const int r0 = i * ST + WTOK * warp;  // split-relative first token of this warp's block
+    if (r0 >= n_in) {                     // past the split's end (its last stage only)
       release_stage(i);
-      const int r0 = i * DT + WT * pw + gid;  // split-relative token of row m: r0 + 8 m
-      float zk[4], sk[4];
+      continue;
+    }
+    // ---- logits: A = key codes (16 tokens x 16 channels) of m-tiles 0 (rows gid, gid + 8) and 1 (+16); two
+    // accumulators per m-tile (even and odd channel blocks) halve the MMA dependency chain ----
+    float acc[2][2][NB][4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float2 fk = __half22float2(*reinterpret_cast<const __half2*>(&kzw[m]));
-        zk[m] = fk.x;
-        sk[m] = fk.y;
-      }
-      float pv[4][NB];
-      float corr[NB];
-      // logits, online softmax; FULL: every token of the stage is in the split (no masking)
-      auto softmax = [&](auto full_tag) {
-        constexpr bool FULL = decltype(full_tag)::value;
-        bool val[4];
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) val[m] = FULL || r0 + 8 * m < n_in;
-        float l[NB][4];
-        bool up = false;  // a logit above the running maximum of its head
+      for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
+          acc[mt][pr][nb][0] = acc[mt][pr][nb][1] = acc[mt][pr][nb][2] = acc[mt][pr][nb][3] = 0.f;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float* c0 = acc[m >> 1][0][nb];
-            const float* c1 = acc[m >> 1][1][nb];
-            const int e = 2 * (m & 1);
-            const float r = fmaf((c0[e] + c1[e]) + (c0[e + 1] + c1[e + 1]), qsc[nb], -C2[nb]);
-            const float lv = fmaf(sk[m], r, fmaf(zk[m], C1[nb], C0[nb]));
-            l[nb][m] = val[m] ? lv : -INFINITY;
-            up |= l[nb][m] > m_run[nb];
-          }
-        if (__any_sync(0xffffffffu, up)) {  // the running maxima move: recompute them across the warp
+    for (int kb = 0; kb < NBLK; ++kb) {
+      uint32_t af[2][4];  // rows gid, gid + 8 (m-tile 0), gid + 16, gid + 24 (m-tile 1)
+      lds_x4<KSTR>(sb + (kd[kb][0] >> 5), kstr, af[0][0], af[0][1], af[1][0], af[1][1]);
+      lds_x4<KSTR>(sb + (kd[kb][1] >> 5), kstr, af[0][2], af[0][3], af[1][2], af[1][3]);
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            float mt = fmaxf(fmaxf(l[nb][0], l[nb][1]), fmaxf(l[nb][2], l[nb][3]));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-            const float m_new = fmaxf(m_run[nb], mt);
-            corr[nb] = (m_run[nb] == m_new) ? 1.f : ex2_approx(m_run[nb] - m_new);
-            m_run[nb] = m_new;
-          }
-        } else {
+      for (int mt = 0; mt < 2; ++mt) {
+        af[mt][0] = slot_f16x2(af[mt][0], kd[kb][0], km[kb][0]);
+        af[mt][1] = slot_f16x2(af[mt][1], kd[kb][0], km[kb][0]);
+        af[mt][2] = slot_f16x2(af[mt][2], kd[kb][1], km[kb][1]);
+        af[mt][3] = slot_f16x2(af[mt][3], kd[kb][1], km[kb][1]);
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) corr[nb] = 1.f;
-        }
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          float ps = 0.f;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float e2 = ex2_approx(l[nb][m] - m_run[nb]);
-            pv[m][nb] = val[m] ? e2 : 0.f;
-            ps += pv[m][nb];
-          }
-          l_run[nb] = fmaf(l_run[nb], corr[nb], ps);
-        }
-      };
-      if ((i + 1) * DT <= n_in)
-        softmax(std::true_type{});
-      else
-        softmax(std::false_type{});
-      // ---- hand p and the rescale factors to the value warp ----
-      const int slot = i & 1;
-      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&pE[pw][slot]),
-                                                            (uint32_t)(((i >> 1) - 1) & 1), a.wait_ns, 64))) {
-        s_abort = 1;
-        break;
-      }
-      float* pt = reinterpret_cast<float*>(pbase + slot * pbuf_bytes(NB));
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) pt[((m >> 1) * 4 * NB + 4 * nb + tig) * PROW + gid + 8 * (m & 1)] = pv[m][nb];
-      if (gid == 0) {
-        float* pc = reinterpret_cast<float*>(pbase + slot * pbuf_bytes(NB) + PCORR);
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) pc[nb * 4 + tig] = corr[nb];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&pF[pw][slot]));
-    }
-    // this warp's softmax state into the per-warp partial
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      float lsum = l_run[nb];
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-      const int h = tig + 4 * nb;
-      if (h < g && gid == 0) {
-        float* w = ws + (pw * 8 + h) * PSTR;
-        w[0] = m_run[nb];
-        w[1] = lsum;
+        for (int nb = 0; nb < NB; ++nb) mma_f16(acc[mt][kb & 1][nb], af[mt], qb[kb][nb][0], qb[kb][nb][1]);
       }
     }
-  } else {
-    // ---------------- value warp: W = p s_V as fp16 hi/lo (the B operand), Z = sum p z_V, S = sum W, and
-    // M_j = sum_t W_t A_tj on the MMA (A = value codes) ----------------
-    float acc[NBLK][NB][4];
+    // z/s words of this lane's four tokens (rows gid + 8 m): key records, and the value records' halves
+    uint32_t kzw[4], vzw[4];
+    lds_x4<KSTR>(sb + kzo, kstr, kzw[0], kzw[1], kzw[2], kzw[3]);
+    lds_x4<VSTR>(sb + vzo, vstr, vzw[0], vzw[1], vzw[2], vzw[3]);
+    float zk[4], sk[4], zv[4], sv[4];
 #pragma unroll
-    for (int mb = 0; mb < NBLK; ++mb)
+    for (int m = 0; m < 4; ++m) {
+      const float2 fk = __half22float2(*reinterpret_cast<const __half2*>(&kzw[m]));
+      const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&vzw[m]));
+      zk[m] = fk.x;
+      sk[m] = fk.y;
+      zv[m] = fv.x;
+      sv[m] = fv.y;
+    }
+    // ---- logits, online softmax, W = p s_V as packed fp16 (hi, lo), this stage's shares of Z and S; FULL: every
+    // token of the warp's block is in the split (no masking) ----
+    float corr[NB];
+    uint32_t pk[4][NB];
+    auto softmax = [&](auto full_tag) {
+      constexpr bool FULL = decltype(full_tag)::value;
+      bool val[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) val[m] = FULL || r0 + gid + 8 * m < n_in;
+      float l[NB][4];
+      bool up = false;  // a logit above the running maximum of its head
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mb][nb][e] = 0.f;
-    // B fragment of a 16-token m-tile: this lane holds column gid (head gid / 2 + 4 nb, fp16 hi part for even gid,
-    // lo part for odd gid) at tokens 2 tig, 2 tig + 1 (first register) and 2 tig + 8, 2 tig + 9 (second); Z and S
-    // of head gid / 2 + 4 nb are summed over those tokens (the odd lanes repeat the even lanes' sums)
-    float zsum[NB], ssum[NB];
+        for (int m = 0; m < 4; ++m) {
+          const float* c0 = acc[m >> 1][0][nb];
+          const float* c1 = acc[m >> 1][1][nb];
+          const int e = 2 * (m & 1);
+          const float r = fmaf((c0[e] + c1[e]) + (c0[e + 1] + c1[e + 1]), qsc[nb], -C2[nb]);
+          const float lv = fmaf(sk[m], r, fmaf(zk[m], C1[nb], C0[nb]));
+          l[nb][m] = val[m] ? lv : -INFINITY;
+          up |= l[nb][m] > m_run[nb];
+        }
+      if (__any_sync(0xffffffffu, up)) {  // the running maxima move: recompute them across the warp
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) zsum[nb] = ssum[nb] = 0.f;
-    const bool lo_part = gid & 1;
-    constexpr int VSTR = RV_ ? 4 * 2 * RV_ * 4 : 0;  // records +4
-    const uint32_t vstr = 4u * 2u * RV * 4u;
-    // z/s words of tokens 2 tig, 2 tig + 1 (record (WT/2) pw + 8 mt + tig) and 2 tig + 8, 2 tig + 9 (+4 records)
-    const uint32_t vzo = (uint32_t)DT * RK * 4u + (uint32_t)((WT / 2) * pw + tig) * 2u * RV * 4u;
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i % NS, slot = i & 1;
-      const uint32_t sb = ring + (uint32_t)s * stage_bytes;
-      // p of this stage comes from the key warp, usually later than the stage's records: sleep while waiting,
-      // leaving the issue slots to the key warps
-      if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&pF[pw][slot]), (uint32_t)((i >> 1) & 1), a.wait_ns, 128))) {
-        s_abort = 1;
-        break;
+        for (int nb = 0; nb < NB; ++nb) {
+          float mt = fmaxf(fmaxf(l[nb][0], l[nb][1]), fmaxf(l[nb][2], l[nb][3]));
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+          const float m_new = fmaxf(m_run[nb], mt);
+          corr[nb] = (m_run[nb] == m_new) ? 1.f : ex2_approx(m_run[nb] - m_new);
+          m_run[nb] = m_new;
+        }
+      } else {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) corr[nb] = 1.f;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((i / NS) & 1), a.wait_ns))) {
-        s_abort = 1;
-        break;
-      }
-      const float* pb = reinterpret_cast<const float*>(pbase + slot * pbuf_bytes(NB));
-      float2 pp[2][NB][2];
-      float cacc[NB], czs[NB];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
-        const int hh = (gid >> 1) + 4 * nb;
+        float ps = 0.f, pz = 0.f, pw = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const float* row = pb + (mt * 4 * NB + hh) * PROW + 2 * tig;
-          pp[mt][nb][0] = *reinterpret_cast<const float2*>(row);
-          pp[mt][nb][1] = *reinterpret_cast<const float2*>(row + 8);
+        for (int m = 0; m < 4; ++m) {
+          const float p = ex2_approx(l[nb][m] - m_run[nb]);  // 0 for a masked token
+          const float w = val[m] ? p * sv[m] : 0.f;
+          ps += p;
+          pz += val[m] ? p * zv[m] : 0.f;
+          pw += w;
+          const __half hi = __float2half_rn(w);
+          const __half lo = __float2half_rn(w - __half2float(hi));
+          pk[m][nb] = pack_half2(hi, lo);
         }
-        cacc[nb] = pb[PCORR / 4 + nb * 4 + tig];          // accumulator columns: head tig + 4 nb
-        czs[nb] = pb[PCORR / 4 + nb * 4 + (gid >> 1)];    // this lane's Z, S: head gid / 2 + 4 nb
+        l_run[nb] = fmaf(l_run[nb], corr[nb], ps);
+        zsum[nb] = fmaf(zsum[nb], corr[nb], pz);
+        ssum[nb] = fmaf(ssum[nb], corr[nb], pw);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&pE[pw][slot]));
-      uint32_t zs[2][4];  // [m-tile][tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9]: z/s words
-      {
-        uint32_t t0w, t1w, t2w, t3w, t4w, t5w, t6w, t7w;
-        lds_x4<VSTR>(sb + vzo, vstr, t0w, t2w, t4w, t6w);
-        lds_x4<VSTR>(sb + vzo + 4u, vstr, t1w, t3w, t5w, t7w);
-        zs[0][0] = t0w, zs[0][1] = t1w, zs[0][2] = t2w, zs[0][3] = t3w;
-        zs[1][0] = t4w, zs[1][1] = t5w, zs[1][2] = t6w, zs[1][3] = t7w;
-      }
-      const int rb = i * DT + WT * pw;  // split-relative first token of this warp's 32
-      const bool full_stage = (i + 1) * DT <= n_in;
-      uint32_t bp[2][NB][2];
-      float pz[NB], psw[NB];  // this stage's shares of Z and S (both m-tiles), folded in once below
+    };
+    if (r0 + WTOK <= n_in)
+      softmax(std::true_type{});
+    else
+      softmax(std::false_type{});
+    // ---- W into the value MMA's B layout: k = tile tokens 2 tig, 2 tig + 1 (+8), n = column gid ----
+    uint32_t bp[2][NB][2];
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) pz[nb] = psw[nb] = 0.f;
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const uint32_t x0 = __shfl_sync(0xffffffffu, pk[2 * mt][nb], srcA);
+        const uint32_t x1 = __shfl_sync(0xffffffffu, pk[2 * mt][nb], srcB);
+        const uint32_t x2 = __shfl_sync(0xffffffffu, pk[2 * mt + 1][nb], srcA);
+        const uint32_t x3 = __shfl_sync(0xffffffffu, pk[2 * mt + 1][nb], srcB);
+        bp[mt][nb][0] = __byte_perm(x0, x1, psel);
+        bp[mt][nb][1] = __byte_perm(x2, x3, psel);
+      }
+    // ---- M_j += W A_j: A = value codes (16 channels x 16 tokens) per m-tile; the stage's 32-token products are
+    // summed by the MMA from zero and folded into the running sums by round-to-nearest FMAs (acc = acc corr +
+    // stage): accumulating inside the MMA across all stages would bias these sums of positive terms by a rounding
+    // step per stage, which the near-cancellation of Z, S and M in the output magnifies ----
+#pragma unroll
+    for (int mb = 0; mb < NBLK; ++mb) {
+      // m-tile mt: records 8 mt + tig (tokens 2 tig, +1) and 8 mt + 4 + tig; channels gid (slot 0), gid + 8 (slot 1)
+      uint32_t af[2][4];
+      lds_x4<VSTR>(sb + (vd[mb][0] >> 5), vstr, af[0][0], af[0][2], af[1][0], af[1][2]);
+      lds_x4<VSTR>(sb + (vd[mb][1] >> 5), vstr, af[0][1], af[0][3], af[1][1], af[1][3]);
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        float zv[4], sv[4];
-        bool val[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&zs[mt][k]));
-          zv[k] = f.x;
-          sv[k] = f.y;
-          val[k] = full_stage || rb + 16 * mt + 2 * tig + (k & 1) + 8 * (k >> 1) < n_in;
-        }
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const float p4[4] = {pp[mt][nb][0].x, pp[mt][nb][0].y, pp[mt][nb][1].x, pp[mt][nb][1].y};
-          __half hv[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float wv = val[k] ? p4[k] * sv[k] : 0.f;
-            pz[nb] += val[k] ? p4[k] * zv[k] : 0.f;
-            psw[nb] += wv;
-            const __half hi = __float2half_rn(wv);
-            hv[k] = lo_part ? __float2half_rn(wv - __half2float(hi)) : hi;
-          }
-          bp[mt][nb][0] = pack_half2(hv[0], hv[1]);
-          bp[mt][nb][1] = pack_half2(hv[2], hv[3]);
-        }
+        af[mt][0] = slot_f16x2(af[mt][0], vd[mb][0], vm[mb][0]);
+        af[mt][1] = slot_f16x2(af[mt][1], vd[mb][1], vm[mb][1]);
+        af[mt][2] = slot_f16x2(af[mt][2], vd[mb][0], vm[mb][0]);
+        af[mt][3] = slot_f16x2(af[mt][3], vd[mb][1], vm[mb][1]);
       }
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
-        zsum[nb] = fmaf(zsum[nb], czs[nb], pz[nb]);
-        ssum[nb] = fmaf(ssum[nb], czs[nb], psw[nb]);
-      }
-      // accumulator columns 2 tig, 2 tig + 1 are head tig (+4 nb), fp16 hi and lo parts of W. The stage's 32-token
-      // products are summed by the MMA from zero and folded into the running sums by round-to-nearest FMAs
-      // (acc = acc corr + stage): accumulating inside the MMA across all stages would bias these sums of positive
-      // terms by a rounding step per stage, which the near-cancellation of Z, S and M in the output magnifies.
+        float tile[4];
+        mma_f16_zero(tile, af[0], bp[0][nb][0], bp[0][nb][1]);
+        mma_f16(tile, af[1], bp[1][nb][0], bp[1][nb][1]);
 #pragma unroll
-      for (int mb = 0; mb < NBLK; ++mb) {
-        // m-tile mt: records 8 mt + tig (tokens 2 tig, +1) and 8 mt + 4 + tig; channels gid (slot 0), gid + 8 (slot 1)
-        uint32_t af[2][4];
-        lds_x4<VSTR>(sb + (sd[mb][0] >> 5), vstr, af[0][0], af[0][2], af[1][0], af[1][2]);
-        lds_x4<VSTR>(sb + (sd[mb][1] >> 5), vstr, af[0][1], af[0][3], af[1][1], af[1][3]);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          af[mt][0] = slot_f16x2(af[mt][0], sd[mb][0], sm[mb][0]);
-          af[mt][1] = slot_f16x2(af[mt][1], sd[mb][1], sm[mb][1]);
-          af[mt][2] = slot_f16x2(af[mt][2], sd[mb][0], sm[mb][0]);
-          af[mt][3] = slot_f16x2(af[mt][3], sd[mb][1], sm[mb][1]);
-        }
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          float tile[4];
-          mma_f16_zero(tile, af[0], bp[0][nb][0], bp[0][nb][1]);
-          mma_f16(tile, af[1], bp[1][nb][0], bp[1][nb][1]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[mb][nb][e] = fmaf(acc[mb][nb][e], cacc[nb], tile[e]);
-        }
-      }
-      release_stage(i);
-    }
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const int h = tig + 4 * nb;
-      if (h < g) {
-        float* w = ws + (pw * 8 + h) * PSTR;
-#pragma unroll
-        for (int mb = 0; mb < NBLK; ++mb) {
-          if (mb < nmb) {
-            w[4 + mb * 16 + gid] = acc[mb][nb][0] + acc[mb][nb][1];
-            w[4 + mb * 16 + gid + 8] = acc[mb][nb][2] + acc[mb][nb][3];
-          }
-        }
-      }
-      // Z and S of head gid / 2 + 4 nb: the four tig lanes of an even gid hold the 16 tokens' shares
-      float zt = zsum[nb], st = ssum[nb];
-      zt += __shfl_xor_sync(0xffffffffu, zt, 1);
-      zt += __shfl_xor_sync(0xffffffffu, zt, 2);
-      st += __shfl_xor_sync(0xffffffffu, st, 1);
-      st += __shfl_xor_sync(0xffffffffu, st, 2);
-      const int hh = (gid >> 1) + 4 * nb;
-      if (hh < g && tig == 0 && !lo_part) {
-        float* w = ws + (pw * 8 + hh) * PSTR;
-        w[2] = zt;
-        w[3] = st;
+        for (int e = 0; e < 4; ++e) vacc[mb][nb][e] = fmaf(vacc[mb][nb][e], corr[nb], tile[e]);
       }
     }
+    release_stage(i);
   }
 
   __syncthreads();
-  float* part = a.part + ((size_t)bh * a.splits + split) * g * PSTR;
+  const DecEpi E = decode_epi(NW, NT);
+  float* const fs = reinterpret_cast<float*>(smem);
+  float* wpart = fs + E.wpart;  // [NW][g][PSTR]
+  float* mrg = fs + E.mrg;      // [g][PSTR]: the CTA's m, l, Z, S, M (rotated basis)
+  float* mg = fs + E.mg;        // [8][128]: merged M
+  float* hs = fs + E.hs;        // [8][4]: merged l, Z, S
+  float* esw = fs + E.esw;      // [MAX_SPLITS][8]: split weights
+  float* rot = fs + E.rot;
+  float* outp = a.out + ((size_t)b * a.Hq + (size_t)kh * g) * D;
   if (s_abort) {  // drain the copies this CTA may still have in flight, then leave an empty partial
     if (tid == 0) {
       const int issued = s_issued;
       for (int i = max(0, issued - NS); i < issued; ++i)
         mbar_wait_bounded(smem_u32(&full[i % NS]), (uint32_t)((i / NS) & 1), a.wait_ns);
     }
-    for (int idx = tid; idx < g * PSTR; idx += DTHREADS) part[idx] = (idx % PSTR) == 0 ? -INFINITY : 0.f;
+    __syncthreads();
+    for (int idx = tid; idx < g * PSTR; idx += NT) mrg[idx] = (idx % PSTR) == 0 ? -INFINITY : 0.f;
   } else {
-    // ======== this split's partial (rotated basis): the warp pairs' sums weighted by 2^(m_w - max_w m_w) ========
-    const int acols = 4 + nmb * 16;
-    for (int idx = tid; idx < g * acols; idx += DTHREADS) {
-      const int h = idx / acols, cidx = idx - h * acols;
+    // ======== the warps' partials (rotated basis) into shared memory: the ring is consumed ========
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      float lsum = l_run[nb], zt = zsum[nb], st = ssum[nb];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        zt += __shfl_xor_sync(0xffffffffu, zt, o);
+        st += __shfl_xor_sync(0xffffffffu, st, o);
+      }
+      const int h = tig + 4 * nb;
+      if (h < g) {
+        float* w = wpart + (warp * g + h) * PSTR;
+        if (gid == 0) {
+          w[0] = m_run[nb];
+          w[1] = lsum;
+          w[2] = zt;
+          w[3] = st;
+        }
+#pragma unroll
+        for (int mb = 0; mb < NBLK; ++mb)
+          if (mb < nmb) {
+            w[4 + mb * 16 + gid] = vacc[mb][nb][0] + vacc[mb][nb][1];
+            w[4 + mb * 16 + gid + 8] = vacc[mb][nb][2] + vacc[mb][nb][3];
+          }
+      }
+    }
+    __syncthreads();
+    // ---- the CTA's partial: the warps' sums weighted by 2^(m_w - max_w m_w) ----
+    const int icols = 4 + nzV;
+    for (int idx = tid; idx < g * icols; idx += NT) {
+      const int h = idx / icols, cidx = idx - h * icols;
+      float mw[NW];
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < DW; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
+      for (int w = 0; w < NW; ++w) {
+        mw[w] = wpart[(w * g + h) * PSTR];
+        M = fmaxf(M, mw[w]);
+      }
       float val = M;
       if (cidx > 0) {
         val = 0.f;
 #pragma unroll
-        for (int w = 0; w < DW; ++w) {
-          const float mw = ws[(w * 8 + h) * PSTR];
-          const float e = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
-          val = fmaf(e, ws[(w * 8 + h) * PSTR + cidx], val);
+        for (int w = 0; w < NW; ++w) {
+          const float e = (mw[w] == -INFINITY) ? 0.f : ex2_approx(mw[w] - M);
+          val = fmaf(e, wpart[(w * g + h) * PSTR + cidx], val);
         }
       }
-      part[h * PSTR + cidx] = val;
+      mrg[h * PSTR + cidx] = val;
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const bool last = atomicAdd(&a.cnt[bh], 1u) == (unsigned)(a.splits - 1);
-    if (last) a.cnt[bh] = 0u;  // every split has arrived: the counter is ready for the next call
-    s_last = last;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
 
-  // ======== last CTA of (b, kh): weighted sum of the split partials, then the map to the original basis ========
-  // T'_V arrives by one bulk copy while the partials arrive in chunks of splits; warp h (< g) keeps head h's running
-  // maximum M_h and rescales with the weights e_s = 2^(m_s - M_h) (lanes over the chunk's splits); every thread
-  // adds its items' sum e_s x_s (x: l, Z, S, M_j).
-  float* Tsc = reinterpret_cast<float*>(smem);                     // [nzV][128]
-  float* cp = reinterpret_cast<float*>(smem + L.chunks);           // chunk of split partials
-  float* mrg = reinterpret_cast<float*>(smem + L.tail_reserve);    // merged partial [8][PSTR]
-  float* escw = mrg + MAX_G * PSTR + 4 * MAX_G;                    // [MAX_SPLITS][8] weights of the chunk
-  float* hst = escw + MAX_SPLITS * MAX_G;                          // rescale of the running sums [8]
-  const float* pbp = a.part + (size_t)bh * a.splits * g * PSTR;
-  const int S = a.splits;
-  const uint32_t per_split = (uint32_t)g * PSTR * 4;
-  const int chunk_splits = max(1, min(S, min((int)((L.tail_reserve - L.chunks) / per_split), MAX_SPLITS)));
-  constexpr int ITEMS = (MAX_G * PSTR + DTHREADS - 1) / DTHREADS;
-  constexpr int SPL = MAX_SPLITS / 32;  // splits per lane within a chunk
-  const int icols = 4 + nzV;            // items of a head: m (unused), l, Z, S, M_0 .. M_(nzV - 1)
-  float accI[ITEMS];
-#pragma unroll
-  for (int r = 0; r < ITEMS; ++r) accI[r] = 0.f;
-  float M_run = -INFINITY;  // warp h's running maximum of head h
-  uint32_t tphase = 0;
-  fence_proxy_async_global();
-  if (tid == 0 && nzV > 0) {  // T'_V on its own barrier
-    fence_proxy_async_smem();
-    mbar_expect_tx(smem_u32(&vbar_s), (uint32_t)nzV * D * 4);
-    bulk_g2s(smem_u32(Tsc), TV.Tsc + so * D, (uint32_t)nzV * D * 4, smem_u32(&vbar_s));
-  }
-  for (int c0s = 0; c0s < S; c0s += chunk_splits) {
-    const int n = min(chunk_splits, S - c0s);
-    __syncthreads();  // previous chunk consumed
-    if (tid == 0) {
-      fence_proxy_async_smem();
-      mbar_expect_tx(smem_u32(tbar), (uint32_t)n * per_split);
-      bulk_g2s(smem_u32(cp), pbp + (size_t)c0s * g * PSTR, (uint32_t)n * per_split, smem_u32(tbar));
-    }
-    const bool okc = mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);
-    if (!okc && tid == 0) mbar_wait_bounded(smem_u32(tbar), tphase, a.wait_ns);  // drain before leaving
-    tphase ^= 1u;
-    if (!__syncthreads_and(okc)) return;
-    if (warp < g) {
+  if constexpr (CL) {
+    // ======== the cluster's splits merge through distributed shared memory; CTA r finishes columns
+    // [r 128 / CS, (r + 1) 128 / CS) of every head ========
+    cp_async_wait_all();  // this thread's share of the T'_V columns has landed
+    cluster_sync_all();   // every split's partial is complete (and every thread's copies, CTA-wide)
+    const uint32_t mrg_a = smem_u32(mrg);
+    if (warp < g) {  // head h = warp, lane = split: weights e_s = 2^(m_s - max m), merged l, Z, S
       const int h = warp;
-      float msp[SPL];
-      float cm = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < SPL; ++i) {
-        const int sp = lane + 32 * i;
-        msp[i] = sp < n ? cp[(sp * g + h) * PSTR] : -INFINITY;
-        cm = fmaxf(cm, msp[i]);
+      const bool in = lane < CS;
+      const uint32_t ra = dsmem_addr(mrg_a + (uint32_t)(h * PSTR) * 4u, in ? lane : 0);
+      const float ms = in ? ld_dsmem(ra) : -INFINITY;
+      const float ls = in ? ld_dsmem(ra + 4) : 0.f, zs = in ? ld_dsmem(ra + 8) : 0.f, ss = in ? ld_dsmem(ra + 12) : 0.f;
+      const float M = warp_max(ms);
+      const float e = ms == -INFINITY ? 0.f : ex2_approx(ms - M);
+      const float den = warp_sum(e * ls), zt = warp_sum(e * zs), st = warp_sum(e * ss);
+      if (in) esw[lane * MAX_G + h] = e;
+      if (lane == 0) {
+        hs[h * 4 + 0] = den;
+        hs[h * 4 + 1] = zt;
+        hs[h * 4 + 2] = st;
       }
-      cm = warp_max(cm);
-      const float Mn = fmaxf(M_run, cm);
-      const float sc = (M_run == Mn) ? 1.f : exp2f(M_run - Mn);
-#pragma unroll
-      for (int i = 0; i < SPL; ++i) {
-        const int sp = lane + 32 * i;
-        if (sp < n) escw[sp * MAX_G + h] = msp[i] == -INFINITY ? 0.f : exp2f(msp[i] - Mn);
-      }
-      M_run = Mn;
-      if (lane == 0) hst[h] = sc;
     }
     __syncthreads();
+    switch (CS) {  // merged M_j
+      case 16: cluster_merge_m<16, NT>(mrg_a, esw, mg, g, nzV); break;
+      case 8: cluster_merge_m<8, NT>(mrg_a, esw, mg, g, nzV); break;
+      case 4: cluster_merge_m<4, NT>(mrg_a, esw, mg, g, nzV); break;
+      case 2: cluster_merge_m<2, NT>(mrg_a, esw, mg, g, nzV); break;
+      default: cluster_merge_m<1, NT>(mrg_a, esw, mg, g, nzV); break;
+    }
+    cluster_sync_all();  // no split reads another's partial after this: each may finish and exit
+    const int KW = D / CS;
+    const float* tsl = reinterpret_cast<const float*>(smem + L.tsl);
+    rotate_out<NT>(tsl, tsl + D * KW, mg, hs, rot, g, KW, split * KW, nzV, outp);
+  } else {
+    // ======== the splits merge through the workspace: each leaves (m, l, Z, S, M) there, the last to arrive
+    // merges them and maps the result to the original basis ========
+    float* part = a.part + ((size_t)bh * a.splits + split) * g * PSTR;
+    for (int idx = tid; idx < g * (4 + nzV); idx += NT) {
+      const int h = idx / (4 + nzV), c = idx - h * (4 + nzV);
+      part[h * PSTR + c] = mrg[h * PSTR + c];
+    }
+    // arrival: thread 0's acquire-release add at GPU scope publishes the CTA's partial (ordered before it by the
+    // barrier) and, in the last CTA, makes the other splits' partials visible to the whole CTA after the next
+    // barrier
+    __syncthreads();
+    if (tid == 0) {
+      unsigned old;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.cnt + bh) : "memory");
+      const bool last = old == (unsigned)(a.splits - 1);
+      if (last) a.cnt[bh] = 0u;  // every split has arrived: the counter is ready for the next call
+      s_last = last;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    // the splits' partials in chunks of up to 32 splits, each staged by one round of 16-byte copies: warp h keeps
+    // head h's running maximum M_h, weights e_s = 2^(m_s - M_h) and the running l, Z, S; every thread keeps its
+    // items' sums of e_s M_sj
+    const float* pb = a.part + (size_t)bh * a.splits * g * PSTR;
+    const int S = a.splits;
+    float* chunk = fs + E.chunk;
+    float* tfull = fs + E.tfull;
+    const int per = min(32, (int)(MERGE_CHUNK / (uint32_t)(g * PSTR)));  // splits per chunk
+    constexpr int IT = (MAX_G * D + NT - 1) / NT;
+    float accI[IT];
 #pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
-      const int it = tid + r * DTHREADS;
-      const int h = it / PSTR, col = it - h * PSTR;
-      if (h < g && col >= 1 && col < icols) {
-        float acc = accI[r] * hst[h];
-        for (int sp = 0; sp < n; ++sp) acc = fmaf(escw[sp * MAX_G + h], cp[(sp * g + h) * PSTR + col], acc);
-        accI[r] = acc;
+    for (int r = 0; r < IT; ++r) accI[r] = 0.f;
+    float M_run = -INFINITY, den = 0.f, zt = 0.f, st = 0.f;
+    for (int s0 = 0; s0 < S; s0 += per) {
+      const int n = min(per, S - s0);
+      __syncthreads();  // the previous chunk is consumed
+      {
+        const uint32_t cdst = smem_u32(chunk);
+        const float* src = pb + (size_t)s0 * g * PSTR;
+        for (int c = tid; c < n * g * PSTR / 4; c += NT) cp_async16(cdst + 16u * c, src + 4 * c);
+        cp_async_commit();
+        if (s0 == 0) {  // T'_V and T_V^T mu, w, w2 (all 128 columns) follow the first chunk, landing meanwhile
+          const uint32_t tdst = smem_u32(tfull);
+          for (int c = tid; c < (D + 3) * (D / 4); c += NT) {
+            const int row = c >> 5, cc = c & 31;
+            const float* tsrc =
+                row < D ? TV.Tsc + (so + row) * D : (row == D ? TV.base : row == D + 1 ? TV.wsum : TV.wsum2) + so;
+            cp_async16(tdst + (uint32_t)(row * D + 4 * cc) * 4u, tsrc + 4 * cc);
+          }
+          cp_async_commit();
+          cp_async_wait_prior();
+        } else {
+          cp_async_wait_all();
+        }
+      }
+      __syncthreads();
+      if (warp < g) {
+        const int h = warp;
+        const float* ph = chunk + (size_t)min(lane, n - 1) * g * PSTR + h * PSTR;
+        const float ms = lane < n ? ph[0] : -INFINITY;
+        const float Mn = fmaxf(M_run, warp_max(ms));
+        const float sc = (M_run == Mn) ? 1.f : exp2f(M_run - Mn);
+        const float e = ms == -INFINITY ? 0.f : exp2f(ms - Mn);
+        den = fmaf(den, sc, warp_sum(e * ph[1]));
+        zt = fmaf(zt, sc, warp_sum(e * ph[2]));
+        st = fmaf(st, sc, warp_sum(e * ph[3]));
+        M_run = Mn;
+        if (lane < n) esw[lane * MAX_G + h] = e;
+        if (lane == 0) hs[h * 4 + 3] = sc;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < IT; ++r) {
+        const int idx = tid + NT * r;
+        if (idx < g * nzV) {
+          const int h = idx / nzV, j = idx - h * nzV;
+          float acc = accI[r] * hs[h * 4 + 3];
+          for (int sp = 0; sp < n; ++sp) acc = fmaf(esw[sp * MAX_G + h], chunk[(sp * g + h) * PSTR + 4 + j], acc);
+          accI[r] = acc;
+        }
       }
     }
-  }
 #pragma unroll
-  for (int r = 0; r < ITEMS; ++r) {
-    const int it = tid + r * DTHREADS;
-    const int h = it / PSTR, col = it - h * PSTR;
-    if (h < g && col >= 1 && col < icols) mrg[h * PSTR + col] = accI[r];
-  }
-  bool okv = true;
-  if (nzV > 0) okv = mbar_wait_bounded(smem_u32(&vbar_s), 0u, a.wait_ns);
-  if (!okv && tid == 0) mbar_wait_bounded(smem_u32(&vbar_s), 0u, a.wait_ns);  // drain before leaving
-  if (!__syncthreads_and(okv)) return;
-  // the map to the original basis: wph warps per head, each over a range of the rotated channels, lane = four
-  // original channels (a 128-bit segment of each T' row); the partial sums meet in shared memory
-  constexpr int NWARPS = DTHREADS / 32;
-  const int wph = max(1, NWARPS / g), h = warp / wph, qr = warp - h * wph;
-  float4* rbuf = reinterpret_cast<float4*>(cp);  // [NWARPS][32] (the chunks are consumed)
-  {
-    float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (h < g) {
-      const float* mh = mrg + h * PSTR;
-      const int j0 = nzV * qr / wph, j1 = nzV * (qr + 1) / wph;
-#pragma unroll 4
-      for (int jj = j0; jj < j1; ++jj) {
-        const float4 t = reinterpret_cast<const float4*>(Tsc + jj * D)[lane];
-        const float aj = mh[4 + jj];
-        n.x = fmaf(t.x, aj, n.x);
-        n.y = fmaf(t.y, aj, n.y);
-        n.z = fmaf(t.z, aj, n.z);
-        n.w = fmaf(t.w, aj, n.w);
-      }
+    for (int r = 0; r < IT; ++r) {
+      const int idx = tid + NT * r;
+      if (idx < g * nzV) mg[(idx / nzV) * D + idx % nzV] = accI[r];
     }
-    rbuf[warp * 32 + lane] = n;
-  }
-  __syncthreads();
-  if (h < g && qr == 0) {  // o_h[k] = base_k + (Z w_k - S w2_k + sum_j T'[j][k] M_j) / l
-    const float* mh = mrg + h * PSTR;
-    const float Lh = mh[1], zh = mh[2], sh = mh[3];
-    const float4 w4 = reinterpret_cast<const float4*>(TV.wsum + so)[lane];
-    const float4 v4 = reinterpret_cast<const float4*>(TV.wsum2 + so)[lane];
-    const float4 b4 = reinterpret_cast<const float4*>(TV.base + so)[lane];
-    float4 n = make_float4(fmaf(zh, w4.x, -sh * v4.x), fmaf(zh, w4.y, -sh * v4.y), fmaf(zh, w4.z, -sh * v4.z),
-                           fmaf(zh, w4.w, -sh * v4.w));
-    for (int q = 0; q < wph; ++q) {
-      const float4 r = rbuf[(h * wph + q) * 32 + lane];
-      n.x += r.x;
-      n.y += r.y;
-      n.z += r.z;
-      n.w += r.w;
+    if (warp < g && lane == 0) {
+      hs[warp * 4 + 0] = den;
+      hs[warp * 4 + 1] = zt;
+      hs[warp * 4 + 2] = st;
     }
-    const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
-    float4 o = make_float4(b4.x + n.x * inv, b4.y + n.y * inv, b4.z + n.z * inv, b4.w + n.w * inv);
-    if (!(Lh > 0.f)) o = make_float4(0.f, 0.f, 0.f, 0.f);
-    reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + (size_t)kh * g + h) * D)[lane] = o;
+    cp_async_wait_all();
+    __syncthreads();
+    rotate_out<NT>(tfull, tfull + D * D, mg, hs, rot, g, D, 0, nzV, outp);
   }
 }
 
@@ -869,7 +905,7 @@ static void split_plan(int B, int Hkv, int64_t T_cap, int device, int tile, int 
 DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device) {
   DecodeLayout L{};
   const int g = Hq / Hkv;
-  split_plan(B, Hkv, T_cap, device, dec_stage_tokens(g <= 4 ? 1 : 2), 1, MAX_SPLITS, &L.splits, &L.chunk);
+  split_plan(B, Hkv, T_cap, device, WTOK, 1, MAX_SPLITS, &L.splits, &L.chunk);
   const size_t bh = (size_t)B * Hkv;
   size_t o = 0;
   L.off_cnt = o;
@@ -880,20 +916,122 @@ DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device) {
   return L;
 }
 
+// Largest number of clusters of cs CTAs of kernel fn (with this launch's block and shared memory) that the device
+// holds at once; asked once per (kernel, shared memory, cluster size, device). 0 when the device cannot run one.
+static int max_active_clusters(const void* fn, const cudaLaunchConfig_t& base, int cs) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, size_t, int, int>, int> known;
+  const int dev = current_device();
+  const auto key = std::make_tuple(fn, base.dynamicSmemBytes, cs, dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = known.find(key);
+    if (it != known.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = base;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)cs;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)cs, 1, 1);
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    n = 0;
+    cudaGetLastError();  // the query's error is not the caller's
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  known[key] = n;
+  return n;
+}
+
+// Cluster sizes above eight need the kernel's consent, given once per (kernel, device).
+static cudaError_t allow_large_clusters(const void* fn) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, bool> done;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  bool& d = done[{fn, dev}];
+  if (d) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) d = true;
+  return e;
+}
+
+// One launch of decode_kernel<NB, RK, RV, NBLK, *>. The splits of each (sequence, KV head) form a thread-block
+// cluster when the device holds all B * Hkv clusters at once with a cluster size that keeps at least half the SMs
+// busy (sizes 16, 8, 4, 2, 1 tried in turn, each at most SMs / (B * Hkv)); otherwise (few sequence-head pairs)
+// the workspace's split plan applies and the splits merge through global memory. plan != nullptr: fill the plan
+// (cluster size or 0, splits, stages, warps, channel blocks, shared memory, clusters held for sizes 16 .. 1 or -1
+// when not asked) and launch nothing.
 template <int NB, int RK, int RV, int NBLK>
-static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a) {
-  const cudaError_t e = ensure_dyn_smem((const void*)decode_kernel<NB, RK, RV, NBLK>, cfg.dynamicSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RK, RV, NBLK>, P, a);
+static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, DecArgs a, int ws_splits,
+                                        int32_t* plan) {
+  const int rk = P.t[0].r_words, rv = P.t[1].r_words;
+  const int bh = a.B * a.Hkv, sms = sm_count(current_device());
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (plan)
+    for (int i = 0; i < 11; ++i) plan[i] = i >= 6 ? -1 : 0;
+  if (16 * bh >= sms / 2) {
+    const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, true>;
+    if ((e = allow_large_clusters(fn)) != cudaSuccess) return e;
+    const int cap = std::max(1, sms / bh);
+    for (int cs = 16, slot = 6; cs >= 1; cs >>= 1, ++slot) {
+      if (cs > cap) continue;
+      cudaLaunchConfig_t c = cfg;
+      const int stages = ring_stages_for(rk, rv, NB, NBLK, cs);
+      c.dynamicSmemBytes = decode_smem(rk, rv, stages, NB, NBLK, cs).total;
+      if ((e = ensure_dyn_smem(fn, c.dynamicSmemBytes)) != cudaSuccess) return e;
+      const int held = cs == 1 ? bh : max_active_clusters(fn, c, cs);
+      if (plan) plan[slot] = held;
+      if (held < bh) continue;
+      if (cs * bh < sms / 2) break;  // too few CTAs: the workspace plan does better
+      a.splits = cs;
+      a.stages = stages;
+      if (plan) {
+        plan[0] = cs, plan[1] = cs, plan[2] = stages, plan[3] = dec_warps(NB, NBLK), plan[4] = NBLK;
+        plan[5] = (int32_t)c.dynamicSmemBytes;
+        return cudaSuccess;
+      }
+      c.gridDim.x = (unsigned)cs;
+      at[1].id = cudaLaunchAttributeClusterDimension;
+      at[1].val.clusterDim.x = (unsigned)cs;
+      at[1].val.clusterDim.y = 1;
+      at[1].val.clusterDim.z = 1;
+      c.attrs = at;
+      c.numAttrs = 2;
+      return cudaLaunchKernelEx(&c, decode_kernel<NB, RK, RV, NBLK, true>, P, a);
+    }
+  }
+  const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, false>;
+  a.splits = ws_splits;
+  a.stages = ring_stages_for(rk, rv, NB, NBLK, 0);
+  cfg.gridDim.x = (unsigned)ws_splits;
+  cfg.dynamicSmemBytes = decode_smem(rk, rv, a.stages, NB, NBLK, 0).total;
+  if (plan) {
+    plan[0] = 0, plan[1] = ws_splits, plan[2] = a.stages, plan[3] = dec_warps(NB, NBLK), plan[4] = NBLK;
+    plan[5] = (int32_t)cfg.dynamicSmemBytes;
+    return cudaSuccess;
+  }
+  if ((e = ensure_dyn_smem(fn, cfg.dynamicSmemBytes)) != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RK, RV, NBLK, false>, P, a);
 }
 
 // record lengths with a compile-time decode kernel: equal key and value budgets of 1.25 - 4 bits/element and the
 // joint key/value splits of the Llama-shaped layer at 2.75, 2 and 1.33 bits/element
 template <int NB, int NBLK>
-static cudaError_t launch_decode_rw(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a) {
+static cudaError_t launch_decode_rw(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a, int ws_splits,
+                                    int32_t* plan) {
   const int rk = P.t[0].r_words, rv = P.t[1].r_words;
 #define KVTC_DECODE_RW(K, V) \
-  if (rk == K && rv == V) return launch_decode_kernel<NB, K, V, NBLK>(cfg, P, a);
+  if (rk == K && rv == V) return launch_decode_kernel<NB, K, V, NBLK>(cfg, P, a, ws_splits, plan);
   KVTC_DECODE_RW(5, 5)
   KVTC_DECODE_RW(6, 4)
   KVTC_DECODE_RW(8, 8)
@@ -903,14 +1041,14 @@ static cudaError_t launch_decode_rw(cudaLaunchConfig_t& cfg, const ParamsDev& P,
   KVTC_DECODE_RW(14, 8)
   KVTC_DECODE_RW(10, 6)
 #undef KVTC_DECODE_RW
-  return launch_decode_kernel<NB, 0, 0, NBLK>(cfg, P, a);
+  return launch_decode_kernel<NB, 0, 0, NBLK>(cfg, P, a, ws_splits, plan);
 }
 
 kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
                         const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
-                        cudaStream_t s) {
+                        cudaStream_t s, int32_t* plan) {
   DecArgs a;
-  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint8_t* w = static_cast<uint8_t*>(ws);  // null when only planning
   a.rec[0] = c.k_rec;
   a.rec[1] = c.v_rec;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -926,26 +1064,30 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   a.g = Hq / c.Hkv;
   a.per_seq = c.per_seq_params;
   a.splits = L.splits;
-  const int nb = a.g <= 4 ? 1 : 2;
-  a.stages = ring_stages_for(P.t[0].r_words, P.t[1].r_words, nb);
+  a.stages = 2;
   a.scale_log2 = scale * 1.4426950408889634f;
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  const int nblk = std::max(P.t[0].max_nz, P.t[1].max_nz) <= 64 ? 4 : 8;
-  const size_t smem = decode_smem(P.t[0].r_words, P.t[1].r_words, a.stages, nb).total;
+  const int nb = a.g <= 4 ? 1 : 2;
+  const int rk = P.t[0].r_words, rv = P.t[1].r_words;
+  // four channel blocks when every set's nonzero channels fit them and two stages of sixteen warps fit the ring
+  const int nblk =
+      (std::max(P.t[0].max_nz, P.t[1].max_nz) <= 64 && 2 * dec_stage_tokens(nb, 4) * (rk + rv) * 4 <= RING_BUDGET) ? 4
+                                                                                                                   : 8;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.splits, c.Hkv, B);
-  cfg.blockDim = dim3(dec_threads(nb));
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(dec_threads(nb, nblk));
   cfg.stream = s;
-  cfg.attrs = pdl;
-  cfg.numAttrs = 1;
   cudaError_t e;
   if (nb == 1)
-    e = nblk == 4 ? launch_decode_rw<1, 4>(cfg, P, a) : launch_decode_rw<1, 8>(cfg, P, a);
+    e = nblk == 4 ? launch_decode_rw<1, 4>(cfg, P, a, L.splits, plan) : launch_decode_rw<1, 8>(cfg, P, a, L.splits, plan);
   else
-    e = nblk == 4 ? launch_decode_rw<2, 4>(cfg, P, a) : launch_decode_rw<2, 8>(cfg, P, a);
+    e = nblk == 4 ? launch_decode_rw<2, 4>(cfg, P, a, L.splits, plan) : launch_decode_rw<2, 8>(cfg, P, a, L.splits, plan);
+  if (plan) {
+    if (e != cudaSuccess) {
+      set_error("decode plan: %s", cudaGetErrorString(e));
+      return KV_ERR_CUDA;
+    }
+    return KV_OK;
+  }
   if (e != cudaSuccess) {
     set_error("decode_kernel launch: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;

@@ -1173,6 +1173,23 @@ extern "C" kv_status kv_debug_set_wait_limit_ns(long long ns) {
   return KV_OK;
 }
 
+extern "C" kv_status kv_debug_decode_plan(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap,
+                                          int32_t* info) {
+  clear_error();
+  kv_status st;
+  int dev = 0;
+  if ((st = check_params_on_device(p, &dev)) != KV_OK) return st;
+  KV_REQUIRE(info && B >= 1 && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0 && Hq / Hkv <= MAX_G && T_cap >= 16 &&
+                 T_cap % 16 == 0,
+             KV_ERR_INVALID_ARG, "kv_debug_decode_plan: bad argument");
+  kv_cache c{};
+  c.B = B;
+  c.Hkv = Hkv;
+  c.T_cap = T_cap;
+  const DecodeLayout L = kvtc::decode_layout(B, Hkv, Hq, T_cap, dev);
+  return kvtc::launch_decode(p->dev, c, nullptr, B, Hq, nullptr, 1.f, nullptr, nullptr, L, nullptr, info);
+}
+
 extern "C" kv_status kv_debug_wait_timeout_selftest(kv_stream_t stream) {
   clear_error();
   return kvtc::launch_wait_selftest((cudaStream_t)stream);

@@ -69,9 +69,10 @@ struct DecodeLayout {
 };
 DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device);
 DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device);
+// plan != nullptr: fill plan[11] (see kv_debug_decode_plan) and launch nothing
 kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
                         const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
-                        cudaStream_t s);
+                        cudaStream_t s, int32_t* plan = nullptr);
 // (dev: receives the current device, which holds the parameter table)
 kv_status check_decode_args(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
                             const int32_t* seq_lens_dev, float softmax_scale, const float* out, int* dev);

@@ -27,6 +27,7 @@
 #include <algorithm>
 #include <atomic>
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <utility>
 

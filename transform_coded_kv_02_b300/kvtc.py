@@ -79,6 +79,7 @@ _sig("kv_debug_eigh", c_int, [_P, c_int, _P, _P])
 _sig("kv_debug_set_encode_path", c_int, [c_int])
 _sig("kv_debug_set_wait_limit_ns", c_int, [ctypes.c_longlong])
 _sig("kv_debug_wait_timeout_selftest", c_int, [_P])
+_sig("kv_debug_decode_plan", c_int, [_P, c_int, c_int, c_int, ctypes.c_int64, _P])
 
 
 class KvError(RuntimeError):
@@ -301,6 +302,15 @@ def kv_debug_set_encode_path(path):
 
 def kv_debug_set_wait_limit_ns(ns):
     _check("kv_debug_set_wait_limit_ns", _lib.kv_debug_set_wait_limit_ns(ns))
+
+
+def kv_debug_decode_plan(params, B, Hkv, Hq, T_cap):
+    """The decode launch plan (see include/kvtc.h) as a dict."""
+    info = (ctypes.c_int32 * 11)()
+    _check("kv_debug_decode_plan", _lib.kv_debug_decode_plan(params.handle, B, Hkv, Hq, T_cap, info))
+    v = list(info)
+    return {"cluster": v[0], "splits": v[1], "stages": v[2], "warps": v[3], "channel_blocks": v[4],
+            "smem_bytes": v[5], "clusters_held": dict(zip((16, 8, 4, 2, 1), v[6:11]))}
 
 
 def kv_debug_wait_timeout_selftest(stream=None):
