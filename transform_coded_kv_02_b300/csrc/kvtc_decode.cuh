@@ -45,11 +45,11 @@ constexpr int MAX_STAGES = 8;
 constexpr int MAX_SPLITS = 256;
 constexpr int HC = 4;                  // per-head constants: C0, C1, C2, 2^-e
 
-// Warps per CTA: sixteen when the per-lane operand arrays fit 128 registers (one 8-column block of heads, at most
-// four 16-channel blocks), eight otherwise.
-__host__ __device__ constexpr int dec_warps(int nb, int nblk) { return (nb == 1 && nblk <= 4) ? 16 : 8; }
-__host__ __device__ constexpr int dec_threads(int nb, int nblk) { return 32 * dec_warps(nb, nblk); }
-__host__ __device__ constexpr int dec_stage_tokens(int nb, int nblk) { return WTOK * dec_warps(nb, nblk); }
+// Warps per CTA (nw): sixteen for one 8-column block of heads when two stages of 512 tokens fit the ring (more
+// than four 16-channel blocks then keep their slot descriptors and q' operands in shared memory, so that a thread
+// fits 128 registers), eight otherwise.
+__host__ __device__ constexpr bool dec_desc_smem(int nw, int nblk) { return nw == 16 && nblk > 4; }
+__host__ __device__ constexpr int dec_stage_tokens(int nw) { return WTOK * nw; }
 
 struct DecArgs {
   const uint32_t* rec[2];
@@ -78,8 +78,11 @@ __device__ __forceinline__ float warp_max(float v) {
 __host__ __device__ __forceinline__ uint32_t align128u(uint32_t x) { return (x + 127u) & ~127u; }
 
 struct DecSmem {  // byte offsets into the dynamic shared memory of decode_kernel
-  uint32_t stage_bytes, qa, hc, pro, tsl, total;
+  uint32_t stage_bytes, qa, hc, tab, pro, tsl, total;
 };
+// slot descriptor tables: keys [8 blocks][4 tig][2 slots] and values [8 blocks][8 gid][2 slots] of (descriptor,
+// mask), then the logit MMA's B fragments per lane [8 blocks][32 lanes] (two words)
+constexpr uint32_t TAB_BYTES = (8u * 4u * 2u + 8u * 8u * 2u) * 8u + 8u * 32u * 8u;
 constexpr uint32_t SMEM_LIMIT = 227u * 1024u;   // dynamic shared memory a CTA may hold
 constexpr uint32_t SMEM_STATIC = 1024u;         // room left for the kernel's static shared variables
 
@@ -112,27 +115,28 @@ __host__ __device__ inline DecEpi decode_epi(int nw, int nt) {
 }
 
 // [0, qa): the ring of record stages, then the epilogue scratch above | qa: q' operands [16 columns][128] fp16 |
-// hc: per-head constants [8][HC] | pro: prologue scratch (q [8][128], partial q~ [QPARTS][8][128], coefficient
+// hc: per-head constants [8][HC] | tab: slot descriptor tables | pro: prologue scratch (q [8][128], partial q~ [QPARTS][8][128], coefficient
 // scales [8]) | tsl (cluster merge, cs > 0): this CTA's columns of T'_V [128][128 / cs] and of T_V^T mu, w, w2
 // [3][128 / cs]
-__host__ __device__ inline DecSmem decode_smem(int RK, int RV, int stages, int nb, int nblk, int cs) {
+__host__ __device__ inline DecSmem decode_smem(int RK, int RV, int stages, int nw, int cs) {
   DecSmem s;
-  const int nt = dec_threads(nb, nblk), parts = nt / D, nw = nt / 32;
-  s.stage_bytes = (uint32_t)dec_stage_tokens(nb, nblk) * (RK + RV) * 4u;
+  const int nt = 32 * nw, parts = nt / D;
+  s.stage_bytes = (uint32_t)dec_stage_tokens(nw) * (RK + RV) * 4u;
   const uint32_t ring = (uint32_t)stages * s.stage_bytes;
   const uint32_t epi = decode_epi(nw, nt).end * 4u;
   const uint32_t r = ring > epi ? ring : epi;
   s.qa = align128u(r);
   s.hc = s.qa + 16u * D * 2u;
-  s.pro = align128u(s.hc + MAX_G * HC * 4u);
+  s.tab = align128u(s.hc + MAX_G * HC * 4u);
+  s.pro = align128u(s.tab + TAB_BYTES);
   s.tsl = align128u(s.pro + (uint32_t)(MAX_G * D + parts * MAX_G * D + MAX_G) * 4u);
   s.total = s.tsl + (cs > 0 ? (uint32_t)(D + 3) * (D / cs) * 4u : 0u);
   return s;
 }
 
 // ring stages: as many as RING_BUDGET (and the CTA's shared memory left beside the other regions) holds, 2 to 8
-__host__ __device__ inline int ring_stages_for(int RK, int RV, int nb, int nblk, int cs) {
-  const DecSmem z = decode_smem(RK, RV, 0, nb, nblk, cs);
+__host__ __device__ inline int ring_stages_for(int RK, int RV, int nw, int cs) {
+  const DecSmem z = decode_smem(RK, RV, 0, nw, cs);
   const uint32_t other = z.total - z.qa;
   uint32_t budget = SMEM_LIMIT - SMEM_STATIC - other;
   budget = budget < (uint32_t)RING_BUDGET ? budget : (uint32_t)RING_BUDGET;
@@ -142,34 +146,30 @@ __host__ __device__ inline int ring_stages_for(int RK, int RV, int nb, int nblk,
 
 // The map of merged rotated-basis sums to the original basis for output columns [k0, k0 + KW) of every head:
 // o_k = (l base_k + Z w_k - S w2_k + sum_j T'[j][k] M_j) / l, with tsl = T' columns [128][KW], bsl = base, w, w2
-// columns [3][KW], mg = merged M [8][128], hs = merged (l, Z, S) [8][4]. Thread (row block, column) sums its rows
-// for every head (one T' element serves all heads); rot [NT / KW][8][KW] gathers the row blocks' sums.
+// columns [3][KW], mg = merged M [8][128] (16-byte aligned, zero past nzV up to a multiple of four), hs = merged
+// (l, Z, S) [8][4]. Thread (row block, column) sums its rows for every head (one T' element serves all heads, one
+// 16-byte load four rows of M); rot [NT / KW][8][KW] gathers the row blocks' sums.
 template <int NT>
 __device__ __forceinline__ void rotate_out(const float* tsl, const float* bsl, const float* mg, const float* hs,
                                            float* rot, int g, int KW, int k0, int nzV, float* outp) {
   const int tid = threadIdx.x;
   const int JP = NT / KW, kl = tid % KW, jp = tid / KW;
-  const int j0 = nzV * jp / JP, j1 = nzV * (jp + 1) / JP;
+  const int n4 = (nzV + 3) >> 2;  // groups of four rows (rows past nzV are zero in T' and in mg)
+  const int q0 = n4 * jp / JP, q1 = n4 * (jp + 1) / JP;
   float acc[MAX_G];
 #pragma unroll
   for (int h = 0; h < MAX_G; ++h) acc[h] = 0.f;
-  int j = j0;
-  for (; j + 4 <= j1; j += 4) {  // four rows per step: their loads in flight together
+  for (int q = q0; q < q1; ++q) {
+    const int j = 4 * q;
     float t[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) t[u] = tsl[(j + u) * KW + kl];
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h)
       if (h < g) {
-        const float* m = mg + h * D + j;
-        acc[h] = fmaf(t[0], m[0], fmaf(t[1], m[1], fmaf(t[2], m[2], fmaf(t[3], m[3], acc[h]))));
+        const float4 m = *reinterpret_cast<const float4*>(mg + h * D + j);
+        acc[h] = fmaf(t[0], m.x, fmaf(t[1], m.y, fmaf(t[2], m.z, fmaf(t[3], m.w, acc[h]))));
       }
-  }
-  for (; j < j1; ++j) {
-    const float t = tsl[j * KW + kl];
-#pragma unroll
-    for (int h = 0; h < MAX_G; ++h)
-      if (h < g) acc[h] = fmaf(t, mg[h * D + j], acc[h]);
   }
 #pragma unroll
   for (int h = 0; h < MAX_G; ++h)
@@ -255,9 +255,9 @@ __device__ __forceinline__ void slot_decode_desc(uint32_t stage_off, uint32_t r,
 // blocks processed per tensor (blocks past a set's last nonzero-width channel hold zero masks and coefficients).
 // CL: the splits of a (sequence, head) form one thread-block cluster (gridDim.x = cluster size) and merge through
 // distributed shared memory; otherwise they merge through the workspace, the last to arrive doing the merge.
-template <int NB, int RK_, int RV_, int NBLK, bool CL>
-__global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(ParamsDev P, DecArgs a) {
-  constexpr int NW = dec_warps(NB, NBLK), NT = 32 * NW, ST = WTOK * NW;
+template <int NB, int RK_, int RV_, int NBLK, bool CL, int NW>
+__global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs a) {
+  constexpr int NT = 32 * NW, ST = WTOK * NW;
   constexpr int QPARTS = NT / D, KQ = D / QPARTS;  // q preparation: threads per channel, k's per thread
   extern __shared__ __align__(128) uint8_t smem[];
   // barriers live outside the dynamic region, which the epilogue reuses wholesale
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(Params
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   const size_t so = (size_t)set * D;
   const int CS = CL ? a.splits : 0;  // cluster size
-  const DecSmem L = decode_smem(RK, RV, NS, NB, NBLK, CS);
+  const DecSmem L = decode_smem(RK, RV, NS, NW, CS);
   const uint32_t stage_bytes = L.stage_bytes;
   __half* qa = reinterpret_cast<__half*>(smem + L.qa);  // [16 columns][128 channels]
   float* hc = reinterpret_cast<float*>(smem + L.hc);    // [8 heads][HC]
@@ -293,14 +293,22 @@ __global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(Params
   // key slots: pair 8 kb + 4 i + tig of token rows 32 warp + gid (+ 8, 16, 24); value slots: channel 16 mb + 8 i +
   // gid of the two-token records 16 warp + tig (+ 4, 8, 12)
   const int nzK = __ldg(TK.nz + set), nzV = __ldg(TV.nz + set);
-  uint32_t kd[NBLK][2], km[NBLK][2], vd[NBLK][2], vm[NBLK][2];  // raw slot entries first, descriptors later
+  constexpr bool DS = dec_desc_smem(NW, NBLK);
+  constexpr int NR = DS ? 1 : NBLK;  // blocks whose descriptors and q' operands live in registers
+  uint32_t kd[NR][2], km[NR][2], vd[NR][2], vm[NR][2];  // raw slot entries first, descriptors later
+  uint32_t rawk = 0u, rawv = 0u;  // DS: the table entry this thread fills (entry e is slot e)
+  if constexpr (DS) {
+    if (tid < NBLK * 8) rawk = __ldg(TK.slots + so + tid);
+    if (tid < NBLK * 16) rawv = __ldg(TV.slots + so + tid);
+  } else {
 #pragma unroll
-  for (int kb = 0; kb < NBLK; ++kb)
+    for (int kb = 0; kb < NBLK; ++kb)
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      kd[kb][i] = __ldg(TK.slots + so + 8 * kb + 4 * i + tig);
-      vd[kb][i] = __ldg(TV.slots + so + 16 * kb + 8 * i + gid);
-    }
+      for (int i = 0; i < 2; ++i) {
+        kd[kb][i] = __ldg(TK.slots + so + 8 * kb + 4 * i + tig);
+        vd[kb][i] = __ldg(TV.slots + so + 16 * kb + 8 * i + gid);
+      }
+  }
   if constexpr (CL) {  // this CTA's output columns of T'_V and of T_V^T mu, w, w2, copied while the CTA works
     const int KW = D / CS, k0 = split * KW, cpr = KW / 4;  // 16-byte chunks per row
     const uint32_t tdst = smem_u32(smem + L.tsl);
@@ -394,20 +402,42 @@ __global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(Params
   }
   // slot descriptors (blocks past the set's last nonzero-width channel get zero masks)
   const int nkb = (nzK + 15) >> 4, nmb = (nzV + 15) >> 4;
-#pragma unroll
-  for (int kb = 0; kb < NBLK; ++kb)
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t dk = kb < nkb ? kd[kb][i] : 0u;
+  // byte offsets of this lane's key token row (gid of the warp's block) and value record (tig) in a stage
+  const uint32_t krow = (uint32_t)(WTOK * warp + gid) * RK * 4u;
+  const uint32_t vrow = (uint32_t)ST * RK * 4u + (uint32_t)((WTOK / 2) * warp + tig) * 2u * RV * 4u;
+  uint2* const ktab = reinterpret_cast<uint2*>(smem + L.tab);  // [NBLK][4 tig][2 slots]: descriptor, mask
+  uint2* const vtab = ktab + 8 * 4 * 2;                         // [NBLK][8 gid][2 slots]
+  uint2* const qfrag = vtab + 8 * 8 * 2;                        // [NBLK][32 lanes]: logit B fragments
+  if constexpr (DS) {  // record-relative descriptors; the lanes add their row offsets
+    if (tid < NBLK * 8) {  // key slot 8 kb + 4 i + t
+      const int kb = tid >> 3, i = (tid >> 2) & 1, t = tid & 3;
+      const uint32_t dk = kb < nkb ? rawk : 0u;
       const uint32_t b0 = (dk >> 16) & 255u, b1 = dk >> 24, w = b0 > b1 ? b0 : b1;
-      const uint32_t off = (uint32_t)(WTOK * warp + gid) * RK * 4u + 4u * (1u + (dk & 255u));
-      slot_decode_desc(off, (dk >> 8) & 255u, w, b0, b1, kd[kb][i], km[kb][i]);
-      const uint32_t dv = kb < nmb ? vd[kb][i] : 0u;
-      const uint32_t bw = (dv >> 16) & 255u;
-      const uint32_t voff = (uint32_t)ST * RK * 4u + (uint32_t)((WTOK / 2) * warp + tig) * 2u * RV * 4u +
-                            4u * (2u + (dv & 255u));
-      slot_decode_desc(voff, (dv >> 8) & 255u, bw, bw, bw, vd[kb][i], vm[kb][i]);
+      uint2 e;
+      slot_decode_desc(4u * (1u + (dk & 255u)), (dk >> 8) & 255u, w, b0, b1, e.x, e.y);
+      ktab[(kb * 4 + t) * 2 + i] = e;
     }
+    if (tid < NBLK * 16) {  // value channel 16 mb + 8 i + c
+      const int mb = tid >> 4, i = (tid >> 3) & 1, c = tid & 7;
+      const uint32_t dv = mb < nmb ? rawv : 0u;
+      const uint32_t bw = (dv >> 16) & 255u;
+      uint2 e;
+      slot_decode_desc(4u * (2u + (dv & 255u)), (dv >> 8) & 255u, bw, bw, bw, e.x, e.y);
+      vtab[(mb * 8 + c) * 2 + i] = e;
+    }
+  } else {
+#pragma unroll
+    for (int kb = 0; kb < NBLK; ++kb)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t dk = kb < nkb ? kd[kb][i] : 0u;
+        const uint32_t b0 = (dk >> 16) & 255u, b1 = dk >> 24, w = b0 > b1 ? b0 : b1;
+        slot_decode_desc(krow + 4u * (1u + (dk & 255u)), (dk >> 8) & 255u, w, b0, b1, kd[kb][i], km[kb][i]);
+        const uint32_t dv = kb < nmb ? vd[kb][i] : 0u;
+        const uint32_t bw = (dv >> 16) & 255u;
+        slot_decode_desc(vrow + 4u * (2u + (dv & 255u)), (dv >> 8) & 255u, bw, bw, bw, vd[kb][i], vm[kb][i]);
+      }
+  }
 
   // ---- q preparation: per-head constants from dot products of q with the folded vectors, then
   // q~ = T_K q and the MMA coefficients Q_j 2^(w_j - b_j) 2^e_h as fp16 hi + lo pairs ----
@@ -484,14 +514,22 @@ __global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(Params
       }
     }
     __syncthreads();
+    if constexpr (DS) {  // each lane's B fragments of every channel block, one 8-byte row per lane
+      if (tid < NBLK * 32) {
+        const int kb = tid >> 5, ln = tid & 31, col = ln >> 2, t = ln & 3;
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qa);
+        qfrag[tid] = make_uint2(q32[(col * D + kb * 16 + 2 * t) >> 1], q32[(col * D + kb * 16 + 8 + 2 * t) >> 1]);
+      }
+      __syncthreads();
+    }
   }
 
   // ============ main loop: warp w owns tokens [32 w, 32 w + 32) of every stage ============
   // B operand of the logit MMA: coefficients, k = channels 16 kb + 2 tig (+1, +8, +9), n = column gid (head
   // gid / 2 + 4 nb, fp16 hi part for even gid, lo part for odd gid)
-  uint32_t qb[NBLK][NB][2];
-  {
-    const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(qa);
+  const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(qa);
+  uint32_t qb[NR][NB][2];  // (DS: read from qa at each use)
+  if constexpr (!DS) {
 #pragma unroll
     for (int kb = 0; kb < NBLK; ++kb)
 #pragma unroll
@@ -555,17 +593,39 @@ __global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(Params
           acc[mt][pr][nb][0] = acc[mt][pr][nb][1] = acc[mt][pr][nb][2] = acc[mt][pr][nb][3] = 0.f;
 #pragma unroll
     for (int kb = 0; kb < NBLK; ++kb) {
+      if (kb >= nkb) break;  // blocks past the set's last nonzero-width key channel (the same for the whole CTA)
+      uint32_t d0, m0, d1, m1, a0, a1;  // the two slots' descriptors, masks and stage addresses
+      if constexpr (DS) {
+        const uint4 e = reinterpret_cast<const uint4*>(ktab)[kb * 4 + tig];
+        d0 = e.x, m0 = e.y, d1 = e.z, m1 = e.w;
+        a0 = sb + krow + (d0 >> 5), a1 = sb + krow + (d1 >> 5);
+      } else {
+        d0 = kd[kb][0], m0 = km[kb][0], d1 = kd[kb][1], m1 = km[kb][1];
+        a0 = sb + (d0 >> 5), a1 = sb + (d1 >> 5);
+      }
       uint32_t af[2][4];  // rows gid, gid + 8 (m-tile 0), gid + 16, gid + 24 (m-tile 1)
-      lds_x4<KSTR>(sb + (kd[kb][0] >> 5), kstr, af[0][0], af[0][1], af[1][0], af[1][1]);
-      lds_x4<KSTR>(sb + (kd[kb][1] >> 5), kstr, af[0][2], af[0][3], af[1][2], af[1][3]);
+      lds_x4<KSTR>(a0, kstr, af[0][0], af[0][1], af[1][0], af[1][1]);
+      lds_x4<KSTR>(a1, kstr, af[0][2], af[0][3], af[1][2], af[1][3]);
+      uint32_t bq[NB][2];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        if constexpr (DS) {  // (one column block)
+          const uint2 f = qfrag[kb * 32 + lane];
+          bq[nb][0] = f.x;
+          bq[nb][1] = f.y;
+        } else {
+          bq[nb][0] = qb[kb][nb][0];
+          bq[nb][1] = qb[kb][nb][1];
+        }
+      }
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        af[mt][0] = slot_f16x2(af[mt][0], kd[kb][0], km[kb][0]);
-        af[mt][1] = slot_f16x2(af[mt][1], kd[kb][0], km[kb][0]);
-        af[mt][2] = slot_f16x2(af[mt][2], kd[kb][1], km[kb][1]);
-        af[mt][3] = slot_f16x2(af[mt][3], kd[kb][1], km[kb][1]);
+        af[mt][0] = slot_f16x2(af[mt][0], d0, m0);
+        af[mt][1] = slot_f16x2(af[mt][1], d0, m0);
+        af[mt][2] = slot_f16x2(af[mt][2], d1, m1);
+        af[mt][3] = slot_f16x2(af[mt][3], d1, m1);
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) mma_f16(acc[mt][kb & 1][nb], af[mt], qb[kb][nb][0], qb[kb][nb][1]);
+        for (int nb = 0; nb < NB; ++nb) mma_f16(acc[mt][kb & 1][nb], af[mt], bq[nb][0], bq[nb][1]);
       }
     }
     // z/s words of this lane's four tokens (rows gid + 8 m): key records, and the value records' halves
@@ -662,16 +722,26 @@ __global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(Params
     // step per stage, which the near-cancellation of Z, S and M in the output magnifies ----
 #pragma unroll
     for (int mb = 0; mb < NBLK; ++mb) {
+      if (mb >= nmb) break;  // blocks past the set's last nonzero-width value channel
       // m-tile mt: records 8 mt + tig (tokens 2 tig, +1) and 8 mt + 4 + tig; channels gid (slot 0), gid + 8 (slot 1)
+      uint32_t d0, m0, d1, m1, a0, a1;
+      if constexpr (DS) {
+        const uint4 e = reinterpret_cast<const uint4*>(vtab)[mb * 8 + gid];
+        d0 = e.x, m0 = e.y, d1 = e.z, m1 = e.w;
+        a0 = sb + vrow + (d0 >> 5), a1 = sb + vrow + (d1 >> 5);
+      } else {
+        d0 = vd[mb][0], m0 = vm[mb][0], d1 = vd[mb][1], m1 = vm[mb][1];
+        a0 = sb + (d0 >> 5), a1 = sb + (d1 >> 5);
+      }
       uint32_t af[2][4];
-      lds_x4<VSTR>(sb + (vd[mb][0] >> 5), vstr, af[0][0], af[0][2], af[1][0], af[1][2]);
-      lds_x4<VSTR>(sb + (vd[mb][1] >> 5), vstr, af[0][1], af[0][3], af[1][1], af[1][3]);
+      lds_x4<VSTR>(a0, vstr, af[0][0], af[0][2], af[1][0], af[1][2]);
+      lds_x4<VSTR>(a1, vstr, af[0][1], af[0][3], af[1][1], af[1][3]);
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        af[mt][0] = slot_f16x2(af[mt][0], vd[mb][0], vm[mb][0]);
-        af[mt][1] = slot_f16x2(af[mt][1], vd[mb][1], vm[mb][1]);
-        af[mt][2] = slot_f16x2(af[mt][2], vd[mb][0], vm[mb][0]);
-        af[mt][3] = slot_f16x2(af[mt][3], vd[mb][1], vm[mb][1]);
+        af[mt][0] = slot_f16x2(af[mt][0], d0, m0);
+        af[mt][1] = slot_f16x2(af[mt][1], d1, m1);
+        af[mt][2] = slot_f16x2(af[mt][2], d0, m0);
+        af[mt][3] = slot_f16x2(af[mt][3], d1, m1);
       }
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
@@ -778,6 +848,7 @@ __global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(Params
         hs[h * 4 + 2] = st;
       }
     }
+    for (int idx = tid; idx < MAX_G * D; idx += NT) mg[idx] = 0.f;
     __syncthreads();
     switch (CS) {  // merged M_j
       case 16: cluster_merge_m<16, NT>(mrg_a, esw, mg, g, nzV); break;
@@ -824,6 +895,7 @@ __global__ void __launch_bounds__(dec_threads(NB, NBLK), 1) decode_kernel(Params
 #pragma unroll
     for (int r = 0; r < IT; ++r) accI[r] = 0.f;
     float M_run = -INFINITY, den = 0.f, zt = 0.f, st = 0.f;
+    for (int idx = tid; idx < MAX_G * D; idx += NT) mg[idx] = 0.f;
     for (int s0 = 0; s0 < S; s0 += per) {
       const int n = min(per, S - s0);
       __syncthreads();  // the previous chunk is consumed
@@ -966,7 +1038,7 @@ static cudaError_t allow_large_clusters(const void* fn) {
 // the workspace's split plan applies and the splits merge through global memory. plan != nullptr: fill the plan
 // (cluster size or 0, splits, stages, warps, channel blocks, shared memory, clusters held for sizes 16 .. 1 or -1
 // when not asked) and launch nothing.
-template <int NB, int RK, int RV, int NBLK>
+template <int NB, int RK, int RV, int NBLK, int NW>
 static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, DecArgs a, int ws_splits,
                                         int32_t* plan) {
   const int rk = P.t[0].r_words, rv = P.t[1].r_words;
@@ -980,14 +1052,14 @@ static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev
   if (plan)
     for (int i = 0; i < 11; ++i) plan[i] = i >= 6 ? -1 : 0;
   if (16 * bh >= sms / 2) {
-    const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, true>;
+    const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, true, NW>;
     if ((e = allow_large_clusters(fn)) != cudaSuccess) return e;
     const int cap = std::max(1, sms / bh);
     for (int cs = 16, slot = 6; cs >= 1; cs >>= 1, ++slot) {
       if (cs > cap) continue;
       cudaLaunchConfig_t c = cfg;
-      const int stages = ring_stages_for(rk, rv, NB, NBLK, cs);
-      c.dynamicSmemBytes = decode_smem(rk, rv, stages, NB, NBLK, cs).total;
+      const int stages = ring_stages_for(rk, rv, NW, cs);
+      c.dynamicSmemBytes = decode_smem(rk, rv, stages, NW, cs).total;
       if ((e = ensure_dyn_smem(fn, c.dynamicSmemBytes)) != cudaSuccess) return e;
       const int held = cs == 1 ? bh : max_active_clusters(fn, c, cs);
       if (plan) plan[slot] = held;
@@ -996,7 +1068,7 @@ static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev
       a.splits = cs;
       a.stages = stages;
       if (plan) {
-        plan[0] = cs, plan[1] = cs, plan[2] = stages, plan[3] = dec_warps(NB, NBLK), plan[4] = NBLK;
+        plan[0] = cs, plan[1] = cs, plan[2] = stages, plan[3] = NW, plan[4] = NBLK;
         plan[5] = (int32_t)c.dynamicSmemBytes;
         return cudaSuccess;
       }
@@ -1007,31 +1079,31 @@ static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev
       at[1].val.clusterDim.z = 1;
       c.attrs = at;
       c.numAttrs = 2;
-      return cudaLaunchKernelEx(&c, decode_kernel<NB, RK, RV, NBLK, true>, P, a);
+      return cudaLaunchKernelEx(&c, decode_kernel<NB, RK, RV, NBLK, true, NW>, P, a);
     }
   }
-  const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, false>;
+  const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, false, NW>;
   a.splits = ws_splits;
-  a.stages = ring_stages_for(rk, rv, NB, NBLK, 0);
+  a.stages = ring_stages_for(rk, rv, NW, 0);
   cfg.gridDim.x = (unsigned)ws_splits;
-  cfg.dynamicSmemBytes = decode_smem(rk, rv, a.stages, NB, NBLK, 0).total;
+  cfg.dynamicSmemBytes = decode_smem(rk, rv, a.stages, NW, 0).total;
   if (plan) {
-    plan[0] = 0, plan[1] = ws_splits, plan[2] = a.stages, plan[3] = dec_warps(NB, NBLK), plan[4] = NBLK;
+    plan[0] = 0, plan[1] = ws_splits, plan[2] = a.stages, plan[3] = NW, plan[4] = NBLK;
     plan[5] = (int32_t)cfg.dynamicSmemBytes;
     return cudaSuccess;
   }
   if ((e = ensure_dyn_smem(fn, cfg.dynamicSmemBytes)) != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RK, RV, NBLK, false>, P, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RK, RV, NBLK, false, NW>, P, a);
 }
 
 // record lengths with a compile-time decode kernel: equal key and value budgets of 1.25 - 4 bits/element and the
 // joint key/value splits of the Llama-shaped layer at 2.75, 2 and 1.33 bits/element
-template <int NB, int NBLK>
+template <int NB, int NBLK, int NW>
 static cudaError_t launch_decode_rw(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a, int ws_splits,
                                     int32_t* plan) {
   const int rk = P.t[0].r_words, rv = P.t[1].r_words;
 #define KVTC_DECODE_RW(K, V) \
-  if (rk == K && rv == V) return launch_decode_kernel<NB, K, V, NBLK>(cfg, P, a, ws_splits, plan);
+  if (rk == K && rv == V) return launch_decode_kernel<NB, K, V, NBLK, NW>(cfg, P, a, ws_splits, plan);
   KVTC_DECODE_RW(5, 5)
   KVTC_DECODE_RW(6, 4)
   KVTC_DECODE_RW(8, 8)
@@ -1041,7 +1113,7 @@ static cudaError_t launch_decode_rw(cudaLaunchConfig_t& cfg, const ParamsDev& P,
   KVTC_DECODE_RW(14, 8)
   KVTC_DECODE_RW(10, 6)
 #undef KVTC_DECODE_RW
-  return launch_decode_kernel<NB, 0, 0, NBLK>(cfg, P, a, ws_splits, plan);
+  return launch_decode_kernel<NB, 0, 0, NBLK, NW>(cfg, P, a, ws_splits, plan);
 }
 
 kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
@@ -1068,19 +1140,24 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   a.scale_log2 = scale * 1.4426950408889634f;
   const int nb = a.g <= 4 ? 1 : 2;
   const int rk = P.t[0].r_words, rv = P.t[1].r_words;
-  // four channel blocks when every set's nonzero channels fit them and two stages of sixteen warps fit the ring
-  const int nblk =
-      (std::max(P.t[0].max_nz, P.t[1].max_nz) <= 64 && 2 * dec_stage_tokens(nb, 4) * (rk + rv) * 4 <= RING_BUDGET) ? 4
-                                                                                                                   : 8;
+  // four channel blocks when every set's nonzero channels fit them, eight otherwise; sixteen warps for one column
+  // block when two 512-token stages of these records fit the ring
+  const int nblk = std::max(P.t[0].max_nz, P.t[1].max_nz) <= 64 ? 4 : 8;
+  const bool w16 = nb == 1 && 2 * dec_stage_tokens(16) * (rk + rv) * 4 <= RING_BUDGET;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.splits, c.Hkv, B);
-  cfg.blockDim = dim3(dec_threads(nb, nblk));
+  cfg.blockDim = dim3(w16 ? 512 : 256);
   cfg.stream = s;
   cudaError_t e;
-  if (nb == 1)
-    e = nblk == 4 ? launch_decode_rw<1, 4>(cfg, P, a, L.splits, plan) : launch_decode_rw<1, 8>(cfg, P, a, L.splits, plan);
+  if (w16)
+    e = nblk == 4 ? launch_decode_rw<1, 4, 16>(cfg, P, a, L.splits, plan)
+                  : launch_decode_rw<1, 8, 16>(cfg, P, a, L.splits, plan);
+  else if (nb == 1)  // long records: the generic kernel with eight warps
+    e = nblk == 4 ? launch_decode_kernel<1, 0, 0, 4, 8>(cfg, P, a, L.splits, plan)
+                  : launch_decode_kernel<1, 0, 0, 8, 8>(cfg, P, a, L.splits, plan);
   else
-    e = nblk == 4 ? launch_decode_rw<2, 4>(cfg, P, a, L.splits, plan) : launch_decode_rw<2, 8>(cfg, P, a, L.splits, plan);
+    e = nblk == 4 ? launch_decode_rw<2, 4, 8>(cfg, P, a, L.splits, plan)
+                  : launch_decode_rw<2, 8, 8>(cfg, P, a, L.splits, plan);
   if (plan) {
     if (e != cudaSuccess) {
       set_error("decode plan: %s", cudaGetErrorString(e));
