@@ -230,7 +230,9 @@ kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache* cache, co
 
 /* Uncompressed bf16 split-K flash-decode over k, v: device bf16 [B][Hkv][T_cap][d]; same q, seq_lens,
  * out conventions. The measurement comparator for the packed path (no page counterpart beyond the
- * full-cache FlashAttention-2 decoding that RDKV compares against). */
+ * full-cache FlashAttention-2 decoding that RDKV compares against). workspace: device, at least
+ * kv_decode_bf16_workspace_bytes(...) bytes, 16-byte aligned, zero-filled before its first use (its arrival
+ * counters are left at zero by every call); calls sharing a workspace must not overlap on the device. */
 size_t kv_decode_bf16_workspace_bytes(int B, int Hkv, int Hq, int64_t T_cap);
 kv_status kv_attend_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap,
                                 const void* q, const int32_t* seq_lens_dev, float softmax_scale,

@@ -472,7 +472,7 @@ def test_decode_bf16_comparator_matches_exact_attention():
     kd, vd, qd = G.to_dev_storage(kp), G.to_dev_storage(vp), G.to_dev_storage(q)
     sl = torch.tensor(seq, dtype=torch.int32, device="cuda")
     out = torch.empty((B, w.Hq, d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(kvtc.kv_decode_bf16_workspace_bytes(B, Hkv, w.Hq, T_cap), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(kvtc.kv_decode_bf16_workspace_bytes(B, Hkv, w.Hq, T_cap), dtype=torch.uint8, device="cuda")
     scale = 1 / math.sqrt(d)
     kvtc.kv_attend_decode_bf16(kd, vd, B, Hkv, w.Hq, T_cap, qd, sl, scale, out, ws)
     assert kvtc.kv_check_status() == kvtc.KV_OK

@@ -7,67 +7,80 @@ namespace kvtc {
 // ======================================================================================================
 // uncompressed bf16 split-K flash-decode (comparator)
 // ======================================================================================================
-constexpr int BDT = 64;
-constexpr int BTHREADS = 128;
+// A CTA of eight warps owns one split of one (sequence, KV head). Tiles of 128 tokens of K and V stream through a
+// ring of shared-memory stages by 16-byte asynchronous copies (each 256-byte token row stored with its 16-byte
+// chunks XOR-swizzled by the row, so that ldmatrix reads are free of bank conflicts); one barrier per tile. Warp w
+// takes tokens [16 w, 16 w + 16) of each tile: logits on the MMA (A = the g query rows, B = K), online softmax in
+// the accumulator layout, P (bf16 hi + lo) straight into the B operand of the P.V MMA (A = V^T). The splits merge
+// through the workspace; the last to arrive writes the output.
+constexpr int BT = 128;                  // tokens per tile
+constexpr int BWARPS = 8;
+constexpr int BTHREADS = 32 * BWARPS;
 constexpr int BSTAGES = 3;
-constexpr int BPITCH = 272;  // bytes per token row in shared memory (256 + 16: conflict-free ldmatrix)
+constexpr int BROW = D * 2;              // bytes per token row
+constexpr int BSTAGE_BYTES = 2 * BT * BROW;
 
 struct DecBf16Args {
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   const __nv_bfloat16* q;
   const int32_t* seq_lens;
-  unsigned* cnt;
-  float* part;
+  unsigned* cnt;    // [B*Hkv] arrival counters: zero before a call, left at zero after it
+  float* part;      // [B*Hkv][splits][8][PSTR]
   float* out;
   long long T_cap;
-  long long wait_ns;
-  int B, Hkv, Hq, g, splits, chunk;
+  int B, Hkv, Hq, g, splits;
   float scale_log2;
 };
 
-static size_t decode_bf16_smem_bytes() { return (size_t)BSTAGES * 2 * BDT * BPITCH + BSTAGES * 8 + 128; }
+static size_t decode_bf16_smem_bytes() { return (size_t)BSTAGES * BSTAGE_BYTES; }
 
-__global__ void __launch_bounds__(BTHREADS, 2) decode_bf16_kernel(DecBf16Args a) {
+// byte offset of 16-byte chunk c (0..15) of token row r in a tile
+__device__ __forceinline__ uint32_t bswz(int r, int c) { return (uint32_t)(r * BROW + ((c ^ (r & 7)) << 4)); }
+
+__global__ void __launch_bounds__(BTHREADS, 1) decode_bf16_kernel(DecBf16Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int bh = b * a.Hkv + kh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   const int g = a.g;
-  const size_t stage_bytes = (size_t)2 * BDT * BPITCH;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BSTAGES * stage_bytes);
   __shared__ int s_last;
 
-  const long long L = min((long long)a.seq_lens[b], a.T_cap);
-  const long long t0 = (long long)split * a.chunk;
-  const long long t1 = min(t0 + (long long)a.chunk, L);
-  const int ntiles = t1 > t0 ? (int)((t1 - t0 + BDT - 1) / BDT) : 0;
+  pdl_wait();
+  const long long L = max(0LL, min((long long)a.seq_lens[b], a.T_cap));
+  const long long chunk = ((L + a.splits - 1) / a.splits + 15) / 16 * 16;  // this sequence's tokens over the splits
+  const long long t0 = min((long long)split * chunk, L);
+  const long long t1 = min(t0 + chunk, L);
+  const int ntiles = (int)((t1 - t0 + BT - 1) / BT);
   const __nv_bfloat16* kg = a.k + (size_t)bh * a.T_cap * D;
   const __nv_bfloat16* vg = a.v + (size_t)bh * a.T_cap * D;
+  const uint32_t ring = smem_u32(smem);
 
-  auto issue = [&](int i) {  // warp 0, all lanes
-    const int s = i % BSTAGES;
-    const long long tb = t0 + (long long)i * BDT;
-    const int n = (int)min((long long)BDT, t1 - tb);
-    const uint32_t bar = smem_u32(&bars[s]);
-    if (lane == 0) mbar_expect_tx(bar, (uint32_t)n * 2 * D * 2);
-    __syncwarp();
-    const uint32_t dk = smem_u32(smem + s * stage_bytes), dv = dk + BDT * BPITCH;
-    for (int r = lane; r < n; r += 32) {
-      bulk_g2s(dk + r * BPITCH, kg + (tb + r) * D, D * 2, bar);
-      bulk_g2s(dv + r * BPITCH, vg + (tb + r) * D, D * 2, bar);
+  // tile i into ring slot i % BSTAGES: thread t copies chunks t, t + 256, ... of K and of V (rows past the split's
+  // end are zero-filled, never read from memory)
+  auto issue = [&](int i) {
+    const uint32_t base = ring + (uint32_t)(i % BSTAGES) * BSTAGE_BYTES;
+    const long long tb = t0 + (long long)i * BT;
+#pragma unroll
+    for (int u = 0; u < BT * 16 / BTHREADS; ++u) {
+      const int idx = tid + u * BTHREADS, r = idx >> 4, c = idx & 15;
+      const bool in = tb + r < t1;
+      const size_t src = (size_t)(in ? tb + r : t0) * D + c * 8;
+      const uint32_t sz = in ? 16u : 0u;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(base + bswz(r, c)), "l"(kg + src), "r"(sz)
+                   : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(base + BT * BROW + bswz(r, c)), "l"(vg + src),
+                   "r"(sz)
+                   : "memory");
     }
   };
-
-  if (tid == 0) {
-    for (int s = 0; s < BSTAGES; ++s) mbar_init(smem_u32(&bars[s]), 1);
-    fence_mbar_init();
+#pragma unroll
+  for (int i = 0; i < BSTAGES - 1; ++i) {
+    if (i < ntiles) issue(i);
+    cp_async_commit();
   }
-  __syncthreads();
-  if (warp == 0)
-    for (int i = 0; i < min(BSTAGES, ntiles); ++i) issue(i);
 
-  // q rows (bf16, exact): row h = head h (h < g), others zero; 8 k-blocks of 16 channels
+  // q rows (bf16, exact): A row h = head h (h < g), others zero; 8 k-blocks of 16 channels
   uint32_t qa[8][4];
   {
     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.Hq + (size_t)kh * g) * D);
@@ -87,106 +100,75 @@ __global__ void __launch_bounds__(BTHREADS, 2) decode_bf16_kernel(DecBf16Args a)
     for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc_o[mb][nb][e] = 0.f;
-  const int lrow = (lane & 7) + ((lane >> 4) << 3);
-  const int lcol = ((lane >> 3) & 1) * 16;
-  int consumed = 0;
-  bool aborted = false;
+  // ldmatrix rows: lanes 0-7 tokens 0-7 chunk +0, 8-15 tokens 0-7 chunk +1, 16-23 tokens 8-15 +0, 24-31 +1
+  const int lr = 16 * warp + (lane & 7) + ((lane >> 4) << 3), lc = (lane >> 3) & 1;
+
   for (int i = 0; i < ntiles; ++i) {
-    const int s = i % BSTAGES;
-    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)((i / BSTAGES) & 1), a.wait_ns);
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      consumed = i;
-      break;
+    cp_async_wait_prior();  // tile i has landed (this thread's copies) ...
+    __syncthreads();        // ... for every thread, and every warp is done with tile i - 1
+    if (i + BSTAGES - 1 < ntiles) issue(i + BSTAGES - 1);
+    cp_async_commit();
+    const uint32_t ks = ring + (uint32_t)(i % BSTAGES) * BSTAGE_BYTES, vs = ks + BT * BROW;
+    const long long tw = t0 + (long long)i * BT + 16 * warp;  // this warp's first token
+    if (tw >= t1) continue;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4(ks + bswz(lr, 2 * kb + lc), r0, r1, r2, r3);
+      mma_bf16(acc[0], qa[kb], r0, r1);
+      mma_bf16(acc[1], qa[kb], r2, r3);
     }
-    consumed = i + 1;
-    uint8_t* ks = smem + s * stage_bytes;
-    uint8_t* vs = ks + BDT * BPITCH;
-    const long long tile_t0 = t0 + (long long)i * BDT;
-    const int lt = warp * 16;
-    const bool warp_live = tile_t0 + lt < t1;
-    if (warp_live) {
-      // rows of this warp's 16 tokens that were not loaded hold stale bytes: zero the value rows so that
-      // P = 0 times them stays 0
-      for (int r = 0; r < 16; ++r)
-        if (tile_t0 + lt + r >= t1) reinterpret_cast<uint2*>(vs + (lt + r) * BPITCH)[lane] = make_uint2(0u, 0u);
-      __syncwarp();
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const uint32_t ka = smem_u32(ks + (lt + lrow) * BPITCH + lcol);
+    const int tl[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
+    float lg[4];
 #pragma unroll
-      for (int kb = 0; kb < 8; ++kb) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(ka + kb * 32, r0, r1, r2, r3);
-        mma_bf16(acc[0], qa[kb], r0, r1);
-        mma_bf16(acc[1], qa[kb], r2, r3);
-      }
-      const int tl[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
-      float lg[4];
+    for (int e = 0; e < 4; ++e) lg[e] = tw + tl[e] < t1 ? a.scale_log2 * acc[e >> 1][e & 1] : -INFINITY;
+    float mt = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+    const float m_new = fmaxf(m_run, mt);
+    const float cr = (m_run == m_new) ? 1.f : ex2_approx(m_run - m_new);
+    float p[4], psum = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool valid = tile_t0 + lt + tl[e] < t1;
-        lg[e] = valid ? a.scale_log2 * acc[e >> 1][e & 1] : -INFINITY;
-      }
-      float mt = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-      const float m_new = fmaxf(m_run, mt);
-      const float cr = (m_run == m_new) ? 1.f : exp2f(m_run - m_new);
-      float p[4], psum = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        p[e] = lg[e] == -INFINITY ? 0.f : exp2f(lg[e] - m_new);
-        psum += p[e];
-      }
-      l_run = l_run * cr + psum;
-      m_run = m_new;
-      __nv_bfloat16 ph[4], pl[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        ph[e] = __float2bfloat16_rn(p[e]);
-        pl[e] = __float2bfloat16_rn(p[e] - __bfloat162float(ph[e]));
-      }
-      const uint32_t bh0 = pack_bf162(ph[0], ph[1]), bh1 = pack_bf162(ph[2], ph[3]);
-      const uint32_t bl0 = pack_bf162(pl[0], pl[1]), bl1 = pack_bf162(pl[2], pl[3]);
-      // accumulator columns 2tig, 2tig+1 = heads 2tig, 2tig+1; their maxima live at lanes 8tig, 8tig+4
-      const float c_lo = __shfl_sync(0xffffffffu, cr, 8 * tig);
-      const float c_hi = __shfl_sync(0xffffffffu, cr, 8 * tig + 4);
-      if (__any_sync(0xffffffffu, c_lo != 1.f || c_hi != 1.f)) {
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-            acc_o[mb][nb][0] *= c_lo;
-            acc_o[mb][nb][1] *= c_hi;
-            acc_o[mb][nb][2] *= c_lo;
-            acc_o[mb][nb][3] *= c_hi;
-          }
-      }
-      const uint32_t va = smem_u32(vs + (lt + lrow) * BPITCH + lcol);
-#pragma unroll
-      for (int mb = 0; mb < 8; ++mb) {
-        uint32_t af[4];
-        ldsm_x4_t(va + mb * 32, af[0], af[1], af[2], af[3]);
-        mma_bf16(acc_o[mb][0], af, bh0, bh1);
-        mma_bf16(acc_o[mb][1], af, bl0, bl1);
-      }
+    for (int e = 0; e < 4; ++e) {
+      p[e] = ex2_approx(lg[e] - m_new);
+      psum += p[e];
     }
-    __syncthreads();  // every warp is done with stage s before it is refilled
-    if (warp == 0 && i + BSTAGES < ntiles) {
-      if (lane == 0) fence_proxy_async_smem();
-      __syncwarp();
-      issue(i + BSTAGES);
+    l_run = fmaf(l_run, cr, psum);
+    m_run = m_new;
+    __nv_bfloat16 ph[4], pl[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ph[e] = __float2bfloat16_rn(p[e]);
+      pl[e] = __float2bfloat16_rn(p[e] - __bfloat162float(ph[e]));
+    }
+    const uint32_t bh0 = pack_bf162(ph[0], ph[1]), bh1 = pack_bf162(ph[2], ph[3]);
+    const uint32_t bl0 = pack_bf162(pl[0], pl[1]), bl1 = pack_bf162(pl[2], pl[3]);
+    // accumulator columns 2 tig, 2 tig + 1 = heads 2 tig, 2 tig + 1: their factors live in lanes 8 tig, 8 tig + 4
+    const float c_lo = __shfl_sync(0xffffffffu, cr, 8 * tig);
+    const float c_hi = __shfl_sync(0xffffffffu, cr, 8 * tig + 4);
+    if (__any_sync(0xffffffffu, c_lo != 1.f || c_hi != 1.f)) {
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          acc_o[mb][nb][0] *= c_lo;
+          acc_o[mb][nb][1] *= c_hi;
+          acc_o[mb][nb][2] *= c_lo;
+          acc_o[mb][nb][3] *= c_hi;
+        }
+    }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      uint32_t af[4];
+      ldsm_x4_t(vs + bswz(lr, 2 * mb + lc), af[0], af[1], af[2], af[3]);
+      mma_bf16(acc_o[mb][0], af, bh0, bh1);
+      mma_bf16(acc_o[mb][1], af, bl0, bl1);
     }
   }
-  if (aborted) {
-    if (tid == 0)
-      for (int i = consumed; i < min(consumed + BSTAGES, ntiles); ++i)
-        mbar_wait_bounded(smem_u32(&bars[i % BSTAGES]), (uint32_t)((i / BSTAGES) & 1), a.wait_ns);
-    __syncthreads();
-    return;
-  }
-  __syncthreads();
-  float* ws = reinterpret_cast<float*>(smem);  // [4][8][PSTR]
+  cp_async_wait_all();
+  __syncthreads();  // the ring is free: the warps' partials go there
+  float* ws = reinterpret_cast<float*>(smem);  // [BWARPS][8][PSTR]
   {
     float l = l_run;
     l += __shfl_xor_sync(0xffffffffu, l, 1);
@@ -212,49 +194,86 @@ __global__ void __launch_bounds__(BTHREADS, 2) decode_bf16_kernel(DecBf16Args a)
   float* part = a.part + ((size_t)bh * a.splits + split) * 8 * PSTR;
   for (int idx = tid; idx < g * PSTR; idx += BTHREADS) {
     const int h = idx / PSTR, cidx = idx - h * PSTR;
+    float mw[BWARPS];
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, ws[(w * 8 + h) * PSTR]);
+    for (int w = 0; w < BWARPS; ++w) {
+      mw[w] = ws[(w * 8 + h) * PSTR];
+      M = fmaxf(M, mw[w]);
+    }
     float val = 0.f;
     if (cidx == 0) {
       val = M;
     } else if (cidx == 1 || cidx >= 4) {
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float mw = ws[(w * 8 + h) * PSTR];
-        const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        val += e * ws[(w * 8 + h) * PSTR + cidx];
+      for (int w = 0; w < BWARPS; ++w) {
+        const float e = (mw[w] == -INFINITY) ? 0.f : ex2_approx(mw[w] - M);
+        val = fmaf(e, ws[(w * 8 + h) * PSTR + cidx], val);
       }
     }
     part[idx] = val;
   }
-  __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&a.cnt[bh], 1u) == (unsigned)(a.splits - 1));
+  if (tid == 0) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.cnt + bh) : "memory");
+    const bool last = old == (unsigned)(a.splits - 1);
+    if (last) a.cnt[bh] = 0u;  // every split has arrived: the counter is ready for the next call
+    s_last = last;
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
+  // the last split: weights e_s = 2^(m_s - max m) per head (warp h, lanes over splits), then o = sum e U / sum e l
   const float* pb = a.part + (size_t)bh * a.splits * 8 * PSTR;
-  const int k = tid;
-  for (int h = 0; h < g; ++h) {
+  const int S = a.splits;
+  float* esw = reinterpret_cast<float*>(smem);  // [MAX_SPLITS][8], then the denominators [8]
+  float* den = esw + MAX_SPLITS * 8;
+  if (warp < g) {
+    const int h = warp;
+    float ms[MAX_SPLITS / 32], ls[MAX_SPLITS / 32];
     float M = -INFINITY;
-    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, __ldcg(pb + ((size_t)sp * 8 + h) * PSTR));
-    float Ls = 0.f, As = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float* pp = pb + ((size_t)sp * 8 + h) * PSTR;
-      const float ms = __ldcg(pp);
-      const float e = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      Ls += e * __ldcg(pp + 1);
-      As += e * __ldcg(pp + 4 + k);
+#pragma unroll
+    for (int r = 0; r < MAX_SPLITS / 32; ++r) {
+      const int sp = min(lane + 32 * r, S - 1);
+      ms[r] = __ldcg(pb + ((size_t)sp * 8 + h) * PSTR);
+      ls[r] = __ldcg(pb + ((size_t)sp * 8 + h) * PSTR + 1);
+      if (lane + 32 * r >= S) ms[r] = -INFINITY;
+      M = fmaxf(M, ms[r]);
     }
-    a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] = Ls > 0.f ? As / Ls : 0.f;
+    M = warp_max(M);
+    float dsum = 0.f;
+#pragma unroll
+    for (int r = 0; r < MAX_SPLITS / 32; ++r) {
+      const int sp = lane + 32 * r;
+      const float e = ms[r] == -INFINITY ? 0.f : exp2f(ms[r] - M);
+      if (sp < S) esw[sp * 8 + h] = e;
+      dsum = fmaf(e, ls[r], dsum);
+    }
+    dsum = warp_sum(dsum);
+    if (lane == 0) den[h] = dsum;
   }
-  if (tid == 0) a.cnt[bh] = 0u;
+  __syncthreads();
+  for (int idx = tid; idx < g * D; idx += BTHREADS) {
+    const int h = idx >> 7, k = idx & (D - 1);
+    const float* ph = pb + (size_t)h * PSTR + 4 + k;
+    float o = 0.f;
+    constexpr int SB = 16;
+    for (int s0 = 0; s0 < S; s0 += SB) {
+      float u[SB];
+#pragma unroll
+      for (int r = 0; r < SB; ++r) u[r] = __ldcg(ph + (size_t)min(s0 + r, S - 1) * 8 * PSTR);
+#pragma unroll
+      for (int r = 0; r < SB; ++r)
+        if (s0 + r < S) o = fmaf(esw[(s0 + r) * 8 + h], u[r], o);
+    }
+    const float dh = den[h];
+    a.out[((size_t)b * a.Hq + (size_t)kh * g + h) * D + k] = dh > 0.f ? o / dh : 0.f;
+  }
 }
 
 DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device) {
   DecodeLayout L{};
-  split_plan(B, Hkv, T_cap, device, BDT, 2, 1 << 20, &L.splits, &L.chunk);
+  split_plan(B, Hkv, T_cap, device, BT, 1, MAX_SPLITS, &L.splits, &L.chunk);
   const size_t bh = (size_t)B * Hkv;
   size_t o = 0;
   L.off_cnt = o;
@@ -263,11 +282,6 @@ DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device) {
   o = align256(o + bh * (size_t)L.splits * 8 * PSTR * sizeof(float));
   L.total = o;
   return L;
-}
-
-__global__ void zero_u32_kernel(unsigned* p, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = 0u;
 }
 
 kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap, const void* q,
@@ -283,25 +297,33 @@ kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int H
   a.part = reinterpret_cast<float*>(w + L.off_part);
   a.out = out;
   a.T_cap = T_cap;
-  a.wait_ns = g_wait_limit_ns;
   a.B = B;
   a.Hkv = Hkv;
   a.Hq = Hq;
   a.g = Hq / Hkv;
   a.splits = L.splits;
-  a.chunk = L.chunk;
   a.scale_log2 = scale * 1.4426950408889634f;
-  const int nbh = B * Hkv;
-  zero_u32_kernel<<<(nbh + 255) / 256, 256, 0, s>>>(a.cnt, nbh);
-  kv_status st = launch_check("zero counters");
-  if (st != KV_OK) return st;
   const size_t smem = decode_bf16_smem_bytes();
-  const cudaError_t e = ensure_dyn_smem((const void*)decode_bf16_kernel, smem);
+  cudaError_t e = ensure_dyn_smem((const void*)decode_bf16_kernel, smem);
   if (e != cudaSuccess) {
     set_error("decode_bf16_kernel shared memory: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;
   }
-  decode_bf16_kernel<<<dim3(L.splits, Hkv, B), BTHREADS, smem, s>>>(a);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.splits, Hkv, B);
+  cfg.blockDim = dim3(BTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a);
+  if (e != cudaSuccess) {
+    set_error("decode_bf16_kernel launch: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
   return launch_check("decode_bf16_kernel");
 }
 
