@@ -95,7 +95,8 @@ constexpr uint32_t MERGE_CHUNK = 12288;  // floats of split partials the global 
 struct DecEpi {
   uint32_t wpart, mrg, mg, hs, esw, rot, chunk, tfull, end;
 };
-__host__ __device__ inline DecEpi decode_epi(int nw, int nt) {
+// chunk: room for the global merge's staged partials (the workspace path only)
+__host__ __device__ inline DecEpi decode_epi(int nw, int nt, bool chunk) {
   DecEpi e;
   e.wpart = 0;
   e.tfull = 0;
@@ -105,7 +106,7 @@ __host__ __device__ inline DecEpi decode_epi(int nw, int nt) {
   e.esw = e.hs + MAX_G * 4;
   e.rot = e.esw + MAX_SPLITS * MAX_G;
   e.chunk = e.rot + (uint32_t)MAX_G * nt;
-  e.end = e.chunk + MERGE_CHUNK;
+  e.end = e.chunk + (chunk ? MERGE_CHUNK : 0u);
   const uint32_t tend = (uint32_t)(D + 3) * D;  // T'_V rows and the three column vectors
   if (e.mrg < tend) {                           // keep the merge scratch clear of the staged T'_V
     const uint32_t sh = tend - e.mrg;
@@ -123,7 +124,7 @@ __host__ __device__ inline DecSmem decode_smem(int RK, int RV, int stages, int n
   const int nt = 32 * nw, parts = nt / D;
   s.stage_bytes = (uint32_t)dec_stage_tokens(nw) * (RK + RV) * 4u;
   const uint32_t ring = (uint32_t)stages * s.stage_bytes;
-  const uint32_t epi = decode_epi(nw, nt).end * 4u;
+  const uint32_t epi = decode_epi(nw, nt, cs == 0).end * 4u;
   const uint32_t r = ring > epi ? ring : epi;
   s.qa = align128u(r);
   s.hc = s.qa + 16u * D * 2u;
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
   }
 
   __syncthreads();
-  const DecEpi E = decode_epi(NW, NT);
+  const DecEpi E = decode_epi(NW, NT, !CL);
   float* const fs = reinterpret_cast<float*>(smem);
   float* wpart = fs + E.wpart;  // [NW][g][PSTR]
   float* mrg = fs + E.mrg;      // [g][PSTR]: the CTA's m, l, Z, S, M (rotated basis)
@@ -1060,7 +1061,10 @@ static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev
       cudaLaunchConfig_t c = cfg;
       const int stages = ring_stages_for(rk, rv, NW, cs);
       c.dynamicSmemBytes = decode_smem(rk, rv, stages, NW, cs).total;
-      if ((e = ensure_dyn_smem(fn, c.dynamicSmemBytes)) != cudaSuccess) return e;
+      if (c.dynamicSmemBytes > SMEM_LIMIT || ensure_dyn_smem(fn, c.dynamicSmemBytes) != cudaSuccess) {
+        cudaGetLastError();  // this size does not fit: try the next
+        continue;
+      }
       const int held = cs == 1 ? bh : max_active_clusters(fn, c, cs);
       if (plan) plan[slot] = held;
       if (held < bh) continue;
