@@ -87,7 +87,8 @@ typedef struct {
   int joint;      /* 0: keys and values each get their own budget (R_wK from bits_k, R_wV from bits_v).
                    * 1: the table keeps R_wK + R_wV words per token but splits them between keys and values
                    *    jointly (see kv_calibrate)                                                      */
-  int key_basis;  /* 0: the KLT of Sigma_K. 1: the attention-aware orthogonal key basis (see kv_calibrate) */
+  int key_basis;  /* 0: the KLT of Sigma_K. 1: the attention-aware orthogonal key basis. 2: the non-orthogonal
+                   *    key transform (see kv_calibrate) */
 } kv_calib_opts;
 
 /* Calibrate n_sets sets: fp64 mean/covariance of K and V, query second moment M_Q, Jacobi
@@ -108,6 +109,12 @@ typedef struct {
  * Starting from the KLT, 8 cyclic Jacobi sweeps rotate each pair (i < j) by the angle on a 48-point grid over
  * [-pi/4, pi/4) that minimises the pair's log s_i + log s_j + log w_i + log w_j (rotating only when that gains
  * more than 1e-10); the key importances are then s_i w_i and the stored variances s_i.
+ * key_basis = 2 ([NOVA-KV], third abstract: the optimal key transform is not orthogonal and satisfies a
+ * generalised Parseval relation): T = c V^T M_Q^(1/2) with V the eigenvectors of M_Q^(1/2) Sigma_K M_Q^(1/2)
+ * (M_Q + 1e-12 tr/d I), so that e^T M_Q e = |T e|^2 / c^2 and the coefficients are uncorrelated with
+ * variances c^2 lambda; the key importances are those variances. c is the largest column norm of
+ * M_Q^(-1/2) V, so every column of T^-1 has norm <= 1. The table keeps T^-1 beside T (kv_params_set_inverse);
+ * the encode applies T, the decode rotates q by T^-T.
  * The result lives on the host; call kv_params_upload before encoding or decoding.
  * Errors: KV_ERR_INVALID_ARG (null, n_tok < 2, n_q < 1), KV_ERR_UNSUPPORTED (d), KV_ERR_BUDGET,
  * KV_ERR_NUMERIC (non-finite input). */
@@ -124,6 +131,17 @@ kv_status kv_params_from_arrays(int d, int n_sets,
                                 const int32_t* widths_k, int r_words_k,
                                 const float* T_v, const float* mu_v, const float* sigma_v,
                                 const int32_t* widths_v, int r_words_v, kv_params** out);
+
+/* Give tensor (0 = keys, 1 = values) of the table a non-orthogonal transform's inverse: Tinv [n_sets][d][d]
+ * host fp32, Tinv[k][j] = (T^-1)[k][j], column j pairing with storage channel j (the same order as T's rows).
+ * The decode then uses k^ = T^-1 y^ ([NOVA-KV] non-orthogonal key transform): q is rotated by T^-T, and the
+ * folded vectors (T^-1 mu, the column sums of T^-1 sigma) are formed with T^-1. Tinv = NULL removes it (T is then
+ * taken as orthogonal, its inverse T^T). Takes effect at the next kv_params_upload; saved by kv_params_save.
+ * Errors: KV_ERR_INVALID_ARG (null table, bad tensor, non-finite entries). */
+kv_status kv_params_set_inverse(kv_params* p, int tensor, const float* Tinv);
+/* Copy one set's inverse of tensor's transform to Tinv [d][d] (host, layout as above). KV_ERR_UNSUPPORTED when the
+ * table holds none (an orthogonal transform); KV_ERR_INVALID_ARG for a bad argument. */
+kv_status kv_params_get_inverse(const kv_params* p, int set, int tensor, float* Tinv);
 
 /* Copy the table to the current CUDA device (allocates device memory owned by the table; the stream
  * orders the copies). Must be called again after switching devices. */

@@ -140,8 +140,49 @@ def test_host_both_calibration_options_match_oracle():
 def test_key_basis_flag_is_checked():
     L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
     with pytest.raises(kvtc.KvError) as e:
-        kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75, attention_aware_keys=2)
+        kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75, attention_aware_keys=3)
     assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama_decode_32k", "qwen_batched_8k"])
+def test_host_whitened_key_transform_matches_oracle(name):
+    """key_basis 2, the non-orthogonal key transform: the library's two Jacobi eigendecompositions give the
+    oracle's transform, its inverse (kept beside it in storage order), variances and widths; values untouched."""
+    w = synth.WORKLOADS[name]
+    L = synth.make_layer(w, T=256, B=2 if w.calib == "own_prefix" else 1, steps=1)
+    sets = list(zip(L.calib_k, L.calib_v, L.calib_q))[:3]
+    bits = w.bits[0]
+    P = kvtc.kv_calibrate(sets, bits, bits, whitened_keys=True)
+    for s, (ck, cv, cq) in enumerate(sets):
+        pk, pv = O.calibrate(ck, cv, cq, bits, bits, whitened_keys=True)
+        info = P.info(s, 0)
+        assert np.array_equal(info["widths"], pk.widths)
+        scale = np.abs(pk.T).max()
+        assert np.max(np.abs(info["T"].astype(np.float64) - pk.T)) < 1e-5 * scale
+        ti = P.inverse(s, 0)
+        assert ti is not None
+        assert np.max(np.abs(ti.astype(np.float64) - pk.T_inv)) < 1e-5 * np.abs(pk.T_inv).max()
+        assert np.allclose(info["eigvals"], pk.eigvals, rtol=1e-6, atol=1e-12 * np.abs(pk.eigvals).max())
+        # the inverse undoes the transform; every column of it has norm <= 1 (the decode's q' scale bound)
+        assert np.max(np.abs(ti.astype(np.float64) @ info["T"].astype(np.float64) - np.eye(128))) < 1e-4
+        assert np.linalg.norm(ti.astype(np.float64), axis=0).max() <= 1 + 1e-6
+        assert P.inverse(s, 1) is None
+        assert np.array_equal(P.info(s, 1)["widths"], pv.widths)
+
+
+def test_params_inverse_survives_save_and_load(tmp_path):
+    """A table with a non-orthogonal key transform keeps its inverse through kv_params_save / kv_params_load;
+    kv_params_set_inverse(None) removes it."""
+    w = synth.WORKLOADS["tiny"]
+    L = synth.make_layer(w, T=256, steps=1)
+    P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75, whitened_keys=True)
+    path = tmp_path / "whitened.kvtc"
+    P.save(str(path))
+    Q = kvtc.kv_params_load(str(path))
+    assert np.array_equal(Q.inverse(0, 0), P.inverse(0, 0))
+    assert Q.inverse(0, 1) is None
+    Q.set_inverse(0, None)
+    assert Q.inverse(0, 0) is None
 
 
 def test_joint_flag_is_checked():

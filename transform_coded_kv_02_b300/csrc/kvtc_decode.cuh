@@ -12,12 +12,13 @@
 // masking them and OR-ing in the fp16 exponent of 1.0 gives the fp16 pair (1 + c_lo 2^-w, 1 + c_hi 2^-w), exact
 // for w <= 10: two instructions per MMA operand register after the shared-memory load.
 //
-// Logits (base 2), per head h, token t, with Q_j = a log2(e) (T_K q_h)_j sigma_j and w_j the slot width of channel
+// Logits (base 2), per head h, token t, with Q_j = a log2(e) (T_K^-T q_h)_j sigma_j (T_K^-T = T_K for an orthogonal
+// key transform; [NOVA-KV]'s key transform is not orthogonal) and w_j the slot width of channel
 // j (b_j its code width; w_j = b_j except for a narrower channel sharing a key slot):
 //   l_t = C0 + z_t C1 + s_t (sum_j Q_j 2^(w_j - b_j) A_tj - C2),  A_tj = 1 + c_tj 2^-w_j,
-//   C0 = a log2(e) q.(T_K^T mu),  C1 = sum_{b_j>0} Q_j = a log2(e) q.w,  C2 = sum_{b_j>0} Q_j (2^(w_j - b_j) -
+//   C0 = a log2(e) q.(T_K^-1 mu),  C1 = sum_{b_j>0} Q_j = a log2(e) q.w,  C2 = sum_{b_j>0} Q_j (2^(w_j - b_j) -
 //   2^(-b_j - 1)) = a log2(e) q.w2  (w, w2: the key table's folded vectors),
-// which is a log2(e) q.k^ for k^ = T_K^T y^, y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j).
+// which is a log2(e) q.k^ for k^ = T_K^-1 y^, y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j).
 // Values, per head, with weights p_t (unnormalised softmax) and W_t = p_t s_t (value slots have w_j = b_j):
 //   sum_t p_t y^_tj = l mu_j + sigma_j (Z - (1 - 2^(-b_j - 1)) S + M_j),  M_j = sum_t W_t A_tj,
 //   Z = sum_t p_t z_t, S = sum_t W_t, l = sum_t p_t,
@@ -320,12 +321,12 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
     }
     cp_async_commit();
   }
-  // q preparation: this thread's slice of T^T (rows KQ part .. KQ part + KQ - 1, column j), channel j's sigma and
-  // widths; warp h < 8: the folded key vectors at its lane's four entries
+  // q preparation: this thread's slice of T^-1 (T^T for an orthogonal T; rows KQ part .. KQ part + KQ - 1,
+  // column j), channel j's sigma and widths; warp h < 8: the folded key vectors at its lane's four entries
   const int qj = tid & (D - 1), qpart = tid / D;
   float tt[KQ];
   {
-    const float* TTc = TK.TT + so * D + (size_t)(KQ * qpart) * D + qj;
+    const float* TTc = TK.Tq + so * D + (size_t)(KQ * qpart) * D + qj;  // q~ = T_K^-T q
 #pragma unroll
     for (int kk = 0; kk < KQ; ++kk) tt[kk] = __ldg(TTc + (size_t)kk * D);
   }

@@ -185,7 +185,7 @@ static int record_words(float bits, int d) { return (int)floor((double)bits * d 
 // calibration of one set
 // ------------------------------------------------------------------------------------------------------
 struct SetResult {
-  std::vector<float> T[2], mu[2], sigma[2];
+  std::vector<float> T[2], mu[2], sigma[2], Tinv[2];
   std::vector<int32_t> widths[2];
   std::vector<double> eig[2], imp[2];
   bool ok = true;
@@ -321,9 +321,11 @@ static void fit_token_layout(int32_t* w, const double* imp, int d, int rw) {
   }
 }
 
+// U: basis as columns (column e = row of T for basis index e). Uinv (null for an orthogonal U): the inverse of
+// U^T, whose column e pairs with basis index e; kept in storage order beside T.
 static void build_tensor(const std::vector<double>& mu_raw, const std::vector<double>& lam,
                          const std::vector<double>& U, const std::vector<double>& imp, int rw, int bmax,
-                         int d, SetResult& r, int t) {
+                         int d, SetResult& r, int t, const std::vector<double>* Uinv = nullptr) {
   std::vector<int32_t> w(d);
   water_fill(imp.data(), d, 32 * rw - 32, bmax, w.data());
   std::vector<int> order(d);
@@ -362,6 +364,12 @@ static void build_tensor(const std::vector<double>& mu_raw, const std::vector<do
     r.widths[t][j] = r.sigma[t][j] > 0.f ? ws[j] : 0;
     r.eig[t][j] = lam[e];
     r.imp[t][j] = imps[j];
+  }
+  r.Tinv[t].clear();
+  if (Uinv) {
+    r.Tinv[t].resize((size_t)d * d);
+    for (int k = 0; k < d; ++k)
+      for (int j = 0; j < d; ++j) r.Tinv[t][(size_t)k * d + j] = (float)(*Uinv)[(size_t)k * d + order[j]];
   }
 }
 
@@ -452,6 +460,7 @@ static void attention_aware_basis(const std::vector<double>& sk, const std::vect
 // Statistics, transforms and importances of one set (everything before the record budget is applied).
 struct SetPrep {
   std::vector<double> mk, lk, uk, ik, mv, lv, uv, iv;
+  std::vector<double> ukinv;  // key_basis 2: the inverse of uk^T (columns pair with uk's)
   double rho = 0.0;  // weight of key against value distortion (joint allocation)
 };
 
@@ -474,6 +483,71 @@ static void prepare_one(const kv_calib_set& s, const kv_calib_opts& o, SetPrep& 
   uv.assign((size_t)d * d, 0.0);
   jacobi_eigh(ck.data(), d, lk.data(), uk.data());
   jacobi_eigh(cv.data(), d, lv.data(), uv.data());
+  if (o.key_basis == 2) {
+    // [NOVA-KV]'s non-orthogonal key transform under the high-resolution model: T = c V^T M_Q^(1/2), V the KLT of
+    // M_Q^(1/2) Sigma_K M_Q^(1/2). Then e^T M_Q e = |T e|^2 / c^2 (the attention-aware key distortion is
+    // mean-squared in the transform domain) and the coefficients are uncorrelated with variances c^2 lambda, so
+    // plain water-filling on those variances allocates the bits. c = the largest column norm of
+    // (V^T M_Q^(1/2))^-1 = M_Q^(-1/2) V, so that every column of T^-1 has norm <= 1. M_Q gets 1e-12 tr/d on the
+    // diagonal.
+    std::vector<double> M(cq), lq(d), Q((size_t)d * d);
+    double tq = 0.0;
+    for (int i = 0; i < d; ++i) tq += M[(size_t)i * d + i];
+    for (int i = 0; i < d; ++i) M[(size_t)i * d + i] += 1e-12 * tq / d;
+    jacobi_eigh(M.data(), d, lq.data(), Q.data());
+    std::vector<double> mh((size_t)d * d, 0.0), mih((size_t)d * d, 0.0);
+    for (int a = 0; a < d; ++a)
+      for (int b = 0; b < d; ++b) {
+        double s1 = 0.0, s2 = 0.0;
+        for (int i = 0; i < d; ++i) {
+          const double l = std::max(lq[i], 1e-300), qa = Q[(size_t)a * d + i] * Q[(size_t)b * d + i];
+          s1 += qa * std::sqrt(l);
+          s2 += qa / std::sqrt(l);
+        }
+        mh[(size_t)a * d + b] = s1;
+        mih[(size_t)a * d + b] = s2;
+      }
+    std::vector<double> tmpm((size_t)d * d, 0.0), A((size_t)d * d, 0.0), V((size_t)d * d);
+    for (int a = 0; a < d; ++a)
+      for (int b = 0; b < d; ++b) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += ck[(size_t)a * d + i] * mh[(size_t)i * d + b];
+        tmpm[(size_t)a * d + b] = acc;
+      }
+    for (int a = 0; a < d; ++a)
+      for (int b = 0; b < d; ++b) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += mh[(size_t)a * d + i] * tmpm[(size_t)i * d + b];
+        A[(size_t)a * d + b] = acc;
+      }
+    std::vector<double> lam(d);
+    jacobi_eigh(A.data(), d, lam.data(), V.data());
+    // U = (V^T M_Q^(1/2))^T = M_Q^(1/2) V (columns), Uinv = M_Q^(-1/2) V (columns), then scaled by c and 1/c
+    std::vector<double> U((size_t)d * d), Ui((size_t)d * d);
+    for (int a = 0; a < d; ++a)
+      for (int e = 0; e < d; ++e) {
+        double s1 = 0.0, s2 = 0.0;
+        for (int i = 0; i < d; ++i) {
+          s1 += mh[(size_t)a * d + i] * V[(size_t)i * d + e];
+          s2 += mih[(size_t)a * d + i] * V[(size_t)i * d + e];
+        }
+        U[(size_t)a * d + e] = s1;
+        Ui[(size_t)a * d + e] = s2;
+      }
+    double c = 0.0;
+    for (int e = 0; e < d; ++e) {
+      double n2 = 0.0;
+      for (int a = 0; a < d; ++a) n2 += Ui[(size_t)a * d + e] * Ui[(size_t)a * d + e];
+      c = std::max(c, std::sqrt(n2));
+    }
+    for (size_t i = 0; i < U.size(); ++i) {
+      U[i] *= c;
+      Ui[i] /= c;
+    }
+    uk.swap(U);
+    P.ukinv.swap(Ui);
+    for (int i = 0; i < d; ++i) lk[i] = std::max(lam[i], 0.0) * c * c;
+  }
   if (o.key_basis == 1) {  // attention-aware key basis; the variances are then the diagonal of U^T Sigma_K U
     attention_aware_basis(ck, cq, d, uk);
     for (int i = 0; i < d; ++i) {
@@ -486,11 +560,17 @@ static void prepare_one(const kv_calib_set& s, const kv_calib_opts& o, SetPrep& 
       lk[i] = acc;
     }
   }
-  // key importances: sigma_i^2 * u_i^T M_Q u_i; value importances: sigma_i^2
+  // key importances: sigma_i^2 * u_i^T M_Q u_i (key_basis 2: the coefficient variances, the distortion being
+  // mean-squared in that domain); value importances: sigma_i^2
   ik.assign(d, 0.0);
   iv.assign(d, 0.0);
   std::vector<double> tmp(d);
   for (int i = 0; i < d; ++i) {
+    iv[i] = std::max(lv[i], 0.0);
+    if (o.key_basis == 2) {
+      ik[i] = std::max(lk[i], 0.0);
+      continue;
+    }
     for (int a = 0; a < d; ++a) {
       double acc = 0.0;
       for (int b = 0; b < d; ++b) acc += cq[(size_t)a * d + b] * uk[(size_t)b * d + i];
@@ -499,7 +579,6 @@ static void prepare_one(const kv_calib_set& s, const kv_calib_opts& o, SetPrep& 
     double w = 0.0;
     for (int a = 0; a < d; ++a) w += uk[(size_t)a * d + i] * tmp[a];
     ik[i] = std::max(lk[i], 0.0) * w;
-    iv[i] = std::max(lv[i], 0.0);
   }
   for (int i = 0; i < d; ++i)
     if (!std::isfinite(ik[i]) || !std::isfinite(iv[i])) {
@@ -527,7 +606,7 @@ static double budget_distortion(const std::vector<double>& imp, int rw, int bmax
 }
 
 static void build_one(const SetPrep& P, int rwk, int rwv, const kv_calib_opts& o, SetResult& r) {
-  build_tensor(P.mk, P.lk, P.uk, P.ik, rwk, o.max_bits, o.d, r, 0);
+  build_tensor(P.mk, P.lk, P.uk, P.ik, rwk, o.max_bits, o.d, r, 0, P.ukinv.empty() ? nullptr : &P.ukinv);
   build_tensor(P.mv, P.lv, P.uv, P.iv, rwv, o.max_bits, o.d, r, 1);
 }
 
@@ -554,7 +633,7 @@ extern "C" kv_status kv_calibrate(int n_sets, const kv_calib_set* sets, const kv
     KV_REQUIRE(sets[i].n_tok >= 2 && sets[i].n_q >= 1, KV_ERR_INVALID_ARG, "set %d: need n_tok >= 2, n_q >= 1", i);
   }
   KV_REQUIRE(opts->joint == 0 || opts->joint == 1, KV_ERR_INVALID_ARG, "joint must be 0 or 1");
-  KV_REQUIRE(opts->key_basis == 0 || opts->key_basis == 1, KV_ERR_INVALID_ARG, "key_basis must be 0 or 1");
+  KV_REQUIRE(opts->key_basis >= 0 && opts->key_basis <= 2, KV_ERR_INVALID_ARG, "key_basis must be 0, 1 or 2");
   std::vector<SetResult> res(n_sets);
   std::vector<SetPrep> prep(n_sets);
   int nth = opts->n_threads > 0 ? opts->n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
@@ -619,9 +698,34 @@ extern "C" kv_status kv_calibrate(int n_sets, const kv_calib_set* sets, const kv
       app(p->widths[t], res[i].widths[t]);
       app(p->eig[t], res[i].eig[t]);
       app(p->imp[t], res[i].imp[t]);
+      app(p->Tinv[t], res[i].Tinv[t]);
     }
   }
   *out = p;
+  return KV_OK;
+}
+
+extern "C" kv_status kv_params_get_inverse(const kv_params* p, int set, int tensor, float* Tinv) {
+  clear_error();
+  KV_REQUIRE(p && Tinv && (tensor == 0 || tensor == 1) && set >= 0 && set < p->n_sets, KV_ERR_INVALID_ARG,
+             "kv_params_get_inverse: bad argument");
+  KV_REQUIRE(!p->Tinv[tensor].empty(), KV_ERR_UNSUPPORTED, "tensor %d has an orthogonal transform (no inverse)",
+             tensor);
+  const size_t n = (size_t)p->d * p->d;
+  memcpy(Tinv, &p->Tinv[tensor][(size_t)set * n], n * 4);
+  return KV_OK;
+}
+
+extern "C" kv_status kv_params_set_inverse(kv_params* p, int tensor, const float* Tinv) {
+  clear_error();
+  KV_REQUIRE(p && (tensor == 0 || tensor == 1), KV_ERR_INVALID_ARG, "kv_params_set_inverse: bad argument");
+  const size_t n = (size_t)p->n_sets * p->d * p->d;
+  if (!Tinv) {
+    p->Tinv[tensor].clear();
+    return KV_OK;
+  }
+  KV_REQUIRE(finite_all(Tinv, n), KV_ERR_INVALID_ARG, "kv_params_set_inverse: non-finite entries");
+  p->Tinv[tensor].assign(Tinv, Tinv + n);
   return KV_OK;
 }
 
@@ -723,11 +827,12 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     blob.resize(off + bytes);
     return Piece{off, bytes};
   };
-  Piece pT[2], pTT[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], pnz[2], psl[2], psc[2], pws[2], pws2[2],
-      psmx[2];
+  Piece pT[2], pTT[2], pTq[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], pnz[2], psl[2], psc[2], pws[2],
+      pws2[2], psmx[2];
   for (int t = 0; t < 2; ++t) {
     pT[t] = reserve((size_t)S * d * d * 4);
     pTT[t] = reserve((size_t)S * d * d * 4);
+    pTq[t] = p->Tinv[t].empty() ? pTT[t] : reserve((size_t)S * d * d * 4);
     pTs[t] = reserve((size_t)S * 3 * d * d * 2);
     pmu[t] = reserve((size_t)S * d * 4);
     psg[t] = reserve((size_t)S * d * 4);
@@ -756,8 +861,17 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     uint8_t* w8 = (uint8_t*)&blob[pw[t].off];
     int32_t* nz = (int32_t*)&blob[pnz[t].off];
     uint32_t* sl = (uint32_t*)&blob[psl[t].off];
+    const bool has_inv = !p->Tinv[t].empty();
+    float* Tq = (float*)&blob[pTq[t].off];
     for (int s = 0; s < S; ++s) {
       const float* Tsrc = &p->T[t][(size_t)s * d * d];
+      // inverse of T: Inv(k, j) = (T^-1)[k][j], T[j][k] for an orthogonal T
+      const float* Isrc = has_inv ? &p->Tinv[t][(size_t)s * d * d] : nullptr;
+      auto Inv = [&](int k, int j) -> double {
+        return has_inv ? (double)Isrc[(size_t)k * d + j] : (double)Tsrc[(size_t)j * d + k];
+      };
+      if (has_inv)
+        for (size_t i = 0; i < (size_t)d * d; ++i) Tq[(size_t)s * d * d + i] = Isrc[i];
       for (int j = 0; j < d; ++j)
         for (int k = 0; k < d; ++k) {
           const float v = Tsrc[(size_t)j * d + k];
@@ -787,7 +901,7 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
       nz[s] = n_nz;
       for (int k = 0; k < d; ++k) {
         double acc = 0.0;
-        for (int j = 0; j < d; ++j) acc += (double)Tsrc[(size_t)j * d + k] * (double)p->mu[t][(size_t)s * d + j];
+        for (int j = 0; j < d; ++j) acc += Inv(k, j) * (double)p->mu[t][(size_t)s * d + j];
         base[(size_t)s * d + k] = (float)acc;
       }
       // The decode's folded constants. Slot width w_j: the wider code width of a key channel pair (both channels
@@ -797,15 +911,23 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
       // scale of the q coefficients; values: the rows and vectors map rotated-basis sums to the original basis.
       std::vector<int> slotw(d);
       for (int j = 0; j < d; ++j) slotw[j] = t == 0 ? std::max(wv[j], wv[j ^ 1]) : wv[j];
+      // (with an inverse, |(T^-T q)_j| <= |q| |column j of T^-1|: the column norm enters the bound)
       double smax = 0.0;
       for (int j = 0; j < d; ++j)
-        if (wv[j] > 0)
-          smax = std::max(smax, (double)p->sigma[t][(size_t)s * d + j] * std::ldexp(1.0, slotw[j] - wv[j]));
+        if (wv[j] > 0) {
+          double cn = 1.0;
+          if (has_inv) {
+            double n2 = 0.0;
+            for (int k = 0; k < d; ++k) n2 += Inv(k, j) * Inv(k, j);
+            cn = std::sqrt(n2);
+          }
+          smax = std::max(smax, cn * (double)p->sigma[t][(size_t)s * d + j] * std::ldexp(1.0, slotw[j] - wv[j]));
+        }
       smx[s] = (float)smax;
       for (int k = 0; k < d; ++k) {
         double wacc = 0.0, wacc2 = 0.0;
         for (int j = 0; j < d; ++j) {
-          const double tj = (double)Tsrc[(size_t)j * d + k];
+          const double tj = Inv(k, j);
           const double sj = (double)p->sigma[t][(size_t)s * d + j];
           const int bj = wv[j];
           tsc[(size_t)s * d * d + (size_t)j * d + k] = bj > 0 ? (float)(tj * sj) : 0.f;
@@ -846,6 +968,7 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     TensorDev& td = p->dev.t[t];
     td.T = (const float*)(b + pT[t].off);
     td.TT = (const float*)(b + pTT[t].off);
+    td.Tq = (const float*)(b + pTq[t].off);
     td.Tsplit = (const __nv_bfloat16*)(b + pTs[t].off);
     td.mu = (const float*)(b + pmu[t].off);
     td.sigma = (const float*)(b + psg[t].off);
@@ -909,7 +1032,7 @@ static uint32_t crc32(const uint8_t* data, size_t n) {
 }
 
 static const uint32_t FILE_MAGIC = 0x4354564Bu;  // "KVTC"
-static const uint32_t FILE_VERSION = 1;
+static const uint32_t FILE_VERSION = 2;  // 2: a per-tensor inverse (non-orthogonal transform) after version 1's data
 
 extern "C" kv_status kv_params_save(const kv_params* p, const char* path) {
   clear_error();
@@ -929,6 +1052,11 @@ extern "C" kv_status kv_params_save(const kv_params* p, const char* path) {
     put(p->eig[t].data(), p->eig[t].size() * 8);
     put(p->imp[t].data(), p->imp[t].size() * 8);
   }
+  for (int t = 0; t < 2; ++t) {
+    const int32_t has = p->Tinv[t].empty() ? 0 : 1;
+    put(&has, 4);
+    if (has) put(p->Tinv[t].data(), p->Tinv[t].size() * 4);
+  }
   FILE* f = fopen(path, "wb");
   KV_REQUIRE(f, KV_ERR_IO, "cannot open %s for writing", path);
   const uint32_t head[4] = {FILE_MAGIC, FILE_VERSION, (uint32_t)pay.size(), crc32(pay.data(), pay.size())};
@@ -944,9 +1072,9 @@ extern "C" kv_status kv_params_load(const char* path, kv_params** out) {
   FILE* f = fopen(path, "rb");
   KV_REQUIRE(f, KV_ERR_IO, "cannot open %s", path);
   uint32_t head[4];
-  if (fread(head, sizeof(head), 1, f) != 1 || head[0] != FILE_MAGIC || head[1] != FILE_VERSION) {
+  if (fread(head, sizeof(head), 1, f) != 1 || head[0] != FILE_MAGIC || head[1] < 1 || head[1] > FILE_VERSION) {
     fclose(f);
-    KV_REQUIRE(false, KV_ERR_IO, "%s: not a version-%u parameter file", path, FILE_VERSION);
+    KV_REQUIRE(false, KV_ERR_IO, "%s: not a parameter file of version 1..%u", path, FILE_VERSION);
   }
   std::vector<uint8_t> pay(head[2]);
   const size_t got = fread(pay.data(), 1, pay.size(), f);
@@ -981,6 +1109,14 @@ extern "C" kv_status kv_params_load(const char* path, kv_params** out) {
     p->imp[t].resize(n);
     ok = get(p->T[t].data(), n * p->d * 4) && get(p->mu[t].data(), n * 4) && get(p->sigma[t].data(), n * 4) &&
          get(p->widths[t].data(), n * 4) && get(p->eig[t].data(), n * 8) && get(p->imp[t].data(), n * 8);
+  }
+  for (int t = 0; t < 2 && ok && head[1] >= 2; ++t) {
+    int32_t has = 0;
+    ok = get(&has, 4) && (has == 0 || has == 1);
+    if (ok && has) {
+      p->Tinv[t].resize(n * p->d);
+      ok = get(p->Tinv[t].data(), n * p->d * 4);
+    }
   }
   if (!ok || pos != pay.size()) {
     delete p;

@@ -24,14 +24,16 @@ constexpr unsigned ST_BAD_INDEX = 2u;
 struct TensorDev {
   const float* T;                  // [S][D][D]  rows = storage channels
   const float* TT;                 // [S][D][D]  TT[k][j] = T[j][k]
+  const float* Tq;                 // [S][D][D]  Tq[k][j] = (T^-1)[k][j]: the decode's q~ = T^-T q (TT when T is
+                                   //            orthogonal)
   const __nv_bfloat16* Tsplit;     // [S][3][D][D]  T = hi + mid + lo, each bf16
   const float* mu;                 // [S][D]  rotated means (storage order)
   const float* sigma;              // [S][D]
   const float* inv_sigma;          // [S][D]  fp32(1/sigma) computed in double; 0 for zero-width
-  const float* base;               // [S][D]  T^T mu (original-basis vector of the all-mean record)
-  const float* Tsc;                // [S][D][D]  T[j][k] sigma_j (0 for zero-width rows)
-  const float* wsum;               // [S][D]  sum over b_j > 0 of T[j][k] sigma_j
-  const float* wsum2;              // [S][D]  sum over b_j > 0 of T[j][k] sigma_j (2^(w_j - b_j) - 2^(-b_j - 1)),
+  const float* base;               // [S][D]  T^-1 mu (original-basis vector of the all-mean record)
+  const float* Tsc;                // [S][D][D]  (T^-1)[k][j] sigma_j at [j][k] (0 for zero-width rows)
+  const float* wsum;               // [S][D]  sum over b_j > 0 of (T^-1)[k][j] sigma_j
+  const float* wsum2;              // [S][D]  sum over b_j > 0 of (T^-1)[k][j] sigma_j (2^(w_j - b_j) - 2^(-b_j - 1)),
                                    //         w_j = slot width (keys: the pair's wider width; values: b_j)
   const float* smax;               // [S]     max over b_j > 0 of sigma_j 2^(w_j - b_j)
   const uint8_t* widths;           // [S][D]
@@ -101,6 +103,8 @@ struct kv_params {
   std::vector<int32_t> widths[2];  // [S][D]
   std::vector<double> eig[2];      // [S][D] variances of the rotated channels (storage order)
   std::vector<double> imp[2];      // [S][D] importances (storage order)
+  std::vector<float> Tinv[2];      // [S][D][D] inverse of a non-orthogonal T (Tinv[k][j]: column j pairs with
+                                   // storage channel j); empty: T is orthogonal and its inverse is T^T
   int device = -1;
   void* dev_blob = nullptr;
   size_t dev_bytes = 0;

@@ -55,6 +55,8 @@ def _sig(name, res, args):
 _P = c_void_p
 _sig("kv_calibrate", c_int, [c_int, ctypes.POINTER(kv_calib_set), ctypes.POINTER(kv_calib_opts), ctypes.POINTER(_P)])
 _sig("kv_params_from_arrays", c_int, [c_int, c_int, _P, _P, _P, _P, c_int, _P, _P, _P, _P, c_int, ctypes.POINTER(_P)])
+_sig("kv_params_set_inverse", c_int, [_P, c_int, _P])
+_sig("kv_params_get_inverse", c_int, [_P, c_int, c_int, _P])
 _sig("kv_params_upload", c_int, [_P, _P])
 _sig("kv_params_num_sets", c_int, [_P])
 _sig("kv_params_record_words", c_int, [_P, c_int])
@@ -157,6 +159,25 @@ class Params:
         _check("kv_params_upload", _lib.kv_params_upload(self.handle, _stream(stream)))
         return self
 
+    def inverse(self, set_idx, tensor, d=128):
+        """The stored inverse of one set's transform [d, d], or None for an orthogonal transform."""
+        out = np.zeros((d, d), np.float32)
+        st = _lib.kv_params_get_inverse(self.handle, set_idx, tensor, _ptr(out))
+        if st == KV_ERR_UNSUPPORTED:
+            return None
+        _check("kv_params_get_inverse", st)
+        return out
+
+    def set_inverse(self, tensor, Tinv):
+        """A non-orthogonal transform's inverse for tensor 0 (keys) or 1 (values): [S, d, d], Tinv[k][j] with
+        column j pairing with storage channel j; None removes it. Takes effect at the next upload."""
+        if Tinv is None:
+            _check("kv_params_set_inverse", _lib.kv_params_set_inverse(self.handle, tensor, None))
+        else:
+            a = np.ascontiguousarray(Tinv, np.float32)
+            _check("kv_params_set_inverse", _lib.kv_params_set_inverse(self.handle, tensor, _ptr(a)))
+        return self
+
     def info(self, set_idx, tensor, d=128):
         w = np.zeros(d, np.int32)
         ev = np.zeros(d, np.float64)
@@ -173,10 +194,12 @@ class Params:
         _check("kv_params_save", _lib.kv_params_save(self.handle, path.encode()))
 
 
-def kv_calibrate(sets, bits_k, bits_v, max_bits=8, n_threads=0, d=128, joint=False, attention_aware_keys=False):
+def kv_calibrate(sets, bits_k, bits_v, max_bits=8, n_threads=0, d=128, joint=False, attention_aware_keys=False,
+                 whitened_keys=False):
     """sets: list of (k [n, d], v [n, d], q [m, d]) host arrays (converted to contiguous fp32); joint: split the
     record words between keys and values jointly instead of by bits_k and bits_v; attention_aware_keys: the
-    attention-aware orthogonal key basis instead of the KLT."""
+    attention-aware orthogonal key basis instead of the KLT; whitened_keys: the non-orthogonal key transform
+    (key_basis 2)."""
     keep = []
     arr = (kv_calib_set * len(sets))()
     for i, (k, v, q) in enumerate(sets):
@@ -185,14 +208,17 @@ def kv_calibrate(sets, bits_k, bits_v, max_bits=8, n_threads=0, d=128, joint=Fal
         q = np.ascontiguousarray(q, np.float32)
         keep += [k, v, q]
         arr[i] = kv_calib_set(_ptr(k), _ptr(v), _ptr(q), k.shape[0], q.shape[0])
-    opts = kv_calib_opts(d, bits_k, bits_v, max_bits, n_threads, int(joint), int(attention_aware_keys))
+    opts = kv_calib_opts(d, bits_k, bits_v, max_bits, n_threads, int(joint),
+                         2 if whitened_keys else int(attention_aware_keys))
     h = c_void_p()
     _check("kv_calibrate", _lib.kv_calibrate(len(sets), arr, ctypes.byref(opts), ctypes.byref(h)))
     return Params(h.value)
 
 
-def kv_params_from_arrays(T_k, mu_k, sigma_k, widths_k, r_words_k, T_v, mu_v, sigma_v, widths_v, r_words_v, d=128):
-    """Arrays with a leading set axis: T [S, d, d], mu/sigma [S, d], widths [S, d]."""
+def kv_params_from_arrays(T_k, mu_k, sigma_k, widths_k, r_words_k, T_v, mu_v, sigma_v, widths_v, r_words_v, d=128,
+                          T_inv_k=None):
+    """Arrays with a leading set axis: T [S, d, d], mu/sigma [S, d], widths [S, d]; T_inv_k [S, d, d]: the key
+    transform's inverse when it is not orthogonal."""
     a = [np.ascontiguousarray(x, t) for x, t in ((T_k, np.float32), (mu_k, np.float32), (sigma_k, np.float32),
                                                  (widths_k, np.int32), (T_v, np.float32), (mu_v, np.float32),
                                                  (sigma_v, np.float32), (widths_v, np.int32))]
@@ -201,7 +227,10 @@ def kv_params_from_arrays(T_k, mu_k, sigma_k, widths_k, r_words_k, T_v, mu_v, si
     _check("kv_params_from_arrays", _lib.kv_params_from_arrays(
         d, S, _ptr(a[0]), _ptr(a[1]), _ptr(a[2]), _ptr(a[3]), r_words_k, _ptr(a[4]), _ptr(a[5]), _ptr(a[6]),
         _ptr(a[7]), r_words_v, ctypes.byref(h)))
-    return Params(h.value)
+    P = Params(h.value)
+    if T_inv_k is not None:
+        P.set_inverse(0, T_inv_k)
+    return P
 
 
 def kv_params_load(path):
