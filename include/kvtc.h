@@ -292,9 +292,11 @@ kv_status kv_debug_set_wait_limit_ns(long long ns);
  * return, leaving KV_ERR_TIMEOUT for kv_check_status. */
 kv_status kv_debug_wait_timeout_selftest(kv_stream_t stream);
 /* The launch kv_attend_decode would make for these parameters and shapes on the current device, without
- * launching: info[11] = cluster size (0: the splits merge through the workspace), splits per (sequence, KV
+ * launching: info[12] = cluster size (0: the splits merge through the workspace), splits per (sequence, KV
  * head), ring stages, warps per CTA, 16-channel blocks, dynamic shared memory bytes, then the clusters the
- * device holds at once for cluster sizes 16, 8, 4, 2, 1 (-1: size not considered). Host memory. */
+ * device holds at once for cluster sizes 16, 8, 4, 2, 1 (-1: size not considered), then 1 when the kernel takes
+ * every channel block's codes in one shared-memory load per lane (each lane's two slots share a code word in all
+ * blocks of all sets), else 0. Host memory. */
 kv_status kv_debug_decode_plan(const kv_params* p, int B, int Hkv, int Hq, int64_t T_cap, int32_t* info);
 
 #ifdef __cplusplus

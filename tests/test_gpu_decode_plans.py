@@ -96,3 +96,47 @@ def test_decode_plan_reports_a_consistent_launch():
             assert held >= B or plan["cluster"] == 1
         else:
             assert plan["splits"] >= 1
+
+
+def _with_widths(p, width, n_channels):
+    """The oracle table p with its first n_channels channels at one width and the rest at zero."""
+    w = np.zeros(p.d, np.int64)
+    w[:n_channels] = width
+    return O.TensorParams(T=p.T, mu=p.mu, sigma=p.sigma, widths=w, r_words=p.r_words, pairing=p.pairing)
+
+
+# (key pair-slot width, value slot width) -> channels of that width that fill the 7 key code words / 14 value half
+# words of 8-word records, and whether every lane's two slots of a block the decode reads can share one word: an
+# even number of slots per word (width 2 or 4) couples within words; an odd number (3 or 5) leaves one slot per word
+# that, without enough zero-width partners in the blocks read, pairs with a slot of another word
+_FILL = {2: (112, 112, True), 3: (70, 70, False), 4: (56, 56, True), 5: (42, 42, False)}
+
+
+@pytest.mark.parametrize("name", ["llama_decode_32k", "qwen_batched_8k"])
+@pytest.mark.parametrize("wk,wv", [(4, 4), (5, 4), (4, 5), (5, 5), (2, 2), (3, 3), (2, 3), (3, 2)])
+def test_decode_single_word_variants(name, wk, wv):
+    """Tables whose key and value blocks do, or do not, hold each lane's two slots in one code word: the decode
+    takes the kernel without the per-block test for the tensors where every set allows it (single_word bit 0:
+    keys, bit 1: values), and matches the oracle decode either way. Widths are set by hand on 8-word records (a
+    compiled record length); four or eight channel blocks as the channels need."""
+    w = synth.WORKLOADS[name]
+    B = 2 if w.calib == "own_prefix" else 1
+    T, T_cap = 700, 704
+    L = synth.make_layer(w, T=T, steps=1, B=B)
+    base = [O.calibrate(ck, cv, cq, 2.0, 2.0) for ck, cv, cq in zip(L.calib_k, L.calib_v, L.calib_q)]
+    assert base[0][0].r_words == 8 and base[0][1].r_words == 8
+    (nk, _, sk), (_, nv, sv) = _FILL[wk], _FILL[wv]
+    sets = [(_with_widths(pk, wk, nk), _with_widths(pv, wv, nv)) for pk, pv in base]
+    P = G.lib_params(sets)
+    per_seq = L.per_seq_params
+    plan = kvtc.kv_debug_decode_plan(P, B, w.Hkv, w.Hq, T_cap)
+    assert plan["single_word"] == (1 if sk else 0) | (2 if sv else 0), plan
+    assert plan["channel_blocks"] == (4 if max(nk, nv) <= 64 else 8)
+    k, v = synth.as_float(L.k), synth.as_float(L.v)
+    rk, rv = G.oracle_cache(k, v, sets, per_seq, T_cap)
+    seq = [T, 433][:B]
+    got = G.run_decode(P, rk, rv, L.q[0], seq, w.Hq, per_seq)
+    ref = G.oracle_decode(rk, rv, L.q[0], seq, sets, w.Hq, per_seq)
+    err = G.rel_l2_rows(got, ref)
+    assert np.all(np.isfinite(got))
+    assert err.max() <= DEC_TOL, (plan, err.max())

@@ -13,9 +13,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libkvtc.so")
-SOURCES = ["kvtc_host.cpp", "kvtc_kernels.cu"]
+SOURCES = ["kvtc_host.cpp", "kvtc_kernels.cu", "kvtc_decode_part.cu"]
 HEADERS = ["kvtc_internal.h", "kvtc_ptx.cuh", "kvtc_codec.cuh", "kvtc_tc.cuh", "kvtc_encode.cuh",
-           "kvtc_encode_tc.cuh", "kvtc_decode.cuh", "kvtc_bf16.cuh", "kvtc_debug.cuh"]
+           "kvtc_encode_tc.cuh", "kvtc_decode.cuh", "kvtc_bf16.cuh", "kvtc_debug.cuh", "kvtc_launch.cuh"]
+DECODE_PARTS = 8  # kvtc_decode_part.cu is compiled once per part (the library's DECODE_PARTS)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -32,16 +33,42 @@ def _stale() -> bool:
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, ptxas_verbose: bool = False) -> str:
+def _units():
+    """(source, object, extra flags) of every translation unit."""
+    obj = os.path.join(LIBDIR, "obj")
+    units = [("kvtc_host.cpp", os.path.join(obj, "kvtc_host.o"), []),
+             ("kvtc_kernels.cu", os.path.join(obj, "kvtc_kernels.o"), [])]
+    units += [("kvtc_decode_part.cu", os.path.join(obj, f"kvtc_decode_part{k}.o"), [f"-DKVTC_DECODE_PART={k}"])
+              for k in range(DECODE_PARTS)]
+    return units
+
+
+def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None) -> str:
+    """Compile every unit (in parallel, up to `jobs` at once) and link lib/libkvtc.so."""
     if not force and not _stale():
         return LIB
-    os.makedirs(LIBDIR, exist_ok=True)
-    cmd = [nvcc(), "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O3",
-           "-shared", "-cudart", "static", "-I", os.path.join(ROOT, "include"),
-           "-o", LIB + ".tmp", *[os.path.join(CSRC, f) for f in SOURCES], "-lpthread"]
+    os.makedirs(os.path.join(LIBDIR, "obj"), exist_ok=True)
+    common = [nvcc(), "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O3",
+              "-I", os.path.join(ROOT, "include")]
     if ptxas_verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+        common.append("-Xptxas=-v")
+    jobs = jobs or max(1, min(len(_units()), os.cpu_count() or 1))
+    pending = list(_units())
+    running = []
+    failed = []
+    while pending or running:
+        while pending and len(running) < jobs:
+            src, obj, extra = pending.pop(0)
+            cmd = [*common, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+            running.append((src, subprocess.Popen(cmd)))
+        src, proc = running.pop(0)
+        if proc.wait() != 0:
+            failed.append(src)
+    if failed:
+        raise subprocess.CalledProcessError(1, f"nvcc ({', '.join(failed)})")
+    link = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", LIB + ".tmp", *[o for _, o, _ in _units()],
+            "-lpthread"]
+    subprocess.run(link, check=True)
     os.replace(LIB + ".tmp", LIB)
     return LIB
 

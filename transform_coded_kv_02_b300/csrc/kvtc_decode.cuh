@@ -1,5 +1,6 @@
 // Decode over packed records: the split-K flash-decode kernel (with the q preparation in its prologue) and its
-// launcher. Part of the single CUDA translation unit of the library (included once by kvtc_kernels.cu).
+// launcher. kvtc_kernels.cu includes this header for the split plan and the dispatch; the kvtc_decode_part.cu
+// units define KVTC_DECODE_KERNELS and compile the kernel's variants.
 //
 // Method: "SPHERICAL KV ..." page, third abstract (NOVA-KV): decode re-reads the whole cache at every step and is
 // bandwidth-bound, so the cost of turning a stored code back into something attention can use has to stay small.
@@ -82,8 +83,9 @@ struct DecSmem {  // byte offsets into the dynamic shared memory of decode_kerne
   uint32_t stage_bytes, qa, hc, tab, pro, tsl, total;
 };
 // slot descriptor tables: keys [8 blocks][4 tig][2 slots] and values [8 blocks][8 gid][2 slots] of (descriptor,
-// mask), then the logit MMA's B fragments per lane [8 blocks][32 lanes] (two words)
-constexpr uint32_t TAB_BYTES = (8u * 4u * 2u + 8u * 8u * 2u) * 8u + 8u * 32u * 8u;
+// mask), then the logit MMA's B fragments per lane [8 blocks][32 lanes] (two words), then the pair (keys, [8][4][2])
+// and channel (values, [8][8][2]) at each position of the decode's lane order
+constexpr uint32_t TAB_BYTES = (8u * 4u * 2u + 8u * 8u * 2u) * 8u + 8u * 32u * 8u + 64u + 128u;
 constexpr uint32_t SMEM_LIMIT = 227u * 1024u;   // dynamic shared memory a CTA may hold
 constexpr uint32_t SMEM_STATIC = 1024u;         // room left for the kernel's static shared variables
 
@@ -257,7 +259,9 @@ __device__ __forceinline__ void slot_decode_desc(uint32_t stage_off, uint32_t r,
 // blocks processed per tensor (blocks past a set's last nonzero-width channel hold zero masks and coefficients).
 // CL: the splits of a (sequence, head) form one thread-block cluster (gridDim.x = cluster size) and merge through
 // distributed shared memory; otherwise they merge through the workspace, the last to arrive doing the merge.
-template <int NB, int RK_, int RV_, int NBLK, bool CL, int NW>
+// SW bit 0 (keys) / bit 1 (values): every channel block the decode reads, in every set, has both slots of each
+// lane in one code word (the table's single_word flags): one shared load per block and no per-block test.
+template <int NB, int RK_, int RV_, int NBLK, bool CL, int NW, int SW>
 __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs a) {
   constexpr int NT = 32 * NW, ST = WTOK * NW;
   constexpr int QPARTS = NT / D, KQ = D / QPARTS;  // q preparation: threads per channel, k's per thread
@@ -298,19 +302,30 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
   constexpr bool DS = dec_desc_smem(NW, NBLK);
   constexpr int NR = DS ? 1 : NBLK;  // blocks whose descriptors and q' operands live in registers
   uint32_t kd[NR][2], km[NR][2], vd[NR][2], vm[NR][2];  // raw slot entries first, descriptors later
-  uint32_t rawk = 0u, rawv = 0u;  // DS: the table entry this thread fills (entry e is slot e)
+  // slot descriptors in the decode's lane order (keys [8][4 tig][2], values [8][8 gid][2]): a lane's two slots of a
+  // channel block sit in one code word wherever the layout allowed it; `single` marks the blocks where every lane's
+  // two slots do (one shared load serves both)
+  const uint32_t* kslp = TK.slp + (size_t)set * 64;
+  const uint32_t* vslp = TV.slp + (size_t)set * 128;
+  const uint32_t smask = __ldg(TK.single + set);
+  uint32_t rawk = 0u, rawv = 0u;  // DS: the table entry this thread fills
   if constexpr (DS) {
-    if (tid < NBLK * 8) rawk = __ldg(TK.slots + so + tid);
-    if (tid < NBLK * 16) rawv = __ldg(TV.slots + so + tid);
+    if (tid < NBLK * 8) rawk = __ldg(kslp + tid);
+    if (tid < NBLK * 16) rawv = __ldg(vslp + tid);
   } else {
 #pragma unroll
     for (int kb = 0; kb < NBLK; ++kb)
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        kd[kb][i] = __ldg(TK.slots + so + 8 * kb + 4 * i + tig);
-        vd[kb][i] = __ldg(TV.slots + so + 16 * kb + 8 * i + gid);
+        kd[kb][i] = __ldg(kslp + (kb * 4 + tig) * 2 + i);
+        vd[kb][i] = __ldg(vslp + (kb * 8 + gid) * 2 + i);
       }
   }
+  // the pair (keys) and channel (values) at each position, for the q' operands and the value sums' write-back
+  uint32_t rawidx = 0u;
+  if (tid < 48)
+    rawidx = __ldg(reinterpret_cast<const uint32_t*>(tid < 16 ? TK.idx + (size_t)set * 64 : TV.idx + (size_t)set * 128) +
+                   (tid < 16 ? tid : tid - 16));
   if constexpr (CL) {  // this CTA's output columns of T'_V and of T_V^T mu, w, w2, copied while the CTA works
     const int KW = D / CS, k0 = split * KW, cpr = KW / 4;  // 16-byte chunks per row
     const uint32_t tdst = smem_u32(smem + L.tsl);
@@ -410,22 +425,24 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
   uint2* const ktab = reinterpret_cast<uint2*>(smem + L.tab);  // [NBLK][4 tig][2 slots]: descriptor, mask
   uint2* const vtab = ktab + 8 * 4 * 2;                         // [NBLK][8 gid][2 slots]
   uint2* const qfrag = vtab + 8 * 8 * 2;                        // [NBLK][32 lanes]: logit B fragments
+  uint32_t* const kidx32 = reinterpret_cast<uint32_t*>(qfrag + 8 * 32);  // [8][4][2] pair indices (bytes)
+  const uint8_t* const kidx = reinterpret_cast<const uint8_t*>(kidx32);
+  const uint8_t* const vidx = kidx + 64;                                  // [8][8][2] channel indices
+  if (tid < 48) kidx32[tid] = rawidx;
   if constexpr (DS) {  // record-relative descriptors; the lanes add their row offsets
-    if (tid < NBLK * 8) {  // key slot 8 kb + 4 i + t
-      const int kb = tid >> 3, i = (tid >> 2) & 1, t = tid & 3;
-      const uint32_t dk = kb < nkb ? rawk : 0u;
+    if (tid < NBLK * 8) {  // key position (block tid / 8, lane (tid / 2) % 4, slot tid % 2)
+      const uint32_t dk = (tid >> 3) < nkb ? rawk : 0u;
       const uint32_t b0 = (dk >> 16) & 255u, b1 = dk >> 24, w = b0 > b1 ? b0 : b1;
       uint2 e;
       slot_decode_desc(4u * (1u + (dk & 255u)), (dk >> 8) & 255u, w, b0, b1, e.x, e.y);
-      ktab[(kb * 4 + t) * 2 + i] = e;
+      ktab[tid] = e;
     }
-    if (tid < NBLK * 16) {  // value channel 16 mb + 8 i + c
-      const int mb = tid >> 4, i = (tid >> 3) & 1, c = tid & 7;
-      const uint32_t dv = mb < nmb ? rawv : 0u;
+    if (tid < NBLK * 16) {  // value position (block tid / 16, lane (tid / 2) % 8, slot tid % 2)
+      const uint32_t dv = (tid >> 4) < nmb ? rawv : 0u;
       const uint32_t bw = (dv >> 16) & 255u;
       uint2 e;
       slot_decode_desc(4u * (2u + (dv & 255u)), (dv >> 8) & 255u, bw, bw, bw, e.x, e.y);
-      vtab[(mb * 8 + c) * 2 + i] = e;
+      vtab[tid] = e;
     }
   } else {
 #pragma unroll
@@ -517,10 +534,10 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
     }
     __syncthreads();
     if constexpr (DS) {  // each lane's B fragments of every channel block, one 8-byte row per lane
-      if (tid < NBLK * 32) {
+      if (tid < NBLK * 32) {  // slot i of lane t: the channel pair kidx[kb][t][i]
         const int kb = tid >> 5, ln = tid & 31, col = ln >> 2, t = ln & 3;
         const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qa);
-        qfrag[tid] = make_uint2(q32[(col * D + kb * 16 + 2 * t) >> 1], q32[(col * D + kb * 16 + 8 + 2 * t) >> 1]);
+        qfrag[tid] = make_uint2(q32[col * (D / 2) + kidx[(kb * 4 + t) * 2]], q32[col * (D / 2) + kidx[(kb * 4 + t) * 2 + 1]]);
       }
       __syncthreads();
     }
@@ -537,8 +554,8 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
         const int col = nb * 8 + gid;
-        qb[kb][nb][0] = qa32[(col * D + kb * 16 + 2 * tig) >> 1];
-        qb[kb][nb][1] = qa32[(col * D + kb * 16 + 8 + 2 * tig) >> 1];
+        qb[kb][nb][0] = qa32[col * (D / 2) + kidx[(kb * 4 + tig) * 2]];
+        qb[kb][nb][1] = qa32[col * (D / 2) + kidx[(kb * 4 + tig) * 2 + 1]];
       }
   }
   // this lane's softmax head in column block nb: tig + 4 nb, over the tokens 32 w + gid + 8 m (m = 0..3)
@@ -607,7 +624,11 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
       }
       uint32_t af[2][4];  // rows gid, gid + 8 (m-tile 0), gid + 16, gid + 24 (m-tile 1)
       lds_x4<KSTR>(a0, kstr, af[0][0], af[0][1], af[1][0], af[1][1]);
-      lds_x4<KSTR>(a1, kstr, af[0][2], af[0][3], af[1][2], af[1][3]);
+      if ((SW & 1) || ((smask >> kb) & 1u)) {  // both slots in the word just loaded
+        af[0][2] = af[0][0], af[0][3] = af[0][1], af[1][2] = af[1][0], af[1][3] = af[1][1];
+      } else {
+        lds_x4<KSTR>(a1, kstr, af[0][2], af[0][3], af[1][2], af[1][3]);
+      }
       uint32_t bq[NB][2];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
@@ -737,7 +758,11 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
       }
       uint32_t af[2][4];
       lds_x4<VSTR>(a0, vstr, af[0][0], af[0][2], af[1][0], af[1][2]);
-      lds_x4<VSTR>(a1, vstr, af[0][1], af[0][3], af[1][1], af[1][3]);
+      if ((SW & 2) || ((smask >> (8 + mb)) & 1u)) {  // both channels in the words just loaded
+        af[0][1] = af[0][0], af[0][3] = af[0][2], af[1][1] = af[1][0], af[1][3] = af[1][2];
+      } else {
+        lds_x4<VSTR>(a1, vstr, af[0][1], af[0][3], af[1][1], af[1][3]);
+      }
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         af[mt][0] = slot_f16x2(af[mt][0], d0, m0);
@@ -797,9 +822,9 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
         }
 #pragma unroll
         for (int mb = 0; mb < NBLK; ++mb)
-          if (mb < nmb) {
-            w[4 + mb * 16 + gid] = vacc[mb][nb][0] + vacc[mb][nb][1];
-            w[4 + mb * 16 + gid + 8] = vacc[mb][nb][2] + vacc[mb][nb][3];
+          if (mb < nmb) {  // rows gid and gid + 8 of block mb hold the channels vidx[mb][gid][0, 1]
+            w[4 + vidx[(mb * 8 + gid) * 2]] = vacc[mb][nb][0] + vacc[mb][nb][1];
+            w[4 + vidx[(mb * 8 + gid) * 2 + 1]] = vacc[mb][nb][2] + vacc[mb][nb][3];
           }
       }
     }
@@ -963,6 +988,7 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
   }
 }
 
+#ifndef KVTC_DECODE_KERNELS
 // splits per (sequence, KV head): one wave of CTAs (per_sm per SM) over the B * Hkv pairs, at most one per tile of
 // the cache's capacity
 static void split_plan(int B, int Hkv, int64_t T_cap, int device, int tile, int per_sm, int max_splits, int* splits,
@@ -989,7 +1015,9 @@ DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device) {
   L.total = o;
   return L;
 }
+#endif
 
+#ifdef KVTC_DECODE_KERNELS
 // Largest number of clusters of cs CTAs of kernel fn (with this launch's block and shared memory) that the device
 // holds at once; asked once per (kernel, shared memory, cluster size, device). 0 when the device cannot run one.
 static int max_active_clusters(const void* fn, const cudaLaunchConfig_t& base, int cs) {
@@ -1039,9 +1067,9 @@ static cudaError_t allow_large_clusters(const void* fn) {
 // busy (sizes 16, 8, 4, 2, 1 tried in turn, each at most SMs / (B * Hkv)); otherwise (few sequence-head pairs)
 // the workspace's split plan applies and the splits merge through global memory. plan != nullptr: fill the plan
 // (cluster size or 0, splits, stages, warps, channel blocks, shared memory, clusters held for sizes 16 .. 1 or -1
-// when not asked) and launch nothing.
-template <int NB, int RK, int RV, int NBLK, int NW>
-static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, DecArgs a, int ws_splits,
+// when not asked, the single-word kernel flag) and launch nothing.
+template <int NB, int RK, int RV, int NBLK, int NW, int SW>
+cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, DecArgs a, int ws_splits,
                                         int32_t* plan) {
   const int rk = P.t[0].r_words, rv = P.t[1].r_words;
   const int bh = a.B * a.Hkv, sms = sm_count(current_device());
@@ -1052,9 +1080,10 @@ static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev
   cfg.numAttrs = 1;
   cudaError_t e;
   if (plan)
-    for (int i = 0; i < 11; ++i) plan[i] = i >= 6 ? -1 : 0;
+    for (int i = 0; i < 12; ++i) plan[i] = i >= 6 && i < 11 ? -1 : 0;
+  if (plan) plan[11] = SW;
   if (16 * bh >= sms / 2) {
-    const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, true, NW>;
+    const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, true, NW, SW>;
     if ((e = allow_large_clusters(fn)) != cudaSuccess) return e;
     const int cap = std::max(1, sms / bh);
     for (int cs = 16, slot = 6; cs >= 1; cs >>= 1, ++slot) {
@@ -1084,10 +1113,10 @@ static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev
       at[1].val.clusterDim.z = 1;
       c.attrs = at;
       c.numAttrs = 2;
-      return cudaLaunchKernelEx(&c, decode_kernel<NB, RK, RV, NBLK, true, NW>, P, a);
+      return cudaLaunchKernelEx(&c, decode_kernel<NB, RK, RV, NBLK, true, NW, SW>, P, a);
     }
   }
-  const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, false, NW>;
+  const void* fn = (const void*)decode_kernel<NB, RK, RV, NBLK, false, NW, SW>;
   a.splits = ws_splits;
   a.stages = ring_stages_for(rk, rv, NW, 0);
   cfg.gridDim.x = (unsigned)ws_splits;
@@ -1098,27 +1127,45 @@ static cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev
     return cudaSuccess;
   }
   if ((e = ensure_dyn_smem(fn, cfg.dynamicSmemBytes)) != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RK, RV, NBLK, false, NW>, P, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<NB, RK, RV, NBLK, false, NW, SW>, P, a);
 }
+#else
+template <int NB, int RK, int RV, int NBLK, int NW, int SW>
+cudaError_t launch_decode_kernel(cudaLaunchConfig_t& cfg, const ParamsDev& P, DecArgs a, int ws_splits, int32_t* plan);
+#endif
 
-// record lengths with a compile-time decode kernel: equal key and value budgets of 1.25 - 4 bits/element and the
-// joint key/value splits of the Llama-shaped layer at 2.75, 2 and 1.33 bits/element
+// The compiled variants of decode_kernel's launcher, X(NB, RK, RV, NBLK, NW, SW, part): record lengths with a
+// compile-time kernel (equal key and value budgets of 1.25 - 4 bits/element and the joint key/value splits of the
+// Llama-shaped layer at 2.75, 2 and 1.33 bits/element) for each single-word mask, and the generic kernel (RK = RV
+// = 0, lengths read at run time) of each warp layout. part: the translation unit that compiles the variant.
+#define KVTC_DECODE_RW_LIST(X, NB, NBLK, NW, SW, PART)                                                       \
+  X(NB, 5, 5, NBLK, NW, SW, PART) X(NB, 6, 4, NBLK, NW, SW, PART) X(NB, 8, 8, NBLK, NW, SW, PART)             \
+  X(NB, 11, 11, NBLK, NW, SW, PART) X(NB, 12, 12, NBLK, NW, SW, PART) X(NB, 16, 16, NBLK, NW, SW, PART)       \
+  X(NB, 14, 8, NBLK, NW, SW, PART) X(NB, 10, 6, NBLK, NW, SW, PART)
+#define KVTC_DECODE_LAYOUT(X, NB, NBLK, NW, P0, P1)                                                          \
+  KVTC_DECODE_RW_LIST(X, NB, NBLK, NW, 0, P0) KVTC_DECODE_RW_LIST(X, NB, NBLK, NW, 1, P0)                    \
+  KVTC_DECODE_RW_LIST(X, NB, NBLK, NW, 2, P1) KVTC_DECODE_RW_LIST(X, NB, NBLK, NW, 3, P1)                    \
+  X(NB, 0, 0, NBLK, NW, 0, P1)
+#define KVTC_DECODE_VARIANTS(X)                                                                             \
+  KVTC_DECODE_LAYOUT(X, 1, 4, 16, 0, 1) KVTC_DECODE_LAYOUT(X, 1, 8, 16, 2, 3)                                \
+  KVTC_DECODE_LAYOUT(X, 2, 4, 8, 4, 5) KVTC_DECODE_LAYOUT(X, 2, 8, 8, 6, 7)                                  \
+  X(1, 0, 0, 4, 8, 0, 0) X(1, 0, 0, 8, 8, 0, 2)
+
+#ifndef KVTC_DECODE_KERNELS
+// the compile-time kernel of the table's record lengths and single-word mask, else the generic one
 template <int NB, int NBLK, int NW>
 static cudaError_t launch_decode_rw(cudaLaunchConfig_t& cfg, const ParamsDev& P, const DecArgs& a, int ws_splits,
                                     int32_t* plan) {
-  const int rk = P.t[0].r_words, rv = P.t[1].r_words;
-#define KVTC_DECODE_RW(K, V) \
-  if (rk == K && rv == V) return launch_decode_kernel<NB, K, V, NBLK, NW>(cfg, P, a, ws_splits, plan);
-  KVTC_DECODE_RW(5, 5)
-  KVTC_DECODE_RW(6, 4)
-  KVTC_DECODE_RW(8, 8)
-  KVTC_DECODE_RW(11, 11)
-  KVTC_DECODE_RW(12, 12)
-  KVTC_DECODE_RW(16, 16)
-  KVTC_DECODE_RW(14, 8)
-  KVTC_DECODE_RW(10, 6)
-#undef KVTC_DECODE_RW
-  return launch_decode_kernel<NB, 0, 0, NBLK, NW>(cfg, P, a, ws_splits, plan);
+  const int rk = P.t[0].r_words, rv = P.t[1].r_words, sw = P.single_word;
+#define KVTC_DECODE_PICK(NB_, K, V, NBLK_, NW_, SW_, PART)        \
+  if (rk == (K) && rv == (V) && sw == (SW_))                       \
+    return launch_decode_kernel<NB, K, V, NBLK, NW, SW_>(cfg, P, a, ws_splits, plan);
+  KVTC_DECODE_RW_LIST(KVTC_DECODE_PICK, NB, NBLK, NW, 0, 0)
+  KVTC_DECODE_RW_LIST(KVTC_DECODE_PICK, NB, NBLK, NW, 1, 0)
+  KVTC_DECODE_RW_LIST(KVTC_DECODE_PICK, NB, NBLK, NW, 2, 0)
+  KVTC_DECODE_RW_LIST(KVTC_DECODE_PICK, NB, NBLK, NW, 3, 0)
+#undef KVTC_DECODE_PICK
+  return launch_decode_kernel<NB, 0, 0, NBLK, NW, 0>(cfg, P, a, ws_splits, plan);
 }
 
 kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
@@ -1158,8 +1205,8 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
     e = nblk == 4 ? launch_decode_rw<1, 4, 16>(cfg, P, a, L.splits, plan)
                   : launch_decode_rw<1, 8, 16>(cfg, P, a, L.splits, plan);
   else if (nb == 1)  // long records: the generic kernel with eight warps
-    e = nblk == 4 ? launch_decode_kernel<1, 0, 0, 4, 8>(cfg, P, a, L.splits, plan)
-                  : launch_decode_kernel<1, 0, 0, 8, 8>(cfg, P, a, L.splits, plan);
+    e = nblk == 4 ? launch_decode_kernel<1, 0, 0, 4, 8, 0>(cfg, P, a, L.splits, plan)
+                  : launch_decode_kernel<1, 0, 0, 8, 8, 0>(cfg, P, a, L.splits, plan);
   else
     e = nblk == 4 ? launch_decode_rw<2, 4, 8>(cfg, P, a, L.splits, plan)
                   : launch_decode_rw<2, 8, 8>(cfg, P, a, L.splits, plan);
@@ -1176,5 +1223,7 @@ kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, in
   }
   return launch_check("decode_kernel");
 }
+
+#endif  // KVTC_DECODE_KERNELS
 
 }  // namespace kvtc

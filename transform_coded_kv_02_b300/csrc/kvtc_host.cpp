@@ -808,6 +808,78 @@ static uint32_t slot_descriptor(int u, int r, int b0, int b1) {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The decode's order of the MMA channel dimension. The logit MMA's k index and the P.V MMA's row index may take the
+// channels in any order (the q' operands and the value sums follow it), so a lane's two key pair slots of a
+// 16-channel block - and a lane's two value channels - are coupled from one code word wherever the word holds two:
+// the decode then loads that word once for both. items: n_blocks * lanes * 2 (pairs, or channels), word[item] (-1:
+// no slot). A couple's slot 0 is real whenever it has a real slot; a real left alone in its word takes an item
+// without a slot as partner (its couple still needs one load), or, where the blocks the decode reads (capacity
+// couples) could not hold every real item that way, another lone real. Order: couples of one word, lone reals with
+// a slotless partner, couples across words, slotless couples. Blocks whose couples all need one load get their bit
+// in single_mask.
+static void couple_positions(const int* word, int n_blocks, int lanes, int capacity, std::vector<int>& order,
+                             uint32_t& single_mask) {
+  const int n = n_blocks * lanes * 2;
+  std::vector<std::pair<int, int>> same, lone, cross, empty;
+  std::vector<int> dummies, left;
+  int max_word = -1;
+  for (int i = 0; i < n; ++i) max_word = std::max(max_word, word[i]);
+  for (int u = 0; u <= max_word; ++u) {
+    int held = -1;
+    for (int i = 0; i < n; ++i)
+      if (word[i] == u) {
+        if (held < 0) {
+          held = i;
+        } else {
+          same.emplace_back(held, i);
+          held = -1;
+        }
+      }
+    if (held >= 0) left.push_back(held);
+  }
+  for (int i = 0; i < n; ++i)
+    if (word[i] < 0) dummies.push_back(i);
+  const int L = (int)left.size();
+  int x = std::max(0, (int)same.size() + L - capacity);  // couples across words needed to fit the capacity
+  x = std::min(x, L / 2);
+  x = std::max(x, (L - (int)dummies.size() + 1) / 2);   // and where slotless partners run out
+  x = std::min(x, L / 2);
+  int li = 0;
+  for (int c = 0; c < x; ++c, li += 2) cross.emplace_back(left[li], left[li + 1]);
+  size_t di = 0;
+  std::vector<int> rest;
+  for (; li < L; ++li) {
+    if (di < dummies.size())
+      lone.emplace_back(left[li], dummies[di++]);
+    else
+      rest.push_back(left[li]);
+  }
+  for (; di < dummies.size(); ++di) rest.push_back(dummies[di]);  // (reals first: left over only when unpaired)
+  std::vector<int> rr, dd;
+  for (int r : rest) (word[r] >= 0 ? rr : dd).push_back(r);
+  for (size_t i = 0; i + 1 < rr.size(); i += 2) cross.emplace_back(rr[i], rr[i + 1]);
+  if (rr.size() % 2) dd.insert(dd.begin(), rr.back());
+  for (size_t i = 0; i + 1 < dd.size(); i += 2) empty.emplace_back(dd[i], dd[i + 1]);
+  std::vector<std::pair<int, int>> all(same);
+  const size_t n_one = same.size() + lone.size();  // couples needing one load: same, lone, and the slotless ones
+  all.insert(all.end(), lone.begin(), lone.end());
+  all.insert(all.end(), cross.begin(), cross.end());
+  all.insert(all.end(), empty.begin(), empty.end());
+  order.assign(n, 0);
+  single_mask = 0u;
+  for (int b = 0; b < n_blocks; ++b) {
+    bool single = true;
+    for (int l = 0; l < lanes; ++l) {
+      const size_t c = (size_t)b * lanes + l;
+      order[(b * lanes + l) * 2 + 0] = all[c].first;
+      order[(b * lanes + l) * 2 + 1] = all[c].second;
+      const bool one = c < n_one || c >= n_one + cross.size();
+      single = single && one;
+    }
+    if (single) single_mask |= 1u << b;
+  }
+}
+
 extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
   clear_error();
   KV_REQUIRE(p, KV_ERR_INVALID_ARG, "kv_params_upload: null");
@@ -828,7 +900,7 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     return Piece{off, bytes};
   };
   Piece pT[2], pTT[2], pTq[2], pTs[2], pmu[2], psg[2], pinv[2], pbase[2], pw[2], pnz[2], psl[2], psc[2], pws[2],
-      pws2[2], psmx[2];
+      pws2[2], psmx[2], pslp[2], pidx[2], pmask;
   for (int t = 0; t < 2; ++t) {
     pT[t] = reserve((size_t)S * d * d * 4);
     pTT[t] = reserve((size_t)S * d * d * 4);
@@ -845,7 +917,11 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     pw[t] = reserve((size_t)S * d);
     pnz[t] = reserve((size_t)S * 4);
     psl[t] = reserve((size_t)S * d * 4);
+    pslp[t] = reserve((size_t)S * (t == 0 ? 64 : 128) * 4);
+    pidx[t] = reserve((size_t)S * (t == 0 ? 64 : 128));
   }
+  pmask = reserve((size_t)S * 4);
+  int single_word = 3;
   for (int t = 0; t < 2; ++t) {
     float* T = (float*)&blob[pT[t].off];
     float* TT = (float*)&blob[pTT[t].off];
@@ -949,6 +1025,28 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
         kvtc::token_slot_layout(wv.data(), d, p->r_words[t], word, pos);
         for (int j = 0; j < d; ++j) sls[j] = slot_descriptor(word[j], pos[j], wv[j], wv[j]);
       }
+      // the decode's lane order (keys: 8 blocks x 4 lanes x 2 pair slots; values: 8 blocks x 8 lanes x 2
+      // channels), the slot descriptors in that order, and the blocks whose couples share a word
+      {
+        const int lanes = t == 0 ? 4 : 8, n_items = 8 * lanes * 2;
+        std::vector<int> ord;
+        uint32_t single = 0u;
+        // the decode reads the channel blocks below the last nonzero width: their items (zero-width ones too) are
+        // ordered among themselves; the blocks past them keep the storage order
+        const int blocks_read = (n_nz + 15) / 16;
+        if (blocks_read > 0) couple_positions(word, blocks_read, lanes, blocks_read * lanes, ord, single);
+        for (int i = (int)ord.size(); i < n_items; ++i) ord.push_back(i);
+        uint32_t* slp = (uint32_t*)&blob[pslp[t].off] + (size_t)s * n_items;
+        uint8_t* idx = (uint8_t*)&blob[pidx[t].off] + (size_t)s * n_items;
+        for (int i = 0; i < n_items; ++i) {
+          slp[i] = sls[ord[i]];
+          idx[i] = (uint8_t)ord[i];
+        }
+        uint32_t* msk = (uint32_t*)&blob[pmask.off] + s;
+        *msk = t == 0 ? single : (*msk | (single << 8));
+        const uint32_t need = (1u << blocks_read) - 1u;  // the blocks the decode reads
+        if ((single & need) != need) single_word &= ~(1 << t);
+      }
     }
   }
   void* dblob = nullptr;
@@ -981,12 +1079,16 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     td.widths = (const uint8_t*)(b + pw[t].off);
     td.nz = (const int32_t*)(b + pnz[t].off);
     td.slots = (const uint32_t*)(b + psl[t].off);
+    td.slp = (const uint32_t*)(b + pslp[t].off);
+    td.idx = (const uint8_t*)(b + pidx[t].off);
+    td.single = (const uint32_t*)(b + pmask.off);
     td.r_words = p->r_words[t];
     const int32_t* nzh = (const int32_t*)&blob[pnz[t].off];
     td.min_nz = S > 0 ? *std::min_element(nzh, nzh + S) : 0;
     td.max_nz = S > 0 ? *std::max_element(nzh, nzh + S) : 0;
   }
   p->dev.n_sets = S;
+  p->dev.single_word = single_word;
   return KV_OK;
 }
 

@@ -41,6 +41,11 @@ struct TensorDev {
   const uint32_t* slots;           // [S][D] slots: code word | bit << 8 | b_lo << 16 | b_hi << 24; keys: entry k =
                                    // channel pair (2k, 2k+1) of a one-token record (k < D/2); values: entry j =
                                    // channel j of a two-token record (code words start at record word 2)
+  const uint32_t* slp;             // [S][8 blocks][lanes][2] slot descriptors in the decode's lane order (keys:
+                                   //   4 lanes of pair slots, values: 8 lanes of channels)
+  const uint8_t* idx;              // [S][8][lanes][2] the pair (keys) or channel (values) at each position
+  const uint32_t* single;          // [S] blocks whose lane couples share a code word: keys bits 0-7, values 8-15
+                                   //   (the same array in both tensors)
   int r_words;                     // record words per token (same for every set)
   int min_nz;                      // smallest nz over the sets
   int max_nz;                      // largest nz over the sets
@@ -49,6 +54,9 @@ struct TensorDev {
 struct ParamsDev {
   TensorDev t[2];
   int n_sets;
+  // bit 0: in every set, every key channel block the decode reads takes both slots of each lane from one code word
+  // (TensorDev::single); bit 1: the same for the value blocks
+  int single_word;
 };
 
 // First-fit placement of the pair slots of widths w[d] in a record of rw words (word/pos [d/2], -1 = empty);
@@ -88,6 +96,11 @@ kv_status launch_debug_unpack(const ParamsDev& P, int set, int tensor, const uin
 kv_status launch_wait_selftest(cudaStream_t s);
 void set_wait_limit_ns(long long ns);
 kv_status read_and_clear_device_status(unsigned* out);
+
+// The decode kernel's variants are compiled in DECODE_PARTS translation units (kvtc_decode_part.cu, once per part
+// number), each with its own device status word; this reads and clears the one of a part.
+constexpr int DECODE_PARTS = 8;
+kv_status read_and_clear_decode_status(int part, unsigned* out);
 
 }  // namespace kvtc
 

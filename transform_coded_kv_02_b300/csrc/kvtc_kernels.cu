@@ -1,12 +1,13 @@
-// sm_103a kernels of the transform-coded KV cache and their launchers: one CUDA translation unit, made of
+// sm_103a kernels of the transform-coded KV cache and their launchers: this CUDA translation unit, made of
 //  kvtc_encode.cuh     encode_warp_kernel: one warp per (tensor, sequence, head, token); y = T x with CUDA-core
 //                      FMAs, then the warp quantiser/packer (append and fp32 inputs)
 //  kvtc_encode_tc.cuh  encode_tc_kernel: 128-token tiles staged by TMA, y = X T^T on the tensor cores (tcgen05,
 //                      split-bf16 T, fp32 accumulators in tensor memory), thread-per-token quantiser/packer
-//  kvtc_decode.cuh     decode_kernel (split-K flash-decode over the packed records: q~ = T_K q and the folded
-//                      logit constants in the prologue, bulk-copy ring, codes unpacked straight into warp-MMA
-//                      operands, key warps for logits and softmax, value warps for P.V, per-split inverse
-//                      rotation, last-CTA merge of the splits)
+//  kvtc_decode.cuh     the decode's split plan, workspace layout and dispatch; decode_kernel itself (split-K
+//                      flash-decode over the packed records: q' and the folded logit constants in the prologue,
+//                      bulk-copy ring, codes unpacked straight into warp-MMA operands, logits, softmax and P.V in
+//                      every warp, split merge in a cluster or through the workspace) is compiled in the
+//                      kvtc_decode_part.cu units
 //  kvtc_bf16.cuh       decode_bf16_kernel: the same split-K structure over an uncompressed bf16 cache
 //  kvtc_debug.cuh      parity and self-test kernels behind the kv_debug_* entry points
 //
@@ -33,6 +34,7 @@
 
 #include "kvtc_codec.cuh"
 #include "kvtc_internal.h"
+#include "kvtc_launch.cuh"
 #include "kvtc_ptx.cuh"
 
 namespace kvtc {
@@ -50,6 +52,31 @@ static kv_status launch_check(const char* what) {
   return KV_OK;
 }
 
+// the decode parts' status readers (kvtc_decode_part.cu)
+kv_status read_and_clear_decode_status_0(unsigned* out);
+kv_status read_and_clear_decode_status_1(unsigned* out);
+kv_status read_and_clear_decode_status_2(unsigned* out);
+kv_status read_and_clear_decode_status_3(unsigned* out);
+kv_status read_and_clear_decode_status_4(unsigned* out);
+kv_status read_and_clear_decode_status_5(unsigned* out);
+kv_status read_and_clear_decode_status_6(unsigned* out);
+kv_status read_and_clear_decode_status_7(unsigned* out);
+static_assert(DECODE_PARTS == 8, "one status reader per decode part");
+
+kv_status read_and_clear_decode_status(int part, unsigned* out) {
+  using Reader = kv_status (*)(unsigned*);
+  static const Reader readers[DECODE_PARTS] = {
+      read_and_clear_decode_status_0, read_and_clear_decode_status_1, read_and_clear_decode_status_2,
+      read_and_clear_decode_status_3, read_and_clear_decode_status_4, read_and_clear_decode_status_5,
+      read_and_clear_decode_status_6, read_and_clear_decode_status_7};
+  if (part < 0 || part >= DECODE_PARTS) {
+    set_error("decode part %d out of range", part);
+    return KV_ERR_INVALID_ARG;
+  }
+  return readers[part](out);
+}
+
+// the status word of this translation unit, then those of the decode parts
 kv_status read_and_clear_device_status(unsigned* out) {
   unsigned v = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
@@ -58,48 +85,17 @@ kv_status read_and_clear_device_status(unsigned* out) {
     set_error("device status: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;
   }
+  for (int part = 0; part < DECODE_PARTS; ++part) {
+    unsigned pv = 0;
+    const kv_status st = read_and_clear_decode_status(part, &pv);
+    if (st != KV_OK) return st;
+    v |= pv;
+  }
   *out = v;
   return KV_OK;
 }
 
-__device__ __forceinline__ float bf16_bits_f(uint32_t b) { return __uint_as_float(b << 16); }
-
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-// SM count of a device, queried once per device.
-static int sm_count(int device) {
-  static std::atomic<int> cached[64];
-  const bool slot = device >= 0 && device < 64;
-  if (slot) {
-    const int v = cached[device].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-  }
-  int n = 148;
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
-  n = n > 0 ? n : 148;
-  if (slot) cached[device].store(n, std::memory_order_relaxed);
-  return n;
-}
-
-static int current_device() {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  return dev;
-}
-
-// Raise a kernel's dynamic shared-memory ceiling on the current device, once: cudaFuncSetAttribute runs only
-// when a launch asks for more than the value last set for that (kernel, device).
-static cudaError_t ensure_dyn_smem(const void* fn, size_t bytes) {
-  static std::mutex mu;
-  static std::map<std::pair<const void*, int>, size_t> set_to;
-  const int dev = current_device();
-  std::lock_guard<std::mutex> lock(mu);
-  size_t& cur = set_to[{fn, dev}];
-  if (bytes <= cur) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) cur = bytes;
-  return e;
-}
 
 }  // namespace kvtc
 

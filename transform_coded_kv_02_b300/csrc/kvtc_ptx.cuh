@@ -8,9 +8,9 @@
 
 namespace kvtc {
 
-// device status word (ST_* bits), read and cleared by kv_check_status; this header is included by the
-// single CUDA translation unit of the library
-__device__ unsigned int g_status = 0;
+// device status word (ST_* bits): one per CUDA translation unit of the library (internal linkage), each read and
+// cleared by kv_check_status
+static __device__ unsigned int g_status = 0;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -191,6 +191,7 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
 __device__ __forceinline__ uint32_t pack_bf162(__nv_bfloat16 lo, __nv_bfloat16 hi) {
   return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
 }
+__device__ __forceinline__ float bf16_bits_f(uint32_t b) { return __uint_as_float(b << 16); }  // low 16 bits
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
   return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xFFFFu)));
 }

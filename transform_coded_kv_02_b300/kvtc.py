@@ -335,11 +335,11 @@ def kv_debug_set_wait_limit_ns(ns):
 
 def kv_debug_decode_plan(params, B, Hkv, Hq, T_cap):
     """The decode launch plan (see include/kvtc.h) as a dict."""
-    info = (ctypes.c_int32 * 11)()
+    info = (ctypes.c_int32 * 12)()
     _check("kv_debug_decode_plan", _lib.kv_debug_decode_plan(params.handle, B, Hkv, Hq, T_cap, info))
     v = list(info)
     return {"cluster": v[0], "splits": v[1], "stages": v[2], "warps": v[3], "channel_blocks": v[4],
-            "smem_bytes": v[5], "clusters_held": dict(zip((16, 8, 4, 2, 1), v[6:11]))}
+            "smem_bytes": v[5], "clusters_held": dict(zip((16, 8, 4, 2, 1), v[6:11])), "single_word": v[11]}
 
 
 def kv_debug_wait_timeout_selftest(stream=None):
