@@ -143,6 +143,16 @@ kv_status kv_params_set_inverse(kv_params* p, int tensor, const float* Tinv);
  * table holds none (an orthogonal transform); KV_ERR_INVALID_ARG for a bad argument. */
 kv_status kv_params_get_inverse(const kv_params* p, int set, int tensor, float* Tinv);
 
+/* Rotary position embedding of the decode's queries, for kv_attend_decode_paged with q positions: pairs of
+ * channels (i, i + d/2) of q are rotated by the angle pos * base^(-2i/d), i < d/2 (the half-split convention,
+ * without frequency rescaling). base > 0 sets it, base = 0 removes it. Takes effect at the next kv_params_upload,
+ * which stores the 64 frequencies as fractions of a turn in 64-bit fixed point, so that the angle of any position
+ * is reduced exactly before its sine and cosine are taken; saved by kv_params_save. [SPECTRA abstract: longer
+ * contexts and larger batches; the in-kernel embedding spares a separate pass over q.] Errors:
+ * KV_ERR_INVALID_ARG (null table, negative or non-finite base). */
+kv_status kv_params_set_rope(kv_params* p, double base);
+double kv_params_get_rope(const kv_params* p);
+
 /* Copy the table to the current CUDA device (allocates device memory owned by the table; the stream
  * orders the copies). Must be called again after switching devices. */
 kv_status kv_params_upload(kv_params* p, kv_stream_t stream);
@@ -245,6 +255,56 @@ kv_status kv_attend_decode(const kv_params* p, const kv_cache* cache, const void
 kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache* cache, const void* q, int B, int Hq,
                                    const int32_t* seq_lens_dev, float softmax_scale, float* out,
                                    kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------------------
+ * Paged, multi-layer cache (device, caller-owned).  [SPECTRA abstract: longer contexts and larger batches]
+ * Records as in kv_cache, kept in fixed-size pages of page_tokens tokens of one KV head:
+ *   k_pages: [n_pages][Hkv][page_tokens][r_words_k]; v_pages: [n_pages][Hkv][page_tokens / 2][2 r_words_v].
+ * The view holds n_layers layers of B sequences; virtual sequence z = l * B + b (layer l, sequence b) finds the
+ * page of its tokens [i P, (i + 1) P) at block_table[z * max_pages + i] (device int32; only the pages below a
+ * sequence's length are read or written). Layer l of the view uses the parameter sets of layer first_layer + l:
+ * sets (first_layer + l) * S + (per_seq_params ? b * Hkv + h : h), S = per_seq_params ? B * Hkv : Hkv; so a
+ * table calibrated over every layer's heads (layer-major) serves a whole model, and a view of one layer
+ * (n_layers = 1, first_layer = l, the block table's rows of that layer) serves one layer at a time.
+ * ------------------------------------------------------------------------------------------------------ */
+typedef struct {
+  uint32_t* k_pages;           /* 16-byte aligned                                                             */
+  uint32_t* v_pages;           /* 16-byte aligned                                                             */
+  int64_t n_pages;             /* pages in each pool; block-table entries outside 0..n_pages-1 are reported as
+                                  KV_ERR_DEVICE by kv_check_status and their tokens are left out (or unwritten) */
+  int page_tokens;             /* tokens per page: a power of two from 32 to 2^20                             */
+  int Hkv;
+  int B;                       /* sequences per layer                                                         */
+  int n_layers;                /* layers in the view (>= 1)                                                   */
+  int max_pages;               /* block-table row length (pages per sequence); max_pages * page_tokens < 2^31 */
+  const int32_t* block_table;  /* device [n_layers * B][max_pages]                                            */
+  int per_seq_params;
+  int first_layer;             /* parameter layer of the view's layer 0                                       */
+} kv_paged_cache;
+
+size_t kv_paged_cache_bytes(const kv_params* p, int tensor, int64_t n_pages, int page_tokens, int Hkv);
+
+/* Encode into a paged cache: as kv_encode, for every layer of the view in one launch.
+ *   k, v: device [n_layers][B][Hkv][t_new][d] in dtype; dst_pos_dev: device int64 [B] (the same positions in
+ *   every layer); token i of (layer l, sequence b) goes to position dst_pos[b] + i of virtual sequence l B + b,
+ *   which must lie below max_pages * page_tokens (checked on the device: violations and bad page indices are
+ *   skipped and reported as KV_ERR_DEVICE). Same kernels and codes as kv_encode. */
+kv_status kv_encode_paged(const kv_params* p, const kv_paged_cache* cache, const void* k, const void* v,
+                          int dtype, int64_t t_new, const int64_t* dst_pos_dev, kv_stream_t stream);
+
+/* Decode attention over a paged cache for every layer of the view in one launch.
+ *   q: device bf16 [n_layers][B][Hq][d]; out: device fp32 [n_layers][B][Hq][d]; seq_lens_dev: device int32 [B]
+ *   (shared by the layers, 1 <= seq_len <= max_pages * page_tokens, 0 gives zeros).
+ *   q_pos_dev: device int32 [B], the position of each sequence's query for the rotary embedding set by
+ *   kv_params_set_rope (q is embedded in the kernel's prologue, before the rotation into the key basis), or NULL
+ *   when q arrives embedded. Otherwise the same results, precision and conventions as kv_attend_decode: the
+ *   records of virtual sequence z stream page by page into the same split-K decode kernel.
+ *   workspace: at least kv_decode_paged_workspace_bytes(...) bytes, 16-byte aligned, zero-filled before its
+ *   first use and reusable across calls that do not overlap on the device. */
+size_t kv_decode_paged_workspace_bytes(const kv_params* p, const kv_paged_cache* cache, int Hq);
+kv_status kv_attend_decode_paged(const kv_params* p, const kv_paged_cache* cache, const void* q, int Hq,
+                                 const int32_t* seq_lens_dev, const int32_t* q_pos_dev, float softmax_scale,
+                                 float* out, void* workspace, size_t ws_bytes, kv_stream_t stream);
 
 /* Uncompressed bf16 split-K flash-decode over k, v: device bf16 [B][Hkv][T_cap][d]; same q, seq_lens,
  * out conventions. The measurement comparator for the packed path (no page counterpart beyond the

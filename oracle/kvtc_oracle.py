@@ -51,6 +51,11 @@ attention; IEEE fp32 for the quantiser, whose op sequence is part of the record 
     token is the same. Unused bits are 0.
  8. Decode attention over the records: y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j) for b_j > 0, else
     mu_j; k^ = T^T y^ (and v^); o_h = softmax_t(alpha q_h . k^_t) v^ over t < seq_len, all in fp64.
+ 9. Serving layout [SPECTRA abstract: "longer contexts and larger batches"]: the query may arrive without its
+    rotary position embedding, which the decode then applies first: pair (i, i + d/2) of q rotated by the angle
+    pos * base^(-2i/d) (the half-split convention of the Llama models, no frequency rescaling), in fp64. Paged
+    and multi-layer caches change where records live, not what they hold: the tests gather a sequence's
+    records page by page and decode them with 8.
 
 Where the pages are silent this module takes the plainest reading the rest of them supports: the same
 bits/element for keys and values, an orthogonal key KLT with the query weighting in the allocation, a
@@ -643,3 +648,20 @@ def attend_decode(q, rec_k, rec_v, pk: TensorParams, pv: TensorParams, seq_len: 
     kh = reconstruct(records_for(rec_k, pk, seq_len), pk)[:seq_len]
     vh = reconstruct(records_for(rec_v, pv, seq_len), pv)[:seq_len]
     return attention(q, kh, vh, scale)
+
+
+# ----------------------------------------------------------------------------------------------------
+# 9. rotary position embedding of the query
+# ----------------------------------------------------------------------------------------------------
+def rotary_embed(x, pos: int, base: float):
+    """Rotary embedding of x [..., d] at integer position pos (fp64): for i < d/2 the pair (x_i, x_{i+d/2}) is
+    turned by the angle pos * base^(-2i/d), x_i' = x_i cos - x_{i+d/2} sin, x_{i+d/2}' = x_i sin + x_{i+d/2} cos."""
+    x = np.asarray(x, F64)
+    d = x.shape[-1]
+    half = d // 2
+    freq = np.array([float(base) ** (-2.0 * i / d) for i in range(half)], F64)
+    ang = float(pos) * freq
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = x[..., :half], x[..., half:]
+    return np.concatenate([lo * c - hi * s, lo * s + hi * c], axis=-1)
+

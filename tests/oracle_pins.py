@@ -744,3 +744,35 @@ def pin_calibrate_structure():
         assert O.code_bits(11) - 32 < p.widths.sum() <= O.code_bits(11)
         assert np.allclose(p.mu, t @ np.asarray(x, np.float64).mean(0), atol=1e-5)
         assert np.allclose(p.sigma.astype(np.float64) ** 2, p.eigvals, rtol=1e-5)
+
+# --- rotary embedding of the query ------------------------------------------------------------------
+def pin_rotary_embedding():
+    """Closed forms where the frequency is exact (channel 0 turns by one radian per position; channel d/4 by
+    base^(-1/2), 0.01 rad for base 10000), with cos and sin of 1 and 3 rad as printed in tables; then what any
+    rotation by position must satisfy: position 0 is the identity, norms are kept, two embeddings compose, and
+    an embedded query and key meet through their position difference only."""
+    d = 128
+    e = np.eye(d)
+    cos1, sin1 = 0.5403023058681398, 0.8414709848078965
+    cos3, sin3 = -0.9899924966004454, 0.1411200080598672
+    want = np.zeros(d)
+    want[0], want[64] = cos3, sin3
+    assert np.allclose(O.rotary_embed(e[0], 3, 10000.0), want, rtol=0, atol=1e-15)
+    want = np.zeros(d)
+    want[0], want[64] = -sin3, cos3
+    assert np.allclose(O.rotary_embed(e[64], 3, 10000.0), want, rtol=0, atol=1e-15)
+    want = np.zeros(d)
+    want[32], want[96] = cos1, sin1
+    assert np.allclose(O.rotary_embed(e[32], 100, 10000.0), want, rtol=0, atol=1e-14)
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, d))
+    k = rng.standard_normal(d)
+    assert np.array_equal(O.rotary_embed(x, 0, 500000.0), x)
+    for pos in (1, 77, 131071):
+        y = O.rotary_embed(x, pos, 500000.0)
+        assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    assert np.allclose(O.rotary_embed(O.rotary_embed(x, 1000, 5e5), 234, 5e5), O.rotary_embed(x, 1234, 5e5),
+                       atol=1e-12)
+    a1 = O.rotary_embed(x, 5000, 5e5) @ O.rotary_embed(k, 4000, 5e5)
+    a2 = O.rotary_embed(x, 1000, 5e5) @ k
+    assert np.allclose(a1, a2, atol=1e-10)

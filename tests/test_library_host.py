@@ -303,3 +303,45 @@ def test_sizes():
     P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 1.33)
     assert kvtc.kv_cache_bytes(P, 0, 2, 8, 1024) == 2 * 8 * 1024 * 11 * 4
     assert kvtc.kv_cache_bytes(P, 1, 2, 8, 1024) == 2 * 8 * 1024 * 5 * 4
+
+
+def test_rope_base_is_kept_and_checked(tmp_path):
+    """The rotary base set on a table survives save and load (file version 3); negative or non-finite bases are
+    refused; 0 removes it."""
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75)
+    assert P.rope_base == 0.0
+    P.set_rope(500000.0)
+    path = str(tmp_path / "rope.kvtc")
+    P.save(path)
+    assert kvtc.kv_params_load(path).rope_base == 500000.0
+    for bad in (-1.0, float("inf"), float("nan")):
+        with pytest.raises(kvtc.KvError) as e:
+            P.set_rope(bad)
+        assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+    P.set_rope(0.0)
+    P.save(path)
+    assert kvtc.kv_params_load(path).rope_base == 0.0
+
+
+def test_paged_calls_refuse_params_not_uploaded():
+    d = 128
+    T = np.eye(d, dtype=np.float32)[None]
+    z = np.zeros((1, d), np.float32)
+    w = np.zeros((1, d), np.int32)
+    P = kvtc.kv_params_from_arrays(T, z, z + 1, w, 1, T, z, z + 1, w, 1)
+    cache = kvtc.make_paged_cache(16, 16, 4, 32, 1, 1, 1, 4, 16)
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_encode_paged(P, cache, 16, 16, kvtc.KV_DTYPE_BF16, 4, 16, stream=0)
+    assert e.value.status == kvtc.KV_ERR_INVALID_ARG and "not uploaded" in str(e.value)
+    with pytest.raises(kvtc.KvError) as e:
+        kvtc.kv_attend_decode_paged(P, cache, 16, 4, 16, None, 0.1, 16, 16, ws_bytes=1 << 20, stream=0)
+    assert e.value.status == kvtc.KV_ERR_INVALID_ARG and "not uploaded" in str(e.value)
+
+
+def test_paged_sizes():
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=16, steps=1)
+    P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 1.33)
+    assert kvtc.kv_paged_cache_bytes(P, 0, 100, 64, 8) == 100 * 8 * 64 * 11 * 4
+    assert kvtc.kv_paged_cache_bytes(P, 1, 100, 64, 8) == 100 * 8 * 64 * 5 * 4
+    assert kvtc.kv_paged_cache_bytes(P, 0, 0, 64, 8) == 0

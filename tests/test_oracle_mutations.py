@@ -10,7 +10,7 @@ _orig = {name: getattr(O, name) for name in
          ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
           "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat",
           "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout", "storage_order", "attend_decode",
-          "exchange_rate", "joint_split", "attention_aware_key_basis", "whitened_key_transform"]}
+          "exchange_rate", "joint_split", "attention_aware_key_basis", "whitened_key_transform", "rotary_embed"]}
 
 
 def _klt_transposed(sigma):
@@ -273,6 +273,27 @@ def _whitened_ignores_queries(sigma_k, m_q):
     return _orig["whitened_key_transform"](sigma_k, np.eye(len(m_q)))
 
 
+def _rope_interleaved(x, pos, base):
+    """Pairs (2i, 2i + 1) instead of (i, i + d/2)."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    freq = np.array([float(base) ** (-2.0 * i / d) for i in range(d // 2)])
+    c, s = np.cos(pos * freq), np.sin(pos * freq)
+    a, b = x[..., 0::2], x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., 0::2], y[..., 1::2] = a * c - b * s, a * s + b * c
+    return y
+
+
+def _rope_backwards(x, pos, base):
+    return _orig["rotary_embed"](x, -pos, base)
+
+
+def _rope_frequency_halved(x, pos, base):
+    """Exponent -i/d instead of -2i/d."""
+    return _orig["rotary_embed"](x, pos, np.sqrt(base))
+
+
 MUTATIONS = [
     ("klt", _klt_transposed, P.pin_klt_known_spectrum),
     ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
@@ -305,6 +326,9 @@ MUTATIONS = [
     ("attention_aware_key_basis", _aware_rotates_u_backwards, P.pin_aware_basis_two_channels),
     ("whitened_key_transform", _whitened_full_power, P.pin_whitened_key_transform),
     ("whitened_key_transform", _whitened_ignores_queries, P.pin_whitened_key_transform),
+    ("rotary_embed", _rope_interleaved, P.pin_rotary_embedding),
+    ("rotary_embed", _rope_backwards, P.pin_rotary_embedding),
+    ("rotary_embed", _rope_frequency_halved, P.pin_rotary_embedding),
 ]
 
 

@@ -122,3 +122,7 @@ def test_aware_basis_bounds():
 
 def test_whitened_key_transform():
     P.pin_whitened_key_transform()
+
+
+def test_rotary_embedding():
+    P.pin_rotary_embedding()

@@ -54,15 +54,15 @@ __host__ __device__ constexpr bool dec_desc_smem(int nw, int nblk) { return nw =
 __host__ __device__ constexpr int dec_stage_tokens(int nw) { return WTOK * nw; }
 
 struct DecArgs {
-  const uint32_t* rec[2];
-  const __nv_bfloat16* q;
-  const int32_t* seq_lens;
+  CacheView c;              // the records (dense or paged) and the parameter set of each (z, KV head)
+  const __nv_bfloat16* q;   // [B][Hq][128]
+  const int32_t* seq_lens;  // [c.B]
+  const int32_t* q_pos;     // [c.B] query positions for the rotary embedding, or null
   unsigned* cnt;    // [B*Hkv] arrival counters: zero before a call, left at zero after it
   float* part;      // [B*Hkv][splits][g][PSTR] split partials (m, l, -, -, U[128])
   float* out;       // [B][Hq][128]
-  long long T_cap;
   long long wait_ns;
-  int B, Hkv, Hq, g, per_seq, splits, stages;
+  int B, Hkv, Hq, g, splits, stages;  // B: virtual sequences z of the launch (layers x sequences)
   float scale_log2;
 };
 
@@ -270,9 +270,11 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
   __shared__ __align__(8) uint64_t full[MAX_STAGES];
   __shared__ unsigned rel[MAX_STAGES];  // warps done with the stage in each ring slot
   __shared__ int s_abort, s_last, s_issued;
-  const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  __shared__ long long s_trange[2];  // the split's token range, for the refills (kept out of the loop's registers)
+  const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;  // b: virtual sequence (layer, sequence)
   const int bh = b * a.Hkv + kh;
-  const int set = a.per_seq ? bh : kh;
+  const int set = view_set(a.c, b, kh);
+  const int bseq = b % a.c.B;  // the sequence within its layer
   const TensorDev& TK = P.t[0];
   const TensorDev& TV = P.t[1];
   const int RK = RK_ ? RK_ : TK.r_words, RV = RV_ ? RV_ : TV.r_words;
@@ -355,6 +357,14 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
     kv4 = reinterpret_cast<const float4*>(TK.wsum2 + so)[lane];
     ksmax = __ldg(TK.smax + set);
   }
+  // rotary embedding of q: warp h's copy of the 64 frequencies (turns), by asynchronous copies into the prologue's
+  // partial-q~ scratch, which the q preparation writes only after the embedding has read them
+  unsigned long long* const rturn =
+      reinterpret_cast<unsigned long long*>(smem + L.pro + (uint32_t)(MAX_G * D) * 4u) + warp * (D / 2);
+  if (a.q_pos && warp < g) {
+    cp_async16(smem_u32(rturn + 2 * lane), P.rope_turns + 2 * lane);
+    cp_async_commit();
+  }
   __syncthreads();
 
   // The previous kernel of the stream (an append, say) may still be running: q, the lengths and the records are
@@ -363,7 +373,8 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
   // q and the length first, so that their loads do not queue behind the ring's copies
   uint2 qraw = make_uint2(0u, 0u);
   if (warp < g) qraw = reinterpret_cast<const uint2*>(a.q + ((size_t)b * a.Hq + (size_t)kh * g + warp) * D)[lane];
-  const long long Lseq = max(0LL, min((long long)a.seq_lens[b], a.T_cap));
+  const long long Lseq = max(0LL, min((long long)a.seq_lens[bseq], a.c.T_cap));
+  const long long qpos = a.q_pos ? (long long)a.q_pos[bseq] : 0LL;
 
   // this sequence's tokens spread over all the splits in whole warp blocks, sized from its own length, so that a
   // short sequence in a long cache (or in a ragged batch) keeps every split busy
@@ -375,20 +386,52 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
 
   // ---- record stages stream into the ring by bulk copies: thread 0 fills the ring, then the last of the NW warps
   // to release a slot refills it at once with the stage NS further on ----
-  const uint32_t* krec = a.rec[0] + (size_t)bh * a.T_cap * RK;
-  const uint32_t* vrec = a.rec[1] + (size_t)bh * a.T_cap * RV;  // two-token records: same bytes per token
   const uint32_t ring = smem_u32(smem);
-  auto issue_tile = [&](int i) {
+  // stage i of the split's token range [ta, tz)
+  auto issue_tile = [&](int i, long long ta, long long tz) {
     const int s = i % NS;
-    const long long tb = t0 + (long long)i * ST;
-    long long n = min((long long)ST, t1 - tb);
-    n = min((n + 3) & ~3LL, a.T_cap - tb);
-    const uint32_t kbytes = (uint32_t)(n * RK * 4), vbytes = (uint32_t)(n * RV * 4);
+    const long long tb = ta + (long long)i * ST;
+    long long n = min((long long)ST, tz - tb);
+    n = min((n + 3) & ~3LL, a.c.T_cap - tb);
     const uint32_t bar = smem_u32(&full[s]);
     const uint32_t dst = ring + (uint32_t)s * stage_bytes;
-    mbar_expect_tx(bar, kbytes + vbytes);
-    bulk_g2s(dst, krec + tb * RK, kbytes, bar);
-    bulk_g2s(dst + ST * RK * 4, vrec + tb * RV, vbytes, bar);
+    if (a.c.bt == nullptr) {
+      const uint32_t* krec = a.c.rec[0] + (size_t)bh * a.c.T_cap * RK;
+      const uint32_t* vrec = a.c.rec[1] + (size_t)bh * a.c.T_cap * RV;  // two-token records: same bytes per token
+      const uint32_t kbytes = (uint32_t)(n * RK * 4), vbytes = (uint32_t)(n * RV * 4);
+      mbar_expect_tx(bar, kbytes + vbytes);
+      bulk_g2s(dst, krec + tb * RK, kbytes, bar);
+      bulk_g2s(dst + ST * RK * 4, vrec + tb * RV, vbytes, bar);
+      return;
+    }
+    // paged: one copy per tensor and page the stage touches (pages start at multiples of 32 tokens, so every
+    // piece starts and ends on a 16-byte boundary); the barrier expects the bytes of the pages in range, and a
+    // page index out of range is reported and its tokens left as they are. Positions fit 32 bits (checked by the
+    // host) and pages hold a power of two of tokens.
+    const int psh = a.c.P_shift, p0 = (int)tb, p1 = (int)(tb + n);
+    const int32_t* btr = a.c.bt + (size_t)b * a.c.max_pages;
+    uint32_t bytes = 0;
+    for (int p = p0; p < p1;) {
+      const int e = min(p1, ((p >> psh) + 1) << psh);
+      const unsigned pg = (unsigned)__ldg(btr + (p >> psh));
+      if (pg < (unsigned long long)a.c.n_pages) bytes += (uint32_t)(e - p) * (uint32_t)(RK + RV) * 4u;
+      p = e;
+    }
+    mbar_expect_tx(bar, bytes);
+    for (int p = p0; p < p1;) {
+      const int e = min(p1, ((p >> psh) + 1) << psh);
+      const unsigned pg = (unsigned)__ldg(btr + (p >> psh));
+      if (pg < (unsigned long long)a.c.n_pages) {
+        const uint32_t cnt = (uint32_t)(e - p), o = (uint32_t)(p - p0);
+        // token row within the pool
+        const size_t row = (((size_t)pg * a.Hkv + kh) << psh) + (size_t)(p & ((1 << psh) - 1));
+        bulk_g2s(dst + o * RK * 4u, a.c.rec[0] + row * RK, cnt * RK * 4u, bar);
+        bulk_g2s(dst + ST * RK * 4 + o * RV * 4u, a.c.rec[1] + row * RV, cnt * RV * 4u, bar);
+      } else {
+        atomicOr(&g_status, ST_BAD_INDEX);
+      }
+      p = e;
+    }
   };
   // this warp is done reading stage i: the last warp to say so issues stage i + NS into the same slot (its
   // acquire-release count orders every warp's reads of the slot before the refill's writes)
@@ -402,15 +445,17 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
         rel[s] = 0u;
         if (i + NS < ntiles) {
           fence_proxy_async_smem();
-          issue_tile(i + NS);
+          issue_tile(i + NS, s_trange[0], s_trange[1]);
           atomicMax(&s_issued, i + NS + 1);
         }
       }
     }
   };
   if (warp == NW - 1) {  // the last warp fills the ring, a stage per lane (the q preparation runs meanwhile)
-    if (lane < NS && lane < ntiles) issue_tile(lane);
+    if (lane < NS && lane < ntiles) issue_tile(lane, t0, t1);
     if (lane == 0) {
+      s_trange[0] = t0;
+      s_trange[1] = t1;
       if (!CL && split == 0 && nzV > 0)  // the merging split reads the scaled T_V rows at its end
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(TV.Tsc + so * D), "r"((uint32_t)nzV * D * 4)
                      : "memory");
@@ -471,8 +516,24 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
     }
     if (warp < g) {  // warp h: head h's row of q, its norm and its three dot products
       const int h = warp;
-      const float4 qv = make_float4(bf16_bits_f(qraw.x & 0xFFFFu), bf16_bits_f(qraw.x >> 16),
-                                    bf16_bits_f(qraw.y & 0xFFFFu), bf16_bits_f(qraw.y >> 16));
+      float4 qv = make_float4(bf16_bits_f(qraw.x & 0xFFFFu), bf16_bits_f(qraw.x >> 16),
+                              bf16_bits_f(qraw.y & 0xFFFFu), bf16_bits_f(qraw.y >> 16));
+      if (a.q_pos) {  // rotary embedding at the query's position: pairs (e, e + 64) sit in lanes l and l ^ 16
+        cp_async_wait_all();
+        __syncwarp();
+        float* v = reinterpret_cast<float*>(&qv);
+        const float sg = lane < 16 ? -1.f : 1.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          // the angle in turns, reduced exactly (64-bit fixed point, wrapping), as a signed fraction in [-1/2, 1/2)
+          const unsigned long long fr = rturn[(4 * lane + u) & (D / 2 - 1)];
+          const long long tw = (long long)((unsigned long long)qpos * fr);
+          float sn, cs;
+          sincospif((float)tw * 0x1p-63f, &sn, &cs);
+          const float pv = __shfl_xor_sync(0xffffffffu, v[u], 16);
+          v[u] = fmaf(sg * pv, sn, v[u] * cs);
+        }
+      }
       reinterpret_cast<float4*>(qs + h * D)[lane] = qv;
       const float n2 = warp_sum(qv.x * qv.x + qv.y * qv.y + qv.z * qv.z + qv.w * qv.w);
       const float c0 = warp_sum(qv.x * kb4.x + qv.y * kb4.y + qv.z * kb4.z + qv.w * kb4.w);
@@ -791,7 +852,7 @@ __global__ void __launch_bounds__(32 * NW, 1) decode_kernel(ParamsDev P, DecArgs
   float* hs = fs + E.hs;        // [8][4]: merged l, Z, S
   float* esw = fs + E.esw;      // [MAX_SPLITS][8]: split weights
   float* rot = fs + E.rot;
-  float* outp = a.out + ((size_t)b * a.Hq + (size_t)kh * g) * D;
+  float* outp = a.out + ((size_t)b * a.Hq + (size_t)kh * g) * D;  // (b: the virtual sequence)
   if (s_abort) {  // drain the copies this CTA may still have in flight, then leave an empty partial
     if (tid == 0) {
       const int issued = s_issued;
@@ -1168,25 +1229,23 @@ static cudaError_t launch_decode_rw(cudaLaunchConfig_t& cfg, const ParamsDev& P,
   return launch_decode_kernel<NB, 0, 0, NBLK, NW, 0>(cfg, P, a, ws_splits, plan);
 }
 
-kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
-                        const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
-                        cudaStream_t s, int32_t* plan) {
+kv_status launch_decode(const ParamsDev& P, const CacheView& c, const void* q, int B, int Hq,
+                        const int32_t* seq_lens, const int32_t* q_pos, float scale, float* out, void* ws,
+                        const DecodeLayout& L, cudaStream_t s, int32_t* plan) {
   DecArgs a;
   uint8_t* w = static_cast<uint8_t*>(ws);  // null when only planning
-  a.rec[0] = c.k_rec;
-  a.rec[1] = c.v_rec;
+  a.c = c;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.seq_lens = seq_lens;
+  a.q_pos = q_pos;
   a.cnt = reinterpret_cast<unsigned*>(w + L.off_cnt);
   a.part = reinterpret_cast<float*>(w + L.off_part);
   a.out = out;
-  a.T_cap = c.T_cap;
   a.wait_ns = g_wait_limit_ns;
   a.B = B;
   a.Hkv = c.Hkv;
   a.Hq = Hq;
   a.g = Hq / c.Hkv;
-  a.per_seq = c.per_seq_params;
   a.splits = L.splits;
   a.stages = 2;
   a.scale_log2 = scale * 1.4426950408889634f;

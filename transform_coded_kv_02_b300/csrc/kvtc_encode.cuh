@@ -8,11 +8,11 @@ namespace kvtc {
 // encode: warp per token
 // ======================================================================================================
 struct EncArgs {
-  const void* src[2];
-  uint32_t* dst[2];
-  const int64_t* dst_pos;
-  int B, Hkv, per_seq;
-  long long t_new, T_cap;
+  const void* src[2];  // [Z][Hkv][t_new][D]
+  CacheView c;
+  const int64_t* dst_pos;  // [B]: write position of each sequence's first new token (every layer alike)
+  int Z;                   // virtual sequences (layers x sequences)
+  long long t_new;
   long long wait_ns;
 };
 
@@ -20,18 +20,19 @@ template <bool BF16>
 __global__ void __launch_bounds__(256) encode_warp_kernel(ParamsDev P, EncArgs a) {
   __shared__ uint32_t rec_s[8][2 * MAX_RW + 4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long per_tensor = (long long)a.B * a.Hkv * a.t_new;
+  const int Hkv = a.c.Hkv;
+  const long long per_tensor = (long long)a.Z * Hkv * a.t_new;
   const long long idx = (long long)blockIdx.x * 8 + warp;
   if (idx >= 2 * per_tensor) return;
   const int tensor = (int)(idx / per_tensor);
   long long r = idx - (long long)tensor * per_tensor;
   const long long t = r % a.t_new;
   r /= a.t_new;
-  const int h = (int)(r % a.Hkv);
-  const int b = (int)(r / a.Hkv);
-  const int set = a.per_seq ? b * a.Hkv + h : h;
+  const int h = (int)(r % Hkv);
+  const int z = (int)(r / Hkv);
+  const int set = view_set(a.c, z, h);
   const TensorDev& td = P.t[tensor];
-  const size_t xo = (((size_t)b * a.Hkv + h) * a.t_new + t) * D + 4 * lane;
+  const size_t xo = (((size_t)z * Hkv + h) * a.t_new + t) * D + 4 * lane;
   float x[4];
   if (BF16) {
     const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.src[tensor]) + xo);
@@ -61,15 +62,11 @@ __global__ void __launch_bounds__(256) encode_warp_kernel(ParamsDev P, EncArgs a
       y[3] = fmaf(tt.w, xk, y[3]);
     }
   }
-  const long long pos = a.dst_pos[b] + t;
+  const long long pos = a.dst_pos[z % a.c.B] + t;
   uint32_t* out = nullptr;
-  if (pos >= 0 && pos < a.T_cap) {
-    const size_t bh = (size_t)b * a.Hkv + h;
-    out = tensor == 0 ? a.dst[0] + (bh * (size_t)a.T_cap + (size_t)pos) * td.r_words
-                      : a.dst[1] + (bh * (size_t)(a.T_cap / 2) + (size_t)(pos >> 1)) * 2 * td.r_words;
-  } else if (lane == 0) {
-    atomicOr(&g_status, ST_BAD_INDEX);
-  }
+  if (pos >= 0 && pos < a.c.T_cap)
+    out = tensor == 0 ? view_key_record(a.c, z, h, pos, td.r_words) : view_value_record(a.c, z, h, pos, td.r_words);
+  if (!out && lane == 0) atomicOr(&g_status, ST_BAD_INDEX);
   quantize_pack_warp(td, set, y, lane, rec_s[warp], out, tensor == 1, (int)(pos & 1));
 }
 
@@ -95,8 +92,8 @@ __global__ void __launch_bounds__(AP_THREADS) encode_append_kernel(ParamsDev P, 
   // a decode call that follows may start preparing (it waits for this grid before it reads q or any record)
   pdl_launch_dependents();
   const int tensor = blockIdx.y, bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, j = tid;
-  const int b = bh / a.Hkv, h = bh - b * a.Hkv;
-  const int set = a.per_seq ? bh : h;
+  const int z = bh / a.c.Hkv, h = bh - z * a.c.Hkv;
+  const int set = view_set(a.c, z, h);
   const TensorDev& td = tensor == 0 ? P.t[0] : P.t[1];
   if (tid == 0) {
     mbar_init(smem_u32(&bar), 1);
@@ -123,7 +120,7 @@ __global__ void __launch_bounds__(AP_THREADS) encode_append_kernel(ParamsDev P, 
     cw = 2u + (dsc & 255u);
     cb = (dsc >> 8) & 255u;
   }
-  const long long p0 = a.dst_pos[b];
+  const long long p0 = a.dst_pos[z % a.c.B];
   const void* src = tensor == 0 ? a.src[0] : a.src[1];
   auto load_x = [&](long long t) {
     const size_t xo = ((size_t)bh * a.t_new + t) * D + j;
@@ -166,13 +163,14 @@ __global__ void __launch_bounds__(AP_THREADS) encode_append_kernel(ParamsDev P, 
     __syncthreads();
     const long long pos = p0 + t;
     const uint32_t zs = (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
-    if (pos >= 0 && pos < a.T_cap) {
+    uint32_t* out = nullptr;
+    if (pos >= 0 && pos < a.c.T_cap)
+      out = tensor == 0 ? view_key_record(a.c, z, h, pos, R) : view_value_record(a.c, z, h, pos, R);
+    if (out) {
       if (tensor == 0) {
-        uint32_t* out = a.dst[0] + ((size_t)bh * a.T_cap + (size_t)pos) * R;
         for (int i = tid; i < R; i += AP_THREADS) out[i] = i == 0 ? zs : rec_s[i];
       } else {
         // the token's half of its two-token record: its z/s word and its 16-bit half of every code word
-        uint32_t* out = a.dst[1] + ((size_t)bh * (a.T_cap / 2) + (size_t)(pos >> 1)) * 2 * R;
         const int hf = (int)(pos & 1);
         for (int i = tid; i < W; i += AP_THREADS) {
           if (i < 2) {
@@ -192,32 +190,28 @@ __global__ void __launch_bounds__(AP_THREADS) encode_append_kernel(ParamsDev P, 
 // path: 0 = automatic, 1 = CUDA cores (append kernel for a few tokens per head, else warp per token),
 // 2 = tensor cores (bf16 only). Every path writes records within the codec's end-to-end bar; the two CUDA-core
 // kernels write identical records.
-kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, const void* v, int dtype, int B,
+kv_status launch_encode(const ParamsDev& P, const CacheView& c, const void* k, const void* v, int dtype, int Z,
                         int64_t t_new, const int64_t* dst_pos, int path, cudaStream_t s) {
   if (path == 2 && dtype != KV_DTYPE_BF16) {
     set_error("the tensor-core encode takes bf16 tokens only");
     return KV_ERR_UNSUPPORTED;
   }
   if (path == 2 || (path == 0 && dtype == KV_DTYPE_BF16 && t_new >= TC_TILE)) {
-    const kv_status st = launch_encode_tc(P, c, k, v, B, t_new, dst_pos, s);
+    const kv_status st = launch_encode_tc(P, c, k, v, Z, t_new, dst_pos, s);
     if (st != KV_ERR_UNSUPPORTED || path == 2) return st;
     clear_error();
   }
   EncArgs a;
   a.src[0] = k;
   a.src[1] = v;
-  a.dst[0] = c.k_rec;
-  a.dst[1] = c.v_rec;
+  a.c = c;
   a.dst_pos = dst_pos;
-  a.B = B;
-  a.Hkv = c.Hkv;
-  a.per_seq = c.per_seq_params;
+  a.Z = Z;
   a.t_new = t_new;
-  a.T_cap = c.T_cap;
   a.wait_ns = g_wait_limit_ns;
   if (t_new <= AP_MAX_TOKENS) {
     const size_t smem = append_smem_bytes();
-    const dim3 grid((unsigned)(B * c.Hkv), 2);
+    const dim3 grid((unsigned)(Z * c.Hkv), 2);
     const void* fn = dtype == KV_DTYPE_BF16 ? (const void*)encode_append_kernel<true>
                                             : (const void*)encode_append_kernel<false>;
     const cudaError_t e = ensure_dyn_smem(fn, smem);
@@ -231,7 +225,7 @@ kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, co
       encode_append_kernel<false><<<grid, AP_THREADS, smem, s>>>(P, a);
     return launch_check("encode_append_kernel");
   }
-  const long long warps = 2LL * B * c.Hkv * t_new;
+  const long long warps = 2LL * Z * c.Hkv * t_new;
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   if (dtype == KV_DTYPE_BF16)
     encode_warp_kernel<true><<<blocks, 256, 0, s>>>(P, a);

@@ -32,10 +32,10 @@ constexpr uint32_t TC_OP_BYTES = 128u * 128u * 2u;   // one 128 x 128 bf16 opera
 constexpr uint32_t TC_BOX_BYTES = 128u * 128u;       // one 128-row x 128-byte box
 
 struct EncTcArgs {
-  const int64_t* dst_pos;
-  uint32_t* dst[2];
-  int B, Hkv, per_seq, n_sets;
-  long long t_new, T_cap;
+  const int64_t* dst_pos;  // [B] (every layer alike)
+  CacheView c;
+  int Z, n_sets;           // Z: virtual sequences (layers x sequences)
+  long long t_new;
   int units, tiles_per_head;
   long long wait_ns;
 };
@@ -210,12 +210,12 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
   // contiguous run of units of this CTA
   const long long U = a.units;
   const int u0 = (int)(U * blockIdx.x / gridDim.x), u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
-  const int per_tensor = a.B * a.Hkv * a.tiles_per_head;
+  const int per_tensor = a.Z * a.c.Hkv * a.tiles_per_head;
   // unit -> (tensor, bh, tile); the transform key (tensor, set) decides when T is restaged
   auto unit_tensor = [&](int u) { return u / per_tensor; };
   auto unit_bh = [&](int u) { return (u - unit_tensor(u) * per_tensor) / a.tiles_per_head; };
   auto unit_tile = [&](int u) { return (u - unit_tensor(u) * per_tensor) % a.tiles_per_head; };
-  auto unit_set = [&](int u) { const int bh = unit_bh(u); return a.per_seq ? bh : bh % a.Hkv; };
+  auto unit_set = [&](int u) { const int bh = unit_bh(u); return view_set(a.c, bh / a.c.Hkv, bh % a.c.Hkv); };
   auto unit_tkey = [&](int u) { return unit_tensor(u) * a.n_sets + unit_set(u); };
 
   if (tid == 0) {
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       const int tensor = unit_tensor(u), bh = unit_bh(u), tile = unit_tile(u), set = unit_set(u);
       const TensorDev& td = P.t[tensor];
       const int R = td.r_words;
-      const int b = bh / a.Hkv;
+      const int z = bh / a.c.Hkv, hk = bh - z * a.c.Hkv;
       if (unit_tkey(u) != cached_key) {  // this group's channel parameters (the group is idle here)
         tc_stage_channel(td, tensor, set, row, pmi, ptc, phh, pbits);
         cached_key = unit_tkey(u);
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       }
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
-      const long long pos0 = a.dst_pos[b] + (long long)tile * TC_TILE;
+      const long long pos0 = a.dst_pos[z % a.c.B] + (long long)tile * TC_TILE;
       const int half = (int)((pos0 + row) & 1);
       const int lr = (row + (int)(pos0 & 1)) >> 1;  // local two-token record of a value token
       const int PK = R | 1, PV = 2 * R + 1;
@@ -377,12 +377,15 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[g]));
       rec[tensor == 0 ? 0 : half] = zs;
       named_bar(1 + g, 128);
-      // ---- copy-out: the tile's records are contiguous in the cache; the group copies them word by word ----
+      // ---- copy-out: in a dense cache the tile's records are contiguous and the group copies them word by word;
+      // in a paged one record by record, each at its page ----
       const int n_valid = (int)min((long long)TC_TILE, a.t_new - (long long)tile * TC_TILE);
       const int gt = tid & 127;  // thread index within the group
+      const long long T_cap = a.c.T_cap;
+      const bool dense_run = a.c.bt == nullptr && pos0 >= 0 && pos0 + n_valid <= T_cap;
       if (tensor == 0) {
-        uint32_t* dst = a.dst[0] + (size_t)bh * a.T_cap * R;
-        if (pos0 >= 0 && pos0 + n_valid <= a.T_cap) {
+        uint32_t* dst = a.c.rec[0] + (size_t)bh * (a.c.bt ? 0 : T_cap) * R;  // (dense)
+        if (dense_run) {
           const uint32_t mR = 0xFFFFFFFFu / (uint32_t)R + 1u;  // i / R = umulhi(i, mR) for i < 2^16
           uint32_t* d0 = dst + pos0 * R;
           for (int i = gt; i < n_valid * R; i += 128) {
@@ -392,22 +395,23 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
         } else {
           for (int r = gt; r < n_valid; r += 128) {
             const long long pos = pos0 + r;
-            if (pos < 0 || pos >= a.T_cap) {
+            uint32_t* out = pos >= 0 && pos < T_cap ? view_key_record(a.c, z, hk, pos, R) : nullptr;
+            if (!out) {
               atomicOr(&g_status, ST_BAD_INDEX);
               continue;
             }
-            for (int w = 0; w < R; ++w) dst[pos * R + w] = stage[r * PK + w];
+            for (int w = 0; w < R; ++w) out[w] = stage[r * PK + w];
           }
         }
       } else {
         // local record r holds tokens 2r - odd and 2r - odd + 1 of the tile; the first and the last record may
         // hold only one of this tile's tokens (their other halves belong to neighbouring writes)
-        uint32_t* dst = a.dst[1] + (size_t)bh * (a.T_cap / 2) * 2 * R;
+        uint32_t* dst = a.c.rec[1] + (size_t)bh * (a.c.bt ? 0 : T_cap / 2) * 2 * R;  // (dense)
         const int odd = (int)(pos0 & 1);
         const int nrec = ((n_valid - 1 + odd) >> 1) + 1;
         const int f0 = odd, f1 = ((n_valid + odd) & 1) ? nrec - 1 : nrec;  // full records [f0, f1)
         const long long gr0 = pos0 >> 1;  // global record of local record 0 (rounds toward minus infinity)
-        if (pos0 >= 0 && pos0 + n_valid <= a.T_cap) {
+        if (dense_run) {
           const int W2 = 2 * R;
           const uint32_t mW = 0xFFFFFFFFu / (uint32_t)W2 + 1u;
           uint32_t* d0 = dst + (gr0 + f0) * W2;
@@ -437,12 +441,12 @@ __global__ void __launch_bounds__((4 * NACC + 2) * 32, 1)
               const int tr = 2 * r - odd + hh;
               if (tr < 0 || tr >= n_valid) continue;
               const long long pos = pos0 + tr;
-              if (pos < 0 || pos >= a.T_cap) {
+              uint32_t* drec = pos >= 0 && pos < T_cap ? view_value_record(a.c, z, hk, pos, R) : nullptr;
+              if (!drec) {
                 atomicOr(&g_status, ST_BAD_INDEX);
                 continue;
               }
               const uint32_t* src = stage + r * PV;
-              uint32_t* drec = dst + (pos >> 1) * 2 * R;
               drec[hh] = src[hh];
               for (int w = 2; w < 2 * R; ++w)
                 reinterpret_cast<uint16_t*>(drec)[2 * w + hh] = reinterpret_cast<const uint16_t*>(src)[2 * w + hh];
@@ -508,9 +512,9 @@ static cudaError_t launch_encode_tc_n(const ParamsDev& P, const EncTcArgs& a, co
 
 // Tensor-core encode of bf16 tokens. Returns KV_ERR_UNSUPPORTED (nothing launched) when the shapes fall outside
 // what the kernel handles, so the caller can take the CUDA-core path.
-static kv_status launch_encode_tc(const ParamsDev& P, const kv_cache& c, const void* k, const void* v, int B,
+static kv_status launch_encode_tc(const ParamsDev& P, const CacheView& c, const void* k, const void* v, int Z,
                                   int64_t t_new, const int64_t* dst_pos, cudaStream_t s) {
-  const long long rows = (long long)B * c.Hkv * t_new;
+  const long long rows = (long long)Z * c.Hkv * t_new;
   if (rows + TC_TILE >= (1LL << 31) || P.n_sets * TC_NSPLIT * D >= (1 << 30)) {
     set_error("tensor-core encode: %lld token rows exceed the kernel's 32-bit tile coordinates", rows);
     return KV_ERR_UNSUPPORTED;
@@ -533,16 +537,12 @@ static kv_status launch_encode_tc(const ParamsDev& P, const kv_cache& c, const v
   }
   EncTcArgs a;
   a.dst_pos = dst_pos;
-  a.dst[0] = c.k_rec;
-  a.dst[1] = c.v_rec;
-  a.B = B;
-  a.Hkv = c.Hkv;
-  a.per_seq = c.per_seq_params;
+  a.c = c;
+  a.Z = Z;
   a.n_sets = P.n_sets;
   a.t_new = t_new;
-  a.T_cap = c.T_cap;
   a.tiles_per_head = (int)((t_new + TC_TILE - 1) / TC_TILE);
-  const long long units = 2LL * B * c.Hkv * a.tiles_per_head;
+  const long long units = 2LL * Z * c.Hkv * a.tiles_per_head;
   if (units >= (1LL << 31)) {
     set_error("tensor-core encode: too many tiles");
     return KV_ERR_UNSUPPORTED;

@@ -729,6 +729,17 @@ extern "C" kv_status kv_params_set_inverse(kv_params* p, int tensor, const float
   return KV_OK;
 }
 
+static constexpr double kPi = 3.14159265358979323846;
+
+extern "C" kv_status kv_params_set_rope(kv_params* p, double base) {
+  clear_error();
+  KV_REQUIRE(p, KV_ERR_INVALID_ARG, "kv_params_set_rope: null table");
+  KV_REQUIRE(std::isfinite(base) && base >= 0.0, KV_ERR_INVALID_ARG, "rotary base %g must be finite and >= 0", base);
+  p->rope_base = base;
+  return KV_OK;
+}
+extern "C" double kv_params_get_rope(const kv_params* p) { return p ? p->rope_base : 0.0; }
+
 extern "C" kv_status kv_params_from_arrays(int d, int n_sets, const float* T_k, const float* mu_k,
                                            const float* sigma_k, const int32_t* widths_k, int r_words_k,
                                            const float* T_v, const float* mu_v, const float* sigma_v,
@@ -921,6 +932,16 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
     pidx[t] = reserve((size_t)S * (t == 0 ? 64 : 128));
   }
   pmask = reserve((size_t)S * 4);
+  // the rotary embedding's frequencies as fractions of a turn, 64-bit fixed point
+  const bool has_rope = p->rope_base > 0.0;
+  const Piece prope = has_rope ? reserve((size_t)(D / 2) * 8) : Piece{0, 0};
+  if (has_rope) {
+    unsigned long long* rt = (unsigned long long*)&blob[prope.off];
+    for (int i = 0; i < D / 2; ++i) {
+      const double f = std::pow(p->rope_base, -2.0 * i / D) / (2.0 * kPi);  // turns per position, < 1/(2 pi)
+      rt[i] = (unsigned long long)std::llround(std::ldexp(f, 64));
+    }
+  }
   int single_word = 3;
   for (int t = 0; t < 2; ++t) {
     float* T = (float*)&blob[pT[t].off];
@@ -1089,6 +1110,7 @@ extern "C" kv_status kv_params_upload(kv_params* p, kv_stream_t stream) {
   }
   p->dev.n_sets = S;
   p->dev.single_word = single_word;
+  p->dev.rope_turns = has_rope ? (const unsigned long long*)(b + prope.off) : nullptr;
   return KV_OK;
 }
 
@@ -1134,7 +1156,8 @@ static uint32_t crc32(const uint8_t* data, size_t n) {
 }
 
 static const uint32_t FILE_MAGIC = 0x4354564Bu;  // "KVTC"
-static const uint32_t FILE_VERSION = 2;  // 2: a per-tensor inverse (non-orthogonal transform) after version 1's data
+// 2: a per-tensor inverse (non-orthogonal transform) after version 1's data; 3: then the rotary embedding's base
+static const uint32_t FILE_VERSION = 3;
 
 extern "C" kv_status kv_params_save(const kv_params* p, const char* path) {
   clear_error();
@@ -1159,6 +1182,7 @@ extern "C" kv_status kv_params_save(const kv_params* p, const char* path) {
     put(&has, 4);
     if (has) put(p->Tinv[t].data(), p->Tinv[t].size() * 4);
   }
+  put(&p->rope_base, 8);
   FILE* f = fopen(path, "wb");
   KV_REQUIRE(f, KV_ERR_IO, "cannot open %s for writing", path);
   const uint32_t head[4] = {FILE_MAGIC, FILE_VERSION, (uint32_t)pay.size(), crc32(pay.data(), pay.size())};
@@ -1220,6 +1244,7 @@ extern "C" kv_status kv_params_load(const char* path, kv_params** out) {
       ok = get(p->Tinv[t].data(), n * p->d * 4);
     }
   }
+  if (ok && head[1] >= 3) ok = get(&p->rope_base, 8) && std::isfinite(p->rope_base) && p->rope_base >= 0.0;
   if (!ok || pos != pay.size()) {
     delete p;
     KV_REQUIRE(false, KV_ERR_IO, "%s: payload size mismatch", path);
@@ -1298,7 +1323,8 @@ extern "C" kv_status kv_encode(const kv_params* p, const kv_cache* c, const void
   if (t_new == 0) return KV_OK;
   KV_REQUIRE(k && v && dst_pos_dev, KV_ERR_INVALID_ARG, "null k, v or dst_pos");
   KV_REQUIRE(aligned16(k) && aligned16(v), KV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
-  return kvtc::launch_encode(p->dev, *c, k, v, dtype, B, t_new, dst_pos_dev, g_encode_path, (cudaStream_t)stream);
+  return kvtc::launch_encode(p->dev, kvtc::dense_view(*c), k, v, dtype, B, t_new, dst_pos_dev, g_encode_path,
+                             (cudaStream_t)stream);
 }
 
 namespace kvtc {
@@ -1327,8 +1353,119 @@ extern "C" kv_status kv_attend_decode(const kv_params* p, const kv_cache* c, con
   KV_REQUIRE(workspace && aligned16(workspace), KV_ERR_INVALID_ARG, "workspace null or not 16-byte aligned");
   const DecodeLayout L = kvtc::decode_layout(B, c->Hkv, Hq, c->T_cap, dev);
   KV_REQUIRE(ws_bytes >= L.total, KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
-  return kvtc::launch_decode(p->dev, *c, q, B, Hq, seq_lens_dev, softmax_scale, out, workspace, L,
-                             (cudaStream_t)stream);
+  return kvtc::launch_decode(p->dev, kvtc::dense_view(*c), q, B, Hq, seq_lens_dev, nullptr, softmax_scale, out,
+                             workspace, L, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------------------------------------------
+// paged, multi-layer cache
+// ------------------------------------------------------------------------------------------------------
+namespace kvtc {
+CacheView dense_view(const kv_cache& c) {
+  CacheView v{};
+  v.rec[0] = c.k_rec;
+  v.rec[1] = c.v_rec;
+  v.bt = nullptr;
+  v.T_cap = c.T_cap;
+  v.B = c.B;
+  v.Hkv = c.Hkv;
+  v.per_seq = c.per_seq_params;
+  v.set_base = 0;
+  v.sets_per_layer = c.per_seq_params ? c.B * c.Hkv : c.Hkv;
+  return v;
+}
+
+static CacheView paged_view(const kv_paged_cache& c) {
+  CacheView v{};
+  v.rec[0] = c.k_pages;
+  v.rec[1] = c.v_pages;
+  v.bt = c.block_table;
+  v.T_cap = (long long)c.max_pages * c.page_tokens;
+  v.n_pages = c.n_pages;
+  v.P = c.page_tokens;
+  v.P_shift = 0;
+  while ((1 << v.P_shift) < c.page_tokens) ++v.P_shift;
+  v.max_pages = c.max_pages;
+  v.B = c.B;
+  v.Hkv = c.Hkv;
+  v.per_seq = c.per_seq_params;
+  v.sets_per_layer = c.per_seq_params ? c.B * c.Hkv : c.Hkv;
+  v.set_base = c.first_layer * v.sets_per_layer;
+  return v;
+}
+}  // namespace kvtc
+
+static kv_status check_paged_cache(const kv_params* p, const kv_paged_cache* c) {
+  KV_REQUIRE(c && c->k_pages && c->v_pages && c->block_table, KV_ERR_INVALID_ARG, "null paged cache or block table");
+  KV_REQUIRE(aligned16(c->k_pages) && aligned16(c->v_pages), KV_ERR_INVALID_ARG,
+             "page pools must be 16-byte aligned");
+  KV_REQUIRE(c->page_tokens >= 32 && c->page_tokens <= (1 << 20) && (c->page_tokens & (c->page_tokens - 1)) == 0,
+             KV_ERR_INVALID_ARG, "page_tokens=%d must be a power of two from 32 to 2^20", c->page_tokens);
+  KV_REQUIRE(c->n_pages >= 1 && c->max_pages >= 1 && c->B >= 1 && c->Hkv >= 1 && c->n_layers >= 1 &&
+                 c->first_layer >= 0,
+             KV_ERR_INVALID_ARG, "paged cache dims n_pages=%lld max_pages=%d B=%d Hkv=%d n_layers=%d first_layer=%d",
+             (long long)c->n_pages, c->max_pages, c->B, c->Hkv, c->n_layers, c->first_layer);
+  KV_REQUIRE((long long)c->n_layers * c->B <= 65535 && c->Hkv <= 65535, KV_ERR_UNSUPPORTED,
+             "n_layers * B = %lld and Hkv = %d must stay within 65535", (long long)c->n_layers * c->B, c->Hkv);
+  KV_REQUIRE((long long)c->max_pages * c->page_tokens < (1LL << 31), KV_ERR_INVALID_ARG,
+             "max_pages * page_tokens = %lld must stay below 2^31", (long long)c->max_pages * c->page_tokens);
+  const long long S = c->per_seq_params ? (long long)c->B * c->Hkv : c->Hkv;
+  KV_REQUIRE((c->first_layer + (long long)c->n_layers) * S <= p->n_sets, KV_ERR_INVALID_ARG,
+             "layers %d..%d need %lld parameter sets, table has %d", c->first_layer, c->first_layer + c->n_layers - 1,
+             (c->first_layer + (long long)c->n_layers) * S, p->n_sets);
+  return KV_OK;
+}
+
+extern "C" size_t kv_paged_cache_bytes(const kv_params* p, int tensor, int64_t n_pages, int page_tokens, int Hkv) {
+  if (!p || (tensor != 0 && tensor != 1) || n_pages < 1 || page_tokens < 1 || Hkv < 1) return 0;
+  return (size_t)n_pages * Hkv * (size_t)page_tokens * p->r_words[tensor] * 4;
+}
+
+extern "C" kv_status kv_encode_paged(const kv_params* p, const kv_paged_cache* c, const void* k, const void* v,
+                                     int dtype, int64_t t_new, const int64_t* dst_pos_dev, kv_stream_t stream) {
+  clear_error();
+  kv_status st;
+  if ((st = check_params_on_device(p)) != KV_OK) return st;
+  if ((st = check_paged_cache(p, c)) != KV_OK) return st;
+  KV_REQUIRE(dtype == KV_DTYPE_BF16 || dtype == KV_DTYPE_F32, KV_ERR_UNSUPPORTED, "dtype %d unsupported", dtype);
+  const long long cap = (long long)c->max_pages * c->page_tokens;
+  KV_REQUIRE(t_new >= 0 && t_new <= cap, KV_ERR_INVALID_ARG, "t_new=%lld outside 0..%lld", (long long)t_new, cap);
+  if (t_new == 0) return KV_OK;
+  KV_REQUIRE(k && v && dst_pos_dev, KV_ERR_INVALID_ARG, "null k, v or dst_pos");
+  KV_REQUIRE(aligned16(k) && aligned16(v), KV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  return kvtc::launch_encode(p->dev, kvtc::paged_view(*c), k, v, dtype, c->n_layers * c->B, t_new, dst_pos_dev,
+                             g_encode_path, (cudaStream_t)stream);
+}
+
+extern "C" size_t kv_decode_paged_workspace_bytes(const kv_params* p, const kv_paged_cache* c, int Hq) {
+  if (!p || !c || c->B < 1 || c->n_layers < 1 || c->Hkv < 1 || Hq < c->Hkv || c->max_pages < 1 || c->page_tokens < 1)
+    return 0;
+  return kvtc::decode_layout(c->n_layers * c->B, c->Hkv, Hq, (int64_t)c->max_pages * c->page_tokens,
+                             current_device()).total;
+}
+
+extern "C" kv_status kv_attend_decode_paged(const kv_params* p, const kv_paged_cache* c, const void* q, int Hq,
+                                            const int32_t* seq_lens_dev, const int32_t* q_pos_dev,
+                                            float softmax_scale, float* out, void* workspace, size_t ws_bytes,
+                                            kv_stream_t stream) {
+  clear_error();
+  kv_status st;
+  int dev = 0;
+  if ((st = check_params_on_device(p, &dev)) != KV_OK) return st;
+  if ((st = check_paged_cache(p, c)) != KV_OK) return st;
+  KV_REQUIRE(q && seq_lens_dev && out, KV_ERR_INVALID_ARG, "null q, seq_lens or out");
+  KV_REQUIRE(Hq >= c->Hkv && Hq % c->Hkv == 0, KV_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, c->Hkv);
+  KV_REQUIRE(Hq / c->Hkv <= MAX_G, KV_ERR_UNSUPPORTED, "g = Hq/Hkv = %d > 8", Hq / c->Hkv);
+  KV_REQUIRE(aligned16(q) && aligned16(out), KV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  KV_REQUIRE(std::isfinite(softmax_scale), KV_ERR_INVALID_ARG, "non-finite softmax scale");
+  KV_REQUIRE(!q_pos_dev || p->dev.rope_turns, KV_ERR_INVALID_ARG,
+             "query positions given but the parameter table has no rotary embedding (kv_params_set_rope, then upload)");
+  KV_REQUIRE(workspace && aligned16(workspace), KV_ERR_INVALID_ARG, "workspace null or not 16-byte aligned");
+  const int Z = c->n_layers * c->B;
+  const DecodeLayout L = kvtc::decode_layout(Z, c->Hkv, Hq, (int64_t)c->max_pages * c->page_tokens, dev);
+  KV_REQUIRE(ws_bytes >= L.total, KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+  return kvtc::launch_decode(p->dev, kvtc::paged_view(*c), q, Z, Hq, seq_lens_dev, q_pos_dev, softmax_scale, out,
+                             workspace, L, (cudaStream_t)stream);
 }
 
 extern "C" kv_status kv_attend_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap,
@@ -1425,7 +1562,8 @@ extern "C" kv_status kv_debug_decode_plan(const kv_params* p, int B, int Hkv, in
   c.Hkv = Hkv;
   c.T_cap = T_cap;
   const DecodeLayout L = kvtc::decode_layout(B, Hkv, Hq, T_cap, dev);
-  return kvtc::launch_decode(p->dev, c, nullptr, B, Hq, nullptr, 1.f, nullptr, nullptr, L, nullptr, info);
+  return kvtc::launch_decode(p->dev, kvtc::dense_view(c), nullptr, B, Hq, nullptr, nullptr, 1.f, nullptr, nullptr, L,
+                             nullptr, info);
 }
 
 extern "C" kv_status kv_debug_wait_timeout_selftest(kv_stream_t stream) {

@@ -54,10 +54,48 @@ struct TensorDev {
 struct ParamsDev {
   TensorDev t[2];
   int n_sets;
+  // rotary embedding of the decode's queries: frequency i (pairs (i, i + D/2)) as a fraction of a turn in 64-bit
+  // fixed point, turns_i = round(base^(-2i/D) / (2 pi) 2^64) [D/2]; null when the table has no embedding
+  const unsigned long long* rope_turns;
   // bit 0: in every set, every key channel block the decode reads takes both slots of each lane from one code word
   // (TensorDev::single); bit 1: the same for the value blocks
   int single_word;
 };
+
+// Where a launch's records live and which parameter set serves them, built by the entry points from a kv_cache
+// (dense) or a kv_paged_cache. A launch covers Z virtual sequences z = l * B + b (layer l of the view, sequence b).
+struct CacheView {
+  uint32_t* rec[2];      // dense: [Z][Hkv][T_cap] records (values: two-token records); paged: the page pools
+  const int32_t* bt;     // paged: block table [Z][max_pages]; null: dense
+  long long T_cap;       // positions per (z, KV head): the dense capacity, or max_pages * P
+  long long n_pages;     // pages in each pool (paged)
+  int P;                 // tokens per page (paged: a power of two, at least 32)
+  int P_shift;           // log2 P
+  int max_pages;
+  int B;                 // sequences per layer: z % B indexes write positions, lengths and query positions
+  int Hkv;
+  int per_seq;           // one parameter set per (sequence, KV head) instead of per KV head
+  int set_base;          // parameter set of the view's first layer, KV head 0
+  int sets_per_layer;
+};
+__host__ __device__ inline int view_set(const CacheView& c, int z, int h) {
+  const int l = z / c.B, b = z - l * c.B;
+  return c.set_base + l * c.sets_per_layer + (c.per_seq ? b * c.Hkv + h : h);
+}
+// The key record of (z, KV head h, position pos < T_cap), or null when its page index is out of range.
+__host__ __device__ inline uint32_t* view_key_record(const CacheView& c, int z, int h, long long pos, int R) {
+  if (!c.bt) return c.rec[0] + (((size_t)z * c.Hkv + h) * (size_t)c.T_cap + (size_t)pos) * R;
+  const long long pg = c.bt[(size_t)z * c.max_pages + (size_t)(pos >> c.P_shift)];
+  if (pg < 0 || pg >= c.n_pages) return nullptr;
+  return c.rec[0] + ((((size_t)pg * c.Hkv + h) << c.P_shift) + (size_t)(pos & (c.P - 1))) * R;
+}
+// The two-token value record holding position pos (R: words per token), or null (page index out of range).
+__host__ __device__ inline uint32_t* view_value_record(const CacheView& c, int z, int h, long long pos, int R) {
+  if (!c.bt) return c.rec[1] + (((size_t)z * c.Hkv + h) * (size_t)(c.T_cap / 2) + (size_t)(pos >> 1)) * 2 * R;
+  const long long pg = c.bt[(size_t)z * c.max_pages + (size_t)(pos >> c.P_shift)];
+  if (pg < 0 || pg >= c.n_pages) return nullptr;
+  return c.rec[1] + ((((size_t)pg * c.Hkv + h) << (c.P_shift - 1)) + (size_t)((pos & (c.P - 1)) >> 1)) * 2 * R;
+}
 
 // First-fit placement of the pair slots of widths w[d] in a record of rw words (word/pos [d/2], -1 = empty);
 // false when a slot finds no room.
@@ -70,8 +108,9 @@ void set_error(const char* fmt, ...);
 void clear_error();
 
 // Kernel launchers (kvtc_kernels.cu). They assume validated arguments.
-kv_status launch_encode(const ParamsDev& P, const kv_cache& c, const void* k, const void* v, int dtype,
-                        int B, int64_t t_new, const int64_t* dst_pos, int path, cudaStream_t s);
+// (Z: virtual sequences of the view; k, v: [Z][Hkv][t_new][D])
+kv_status launch_encode(const ParamsDev& P, const CacheView& c, const void* k, const void* v, int dtype,
+                        int Z, int64_t t_new, const int64_t* dst_pos, int path, cudaStream_t s);
 struct DecodeLayout {
   int splits;
   int chunk;                  // tokens per split at full capacity, multiple of the decode tile
@@ -79,10 +118,13 @@ struct DecodeLayout {
 };
 DecodeLayout decode_layout(int B, int Hkv, int Hq, int64_t T_cap, int device);
 DecodeLayout decode_bf16_layout(int B, int Hkv, int64_t T_cap, int device);
-// plan != nullptr: fill plan[11] (see kv_debug_decode_plan) and launch nothing
-kv_status launch_decode(const ParamsDev& P, const kv_cache& c, const void* q, int B, int Hq,
-                        const int32_t* seq_lens, float scale, float* out, void* ws, const DecodeLayout& L,
-                        cudaStream_t s, int32_t* plan = nullptr);
+// (Z: virtual sequences of the view; q, out: [Z][Hq][D]; q_pos: [B] query positions for the rotary embedding, or
+// null.) plan != nullptr: fill plan[12] (see kv_debug_decode_plan) and launch nothing
+kv_status launch_decode(const ParamsDev& P, const CacheView& c, const void* q, int Z, int Hq,
+                        const int32_t* seq_lens, const int32_t* q_pos, float scale, float* out, void* ws,
+                        const DecodeLayout& L, cudaStream_t s, int32_t* plan = nullptr);
+// the dense view of a kv_cache (one layer, sets per head or per (sequence, head))
+CacheView dense_view(const kv_cache& c);
 // (dev: receives the current device, which holds the parameter table)
 kv_status check_decode_args(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
                             const int32_t* seq_lens_dev, float softmax_scale, const float* out, int* dev);
@@ -118,6 +160,7 @@ struct kv_params {
   std::vector<double> imp[2];      // [S][D] importances (storage order)
   std::vector<float> Tinv[2];      // [S][D][D] inverse of a non-orthogonal T (Tinv[k][j]: column j pairs with
                                    // storage channel j); empty: T is orthogonal and its inverse is T^T
+  double rope_base = 0.0;          // rotary embedding of the decode's queries (0: none)
   int device = -1;
   void* dev_blob = nullptr;
   size_t dev_bytes = 0;

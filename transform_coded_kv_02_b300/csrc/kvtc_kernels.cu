@@ -156,6 +156,7 @@ extern "C" kv_status kv_attend_decode_noalloc(const kv_params* p, const kv_cache
   }
   void* ws = nullptr;
   if ((st = kvtc::noalloc_scratch_address(dev, &ws)) != KV_OK) return st;
-  return kvtc::launch_decode(p->dev, *c, q, B, Hq, seq_lens_dev, softmax_scale, out, ws, L, (cudaStream_t)stream);
+  return kvtc::launch_decode(p->dev, kvtc::dense_view(*c), q, B, Hq, seq_lens_dev, nullptr, softmax_scale, out, ws,
+                             L, (cudaStream_t)stream);
 }
 

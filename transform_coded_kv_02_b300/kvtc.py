@@ -45,6 +45,12 @@ class kv_cache(ctypes.Structure):
                 ("per_seq_params", c_int)]
 
 
+class kv_paged_cache(ctypes.Structure):
+    _fields_ = [("k_pages", c_void_p), ("v_pages", c_void_p), ("n_pages", c_int64), ("page_tokens", c_int),
+                ("Hkv", c_int), ("B", c_int), ("n_layers", c_int), ("max_pages", c_int), ("block_table", c_void_p),
+                ("per_seq_params", c_int), ("first_layer", c_int)]
+
+
 def _sig(name, res, args):
     f = getattr(_lib, name)
     f.restype = res
@@ -58,6 +64,13 @@ _sig("kv_params_from_arrays", c_int, [c_int, c_int, _P, _P, _P, _P, c_int, _P, _
 _sig("kv_params_set_inverse", c_int, [_P, c_int, _P])
 _sig("kv_params_get_inverse", c_int, [_P, c_int, c_int, _P])
 _sig("kv_params_upload", c_int, [_P, _P])
+_sig("kv_params_set_rope", c_int, [_P, ctypes.c_double])
+_sig("kv_params_get_rope", ctypes.c_double, [_P])
+_sig("kv_paged_cache_bytes", c_size_t, [_P, c_int, c_int64, c_int, c_int])
+_sig("kv_encode_paged", c_int, [_P, ctypes.POINTER(kv_paged_cache), _P, _P, c_int, c_int64, _P, _P])
+_sig("kv_decode_paged_workspace_bytes", c_size_t, [_P, ctypes.POINTER(kv_paged_cache), c_int])
+_sig("kv_attend_decode_paged", c_int, [_P, ctypes.POINTER(kv_paged_cache), _P, c_int, _P, _P, c_float, _P, _P,
+                                       c_size_t, _P])
 _sig("kv_params_num_sets", c_int, [_P])
 _sig("kv_params_record_words", c_int, [_P, c_int])
 _sig("kv_params_info", c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P, _P])
@@ -178,6 +191,16 @@ class Params:
             _check("kv_params_set_inverse", _lib.kv_params_set_inverse(self.handle, tensor, _ptr(a)))
         return self
 
+    def set_rope(self, base):
+        """Rotary embedding of the decode's queries (pairs (i, i + d/2), angle pos * base^(-2i/d)); 0 removes it.
+        Takes effect at the next upload."""
+        _check("kv_params_set_rope", _lib.kv_params_set_rope(self.handle, float(base)))
+        return self
+
+    @property
+    def rope_base(self):
+        return _lib.kv_params_get_rope(self.handle)
+
     def info(self, set_idx, tensor, d=128):
         w = np.zeros(d, np.int32)
         ev = np.zeros(d, np.float64)
@@ -272,6 +295,38 @@ def kv_attend_decode_noalloc(params, cache, q, B, Hq, seq_lens, softmax_scale, o
     _check("kv_attend_decode_noalloc", _lib.kv_attend_decode_noalloc(params.handle, ctypes.byref(cache), _ptr(q), B,
                                                                      Hq, _ptr(seq_lens), softmax_scale, _ptr(out),
                                                                      _stream(stream)))
+
+
+def make_paged_cache(k_pages, v_pages, n_pages, page_tokens, Hkv, B, n_layers, max_pages, block_table,
+                     per_seq_params=False, first_layer=0):
+    """A paged view: pools [n_pages][Hkv][page_tokens][R] (values [n_pages][Hkv][page_tokens / 2][2 R]) and the
+    block table [n_layers * B][max_pages] (device int32)."""
+    return kv_paged_cache(_ptr(k_pages), _ptr(v_pages), n_pages, page_tokens, Hkv, B, n_layers, max_pages,
+                          _ptr(block_table), int(bool(per_seq_params)), first_layer)
+
+
+def kv_paged_cache_bytes(params, tensor, n_pages, page_tokens, Hkv):
+    return _lib.kv_paged_cache_bytes(params.handle, tensor, n_pages, page_tokens, Hkv)
+
+
+def kv_encode_paged(params, cache, k, v, dtype, t_new, dst_pos, stream=None):
+    """k, v: [n_layers][B][Hkv][t_new][d] device arrays; dst_pos: device int64 [B]."""
+    _check("kv_encode_paged", _lib.kv_encode_paged(params.handle, ctypes.byref(cache), _ptr(k), _ptr(v), dtype,
+                                                   t_new, _ptr(dst_pos), _stream(stream)))
+
+
+def kv_decode_paged_workspace_bytes(params, cache, Hq):
+    return _lib.kv_decode_paged_workspace_bytes(params.handle, ctypes.byref(cache), Hq)
+
+
+def kv_attend_decode_paged(params, cache, q, Hq, seq_lens, q_pos, softmax_scale, out, workspace, ws_bytes=None,
+                           stream=None):
+    """q: bf16 [n_layers][B][Hq][d]; out: fp32 likewise; seq_lens: int32 [B]; q_pos: int32 [B] (rotary embedding
+    of q in the kernel) or None."""
+    nbytes = ws_bytes if ws_bytes is not None else workspace.numel() * workspace.element_size()
+    _check("kv_attend_decode_paged", _lib.kv_attend_decode_paged(
+        params.handle, ctypes.byref(cache), _ptr(q), Hq, _ptr(seq_lens), None if q_pos is None else _ptr(q_pos),
+        softmax_scale, _ptr(out), _ptr(workspace), nbytes, _stream(stream)))
 
 
 def kv_decode_bf16_workspace_bytes(B, Hkv, Hq, T_cap):
