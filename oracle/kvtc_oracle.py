@@ -51,6 +51,13 @@ attention; IEEE fp32 for the quantiser, whose op sequence is part of the record 
     token is the same. Unused bits are 0.
  8. Decode attention over the records: y^_j = mu_j + sigma_j (z + (c_j + 1/2) s 2^-b_j) for b_j > 0, else
     mu_j; k^ = T^T y^ (and v^); o_h = softmax_t(alpha q_h . k^_t) v^ over t < seq_len, all in fp64.
+10. Token-axis allocation [RDKV, first abstract on the "SPHERICAL KV" page: per-token widths "from full precision
+    down to zero bits guided by reverse water-filling, applied once after the prefilling stage", each token's
+    weight taken from the distortion its compression induces on attention]: a token's weight is
+    lambda_t = sum_q p_qt^2 over observation queries q (a white error e on token t's value moves query q's output
+    by p_qt e); with one tier above zero bits (the token keeps its record, or is evicted), reverse water-filling
+    keeps the `keep` tokens of largest weight (ties: the earlier token); the kept records are compacted, in
+    order, into a sequence of their own.
  9. Serving layout [SPECTRA abstract: "longer contexts and larger batches"]: the query may arrive without its
     rotary position embedding, which the decode then applies first: pair (i, i + d/2) of q rotated by the angle
     pos * base^(-2i/d) (the half-split convention of the Llama models, no frequency rescaling), in fp64. Paged
@@ -664,4 +671,35 @@ def rotary_embed(x, pos: int, base: float):
     c, s = np.cos(ang), np.sin(ang)
     lo, hi = x[..., :half], x[..., half:]
     return np.concatenate([lo * c - hi * s, lo * s + hi * c], axis=-1)
+
+
+# ----------------------------------------------------------------------------------------------------
+# 10. token-axis allocation
+# ----------------------------------------------------------------------------------------------------
+def token_weights(q_obs, k, scale: float):
+    """Weight of each token of one KV head: lambda_t = sum_q p_qt^2 with p_q = softmax_t(scale q . k_t) over the
+    observation queries q_obs [n_q, d] of the head's query heads and the keys k [T, d], in fp64 -> [T]."""
+    q = np.asarray(q_obs, F64)
+    logits = scale * (q @ np.asarray(k, F64).T)
+    logits -= logits.max(axis=1, keepdims=True)
+    p = np.exp(logits)
+    p /= p.sum(axis=1, keepdims=True)
+    return (p * p).sum(axis=0)
+
+
+def token_keep(lam, keep: int):
+    """Reverse water-filling on the token axis with one tier above zero bits: each token keeps its whole record
+    or is evicted, and the water level leaves the `keep` tokens of largest weight (ties: the earlier token).
+    -> the kept tokens' indices, ascending."""
+    lam = np.asarray(lam, F64)
+    order = sorted(range(lam.shape[0]), key=lambda t: (-lam[t], t))
+    return np.array(sorted(order[:keep]), np.int64)
+
+
+def compact(rec, p: TensorParams, keep_idx):
+    """The records of the kept tokens keep_idx (ascending), in order, as a sequence of their own: one record per
+    token for keys, value tokens paired anew two per record."""
+    z, s, c = unpack(rec, p)
+    idx = np.asarray(keep_idx, np.int64)
+    return pack(z[idx], s[idx], c[idx], p)
 

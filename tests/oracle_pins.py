@@ -776,3 +776,69 @@ def pin_rotary_embedding():
     a1 = O.rotary_embed(x, 5000, 5e5) @ O.rotary_embed(k, 4000, 5e5)
     a2 = O.rotary_embed(x, 1000, 5e5) @ k
     assert np.allclose(a1, a2, atol=1e-10)
+
+
+# --- token-axis allocation --------------------------------------------------------------------------
+def pin_token_weights():
+    """Closed form: identical keys spread every query evenly, lambda_t = n_q / T^2. Bounds: each query's
+    probabilities sum to 1, so n_q / T <= sum_t lambda_t <= n_q. Meaning (Monte Carlo): white noise of variance
+    s2 added to token t's value alone moves the outputs by sum_q |delta o_q|^2 = s2 d lambda_t on average."""
+    rng = np.random.default_rng(21)
+    d, T, nq = 16, 9, 5
+    q = rng.standard_normal((nq, d))
+    k1 = np.tile(rng.standard_normal(d), (T, 1))
+    assert np.allclose(O.token_weights(q, k1, 0.5), nq / T ** 2, rtol=1e-12)
+    k = rng.standard_normal((T, d))
+    lam = O.token_weights(q, k, 0.7)
+    assert nq / T - 1e-12 <= lam.sum() <= nq + 1e-12
+    v = rng.standard_normal((T, d))
+    base = O.attention(q, k, v, 0.7)
+    s2, n = 0.01, 4000
+    for t in (0, 4):
+        acc = 0.0
+        for _ in range(n):
+            vp = v.copy()
+            vp[t] += np.sqrt(s2) * rng.standard_normal(d)
+            acc += np.sum((O.attention(q, k, vp, 0.7) - base) ** 2)
+        assert abs(acc / n - s2 * d * lam[t]) <= 0.08 * s2 * d * lam[t], (t, acc / n, s2 * d * lam[t])
+
+
+def pin_token_keep():
+    """Brute force on small token counts: the kept set is the subset of `keep` tokens with the largest total
+    weight, ties to the lexicographically earliest; and with one tier the library's reverse water-filling over
+    the token axis (widths 0 or 1, `keep` bits in all) keeps the same tokens."""
+    rng = np.random.default_rng(22)
+    for T in (1, 5, 8):
+        lam = rng.choice([1.0, 2.0, 2.0, 5.0, 9.0], size=T)  # repeated values: ties; integer sums are exact
+        for keep in range(T + 1):
+            best = None
+            for sub in itertools.combinations(range(T), keep):
+                key = (-sum(lam[list(sub)]), sub)
+                if best is None or key < best:
+                    best = key
+            got = O.token_keep(lam, keep)
+            assert tuple(got) == best[1], (T, keep, got, best)
+    for _ in range(20):
+        lam = rng.gamma(0.5, 1.0, size=40)
+        keep = int(rng.integers(1, 40))
+        w = O.water_fill_integer(lam, keep, 1)
+        assert tuple(np.nonzero(w)[0]) == tuple(O.token_keep(lam, keep))
+
+
+def pin_compact():
+    """Records are per token (keys) or per token half (values), so compacting encoded records equals encoding
+    the kept tokens; and decoding the compacted records is attention over the kept tokens alone."""
+    L = synth.make_layer(synth.WORKLOADS["tiny"], T=40, steps=1)
+    pk, pv = O.calibrate(L.calib_k[0], L.calib_v[0], L.calib_q[0], 2.75, 2.75)
+    k = synth.as_float(L.k[0, 0])
+    v = synth.as_float(L.v[0, 0])
+    for idx in ([0, 3, 4, 9, 20, 39], [1, 2, 5], [7], list(range(0, 40, 3))):
+        idx = np.array(idx)
+        assert np.array_equal(O.compact(O.encode(k, pk), pk, idx), O.encode(k[idx], pk))
+        assert np.array_equal(O.compact(O.encode(v, pv), pv, idx), O.encode(v[idx], pv))
+    q = synth.as_float(L.q[0, 0])
+    idx = np.array([2, 3, 11, 30])
+    rk, rv = O.compact(O.encode(k, pk), pk, idx), O.compact(O.encode(v, pv), pv, idx)
+    o = O.attend_decode(q, rk, rv, pk, pv, len(idx), 0.1)
+    ref = O.attention(q, O.reconstruct(O.encode(k[idx], pk), pk), O.reconstruct(O.encode(v[idx], pv), pv)[:4], 0.1)
+    assert np.allclose(o, ref, rtol=1e-12, atol=1e-12)

@@ -10,7 +10,8 @@ _orig = {name: getattr(O, name) for name in
          ["klt", "key_weights", "calib_statistics", "water_fill_continuous", "water_fill_integer",
           "quantize", "pack", "dequantize", "rotate", "reconstruct", "attention", "half_rn_sat",
           "slot_layout", "fit_layout", "token_slot_layout", "fit_token_layout", "storage_order", "attend_decode",
-          "exchange_rate", "joint_split", "attention_aware_key_basis", "whitened_key_transform", "rotary_embed"]}
+          "exchange_rate", "joint_split", "attention_aware_key_basis", "whitened_key_transform", "rotary_embed",
+          "token_weights", "token_keep", "compact"]}
 
 
 def _klt_transposed(sigma):
@@ -294,6 +295,28 @@ def _rope_frequency_halved(x, pos, base):
     return _orig["rotary_embed"](x, pos, np.sqrt(base))
 
 
+def _weights_first_power(q_obs, k, scale):
+    """sum_q p_qt instead of sum_q p_qt^2."""
+    q = np.asarray(q_obs, np.float64)
+    lg = scale * (q @ np.asarray(k, np.float64).T)
+    p = np.exp(lg - lg.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    return p.sum(axis=0) / np.sqrt(q.shape[0])
+
+
+def _keep_ties_to_later(lam, keep):
+    lam = np.asarray(lam, np.float64)
+    order = sorted(range(lam.shape[0]), key=lambda t: (-lam[t], -t))
+    return np.array(sorted(order[:keep]), np.int64)
+
+
+def _compact_keeps_pairs(rec, p, keep_idx):
+    """Copies whole value records (the kept token's partner comes along) instead of re-pairing tokens."""
+    if p.pairing == "channels":
+        return _orig["compact"](rec, p, keep_idx)
+    return np.asarray(rec)[np.asarray(keep_idx) // 2]
+
+
 MUTATIONS = [
     ("klt", _klt_transposed, P.pin_klt_known_spectrum),
     ("klt", _klt_no_sign_fix, P.pin_klt_known_spectrum),
@@ -329,6 +352,9 @@ MUTATIONS = [
     ("rotary_embed", _rope_interleaved, P.pin_rotary_embedding),
     ("rotary_embed", _rope_backwards, P.pin_rotary_embedding),
     ("rotary_embed", _rope_frequency_halved, P.pin_rotary_embedding),
+    ("token_weights", _weights_first_power, P.pin_token_weights),
+    ("token_keep", _keep_ties_to_later, P.pin_token_keep),
+    ("compact", _compact_keeps_pairs, P.pin_compact),
 ]
 
 

@@ -126,3 +126,15 @@ def test_whitened_key_transform():
 
 def test_rotary_embedding():
     P.pin_rotary_embedding()
+
+
+def test_token_weights():
+    P.pin_token_weights()
+
+
+def test_token_keep():
+    P.pin_token_keep()
+
+
+def test_compact():
+    P.pin_compact()
