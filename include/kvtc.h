@@ -306,6 +306,38 @@ kv_status kv_attend_decode_paged(const kv_params* p, const kv_paged_cache* cache
                                  const int32_t* seq_lens_dev, const int32_t* q_pos_dev, float softmax_scale,
                                  float* out, void* workspace, size_t ws_bytes, kv_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------------------
+ * Token-axis allocation, once after the prefill.  [RDKV, "SPHERICAL KV" page, first abstract: each token gets a
+ * width from full precision down to zero bits by reverse water-filling over weights taken from the distortion its
+ * compression induces on attention]
+ * A token's weight is lambda_t = sum_q p_qt^2 over the observation queries q of the KV head's g query heads
+ * (p_q = softmax_t(softmax_scale q . k_t) over the T prefill keys): a white error on token t's value moves query
+ * q's output by p_qt times it. With one tier above zero bits (the token keeps its whole record, or is evicted),
+ * reverse water-filling keeps the `keep` heaviest tokens of each (sequence, KV head). The kept records are then
+ * compacted in order into a cache of their own, over which kv_attend_decode runs with seq_len = keep (appends
+ * continue at position keep).
+ * ------------------------------------------------------------------------------------------------------ */
+/* Token weights. q_obs: device bf16 [B][Hq][W][d] observation queries (e.g. the last W prompt positions'
+ * queries, rotary-embedded); k: device bf16 [B][Hkv][T][d] prefill keys; weights: device fp32 [B][Hkv][T].
+ * Requires (Hq / Hkv) * W <= 128 and B * Hkv * T < 2^31. The contraction runs on the tensor cores (bf16 operands,
+ * fp32 accumulation); logits and weights in fp32. workspace: kv_token_weights_workspace_bytes(...) bytes,
+ * 16-byte aligned (no zero fill needed). */
+size_t kv_token_weights_workspace_bytes(int B, int Hkv, int64_t T);
+kv_status kv_token_weights(const void* q_obs, int W, const void* k, int B, int Hkv, int Hq, int64_t T,
+                           float softmax_scale, float* weights, void* workspace, size_t ws_bytes,
+                           kv_stream_t stream);
+/* The kept tokens: keep_idx (device int32 [B][Hkv][keep]) receives, for every (sequence, KV head), the indices of
+ * the keep tokens of largest weight in ascending order (equal weights: the earlier tokens kept; zero, negative
+ * and NaN weights rank lowest). weights: device fp32 [B][Hkv][T]; 0 <= keep <= T < 2^31. */
+kv_status kv_token_select(const float* weights, int B, int Hkv, int64_t T, int64_t keep, int32_t* keep_idx,
+                          kv_stream_t stream);
+/* Compaction: token i < keep of (b, h) in dst becomes token keep_idx[b][h][i] of src (records copied; value tokens
+ * re-paired two per record, a missing second token's halves 0). src and dst: distinct dense caches of this
+ * table's record lengths with the same Hkv; keep <= dst T_cap; indices outside src's T_cap are skipped and
+ * reported as KV_ERR_DEVICE. */
+kv_status kv_cache_compact(const kv_params* p, const kv_cache* src, const kv_cache* dst, int B,
+                           const int32_t* keep_idx, int64_t keep, kv_stream_t stream);
+
 /* Uncompressed bf16 split-K flash-decode over k, v: device bf16 [B][Hkv][T_cap][d]; same q, seq_lens,
  * out conventions. The measurement comparator for the packed path (no page counterpart beyond the
  * full-cache FlashAttention-2 decoding that RDKV compares against). workspace: device, at least

@@ -15,7 +15,8 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libkvtc.so")
 SOURCES = ["kvtc_host.cpp", "kvtc_kernels.cu", "kvtc_decode_part.cu"]
 HEADERS = ["kvtc_internal.h", "kvtc_ptx.cuh", "kvtc_codec.cuh", "kvtc_tc.cuh", "kvtc_encode.cuh",
-           "kvtc_encode_tc.cuh", "kvtc_decode.cuh", "kvtc_bf16.cuh", "kvtc_debug.cuh", "kvtc_launch.cuh"]
+           "kvtc_encode_tc.cuh", "kvtc_decode.cuh", "kvtc_bf16.cuh", "kvtc_debug.cuh", "kvtc_launch.cuh",
+           "kvtc_token.cuh"]
 DECODE_PARTS = 8  # kvtc_decode_part.cu is compiled once per part (the library's DECODE_PARTS)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

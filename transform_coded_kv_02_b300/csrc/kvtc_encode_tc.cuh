@@ -488,13 +488,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D bf16 matrix [rows][128] (256-byte rows), boxes of 128 rows x 64 columns, 128-byte swizzle, zero fill
-static bool make_bf16_map(CUtensorMap* m, const void* ptr, unsigned long long rows) {
+// 2-D bf16 matrix [rows][128] (256-byte rows), boxes of box_rows (at most 128 and at most rows) x 64 columns,
+// 128-byte swizzle, zero fill past the last row
+static bool make_bf16_map(CUtensorMap* m, const void* ptr, unsigned long long rows, unsigned box_rows = 128) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

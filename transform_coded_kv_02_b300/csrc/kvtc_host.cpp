@@ -1468,6 +1468,60 @@ extern "C" kv_status kv_attend_decode_paged(const kv_params* p, const kv_paged_c
                              workspace, L, (cudaStream_t)stream);
 }
 
+// ------------------------------------------------------------------------------------------------------
+// token-axis allocation
+// ------------------------------------------------------------------------------------------------------
+extern "C" size_t kv_token_weights_workspace_bytes(int B, int Hkv, int64_t T) {
+  if (B < 1 || Hkv < 1 || T < 1) return 0;
+  return kvtc::token_layout(B, Hkv, T).total;
+}
+
+extern "C" kv_status kv_token_weights(const void* q_obs, int W, const void* k, int B, int Hkv, int Hq, int64_t T,
+                                      float softmax_scale, float* weights, void* workspace, size_t ws_bytes,
+                                      kv_stream_t stream) {
+  clear_error();
+  KV_REQUIRE(q_obs && k && weights && workspace, KV_ERR_INVALID_ARG, "null q_obs, k, weights or workspace");
+  KV_REQUIRE(aligned16(q_obs) && aligned16(k) && aligned16(workspace), KV_ERR_INVALID_ARG,
+             "q_obs, k and workspace must be 16-byte aligned");
+  KV_REQUIRE(B >= 1 && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0 && W >= 1 && T >= 1, KV_ERR_INVALID_ARG,
+             "bad shape B=%d Hkv=%d Hq=%d W=%d T=%lld", B, Hkv, Hq, W, (long long)T);
+  KV_REQUIRE((Hq / Hkv) * W <= 128, KV_ERR_UNSUPPORTED, "(Hq / Hkv) * W = %d observation rows > 128", (Hq / Hkv) * W);
+  KV_REQUIRE((long long)B * Hkv * T < (1LL << 31) - 128 && (long long)B * Hq * W < (1LL << 31) - 128, KV_ERR_UNSUPPORTED,
+             "B * Hkv * T rows exceed the tensor maps' 32-bit coordinates");
+  KV_REQUIRE(std::isfinite(softmax_scale), KV_ERR_INVALID_ARG, "non-finite softmax scale");
+  const kvtc::TokenLayout L = kvtc::token_layout(B, Hkv, T);
+  KV_REQUIRE(ws_bytes >= L.total, KV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+  return kvtc::launch_token_weights(q_obs, W, k, B, Hkv, Hq, T, softmax_scale, weights, workspace,
+                                    (cudaStream_t)stream);
+}
+
+extern "C" kv_status kv_token_select(const float* weights, int B, int Hkv, int64_t T, int64_t keep,
+                                     int32_t* keep_idx, kv_stream_t stream) {
+  clear_error();
+  KV_REQUIRE(weights && keep_idx, KV_ERR_INVALID_ARG, "null weights or keep_idx");
+  KV_REQUIRE(B >= 1 && Hkv >= 1 && T >= 1 && T < (1LL << 31) && keep >= 0 && keep <= T, KV_ERR_INVALID_ARG,
+             "bad shape B=%d Hkv=%d T=%lld keep=%lld", B, Hkv, (long long)T, (long long)keep);
+  if (keep == 0) return KV_OK;
+  return kvtc::launch_token_select(weights, B, Hkv, T, keep, keep_idx, (cudaStream_t)stream);
+}
+
+extern "C" kv_status kv_cache_compact(const kv_params* p, const kv_cache* src, const kv_cache* dst, int B,
+                                      const int32_t* keep_idx, int64_t keep, kv_stream_t stream) {
+  clear_error();
+  kv_status st;
+  if ((st = check_params_on_device(p)) != KV_OK) return st;
+  if ((st = check_cache(p, src, B)) != KV_OK) return st;
+  if ((st = check_cache(p, dst, B)) != KV_OK) return st;
+  KV_REQUIRE(keep_idx, KV_ERR_INVALID_ARG, "null keep_idx");
+  KV_REQUIRE(src->Hkv == dst->Hkv, KV_ERR_INVALID_ARG, "source and destination KV heads differ");
+  KV_REQUIRE(src->k_rec != dst->k_rec && src->v_rec != dst->v_rec, KV_ERR_INVALID_ARG,
+             "compaction needs a destination distinct from its source");
+  KV_REQUIRE(keep >= 0 && keep <= dst->T_cap && keep <= src->T_cap, KV_ERR_INVALID_ARG,
+             "keep=%lld outside 0..T_cap", (long long)keep);
+  if (keep == 0) return KV_OK;
+  return kvtc::launch_compact(p->dev, *src, *dst, B, keep_idx, keep, (cudaStream_t)stream);
+}
+
 extern "C" kv_status kv_attend_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap,
                                            const void* q, const int32_t* seq_lens_dev, float softmax_scale,
                                            float* out, void* workspace, size_t ws_bytes, kv_stream_t stream) {

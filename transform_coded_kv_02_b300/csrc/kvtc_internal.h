@@ -128,6 +128,18 @@ CacheView dense_view(const kv_cache& c);
 // (dev: receives the current device, which holds the parameter table)
 kv_status check_decode_args(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
                             const int32_t* seq_lens_dev, float softmax_scale, const float* out, int* dev);
+// token-axis allocation: weights workspace (per-tile and merged softmax statistics of the observation queries)
+struct TokenLayout {
+  int nt;  // 128-token tiles per (sequence, KV head)
+  size_t off_stats, off_ml, total;
+};
+TokenLayout token_layout(int B, int Hkv, int64_t T);
+kv_status launch_token_weights(const void* q_obs, int W, const void* k, int B, int Hkv, int Hq, int64_t T,
+                               float scale, float* lam, void* ws, cudaStream_t s);
+kv_status launch_token_select(const float* lam, int B, int Hkv, int64_t T, int64_t keep, int32_t* idx,
+                              cudaStream_t s);
+kv_status launch_compact(const ParamsDev& P, const kv_cache& src, const kv_cache& dst, int B, const int32_t* idx,
+                         int64_t keep, cudaStream_t s);
 kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int Hq, int64_t T_cap,
                              const void* q, const int32_t* seq_lens, float scale, float* out, void* ws,
                              const DecodeLayout& L, cudaStream_t s);

@@ -9,6 +9,8 @@
 //                      every warp, split merge in a cluster or through the workspace) is compiled in the
 //                      kvtc_decode_part.cu units
 //  kvtc_bf16.cuh       decode_bf16_kernel: the same split-K structure over an uncompressed bf16 cache
+//  kvtc_token.cuh      token-axis allocation: token weights from the observation queries' attention (tcgen05),
+//                      the kept tokens per (sequence, KV head), record compaction
 //  kvtc_debug.cuh      parity and self-test kernels behind the kv_debug_* entry points
 //
 // Method sources: "KV Cache Compression Through the Lens of Transform Coding" (AATC), Key points;
@@ -103,6 +105,7 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 #include "kvtc_encode.cuh"
 #include "kvtc_decode.cuh"
 #include "kvtc_bf16.cuh"
+#include "kvtc_token.cuh"
 #include "kvtc_debug.cuh"
 
 namespace kvtc {

@@ -1,0 +1,363 @@
+// Token-axis allocation on the device: token weights from the attention of observation queries, the tokens each
+// (sequence, KV head) keeps, and the compaction of their records. Part of kvtc_kernels.cu's translation unit.
+//
+// Method: RDKV ("SPHERICAL KV ..." page, first abstract): each token gets a width from full precision down to
+// zero bits by reverse water-filling over weights taken from the distortion its compression induces on attention,
+// once after the prefill. Here a token's weight is lambda_t = sum_q p_qt^2 over the observation queries q of the
+// KV head's query heads (a white error e on token t's value moves query q's output by p_qt e), and the tier above
+// zero bits is the token's whole record: reverse water-filling with one tier keeps the `keep` heaviest tokens
+// (ties: the earlier token) and evicts the rest. The decode then runs unchanged over the compacted records.
+//
+//   token_logits_kernel<0|1>  one CTA per (128-token tile, KV head, sequence): the g x W observation queries
+//                             (M = 128 rows, zero rows past g W) and the tile's keys arrive by TMA; one thread
+//                             issues 8 tcgen05 MMAs (K = 16 each) into 128 tensor-memory columns; thread = query
+//                             row reads its 128 logits. Pass 0 leaves each row's tile maximum and sum of
+//                             2^(x - max); pass 1 forms p = 2^(x - M) / L and sums p^2 over the rows (a transpose
+//                             through shared memory) into the tile's token weights.
+//   token_merge_kernel        per (sequence, KV head) and query row: M and L over the tiles.
+//   token_select_kernel       per (sequence, KV head): radix select of the keep-th largest weight (8 bits per
+//                             round over the weights' IEEE bits), then the kept tokens in index order by block
+//                             scans (equal weights at the threshold: the earlier tokens).
+//   compact_*_kernel          the kept records copied in order; value tokens re-paired two per record.
+#pragma once
+
+#include "kvtc_tc.cuh"
+
+namespace kvtc {
+
+constexpr int TK_TILE = 128;        // keys per CTA and query rows per MMA
+constexpr int SEL_THREADS = 1024;
+
+struct TokArgs {
+  float2* stats;   // [B*Hkv][nt][128]: per tile and query row, (max, sum of 2^(x - max)) over the tile's tokens
+  float2* ml;      // [B*Hkv][128]:     (M, L) over all tiles
+  float* lam;      // [B*Hkv][T]:       token weights
+  long long T;
+  int Hkv, Hq, W, g, nq, nt;
+  int qbox, kbox;    // rows of the query and key boxes: 128, or all rows of a smaller tensor (the operand rows past
+                     // them are stale and masked)
+  float scale_log2;  // softmax scale * log2(e): logits in base 2
+  long long wait_ns;
+};
+
+template <int PASS>
+__global__ void __launch_bounds__(TK_TILE, 1)
+    token_logits_kernel(TokArgs a, const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full, done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_ok;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  // pass 1: p^2 [128 rows][128 tokens] (column index XOR-swizzled by the row), over the consumed operands
+  float* const tr = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
+  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = b * a.Hkv + h;
+  const long long t0 = (long long)tile * TK_TILE;
+  const int ntok = (int)min((long long)TK_TILE, a.T - t0);
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&s_tmem), 128);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&full), 1);
+    mbar_init(smem_u32(&done), 1);
+    fence_mbar_init();
+    s_ok = 1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  if (tid == 0) {
+    const uint32_t fb = smem_u32(&full), db = smem_u32(&done);
+    const int qrow = (b * a.Hq + h * a.g) * a.W;         // the g x W observation queries of this KV head
+    const int krow = (int)((long long)bh * a.T + t0);    // the tile's keys (rows past the head's T are masked)
+    mbar_expect_tx(fb, (uint32_t)(a.qbox + a.kbox) * 256u);
+    tma_load_2d(base, &mq, 0, qrow, fb);
+    tma_load_2d(base + TC_BOX_BYTES, &mq, 64, qrow, fb);
+    tma_load_2d(base + 2 * TC_BOX_BYTES, &mk, 0, krow, fb);
+    tma_load_2d(base + 3 * TC_BOX_BYTES, &mk, 64, krow, fb);
+    if (mbar_wait_bounded(fb, 0u, a.wait_ns)) {
+      tc_fence_after();
+      constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t koff = (uint32_t)(kk >> 2) * TC_BOX_BYTES + (uint32_t)(kk & 3) * 32u;
+        tc_mma_bf16(tmem, smem_desc_k128(base + koff), smem_desc_k128(base + 2 * TC_BOX_BYTES + koff), IDESC,
+                    kk ? 1u : 0u);
+      }
+      tc_commit(db);
+    } else {
+      s_ok = 0;
+      mbar_wait_bounded(fb, 0u, a.wait_ns);  // the copies may still land: wait again before the CTA can exit
+      mbar_arrive(db);
+    }
+  }
+  const bool got = mbar_wait_bounded(smem_u32(&done), 0u, a.wait_ns);
+  const bool ok = __syncthreads_and(got) && s_ok;
+  tc_fence_after();
+  const int r = 32 * warp + lane;  // query row = tensor-memory lane
+  const bool rv = ok && r < a.nq;
+  float x[TK_TILE];  // row r's logits (base 2) against the tile's tokens
+#pragma unroll
+  for (int c = 0; c < TK_TILE; c += 32) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[c + j] = __uint_as_float(v[j]) * a.scale_log2;
+  }
+  if constexpr (PASS == 0) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < TK_TILE; ++c)
+      if (c < ntok) m = fmaxf(m, x[c]);
+    float l = 0.f;
+#pragma unroll
+    for (int c = 0; c < TK_TILE; ++c)
+      if (c < ntok) l += exp2f(x[c] - m);
+    a.stats[((size_t)bh * a.nt + tile) * TK_TILE + r] = rv ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
+  } else {
+    const float2 ML = a.ml[(size_t)bh * TK_TILE + r];
+    const float inv = rv && ML.y > 0.f ? 1.f / ML.y : 0.f;
+#pragma unroll
+    for (int c = 0; c < TK_TILE; ++c) {
+      const float p = (inv > 0.f && c < ntok) ? exp2f(x[c] - ML.x) * inv : 0.f;
+      tr[r * TK_TILE + (c ^ (r & 31))] = p * p;
+    }
+    __syncthreads();
+    if (tid < ntok) {
+      float s = 0.f;
+      for (int rr = 0; rr < TK_TILE; ++rr) s += tr[rr * TK_TILE + (tid ^ (rr & 31))];
+      a.lam[(size_t)bh * a.T + t0 + tid] = s;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// per (sequence, KV head): (M, L) of every query row over the tiles
+__global__ void __launch_bounds__(TK_TILE) token_merge_kernel(TokArgs a) {
+  const int bh = blockIdx.x, r = threadIdx.x;
+  const float2* st = a.stats + (size_t)bh * a.nt * TK_TILE + r;
+  float M = -INFINITY;
+  for (int t = 0; t < a.nt; ++t) M = fmaxf(M, st[(size_t)t * TK_TILE].x);
+  float L = 0.f;
+  for (int t = 0; t < a.nt; ++t) {
+    const float2 s = st[(size_t)t * TK_TILE];
+    if (s.x != -INFINITY) L += s.y * exp2f(s.x - M);
+  }
+  a.ml[(size_t)bh * TK_TILE + r] = make_float2(M, L);
+}
+
+// Exclusive count of the set flags before this thread in the block, and the block's total (every thread).
+__device__ __forceinline__ unsigned block_excl_count(bool f, unsigned* wsum, unsigned& total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __syncthreads();  // the previous call's readers are done with wsum
+  const unsigned bal = __ballot_sync(0xffffffffu, f);
+  if (lane == 0) wsum[warp] = __popc(bal);
+  __syncthreads();
+  if (warp == 0) {
+    unsigned v = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    wsum[lane] = v;  // inclusive over the warps
+  }
+  __syncthreads();
+  total = wsum[31];
+  return (warp ? wsum[warp - 1] : 0u) + __popc(bal & ((1u << lane) - 1u));
+}
+
+// Per (sequence, KV head): the keep tokens of largest weight, ascending. A weight's rank key is its IEEE bit pattern
+// (monotone for non-negative floats); zero, negative and NaN weights rank lowest.
+__global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* lam, long long T, int keep, int32_t* idx) {
+  __shared__ unsigned hist[256];
+  __shared__ unsigned wsum[32];
+  __shared__ unsigned s_prefix, s_remaining;
+  const int bh = blockIdx.x, tid = threadIdx.x;
+  const float* lm = lam + (size_t)bh * T;
+  int32_t* out = idx + (size_t)bh * keep;
+  auto key_of = [&](long long t) {
+    const float v = lm[t];
+    return v > 0.f ? __float_as_uint(v) : 0u;
+  };
+  // radix select of the keep-th largest key, eight bits per round
+  unsigned prefix = 0u, mask = 0u, remaining = (unsigned)keep;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += SEL_THREADS) hist[i] = 0u;
+    __syncthreads();
+    for (long long t = tid; t < T; t += SEL_THREADS) {
+      const unsigned k = key_of(t);
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned cum = 0u;
+      int d = 255;
+      for (; d > 0; --d) {
+        if (cum + hist[d] >= remaining) break;
+        cum += hist[d];
+      }
+      s_prefix = prefix | ((unsigned)d << shift);
+      s_remaining = remaining - cum;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    remaining = s_remaining;
+    mask |= 255u << shift;
+  }
+  // prefix: the threshold key; every larger key is kept, and the first `remaining` keys equal to it
+  unsigned kept = 0u, eq_seen = 0u;
+  for (long long c0 = 0; c0 < T; c0 += SEL_THREADS) {
+    const long long t = c0 + tid;
+    const unsigned k = t < T ? key_of(t) : 0u;
+    const bool gt = t < T && k > prefix, eq = t < T && k == prefix;
+    unsigned n_eq, n_sel;
+    const unsigned eq_rank = eq_seen + block_excl_count(eq, wsum, n_eq);
+    const bool sel = gt || (eq && eq_rank < remaining);
+    const unsigned pos = kept + block_excl_count(sel, wsum, n_sel);
+    if (sel && pos < (unsigned)keep) out[pos] = (int32_t)t;
+    kept += n_sel;
+    eq_seen += n_eq;
+  }
+}
+
+struct CompactArgs {
+  const uint32_t* src[2];
+  uint32_t* dst[2];
+  const int32_t* idx;  // [BH][keep]
+  long long Ts, Td;    // token capacities of the source and destination caches
+  int keep, Rk, Rv, BH;
+};
+
+// keys: thread per (sequence-head, kept token, record word)
+__global__ void compact_keys_kernel(CompactArgs a) {
+  const long long per = (long long)a.keep * a.Rk;
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= (long long)a.BH * per) return;
+  const int bh = (int)(g / per);
+  const long long r = g - (long long)bh * per;
+  const int i = (int)(r / a.Rk), w = (int)(r - (long long)i * a.Rk);
+  const int t = a.idx[(size_t)bh * a.keep + i];
+  if (t < 0 || t >= a.Ts) {
+    atomicOr(&g_status, ST_BAD_INDEX);
+    return;
+  }
+  a.dst[0][((size_t)bh * a.Td + i) * a.Rk + w] = a.src[0][((size_t)bh * a.Ts + t) * a.Rk + w];
+}
+
+// values: thread per (sequence-head, destination record, record word); kept tokens 2j and 2j + 1 form record j, each
+// bringing its z/s word and its 16-bit half of every code word from the record that held it
+__global__ void compact_values_kernel(CompactArgs a) {
+  const int W = 2 * a.Rv, nrec = (a.keep + 1) / 2;
+  const long long per = (long long)nrec * W;
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= (long long)a.BH * per) return;
+  const int bh = (int)(g / per);
+  const long long r = g - (long long)bh * per;
+  const int j = (int)(r / W), w = (int)(r - (long long)j * W);
+  const int32_t* id = a.idx + (size_t)bh * a.keep;
+  const int t0 = id[2 * j], t1 = 2 * j + 1 < a.keep ? id[2 * j + 1] : -1;
+  if (t0 < 0 || t0 >= a.Ts || (2 * j + 1 < a.keep && (t1 < 0 || t1 >= a.Ts))) {
+    atomicOr(&g_status, ST_BAD_INDEX);
+    return;
+  }
+  auto src_word = [&](int t, int word) {
+    return a.src[1][((size_t)bh * (a.Ts / 2) + (size_t)(t >> 1)) * W + word];
+  };
+  uint32_t v;
+  if (w < 2) {
+    v = w == 0 ? src_word(t0, t0 & 1) : (t1 >= 0 ? src_word(t1, t1 & 1) : 0u);
+  } else {
+    const uint32_t lo = (src_word(t0, w) >> (16 * (t0 & 1))) & 0xFFFFu;
+    const uint32_t hi = t1 >= 0 ? (src_word(t1, w) >> (16 * (t1 & 1))) & 0xFFFFu : 0u;
+    v = lo | (hi << 16);
+  }
+  a.dst[1][((size_t)bh * (a.Td / 2) + (size_t)j) * W + w] = v;
+}
+
+// ---- host side --------------------------------------------------------------------------------------------
+TokenLayout token_layout(int B, int Hkv, int64_t T) {
+  TokenLayout L{};
+  L.nt = (int)((T + TK_TILE - 1) / TK_TILE);
+  const size_t bh = (size_t)B * Hkv;
+  L.off_stats = 0;
+  L.off_ml = align256(bh * L.nt * TK_TILE * sizeof(float2));
+  L.total = align256(L.off_ml + bh * TK_TILE * sizeof(float2));
+  return L;
+}
+
+kv_status launch_token_weights(const void* q_obs, int W, const void* k, int B, int Hkv, int Hq, int64_t T,
+                               float scale, float* lam, void* ws, cudaStream_t s) {
+  const TokenLayout L = token_layout(B, Hkv, T);
+  CUtensorMap maps[2];
+  const unsigned long long qrows = (unsigned long long)B * Hq * W, krows = (unsigned long long)B * Hkv * T;
+  const unsigned qbox = (unsigned)std::min<unsigned long long>(128, qrows);
+  const unsigned kbox = (unsigned)std::min<unsigned long long>(128, krows);
+  if (!make_bf16_map(&maps[0], q_obs, qrows, qbox) || !make_bf16_map(&maps[1], k, krows, kbox)) {
+    set_error("token weights: tensor map encoding failed");
+    return KV_ERR_CUDA;
+  }
+  TokArgs a;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.stats = reinterpret_cast<float2*>(w + L.off_stats);
+  a.ml = reinterpret_cast<float2*>(w + L.off_ml);
+  a.lam = lam;
+  a.T = T;
+  a.Hkv = Hkv;
+  a.Hq = Hq;
+  a.W = W;
+  a.g = Hq / Hkv;
+  a.nq = a.g * W;
+  a.nt = L.nt;
+  a.qbox = (int)qbox;
+  a.kbox = (int)kbox;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_ns = g_wait_limit_ns;
+  const uint32_t smem = 1024 + 4 * TC_BOX_BYTES;
+  const dim3 grid((unsigned)L.nt, (unsigned)Hkv, (unsigned)B);
+  cudaError_t e = ensure_dyn_smem((const void*)token_logits_kernel<0>, smem);
+  if (e == cudaSuccess) e = ensure_dyn_smem((const void*)token_logits_kernel<1>, smem);
+  if (e != cudaSuccess) {
+    set_error("token_logits_kernel shared memory: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
+  }
+  token_logits_kernel<0><<<grid, TK_TILE, smem, s>>>(a, maps[0], maps[1]);
+  token_merge_kernel<<<B * Hkv, TK_TILE, 0, s>>>(a);
+  token_logits_kernel<1><<<grid, TK_TILE, smem, s>>>(a, maps[0], maps[1]);
+  return launch_check("token weight kernels");
+}
+
+kv_status launch_token_select(const float* lam, int B, int Hkv, int64_t T, int64_t keep, int32_t* idx,
+                              cudaStream_t s) {
+  token_select_kernel<<<B * Hkv, SEL_THREADS, 0, s>>>(lam, T, (int)keep, idx);
+  return launch_check("token_select_kernel");
+}
+
+kv_status launch_compact(const ParamsDev& P, const kv_cache& src, const kv_cache& dst, int B, const int32_t* idx,
+                         int64_t keep, cudaStream_t s) {
+  CompactArgs a;
+  a.src[0] = src.k_rec;
+  a.src[1] = src.v_rec;
+  a.dst[0] = dst.k_rec;
+  a.dst[1] = dst.v_rec;
+  a.idx = idx;
+  a.Ts = src.T_cap;
+  a.Td = dst.T_cap;
+  a.keep = (int)keep;
+  a.Rk = P.t[0].r_words;
+  a.Rv = P.t[1].r_words;
+  a.BH = B * src.Hkv;
+  const long long nk = (long long)a.BH * keep * a.Rk, nv = (long long)a.BH * ((keep + 1) / 2) * 2 * a.Rv;
+  compact_keys_kernel<<<(unsigned)((nk + 255) / 256), 256, 0, s>>>(a);
+  compact_values_kernel<<<(unsigned)((nv + 255) / 256), 256, 0, s>>>(a);
+  return launch_check("compact kernels");
+}
+
+}  // namespace kvtc

@@ -82,6 +82,10 @@ _sig("kv_encode", c_int, [_P, ctypes.POINTER(kv_cache), _P, _P, c_int, c_int, c_
 _sig("kv_decode_workspace_bytes", c_size_t, [_P, c_int, c_int, c_int, c_int64])
 _sig("kv_attend_decode", c_int, [_P, ctypes.POINTER(kv_cache), _P, c_int, c_int, _P, c_float, _P, _P, c_size_t, _P])
 _sig("kv_attend_decode_noalloc", c_int, [_P, ctypes.POINTER(kv_cache), _P, c_int, c_int, _P, c_float, _P, _P])
+_sig("kv_token_weights_workspace_bytes", c_size_t, [c_int, c_int, c_int64])
+_sig("kv_token_weights", c_int, [_P, c_int, _P, c_int, c_int, c_int, c_int64, c_float, _P, _P, c_size_t, _P])
+_sig("kv_token_select", c_int, [_P, c_int, c_int, c_int64, c_int64, _P, _P])
+_sig("kv_cache_compact", c_int, [_P, ctypes.POINTER(kv_cache), ctypes.POINTER(kv_cache), c_int, _P, c_int64, _P])
 _sig("kv_decode_bf16_workspace_bytes", c_size_t, [c_int, c_int, c_int, c_int64])
 _sig("kv_attend_decode_bf16", c_int, [_P, _P, c_int, c_int, c_int, c_int64, _P, _P, c_float, _P, _P, c_size_t, _P])
 _sig("kv_check_status", c_int, [_P])
@@ -327,6 +331,27 @@ def kv_attend_decode_paged(params, cache, q, Hq, seq_lens, q_pos, softmax_scale,
     _check("kv_attend_decode_paged", _lib.kv_attend_decode_paged(
         params.handle, ctypes.byref(cache), _ptr(q), Hq, _ptr(seq_lens), None if q_pos is None else _ptr(q_pos),
         softmax_scale, _ptr(out), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def kv_token_weights_workspace_bytes(B, Hkv, T):
+    return _lib.kv_token_weights_workspace_bytes(B, Hkv, T)
+
+
+def kv_token_weights(q_obs, W, k, B, Hkv, Hq, T, softmax_scale, weights, workspace, ws_bytes=None, stream=None):
+    """q_obs: bf16 [B][Hq][W][d]; k: bf16 [B][Hkv][T][d]; weights: fp32 [B][Hkv][T] (device arrays)."""
+    nbytes = ws_bytes if ws_bytes is not None else workspace.numel() * workspace.element_size()
+    _check("kv_token_weights", _lib.kv_token_weights(_ptr(q_obs), W, _ptr(k), B, Hkv, Hq, T, softmax_scale,
+                                                     _ptr(weights), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def kv_token_select(weights, B, Hkv, T, keep, keep_idx, stream=None):
+    """keep_idx: int32 [B][Hkv][keep] (device) receives the kept tokens' indices, ascending."""
+    _check("kv_token_select", _lib.kv_token_select(_ptr(weights), B, Hkv, T, keep, _ptr(keep_idx), _stream(stream)))
+
+
+def kv_cache_compact(params, src, dst, B, keep_idx, keep, stream=None):
+    _check("kv_cache_compact", _lib.kv_cache_compact(params.handle, ctypes.byref(src), ctypes.byref(dst), B,
+                                                     _ptr(keep_idx), keep, _stream(stream)))
 
 
 def kv_decode_bf16_workspace_bytes(B, Hkv, Hq, T_cap):
