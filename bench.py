@@ -12,8 +12,10 @@ Prints one JSON line. value = algorithmic bytes of a step (packed K/V records re
 appended token in and records out) / device time of the step, in GB/s; L2 is flushed (a 2 x L2 buffer is
 written) before every timed step and the flush is outside the timed events. The line's "workloads" object
 holds the other workloads, measured the same way: the 131072-token layer at 1.33 bits, the Qwen2.5-7B-shaped
-batch at 2, 3 and 4 bits, and the 32-layer prefill stack (encode throughput, calibration time, one decode per
-layer). --impl reference times the CPU oracle (test infrastructure) on full steps of the headline workload,
+batch at 2, 3 and 4 bits, the 32-layer prefill stack (encode throughput, calibration time, one decode per
+layer), the headline layer in 256-token pages (one layer, and four layers in one launch, with the query's rotary
+embedding in the kernel), and the token-axis allocation on the headline layer (token weights, kept tokens, record
+compaction, decode at the retained length). --impl reference times the CPU oracle (test infrastructure) on full steps of the headline workload,
 its KV heads spread over spawned processes.
 """
 from __future__ import annotations
@@ -630,6 +632,118 @@ def prefill_stack(gpu, peak):
             "decode_per_layer_us": float(np.mean(dec_t)) * 1e6}
 
 
+def paged_workload(gpu, w, L, peak, page=256, n_layers=4, rope_base=500000.0):
+    """The headline layer's prefill in pages of `page` tokens scattered over the pool, the query's rotary embedding
+    applied in the decode kernel; decode calls of one layer and of n_layers layers in one launch (the layer's
+    records and parameters repeated per layer), graph replays with L2 flushed before each."""
+    from transform_coded_kv_02_b300 import kvtc
+    torch, dev = gpu.torch, gpu.dev
+    B, Hkv, Hq, d, T = w.B, w.Hkv, w.Hq, w.d, w.T
+    P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)) * n_layers, BITS, BITS)
+    P.set_rope(rope_base).upload()
+    rk_w, rv_w = P.record_words(0), P.record_words(1)
+    max_pages = (T + page - 1) // page
+    Z = n_layers * B
+    n_pages = Z * max_pages
+    bt_np = np.random.default_rng(7).permutation(n_pages).astype(np.int32).reshape(Z, max_pages)
+    bt = torch.from_numpy(bt_np).to(dev)
+    kp = torch.zeros((n_pages, Hkv, page, rk_w), dtype=torch.int32, device=dev)
+    vp = torch.zeros((n_pages, Hkv, page // 2, 2 * rv_w), dtype=torch.int32, device=dev)
+    k = bf16_tensor(L.k[:, :, :T], dev)
+    v = bf16_tensor(L.v[:, :, :T], dev)
+    kl = k.unsqueeze(0).expand(n_layers, *k.shape).contiguous()
+    vl = v.unsqueeze(0).expand(n_layers, *v.shape).contiguous()
+    c_all = kvtc.make_paged_cache(kp, vp, n_pages, page, Hkv, B, n_layers, max_pages, bt, False, 0)
+    kvtc.kv_encode_paged(P, c_all, kl, vl, kvtc.KV_DTYPE_BF16, T, torch.zeros(B, dtype=torch.int64, device=dev))
+    del kl, vl
+    c_one = kvtc.make_paged_cache(kp, vp, n_pages, page, Hkv, B, 1, max_pages, bt, False, 0)
+    q = bf16_tensor(L.q[0], dev)
+    ql = q.unsqueeze(0).expand(n_layers, *q.shape).contiguous()
+    seq = torch.full((B,), T, dtype=torch.int32, device=dev)
+    qpos = torch.full((B,), T - 1, dtype=torch.int32, device=dev)
+    out = torch.zeros((n_layers, B, Hq, d), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(d)
+    ws1 = torch.zeros(kvtc.kv_decode_paged_workspace_bytes(P, c_one, Hq), dtype=torch.uint8, device=dev)
+    wsn = torch.zeros(kvtc.kv_decode_paged_workspace_bytes(P, c_all, Hq), dtype=torch.uint8, device=dev)
+    g1 = gpu.graph(lambda: kvtc.kv_attend_decode_paged(P, c_one, ql[0], Hq, seq, qpos, scale, out[0], ws1))
+    gn = gpu.graph(lambda: kvtc.kv_attend_decode_paged(P, c_all, ql, Hq, seq, qpos, scale, out, wsn))
+    torch.cuda.synchronize()
+    gpu.timed([[g1.replay], [gn.replay]])
+    t1 = gpu.timed([[g1.replay] for _ in range(24)])[:, 0]
+    tn = gpu.timed([[gn.replay] for _ in range(24)])[:, 0]
+    assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
+    assert bool(torch.isfinite(out).all())
+    lb = decode_bytes(T, w, rk_w, rv_w)
+    a1, an = float(np.mean(t1)), float(np.mean(tn))
+    del g1, gn
+    return {"workload": f"{workload_name(w, BITS, rk_w, rv_w, steps=False)}, {page}-token pages in random pool order, "
+                        f"query rotary embedding (base {rope_base:g}) in the kernel",
+            "decode_one_layer": {"avg_us": a1 * 1e6, "gbs": lb / a1 / 1e9, "frac": lb / a1 / 1e9 / peak},
+            f"decode_{n_layers}_layers_one_launch": {"avg_us": an * 1e6, "gbs": n_layers * lb / an / 1e9,
+                                                    "frac": n_layers * lb / an / 1e9 / peak,
+                                                    "us_per_layer": an / n_layers * 1e6},
+            "algorithmic_bytes_per_layer": lb}
+
+
+def token_axis_workload(gpu, w, L, peak, full_decode_us, W=32, keep_frac=0.25):
+    """Token-axis allocation on the headline layer after its prefill: token weights from W observation queries per
+    query head (two tensor-core passes over the bf16 keys), the kept tokens (keep_frac of the context), record
+    compaction, then the decode over the kept tokens; each call timed on its own (graph replays, L2 flushed)."""
+    from transform_coded_kv_02_b300 import kvtc
+    torch, dev = gpu.torch, gpu.dev
+    B, Hkv, Hq, d, T = w.B, w.Hkv, w.Hq, w.d, w.T
+    W = min(W, L.q.shape[0], 128 // (Hq // Hkv))
+    P = kvtc.kv_calibrate(list(zip(L.calib_k, L.calib_v, L.calib_q)), BITS, BITS).upload()
+    rk_w, rv_w = P.record_words(0), P.record_words(1)
+    T_cap = (T + 15) // 16 * 16
+    k = bf16_tensor(L.k[:, :, :T], dev)
+    v = bf16_tensor(L.v[:, :, :T], dev)
+    q_obs = bf16_tensor(np.ascontiguousarray(np.transpose(L.q[:W], (1, 2, 0, 3))), dev)
+    rk = torch.zeros((B, Hkv, T_cap, rk_w), dtype=torch.int32, device=dev)
+    rv = torch.zeros((B, Hkv, T_cap // 2, 2 * rv_w), dtype=torch.int32, device=dev)
+    src = kvtc.make_cache(rk, rv, B, Hkv, T_cap)
+    kvtc.kv_encode(P, src, k, v, kvtc.KV_DTYPE_BF16, B, T, torch.zeros(B, dtype=torch.int64, device=dev))
+    keep = int(keep_frac * T)
+    lam = torch.zeros((B, Hkv, T), dtype=torch.float32, device=dev)
+    wsw = torch.empty(kvtc.kv_token_weights_workspace_bytes(B, Hkv, T), dtype=torch.uint8, device=dev)
+    idx = torch.zeros((B, Hkv, keep), dtype=torch.int32, device=dev)
+    ck = torch.zeros((B, Hkv, T_cap, rk_w), dtype=torch.int32, device=dev)
+    cv = torch.zeros((B, Hkv, T_cap // 2, 2 * rv_w), dtype=torch.int32, device=dev)
+    dst = kvtc.make_cache(ck, cv, B, Hkv, T_cap)
+    scale = 1.0 / math.sqrt(d)
+    q = bf16_tensor(L.q[W % L.q.shape[0]], dev)
+    seq = torch.full((B,), keep, dtype=torch.int32, device=dev)
+    out = torch.zeros((B, Hq, d), dtype=torch.float32, device=dev)
+    wsd = torch.zeros(kvtc.kv_decode_workspace_bytes(P, B, Hkv, Hq, T_cap), dtype=torch.uint8, device=dev)
+    calls = {"weights": lambda: kvtc.kv_token_weights(q_obs, W, k, B, Hkv, Hq, T, scale, lam, wsw),
+             "select": lambda: kvtc.kv_token_select(lam, B, Hkv, T, keep, idx),
+             "compact": lambda: kvtc.kv_cache_compact(P, src, dst, B, idx, keep),
+             "decode": lambda: kvtc.kv_attend_decode(P, dst, q, B, Hq, seq, scale, out, wsd)}
+    graphs = {n: gpu.graph(f) for n, f in calls.items()}
+    torch.cuda.synchronize()
+    order = ["weights", "select", "compact", "decode"]
+    gpu.timed([[graphs[n].replay for n in order]])
+    t = gpu.timed([[graphs[n].replay for n in order] for _ in range(12)])
+    assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
+    assert bool(torch.isfinite(out).all())
+    avg = {n: float(np.mean(t[:, i])) for i, n in enumerate(order)}
+    bh = B * Hkv
+    w_bytes = 2 * bh * T * d * 2 + B * Hq * W * d * 2 + bh * T * 4          # keys read twice, queries, weights out
+    s_bytes = 5 * bh * T * 4 + bh * keep * 4                                  # 4 radix rounds and the output pass
+    c_bytes = 2 * bh * keep * (rk_w + rv_w) * 4 + bh * keep * 4               # kept records in and out, indices
+    d_bytes = decode_bytes(keep, w, rk_w, rv_w)
+    del graphs
+    return {"workload": f"{workload_name(w, BITS, rk_w, rv_w, steps=False)}: {W} observation queries per query "
+                        f"head, {keep} of {T} tokens kept per KV head ({keep_frac:g})",
+            "token_weights": {"avg_us": avg["weights"] * 1e6, "gbs": w_bytes / avg["weights"] / 1e9,
+                              "bound": "hbm (keys read in each of two passes)"},
+            "token_select": {"avg_us": avg["select"] * 1e6, "gbs": s_bytes / avg["select"] / 1e9},
+            "compact": {"avg_us": avg["compact"] * 1e6, "gbs": c_bytes / avg["compact"] / 1e9},
+            "decode_kept": {"avg_us": avg["decode"] * 1e6, "gbs": d_bytes / avg["decode"] / 1e9,
+                            "frac": d_bytes / avg["decode"] / 1e9 / peak,
+                            "speedup_vs_full_context": full_decode_us / (avg["decode"] * 1e6)}}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -705,6 +819,8 @@ def run_ours(args, rank, world, local_rank):
             workloads[f"{name}@{bits}"] = decode_workload(gpu, name, bits, held[name], 28, peak)
         del held
         workloads["llama_prefill_32l@2.75"] = prefill_stack(gpu, peak)
+        workloads["llama_decode_32k_paged@2.75"] = paged_workload(gpu, w, L, peak)
+        workloads["llama_decode_32k_token_axis@2.75"] = token_axis_workload(gpu, w, L, peak, dec_avg * 1e6)
 
     if rank != 0:
         return

@@ -16,8 +16,9 @@
 //                             through shared memory) into the tile's token weights.
 //   token_merge_kernel        per (sequence, KV head) and query row: M and L over the tiles.
 //   token_select_kernel       per (sequence, KV head): radix select of the keep-th largest weight (8 bits per
-//                             round over the weights' IEEE bits), then the kept tokens in index order by block
-//                             scans (equal weights at the threshold: the earlier tokens).
+//                             round over the weights' IEEE bits, keys held in shared memory up to 48K tokens),
+//                             then the kept tokens in index order by block scans (equal weights at the threshold:
+//                             the earlier tokens).
 //   compact_*_kernel          the kept records copied in order; value tokens re-paired two per record.
 #pragma once
 
@@ -175,34 +176,58 @@ __device__ __forceinline__ unsigned block_excl_count(bool f, unsigned* wsum, uns
 }
 
 // Per (sequence, KV head): the keep tokens of largest weight, ascending. A weight's rank key is its IEEE bit pattern
-// (monotone for non-negative floats); zero, negative and NaN weights rank lowest.
+// (monotone for non-negative floats); zero, negative and NaN weights rank lowest. With KEYS_SMEM the keys are read
+// from global memory once and kept in dynamic shared memory (T <= SEL_SMEM_KEYS) for the radix rounds and the output
+// pass; otherwise every round rereads the weights. Each warp counts into its own histogram, lanes with the same
+// digit adding once (match_any), and the warps' histograms are summed per digit.
+constexpr int SEL_SMEM_KEYS = 48 * 1024;
+template <bool KEYS_SMEM>
 __global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* lam, long long T, int keep, int32_t* idx) {
-  __shared__ unsigned hist[256];
+  extern __shared__ unsigned keys_s[];
+  __shared__ unsigned hist[SEL_THREADS / 32][256];
   __shared__ unsigned wsum[32];
   __shared__ unsigned s_prefix, s_remaining;
-  const int bh = blockIdx.x, tid = threadIdx.x;
+  const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* lm = lam + (size_t)bh * T;
   int32_t* out = idx + (size_t)bh * keep;
-  auto key_of = [&](long long t) {
+  auto key_global = [&](long long t) {
     const float v = lm[t];
     return v > 0.f ? __float_as_uint(v) : 0u;
+  };
+  if constexpr (KEYS_SMEM) {
+    for (long long t = tid; t < T; t += SEL_THREADS) keys_s[t] = key_global(t);
+  }
+  auto key_of = [&](long long t) {
+    if constexpr (KEYS_SMEM) return keys_s[t];
+    else return key_global(t);
   };
   // radix select of the keep-th largest key, eight bits per round
   unsigned prefix = 0u, mask = 0u, remaining = (unsigned)keep;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += SEL_THREADS) hist[i] = 0u;
+    for (int i = tid; i < (SEL_THREADS / 32) * 256; i += SEL_THREADS) (&hist[0][0])[i] = 0u;
     __syncthreads();
-    for (long long t = tid; t < T; t += SEL_THREADS) {
-      const unsigned k = key_of(t);
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    for (long long c0 = 0; c0 < T; c0 += SEL_THREADS) {  // whole warps step together (match_any)
+      const long long t = c0 + tid;
+      const unsigned k = t < T ? key_of(t) : 0u;
+      const bool in = t < T && (k & mask) == prefix;
+      const unsigned dig = in ? (k >> shift) & 255u : 256u;  // 256: not counted
+      const unsigned same = __match_any_sync(0xffffffffu, dig);
+      if (in && lane == __ffs(same) - 1) hist[warp][dig] += __popc(same);  // one lane per digit: no race
+    }
+    __syncthreads();
+    if (tid < 256) {  // digit totals over the warps
+      unsigned c = 0u;
+#pragma unroll 8
+      for (int w = 0; w < SEL_THREADS / 32; ++w) c += hist[w][tid];
+      hist[0][tid] = c;
     }
     __syncthreads();
     if (tid == 0) {
       unsigned cum = 0u;
       int d = 255;
       for (; d > 0; --d) {
-        if (cum + hist[d] >= remaining) break;
-        cum += hist[d];
+        if (cum + hist[0][d] >= remaining) break;
+        cum += hist[0][d];
       }
       s_prefix = prefix | ((unsigned)d << shift);
       s_remaining = remaining - cum;
@@ -336,7 +361,17 @@ kv_status launch_token_weights(const void* q_obs, int W, const void* k, int B, i
 
 kv_status launch_token_select(const float* lam, int B, int Hkv, int64_t T, int64_t keep, int32_t* idx,
                               cudaStream_t s) {
-  token_select_kernel<<<B * Hkv, SEL_THREADS, 0, s>>>(lam, T, (int)keep, idx);
+  if (T <= SEL_SMEM_KEYS) {
+    const size_t smem = (size_t)T * 4;
+    const cudaError_t e = ensure_dyn_smem((const void*)token_select_kernel<true>, smem);
+    if (e != cudaSuccess) {
+      set_error("token_select_kernel shared memory: %s", cudaGetErrorString(e));
+      return KV_ERR_CUDA;
+    }
+    token_select_kernel<true><<<B * Hkv, SEL_THREADS, smem, s>>>(lam, T, (int)keep, idx);
+  } else {
+    token_select_kernel<false><<<B * Hkv, SEL_THREADS, 0, s>>>(lam, T, (int)keep, idx);
+  }
   return launch_check("token_select_kernel");
 }
 
