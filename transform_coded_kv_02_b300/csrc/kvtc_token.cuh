@@ -154,32 +154,35 @@ __global__ void __launch_bounds__(TK_TILE) token_merge_kernel(TokArgs a) {
   a.ml[(size_t)bh * TK_TILE + r] = make_float2(M, L);
 }
 
-// Exclusive count of the set flags before this thread in the block, and the block's total (every thread).
-__device__ __forceinline__ unsigned block_excl_count(bool f, unsigned* wsum, unsigned& total) {
+// Exclusive sum over the warps of a per-warp value (every lane of warp w passes the same v): the sum of the warps
+// before this one, and the block's total (every thread).
+__device__ __forceinline__ unsigned block_warp_excl_sum(unsigned v, unsigned* wsum, unsigned& total) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __syncthreads();  // the previous call's readers are done with wsum
-  const unsigned bal = __ballot_sync(0xffffffffu, f);
-  if (lane == 0) wsum[warp] = __popc(bal);
+  if (lane == 0) wsum[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    unsigned v = wsum[lane];
+    unsigned x = wsum[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const unsigned n = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += n;
+      const unsigned n = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += n;
     }
-    wsum[lane] = v;  // inclusive over the warps
+    wsum[lane] = x;  // inclusive over the warps
   }
   __syncthreads();
   total = wsum[31];
-  return (warp ? wsum[warp - 1] : 0u) + __popc(bal & ((1u << lane) - 1u));
+  return warp ? wsum[warp - 1] : 0u;
 }
 
 // Per (sequence, KV head): the keep tokens of largest weight, ascending. A weight's rank key is its IEEE bit pattern
-// (monotone for non-negative floats); zero, negative and NaN weights rank lowest. With KEYS_SMEM the keys are read
-// from global memory once and kept in dynamic shared memory (T <= SEL_SMEM_KEYS) for the radix rounds and the output
-// pass; otherwise every round rereads the weights. Each warp counts into its own histogram, lanes with the same
-// digit adding once (match_any), and the warps' histograms are summed per digit.
+// (monotone for non-negative floats); zero, negative and NaN weights rank lowest. Warp w owns the contiguous token
+// range [w C, (w + 1) C) and walks it 32 tokens at a time (lane = token). With KEYS_SMEM the keys are read from
+// global memory once and kept in dynamic shared memory (T <= SEL_SMEM_KEYS); otherwise every pass rereads the
+// weights. Radix select, 8 bits a round: each warp counts into its own histogram (lanes with the same digit add once,
+// match_any), the warps' histograms are summed per digit. Output: each warp counts its kept tokens (ballots), one
+// exclusive sum over the warps gives its first output slot and its share of the keys equal to the threshold (the
+// earliest ones), and the warp writes its tokens in order.
 constexpr int SEL_SMEM_KEYS = 48 * 1024;
 template <bool KEYS_SMEM>
 __global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* lam, long long T, int keep, int32_t* idx) {
@@ -190,12 +193,16 @@ __global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* 
   const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* lm = lam + (size_t)bh * T;
   int32_t* out = idx + (size_t)bh * keep;
+  constexpr int NWS = SEL_THREADS / 32;
+  const long long C = ((T + NWS - 1) / NWS + 31) / 32 * 32;  // tokens per warp, whole 32-token chunks
+  const long long w0 = min(T, (long long)warp * C), w1 = min(T, w0 + C);
   auto key_global = [&](long long t) {
     const float v = lm[t];
     return v > 0.f ? __float_as_uint(v) : 0u;
   };
   if constexpr (KEYS_SMEM) {
     for (long long t = tid; t < T; t += SEL_THREADS) keys_s[t] = key_global(t);
+    __syncthreads();
   }
   auto key_of = [&](long long t) {
     if constexpr (KEYS_SMEM) return keys_s[t];
@@ -204,21 +211,22 @@ __global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* 
   // radix select of the keep-th largest key, eight bits per round
   unsigned prefix = 0u, mask = 0u, remaining = (unsigned)keep;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < (SEL_THREADS / 32) * 256; i += SEL_THREADS) (&hist[0][0])[i] = 0u;
-    __syncthreads();
-    for (long long c0 = 0; c0 < T; c0 += SEL_THREADS) {  // whole warps step together (match_any)
-      const long long t = c0 + tid;
-      const unsigned k = t < T ? key_of(t) : 0u;
-      const bool in = t < T && (k & mask) == prefix;
+    for (int i = lane; i < 256; i += 32) hist[warp][i] = 0u;
+    __syncwarp();
+    for (long long c0 = w0; c0 < w1; c0 += 32) {
+      const long long t = c0 + lane;
+      const unsigned k = t < w1 ? key_of(t) : 0u;
+      const bool in = t < w1 && (k & mask) == prefix;
       const unsigned dig = in ? (k >> shift) & 255u : 256u;  // 256: not counted
       const unsigned same = __match_any_sync(0xffffffffu, dig);
       if (in && lane == __ffs(same) - 1) hist[warp][dig] += __popc(same);  // one lane per digit: no race
+      __syncwarp();
     }
     __syncthreads();
     if (tid < 256) {  // digit totals over the warps
       unsigned c = 0u;
 #pragma unroll 8
-      for (int w = 0; w < SEL_THREADS / 32; ++w) c += hist[w][tid];
+      for (int w = 0; w < NWS; ++w) c += hist[w][tid];
       hist[0][tid] = c;
     }
     __syncthreads();
@@ -238,18 +246,30 @@ __global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* 
     mask |= 255u << shift;
   }
   // prefix: the threshold key; every larger key is kept, and the first `remaining` keys equal to it
-  unsigned kept = 0u, eq_seen = 0u;
-  for (long long c0 = 0; c0 < T; c0 += SEL_THREADS) {
-    const long long t = c0 + tid;
-    const unsigned k = t < T ? key_of(t) : 0u;
-    const bool gt = t < T && k > prefix, eq = t < T && k == prefix;
-    unsigned n_eq, n_sel;
-    const unsigned eq_rank = eq_seen + block_excl_count(eq, wsum, n_eq);
-    const bool sel = gt || (eq && eq_rank < remaining);
-    const unsigned pos = kept + block_excl_count(sel, wsum, n_sel);
-    if (sel && pos < (unsigned)keep) out[pos] = (int32_t)t;
-    kept += n_sel;
-    eq_seen += n_eq;
+  unsigned n_gt = 0u, n_eq = 0u;
+  for (long long c0 = w0; c0 < w1; c0 += 32) {
+    const long long t = c0 + lane;
+    const unsigned k = t < w1 ? key_of(t) : 0u;
+    n_gt += __popc(__ballot_sync(0xffffffffu, t < w1 && k > prefix));
+    n_eq += __popc(__ballot_sync(0xffffffffu, t < w1 && k == prefix));
+  }
+  unsigned tot;
+  const unsigned eq_before = block_warp_excl_sum(n_eq, wsum, tot);
+  const unsigned eq_take = eq_before >= remaining ? 0u : min(n_eq, remaining - eq_before);
+  unsigned pos = block_warp_excl_sum(n_gt + eq_take, wsum, tot);
+  unsigned eq_used = 0u;
+  const unsigned lt = (1u << lane) - 1u;
+  for (long long c0 = w0; c0 < w1; c0 += 32) {
+    const long long t = c0 + lane;
+    const unsigned k = t < w1 ? key_of(t) : 0u;
+    const bool gt = t < w1 && k > prefix, eq = t < w1 && k == prefix;
+    const unsigned beq = __ballot_sync(0xffffffffu, eq);
+    const bool sel = gt || (eq && eq_used + __popc(beq & lt) < eq_take);
+    const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+    const unsigned p = pos + __popc(bsel & lt);
+    if (sel && p < (unsigned)keep) out[p] = (int32_t)t;
+    pos += __popc(bsel);
+    eq_used += __popc(beq);
   }
 }
 
