@@ -13,7 +13,8 @@
 //                             issues 8 tcgen05 MMAs (K = 16 each) into 128 tensor-memory columns; thread = query
 //                             row reads its 128 logits. Pass 0 leaves each row's tile maximum and sum of
 //                             2^(x - max); pass 1 forms p = 2^(x - M) / L and sums p^2 over the rows (a transpose
-//                             through shared memory) into the tile's token weights.
+//                             through shared memory) into the tile's token weights. The exponentials use the
+//                             hardware approximation (relative error about 2^-22), as the decode's softmax does.
 //   token_merge_kernel        per (sequence, KV head) and query row: M and L over the tiles.
 //   token_select_kernel       per (sequence, KV head): radix select of the keep-th largest weight (8 bits per
 //                             round over the weights' IEEE bits, keys held in shared memory up to 48K tokens),
@@ -100,32 +101,45 @@ __global__ void __launch_bounds__(TK_TILE, 1)
   tc_fence_after();
   const int r = 32 * warp + lane;  // query row = tensor-memory lane
   const bool rv = ok && r < a.nq;
-  float x[TK_TILE];  // row r's logits (base 2) against the tile's tokens
-#pragma unroll
-  for (int c = 0; c < TK_TILE; c += 32) {
+  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+  // row r's logits (base 2) against the tile's tokens, 32 columns at a time
+  auto load_chunk = [&](int c0, float (&x)[32]) {
     uint32_t v[32];
-    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c, v);
+    tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) x[c + j] = __uint_as_float(v[j]) * a.scale_log2;
-  }
-  if constexpr (PASS == 0) {
-    float m = -INFINITY;
+    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * a.scale_log2;
+  };
+  if constexpr (PASS == 0) {  // running maximum and sum of 2^(x - max)
+    float m = -INFINITY, l = 0.f;
+    for (int c0 = 0; c0 < TK_TILE && c0 < ntok; c0 += 32) {
+      float x[32];
+      load_chunk(c0, x);
+      float mc = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < TK_TILE; ++c)
-      if (c < ntok) m = fmaxf(m, x[c]);
-    float l = 0.f;
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < ntok) mc = fmaxf(mc, x[j]);
+      const float mn = fmaxf(m, mc);
+      float lc = 0.f;
 #pragma unroll
-    for (int c = 0; c < TK_TILE; ++c)
-      if (c < ntok) l += exp2f(x[c] - m);
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < ntok) lc += ex2_approx(x[j] - mn);
+      l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + lc;
+      m = mn;
+    }
     a.stats[((size_t)bh * a.nt + tile) * TK_TILE + r] = rv ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
   } else {
     const float2 ML = a.ml[(size_t)bh * TK_TILE + r];
     const float inv = rv && ML.y > 0.f ? 1.f / ML.y : 0.f;
+    for (int c0 = 0; c0 < TK_TILE; c0 += 32) {
+      float x[32];
+      if (c0 < ntok) load_chunk(c0, x);
 #pragma unroll
-    for (int c = 0; c < TK_TILE; ++c) {
-      const float p = (inv > 0.f && c < ntok) ? exp2f(x[c] - ML.x) * inv : 0.f;
-      tr[r * TK_TILE + (c ^ (r & 31))] = p * p;
+      for (int j = 0; j < 32; ++j) {
+        const int c = c0 + j;
+        const float p = (inv > 0.f && c < ntok) ? ex2_approx(x[j] - ML.x) * inv : 0.f;
+        tr[r * TK_TILE + (c ^ (r & 31))] = p * p;
+      }
     }
     __syncthreads();
     if (tid < ntok) {
@@ -149,7 +163,7 @@ __global__ void __launch_bounds__(TK_TILE) token_merge_kernel(TokArgs a) {
   float L = 0.f;
   for (int t = 0; t < a.nt; ++t) {
     const float2 s = st[(size_t)t * TK_TILE];
-    if (s.x != -INFINITY) L += s.y * exp2f(s.x - M);
+    if (s.x != -INFINITY) L += s.y * ex2_approx(s.x - M);
   }
   a.ml[(size_t)bh * TK_TILE + r] = make_float2(M, L);
 }
