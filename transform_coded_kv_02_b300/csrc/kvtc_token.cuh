@@ -193,8 +193,8 @@ __device__ __forceinline__ unsigned block_warp_excl_sum(unsigned v, unsigned* ws
 // (monotone for non-negative floats); zero, negative and NaN weights rank lowest. Warp w owns the contiguous token
 // range [w C, (w + 1) C) and walks it 32 tokens at a time (lane = token). With KEYS_SMEM the keys are read from
 // global memory once and kept in dynamic shared memory (T <= SEL_SMEM_KEYS); otherwise every pass rereads the
-// weights. Radix select, 8 bits a round: each warp counts into its own histogram (lanes with the same digit add once,
-// match_any), the warps' histograms are summed per digit. Output: each warp counts its kept tokens (ballots), one
+// weights. Radix select, 8 bits a round: each warp counts into its own histogram (shared-memory atomics), the
+// warps' histograms are summed per digit. Output: each warp counts its kept tokens (ballots), one
 // exclusive sum over the warps gives its first output slot and its share of the keys equal to the threshold (the
 // earliest ones), and the warp writes its tokens in order.
 constexpr int SEL_SMEM_KEYS = 48 * 1024;
@@ -231,28 +231,33 @@ __global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* 
       const long long t = c0 + lane;
       const unsigned k = t < w1 ? key_of(t) : 0u;
       const bool in = t < w1 && (k & mask) == prefix;
-      const unsigned dig = in ? (k >> shift) & 255u : 256u;  // 256: not counted
-      const unsigned same = __match_any_sync(0xffffffffu, dig);
-      if (in && lane == __ffs(same) - 1) hist[warp][dig] += __popc(same);  // one lane per digit: no race
-      __syncwarp();
+      if (in) atomicAdd(&hist[warp][(k >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (tid < 256) {  // digit totals over the warps
-      unsigned c = 0u;
+    // digit totals over the warps, then the count of keys at or above each digit (threads 0..255 take the digits in
+    // descending order: an inclusive scan over them); the one digit where the count first reaches `remaining` is
+    // the next 8 bits of the threshold
+    unsigned dv = 0u, dx = 0u;
+    if (tid < 256) {
 #pragma unroll 8
-      for (int w = 0; w < NWS; ++w) c += hist[w][tid];
-      hist[0][tid] = c;
+      for (int w = 0; w < NWS; ++w) dv += hist[w][255 - tid];
+      dx = dv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned n = __shfl_up_sync(0xffffffffu, dx, o);
+        if (lane >= o) dx += n;
+      }
+      if (lane == 31) wsum[warp] = dx;
     }
     __syncthreads();
-    if (tid == 0) {
-      unsigned cum = 0u;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (cum + hist[0][d] >= remaining) break;
-        cum += hist[0][d];
+    if (tid < 256) {
+      unsigned incl = dx;
+      for (int w = 0; w < warp; ++w) incl += wsum[w];
+      const unsigned excl = incl - dv;
+      if (excl < remaining && remaining <= incl) {
+        s_prefix = prefix | ((unsigned)(255 - tid) << shift);
+        s_remaining = remaining - excl;
       }
-      s_prefix = prefix | ((unsigned)d << shift);
-      s_remaining = remaining - cum;
     }
     __syncthreads();
     prefix = s_prefix;
