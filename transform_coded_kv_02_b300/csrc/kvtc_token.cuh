@@ -20,7 +20,7 @@
 //                             round over the weights' IEEE bits, keys held in shared memory up to 48K tokens),
 //                             then the kept tokens in index order by block scans (equal weights at the threshold:
 //                             the earlier tokens).
-//   compact_*_kernel          the kept records copied in order; value tokens re-paired two per record.
+//   compact_kernel            the kept records copied in order; value tokens re-paired two per record.
 #pragma once
 
 #include "kvtc_tc.cuh"
@@ -301,10 +301,8 @@ struct CompactArgs {
 };
 
 // keys: thread per (sequence-head, kept token, record word)
-__global__ void compact_keys_kernel(CompactArgs a) {
+__device__ __forceinline__ void compact_key_word(const CompactArgs& a, long long g) {
   const long long per = (long long)a.keep * a.Rk;
-  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (g >= (long long)a.BH * per) return;
   const int bh = (int)(g / per);
   const long long r = g - (long long)bh * per;
   const int i = (int)(r / a.Rk), w = (int)(r - (long long)i * a.Rk);
@@ -318,11 +316,9 @@ __global__ void compact_keys_kernel(CompactArgs a) {
 
 // values: thread per (sequence-head, destination record, record word); kept tokens 2j and 2j + 1 form record j, each
 // bringing its z/s word and its 16-bit half of every code word from the record that held it
-__global__ void compact_values_kernel(CompactArgs a) {
+__device__ __forceinline__ void compact_value_word(const CompactArgs& a, long long g) {
   const int W = 2 * a.Rv, nrec = (a.keep + 1) / 2;
   const long long per = (long long)nrec * W;
-  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (g >= (long long)a.BH * per) return;
   const int bh = (int)(g / per);
   const long long r = g - (long long)bh * per;
   const int j = (int)(r / W), w = (int)(r - (long long)j * W);
@@ -344,6 +340,15 @@ __global__ void compact_values_kernel(CompactArgs a) {
     v = lo | (hi << 16);
   }
   a.dst[1][((size_t)bh * (a.Td / 2) + (size_t)j) * W + w] = v;
+}
+
+// one launch: threads [0, nk) copy key words, the rest value words
+__global__ void compact_kernel(CompactArgs a, long long nk, long long nv) {
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g < nk)
+    compact_key_word(a, g);
+  else if (g < nk + nv)
+    compact_value_word(a, g - nk);
 }
 
 // ---- host side --------------------------------------------------------------------------------------------
@@ -429,9 +434,8 @@ kv_status launch_compact(const ParamsDev& P, const kv_cache& src, const kv_cache
   a.Rv = P.t[1].r_words;
   a.BH = B * src.Hkv;
   const long long nk = (long long)a.BH * keep * a.Rk, nv = (long long)a.BH * ((keep + 1) / 2) * 2 * a.Rv;
-  compact_keys_kernel<<<(unsigned)((nk + 255) / 256), 256, 0, s>>>(a);
-  compact_values_kernel<<<(unsigned)((nv + 255) / 256), 256, 0, s>>>(a);
-  return launch_check("compact kernels");
+  compact_kernel<<<(unsigned)((nk + nv + 255) / 256), 256, 0, s>>>(a, nk, nv);
+  return launch_check("compact_kernel");
 }
 
 }  // namespace kvtc
