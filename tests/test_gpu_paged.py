@@ -265,3 +265,89 @@ def test_query_positions_need_a_rope_table():
         _run_paged_decode(P_lib, kp, vp, bt, n_pages, 32, 1, 1, w.Hkv, w.Hq, layers[0][0].q[0][None], [64], [63],
                           False)
     assert e.value.status == kvtc.KV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kind", ["joint_14_8", "runtime_32_words"])
+def test_paged_decode_other_record_lengths(kind):
+    """Record lengths beyond the equal-budget kernels through the paged path: the joint split's 14 key and 8 value
+    words (a compile-time kernel of unequal lengths) and 8 bits per element, 32 words per token (the kernel that reads
+    the lengths at run time); 64-token pages, two layers, rotary embedding on."""
+    w = synth.WORKLOADS["llama_decode_32k"]
+    n_layers, B, T, T_cap, P = 2, 1, 600, 640, 64
+    layers = []
+    for layer in range(n_layers):
+        L = synth.make_layer(w, layer=layer, T=T, steps=1, B=B)
+        if kind == "joint_14_8":
+            sets = O.calibrate_joint(list(zip(L.calib_k, L.calib_v, L.calib_q)), 2.75, 2.75)
+            assert (sets[0][0].r_words, sets[0][1].r_words) == (14, 8)
+        else:
+            sets = G.calibrate_oracle(L, 8.0, 8.0)
+            assert sets[0][0].r_words == 32
+        layers.append((L, sets))
+    P_lib = G.lib_params([s for _, sets in layers for s in sets])
+    P_lib.set_rope(ROPE_BASE).upload()
+    dense = [G.oracle_cache(synth.as_float(L.k), synth.as_float(L.v), sets, False, T_cap) for L, sets in layers]
+    rk = np.concatenate([d[0] for d in dense])
+    rv = np.concatenate([d[1] for d in dense])
+    seq, q_pos = [T], [4321]
+    bt, n_pages = _page_tables(np.random.default_rng(9), n_layers * B, seq * n_layers, P, T_cap // P)
+    kp, vp = _scatter(rk, rv, bt, n_pages, P)
+    q_bits = np.stack([L.q[0] for L, _ in layers])
+    got, st = _run_paged_decode(P_lib, kp, vp, bt, n_pages, P, B, n_layers, w.Hkv, w.Hq, q_bits, seq, q_pos, False)
+    assert st == kvtc.KV_OK, kvtc.kv_last_error()
+    ref = _oracle(layers, dense, q_bits, seq, q_pos, w.Hkv, w.Hq, False, n_layers, B)
+    assert G.rel_l2_rows(got, ref).max() <= DEC_TOL
+
+
+def test_paged_serving_loop_appends_then_decodes():
+    """A serving loop over a paged cache: prefill 300 tokens into pages, then eight steps that each append one token
+    per sequence (kv_encode_paged, t_new = 1, odd and even positions) and decode over the grown context with the
+    query's rotary embedding at its position; every step's output against the oracle over the oracle's records of the
+    same tokens, and the appended records against the oracle's."""
+    w = synth.WORKLOADS["qwen_batched_8k"]
+    B, T0, steps, P, T_cap = 2, 300, 8, 32, 320
+    L = synth.make_layer(w, T=T0 + steps, steps=steps, B=B)
+    sets = G.calibrate_oracle(L, 3.0, 3.0)
+    per_seq = L.per_seq_params
+    P_lib = G.lib_params(sets)
+    P_lib.set_rope(ROPE_BASE).upload()
+    Rk, Rv = sets[0][0].r_words, sets[0][1].r_words
+    bt, n_pages = _page_tables(np.random.default_rng(4), B, [T_cap] * B, P, T_cap // P)
+    kp = torch.zeros((n_pages, w.Hkv, P, Rk), dtype=torch.int32, device=G.DEV)
+    vp = torch.zeros((n_pages, w.Hkv, P // 2, 2 * Rv), dtype=torch.int32, device=G.DEV)
+    tbt = torch.from_numpy(bt).to(G.DEV)
+    cache = kvtc.make_paged_cache(kp, vp, n_pages, P, w.Hkv, B, 1, bt.shape[1], tbt, per_seq, 0)
+    kvtc.kv_encode_paged(P_lib, cache, G.to_dev_storage(np.ascontiguousarray(L.k[:, :, :T0])),
+                         G.to_dev_storage(np.ascontiguousarray(L.v[:, :, :T0])), kvtc.KV_DTYPE_BF16, T0,
+                         torch.zeros(B, dtype=torch.int64, device=G.DEV))
+    k, v = synth.as_float(L.k), synth.as_float(L.v)
+    out = torch.zeros((1, B, w.Hq, 128), dtype=torch.float32, device=G.DEV)
+    ws = torch.zeros(kvtc.kv_decode_paged_workspace_bytes(P_lib, cache, w.Hq), dtype=torch.uint8, device=G.DEV)
+    scale = 1.0 / math.sqrt(128)
+    g = w.Hq // w.Hkv
+    for i in range(steps):
+        t = T0 + i
+        kvtc.kv_encode_paged(P_lib, cache, G.to_dev_storage(np.ascontiguousarray(L.k[:, :, t:t + 1])),
+                             G.to_dev_storage(np.ascontiguousarray(L.v[:, :, t:t + 1])), kvtc.KV_DTYPE_BF16, 1,
+                             torch.full((B,), t, dtype=torch.int64, device=G.DEV))
+        q = G.to_dev_storage(L.q[i][None])
+        kvtc.kv_attend_decode_paged(P_lib, cache, q, w.Hq, torch.full((B,), t + 1, dtype=torch.int32, device=G.DEV),
+                                    torch.full((B,), t, dtype=torch.int32, device=G.DEV), scale, out, ws)
+        assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
+        got = out.cpu().numpy()[0].astype(np.float64)
+        for b in range(B):
+            for h in range(w.Hkv):
+                pk, pv = sets[G.set_index(b, h, w.Hkv, per_seq)]
+                ork, orv = O.encode(k[b, h, :t + 1], pk), O.encode(v[b, h, :t + 1], pv)
+                qh = O.rotary_embed(synth.as_float(L.q[i, b, h * g:(h + 1) * g]), t, ROPE_BASE)
+                ref = O.attend_decode(qh, ork, orv, pk, pv, t + 1, scale)
+                assert G.rel_l2_rows(got[b, h * g:(h + 1) * g], ref).max() <= 5 * DEC_TOL, (i, b, h)
+    # the appended tokens' records against the oracle's (keys one per token; values in their two-token records)
+    kp_h, vp_h = G.u32(kp), G.u32(vp)
+    for b in range(B):
+        gk, gv = _gather(kp_h, vp_h, bt, b, P, T0 + steps)
+        for h in range(w.Hkv):
+            pk, pv = sets[G.set_index(b, h, w.Hkv, per_seq)]
+            ork = O.encode(k[b, h, :T0 + steps], pk)
+            _, _, _, fk, dk, _ = G.code_diff(gk[h, T0:T0 + steps], ork[T0:T0 + steps], pk)
+            assert dk <= 1 and fk <= 2e-2, (b, h, fk)
