@@ -8,8 +8,9 @@ namespace kvtc {
 // uncompressed bf16 split-K flash-decode (comparator)
 // ======================================================================================================
 // A CTA of eight warps owns one split of one (sequence, KV head). Tiles of 128 tokens of K and V stream through a
-// ring of shared-memory stages by 16-byte asynchronous copies (each 256-byte token row stored with its 16-byte
-// chunks XOR-swizzled by the row, so that ldmatrix reads are free of bank conflicts); one barrier per tile. Warp w
+// ring of shared-memory stages by tiled TMA (one thread issues four 128-row x 64-channel boxes per tile, 128-byte
+// swizzle, completion on the stage's mbarrier), so that ldmatrix reads are free of bank conflicts; one barrier per
+// tile. The V rows of a partial last tile past the split's end are zeroed before use (K rows there are masked). Warp w
 // takes tokens [16 w, 16 w + 16) of each tile: logits on the MMA (A = the g query rows, B = K), online softmax in
 // the accumulator layout, P (bf16 hi + lo) straight into the B operand of the P.V MMA (A = V^T). The splits merge
 // through the workspace; the last to arrive writes the output.
@@ -31,20 +32,35 @@ struct DecBf16Args {
   long long T_cap;
   int B, Hkv, Hq, g, splits;
   float scale_log2;
+  int box_rows;       // rows of a TMA box: 128, or all rows of a smaller cache
+  long long wait_ns;
 };
 
-static size_t decode_bf16_smem_bytes() { return (size_t)BSTAGES * BSTAGE_BYTES; }
+static size_t decode_bf16_smem_bytes() { return (size_t)BSTAGES * BSTAGE_BYTES + 1024; }  // + alignment slack
 
-// byte offset of 16-byte chunk c (0..15) of token row r in a tile
-__device__ __forceinline__ uint32_t bswz(int r, int c) { return (uint32_t)(r * BROW + ((c ^ (r & 7)) << 4)); }
+// byte offset of 16-byte chunk c (0..15) of token row r in a tile stored as two TMA boxes (channels 0-63, 64-127)
+// of 128 rows x 128 bytes with the 128-byte swizzle (chunk index XOR row mod 8)
+__device__ __forceinline__ uint32_t bswz(int r, int c) {
+  return (uint32_t)((c >> 3) * (BT * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
 
-__global__ void __launch_bounds__(BTHREADS, 1) decode_bf16_kernel(DecBf16Args a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(BTHREADS, 1)
+    decode_bf16_kernel(DecBf16Args a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[BSTAGES];
+  __shared__ int s_last, s_abort;
+  const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;  // 1024-byte aligned for the swizzle
+  uint8_t* const smem = smem_raw + (ring - smem_u32(smem_raw));
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int bh = b * a.Hkv + kh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   const int g = a.g;
-  __shared__ int s_last;
+  if (tid == 0) {
+    for (int s = 0; s < BSTAGES; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
 
   pdl_wait();
   const long long L = max(0LL, min((long long)a.seq_lens[b], a.T_cap));
@@ -52,32 +68,25 @@ __global__ void __launch_bounds__(BTHREADS, 1) decode_bf16_kernel(DecBf16Args a)
   const long long t0 = min((long long)split * chunk, L);
   const long long t1 = min(t0 + chunk, L);
   const int ntiles = (int)((t1 - t0 + BT - 1) / BT);
-  const __nv_bfloat16* kg = a.k + (size_t)bh * a.T_cap * D;
-  const __nv_bfloat16* vg = a.v + (size_t)bh * a.T_cap * D;
-  const uint32_t ring = smem_u32(smem);
+  const int row0 = (int)((long long)bh * a.T_cap + t0);  // tensor-map row of the split's first token
 
-  // tile i into ring slot i % BSTAGES: thread t copies chunks t, t + 256, ... of K and of V (rows past the split's
-  // end are zero-filled, never read from memory)
+  // tile i into ring slot i % BSTAGES (thread 0): K and V, each as two boxes of 64 channels
   auto issue = [&](int i) {
     const uint32_t base = ring + (uint32_t)(i % BSTAGES) * BSTAGE_BYTES;
-    const long long tb = t0 + (long long)i * BT;
-#pragma unroll
-    for (int u = 0; u < BT * 16 / BTHREADS; ++u) {
-      const int idx = tid + u * BTHREADS, r = idx >> 4, c = idx & 15;
-      const bool in = tb + r < t1;
-      const size_t src = (size_t)(in ? tb + r : t0) * D + c * 8;
-      const uint32_t sz = in ? 16u : 0u;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(base + bswz(r, c)), "l"(kg + src), "r"(sz)
-                   : "memory");
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(base + BT * BROW + bswz(r, c)), "l"(vg + src),
-                   "r"(sz)
-                   : "memory");
-    }
+    const uint32_t bar = smem_u32(&full[i % BSTAGES]);
+    const int r = row0 + i * BT;
+    mbar_expect_tx(bar, 4u * (uint32_t)a.box_rows * 128u);
+    tma_load_2d(base, &mk, 0, r, bar);
+    tma_load_2d(base + BT * 128, &mk, 64, r, bar);
+    tma_load_2d(base + BT * BROW, &mv, 0, r, bar);
+    tma_load_2d(base + BT * BROW + BT * 128, &mv, 64, r, bar);
   };
-#pragma unroll
-  for (int i = 0; i < BSTAGES - 1; ++i) {
-    if (i < ntiles) issue(i);
-    cp_async_commit();
+  int issued = 0;
+  if (tid == 0) {
+    tma_prefetch_map(&mk);
+    tma_prefetch_map(&mv);
+    for (int i = 0; i < BSTAGES - 1 && i < ntiles; ++i) issue(i);
+    issued = min(BSTAGES - 1, ntiles);
   }
 
   // q rows (bf16, exact): A row h = head h (h < g), others zero; 8 k-blocks of 16 channels
@@ -104,11 +113,27 @@ __global__ void __launch_bounds__(BTHREADS, 1) decode_bf16_kernel(DecBf16Args a)
   const int lr = 16 * warp + (lane & 7) + ((lane >> 4) << 3), lc = (lane >> 3) & 1;
 
   for (int i = 0; i < ntiles; ++i) {
-    cp_async_wait_prior();  // tile i has landed (this thread's copies) ...
-    __syncthreads();        // ... for every thread, and every warp is done with tile i - 1
-    if (i + BSTAGES - 1 < ntiles) issue(i + BSTAGES - 1);
-    cp_async_commit();
+    // tile i has landed, and every warp is done with tile i - 1
+    const bool ok = mbar_wait_bounded(smem_u32(&full[i % BSTAGES]), (uint32_t)((i / BSTAGES) & 1), a.wait_ns);
+    if (!__syncthreads_and(ok)) {
+      if (tid == 0) s_abort = 1;
+      break;
+    }
+    if (tid == 0 && i + BSTAGES - 1 < ntiles) {
+      fence_proxy_async_smem();  // this slot's generic writes (a zeroed tail) before the copy's
+      issue(i + BSTAGES - 1);
+      issued = i + BSTAGES;
+    }
     const uint32_t ks = ring + (uint32_t)(i % BSTAGES) * BSTAGE_BYTES, vs = ks + BT * BROW;
+    const long long tb = t0 + (long long)i * BT;
+    if (tb + BT > t1) {  // a partial last tile: V rows past the split's end hold whatever the cache holds there
+      const int nv = (int)(t1 - tb);
+      for (int idx = tid; idx < (BT - nv) * 16; idx += BTHREADS) {
+        const int r = nv + (idx >> 4), c = idx & 15;
+        *reinterpret_cast<uint4*>(smem + (vs - ring) + bswz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncthreads();
+    }
     const long long tw = t0 + (long long)i * BT + 16 * warp;  // this warp's first token
     if (tw >= t1) continue;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -166,7 +191,9 @@ __global__ void __launch_bounds__(BTHREADS, 1) decode_bf16_kernel(DecBf16Args a)
       mma_bf16(acc_o[mb][1], af, bl0, bl1);
     }
   }
-  cp_async_wait_all();
+  if (tid == 0 && s_abort)  // leave no copy in flight
+    for (int i = max(0, issued - BSTAGES); i < issued; ++i)
+      mbar_wait_bounded(smem_u32(&full[i % BSTAGES]), (uint32_t)((i / BSTAGES) & 1), a.wait_ns);
   __syncthreads();  // the ring is free: the warps' partials go there
   float* ws = reinterpret_cast<float*>(smem);  // [BWARPS][8][PSTR]
   {
@@ -303,6 +330,18 @@ kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int H
   a.g = Hq / Hkv;
   a.splits = L.splits;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_ns = g_wait_limit_ns;
+  const unsigned long long rows = (unsigned long long)B * Hkv * (unsigned long long)T_cap;
+  if (rows + BT >= (1ull << 31)) {
+    set_error("decode_bf16: %llu cache rows exceed the tensor maps' 32-bit coordinates", rows);
+    return KV_ERR_UNSUPPORTED;
+  }
+  a.box_rows = (int)std::min<unsigned long long>(BT, rows);
+  CUtensorMap maps[2];
+  if (!make_bf16_map(&maps[0], k, rows, (unsigned)a.box_rows) || !make_bf16_map(&maps[1], v, rows, (unsigned)a.box_rows)) {
+    set_error("decode_bf16: tensor map encoding failed");
+    return KV_ERR_CUDA;
+  }
   const size_t smem = decode_bf16_smem_bytes();
   cudaError_t e = ensure_dyn_smem((const void*)decode_bf16_kernel, smem);
   if (e != cudaSuccess) {
@@ -319,7 +358,7 @@ kv_status launch_decode_bf16(const void* k, const void* v, int B, int Hkv, int H
   cfg.stream = s;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a);
+  e = cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a, maps[0], maps[1]);
   if (e != cudaSuccess) {
     set_error("decode_bf16_kernel launch: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;
