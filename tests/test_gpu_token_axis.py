@@ -48,9 +48,12 @@ def _gpu_weights(q_obs_bits, k_bits, Hkv, scale):
 
 
 @pytest.mark.parametrize("name,W,T", [("llama_decode_32k", 32, 1000), ("qwen_batched_8k", 16, 777),
-                                      ("llama_decode_32k", 5, 130), ("tiny", 32, 1)])
+                                      ("llama_decode_32k", 5, 130), ("tiny", 32, 1),
+                                      ("llama_decode_32k", 32, 20000), ("qwen_batched_8k", 16, 9000)])
 def test_token_weights_match_oracle(name, W, T):
-    """g x W observation rows (128, 112, 20 and 128 of the MMA's 128), ragged last tiles, one-token sequences."""
+    """g x W observation rows (128, 112, 20 and 128 of the MMA's 128), ragged last tiles, one-token sequences.
+    The two longer cases hold more tiles than two per SM, so each CTA takes a run of tiles (5 and 2 on 148 SMs) with
+    its keys double-buffered, and the last run of a (sequence, KV head) is shorter than the others."""
     w = synth.WORKLOADS[name]
     B = 2 if w.B > 1 else 1
     L = synth.make_layer(w, T=T, steps=W, B=B)

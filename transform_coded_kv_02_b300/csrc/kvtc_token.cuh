@@ -8,13 +8,16 @@
 // zero bits is the token's whole record: reverse water-filling with one tier keeps the `keep` heaviest tokens
 // (ties: the earlier token) and evicts the rest. The decode then runs unchanged over the compacted records.
 //
-//   token_logits_kernel<0|1>  one CTA per (128-token tile, KV head, sequence): the g x W observation queries
-//                             (M = 128 rows, zero rows past g W) and the tile's keys arrive by TMA; one thread
-//                             issues 8 tcgen05 MMAs (K = 16 each) into 128 tensor-memory columns; thread = query
-//                             row reads its 128 logits. Pass 0 leaves each row's tile maximum and sum of
-//                             2^(x - max); pass 1 forms p = 2^(x - M) / L and sums p^2 over the rows (a transpose
-//                             through shared memory) into the tile's token weights. The exponentials use the
-//                             hardware approximation (relative error about 2^-22), as the decode's softmax does.
+//   token_logits_kernel<0|1>  one CTA per run of 128-token tiles of one (sequence, KV head), about two CTAs per
+//                             SM: the g x W observation queries (M = 128 rows, zero rows past g W) arrive once by
+//                             TMA, the tiles' keys through two stages; one thread issues each tile's 8 tcgen05 MMAs
+//                             (K = 16 each) into one of two 128-column tensor-memory accumulators, so that the next
+//                             tile's MMAs and key copy run while this one is read back; each thread reads one
+//                             tensor-memory lane of 128 logits. Pass 0 (thread = query row) leaves each row's
+//                             maximum and sum of 2^(x - max) over the run. Pass 1 takes the transposed product (keys
+//                             as the MMA's A operand: thread = token) and sums p^2 = 2^(2 x - 2 (M + log2 L)) over
+//                             its row of query columns, with no exchange between threads. The exponentials use the hardware
+//                             approximation (relative error about 2^-22), as the decode's softmax does.
 //   token_merge_kernel        per (sequence, KV head) and query row: M and L over the tiles.
 //   token_select_kernel       per (sequence, KV head): radix select of the keep-th largest weight (8 bits per
 //                             round over the weights' IEEE bits, keys held in shared memory up to 48K tokens),
@@ -31,11 +34,12 @@ constexpr int TK_TILE = 128;        // keys per CTA and query rows per MMA
 constexpr int SEL_THREADS = 1024;
 
 struct TokArgs {
-  float2* stats;   // [B*Hkv][nt][128]: per tile and query row, (max, sum of 2^(x - max)) over the tile's tokens
+  float2* stats;   // [B*Hkv][nch][128]: per run of tiles and query row, (max, sum of 2^(x - max)) over its tokens
   float2* ml;      // [B*Hkv][128]:     (M, L) over all tiles
   float* lam;      // [B*Hkv][T]:       token weights
   long long T;
   int Hkv, Hq, W, g, nq, nt;
+  int tpc, nch;      // tiles per CTA, and the CTAs (runs of tiles) per (sequence, KV head): ceil(nt / tpc)
   int qbox, kbox;    // rows of the query and key boxes: 128, or all rows of a smaller tensor (the operand rows past
                      // them are stale and masked)
   float scale_log2;  // softmax scale * log2(e): logits in base 2
@@ -46,24 +50,37 @@ template <int PASS>
 __global__ void __launch_bounds__(TK_TILE, 1)
     token_logits_kernel(TokArgs a, const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full, done;
+  __shared__ __align__(8) uint64_t qfull, kfull[2], mdone[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_ok;
+  __shared__ float cq[TK_TILE];  // pass 1: per query row, 2 (M + log2 L); +inf for rows without a query
+  // the queries (two 64-column boxes), then two key stages of two boxes each
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  // pass 1: p^2 [128 rows][128 tokens] (column index XOR-swizzled by the row), over the consumed operands
-  float* const tr = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
-  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = b * a.Hkv + h;
-  const long long t0 = (long long)tile * TK_TILE;
-  const int ntok = (int)min((long long)TK_TILE, a.T - t0);
+  const int tile0 = chunk * a.tpc;
+  const int ntl = min(a.tpc, a.nt - tile0);  // this CTA's tiles, at least one
   if (warp == 0) {
-    tmem_alloc(smem_u32(&s_tmem), 128);
+    tmem_alloc(smem_u32(&s_tmem), 2 * TK_TILE);
     tmem_relinquish();
   }
+  if constexpr (PASS == 1) {
+    const float2 ML = a.ml[(size_t)bh * TK_TILE + tid];
+    cq[tid] = tid < a.nq && ML.y > 0.f ? 2.f * (ML.x + log2f(ML.y)) : INFINITY;
+  }
+  if (a.qbox < TK_TILE) {  // query rows the box does not cover: zeros, so that their logits stay finite
+    for (int i = a.qbox * 8 + tid; i < TK_TILE * 8; i += TK_TILE)
+      for (int hf = 0; hf < 2; ++hf)
+        *reinterpret_cast<uint4*>(smem_raw + (base - smem_u32(smem_raw)) + hf * TC_BOX_BYTES + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   if (tid == 0) {
-    mbar_init(smem_u32(&full), 1);
-    mbar_init(smem_u32(&done), 1);
+    mbar_init(smem_u32(&qfull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&kfull[s]), 1);
+      mbar_init(smem_u32(&mdone[s]), 1);
+    }
     fence_mbar_init();
     s_ok = 1;
   }
@@ -71,97 +88,143 @@ __global__ void __launch_bounds__(TK_TILE, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  if (tid == 0) {
-    const uint32_t fb = smem_u32(&full), db = smem_u32(&done);
-    const int qrow = (b * a.Hq + h * a.g) * a.W;         // the g x W observation queries of this KV head
-    const int krow = (int)((long long)bh * a.T + t0);    // the tile's keys (rows past the head's T are masked)
-    mbar_expect_tx(fb, (uint32_t)(a.qbox + a.kbox) * 256u);
-    tma_load_2d(base, &mq, 0, qrow, fb);
-    tma_load_2d(base + TC_BOX_BYTES, &mq, 64, qrow, fb);
-    tma_load_2d(base + 2 * TC_BOX_BYTES, &mk, 0, krow, fb);
-    tma_load_2d(base + 3 * TC_BOX_BYTES, &mk, 64, krow, fb);
-    if (mbar_wait_bounded(fb, 0u, a.wait_ns)) {
+  auto kstage = [&](int s) { return base + (uint32_t)(2 + 2 * s) * TC_BOX_BYTES; };
+  // thread 0's bookkeeping: key tiles loaded, key loads seen complete, MMA groups issued and seen complete
+  int n_load = 0, n_kdone = 0, n_mma = 0, n_mdone = 0;
+  auto load_keys = [&](int i) {  // tile i of this CTA into key stage i & 1 (rows past the head's T are masked)
+    const uint32_t fb = smem_u32(&kfull[i & 1]);
+    const int krow = (int)((long long)bh * a.T + (long long)(tile0 + i) * TK_TILE);
+    mbar_expect_tx(fb, (uint32_t)a.kbox * 256u);
+    tma_load_2d(kstage(i & 1), &mk, 0, krow, fb);
+    tma_load_2d(kstage(i & 1) + TC_BOX_BYTES, &mk, 64, krow, fb);
+    ++n_load;
+  };
+  // tile i's logits into accumulator i & 1 once its keys have landed; a key wait that runs out marks the CTA failed
+  // and completes the accumulator's barrier itself, so that no thread waits on MMAs that were never issued
+  auto issue_mma = [&](int i) {
+    const int s = i & 1;
+    if (s_ok && mbar_wait_bounded(smem_u32(&kfull[s]), (uint32_t)(i >> 1) & 1u, a.wait_ns)) {
+      ++n_kdone;
       tc_fence_after();
       constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+      const uint32_t acc = tmem + (uint32_t)(s * TK_TILE);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t koff = (uint32_t)(kk >> 2) * TC_BOX_BYTES + (uint32_t)(kk & 3) * 32u;
-        tc_mma_bf16(tmem, smem_desc_k128(base + koff), smem_desc_k128(base + 2 * TC_BOX_BYTES + koff), IDESC,
-                    kk ? 1u : 0u);
+        // pass 0: logits[query row][token]; pass 1 the transpose, logits[token][query row]
+        const uint64_t dq = smem_desc_k128(base + koff), dk = smem_desc_k128(kstage(s) + koff);
+        tc_mma_bf16(acc, PASS == 0 ? dq : dk, PASS == 0 ? dk : dq, IDESC, kk ? 1u : 0u);
       }
-      tc_commit(db);
+      tc_commit(smem_u32(&mdone[s]));
+      ++n_mma;
     } else {
       s_ok = 0;
-      mbar_wait_bounded(fb, 0u, a.wait_ns);  // the copies may still land: wait again before the CTA can exit
-      mbar_arrive(db);
+      mbar_arrive(smem_u32(&mdone[s]));
     }
-  }
-  const bool got = mbar_wait_bounded(smem_u32(&done), 0u, a.wait_ns);
-  const bool ok = __syncthreads_and(got) && s_ok;
-  tc_fence_after();
-  const int r = 32 * warp + lane;  // query row = tensor-memory lane
-  const bool rv = ok && r < a.nq;
-  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
-  // row r's logits (base 2) against the tile's tokens, 32 columns at a time
-  auto load_chunk = [&](int c0, float (&x)[32]) {
-    uint32_t v[32];
-    tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * a.scale_log2;
   };
-  if constexpr (PASS == 0) {  // running maximum and sum of 2^(x - max)
-    float m = -INFINITY, l = 0.f;
-    for (int c0 = 0; c0 < TK_TILE && c0 < ntok; c0 += 32) {
-      float x[32];
-      load_chunk(c0, x);
-      float mc = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < ntok) mc = fmaxf(mc, x[j]);
-      const float mn = fmaxf(m, mc);
-      float lc = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < ntok) lc += ex2_approx(x[j] - mn);
-      l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + lc;
-      m = mn;
+  if (tid == 0) {
+    const uint32_t qb = smem_u32(&qfull);
+    const int qrow = (b * a.Hq + h * a.g) * a.W;  // the g x W observation queries of this KV head
+    mbar_expect_tx(qb, (uint32_t)a.qbox * 256u);
+    tma_load_2d(base, &mq, 0, qrow, qb);
+    tma_load_2d(base + TC_BOX_BYTES, &mq, 64, qrow, qb);
+    load_keys(0);
+    if (ntl > 1) load_keys(1);
+    if (!mbar_wait_bounded(qb, 0u, a.wait_ns)) {
+      s_ok = 0;
+      mbar_wait_bounded(qb, 0u, a.wait_ns);  // the copy may still land: wait again before the CTA can exit
     }
-    a.stats[((size_t)bh * a.nt + tile) * TK_TILE + r] = rv ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
-  } else {
-    const float2 ML = a.ml[(size_t)bh * TK_TILE + r];
-    const float inv = rv && ML.y > 0.f ? 1.f / ML.y : 0.f;
-    for (int c0 = 0; c0 < TK_TILE; c0 += 32) {
-      float x[32];
-      if (c0 < ntok) load_chunk(c0, x);
+    issue_mma(0);
+  }
+  const int r = 32 * warp + lane;  // tensor-memory lane: pass 0 the query row, pass 1 the tile's token
+  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+  const bool rows_here = PASS == 1 || 32 * warp < a.nq;  // pass 0: warps without a query row read nothing back
+  float m = -INFINITY, l = 0.f;  // pass 0: running maximum and sum of 2^(x - max) over this CTA's tokens
+  const float two_s = 2.f * a.scale_log2;
+  bool ok = true;
+  for (int i = 0; i < ntl; ++i) {
+    const int s = i & 1;
+    // the next tile's MMAs go out while this tile is read back (its accumulator was released at the end of the
+    // previous iteration)
+    if (tid == 0 && i + 1 < ntl) issue_mma(i + 1);
+    const bool got = mbar_wait_bounded(smem_u32(&mdone[s]), (uint32_t)(i >> 1) & 1u, a.wait_ns);
+    if (tid == 0 && got && n_mdone == i) ++n_mdone;
+    tc_fence_after();
+    // this tile's keys are consumed: the stage takes the tile after next
+    if (tid == 0 && got && s_ok && i + 2 < ntl) load_keys(i + 2);
+    const long long t0 = (long long)(tile0 + i) * TK_TILE;
+    const int ntok = (int)min((long long)TK_TILE, a.T - t0);
+    const uint32_t trow = tmem + lane_off + (uint32_t)(s * TK_TILE);
+    if constexpr (PASS == 0) {  // row r's logits (base 2) against the tile's tokens, 32 columns at a time
+      for (int c0 = 0; c0 < ntok && rows_here; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
+        tmem_ld_wait();
+        float x[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int c = c0 + j;
-        const float p = (inv > 0.f && c < ntok) ? ex2_approx(x[j] - ML.x) * inv : 0.f;
-        tr[r * TK_TILE + (c ^ (r & 31))] = p * p;
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * a.scale_log2;
+        const int nc = min(32, ntok - c0);
+        float mc = -INFINITY, lc = 0.f;
+        if (nc == 32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mc = fmaxf(mc, x[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nc) mc = fmaxf(mc, x[j]);
+        }
+        const float mn = fmaxf(m, mc);
+        if (nc == 32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) lc += ex2_approx(x[j] - mn);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nc) lc += ex2_approx(x[j] - mn);
+        }
+        l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + lc;
+        m = mn;
       }
+    } else {  // token r's weight: sum over the query rows of p^2 = 2^(2 s x - 2 (M + log2 L))
+      float sum = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < TK_TILE; c0 += 32) {
+        if (c0 < a.nq) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum += ex2_approx(fmaf(__uint_as_float(v[j]), two_s, -cq[c0 + j]));
+        }
+      }
+      if (got && s_ok && r < ntok) a.lam[(size_t)bh * a.T + t0 + r] = sum;
     }
-    __syncthreads();
-    if (tid < ntok) {
-      float s = 0.f;
-      for (int rr = 0; rr < TK_TILE; ++rr) s += tr[rr * TK_TILE + (tid ^ (rr & 31))];
-      a.lam[(size_t)bh * a.T + t0 + tid] = s;
-    }
+    tc_fence_before();
+    ok = __syncthreads_and(got) && s_ok;  // also: red and this accumulator are free again
+    if (!ok) break;
+  }
+  if constexpr (PASS == 0) {
+    const bool rv = ok && r < a.nq;
+    a.stats[((size_t)bh * a.nch + chunk) * TK_TILE + r] = rv ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
+  }
+  if (tid == 0) {  // after a failure: let the copies and MMAs in flight finish before the CTA releases its memory
+    for (int j = n_kdone; j < n_load; ++j) mbar_wait_bounded(smem_u32(&kfull[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
+    for (int j = n_mdone; j < n_mma; ++j) mbar_wait_bounded(smem_u32(&mdone[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 128);
+  if (warp == 0) tmem_dealloc(tmem, 2 * TK_TILE);
 }
 
-// per (sequence, KV head): (M, L) of every query row over the tiles
+// per (sequence, KV head): (M, L) of every query row over the chunks of tiles
 __global__ void __launch_bounds__(TK_TILE) token_merge_kernel(TokArgs a) {
   const int bh = blockIdx.x, r = threadIdx.x;
-  const float2* st = a.stats + (size_t)bh * a.nt * TK_TILE + r;
+  const float2* st = a.stats + (size_t)bh * a.nch * TK_TILE + r;
   float M = -INFINITY;
-  for (int t = 0; t < a.nt; ++t) M = fmaxf(M, st[(size_t)t * TK_TILE].x);
+  for (int t = 0; t < a.nch; ++t) M = fmaxf(M, st[(size_t)t * TK_TILE].x);
   float L = 0.f;
-  for (int t = 0; t < a.nt; ++t) {
+  for (int t = 0; t < a.nch; ++t) {
     const float2 s = st[(size_t)t * TK_TILE];
     if (s.x != -INFINITY) L += s.y * ex2_approx(s.x - M);
   }
@@ -385,12 +448,16 @@ kv_status launch_token_weights(const void* q_obs, int W, const void* k, int B, i
   a.g = Hq / Hkv;
   a.nq = a.g * W;
   a.nt = L.nt;
+  // about two CTAs per SM (shared memory admits two), each over a run of tiles of one (sequence, KV head)
+  const long long tiles = (long long)L.nt * Hkv * B, target = 2LL * sm_count(current_device());
+  a.tpc = (int)std::max(1LL, (tiles + target - 1) / target);
+  a.nch = (L.nt + a.tpc - 1) / a.tpc;
   a.qbox = (int)qbox;
   a.kbox = (int)kbox;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_ns = g_wait_limit_ns;
-  const uint32_t smem = 1024 + 4 * TC_BOX_BYTES;
-  const dim3 grid((unsigned)L.nt, (unsigned)Hkv, (unsigned)B);
+  const uint32_t smem = 1024 + 6 * TC_BOX_BYTES;
+  const dim3 grid((unsigned)a.nch, (unsigned)Hkv, (unsigned)B);
   cudaError_t e = ensure_dyn_smem((const void*)token_logits_kernel<0>, smem);
   if (e == cudaSuccess) e = ensure_dyn_smem((const void*)token_logits_kernel<1>, smem);
   if (e != cudaSuccess) {
