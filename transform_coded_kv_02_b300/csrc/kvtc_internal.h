@@ -128,10 +128,10 @@ CacheView dense_view(const kv_cache& c);
 // (dev: receives the current device, which holds the parameter table)
 kv_status check_decode_args(const kv_params* p, const kv_cache* c, const void* q, int B, int Hq,
                             const int32_t* seq_lens_dev, float softmax_scale, const float* out, int* dev);
-// token-axis allocation: weights workspace (per-tile and merged softmax statistics of the observation queries)
+// token-axis allocation: weights workspace (per-run softmax statistics of the observation queries)
 struct TokenLayout {
   int nt;  // 128-token tiles per (sequence, KV head)
-  size_t off_stats, off_ml, total;
+  size_t off_stats, total;
 };
 TokenLayout token_layout(int B, int Hkv, int64_t T);
 kv_status launch_token_weights(const void* q_obs, int W, const void* k, int B, int Hkv, int Hq, int64_t T,

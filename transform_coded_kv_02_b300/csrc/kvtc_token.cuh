@@ -12,13 +12,14 @@
 //                             SM: the g x W observation queries (M = 128 rows, zero rows past g W) arrive once by
 //                             TMA, the tiles' keys through two stages; one thread issues each tile's 8 tcgen05 MMAs
 //                             (K = 16 each) into one of two 128-column tensor-memory accumulators, so that the next
-//                             tile's MMAs and key copy run while this one is read back; each thread reads one
-//                             tensor-memory lane of 128 logits. Pass 0 (thread = query row) leaves each row's
-//                             maximum and sum of 2^(x - max) over the run. Pass 1 takes the transposed product (keys
-//                             as the MMA's A operand: thread = token) and sums p^2 = 2^(2 x - 2 (M + log2 L)) over
-//                             its row of query columns, with no exchange between threads. The exponentials use the hardware
-//                             approximation (relative error about 2^-22), as the decode's softmax does.
-//   token_merge_kernel        per (sequence, KV head) and query row: M and L over the tiles.
+//                             tile's MMAs and key copy run while this one is read back. Eight warps, two on each
+//                             quarter of the tensor-memory lanes, each thread reading 64 of its lane's 128 logits.
+//                             Pass 0 (lane = query row) leaves each row's maximum and sum of 2^(x - max) over the
+//                             run. Pass 1 first merges those runs into each row's M and L (every CTA for its own
+//                             sequence and KV head), then takes the transposed product (keys as the MMA's A operand:
+//                             lane = token) and sums p^2 = 2^(2 x - 2 (M + log2 L)) over the lane's query columns,
+//                             the two halves added through shared memory. The exponentials use the hardware approximation
+//                             (relative error about 2^-22), as the decode's softmax does.
 //   token_select_kernel       per (sequence, KV head): radix select of the keep-th largest weight (8 bits per
 //                             round over the weights' IEEE bits, keys held in shared memory up to 48K tokens),
 //                             then the kept tokens in index order by block scans (equal weights at the threshold:
@@ -30,12 +31,12 @@
 
 namespace kvtc {
 
-constexpr int TK_TILE = 128;        // keys per CTA and query rows per MMA
+constexpr int TK_TILE = 128;        // keys per tile and query rows per MMA
+constexpr int TK_THREADS = 256;     // two warps per tensor-memory lane quarter, each over half of the columns
 constexpr int SEL_THREADS = 1024;
 
 struct TokArgs {
   float2* stats;   // [B*Hkv][nch][128]: per run of tiles and query row, (max, sum of 2^(x - max)) over its tokens
-  float2* ml;      // [B*Hkv][128]:     (M, L) over all tiles
   float* lam;      // [B*Hkv][T]:       token weights
   long long T;
   int Hkv, Hq, W, g, nq, nt;
@@ -47,13 +48,14 @@ struct TokArgs {
 };
 
 template <int PASS>
-__global__ void __launch_bounds__(TK_TILE, 1)
+__global__ void __launch_bounds__(TK_THREADS, 2)
     token_logits_kernel(TokArgs a, const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t qfull, kfull[2], mdone[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_ok;
   __shared__ float cq[TK_TILE];  // pass 1: per query row, 2 (M + log2 L); +inf for rows without a query
+  __shared__ float2 part[TK_TILE];  // the upper column half's partial result per lane: pass 0 (m, l), pass 1 (sum, -)
   // the queries (two 64-column boxes), then two key stages of two boxes each
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -65,12 +67,40 @@ __global__ void __launch_bounds__(TK_TILE, 1)
     tmem_alloc(smem_u32(&s_tmem), 2 * TK_TILE);
     tmem_relinquish();
   }
-  if constexpr (PASS == 1) {
-    const float2 ML = a.ml[(size_t)bh * TK_TILE + tid];
-    cq[tid] = tid < a.nq && ML.y > 0.f ? 2.f * (ML.x + log2f(ML.y)) : INFINITY;
+  if constexpr (PASS == 1) {  // (M, L) of every query row over pass 0's runs: two threads a row, every other run
+    const int row = tid & (TK_TILE - 1), hh = tid >> 7;
+    const float2* st = a.stats + (size_t)bh * a.nch * TK_TILE + row;
+    float mm = -INFINITY, ll = 0.f;
+    for (int t0 = hh; t0 < a.nch; t0 += 16) {  // eight runs a batch: their loads are independent of one another
+      float2 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = t0 + 2 * k < a.nch ? st[(size_t)(t0 + 2 * k) * TK_TILE] : make_float2(-INFINITY, 0.f);
+      float mb = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mb = fmaxf(mb, v[k].x);
+      const float mn = fmaxf(mm, mb);
+      if (mn != -INFINITY) {
+        float lb = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lb += v[k].x == -INFINITY ? 0.f : v[k].y * ex2_approx(v[k].x - mn);
+        ll = (mm == -INFINITY ? 0.f : ll * ex2_approx(mm - mn)) + lb;
+        mm = mn;
+      }
+    }
+    if (hh) part[row] = make_float2(mm, ll);
+    __syncthreads();
+    if (!hh) {
+      const float2 o = part[row];
+      const float M = fmaxf(mm, o.x);
+      const float L = M == -INFINITY ? 0.f
+                                     : (mm == -INFINITY ? 0.f : ll * ex2_approx(mm - M)) +
+                                           (o.x == -INFINITY ? 0.f : o.y * ex2_approx(o.x - M));
+      cq[row] = row < a.nq && L > 0.f ? 2.f * (M + log2f(L)) : INFINITY;
+    }
   }
   if (a.qbox < TK_TILE) {  // query rows the box does not cover: zeros, so that their logits stay finite
-    for (int i = a.qbox * 8 + tid; i < TK_TILE * 8; i += TK_TILE)
+    for (int i = a.qbox * 8 + tid; i < TK_TILE * 8; i += TK_THREADS)
       for (int hf = 0; hf < 2; ++hf)
         *reinterpret_cast<uint4*>(smem_raw + (base - smem_u32(smem_raw)) + hf * TC_BOX_BYTES + i * 16) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
@@ -136,27 +166,33 @@ __global__ void __launch_bounds__(TK_TILE, 1)
     }
     issue_mma(0);
   }
-  const int r = 32 * warp + lane;  // tensor-memory lane: pass 0 the query row, pass 1 the tile's token
-  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-  const bool rows_here = PASS == 1 || 32 * warp < a.nq;  // pass 0: warps without a query row read nothing back
+  // tensor-memory lane quarter (warp % 4) and column half (warp / 4) of this warp; r = its lane: pass 0 the query
+  // row, pass 1 the tile's token
+  const int wq = warp & 3, half = warp >> 2;
+  const int r = 32 * wq + lane;
+  const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+  const int cbeg = 64 * half;
+  const bool rows_here = PASS == 1 || 32 * wq < a.nq;  // pass 0: warps without a query row read nothing back
   float m = -INFINITY, l = 0.f;  // pass 0: running maximum and sum of 2^(x - max) over this CTA's tokens
   const float two_s = 2.f * a.scale_log2;
   bool ok = true;
   for (int i = 0; i < ntl; ++i) {
     const int s = i & 1;
-    // the next tile's MMAs go out while this tile is read back (its accumulator was released at the end of the
-    // previous iteration)
-    if (tid == 0 && i + 1 < ntl) issue_mma(i + 1);
     const bool got = mbar_wait_bounded(smem_u32(&mdone[s]), (uint32_t)(i >> 1) & 1u, a.wait_ns);
-    if (tid == 0 && got && n_mdone == i) ++n_mdone;
     tc_fence_after();
-    // this tile's keys are consumed: the stage takes the tile after next
-    if (tid == 0 && got && s_ok && i + 2 < ntl) load_keys(i + 2);
+    if (tid == 0) {
+      if (got && n_mdone == i) ++n_mdone;
+      // this tile's keys are consumed: the stage takes the tile after next, before the wait for the next tile's
+      // keys, so that two copies are in flight; then the next tile's MMAs go out while this one is read back (its
+      // accumulator was released at the end of the previous iteration)
+      if (got && s_ok && i + 2 < ntl) load_keys(i + 2);
+      if (i + 1 < ntl) issue_mma(i + 1);
+    }
     const long long t0 = (long long)(tile0 + i) * TK_TILE;
     const int ntok = (int)min((long long)TK_TILE, a.T - t0);
     const uint32_t trow = tmem + lane_off + (uint32_t)(s * TK_TILE);
     if constexpr (PASS == 0) {  // row r's logits (base 2) against the tile's tokens, 32 columns at a time
-      for (int c0 = 0; c0 < ntok && rows_here; c0 += 32) {
+      for (int c0 = cbeg; c0 < cbeg + 64 && c0 < ntok && rows_here; c0 += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
         tmem_ld_wait();
@@ -164,48 +200,60 @@ __global__ void __launch_bounds__(TK_TILE, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * a.scale_log2;
         const int nc = min(32, ntok - c0);
-        float mc = -INFINITY, lc = 0.f;
-        if (nc == 32) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) mc = fmaxf(mc, x[j]);
-        } else {
+        if (nc < 32) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < nc) mc = fmaxf(mc, x[j]);
+            if (j >= nc) x[j] = -INFINITY;  // 2^-inf = 0
         }
-        const float mn = fmaxf(m, mc);
-        if (nc == 32) {
+        // the chunk's maximum as a tree and its sum in four partial sums: short dependency chains
+        float t[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) lc += ex2_approx(x[j] - mn);
-        } else {
+        for (int j = 0; j < 16; ++j) t[j] = fmaxf(x[j], x[j + 16]);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nc) lc += ex2_approx(x[j] - mn);
-        }
-        l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + lc;
+        for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+          for (int j = 0; j < o; ++j) t[j] = fmaxf(t[j], t[j + o]);
+        const float mn = fmaxf(m, t[0]);
+        float lc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 32; ++j) lc[j & 3] += ex2_approx(x[j] - mn);
+        l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + ((lc[0] + lc[1]) + (lc[2] + lc[3]));
         m = mn;
       }
     } else {  // token r's weight: sum over the query rows of p^2 = 2^(2 s x - 2 (M + log2 L))
-      float sum = 0.f;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
 #pragma unroll
-      for (int c0 = 0; c0 < TK_TILE; c0 += 32) {
+      for (int k = 0; k < 2; ++k) {
+        const int c0 = cbeg + 32 * k;
         if (c0 < a.nq) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sum += ex2_approx(fmaf(__uint_as_float(v[j]), two_s, -cq[c0 + j]));
+          for (int j = 0; j < 32; ++j) sum[j & 3] += ex2_approx(fmaf(__uint_as_float(v[j]), two_s, -cq[c0 + j]));
         }
       }
-      if (got && s_ok && r < ntok) a.lam[(size_t)bh * a.T + t0 + r] = sum;
+      const float sh = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      if (half) part[r].x = sh;
+      __syncthreads();
+      if (!half && got && s_ok && r < ntok) a.lam[(size_t)bh * a.T + t0 + r] = sh + part[r].x;
     }
     tc_fence_before();
     ok = __syncthreads_and(got) && s_ok;  // also: red and this accumulator are free again
     if (!ok) break;
   }
-  if constexpr (PASS == 0) {
-    const bool rv = ok && r < a.nq;
-    a.stats[((size_t)bh * a.nch + chunk) * TK_TILE + r] = rv ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
+  if constexpr (PASS == 0) {  // the two column halves' (m, l) of a row, then the run's statistics
+    if (half) part[r] = make_float2(m, l);
+    __syncthreads();
+    if (!half) {
+      const float2 o = part[r];
+      const float mm = fmaxf(m, o.x);
+      const float ll = mm == -INFINITY ? 0.f
+                                       : (m == -INFINITY ? 0.f : l * ex2_approx(m - mm)) +
+                                             (o.x == -INFINITY ? 0.f : o.y * ex2_approx(o.x - mm));
+      const bool rv = ok && r < a.nq;
+      a.stats[((size_t)bh * a.nch + chunk) * TK_TILE + r] = rv ? make_float2(mm, ll) : make_float2(-INFINITY, 0.f);
+    }
   }
   if (tid == 0) {  // after a failure: let the copies and MMAs in flight finish before the CTA releases its memory
     for (int j = n_kdone; j < n_load; ++j) mbar_wait_bounded(smem_u32(&kfull[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
@@ -215,20 +263,6 @@ __global__ void __launch_bounds__(TK_TILE, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, 2 * TK_TILE);
-}
-
-// per (sequence, KV head): (M, L) of every query row over the chunks of tiles
-__global__ void __launch_bounds__(TK_TILE) token_merge_kernel(TokArgs a) {
-  const int bh = blockIdx.x, r = threadIdx.x;
-  const float2* st = a.stats + (size_t)bh * a.nch * TK_TILE + r;
-  float M = -INFINITY;
-  for (int t = 0; t < a.nch; ++t) M = fmaxf(M, st[(size_t)t * TK_TILE].x);
-  float L = 0.f;
-  for (int t = 0; t < a.nch; ++t) {
-    const float2 s = st[(size_t)t * TK_TILE];
-    if (s.x != -INFINITY) L += s.y * ex2_approx(s.x - M);
-  }
-  a.ml[(size_t)bh * TK_TILE + r] = make_float2(M, L);
 }
 
 // Exclusive sum over the warps of a per-warp value (every lane of warp w passes the same v): the sum of the warps
@@ -420,8 +454,7 @@ TokenLayout token_layout(int B, int Hkv, int64_t T) {
   L.nt = (int)((T + TK_TILE - 1) / TK_TILE);
   const size_t bh = (size_t)B * Hkv;
   L.off_stats = 0;
-  L.off_ml = align256(bh * L.nt * TK_TILE * sizeof(float2));
-  L.total = align256(L.off_ml + bh * TK_TILE * sizeof(float2));
+  L.total = align256(bh * L.nt * TK_TILE * sizeof(float2));
   return L;
 }
 
@@ -439,7 +472,6 @@ kv_status launch_token_weights(const void* q_obs, int W, const void* k, int B, i
   TokArgs a;
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.stats = reinterpret_cast<float2*>(w + L.off_stats);
-  a.ml = reinterpret_cast<float2*>(w + L.off_ml);
   a.lam = lam;
   a.T = T;
   a.Hkv = Hkv;
@@ -464,9 +496,8 @@ kv_status launch_token_weights(const void* q_obs, int W, const void* k, int B, i
     set_error("token_logits_kernel shared memory: %s", cudaGetErrorString(e));
     return KV_ERR_CUDA;
   }
-  token_logits_kernel<0><<<grid, TK_TILE, smem, s>>>(a, maps[0], maps[1]);
-  token_merge_kernel<<<B * Hkv, TK_TILE, 0, s>>>(a);
-  token_logits_kernel<1><<<grid, TK_TILE, smem, s>>>(a, maps[0], maps[1]);
+  token_logits_kernel<0><<<grid, TK_THREADS, smem, s>>>(a, maps[0], maps[1]);
+  token_logits_kernel<1><<<grid, TK_THREADS, smem, s>>>(a, maps[0], maps[1]);
   return launch_check("token weight kernels");
 }
 
