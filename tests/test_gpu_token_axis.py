@@ -71,24 +71,42 @@ def test_token_weights_match_oracle(name, W, T):
     assert np.all(s >= nq / T * (1 - 1e-5)) and np.all(s <= nq * (1 + 1e-5))
 
 
-@pytest.mark.parametrize("T,keeps", [(1, [0, 1]), (5, [1, 2, 5]), (1000, [1, 333, 999, 1000]),
-                                     (5000, [2500, 1]), (60000, [15000, 59999])])
-def test_token_select_matches_oracle(T, keeps):
-    """Seeded weights with many exact ties and zeros: the kept set equals the oracle's, index for index (up to
-    48K tokens the keys sit in shared memory; the 60000-token case rereads them from global memory)."""
+def _select_inputs(B, Hkv, T):
     rng = np.random.default_rng(T)
-    B, Hkv = 2, 3
     lam = rng.choice(np.array([0.0, 1e-3, 0.25, 0.5, 0.5, 1.0, 7.0], np.float32), size=(B, Hkv, T))
-    lam[0, 1] = rng.random(T).astype(np.float32)  # one row without ties
+    lam[0, min(1, Hkv - 1)] = rng.random(T).astype(np.float32)  # one row without ties
+    return lam
+
+
+def _check_select(lam, keeps):
+    B, Hkv, T = lam.shape
     lam_dev = torch.from_numpy(lam).to(G.DEV)
     for keep in keeps:
         idx = torch.full((B, Hkv, max(keep, 1)), -7, dtype=torch.int32, device=G.DEV)
         kvtc.kv_token_select(lam_dev, B, Hkv, T, keep, idx)
+        assert kvtc.kv_check_status() == kvtc.KV_OK, kvtc.kv_last_error()
         got = idx.cpu().numpy()
         for b in range(B):
             for h in range(Hkv):
                 want = O.token_keep(lam[b, h].astype(np.float64), keep)
                 assert np.array_equal(got[b, h, :keep], want), (b, h, keep)
+
+
+@pytest.mark.parametrize("T,keeps", [(1, [0, 1]), (5, [1, 2, 5]), (1000, [1, 333, 999, 1000]),
+                                     (5000, [2500, 1]), (60000, [15000, 59999])])
+def test_token_select_matches_oracle(T, keeps):
+    """Seeded weights with many exact ties and zeros: the kept set equals the oracle's, index for index. Six rows
+    take clusters of 8 CTAs on 148 SMs, so the CTAs hold from nothing (1 and 5 tokens) to 7500 tokens each."""
+    _check_select(_select_inputs(2, 3, T), keeps)
+
+
+@pytest.mark.parametrize("B,Hkv,T,keeps", [(5, 8, 3000, [1, 1500, 2999]), (20, 8, 700, [350, 699]),
+                                           (1, 1, 400000, [100000, 1])])
+def test_token_select_cluster_sizes(B, Hkv, T, keeps):
+    """The cluster per (sequence, KV head) is sized to the SMs: on 148 SMs 40 rows take clusters of 2 CTAs and 160
+    rows single CTAs; one row of 400000 tokens takes 8 CTAs of 50000 tokens, more than shared memory holds, so
+    every pass rereads the weights from global memory."""
+    _check_select(_select_inputs(B, Hkv, T), keeps)
 
 
 def _keep_at_gap(lam_rows, target, rel=1e-3):

@@ -20,10 +20,11 @@
 //                             lane = token) and sums p^2 = 2^(2 x - 2 (M + log2 L)) over the lane's query columns,
 //                             the two halves added through shared memory. The exponentials use the hardware approximation
 //                             (relative error about 2^-22), as the decode's softmax does.
-//   token_select_kernel       per (sequence, KV head): radix select of the keep-th largest weight (8 bits per
-//                             round over the weights' IEEE bits, keys held in shared memory up to 48K tokens),
-//                             then the kept tokens in index order by block scans (equal weights at the threshold:
-//                             the earlier tokens).
+//   token_select_kernel       per (sequence, KV head), a cluster of up to 8 CTAs: radix select of the keep-th
+//                             largest weight (8 bits per round over the weights' IEEE bits, the CTAs' histograms
+//                             summed through distributed shared memory, keys held in shared memory up to 48K tokens
+//                             per CTA), then the kept tokens in index order by scans over the CTAs and their warps
+//                             (equal weights at the threshold: the earlier tokens).
 //   compact_kernel            the kept records copied in order; value tokens re-paired two per record.
 #pragma once
 
@@ -286,63 +287,80 @@ __device__ __forceinline__ unsigned block_warp_excl_sum(unsigned v, unsigned* ws
   return warp ? wsum[warp - 1] : 0u;
 }
 
-// Per (sequence, KV head): the keep tokens of largest weight, ascending. A weight's rank key is its IEEE bit pattern
-// (monotone for non-negative floats); zero, negative and NaN weights rank lowest. Warp w owns the contiguous token
-// range [w C, (w + 1) C) and walks it 32 tokens at a time (lane = token). With KEYS_SMEM the keys are read from
-// global memory once and kept in dynamic shared memory (T <= SEL_SMEM_KEYS); otherwise every pass rereads the
-// weights. Radix select, 8 bits a round: each warp counts into its own histogram (shared-memory atomics), the
-// warps' histograms are summed per digit. Output: each warp counts its kept tokens (ballots), one
-// exclusive sum over the warps gives its first output slot and its share of the keys equal to the threshold (the
-// earliest ones), and the warp writes its tokens in order.
+// Per (sequence, KV head): the keep tokens of largest weight, ascending, found by a cluster of cs CTAs (1, 2, 4 or 8:
+// as many as leave every CTA an SM of its own). A weight's rank key is its IEEE bit pattern (monotone for
+// non-negative floats); zero, negative and NaN weights rank lowest. CTA c of the cluster owns the token range
+// [c Tc, (c + 1) Tc) and its warp w the contiguous sub-range [w C, (w + 1) C), walked 32 tokens at a time (lane =
+// token). With KEYS_SMEM the CTA's keys are read from global memory once and kept in dynamic shared memory
+// (Tc <= SEL_SMEM_KEYS); otherwise every pass rereads the weights. Radix select, 8 bits a round: each warp counts
+// into its own histogram (shared-memory atomics), the CTA sums its warps' histograms per digit, and every CTA sums
+// the cluster's CTA histograms through distributed shared memory, so that all of them take the same digit. Output:
+// each warp counts its kept tokens (ballots); the CTAs publish their counts above and at the threshold, which gives
+// each CTA its first output slot and its share of the keys equal to the threshold (the earliest ones); one exclusive
+// sum over the CTA's warps does the same per warp, and each warp writes its tokens in order.
 constexpr int SEL_SMEM_KEYS = 48 * 1024;
+constexpr int SEL_MAX_CLUSTER = 8;
 template <bool KEYS_SMEM>
-__global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* lam, long long T, int keep, int32_t* idx) {
+__global__ void __launch_bounds__(SEL_THREADS, 1) token_select_kernel(const float* lam, int T, int keep, int cs, int32_t* idx) {
   extern __shared__ unsigned keys_s[];
   __shared__ unsigned hist[SEL_THREADS / 32][256];
+  __shared__ unsigned cta_hist[256];  // this CTA's count per digit, read by the whole cluster
   __shared__ unsigned wsum[32];
   __shared__ unsigned s_prefix, s_remaining;
-  const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ unsigned s_cnt[2];   // this CTA's keys above the threshold and equal to it, read by the later CTAs
+  __shared__ unsigned s_base[2];  // keys equal to the threshold and output slots before this CTA
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int crank = (int)cluster_ctarank(), bh = (int)(blockIdx.x / (unsigned)cs);
   const float* lm = lam + (size_t)bh * T;
   int32_t* out = idx + (size_t)bh * keep;
   constexpr int NWS = SEL_THREADS / 32;
-  const long long C = ((T + NWS - 1) / NWS + 31) / 32 * 32;  // tokens per warp, whole 32-token chunks
-  const long long w0 = min(T, (long long)warp * C), w1 = min(T, w0 + C);
-  auto key_global = [&](long long t) {
-    const float v = lm[t];
+  const long long Tc = ((long long)T + cs - 1) / cs;
+  const int c0 = (int)min((long long)T, crank * Tc);
+  const int n = (int)min((long long)T, c0 + Tc) - c0;                          // this CTA's tokens
+  const long long C = (((long long)n + NWS - 1) / NWS + 31) / 32 * 32;         // per warp, whole 32-token chunks
+  const int w0 = (int)min((long long)n, warp * C), w1 = (int)min((long long)n, w0 + C);
+  auto key_global = [&](int i) {
+    const float v = lm[c0 + i];
     return v > 0.f ? __float_as_uint(v) : 0u;
   };
   if constexpr (KEYS_SMEM) {
-    for (long long t = tid; t < T; t += SEL_THREADS) keys_s[t] = key_global(t);
+    for (int i = tid; i < n; i += SEL_THREADS) keys_s[i] = key_global(i);
     __syncthreads();
   }
-  auto key_of = [&](long long t) {
-    if constexpr (KEYS_SMEM) return keys_s[t];
-    else return key_global(t);
+  auto key_of = [&](int i) {
+    if constexpr (KEYS_SMEM) return keys_s[i];
+    else return key_global(i);
   };
   // radix select of the keep-th largest key, eight bits per round
   unsigned prefix = 0u, mask = 0u, remaining = (unsigned)keep;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = lane; i < 256; i += 32) hist[warp][i] = 0u;
     __syncwarp();
-    for (long long c0 = w0; c0 < w1; c0 += 32) {
-      const long long t = c0 + lane;
-      const unsigned k = t < w1 ? key_of(t) : 0u;
-      const bool in = t < w1 && (k & mask) == prefix;
-      if (in) atomicAdd(&hist[warp][(k >> shift) & 255u], 1u);
+    for (int b0 = w0; b0 < w1; b0 += 32) {
+      const int i = b0 + lane;
+      const unsigned k = i < w1 ? key_of(i) : 0u;
+      if (i < w1 && (k & mask) == prefix) atomicAdd(&hist[warp][(k >> shift) & 255u], 1u);
     }
     __syncthreads();
-    // digit totals over the warps, then the count of keys at or above each digit (threads 0..255 take the digits in
-    // descending order: an inclusive scan over them); the one digit where the count first reaches `remaining` is
-    // the next 8 bits of the threshold
+    if (tid < 256) {
+      unsigned c = 0u;
+#pragma unroll 8
+      for (int w = 0; w < NWS; ++w) c += hist[w][tid];
+      cta_hist[tid] = c;
+    }
+    cluster_sync_all();  // every CTA's digit counts are in place
+    // digit totals over the cluster, then the count of keys at or above each digit (threads 0..255 take the digits
+    // in descending order: an inclusive scan over them); the one digit where the count first reaches `remaining`
+    // is the next 8 bits of the threshold
     unsigned dv = 0u, dx = 0u;
     if (tid < 256) {
-#pragma unroll 8
-      for (int w = 0; w < NWS; ++w) dv += hist[w][255 - tid];
+      const uint32_t a0 = smem_u32(&cta_hist[255 - tid]);
+      for (int c = 0; c < cs; ++c) dv += ld_dsmem_u32(dsmem_addr(a0, (uint32_t)c));
       dx = dv;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const unsigned n = __shfl_up_sync(0xffffffffu, dx, o);
-        if (lane >= o) dx += n;
+        const unsigned nb = __shfl_up_sync(0xffffffffu, dx, o);
+        if (lane >= o) dx += nb;
       }
       if (lane == 31) wsum[warp] = dx;
     }
@@ -360,33 +378,55 @@ __global__ void __launch_bounds__(SEL_THREADS) token_select_kernel(const float* 
     prefix = s_prefix;
     remaining = s_remaining;
     mask |= 255u << shift;
+    cluster_sync_all();  // the cluster has read this round's counts before the next round rewrites them
   }
   // prefix: the threshold key; every larger key is kept, and the first `remaining` keys equal to it
   unsigned n_gt = 0u, n_eq = 0u;
-  for (long long c0 = w0; c0 < w1; c0 += 32) {
-    const long long t = c0 + lane;
-    const unsigned k = t < w1 ? key_of(t) : 0u;
-    n_gt += __popc(__ballot_sync(0xffffffffu, t < w1 && k > prefix));
-    n_eq += __popc(__ballot_sync(0xffffffffu, t < w1 && k == prefix));
+  for (int b0 = w0; b0 < w1; b0 += 32) {
+    const int i = b0 + lane;
+    const unsigned k = i < w1 ? key_of(i) : 0u;
+    n_gt += __popc(__ballot_sync(0xffffffffu, i < w1 && k > prefix));
+    n_eq += __popc(__ballot_sync(0xffffffffu, i < w1 && k == prefix));
   }
-  unsigned tot;
-  const unsigned eq_before = block_warp_excl_sum(n_eq, wsum, tot);
+  unsigned gt_tot, eq_tot;
+  const unsigned eq_before_w = block_warp_excl_sum(n_eq, wsum, eq_tot);
+  block_warp_excl_sum(n_gt, wsum, gt_tot);
+  if (tid == 0) {
+    s_cnt[0] = gt_tot;
+    s_cnt[1] = eq_tot;
+  }
+  cluster_sync_all();
+  if (tid == 0) {
+    unsigned eqb = 0u, slots = 0u;
+    for (int c = 0; c < crank; ++c) {
+      const unsigned g = ld_dsmem_u32(dsmem_addr(smem_u32(&s_cnt[0]), (uint32_t)c));
+      const unsigned e = ld_dsmem_u32(dsmem_addr(smem_u32(&s_cnt[1]), (uint32_t)c));
+      slots += g + (eqb >= remaining ? 0u : min(e, remaining - eqb));
+      eqb += e;
+    }
+    s_base[0] = eqb;
+    s_base[1] = slots;
+  }
+  __syncthreads();
+  const unsigned eq_before = s_base[0] + eq_before_w;
   const unsigned eq_take = eq_before >= remaining ? 0u : min(n_eq, remaining - eq_before);
-  unsigned pos = block_warp_excl_sum(n_gt + eq_take, wsum, tot);
+  unsigned tot;
+  unsigned pos = s_base[1] + block_warp_excl_sum(n_gt + eq_take, wsum, tot);
   unsigned eq_used = 0u;
   const unsigned lt = (1u << lane) - 1u;
-  for (long long c0 = w0; c0 < w1; c0 += 32) {
-    const long long t = c0 + lane;
-    const unsigned k = t < w1 ? key_of(t) : 0u;
-    const bool gt = t < w1 && k > prefix, eq = t < w1 && k == prefix;
+  for (int b0 = w0; b0 < w1; b0 += 32) {
+    const int i = b0 + lane;
+    const unsigned k = i < w1 ? key_of(i) : 0u;
+    const bool gt = i < w1 && k > prefix, eq = i < w1 && k == prefix;
     const unsigned beq = __ballot_sync(0xffffffffu, eq);
     const bool sel = gt || (eq && eq_used + __popc(beq & lt) < eq_take);
     const unsigned bsel = __ballot_sync(0xffffffffu, sel);
     const unsigned p = pos + __popc(bsel & lt);
-    if (sel && p < (unsigned)keep) out[p] = (int32_t)t;
+    if (sel && p < (unsigned)keep) out[p] = c0 + i;
     pos += __popc(bsel);
     eq_used += __popc(beq);
   }
+  cluster_sync_all();  // the later CTAs have read this CTA's counts before it exits
 }
 
 struct CompactArgs {
@@ -503,16 +543,38 @@ kv_status launch_token_weights(const void* q_obs, int W, const void* k, int B, i
 
 kv_status launch_token_select(const float* lam, int B, int Hkv, int64_t T, int64_t keep, int32_t* idx,
                               cudaStream_t s) {
-  if (T <= SEL_SMEM_KEYS) {
-    const size_t smem = (size_t)T * 4;
+  // one cluster per (sequence, KV head), as many CTAs (of a whole SM each) as the SMs hold for all of them at once
+  const long long bh = (long long)B * Hkv;
+  const int sms = sm_count(current_device());
+  int cs = 1;
+  while (cs < SEL_MAX_CLUSTER && bh * cs * 2 <= sms) cs *= 2;
+  const long long Tc = (T + cs - 1) / cs;
+  const bool in_smem = Tc <= SEL_SMEM_KEYS;
+  const size_t smem = in_smem ? (size_t)Tc * 4 : 0;
+  if (in_smem) {
     const cudaError_t e = ensure_dyn_smem((const void*)token_select_kernel<true>, smem);
     if (e != cudaSuccess) {
       set_error("token_select_kernel shared memory: %s", cudaGetErrorString(e));
       return KV_ERR_CUDA;
     }
-    token_select_kernel<true><<<B * Hkv, SEL_THREADS, smem, s>>>(lam, T, (int)keep, idx);
-  } else {
-    token_select_kernel<false><<<B * Hkv, SEL_THREADS, 0, s>>>(lam, T, (int)keep, idx);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(bh * cs), 1, 1);
+  cfg.blockDim = dim3(SEL_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)cs;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = in_smem ? cudaLaunchKernelEx(&cfg, token_select_kernel<true>, lam, (int)T, (int)keep, cs, idx)
+                                : cudaLaunchKernelEx(&cfg, token_select_kernel<false>, lam, (int)T, (int)keep, cs, idx);
+  if (e != cudaSuccess) {
+    set_error("token_select_kernel launch: %s", cudaGetErrorString(e));
+    return KV_ERR_CUDA;
   }
   return launch_check("token_select_kernel");
 }
