@@ -334,7 +334,8 @@ kv_status kv_token_select(const float* weights, int B, int Hkv, int64_t T, int64
 /* Compaction: token i < keep of (b, h) in dst becomes token keep_idx[b][h][i] of src (records copied; value tokens
  * re-paired two per record, a missing second token's halves 0). src and dst: distinct dense caches of this
  * table's record lengths with the same Hkv; keep <= dst T_cap; indices outside src's T_cap are skipped and
- * reported as KV_ERR_DEVICE. */
+ * reported as KV_ERR_DEVICE. KV_ERR_UNSUPPORTED when B * Hkv > 65535 or one head's kept records exceed 2^31 - 256
+ * words. */
 kv_status kv_cache_compact(const kv_params* p, const kv_cache* src, const kv_cache* dst, int B,
                            const int32_t* keep_idx, int64_t keep, kv_stream_t stream);
 

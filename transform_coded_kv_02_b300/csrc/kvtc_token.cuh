@@ -343,10 +343,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) token_select_kernel(const floa
     }
     __syncthreads();
     if (tid < 256) {
-      unsigned c = 0u;
-#pragma unroll 8
-      for (int w = 0; w < NWS; ++w) c += hist[w][tid];
-      cta_hist[tid] = c;
+      unsigned c[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int w = 0; w < NWS; ++w) c[w & 3] += hist[w][tid];
+      cta_hist[tid] = (c[0] + c[1]) + (c[2] + c[3]);
     }
     cluster_sync_all();  // every CTA's digit counts are in place
     // digit totals over the cluster, then the count of keys at or above each digit (threads 0..255 take the digits
@@ -355,7 +355,11 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) token_select_kernel(const floa
     unsigned dv = 0u, dx = 0u;
     if (tid < 256) {
       const uint32_t a0 = smem_u32(&cta_hist[255 - tid]);
-      for (int c = 0; c < cs; ++c) dv += ld_dsmem_u32(dsmem_addr(a0, (uint32_t)c));
+      unsigned pc[SEL_MAX_CLUSTER];  // the cluster's loads issued together
+#pragma unroll
+      for (int c = 0; c < SEL_MAX_CLUSTER; ++c) pc[c] = c < cs ? ld_dsmem_u32(dsmem_addr(a0, (uint32_t)c)) : 0u;
+#pragma unroll
+      for (int c = 0; c < SEL_MAX_CLUSTER; ++c) dv += pc[c];
       dx = dv;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -437,12 +441,9 @@ struct CompactArgs {
   int keep, Rk, Rv, BH;
 };
 
-// keys: thread per (sequence-head, kept token, record word)
-__device__ __forceinline__ void compact_key_word(const CompactArgs& a, long long g) {
-  const long long per = (long long)a.keep * a.Rk;
-  const int bh = (int)(g / per);
-  const long long r = g - (long long)bh * per;
-  const int i = (int)(r / a.Rk), w = (int)(r - (long long)i * a.Rk);
+// keys: thread per (sequence-head, kept token, record word); r = kept token * Rk + word
+__device__ __forceinline__ void compact_key_word(const CompactArgs& a, int bh, int r) {
+  const int i = r / a.Rk, w = r - i * a.Rk;
   const int t = a.idx[(size_t)bh * a.keep + i];
   if (t < 0 || t >= a.Ts) {
     atomicOr(&g_status, ST_BAD_INDEX);
@@ -453,12 +454,10 @@ __device__ __forceinline__ void compact_key_word(const CompactArgs& a, long long
 
 // values: thread per (sequence-head, destination record, record word); kept tokens 2j and 2j + 1 form record j, each
 // bringing its z/s word and its 16-bit half of every code word from the record that held it
-__device__ __forceinline__ void compact_value_word(const CompactArgs& a, long long g) {
-  const int W = 2 * a.Rv, nrec = (a.keep + 1) / 2;
-  const long long per = (long long)nrec * W;
-  const int bh = (int)(g / per);
-  const long long r = g - (long long)bh * per;
-  const int j = (int)(r / W), w = (int)(r - (long long)j * W);
+// r = destination record * 2 Rv + word
+__device__ __forceinline__ void compact_value_word(const CompactArgs& a, int bh, int r) {
+  const int W = 2 * a.Rv;
+  const int j = r / W, w = r - j * W;
   const int32_t* id = a.idx + (size_t)bh * a.keep;
   const int t0 = id[2 * j], t1 = 2 * j + 1 < a.keep ? id[2 * j + 1] : -1;
   if (t0 < 0 || t0 >= a.Ts || (2 * j + 1 < a.keep && (t1 < 0 || t1 >= a.Ts))) {
@@ -479,13 +478,15 @@ __device__ __forceinline__ void compact_value_word(const CompactArgs& a, long lo
   a.dst[1][((size_t)bh * (a.Td / 2) + (size_t)j) * W + w] = v;
 }
 
-// one launch: threads [0, nk) copy key words, the rest value words
-__global__ void compact_kernel(CompactArgs a, long long nk, long long nv) {
-  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (g < nk)
-    compact_key_word(a, g);
-  else if (g < nk + nv)
-    compact_value_word(a, g - nk);
+// one launch: blockIdx.y = sequence-head, blockIdx.z = 0 for the key words (keep * Rk of them), 1 for the value
+// words ((keep + 1) / 2 records of 2 Rv words)
+__global__ void compact_kernel(CompactArgs a) {
+  const int r = (int)(blockIdx.x * blockDim.x + threadIdx.x), bh = (int)blockIdx.y;
+  if (blockIdx.z == 0) {
+    if (r < a.keep * a.Rk) compact_key_word(a, bh, r);
+  } else if (r < (a.keep + 1) / 2 * 2 * a.Rv) {
+    compact_value_word(a, bh, r);
+  }
 }
 
 // ---- host side --------------------------------------------------------------------------------------------
@@ -593,8 +594,13 @@ kv_status launch_compact(const ParamsDev& P, const kv_cache& src, const kv_cache
   a.Rk = P.t[0].r_words;
   a.Rv = P.t[1].r_words;
   a.BH = B * src.Hkv;
-  const long long nk = (long long)a.BH * keep * a.Rk, nv = (long long)a.BH * ((keep + 1) / 2) * 2 * a.Rv;
-  compact_kernel<<<(unsigned)((nk + nv + 255) / 256), 256, 0, s>>>(a, nk, nv);
+  const long long per = std::max((long long)keep * a.Rk, (keep + 1) / 2 * 2LL * a.Rv);  // words per head
+  if (per == 0) return KV_OK;
+  if (per >= (1LL << 31) - 256 || a.BH > 65535) {
+    set_error("compaction: %lld record words per head or %d sequence-heads beyond the launch's range", per, a.BH);
+    return KV_ERR_UNSUPPORTED;
+  }
+  compact_kernel<<<dim3((unsigned)((per + 255) / 256), (unsigned)a.BH, 2), 256, 0, s>>>(a);
   return launch_check("compact_kernel");
 }
 
