@@ -18,8 +18,8 @@
 //                             run. Pass 1 first merges those runs into each row's M and L (every CTA for its own
 //                             sequence and KV head), then takes the transposed product (keys as the MMA's A operand:
 //                             lane = token) and sums p^2 = 2^(2 x - 2 (M + log2 L)) over the lane's query columns,
-//                             the two halves added through shared memory. The exponentials use the hardware approximation
-//                             (relative error about 2^-22), as the decode's softmax does.
+//                             the two halves added through shared memory. The exponentials use the hardware
+//                             approximation (relative error about 2^-22), as the decode's softmax does.
 //   token_select_kernel       per (sequence, KV head), a cluster of up to 8 CTAs: radix select of the keep-th
 //                             largest weight (8 bits per round over the weights' IEEE bits, the CTAs' histograms
 //                             summed through distributed shared memory, keys held in shared memory up to 48K tokens
@@ -42,8 +42,8 @@ struct TokArgs {
   long long T;
   int Hkv, Hq, W, g, nq, nt;
   int tpc, nch;      // tiles per CTA, and the CTAs (runs of tiles) per (sequence, KV head): ceil(nt / tpc)
-  int qbox, kbox;    // rows of the query and key boxes: 128, or all rows of a smaller tensor (the operand rows past
-                     // them are stale and masked)
+  int qbox, kbox;    // rows of the query and key boxes: 128, or all rows of a smaller tensor (query rows past qbox
+                     // are zeroed in shared memory; key rows past kbox are stale and masked)
   float scale_log2;  // softmax scale * log2(e): logits in base 2
   long long wait_ns;
 };
@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
   if (a.qbox < TK_TILE) {  // query rows the box does not cover: zeros, so that their logits stay finite
     for (int i = a.qbox * 8 + tid; i < TK_TILE * 8; i += TK_THREADS)
       for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<uint4*>(smem_raw + (base - smem_u32(smem_raw)) + hf * TC_BOX_BYTES + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem_raw + (base - smem_u32(smem_raw)) + hf * TC_BOX_BYTES + i * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
   if (tid == 0) {
@@ -257,8 +258,10 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
     }
   }
   if (tid == 0) {  // after a failure: let the copies and MMAs in flight finish before the CTA releases its memory
-    for (int j = n_kdone; j < n_load; ++j) mbar_wait_bounded(smem_u32(&kfull[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
-    for (int j = n_mdone; j < n_mma; ++j) mbar_wait_bounded(smem_u32(&mdone[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
+    for (int j = n_kdone; j < n_load; ++j)
+      mbar_wait_bounded(smem_u32(&kfull[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
+    for (int j = n_mdone; j < n_mma; ++j)
+      mbar_wait_bounded(smem_u32(&mdone[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -301,7 +304,8 @@ __device__ __forceinline__ unsigned block_warp_excl_sum(unsigned v, unsigned* ws
 constexpr int SEL_SMEM_KEYS = 48 * 1024;
 constexpr int SEL_MAX_CLUSTER = 8;
 template <bool KEYS_SMEM>
-__global__ void __launch_bounds__(SEL_THREADS, 1) token_select_kernel(const float* lam, int T, int keep, int cs, int32_t* idx) {
+__global__ void __launch_bounds__(SEL_THREADS, 1)
+    token_select_kernel(const float* lam, int T, int keep, int cs, int32_t* idx) {
   extern __shared__ unsigned keys_s[];
   __shared__ unsigned hist[SEL_THREADS / 32][256];
   __shared__ unsigned cta_hist[256];  // this CTA's count per digit, read by the whole cluster
