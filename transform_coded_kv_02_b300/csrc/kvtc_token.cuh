@@ -32,6 +32,13 @@
 
 namespace kvtc {
 
+// 32-bit load from a peer CTA's shared memory (an address from dsmem_addr)
+__device__ __forceinline__ unsigned ld_dsmem_u32(uint32_t addr) {
+  unsigned v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 constexpr int TK_TILE = 128;        // keys per tile and query rows per MMA
 constexpr int TK_THREADS = 256;     // two warps per tensor-memory lane quarter, each over half of the columns
 constexpr int SEL_THREADS = 1024;
