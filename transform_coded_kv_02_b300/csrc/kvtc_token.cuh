@@ -41,7 +41,8 @@ __device__ __forceinline__ unsigned ld_dsmem_u32(uint32_t addr) {
 
 constexpr int TK_TILE = 128;        // keys per tile and query rows per MMA
 constexpr int TK_THREADS = 256;     // two warps per tensor-memory lane quarter, each over half of the columns
-constexpr int SEL_THREADS = 1024;
+constexpr int SEL_THREADS = 256;  // the selection: one thread per radix digit
+static_assert(SEL_THREADS == 256, "the selection kernel gives each thread one 8-bit digit");
 
 struct TokArgs {
   float2* stats;   // [B*Hkv][nch][128]: per run of tiles and query row, (max, sum of 2^(x - max)) over its tokens
@@ -277,14 +278,14 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 }
 
 // Exclusive sum over the warps of a per-warp value (every lane of warp w passes the same v): the sum of the warps
-// before this one, and the block's total (every thread).
+// before this one, and the block's total (every thread). Up to 32 warps.
 __device__ __forceinline__ unsigned block_warp_excl_sum(unsigned v, unsigned* wsum, unsigned& total) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)(blockDim.x >> 5);
   __syncthreads();  // the previous call's readers are done with wsum
   if (lane == 0) wsum[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    unsigned x = wsum[lane];
+    unsigned x = lane < nw ? wsum[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const unsigned n = __shfl_up_sync(0xffffffffu, x, o);
@@ -293,7 +294,7 @@ __device__ __forceinline__ unsigned block_warp_excl_sum(unsigned v, unsigned* ws
     wsum[lane] = x;  // inclusive over the warps
   }
   __syncthreads();
-  total = wsum[31];
+  total = wsum[nw - 1];
   return warp ? wsum[warp - 1] : 0u;
 }
 
