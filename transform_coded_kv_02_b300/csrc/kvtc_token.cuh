@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     token_select_kernel(const float* lam, int T, int keep, int cs, int32_t* idx) {
   extern __shared__ unsigned keys_s[];
   __shared__ unsigned hist[SEL_THREADS / 32][256];
-  __shared__ unsigned cta_hist[256];  // this CTA's count per digit, read by the whole cluster
+  // this CTA's count per digit, read by the whole cluster; by round parity, so that a round's counts are written
+  // while the previous round's may still be read (a peer reads round r's before it arrives at round r + 1's cluster
+  // barrier, which every CTA passes before it writes round r + 2's)
+  __shared__ unsigned cta_hist[2][256];
   __shared__ unsigned wsum[32];
   __shared__ unsigned s_prefix, s_remaining;
   __shared__ unsigned s_cnt[2];   // this CTA's keys above the threshold and equal to it, read by the later CTAs
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   // radix select of the keep-th largest key, eight bits per round
   unsigned prefix = 0u, mask = 0u, remaining = (unsigned)keep;
   for (int shift = 24; shift >= 0; shift -= 8) {
+    unsigned* const ch = cta_hist[(shift >> 3) & 1];
     for (int i = lane; i < 256; i += 32) hist[warp][i] = 0u;
     __syncwarp();
     for (int b0 = w0; b0 < w1; b0 += 32) {
@@ -358,7 +362,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       unsigned c[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int w = 0; w < NWS; ++w) c[w & 3] += hist[w][tid];
-      cta_hist[tid] = (c[0] + c[1]) + (c[2] + c[3]);
+      ch[tid] = (c[0] + c[1]) + (c[2] + c[3]);
     }
     cluster_sync_all();  // every CTA's digit counts are in place
     // digit totals over the cluster, then the count of keys at or above each digit (threads 0..255 take the digits
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     // is the next 8 bits of the threshold
     unsigned dv = 0u, dx = 0u;
     if (tid < 256) {
-      const uint32_t a0 = smem_u32(&cta_hist[255 - tid]);
+      const uint32_t a0 = smem_u32(&ch[255 - tid]);
       unsigned pc[SEL_MAX_CLUSTER];  // the cluster's loads issued together
 #pragma unroll
       for (int c = 0; c < SEL_MAX_CLUSTER; ++c) pc[c] = c < cs ? ld_dsmem_u32(dsmem_addr(a0, (uint32_t)c)) : 0u;
@@ -394,7 +398,6 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     prefix = s_prefix;
     remaining = s_remaining;
     mask |= 255u << shift;
-    cluster_sync_all();  // the cluster has read this round's counts before the next round rewrites them
   }
   // prefix: the threshold key; every larger key is kept, and the first `remaining` keys equal to it
   unsigned n_gt = 0u, n_eq = 0u;
