@@ -10,10 +10,12 @@
 //
 //   token_logits_kernel<0|1>  one CTA per run of 128-token tiles of one (sequence, KV head), about two CTAs per
 //                             SM: the g x W observation queries (M = 128 rows, zero rows past g W) arrive once by
-//                             TMA, the tiles' keys through two stages; one thread issues each tile's 8 tcgen05 MMAs
-//                             (K = 16 each) into one of two 128-column tensor-memory accumulators, so that the next
-//                             tile's MMAs and key copy run while this one is read back. Eight warps, two on each
-//                             quarter of the tensor-memory lanes, each thread reading 64 of its lane's 128 logits.
+//                             TMA, the tiles' keys through two stages; a producer warp issues each tile's 8 tcgen05
+//                             MMAs (K = 16 each) into one of two 128-column tensor-memory accumulators, so that the
+//                             next tile's MMAs and key copy run while this one is read back. Eight epilogue warps,
+//                             two on each quarter of the tensor-memory lanes, each thread reading 64 of its lane's
+//                             128 logits; mbarriers alone pace them (accumulator done, accumulator released, the
+//                             column halves' hand-over), with no CTA-wide barrier per tile.
 //                             Pass 0 (lane = query row) leaves each row's maximum and sum of 2^(x - max) over the
 //                             run. Pass 1 first merges those runs into each row's M and L (every CTA for its own
 //                             sequence and KV head), then takes the transposed product (keys as the MMA's A operand:
@@ -40,7 +42,8 @@ __device__ __forceinline__ unsigned ld_dsmem_u32(uint32_t addr) {
 }
 
 constexpr int TK_TILE = 128;        // keys per tile and query rows per MMA
-constexpr int TK_THREADS = 256;     // two warps per tensor-memory lane quarter, each over half of the columns
+constexpr int TK_EPI_WARPS = 8;     // two warps per tensor-memory lane quarter, each over half of the columns
+constexpr int TK_THREADS = 32 * (TK_EPI_WARPS + 1);  // and one producer warp (copies and MMAs)
 constexpr int SEL_THREADS = 256;  // the selection: one thread per radix digit
 static_assert(SEL_THREADS == 256, "the selection kernel gives each thread one 8-bit digit");
 
@@ -60,11 +63,14 @@ template <int PASS>
 __global__ void __launch_bounds__(TK_THREADS, 2)
     token_logits_kernel(TokArgs a, const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t qfull, kfull[2], mdone[2];
+  // by slot (tile parity): keys landed, MMAs done, accumulator released by the eight epilogue warps; pass 1's
+  // hand-over of the upper column half's sums, per lane quarter: written, and read
+  __shared__ __align__(8) uint64_t qfull, kfull[2], mdone[2], afree[2], pready[2][4], pfree[2][4];
   __shared__ uint32_t s_tmem;
   __shared__ int s_ok;
   __shared__ float cq[TK_TILE];  // pass 1: per query row, 2 (M + log2 L); +inf for rows without a query
-  __shared__ float2 part[TK_TILE];  // the upper column half's partial result per lane: pass 0 (m, l), pass 1 (sum, -)
+  // the upper column half's partial result per lane, by slot: pass 0 (m, l) at the end, pass 1 (sum, -) per tile
+  __shared__ float2 part[2][TK_TILE];
   // the queries (two 64-column boxes), then two key stages of two boxes each
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -77,10 +83,11 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
     tmem_relinquish();
   }
   if constexpr (PASS == 1) {  // (M, L) of every query row over pass 0's runs: two threads a row, every other run
-    const int row = tid & (TK_TILE - 1), hh = tid >> 7;
+    const int row = tid & (TK_TILE - 1), hh = tid >> 7;  // (the producer warp, hh = 2, takes no part)
     const float2* st = a.stats + (size_t)bh * a.nch * TK_TILE + row;
     float mm = -INFINITY, ll = 0.f;
-    for (int t0 = hh; t0 < a.nch; t0 += 16) {  // eight runs a batch: their loads are independent of one another
+    // eight runs a batch: their loads are independent of one another
+    for (int t0 = hh; hh < 2 && t0 < a.nch; t0 += 16) {
       float2 v[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -97,10 +104,10 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
         mm = mn;
       }
     }
-    if (hh) part[row] = make_float2(mm, ll);
+    if (hh == 1) part[0][row] = make_float2(mm, ll);
     __syncthreads();
-    if (!hh) {
-      const float2 o = part[row];
+    if (hh == 0) {
+      const float2 o = part[0][row];
       const float M = fmaxf(mm, o.x);
       const float L = M == -INFINITY ? 0.f
                                      : (mm == -INFINITY ? 0.f : ll * ex2_approx(mm - M)) +
@@ -120,6 +127,11 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&kfull[s]), 1);
       mbar_init(smem_u32(&mdone[s]), 1);
+      mbar_init(smem_u32(&afree[s]), TK_EPI_WARPS);
+      for (int q = 0; q < 4; ++q) {
+        mbar_init(smem_u32(&pready[s][q]), 1);
+        mbar_init(smem_u32(&pfree[s][q]), 1);
+      }
     }
     fence_mbar_init();
     s_ok = 1;
@@ -129,147 +141,165 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   auto kstage = [&](int s) { return base + (uint32_t)(2 + 2 * s) * TC_BOX_BYTES; };
-  // thread 0's bookkeeping: key tiles loaded, key loads seen complete, MMA groups issued and seen complete
-  int n_load = 0, n_kdone = 0, n_mma = 0, n_mdone = 0;
-  auto load_keys = [&](int i) {  // tile i of this CTA into key stage i & 1 (rows past the head's T are masked)
-    const uint32_t fb = smem_u32(&kfull[i & 1]);
-    const int krow = (int)((long long)bh * a.T + (long long)(tile0 + i) * TK_TILE);
-    mbar_expect_tx(fb, (uint32_t)a.kbox * 256u);
-    tma_load_2d(kstage(i & 1), &mk, 0, krow, fb);
-    tma_load_2d(kstage(i & 1) + TC_BOX_BYTES, &mk, 64, krow, fb);
-    ++n_load;
+  // use i of a two-slot barrier: slot i & 1, phase parity (i >> 1) & 1
+  auto wait_use = [&](uint64_t& bar, int i) {
+    return mbar_wait_bounded(smem_u32(&bar), (uint32_t)(i >> 1) & 1u, a.wait_ns);
   };
-  // tile i's logits into accumulator i & 1 once its keys have landed; a key wait that runs out marks the CTA failed
-  // and completes the accumulator's barrier itself, so that no thread waits on MMAs that were never issued
-  auto issue_mma = [&](int i) {
-    const int s = i & 1;
-    if (s_ok && mbar_wait_bounded(smem_u32(&kfull[s]), (uint32_t)(i >> 1) & 1u, a.wait_ns)) {
-      ++n_kdone;
-      tc_fence_after();
-      constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
-      const uint32_t acc = tmem + (uint32_t)(s * TK_TILE);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t koff = (uint32_t)(kk >> 2) * TC_BOX_BYTES + (uint32_t)(kk & 3) * 32u;
-        // pass 0: logits[query row][token]; pass 1 the transpose, logits[token][query row]
-        const uint64_t dq = smem_desc_k128(base + koff), dk = smem_desc_k128(kstage(s) + koff);
-        tc_mma_bf16(acc, PASS == 0 ? dq : dk, PASS == 0 ? dk : dq, IDESC, kk ? 1u : 0u);
-      }
-      tc_commit(smem_u32(&mdone[s]));
-      ++n_mma;
-    } else {
-      s_ok = 0;
-      mbar_arrive(smem_u32(&mdone[s]));
-    }
-  };
-  if (tid == 0) {
-    const uint32_t qb = smem_u32(&qfull);
-    const int qrow = (b * a.Hq + h * a.g) * a.W;  // the g x W observation queries of this KV head
-    mbar_expect_tx(qb, (uint32_t)a.qbox * 256u);
-    tma_load_2d(base, &mq, 0, qrow, qb);
-    tma_load_2d(base + TC_BOX_BYTES, &mq, 64, qrow, qb);
-    load_keys(0);
-    if (ntl > 1) load_keys(1);
-    if (!mbar_wait_bounded(qb, 0u, a.wait_ns)) {
-      s_ok = 0;
-      mbar_wait_bounded(qb, 0u, a.wait_ns);  // the copy may still land: wait again before the CTA can exit
-    }
-    issue_mma(0);
-  }
-  // tensor-memory lane quarter (warp % 4) and column half (warp / 4) of this warp; r = its lane: pass 0 the query
-  // row, pass 1 the tile's token
+  // tensor-memory lane quarter (warp % 4) and column half (warp / 4) of an epilogue warp; r = its lane: pass 0 the
+  // query row, pass 1 the tile's token
+  const bool epi = warp < TK_EPI_WARPS;
   const int wq = warp & 3, half = warp >> 2;
   const int r = 32 * wq + lane;
-  const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
-  const int cbeg = 64 * half;
-  const bool rows_here = PASS == 1 || 32 * wq < a.nq;  // pass 0: warps without a query row read nothing back
   float m = -INFINITY, l = 0.f;  // pass 0: running maximum and sum of 2^(x - max) over this CTA's tokens
-  const float two_s = 2.f * a.scale_log2;
-  bool ok = true;
-  for (int i = 0; i < ntl; ++i) {
-    const int s = i & 1;
-    const bool got = mbar_wait_bounded(smem_u32(&mdone[s]), (uint32_t)(i >> 1) & 1u, a.wait_ns);
-    tc_fence_after();
-    if (tid == 0) {
-      if (got && n_mdone == i) ++n_mdone;
-      // this tile's keys are consumed: the stage takes the tile after next, before the wait for the next tile's
-      // keys, so that two copies are in flight; then the next tile's MMAs go out while this one is read back (its
-      // accumulator was released at the end of the previous iteration)
-      if (got && s_ok && i + 2 < ntl) load_keys(i + 2);
-      if (i + 1 < ntl) issue_mma(i + 1);
-    }
-    const long long t0 = (long long)(tile0 + i) * TK_TILE;
-    const int ntok = (int)min((long long)TK_TILE, a.T - t0);
-    const uint32_t trow = tmem + lane_off + (uint32_t)(s * TK_TILE);
-    if constexpr (PASS == 0) {  // row r's logits (base 2) against the tile's tokens, 32 columns at a time
-      for (int c0 = cbeg; c0 < cbeg + 64 && c0 < ntok && rows_here; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
-        tmem_ld_wait();
-        float x[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * a.scale_log2;
-        const int nc = min(32, ntok - c0);
-        if (nc < 32) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j >= nc) x[j] = -INFINITY;  // 2^-inf = 0
-        }
-        // the chunk's maximum as a tree and its sum in four partial sums: short dependency chains
-        float t[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) t[j] = fmaxf(x[j], x[j + 16]);
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
-#pragma unroll
-          for (int j = 0; j < o; ++j) t[j] = fmaxf(t[j], t[j + o]);
-        const float mn = fmaxf(m, t[0]);
-        float lc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 32; ++j) lc[j & 3] += ex2_approx(x[j] - mn);
-        l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + ((lc[0] + lc[1]) + (lc[2] + lc[3]));
-        m = mn;
+  bool all_got = true;
+  if (!epi) {
+    if (lane == 0) {  // the producer: queries once, keys through the two stages, each tile's MMAs
+      int n_load = 0, n_kdone = 0;
+      auto load_keys = [&](int i) {  // tile i of this CTA into key stage i & 1 (rows past the head's T are masked)
+        const uint32_t fb = smem_u32(&kfull[i & 1]);
+        const int krow = (int)((long long)bh * a.T + (long long)(tile0 + i) * TK_TILE);
+        mbar_expect_tx(fb, (uint32_t)a.kbox * 256u);
+        tma_load_2d(kstage(i & 1), &mk, 0, krow, fb);
+        tma_load_2d(kstage(i & 1) + TC_BOX_BYTES, &mk, 64, krow, fb);
+        ++n_load;
+      };
+      const uint32_t qb = smem_u32(&qfull);
+      const int qrow = (b * a.Hq + h * a.g) * a.W;  // the g x W observation queries of this KV head
+      mbar_expect_tx(qb, (uint32_t)a.qbox * 256u);
+      tma_load_2d(base, &mq, 0, qrow, qb);
+      tma_load_2d(base + TC_BOX_BYTES, &mq, 64, qrow, qb);
+      load_keys(0);
+      if (ntl > 1) load_keys(1);
+      if (!mbar_wait_bounded(qb, 0u, a.wait_ns)) {
+        s_ok = 0;
+        mbar_wait_bounded(qb, 0u, a.wait_ns);  // the copy may still land: wait again before the CTA can exit
       }
-    } else {  // token r's weight: sum over the query rows of p^2 = 2^(2 s x - 2 (M + log2 L))
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
+      for (int i = 0; i < ntl; ++i) {
+        const int s = i & 1;
+        // accumulator s is free once the epilogue warps are done with tile i - 2; after a failed wait the CTA is
+        // marked failed and each remaining tile's barrier is completed without MMAs, so that no warp waits on
+        // MMAs that were never issued
+        if (i >= 2 && !wait_use(afree[s], i - 2)) s_ok = 0;
+        bool issued = false;
+        if (s_ok && wait_use(kfull[s], i)) {
+          ++n_kdone;
+          tc_fence_after();
+          constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+          const uint32_t acc = tmem + (uint32_t)(s * TK_TILE);
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int c0 = cbeg + 32 * k;
-        if (c0 < a.nq) {
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = (uint32_t)(kk >> 2) * TC_BOX_BYTES + (uint32_t)(kk & 3) * 32u;
+            // pass 0: logits[query row][token]; pass 1 the transpose, logits[token][query row]
+            const uint64_t dq = smem_desc_k128(base + koff), dk = smem_desc_k128(kstage(s) + koff);
+            tc_mma_bf16(acc, PASS == 0 ? dq : dk, PASS == 0 ? dk : dq, IDESC, kk ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&mdone[s]));
+          issued = true;
+        } else {
+          s_ok = 0;
+          mbar_arrive(smem_u32(&mdone[s]));
+        }
+        // the stage takes tile i + 2 once tile i's MMAs have read it
+        if (issued && i + 2 < ntl) {
+          if (wait_use(mdone[s], i))
+            load_keys(i + 2);
+          else
+            s_ok = 0;
+        }
+      }
+      // before the CTA releases its memory: copies still in flight after a failure, and the last tiles' MMAs (a
+      // barrier whose phase has completed, with no later use, passes at once)
+      for (int j = n_kdone; j < n_load; ++j) wait_use(kfull[j & 1], j);
+      for (int j = max(0, ntl - 2); j < ntl; ++j) wait_use(mdone[j & 1], j);
+    }
+  } else {
+    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+    const int cbeg = 64 * half;
+    const bool rows_here = PASS == 1 || 32 * wq < a.nq;  // pass 0: warps without a query row read nothing back
+    const float two_s = 2.f * a.scale_log2;
+    for (int i = 0; i < ntl; ++i) {
+      const int s = i & 1;
+      const bool got = wait_use(mdone[s], i);
+      all_got = all_got && got;
+      tc_fence_after();
+      const long long t0 = (long long)(tile0 + i) * TK_TILE;
+      const int ntok = (int)min((long long)TK_TILE, a.T - t0);
+      const uint32_t trow = tmem + lane_off + (uint32_t)(s * TK_TILE);
+      if constexpr (PASS == 0) {  // row r's logits (base 2) against the tile's tokens, 32 columns at a time
+        for (int c0 = cbeg; c0 < cbeg + 64 && c0 < ntok && rows_here; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
           tmem_ld_wait();
+          float x[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sum[j & 3] += ex2_approx(fmaf(__uint_as_float(v[j]), two_s, -cq[c0 + j]));
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * a.scale_log2;
+          const int nc = min(32, ntok - c0);
+          if (nc < 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j >= nc) x[j] = -INFINITY;  // 2^-inf = 0
+          }
+          // the chunk's maximum as a tree and its sum in four partial sums: short dependency chains
+          float t[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) t[j] = fmaxf(x[j], x[j + 16]);
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+            for (int j = 0; j < o; ++j) t[j] = fmaxf(t[j], t[j + o]);
+          const float mn = fmaxf(m, t[0]);
+          float lc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < 32; ++j) lc[j & 3] += ex2_approx(x[j] - mn);
+          l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + ((lc[0] + lc[1]) + (lc[2] + lc[3]));
+          m = mn;
+        }
+      } else {  // token r's weight: sum over the query rows of p^2 = 2^(2 s x - 2 (M + log2 L))
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int c0 = cbeg + 32 * k;
+          if (c0 < a.nq) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(trow + (uint32_t)c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sum[j & 3] += ex2_approx(fmaf(__uint_as_float(v[j]), two_s, -cq[c0 + j]));
+          }
+        }
+        const float sh = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        // the upper half hands its sums to the lower half of the same lane quarter through slot s of part
+        if (half) {
+          if (i >= 2) wait_use(pfree[s][wq], i - 2);
+          part[s][r].x = sh;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&pready[s][wq]));
+        } else {
+          const bool in = wait_use(pready[s][wq], i);
+          const float o = part[s][r].x;
+          if (got && in && s_ok && r < ntok) a.lam[(size_t)bh * a.T + t0 + r] = sh + o;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&pfree[s][wq]));
         }
       }
-      const float sh = (sum[0] + sum[1]) + (sum[2] + sum[3]);
-      if (half) part[r].x = sh;
-      __syncthreads();
-      if (!half && got && s_ok && r < ntok) a.lam[(size_t)bh * a.T + t0 + r] = sh + part[r].x;
+      // this warp is done with accumulator s
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&afree[s]));
     }
-    tc_fence_before();
-    ok = __syncthreads_and(got) && s_ok;  // also: red and this accumulator are free again
-    if (!ok) break;
   }
   if constexpr (PASS == 0) {  // the two column halves' (m, l) of a row, then the run's statistics
-    if (half) part[r] = make_float2(m, l);
+    if (epi && half) part[0][r] = make_float2(m, l);
     __syncthreads();
-    if (!half) {
-      const float2 o = part[r];
+    if (epi && !half) {
+      const float2 o = part[0][r];
       const float mm = fmaxf(m, o.x);
       const float ll = mm == -INFINITY ? 0.f
                                        : (m == -INFINITY ? 0.f : l * ex2_approx(m - mm)) +
                                              (o.x == -INFINITY ? 0.f : o.y * ex2_approx(o.x - mm));
-      const bool rv = ok && r < a.nq;
+      const bool rv = all_got && s_ok && r < a.nq;
       a.stats[((size_t)bh * a.nch + chunk) * TK_TILE + r] = rv ? make_float2(mm, ll) : make_float2(-INFINITY, 0.f);
     }
-  }
-  if (tid == 0) {  // after a failure: let the copies and MMAs in flight finish before the CTA releases its memory
-    for (int j = n_kdone; j < n_load; ++j)
-      mbar_wait_bounded(smem_u32(&kfull[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
-    for (int j = n_mdone; j < n_mma; ++j)
-      mbar_wait_bounded(smem_u32(&mdone[j & 1]), (uint32_t)(j >> 1) & 1u, a.wait_ns);
   }
   tc_fence_before();
   __syncthreads();
